@@ -1,0 +1,239 @@
+"""ctypes binding of libattnbwd (include/attn_bwd.h).
+
+The functions named like the C entry points take raw integers (device pointers,
+sizes, a cudaStream_t handle) and return the status code unchanged.  The
+torch-tensor helpers (:func:`dense_backward`, :func:`paged_backward`,
+:func:`paged_row_stats`) only marshal arguments: they check shapes, allocate the
+outputs and the workspace with torch, pass ``data_ptr()`` values and the current
+stream, and raise on a non-OK status.  Every step of the computation runs in the
+library's CUDA kernels; there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libattnbwd.so")
+HEADER = os.path.join(os.path.dirname(_HERE), "include", "attn_bwd.h")
+
+ATTN_OK = 0
+ATTN_ERR_INVALID_ARG = 1
+ATTN_ERR_UNSUPPORTED = 2
+ATTN_ERR_ALIAS = 3
+ATTN_ERR_WORKSPACE = 4
+ATTN_ERR_CUDA = 5
+ATTN_ERR_TIMEOUT = 6
+
+ATTN_DTYPE_F32 = 0
+ATTN_DTYPE_BF16 = 1
+ATTN_LAYOUT_BSHD = 0
+ATTN_LAYOUT_BHSD = 1
+ATTN_MASK_CAUSAL = 1
+ATTN_MASK_WINDOW = 2
+ATTN_MASK_KEY = 4
+ATTN_MASK_BIAS = 8
+ATTN_WRT_DQ = 1
+ATTN_WRT_DK = 2
+ATTN_WRT_DV = 4
+ATTN_WRT_DKP = 8
+
+
+class AttnError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{status_string(status)}: {message}")
+        self.status = status
+
+
+class attn_dense_desc(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int64), ("heads", ctypes.c_int64), ("seq_q", ctypes.c_int64),
+                ("seq_k", ctypes.c_int64), ("head_dim", ctypes.c_int64), ("dtype", ctypes.c_int32),
+                ("layout", ctypes.c_int32), ("mask_flags", ctypes.c_uint32), ("window", ctypes.c_int32),
+                ("mask_thr", ctypes.c_float), ("mask_neg", ctypes.c_float), ("scale", ctypes.c_float),
+                ("reserved", ctypes.c_int32)]
+
+
+class attn_paged_desc(ctypes.Structure):
+    _fields_ = [("num_queries", ctypes.c_int64), ("num_seqs", ctypes.c_int64), ("heads", ctypes.c_int64),
+                ("kv_heads", ctypes.c_int64), ("page_size", ctypes.c_int64), ("num_pages", ctypes.c_int64),
+                ("max_pages_per_seq", ctypes.c_int64), ("key_dim", ctypes.c_int64),
+                ("value_dim", ctypes.c_int64), ("position_dim", ctypes.c_int64), ("dtype", ctypes.c_int32),
+                ("causal", ctypes.c_int32), ("scale", ctypes.c_float), ("reserved", ctypes.c_int32)]
+
+
+_lib = None
+_P = ctypes.c_void_p
+_SIG = {
+    "attn_dense_desc_init": (None, [ctypes.POINTER(attn_dense_desc)]),
+    "attn_bwd_dense_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(attn_dense_desc)]),
+    "attn_bwd_dense": (ctypes.c_int32, [ctypes.POINTER(attn_dense_desc), _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                        _P, ctypes.c_uint, _P, ctypes.c_size_t, _P]),
+    "attn_bwd_paged_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(attn_paged_desc)]),
+    "attn_bwd_paged": (ctypes.c_int32, [ctypes.POINTER(attn_paged_desc), _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                        _P, _P, _P, ctypes.c_uint, _P, ctypes.c_size_t, _P]),
+    "attn_paged_row_stats": (ctypes.c_int32, [ctypes.POINTER(attn_paged_desc), _P, _P, _P, _P, _P, _P, _P, _P,
+                                              _P, _P, _P, ctypes.c_size_t, _P]),
+    "attn_last_error": (ctypes.c_char_p, []),
+    "attn_status_string": (ctypes.c_char_p, [ctypes.c_int32]),
+    "attn_check_device_error": (ctypes.c_int32, [_P]),
+    "attn_version": (ctypes.c_int, []),
+}
+
+
+def lib() -> ctypes.CDLL:
+    """Load libattnbwd.so from the package directory (raises if it is absent)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it first "
+                               "(python -c 'import __graft_entry__ as g; g.build()')")
+        l = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIG.items():
+            if hasattr(l, name):
+                f = getattr(l, name)
+                f.restype = res
+                f.argtypes = args
+        _lib = l
+    return _lib
+
+
+def header_symbols() -> list[str]:
+    """Names of the functions include/attn_bwd.h declares with ATTN_API."""
+    with open(HEADER) as fh:
+        text = fh.read()
+    return re.findall(r"ATTN_API\s+[\w\s\*]+?\b(attn_\w+)\s*\(", text)
+
+
+def status_string(st: int) -> str:
+    return lib().attn_status_string(st).decode()
+
+
+def last_error() -> str:
+    return lib().attn_last_error().decode()
+
+
+# ---- raw entry points (same names as the C ABI) ----------------------------
+
+def attn_dense_desc_init(desc: attn_dense_desc) -> None:
+    lib().attn_dense_desc_init(ctypes.byref(desc))
+
+
+def attn_bwd_dense_workspace_bytes(desc: attn_dense_desc) -> int:
+    return int(lib().attn_bwd_dense_workspace_bytes(ctypes.byref(desc)))
+
+
+def attn_bwd_dense(desc, q, k, v, dy, key_mask, bias, o, lse, dq, dk, dv, wrt_mask, workspace,
+                   workspace_bytes, stream) -> int:
+    return int(lib().attn_bwd_dense(ctypes.byref(desc), q, k, v, dy, key_mask, bias, o, lse, dq, dk, dv,
+                                    wrt_mask, workspace, workspace_bytes, stream))
+
+
+def attn_bwd_paged_workspace_bytes(desc: attn_paged_desc) -> int:
+    return int(lib().attn_bwd_paged_workspace_bytes(ctypes.byref(desc)))
+
+
+def attn_bwd_paged(desc, q, qp, k_pool, v_pool, kp_pool, dy, page_table, seq_meta, lse, delta, dk_pool, dv_pool,
+                   dkp_pool, wrt_mask, workspace, workspace_bytes, stream) -> int:
+    return int(lib().attn_bwd_paged(ctypes.byref(desc), q, qp, k_pool, v_pool, kp_pool, dy, page_table, seq_meta,
+                                    lse, delta, dk_pool, dv_pool, dkp_pool, wrt_mask, workspace, workspace_bytes,
+                                    stream))
+
+
+def attn_paged_row_stats(desc, q, qp, k_pool, v_pool, kp_pool, dy, page_table, seq_meta, lse, delta, workspace,
+                         workspace_bytes, stream) -> int:
+    return int(lib().attn_paged_row_stats(ctypes.byref(desc), q, qp, k_pool, v_pool, kp_pool, dy, page_table,
+                                          seq_meta, lse, delta, workspace, workspace_bytes, stream))
+
+
+def attn_check_device_error(stream) -> int:
+    return int(lib().attn_check_device_error(stream))
+
+
+def attn_version() -> int:
+    return int(lib().attn_version())
+
+
+# ---- torch helpers (argument marshalling only) ------------------------------
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(st: int):
+    if st != ATTN_OK:
+        raise AttnError(st, last_error())
+
+
+def _dtype_code(t):
+    import torch
+    if t.dtype == torch.bfloat16:
+        return ATTN_DTYPE_BF16
+    if t.dtype == torch.float32:
+        return ATTN_DTYPE_F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def make_dense_desc(*, batch, heads, seq_q, seq_k, head_dim, dtype=ATTN_DTYPE_BF16, layout=ATTN_LAYOUT_BSHD,
+                    causal=False, window=None, key_mask=False, bias=False, mask_thr=0.5, mask_neg=-1e9,
+                    scale=0.0) -> attn_dense_desc:
+    d = attn_dense_desc()
+    attn_dense_desc_init(d)
+    d.batch, d.heads, d.seq_q, d.seq_k, d.head_dim = batch, heads, seq_q, seq_k, head_dim
+    d.dtype, d.layout = dtype, layout
+    flags = 0
+    if causal:
+        flags |= ATTN_MASK_CAUSAL
+    if window is not None:
+        flags |= ATTN_MASK_WINDOW
+        d.window = int(window)
+    if key_mask:
+        flags |= ATTN_MASK_KEY
+    if bias:
+        flags |= ATTN_MASK_BIAS
+    d.mask_flags = flags
+    d.mask_thr, d.mask_neg, d.scale = mask_thr, mask_neg, scale
+    return d
+
+
+def dense_backward(q, k, v, dy, *, layout="bshd", causal=False, window=None, key_mask=None, bias=None, o=None,
+                   lse=None, wrt=ATTN_WRT_DQ | ATTN_WRT_DK | ATTN_WRT_DV, scale=0.0, mask_thr=0.5, mask_neg=-1e9,
+                   outputs=None, workspace=None, stream=None):
+    """dQ, dK, dV for CUDA tensors q, k, v, dy ([B,S,H,D] or [B,H,S,D]).
+
+    Returns (dq, dk, dv) with None for gradients not selected in ``wrt``."""
+    import torch
+    lay = {"bshd": ATTN_LAYOUT_BSHD, "bhsd": ATTN_LAYOUT_BHSD}[layout]
+    if lay == ATTN_LAYOUT_BSHD:
+        B, Sq, H, D = q.shape
+        Sk = k.shape[1]
+    else:
+        B, H, Sq, D = q.shape
+        Sk = k.shape[2]
+    desc = make_dense_desc(batch=B, heads=H, seq_q=Sq, seq_k=Sk, head_dim=D, dtype=_dtype_code(q), layout=lay,
+                           causal=causal, window=window, key_mask=key_mask is not None, bias=bias is not None,
+                           mask_thr=mask_thr, mask_neg=mask_neg, scale=scale)
+    if outputs is None:
+        dq = torch.empty_like(q) if wrt & ATTN_WRT_DQ else None
+        dk = torch.empty_like(k) if wrt & ATTN_WRT_DK else None
+        dv = torch.empty_like(v) if wrt & ATTN_WRT_DV else None
+    else:
+        dq, dk, dv = outputs
+    nbytes = attn_bwd_dense_workspace_bytes(desc)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=q.device)
+    st = attn_bwd_dense(desc, _ptr(q), _ptr(k), _ptr(v), _ptr(dy), _ptr(key_mask), _ptr(bias), _ptr(o), _ptr(lse),
+                        _ptr(dq), _ptr(dk), _ptr(dv), wrt, _ptr(workspace), workspace.numel(),
+                        _stream_handle(stream))
+    _check(st)
+    return dq, dk, dv
+
+
+def check_device_error(stream=None) -> None:
+    _check(attn_check_device_error(_stream_handle(stream)))

@@ -1,0 +1,299 @@
+// C ABI of libattnbwd: argument validation, workspace carving, TMA descriptor
+// construction and kernel orchestration.  See include/attn_bwd.h for the
+// contract of every entry point.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/attn_bwd.h"
+#include "dense_launch.h"
+
+namespace {
+
+thread_local char g_msg[512] = "";
+
+attn_status_t fail(attn_status_t st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+attn_status_t ok_status() {
+  g_msg[0] = '\0';
+  return ATTN_OK;
+}
+
+// ---------------------------------------------------------------------------
+// device error word (one per device), set by kernels whose bounded waits expire
+// ---------------------------------------------------------------------------
+__device__ uint32_t g_device_error;
+
+uint32_t* device_error_word() {
+  static uint32_t* ptrs[64] = {nullptr};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<uint32_t*>(p);
+  }
+  return ptrs[dev];
+}
+
+// ---------------------------------------------------------------------------
+// TMA descriptor encoding through the driver entry point
+// ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 4-D map over a [B, S, H, D]-like tensor addressed as (d, s, h, b).
+bool encode4d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, const uint64_t dims[4],
+              const uint64_t strides_bytes[3], uint32_t box0, uint32_t box1) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t gd[4] = {dims[0], dims[1], dims[2], dims[3]};
+  cuuint64_t gs[3] = {strides_bytes[0], strides_bytes[1], strides_bytes[2]};
+  cuuint32_t box[4] = {box0, box1, 1, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return fn(m, dt, 4, const_cast<void*>(base), gd, gs, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb) {
+  if (!a || !b || na == 0 || nb == 0) return false;
+  const uintptr_t x0 = reinterpret_cast<uintptr_t>(a), x1 = x0 + na;
+  const uintptr_t y0 = reinterpret_cast<uintptr_t>(b), y1 = y0 + nb;
+  return x0 < y1 && y0 < x1;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct DenseSizes {
+  size_t es, q_bytes, k_bytes, bias_bytes, mask_bytes, stat_bytes, ws_bytes;
+};
+
+attn_status_t check_dense_desc(const attn_dense_desc* d, DenseSizes* z) {
+  if (!d) return fail(ATTN_ERR_INVALID_ARG, "descriptor is NULL");
+  if (d->batch < 0 || d->heads < 0 || d->seq_q < 0 || d->seq_k < 0 || d->head_dim <= 0)
+    return fail(ATTN_ERR_INVALID_ARG, "negative size or head_dim <= 0");
+  if (d->dtype != ATTN_DTYPE_F32 && d->dtype != ATTN_DTYPE_BF16)
+    return fail(ATTN_ERR_INVALID_ARG, "unknown dtype %d", d->dtype);
+  if (d->layout != ATTN_LAYOUT_BSHD && d->layout != ATTN_LAYOUT_BHSD)
+    return fail(ATTN_ERR_INVALID_ARG, "unknown layout %d", d->layout);
+  if (d->mask_flags & ~15u) return fail(ATTN_ERR_INVALID_ARG, "unknown mask flag bits 0x%x", d->mask_flags);
+  if ((d->mask_flags & ATTN_MASK_WINDOW) && d->window < 0) return fail(ATTN_ERR_INVALID_ARG, "window < 0");
+  if (d->reserved != 0) return fail(ATTN_ERR_INVALID_ARG, "reserved field must be 0");
+  if (!std::isfinite(d->mask_neg) || !(d->mask_neg < 0.f)) return fail(ATTN_ERR_INVALID_ARG, "mask_neg must be finite and < 0");
+  if (!std::isfinite(d->mask_thr)) return fail(ATTN_ERR_INVALID_ARG, "mask_thr must be finite");
+  if (!std::isfinite(d->scale) || d->scale < 0.f) return fail(ATTN_ERR_INVALID_ARG, "scale must be finite and >= 0");
+  const int64_t D = d->head_dim;
+  if (D != 16 && D != 32 && D != 64 && D != 128)
+    return fail(ATTN_ERR_UNSUPPORTED, "head_dim %lld not supported (16, 32, 64, 128)", (long long)D);
+  const int64_t lim = int64_t(1) << 31;
+  if (d->batch * d->heads >= lim || d->seq_q >= lim || d->seq_k >= lim || d->batch * d->heads * d->seq_q >= lim)
+    return fail(ATTN_ERR_UNSUPPORTED, "sizes exceed 32-bit indexing");
+  if (d->seq_k > 65535LL * 128 || d->seq_q > 65535LL * 128) return fail(ATTN_ERR_UNSUPPORTED, "sequence too long");
+  z->es = d->dtype == ATTN_DTYPE_BF16 ? 2 : 4;
+  z->q_bytes = size_t(d->batch) * d->heads * d->seq_q * D * z->es;
+  z->k_bytes = size_t(d->batch) * d->heads * d->seq_k * D * z->es;
+  z->bias_bytes = size_t(d->batch) * d->heads * d->seq_q * d->seq_k * z->es;
+  z->mask_bytes = size_t(d->batch) * d->seq_k * 4;
+  z->stat_bytes = size_t(d->batch) * d->heads * d->seq_q * 4;
+  z->ws_bytes = 3 * align256(z->stat_bytes);
+  if (z->ws_bytes == 0) z->ws_bytes = 256;
+  return ATTN_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+ATTN_API void attn_dense_desc_init(attn_dense_desc* d) {
+  if (!d) return;
+  std::memset(d, 0, sizeof(*d));
+  d->dtype = ATTN_DTYPE_BF16;
+  d->layout = ATTN_LAYOUT_BSHD;
+  d->mask_thr = 0.5f;
+  d->mask_neg = -1e9f;
+}
+
+ATTN_API size_t attn_bwd_dense_workspace_bytes(const attn_dense_desc* d) {
+  DenseSizes z;
+  if (check_dense_desc(d, &z) != ATTN_OK) return 0;
+  return z.ws_bytes;
+}
+
+ATTN_API attn_status_t attn_bwd_dense(const attn_dense_desc* d, const void* q, const void* k, const void* v,
+                                      const void* dy, const float* key_mask, const void* bias, const void* o,
+                                      const float* lse, void* dq, void* dk, void* dv, unsigned wrt_mask,
+                                      void* workspace, size_t workspace_bytes, void* stream) {
+  DenseSizes z;
+  attn_status_t st = check_dense_desc(d, &z);
+  if (st != ATTN_OK) return st;
+  if (wrt_mask == 0 || (wrt_mask & ~7u)) return fail(ATTN_ERR_INVALID_ARG, "wrt_mask must be a non-empty subset of dQ|dK|dV");
+  const bool has_km = (d->mask_flags & ATTN_MASK_KEY) != 0;
+  const bool has_bias = (d->mask_flags & ATTN_MASK_BIAS) != 0;
+  if (has_km != (key_mask != nullptr)) return fail(ATTN_ERR_INVALID_ARG, "key_mask must be given iff ATTN_MASK_KEY is set");
+  if (has_bias != (bias != nullptr)) return fail(ATTN_ERR_INVALID_ARG, "bias must be given iff ATTN_MASK_BIAS is set");
+  if ((o == nullptr) != (lse == nullptr)) return fail(ATTN_ERR_INVALID_ARG, "o and lse must be given together");
+  const bool want_dq = wrt_mask & ATTN_WRT_DQ, want_dk = wrt_mask & ATTN_WRT_DK, want_dv = wrt_mask & ATTN_WRT_DV;
+  if ((want_dq && !dq && z.q_bytes) || (want_dk && !dk && z.k_bytes) || (want_dv && !dv && z.k_bytes))
+    return fail(ATTN_ERR_INVALID_ARG, "requested gradient pointer is NULL");
+  const int64_t B = d->batch, H = d->heads, Sq = d->seq_q, Sk = d->seq_k, D = d->head_dim;
+  const bool empty_q = B * H * Sq == 0, empty_k = B * H * Sk == 0;
+  // required inputs (only when they have elements)
+  if (!empty_q && (!q || !dy)) return fail(ATTN_ERR_INVALID_ARG, "q/dy is NULL");
+  if (!empty_k && (!k || !v)) return fail(ATTN_ERR_INVALID_ARG, "k/v is NULL");
+  const void* ptrs[] = {q, k, v, dy, key_mask, bias, o, lse, dq, dk, dv, workspace};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return fail(ATTN_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  if (has_bias && (Sk * z.es) % 16 != 0) return fail(ATTN_ERR_UNSUPPORTED, "bias needs Sk * element size to be a multiple of 16");
+  // aliasing: no output may overlap an input, the workspace or another output
+  struct R { const void* p; size_t n; };
+  const R ins[] = {{q, z.q_bytes}, {k, z.k_bytes}, {v, z.k_bytes}, {dy, z.q_bytes}, {key_mask, has_km ? z.mask_bytes : 0},
+                   {bias, has_bias ? z.bias_bytes : 0}, {o, o ? z.q_bytes : 0}, {lse, lse ? z.stat_bytes : 0},
+                   {workspace, workspace_bytes}};
+  const R outs[] = {{want_dq ? dq : nullptr, z.q_bytes}, {want_dk ? dk : nullptr, z.k_bytes}, {want_dv ? dv : nullptr, z.k_bytes}};
+  for (int i = 0; i < 3; ++i) {
+    for (const R& r : ins)
+      if (ranges_overlap(outs[i].p, outs[i].n, r.p, r.n)) return fail(ATTN_ERR_ALIAS, "output %d overlaps an input or the workspace", i);
+    for (int j = i + 1; j < 3; ++j)
+      if (ranges_overlap(outs[i].p, outs[i].n, outs[j].p, outs[j].n)) return fail(ATTN_ERR_ALIAS, "outputs %d and %d overlap", i, j);
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // zero-size problems: zero the selected gradients that have elements
+  if (empty_q || empty_k) {
+    if (want_dq && z.q_bytes && cudaMemsetAsync(dq, 0, z.q_bytes, s) != cudaSuccess) return fail(ATTN_ERR_CUDA, "memset failed");
+    if (want_dk && z.k_bytes && cudaMemsetAsync(dk, 0, z.k_bytes, s) != cudaSuccess) return fail(ATTN_ERR_CUDA, "memset failed");
+    if (want_dv && z.k_bytes && cudaMemsetAsync(dv, 0, z.k_bytes, s) != cudaSuccess) return fail(ATTN_ERR_CUDA, "memset failed");
+    return ok_status();
+  }
+  if (!workspace || workspace_bytes < z.ws_bytes)
+    return fail(ATTN_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", z.ws_bytes, workspace_bytes);
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return fail(ATTN_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  if (d->dtype != ATTN_DTYPE_BF16) return fail(ATTN_ERR_UNSUPPORTED, "f32 storage is not available in this build");
+
+  attn::DenseParams p{};
+  p.B = int(B); p.H = int(H); p.Sq = int(Sq); p.Sk = int(Sk); p.D = int(D);
+  p.q_off = Sk > Sq ? int(Sk - Sq) : 0;
+  p.causal = (d->mask_flags & (ATTN_MASK_CAUSAL | ATTN_MASK_WINDOW)) ? 1 : 0;
+  p.window = (d->mask_flags & ATTN_MASK_WINDOW) ? d->window : -1;
+  p.has_key_mask = has_km ? 1 : 0;
+  p.scale = d->scale > 0.f ? d->scale : float(1.0 / std::sqrt(double(D)));
+  p.scale_log2 = p.scale * attn::kLog2e;
+  p.masked_x2 = d->mask_neg * attn::kLog2e;
+  p.mask_thr = d->mask_thr;
+  p.mask_neg = d->mask_neg;
+  p.key_mask = key_mask;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.L2 = reinterpret_cast<float*>(ws);
+  p.delta = reinterpret_cast<float*>(ws + align256(z.stat_bytes));
+  p.pm = reinterpret_cast<float*>(ws + 2 * align256(z.stat_bytes));
+  p.o = o; p.lse = lse; p.dy = dy;
+  p.dq = dq; p.dk = dk; p.dv = dv;
+  if (d->layout == ATTN_LAYOUT_BSHD) {
+    p.q_ss = H * D; p.q_sh = D; p.q_sb = Sq * H * D;
+    p.k_ss = H * D; p.k_sh = D; p.k_sb = Sk * H * D;
+  } else {
+    p.q_ss = D; p.q_sh = Sq * D; p.q_sb = H * Sq * D;
+    p.k_ss = D; p.k_sh = Sk * D; p.k_sb = H * Sk * D;
+  }
+  p.wrt = wrt_mask;
+  p.err = device_error_word();
+  if (!p.err) return fail(ATTN_ERR_CUDA, "no CUDA device / symbol address unavailable");
+
+  // TMA descriptors: (d, s, h, b) with byte strides of s, h, b
+  const CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const uint64_t es = z.es;
+  const uint64_t qdims[4] = {uint64_t(D), uint64_t(Sq), uint64_t(H), uint64_t(B)};
+  const uint64_t kdims[4] = {uint64_t(D), uint64_t(Sk), uint64_t(H), uint64_t(B)};
+  const uint64_t qstr[3] = {uint64_t(p.q_ss) * es, uint64_t(p.q_sh) * es, uint64_t(p.q_sb) * es};
+  const uint64_t kstr[3] = {uint64_t(p.k_ss) * es, uint64_t(p.k_sh) * es, uint64_t(p.k_sb) * es};
+  attn::DenseMaps m;
+  std::memset(&m, 0, sizeof(m));
+  bool enc = encode4d(&m.q64, dt, q, qdims, qstr, 64, 64) && encode4d(&m.q128, dt, q, qdims, qstr, 64, 128) &&
+             encode4d(&m.dy64, dt, dy, qdims, qstr, 64, 64) && encode4d(&m.dy128, dt, dy, qdims, qstr, 64, 128) &&
+             encode4d(&m.k64, dt, k, kdims, kstr, 64, 64) && encode4d(&m.k128, dt, k, kdims, kstr, 64, 128) &&
+             encode4d(&m.v64, dt, v, kdims, kstr, 64, 64) && encode4d(&m.v128, dt, v, kdims, kstr, 64, 128);
+  if (enc && has_bias) {
+    const uint64_t bdims[4] = {uint64_t(Sk), uint64_t(Sq), uint64_t(H), uint64_t(B)};
+    const uint64_t bstr[3] = {uint64_t(Sk) * es, uint64_t(Sq * Sk) * es, uint64_t(H * Sq * Sk) * es};
+    enc = encode4d(&m.bias64, dt, bias, bdims, bstr, 64, 64) && encode4d(&m.bias128, dt, bias, bdims, bstr, 64, 128);
+  } else if (enc) {
+    m.bias64 = m.q64;  // unused by the kernels without bias
+    m.bias128 = m.q128;
+  }
+  if (!enc) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed (driver entry point or arguments)");
+
+  cudaError_t e = o ? attn::launch_delta_only(p, 1, s) : attn::launch_fwd_stats(m, p, has_bias, s);
+  if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "row-statistics launch failed: %s", cudaGetErrorString(e));
+  if (want_dk || want_dv) {
+    e = attn::launch_dkdv(m, p, has_bias, s);
+    if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "dK/dV launch failed: %s", cudaGetErrorString(e));
+  }
+  if (want_dq) {
+    e = attn::launch_dq(m, p, has_bias, s);
+    if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "dQ launch failed: %s", cudaGetErrorString(e));
+  }
+  return ok_status();
+}
+
+ATTN_API const char* attn_last_error(void) { return g_msg; }
+
+ATTN_API const char* attn_status_string(attn_status_t s) {
+  switch (s) {
+    case ATTN_OK: return "ATTN_OK";
+    case ATTN_ERR_INVALID_ARG: return "ATTN_ERR_INVALID_ARG";
+    case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED";
+    case ATTN_ERR_ALIAS: return "ATTN_ERR_ALIAS";
+    case ATTN_ERR_WORKSPACE: return "ATTN_ERR_WORKSPACE";
+    case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA";
+    case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT";
+    default: return "ATTN_ERR_UNKNOWN";
+  }
+}
+
+ATTN_API attn_status_t attn_check_device_error(void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "stream failed: %s", cudaGetErrorString(e));
+  uint32_t* w = device_error_word();
+  if (!w) return fail(ATTN_ERR_CUDA, "no CUDA device");
+  uint32_t h = 0;
+  if (cudaMemcpy(&h, w, 4, cudaMemcpyDeviceToHost) != cudaSuccess || cudaMemset(w, 0, 4) != cudaSuccess)
+    return fail(ATTN_ERR_CUDA, "reading the device error word failed");
+  if (h & 1u) return fail(ATTN_ERR_TIMEOUT, "a device-side wait timed out (error word 0x%x)", h);
+  if (h) return fail(ATTN_ERR_CUDA, "device error word 0x%x", h);
+  return ok_status();
+}
+
+ATTN_API int attn_version(void) { return 100; }
+
+}  // extern "C"

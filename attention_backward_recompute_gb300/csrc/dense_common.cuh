@@ -1,0 +1,107 @@
+// Shared definitions of the dense backward kernels: launch parameters, the
+// structural-mask tile arithmetic and the row-statistics layout.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+
+namespace attn {
+
+// log2(e): scores are carried in base-2 units so that exp() is one ex2.
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct DenseParams {
+  int B, H, Sq, Sk, D;   // problem sizes (D = real head dim)
+  int q_off;             // max(Sk - Sq, 0): bottom-right alignment of the masks
+  int causal;            // 1 when keys k > abs_q are hidden (causal or window)
+  int window;            // window w, or -1 when there is no lower bound
+  int has_key_mask;      // custom per-key mask present
+  float scale;           // softmax scale
+  float scale_log2;      // scale * log2(e)
+  float masked_x2;       // mask_neg * log2(e): a custom-masked score in base-2 units
+  float mask_thr;        // key masked when key_mask[b, k] < mask_thr
+  float mask_neg;        // masked score (natural units)
+  const float* key_mask; // [B, Sk] or null
+  // Row statistics (workspace), [B, H, Sq] each:
+  float* L2;             // lse * log2(e); +inf for rows with no visible key
+  float* delta;          // rowsum(P * dP) = dY . O
+  float* pm;             // probability of a custom-masked visible key in the row
+  // Optional forward outputs (delta-only prologue).
+  const void* o;
+  const float* lse;
+  const void* dy;        // dY (plain loads in the delta-only prologue)
+  // Outputs and their element strides (sequence, head, batch).
+  void* dq;
+  void* dk;
+  void* dv;
+  int64_t q_ss, q_sh, q_sb;   // strides of q / dy / o / dq
+  int64_t k_ss, k_sh, k_sb;   // strides of k / v / dk / dv
+  unsigned wrt;               // ATTN_WRT_* bits
+  uint32_t* err;              // device error word
+};
+
+__host__ __device__ inline int cdiv(int a, int b) { return (a + b - 1) / b; }
+__host__ __device__ inline int imax(int a, int b) { return a > b ? a : b; }
+__host__ __device__ inline int imin(int a, int b) { return a < b ? a : b; }
+// floor(a / b) for b > 0 and any sign of a
+__host__ __device__ inline int floordiv(int a, int b) { return a >= 0 ? a / b : -((-a + b - 1) / b); }
+
+// Range [lo, hi) of query tiles (rows tq*i .. tq*i+tq-1) that can see at least
+// one key of [k0, k1] (inclusive, k1 < Sk).  Query q sees key k when
+// k <= q + q_off (causal) and k >= q + q_off - w (window).
+__host__ __device__ inline void query_tile_range(const DenseParams& p, int k0, int k1, int tq, int* lo, int* hi) {
+  const int nq = cdiv(p.Sq, tq);
+  int l = 0, h = nq;
+  if (p.causal) l = imax(0, floordiv(k0 - p.q_off, tq));
+  if (p.window >= 0) {
+    const int qmax = k1 + p.window - p.q_off;  // largest query that sees key k1
+    h = qmax < 0 ? 0 : imin(nq, qmax / tq + 1);
+  }
+  *lo = l;
+  *hi = imax(l, h);
+}
+
+// Range [lo, hi) of key tiles (keys tk*j .. tk*j+tk-1) visible to at least one
+// query of [q0, q1] (inclusive, q1 < Sq).
+__host__ __device__ inline void key_tile_range(const DenseParams& p, int q0, int q1, int tk, int* lo, int* hi) {
+  const int nk = cdiv(p.Sk, tk);
+  int l = 0, h = nk;
+  if (p.causal) {
+    const int kmax = q1 + p.q_off;  // largest key that query q1 sees
+    h = imin(nk, kmax / tk + 1);
+  }
+  if (p.window >= 0) {
+    const int kmin = q0 + p.q_off - p.window;  // smallest key that query q0 sees
+    l = kmin <= 0 ? 0 : kmin / tk;
+  }
+  *lo = l;
+  *hi = imax(l, h);
+}
+
+// True when every (query, key) pair of the tile is structurally visible and
+// in range, so the per-element mask test can be skipped.
+__host__ __device__ inline bool tile_fully_visible(const DenseParams& p, int q0, int q1, int k0, int k1) {
+  if (q1 >= p.Sq || k1 >= p.Sk) return false;
+  if (p.causal && k1 > q0 + p.q_off) return false;
+  if (p.window >= 0 && k0 < q1 + p.q_off - p.window) return false;
+  return true;
+}
+
+__device__ __forceinline__ bool pair_visible(const DenseParams& p, int q, int k) {
+  if (k >= p.Sk || q >= p.Sq) return false;
+  const int aq = q + p.q_off;
+  if (p.causal && k > aq) return false;
+  if (p.window >= 0 && k < aq - p.window) return false;
+  return true;
+}
+
+// Number of structurally visible keys of query row q.
+__host__ __device__ inline int visible_keys(const DenseParams& p, int q) {
+  const int aq = q + p.q_off;
+  int hi = p.Sk - 1, lo = 0;
+  if (p.causal) hi = imin(hi, aq);
+  if (p.window >= 0) lo = imax(0, aq - p.window);
+  return imax(0, hi - lo + 1);
+}
+
+}  // namespace attn

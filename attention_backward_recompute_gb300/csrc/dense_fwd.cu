@@ -1,0 +1,421 @@
+// Row-statistics prologue of the dense backward.
+//
+// fwd_stats_kernel (self-contained mode): one CTA per (batch*head, 128-query
+// tile) sweeps the visible 64-key tiles like a forward pass with an online
+// softmax (scores S = Q K^T on tcgen05, P in registers, O += P V on tcgen05
+// into TMEM) and writes per query row
+//   L2    = (max + log(sum)) * log2(e)          (+inf for a row with no visible key)
+//   delta = rowsum(P * dP) = dY . O              (O normalised)
+//   pm    = probability of each custom-masked visible key of the row
+// The softmax follows rlx-wgpu src/kernels/attention_bwd.wgsl (fn softmax_row:
+// max-subtracted exponentials) and the masks rlx-cpu src/attention_bwd.rs
+// (fn apply_synthetic_mask) / attention_bwd.wgsl (fn mask_score).
+//
+// delta_only_kernel (O and LSE supplied): delta = dY . O per row, L2 from the
+// given LSE, pm from LSE and the row's visible-key count.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "dense_common.cuh"
+#include "dense_launch.h"
+#include "sm103.cuh"
+
+namespace attn {
+using namespace sm103;
+
+namespace {
+
+template <int DP>
+struct FwdLayout {
+  static constexpr int NCH = DP / 64;
+  static constexpr int BQ = 128, BK = 64;
+  static constexpr int QT = NCH * BQ * 128;
+  static constexpr int KT = NCH * BK * 128;
+  static constexpr int BIAS = BQ * 128;
+  static constexpr int PT = BQ * 128;              // P: 128 queries x 64 keys bf16
+  static constexpr int Q_OFF = 0;
+  static constexpr int DY_OFF = Q_OFF + QT;
+  static constexpr int K_OFF = DY_OFF + QT;        // 2 stages
+  static constexpr int V_OFF = K_OFF + 2 * KT;     // 2 stages
+  static constexpr int BIAS_OFF = V_OFF + 2 * KT;  // 2 stages
+  static constexpr int P_OFF = BIAS_OFF + 2 * BIAS;  // 2 buffers
+  static constexpr int BYTES = P_OFF + 2 * PT;
+  static constexpr int TMEM_COLS = 256;  // O [0, DP), S0 [DP, DP+64), S1 [DP+64, DP+128)
+};
+
+// Lazy rescaling threshold (base-2 units): the running maximum used for the
+// exponentials is only raised when a score exceeds it by more than this, so
+// P stays <= 2^8 and the O accumulator is rarely rescaled.
+constexpr float kRescaleThreshold = 8.0f;
+
+__device__ __forceinline__ bool drain_wait(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_test(bar, parity)) {
+    if (global_timer_ns() - t0 > ATTN_WAIT_TIMEOUT_NS) return false;
+  }
+  return true;
+}
+
+template <int DP, bool HAS_BIAS>
+__global__ void __launch_bounds__(256, 1)
+    fwd_stats_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_dy,
+                     const __grid_constant__ CUtensorMap tm_bias, const DenseParams p) {
+  using L = FwdLayout<DP>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ uint64_t bar_q, bar_dy, bar_full[2], bar_empty[2], bar_s_full[2], bar_p_full[2], bar_p_free[2];
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bh = blockIdx.x;
+  const int b = bh / p.H, h = bh - b * p.H;
+  const int nqt = cdiv(p.Sq, L::BQ);
+  const int it = nqt - 1 - static_cast<int>(blockIdx.y);
+  const int q0 = it * L::BQ;
+  const int q1 = imin(q0 + L::BQ - 1, p.Sq - 1);
+  int j_lo, j_hi;
+  key_tile_range(p, q0, q1, L::BK, &j_lo, &j_hi);
+  const int n = j_hi - j_lo;
+  const Abort ab{&abort_flag, p.err};
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&bar_q, 1);
+    mbar_init(&bar_dy, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bar_full[s], 1);
+      mbar_init(&bar_empty[s], 1);
+      mbar_init(&bar_s_full[s], 1);
+      mbar_init(&bar_p_full[s], 4);
+      mbar_init(&bar_p_free[s], 1);
+    }
+    mbar_fence_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_sh, L::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+  const uint32_t t_o = tmem, t_s0 = tmem + DP;
+
+  if (n > 0 && warp == 0) {
+    if (lane == 0) {
+      tma_prefetch_map(&tm_q);
+      tma_prefetch_map(&tm_k);
+      tma_prefetch_map(&tm_v);
+      tma_prefetch_map(&tm_dy);
+      if (HAS_BIAS) tma_prefetch_map(&tm_bias);
+      mbar_arrive_expect_tx(&bar_q, L::QT);
+      for (int c = 0; c < L::NCH; ++c)
+        tma_load_4d(sm + L::Q_OFF + c * (L::BQ * 128), &tm_q, &bar_q, c * 64, q0, h, b);
+      int last_use[2] = {-1, -1};
+      bool ok = true;
+      for (int t = 0; t < n && ok; ++t) {
+        const int s = t & 1;
+        if (t >= 2) ok = mbar_wait(&bar_empty[s], ((t >> 1) - 1) & 1, ab);
+        if (!ok) break;
+        const int kk0 = (j_lo + t) * L::BK;
+        mbar_arrive_expect_tx(&bar_full[s], 2 * L::KT + (HAS_BIAS ? L::BIAS : 0));
+        for (int c = 0; c < L::NCH; ++c) {
+          tma_load_4d(sm + L::K_OFF + s * L::KT + c * (L::BK * 128), &tm_k, &bar_full[s], c * 64, kk0, h, b);
+          tma_load_4d(sm + L::V_OFF + s * L::KT + c * (L::BK * 128), &tm_v, &bar_full[s], c * 64, kk0, h, b);
+        }
+        if (HAS_BIAS) tma_load_4d(sm + L::BIAS_OFF + s * L::BIAS, &tm_bias, &bar_full[s], kk0, q0, h, b);
+        last_use[s] = t;
+        if (t == 0) {  // dY is only needed at the end; load it behind the first tile
+          mbar_arrive_expect_tx(&bar_dy, L::QT);
+          for (int c = 0; c < L::NCH; ++c)
+            tma_load_4d(sm + L::DY_OFF + c * (L::BQ * 128), &tm_dy, &bar_dy, c * 64, q0, h, b);
+        }
+      }
+      for (int s = 0; s < 2; ++s)
+        if (last_use[s] >= 0) drain_wait(&bar_full[s], (last_use[s] >> 1) & 1);
+      drain_wait(&bar_q, 0);
+      if (last_use[0] >= 0) drain_wait(&bar_dy, 0);
+    }
+    __syncwarp();
+  } else if (n > 0 && warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t id_s = idesc_bf16(128, 64, false, false);
+      constexpr uint32_t id_o = idesc_bf16(128, DP, false, true);
+      const uint32_t sQ = smem_addr(sm + L::Q_OFF);
+      auto k_at = [&](int s) { return smem_addr(sm + L::K_OFF + s * L::KT); };
+      auto v_at = [&](int s) { return smem_addr(sm + L::V_OFF + s * L::KT); };
+      auto p_at = [&](int s) { return smem_addr(sm + L::P_OFF + s * L::PT); };
+      auto issue_s = [&](int t) {
+        const int s = t & 1;
+#pragma unroll
+        for (int kk = 0; kk < DP / 16; ++kk) {
+          const int c = kk >> 2, o = (kk & 3) * 32;
+          const uint64_t ad = sdesc_sw128(sQ + c * (L::BQ * 128) + o, 16, 1024);
+          const uint64_t bd = sdesc_sw128(k_at(s) + c * (L::BK * 128) + o, 16, 1024);
+          mma_bf16_ss(t_s0 + s * 64, ad, bd, id_s, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(&bar_s_full[s]);
+      };
+      bool ok = mbar_wait(&bar_q, 0, ab);
+      if (ok) ok = mbar_wait(&bar_full[0], 0, ab);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0);
+      }
+      if (ok && n > 1) {
+        ok = mbar_wait(&bar_full[1], 0, ab);
+        if (ok) {
+          tc_fence_after();
+          issue_s(1);
+        }
+      }
+      for (int t = 0; t < n && ok; ++t) {
+        const int s = t & 1;
+        if (!(ok = mbar_wait(&bar_p_full[s], (t >> 1) & 1, ab))) break;
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < L::BK / 16; ++kk) {
+          const uint64_t ad = sdesc_sw128(p_at(s) + kk * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw128(v_at(s) + kk * 16 * 128, L::BK * 128, 1024);
+          mma_bf16_ss(t_o, ad, bd, id_o, (t == 0 && kk == 0) ? 0u : 1u);
+        }
+        mma_commit(&bar_p_free[s]);
+        mma_commit(&bar_empty[s]);
+        if (t + 2 < n) {
+          if (!(ok = mbar_wait(&bar_full[s], ((t + 2) >> 1) & 1, ab))) break;
+          tc_fence_after();
+          issue_s(t + 2);
+        }
+      }
+      // the commit after the last O update already tracks every MMA; wait for it
+      if (n > 0) drain_wait(&bar_p_free[(n - 1) & 1], ((n - 1) >> 1) & 1);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    const int lg = warp & 3;
+    const int row = lg * 32 + lane;
+    const int q = q0 + row;
+    const uint32_t lane_addr = static_cast<uint32_t>(lg * 32) << 16;
+    const float kInf = __int_as_float(0x7f800000);
+    float m2 = -kInf, l = 0.f;
+    bool any_unmasked = false;
+    bool ok = n > 0;
+    for (int t = 0; t < n && ok; ++t) {
+      const int s = t & 1;
+      const int kk0 = (j_lo + t) * L::BK;
+      uint32_t kb0 = 0, kb1 = 0;
+      if (p.has_key_mask) {
+        const float* km = p.key_mask + static_cast<size_t>(b) * p.Sk;
+        const int ka = kk0 + lane, kb = kk0 + 32 + lane;
+        kb0 = __ballot_sync(0xffffffffu, ka < p.Sk && km[ka] < p.mask_thr);
+        kb1 = __ballot_sync(0xffffffffu, kb < p.Sk && km[kb] < p.mask_thr);
+      }
+      if (!(ok = mbar_wait_warp(&bar_full[s], (t >> 1) & 1, ab))) break;
+      if (!(ok = mbar_wait_warp(&bar_s_full[s], (t >> 1) & 1, ab))) break;
+      tc_fence_after();
+      float x[64];
+      {
+        uint32_t r0[32], r1[32];
+        tmem_ld32(t_s0 + s * 64 + lane_addr, r0);
+        tmem_ld32(t_s0 + s * 64 + lane_addr + 32, r1);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          x[c] = __uint_as_float(r0[c]) * p.scale_log2;
+          x[32 + c] = __uint_as_float(r1[c]) * p.scale_log2;
+        }
+      }
+      if (HAS_BIAS) {
+        const uint32_t bs = smem_addr(sm + L::BIAS_OFF + s * L::BIAS);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          uint32_t w0, w1, w2, w3;
+          asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(w0), "=r"(w1), "=r"(w2), "=r"(w3)
+                       : "r"(bs + sw128_offset(row, j)));
+          const uint32_t w[4] = {w0, w1, w2, w3};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            x[8 * j + 2 * e] = fmaf(__uint_as_float(w[e] << 16), kLog2e, x[8 * j + 2 * e]);
+            x[8 * j + 2 * e + 1] = fmaf(__uint_as_float(w[e] & 0xffff0000u), kLog2e, x[8 * j + 2 * e + 1]);
+          }
+        }
+      }
+      const bool full = tile_fully_visible(p, q0, q0 + L::BQ - 1, kk0, kk0 + L::BK - 1);
+      float mt = -kInf;
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        const bool vis = full || pair_visible(p, q, kk0 + c);
+        const bool masked = ((c < 32 ? kb0 >> c : kb1 >> (c - 32)) & 1u) != 0;
+        if (masked) x[c] = p.masked_x2;
+        if (!vis) x[c] = -kInf;
+        any_unmasked |= vis && !masked;
+        mt = fmaxf(mt, x[c]);
+      }
+      float alpha = 1.f;
+      bool rescale = false;
+      if (mt > m2 + kRescaleThreshold || (m2 == -kInf && mt > -kInf)) {
+        if (m2 > -kInf) {
+          alpha = ex2_approx(m2 - mt);
+          rescale = true;
+        }
+        l *= alpha;
+        m2 = mt;
+      }
+      float sum = 0.f;
+      float pr[64];
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        pr[c] = m2 > -kInf ? ex2_approx(x[c] - m2) : 0.f;
+        sum += pr[c];
+      }
+      l += sum;
+      // O rows scaled by alpha once every earlier O update has landed
+      if (__any_sync(0xffffffffu, rescale) && t > 0) {
+        const int ps = (t - 1) & 1;
+        if (!(ok = mbar_wait_warp(&bar_p_free[ps], ((t - 1) >> 1) & 1, ab))) break;
+        tc_fence_after();
+        const float a = rescale ? alpha : 1.f;
+#pragma unroll 1
+        for (int cc = 0; cc < DP / 32; ++cc) {
+          uint32_t r[32];
+          tmem_ld32(t_o + lane_addr + cc * 32, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * a);
+          tmem_st32(t_o + lane_addr + cc * 32, r);
+        }
+        tmem_st_wait();
+      }
+      if (t >= 2 && !(ok = mbar_wait_warp(&bar_p_free[s], ((t - 2) >> 1) & 1, ab))) break;
+      const uint32_t sp = smem_addr(sm + L::P_OFF + s * L::PT);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        st_shared_v4(sp + sw128_offset(row, j), pack_bf16x2(pr[8 * j], pr[8 * j + 1]),
+                     pack_bf16x2(pr[8 * j + 2], pr[8 * j + 3]), pack_bf16x2(pr[8 * j + 4], pr[8 * j + 5]),
+                     pack_bf16x2(pr[8 * j + 6], pr[8 * j + 7]));
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_p_full[s]);
+    }
+    float L2 = kInf, dl = 0.f, pm = 0.f;
+    if (ok && n > 0) {
+      ok = mbar_wait_warp(&bar_p_free[(n - 1) & 1], ((n - 1) >> 1) & 1, ab);
+      if (ok) ok = mbar_wait_warp(&bar_dy, 0, ab);
+      tc_fence_after();
+      if (ok) {
+        // delta = dY . O / l, O read back from TMEM, dY from the swizzled tile
+        float acc = 0.f;
+        const uint8_t* dys = sm + L::DY_OFF;
+#pragma unroll 1
+        for (int cc = 0; cc < DP / 32; ++cc) {
+          uint32_t r[32];
+          tmem_ld32(t_o + lane_addr + cc * 32, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int col = cc * 32 + j * 8;  // 8 bf16 per 16-byte chunk
+            const uint4 w = *reinterpret_cast<const uint4*>(dys + (col >> 6) * (L::BQ * 128) +
+                                                            sw128_offset(row, (col & 63) >> 3));
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              acc = fmaf(__uint_as_float(ws[e] << 16), __uint_as_float(r[8 * j + 2 * e]), acc);
+              acc = fmaf(__uint_as_float(ws[e] & 0xffff0000u), __uint_as_float(r[8 * j + 2 * e + 1]), acc);
+            }
+          }
+        }
+        if (l > 0.f) {
+          L2 = m2 + __log2f(l);
+          dl = acc / l;
+          if (p.has_key_mask) pm = any_unmasked ? ex2_approx(p.masked_x2 - L2) : 1.f / l;
+        }
+      }
+    }
+    if ((ok || n == 0) && q < p.Sq) {
+      const size_t idx = static_cast<size_t>(bh) * p.Sq + q;
+      p.L2[idx] = L2;
+      p.delta[idx] = dl;
+      if (p.has_key_mask) p.pm[idx] = pm;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, L::TMEM_COLS);
+  }
+}
+
+template <int DP, bool HAS_BIAS>
+cudaError_t launch_fwd_t(const DenseMaps& m, const DenseParams& p, cudaStream_t s) {
+  using L = FwdLayout<DP>;
+  auto kern = fwd_stats_kernel<DP, HAS_BIAS>;
+  const int smem = L::BYTES + 1024;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(p.B * p.H, cdiv(p.Sq, L::BQ));
+  kern<<<grid, 256, smem, s>>>(m.q128, m.k64, m.v64, m.dy128, m.bias128, p);
+  return cudaGetLastError();
+}
+
+// One warp per query row: delta = dY . O, L2 from the supplied LSE.
+template <typename T>
+__global__ void __launch_bounds__(256) delta_only_kernel(const DenseParams p) {
+  const int64_t rows = static_cast<int64_t>(p.B) * p.H * p.Sq;
+  const int lane = threadIdx.x & 31;
+  const int64_t w0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const float kInf = __int_as_float(0x7f800000);
+  for (int64_t r = w0; r < rows; r += nw) {
+    const int q = static_cast<int>(r % p.Sq);
+    const int64_t bh = r / p.Sq;
+    const int h = static_cast<int>(bh % p.H), b = static_cast<int>(bh / p.H);
+    const int64_t off = b * p.q_sb + h * p.q_sh + static_cast<int64_t>(q) * p.q_ss;
+    const T* dy = reinterpret_cast<const T*>(p.dy) + off;
+    const T* o = reinterpret_cast<const T*>(p.o) + off;
+    float acc = 0.f;
+    for (int d = lane; d < p.D; d += 32) acc = fmaf(static_cast<float>(dy[d]), static_cast<float>(o[d]), acc);
+#pragma unroll
+    for (int sft = 16; sft > 0; sft >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, sft);
+    if (lane == 0) {
+      const float lse = p.lse[r];
+      const int nvis = visible_keys(p, q);
+      const bool empty = nvis == 0 || lse == -kInf;
+      p.L2[r] = empty ? kInf : lse * kLog2e;
+      p.delta[r] = empty ? 0.f : acc;
+      if (p.has_key_mask) {
+        // a row whose visible keys are all custom-masked has LSE = mask_neg +
+        // log(n), which rounds to mask_neg when |mask_neg| is large
+        float pm = 0.f;
+        if (!empty) pm = (lse == p.mask_neg) ? 1.f / static_cast<float>(nvis) : ex2_approx((p.mask_neg - lse) * kLog2e);
+        p.pm[r] = pm;
+      }
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_stats(const DenseMaps& m, const DenseParams& p, bool bias, cudaStream_t s) {
+  const int DP = padded_head_dim(p.D);
+  if (DP == 64) return bias ? launch_fwd_t<64, true>(m, p, s) : launch_fwd_t<64, false>(m, p, s);
+  return bias ? launch_fwd_t<128, true>(m, p, s) : launch_fwd_t<128, false>(m, p, s);
+}
+
+cudaError_t launch_delta_only(const DenseParams& p, int dtype_bf16, cudaStream_t s) {
+  const int64_t rows = static_cast<int64_t>(p.B) * p.H * p.Sq;
+  if (rows == 0) return cudaSuccess;
+  const int64_t blocks64 = (rows * 32 + 255) / 256;
+  const int blocks = static_cast<int>(blocks64 < 152 * 64 ? blocks64 : 152 * 64);
+  if (dtype_bf16)
+    delta_only_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(p);
+  else
+    delta_only_kernel<float><<<blocks, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace attn

@@ -1,0 +1,29 @@
+// Host-side launchers of the dense kernels (called from api.cu).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "dense_common.cuh"
+
+namespace attn {
+
+// TMA descriptors of one dense call.  Q-like tensors (q, dy) and K-like tensors
+// (k, v) are described twice, with boxes of 64 and 128 rows (64 columns each,
+// 128-byte swizzle); the bias tensor [B,H,Sq,Sk] with boxes of 64 keys x 64 or
+// 128 queries.
+struct DenseMaps {
+  CUtensorMap q64, q128, dy64, dy128;
+  CUtensorMap k64, k128, v64, v128;
+  CUtensorMap bias64, bias128;
+};
+
+// padded head dim handled by the tensor-core kernels: 64 or 128
+inline int padded_head_dim(int D) { return D <= 64 ? 64 : 128; }
+
+cudaError_t launch_fwd_stats(const DenseMaps& m, const DenseParams& p, bool bias, cudaStream_t s);
+cudaError_t launch_delta_only(const DenseParams& p, int dtype_bf16, cudaStream_t s);
+cudaError_t launch_dkdv(const DenseMaps& m, const DenseParams& p, bool bias, cudaStream_t s);
+cudaError_t launch_dq(const DenseMaps& m, const DenseParams& p, bool bias, cudaStream_t s);
+
+}  // namespace attn

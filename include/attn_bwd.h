@@ -1,0 +1,235 @@
+/*
+ * attn_bwd.h -- C ABI of libattnbwd, an sm_103a (GB300) library for the
+ * backward pass of scaled dot-product attention with recomputed scores and
+ * softmax, dense and over a paged KV history.
+ *
+ * What is computed (dense), per batch b and head h, following rlx-cpu
+ * src/attention_bwd.rs (fn backward_dense_head_all, fn apply_synthetic_mask)
+ * and rlx-wgpu src/kernels/attention_bwd.wgsl (fn mask_score):
+ *
+ *   S   = scale * Q K^T                                    [Sq, Sk]
+ *   S  += bias[b,h]                          (ATTN_MASK_BIAS)
+ *   S[:, k] = mask_neg where key_mask[b,k] < mask_thr      (ATTN_MASK_KEY)
+ *   structural masks, bottom-right aligned, q_off = max(Sk - Sq, 0),
+ *   abs_q = q_off + q:   causal hides k > abs_q;  window w hides
+ *   k < abs_q - w (saturating at 0) or k > abs_q.  Hidden entries get P = 0.
+ *   P   = softmax over the visible keys of each row        (a row with no
+ *                                                          visible key: P = 0)
+ *   dV  = P^T dY
+ *   dP  = dY V^T
+ *   dS  = P * (dP - rowsum(P * dP)) * scale
+ *   dQ  = dS K
+ *   dK  = dS^T Q
+ *
+ * Paged (ruDNN src/paged_attention/ordered_kernel.rs, fn history_backward):
+ * the same backward for packed query rows against a KV history stored in
+ * pages of a pool, producing dK, dV (GQA) or dK_latent, dKp (MLA) for every
+ * pool row with no atomics and a fixed summation order.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers on the current CUDA device,
+ *     owned by the caller; the library never allocates on the call path.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
+ *     asynchronous on that stream; only attn_check_device_error synchronises.
+ *   - Every call validates its arguments first and returns a status; nothing
+ *     is launched when the status is not ATTN_OK.  There is no silent no-op
+ *     and no CPU fallback: an unsupported case returns ATTN_ERR_UNSUPPORTED.
+ *   - attn_last_error() returns a human-readable reason for the last non-OK
+ *     status returned on the calling host thread.
+ */
+#ifndef ATTN_BWD_H
+#define ATTN_BWD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define ATTN_API __attribute__((visibility("default")))
+#else
+#define ATTN_API
+#endif
+
+typedef int32_t attn_status_t;
+#define ATTN_OK 0
+#define ATTN_ERR_INVALID_ARG 1 /* null pointer, negative size, bad enum, ... */
+#define ATTN_ERR_UNSUPPORTED 2 /* valid request this build does not implement */
+#define ATTN_ERR_ALIAS 3       /* an output overlaps an input or another output */
+#define ATTN_ERR_WORKSPACE 4   /* workspace missing, too small or misaligned */
+#define ATTN_ERR_CUDA 5        /* a CUDA runtime/driver call or launch failed */
+#define ATTN_ERR_TIMEOUT 6     /* a device-side bounded wait expired */
+
+/* Storage types of q, k, v, dy, o, bias and of the gradients. */
+#define ATTN_DTYPE_F32 0  /* fp32 in and out; products on TF32 tensor cores, 3xTF32 split */
+#define ATTN_DTYPE_BF16 1 /* bf16 in and out; bf16 tensor cores, fp32 accumulation */
+
+/* Dense layouts (rlx-cpu attention_bwd.rs, fn attention_backward: `bhsd`). */
+#define ATTN_LAYOUT_BSHD 0 /* [B, S, H, D], D contiguous */
+#define ATTN_LAYOUT_BHSD 1 /* [B, H, S, D], D contiguous */
+
+/* Dense mask flags (combinable). */
+#define ATTN_MASK_CAUSAL 1u /* hide k > abs_q */
+#define ATTN_MASK_WINDOW 2u /* hide k < abs_q - window and k > abs_q */
+#define ATTN_MASK_KEY 4u    /* custom per-key mask key_mask[B, Sk] (fp32) */
+#define ATTN_MASK_BIAS 8u   /* additive bias[B, H, Sq, Sk] in the storage type */
+
+/* Gradient selection (enum order of the pages: Query = 0, Key = 1, Value = 2). */
+#define ATTN_WRT_DQ 1u
+#define ATTN_WRT_DK 2u
+#define ATTN_WRT_DV 4u
+#define ATTN_WRT_DKP 8u /* paged MLA: gradient of the position keys */
+
+typedef struct attn_dense_desc {
+  int64_t batch;      /* B  >= 0 */
+  int64_t heads;      /* H  >= 0 */
+  int64_t seq_q;      /* Sq >= 0 */
+  int64_t seq_k;      /* Sk >= 0 */
+  int64_t head_dim;   /* D: 16, 32, 64 or 128 (head_dim * element size must be a multiple of 16) */
+  int32_t dtype;      /* ATTN_DTYPE_* */
+  int32_t layout;     /* ATTN_LAYOUT_* */
+  uint32_t mask_flags;/* OR of ATTN_MASK_* */
+  int32_t window;     /* window w >= 0 when ATTN_MASK_WINDOW is set */
+  float mask_thr;     /* key masked when key_mask[b,k] < mask_thr (default 0.5) */
+  float mask_neg;     /* masked score value, finite and < 0 (default -1e9) */
+  float scale;        /* softmax scale; 0 means 1/sqrt(head_dim) */
+  int32_t reserved;   /* must be 0 */
+} attn_dense_desc;
+
+/* Fill `d` with defaults: zeros, BSHD, bf16, mask_thr 0.5, mask_neg -1e9. */
+ATTN_API void attn_dense_desc_init(attn_dense_desc* d);
+
+/* Bytes of workspace attn_bwd_dense needs for `d` (row statistics: three fp32
+ * values per (b, h, query row), each array 256-byte aligned).  Returns 0 for an
+ * invalid descriptor. */
+ATTN_API size_t attn_bwd_dense_workspace_bytes(const attn_dense_desc* d);
+
+/*
+ * Dense backward: dQ, dK, dV from Q, K, V, dY (and optionally O, LSE).
+ *
+ *   q, dy   [B,Sq,H,D] or [B,H,Sq,D] (layout), storage type `dtype`
+ *   k, v    [B,Sk,H,D] or [B,H,Sk,D]
+ *   key_mask fp32 [B, Sk], required iff ATTN_MASK_KEY (else must be NULL)
+ *   bias    [B, H, Sq, Sk] in `dtype`, required iff ATTN_MASK_BIAS (else NULL);
+ *           Sk * element size must be a multiple of 16 bytes
+ *   o, lse  optional forward output [layout of q] and fp32 log-sum-exp
+ *           [B, H, Sq] (natural log).  Both NULL: the library recomputes the
+ *           row statistics with a forward sweep (self-contained mode).  Both
+ *           given: only rowsum(dY * O) is computed.  One without the other is
+ *           ATTN_ERR_INVALID_ARG.
+ *   dq, dk, dv outputs in the layout of q / k / v; a gradient not selected in
+ *           `wrt_mask` is not written and its pointer may be NULL.  Selected
+ *           gradients are bit-identical to those of a call with all three.
+ *   workspace device memory of at least attn_bwd_dense_workspace_bytes(d),
+ *           256-byte aligned, not shared with a concurrently running call.
+ *
+ * All tensor pointers must be 16-byte aligned.  No output may overlap any
+ * input, the workspace or another output (ATTN_ERR_ALIAS); in particular the
+ * outputs may not alias v (the hazard rlx-cpu attention_backward_all guards).
+ * A zero-size dimension writes zeros to the selected gradients that have
+ * elements and returns ATTN_OK.
+ */
+ATTN_API attn_status_t attn_bwd_dense(const attn_dense_desc* d, const void* q, const void* k, const void* v,
+                                      const void* dy, const float* key_mask, const void* bias, const void* o,
+                                      const float* lse, void* dq, void* dk, void* dv, unsigned wrt_mask,
+                                      void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Paged KV history.
+ *
+ * Pools hold `num_pages * page_size` slots; slot = page * page_size + offset,
+ * and pool row (slot, g) for KV head g is at element offset
+ * (slot * kv_heads + g) * dim.  Logical page p of sequence s lives in physical
+ * page page_table[s * max_pages_per_seq + p].  A physical page may be mapped
+ * by several (sequence, logical page) links (prefix sharing); its gradient is
+ * then the sum over its links, taken in increasing (sequence, logical page)
+ * order.
+ *
+ * seq_meta is one int32 array:  seq_len[num_seqs] | q_start[num_seqs + 1] |
+ * q_pos[num_queries].  Query rows of sequence s are rows q_start[s] ..
+ * q_start[s+1]-1 of q/dy (packed, sequence-major); q_pos[r] is the absolute
+ * position of row r.  With `causal`, row r sees history tokens t <= q_pos[r].
+ *
+ * GQA (position_dim == 0): query head h reads KV head h / (heads / kv_heads).
+ * MLA (position_dim > 0): the score is q.k_latent + qp.k_position, the latent
+ * is both key and value (value_dim == key_dim, v_pool unused), and the
+ * gradients are dK_latent = dS^T Q + P^T dY and dKp = dS^T Qp.
+ */
+typedef struct attn_paged_desc {
+  int64_t num_queries;       /* Nq: packed query rows */
+  int64_t num_seqs;          /* S */
+  int64_t heads;             /* query heads H */
+  int64_t kv_heads;          /* KV heads; H % kv_heads == 0 */
+  int64_t page_size;         /* tokens per page: 16 */
+  int64_t num_pages;         /* physical pages in the pool */
+  int64_t max_pages_per_seq; /* row length of page_table */
+  int64_t key_dim;           /* 128 (GQA) or 512 (MLA latent) */
+  int64_t value_dim;         /* == key_dim */
+  int64_t position_dim;      /* 0 (GQA) or 64 (MLA) */
+  int32_t dtype;             /* ATTN_DTYPE_BF16 */
+  int32_t causal;            /* 0 or 1 */
+  float scale;               /* 0 means 1/sqrt(key_dim + position_dim) */
+  int32_t reserved;          /* must be 0 */
+} attn_paged_desc;
+
+/* Bytes of workspace attn_bwd_paged / attn_paged_row_stats need. */
+ATTN_API size_t attn_bwd_paged_workspace_bytes(const attn_paged_desc* d);
+
+/*
+ * Paged history backward (gradients of the pool rows).
+ *   q [Nq, H, key_dim], qp [Nq, H, position_dim] (MLA, else NULL),
+ *   dy [Nq, H, value_dim]; k_pool, v_pool (GQA), kp_pool (MLA) as above;
+ *   page_table int32 [num_seqs, max_pages_per_seq]; seq_meta as above;
+ *   lse, delta fp32 [Nq, H]: row statistics (natural-log LSE and
+ *   rowsum(P * dP)), e.g. from attn_paged_row_stats.  lse = -inf marks a row
+ *   with no visible token; it contributes nothing.
+ *   dk_pool, dv_pool (GQA) / dk_pool, dkp_pool (MLA): outputs shaped like the
+ *   pools.  EVERY pool row is written exactly once: rows of slots that hold no
+ *   valid token (unreferenced pages, tail slots past a sequence's length) get
+ *   zero, so no clearing pass is needed.  wrt_mask selects among ATTN_WRT_DK,
+ *   ATTN_WRT_DV (GQA) and ATTN_WRT_DKP (MLA).
+ * The result is bit-identical from run to run (no atomics; fixed order).
+ */
+ATTN_API attn_status_t attn_bwd_paged(const attn_paged_desc* d, const void* q, const void* qp, const void* k_pool,
+                                      const void* v_pool, const void* kp_pool, const void* dy,
+                                      const int32_t* page_table, const int32_t* seq_meta, const float* lse,
+                                      const float* delta, void* dk_pool, void* dv_pool, void* dkp_pool,
+                                      unsigned wrt_mask, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Row statistics for the paged path by a forward sweep over each sequence's
+ * pages: lse[r, h] = log sum_t exp(s_rt) over visible tokens (-inf if none)
+ * and delta[r, h] = rowsum(P * dP) = dY . O.  Same arguments as
+ * attn_bwd_paged; lse and delta are fp32 [Nq, H] outputs.
+ */
+ATTN_API attn_status_t attn_paged_row_stats(const attn_paged_desc* d, const void* q, const void* qp,
+                                            const void* k_pool, const void* v_pool, const void* kp_pool,
+                                            const void* dy, const int32_t* page_table, const int32_t* seq_meta,
+                                            float* lse, float* delta, void* workspace, size_t workspace_bytes,
+                                            void* stream);
+
+/* Reason for the last non-OK status on this host thread ("" if none). */
+ATTN_API const char* attn_last_error(void);
+
+/* Name of a status code. */
+ATTN_API const char* attn_status_string(attn_status_t s);
+
+/*
+ * Synchronise `stream` and report device-side errors raised since the last
+ * check by kernels of this library on the current device: ATTN_ERR_TIMEOUT if
+ * a bounded wait expired (the kernel stopped early and its outputs are
+ * invalid), ATTN_ERR_CUDA if the stream itself failed, else ATTN_OK.  Clears
+ * the device error word.
+ */
+ATTN_API attn_status_t attn_check_device_error(void* stream);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+ATTN_API int attn_version(void);
+
+#ifdef __cplusplus
+} /* extern "C" */
+#endif
+
+#endif /* ATTN_BWD_H */

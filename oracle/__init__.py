@@ -24,5 +24,5 @@ Every function here has pins in ``tests/test_oracle_*.py`` that do not reuse its
 formulas: central finite differences of the loss, invariants, closed forms and
 brute force on tiny inputs.
 """
-from .dense import attn_bwd_dense, head_backward, visibility  # noqa: F401
+from .dense import attn_bwd_dense, attn_fwd_dense, head_backward, visibility  # noqa: F401
 from .paged import attn_bwd_paged, paged_row_stats  # noqa: F401

@@ -125,3 +125,32 @@ def attn_bwd_dense(q, k, v, dy, *, layout="bshd", causal=False, window=None, key
     if return_stats:
         return dq, dk, dv, lse, delta
     return dq, dk, dv
+
+
+def attn_fwd_dense(q, k, v, *, layout="bshd", causal=False, window=None, key_mask=None, bias=None,
+                   mask_thr=0.5, mask_neg=-1e9, scale=None):
+    """Forward output O = P V and lse = log-sum-exp of the masked scores, float64.
+
+    The probabilities are those of the backward (same masks, same softmax); a
+    row with no visible key has O = 0 and lse = -inf.  Returns (o in the input
+    layout, lse [B, H, Sq])."""
+    qh, kh, vh = (_heads(np.asarray(x), layout) for x in (q, k, v))
+    B, H, Sq, D = qh.shape
+    Sk = kh.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    vis = visibility(Sq, Sk, causal, window)
+    o = np.zeros((B, H, Sq, vh.shape[3]))
+    lse = np.full((B, H, Sq), -np.inf)
+    for b in range(B):
+        for h in range(H):
+            km = None if key_mask is None else (np.asarray(key_mask[b]) < mask_thr)
+            bi = None if bias is None else bias[b, h]
+            # the backward's P with a zero upstream gradient
+            r = head_backward(qh[b, h], kh[b, h], vh[b, h], np.zeros((Sq, vh.shape[3])), vis, scale,
+                              key_masked=km, bias=bi, mask_neg=mask_neg)
+            o[b, h] = r["p"] @ np.asarray(vh[b, h], dtype=np.float64)
+            lse[b, h] = r["lse"]
+    if layout == "bshd":
+        o = np.transpose(o, (0, 2, 1, 3))
+    return o, lse

@@ -1,0 +1,100 @@
+"""The C-ABI library builds, loads and exports every symbol the header
+declares; host-side validation returns the documented status codes without
+touching a GPU."""
+import ctypes
+
+import pytest
+
+from attention_backward_recompute_gb300 import binding as bd
+from attention_backward_recompute_gb300 import build as bld
+
+
+@pytest.fixture(scope="module")
+def lib():
+    bld.build()
+    return bd.lib()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = bd.header_symbols()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/attn_bwd.h but not exported"
+
+
+def test_version_and_status_strings(lib):
+    assert bd.attn_version() >= 100
+    assert bd.status_string(bd.ATTN_ERR_ALIAS) == "ATTN_ERR_ALIAS"
+
+
+def _desc(**kw):
+    base = dict(batch=2, heads=2, seq_q=64, seq_k=64, head_dim=128)
+    base.update(kw)
+    return bd.make_dense_desc(**base)
+
+
+FAKE = 1 << 40          # 16-byte-aligned fake device addresses; never dereferenced
+MB = 1 << 20
+
+
+def _call(desc, q=FAKE, k=FAKE + 4 * MB, v=FAKE + 8 * MB, dy=FAKE + 12 * MB, km=None, bias=None, o=None,
+          lse=None, dq=FAKE + 16 * MB, dk=FAKE + 20 * MB, dv=FAKE + 24 * MB, wrt=7, ws=FAKE + 28 * MB,
+          ws_bytes=1 << 20):
+    return bd.attn_bwd_dense(desc, q, k, v, dy, km, bias, o, lse, dq, dk, dv, wrt, ws, ws_bytes, None)
+
+
+def test_workspace_query(lib):
+    d = _desc()
+    n = bd.attn_bwd_dense_workspace_bytes(d)
+    assert n >= 3 * 2 * 2 * 64 * 4 and n % 256 == 0
+    assert bd.attn_bwd_dense_workspace_bytes(_desc(head_dim=0)) == 0
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(head_dim=96), bd.ATTN_ERR_UNSUPPORTED),
+    (dict(head_dim=-1), bd.ATTN_ERR_INVALID_ARG),
+    (dict(batch=-2), bd.ATTN_ERR_INVALID_ARG),
+    (dict(dtype=7), bd.ATTN_ERR_INVALID_ARG),
+    (dict(layout=3), bd.ATTN_ERR_INVALID_ARG),
+    (dict(window=-5), bd.ATTN_ERR_INVALID_ARG),
+])
+def test_bad_descriptors(lib, kw, status):
+    d = _desc(**{k: v for k, v in kw.items() if k != "window"})
+    if "window" in kw:
+        d.mask_flags |= bd.ATTN_MASK_WINDOW
+        d.window = kw["window"]
+    assert _call(d) == status
+    assert bd.last_error() != ""
+
+
+def test_null_descriptor(lib):
+    st = lib.attn_bwd_dense(None, None, None, None, None, None, None, None, None, None, None, None, 7, None, 0, None)
+    assert st == bd.ATTN_ERR_INVALID_ARG
+
+
+def test_argument_errors(lib):
+    d = _desc()
+    assert _call(d, wrt=0) == bd.ATTN_ERR_INVALID_ARG
+    assert _call(d, wrt=16) == bd.ATTN_ERR_INVALID_ARG
+    assert _call(d, dq=None) == bd.ATTN_ERR_INVALID_ARG
+    assert _call(d, q=FAKE + 8) == bd.ATTN_ERR_INVALID_ARG           # misaligned
+    assert _call(d, km=FAKE + 40 * MB) == bd.ATTN_ERR_INVALID_ARG     # key mask without the flag
+    dk = _desc(key_mask=True)
+    assert _call(dk) == bd.ATTN_ERR_INVALID_ARG                      # flag without the key mask
+    assert _call(d, o=FAKE + 40 * MB) == bd.ATTN_ERR_INVALID_ARG      # o without lse
+
+
+def test_alias_detection(lib):
+    d = _desc()
+    # dv overlaps v (the arena hazard of the CPU reference)
+    assert _call(d, dv=FAKE + 8 * MB + 4096) == bd.ATTN_ERR_ALIAS
+    # dq overlaps dk
+    assert _call(d, dq=FAKE + 20 * MB) == bd.ATTN_ERR_ALIAS
+    # output overlaps the workspace
+    assert _call(d, dk=FAKE + 28 * MB) == bd.ATTN_ERR_ALIAS
+
+
+def test_workspace_errors(lib):
+    d = _desc()
+    assert _call(d, ws_bytes=16) == bd.ATTN_ERR_WORKSPACE
+    assert _call(d, ws=FAKE + 28 * MB + 16) == bd.ATTN_ERR_WORKSPACE

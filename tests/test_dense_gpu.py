@@ -1,0 +1,188 @@
+"""GPU parity of the dense backward (C ABI -> sm_103a kernels) with the CPU oracle.
+
+Tolerance (stated by the method's acceptance criterion): per output tensor,
+max|gpu - oracle| <= 2e-2 * max|oracle| for bf16 storage.  Inputs are the
+seeded synthetic draws of ``attention_backward_recompute_gb300.inputs``; the
+oracle reads exactly the bf16-rounded values the GPU reads.
+"""
+import numpy as np
+import pytest
+
+from attention_backward_recompute_gb300 import inputs
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+TOL_BF16 = 2e-2
+
+
+@pytest.fixture(scope="module")
+def bd():
+    from attention_backward_recompute_gb300 import binding, build
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build.build()
+    binding.lib()
+    return binding
+
+
+def _dev(x, dtype=torch.bfloat16):
+    return torch.from_numpy(np.ascontiguousarray(x)).cuda().to(dtype)
+
+
+def run_gpu(bd, c, wrt=7, o=None, lse=None, outputs=None):
+    q, k, v, dy = (_dev(x) for x in (c.q, c.k, c.v, c.dy))
+    km = None if c.key_mask is None else torch.from_numpy(c.key_mask).cuda()
+    bias = None if c.bias is None else _dev(c.bias)
+    res = bd.dense_backward(q, k, v, dy, layout=c.layout, causal=c.causal, window=c.window, key_mask=km,
+                            bias=bias, o=o, lse=lse, wrt=wrt, outputs=outputs)
+    bd.check_device_error()
+    return res
+
+
+def oracle(c, heads=None):
+    from oracle import attn_bwd_dense
+    return attn_bwd_dense(c.q, c.k, c.v, c.dy, layout=c.layout, causal=c.causal, window=c.window,
+                          key_mask=c.key_mask, bias=c.bias, heads_subset=heads)
+
+
+def rel_err(got, want):
+    g = got.float().cpu().numpy().astype(np.float64)
+    return np.max(np.abs(g - want)) / max(np.max(np.abs(want)), 1e-30)
+
+
+def assert_close(res, ref, tol=TOL_BF16, names=("dq", "dk", "dv")):
+    for n, g, w in zip(names, res, ref):
+        if g is None:
+            continue
+        e = rel_err(g, w)
+        assert e <= tol, f"{n}: max-abs-err / max|ref| = {e:.3e} > {tol}"
+
+
+# (B, H, Sq, Sk, D, causal, window, key-mask zero fraction, bias, layout)
+CASES = [
+    (2, 3, 200, 328, 128, False, None, None, False, "bshd"),
+    (2, 3, 200, 328, 128, True, None, None, False, "bshd"),
+    (1, 2, 330, 200, 128, True, None, None, False, "bshd"),
+    (2, 2, 256, 256, 128, True, None, 0.3, True, "bshd"),
+    (1, 2, 300, 300, 128, False, 37, None, False, "bshd"),
+    (1, 2, 256, 456, 128, False, 100, None, True, "bhsd"),
+    (2, 2, 192, 192, 64, True, None, 0.2, False, "bhsd"),
+    (1, 3, 130, 264, 64, False, None, None, True, "bshd"),
+    (1, 2, 77, 513, 32, True, None, None, False, "bshd"),
+    (1, 2, 150, 96, 16, False, None, 0.5, False, "bhsd"),
+    (1, 1, 1, 1, 128, False, None, None, False, "bshd"),
+    (1, 1, 5, 700, 128, True, None, None, False, "bhsd"),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "B%dH%dq%dk%dD%d_c%d_w%s_km%s_b%d_%s" % (
+    c[0], c[1], c[2], c[3], c[4], c[5], c[6], c[7], c[8], c[9]))
+def test_parity_small(bd, case):
+    B, H, Sq, Sk, D, causal, window, kmz, bias, layout = case
+    c = inputs.dense_inputs(batch=B, heads=H, seq_q=Sq, seq_k=Sk, head_dim=D, dtype="bf16", layout=layout,
+                            seed=100 + CASES.index(case), scale=0.5, causal=causal, window=window,
+                            key_mask_zero_frac=kmz, bias=bias)
+    assert_close(run_gpu(bd, c), oracle(c))
+
+
+@pytest.mark.parametrize("name,heads", [
+    ("dense_bf16_s2048", [(0, 0), (1, 7), (3, 15)]),
+    ("dense_bf16_cross", [(0, 0), (5, 9), (7, 15)]),
+])
+def test_parity_full_size_sampled_heads(bd, name, heads):
+    """Full-size configurations, in the launch configuration the bench times;
+    the oracle evaluates a sample of (batch, head) pairs."""
+    c = inputs.dense_config(name)
+    res = run_gpu(bd, c)
+    ref = oracle(c, heads=heads)
+    for b, h in heads:
+        got = [x[b, :, h] for x in res]
+        want = [x[b, :, h] for x in ref]
+        assert_close(got, want)
+
+
+def test_wrt_subsets_bit_identical(bd):
+    c = inputs.dense_inputs(batch=1, heads=2, seq_q=200, seq_k=264, head_dim=128, dtype="bf16", seed=21,
+                            scale=0.5, causal=True, key_mask_zero_frac=0.1, bias=True)
+    full = run_gpu(bd, c, wrt=7)
+    for wrt in (1, 2, 4, 3, 5, 6):
+        part = run_gpu(bd, c, wrt=wrt)
+        for i, bit in enumerate((1, 2, 4)):
+            if wrt & bit:
+                assert torch.equal(part[i], full[i]), (wrt, i)
+            else:
+                assert part[i] is None
+
+
+def test_deterministic(bd):
+    c = inputs.dense_config("dense_bf16_s2048", batch=1, heads=4)
+    a = run_gpu(bd, c)
+    b = run_gpu(bd, c)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+
+
+def test_o_lse_supplied_mode(bd):
+    """With O (bf16) and LSE from a forward, only rowsum(dY * O) is recomputed."""
+    from oracle import attn_fwd_dense
+    c = inputs.dense_inputs(batch=2, heads=2, seq_q=256, seq_k=320, head_dim=128, dtype="bf16", seed=31,
+                            scale=0.5, causal=True, key_mask_zero_frac=0.1, bias=True)
+    o, lse = attn_fwd_dense(c.q, c.k, c.v, causal=True, key_mask=c.key_mask, bias=c.bias)
+    o_t = _dev(o.astype(np.float32))
+    lse_t = torch.from_numpy(lse.astype(np.float32)).cuda().contiguous()
+    assert_close(run_gpu(bd, c, o=o_t, lse=lse_t), oracle(c))
+
+
+def test_fully_custom_masked_rows(bd):
+    """The first keys are custom-masked, so under the causal mask the first
+    rows see only masked keys: their softmax is uniform over the visible keys."""
+    c = inputs.dense_inputs(batch=1, heads=2, seq_q=256, seq_k=256, head_dim=128, dtype="bf16", seed=41,
+                            scale=0.5, causal=True, key_mask_zero_frac=0.0)
+    c.key_mask[0, :5] = 0.0
+    assert_close(run_gpu(bd, c), oracle(c))
+
+
+def test_rows_without_visible_keys(bd):
+    """Sq > Sk with a narrow window: rows q >= Sk + w see no key; their dQ is 0."""
+    c = inputs.dense_inputs(batch=1, heads=2, seq_q=300, seq_k=96, head_dim=64, dtype="bf16", seed=51,
+                            scale=0.5, window=10)
+    res = run_gpu(bd, c)
+    assert_close(res, oracle(c))
+    assert torch.all(res[0][:, 110:] == 0)
+
+
+def test_zero_size_dims(bd):
+    for sq, sk in ((0, 64), (64, 0)):
+        c = inputs.dense_inputs(batch=1, heads=2, seq_q=sq, seq_k=sk, head_dim=64, dtype="bf16", seed=1)
+        q = torch.zeros((1, sq, 2, 64), dtype=torch.bfloat16, device="cuda")
+        k = torch.zeros((1, sk, 2, 64), dtype=torch.bfloat16, device="cuda")
+        outs = (torch.full_like(q, 7.0), torch.full_like(k, 7.0), torch.full_like(k, 7.0))
+        bd.dense_backward(q, k, k.clone(), q.clone(), outputs=outs)
+        bd.check_device_error()
+        for t in outs:
+            assert t.numel() == 0 or torch.all(t == 0)
+
+
+def test_guard_bands_untouched(bd):
+    """Outputs live inside larger buffers whose margins hold a NaN pattern;
+    the kernels must write exactly the output elements."""
+    c = inputs.dense_inputs(batch=1, heads=2, seq_q=200, seq_k=136, head_dim=64, dtype="bf16", seed=61,
+                            scale=0.5, causal=True)
+    pad = 4096
+    outs, views = [], []
+    for shape in ((1, 200, 2, 64), (1, 136, 2, 64), (1, 136, 2, 64)):
+        n = int(np.prod(shape))
+        buf = torch.full((n + 2 * pad,), float("nan"), dtype=torch.bfloat16, device="cuda")
+        outs.append(buf)
+        views.append(buf[pad:pad + n].view(shape))
+    res = run_gpu(bd, c, outputs=tuple(views))
+    assert_close(res, oracle(c))
+    for buf in outs:
+        assert torch.all(torch.isnan(buf[:pad])) and torch.all(torch.isnan(buf[-pad:]))
+
+
+def test_error_word_clear_after_normal_runs(bd):
+    c = inputs.dense_inputs(batch=1, heads=1, seq_q=64, seq_k=64, head_dim=64, dtype="bf16", seed=3)
+    run_gpu(bd, c)
+    assert bd.attn_check_device_error(None) == bd.ATTN_OK

@@ -303,3 +303,19 @@ def test_visible_fractions_by_counting():
     v = visibility(512, 512, False, 128)
     assert v.sum() == sum(min(i, 128) + 1 for i in range(512))
     assert abs(v.sum() / 512 ** 2 - 0.220459) < 1e-6
+
+
+def test_forward_output_by_loops():
+    """O from the oracle's forward equals the loop forward's attention output:
+    sum(dY * O) must equal the loop loss for any dY."""
+    from oracle import attn_fwd_dense
+    rng = np.random.default_rng(12)
+    q, k, v = rng.standard_normal((1, 6, 2, 4)), rng.standard_normal((1, 9, 2, 4)), rng.standard_normal((1, 9, 2, 4))
+    km = np.ones((1, 9)); km[0, 5] = 0
+    bias = rng.standard_normal((1, 2, 6, 9))
+    o, lse = attn_fwd_dense(q, k, v, causal=True, key_mask=km, bias=bias)
+    for _ in range(3):
+        dy = rng.standard_normal(q.shape)
+        assert abs(np.sum(dy * o) - loop_loss(q, k, v, dy, True, None, km, bias)) < 1e-12
+    # lse: exp(lse) is the softmax normaliser, so sum_k exp(s - lse) = 1 per row
+    assert np.all(np.isfinite(lse))
