@@ -78,6 +78,7 @@ _SIG = {
     "attn_status_string": (ctypes.c_char_p, [ctypes.c_int32]),
     "attn_check_device_error": (ctypes.c_int32, [_P]),
     "attn_version": (ctypes.c_int, []),
+    "attn_set_timing_events": (None, [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]),
 }
 
 
@@ -148,6 +149,16 @@ def attn_paged_row_stats(desc, q, qp, k_pool, v_pool, kp_pool, dy, page_table, s
 
 def attn_check_device_error(stream) -> int:
     return int(lib().attn_check_device_error(stream))
+
+
+def attn_set_timing_events(events) -> None:
+    """Record cudaEvent handles (ints) around the kernels of the next call."""
+    if events is None:
+        lib().attn_set_timing_events(None, 0)
+        return
+    arr = (ctypes.c_void_p * len(events))(*events)
+    attn_set_timing_events._keep = arr  # the library reads the array during the next call
+    lib().attn_set_timing_events(arr, len(events))
 
 
 def attn_version() -> int:
@@ -237,3 +248,70 @@ def dense_backward(q, k, v, dy, *, layout="bshd", causal=False, window=None, key
 
 def check_device_error(stream=None) -> None:
     _check(attn_check_device_error(_stream_handle(stream)))
+
+
+def make_paged_desc(*, num_queries, num_seqs, heads, kv_heads, page_size, num_pages, max_pages_per_seq, key_dim,
+                    value_dim, position_dim=0, causal=True, scale=0.0, dtype=ATTN_DTYPE_BF16) -> attn_paged_desc:
+    d = attn_paged_desc()
+    d.num_queries, d.num_seqs, d.heads, d.kv_heads = num_queries, num_seqs, heads, kv_heads
+    d.page_size, d.num_pages, d.max_pages_per_seq = page_size, num_pages, max_pages_per_seq
+    d.key_dim, d.value_dim, d.position_dim = key_dim, value_dim, position_dim
+    d.dtype, d.causal, d.scale, d.reserved = dtype, int(bool(causal)), scale, 0
+    return d
+
+
+def seq_meta_tensor(seq_len, q_start, q_pos, device):
+    """Pack seq_len | q_start | q_pos into the single int32 array the ABI takes."""
+    import torch
+    parts = [torch.as_tensor(x, dtype=torch.int32).reshape(-1) for x in (seq_len, q_start, q_pos)]
+    return torch.cat(parts).to(device).contiguous()
+
+
+def _paged_desc_for(q, dy, k_pool, page_table, seq_meta, heads, kv_heads, page_size, causal, scale, qp, kp_pool):
+    num_seqs = page_table.shape[0]
+    return make_paged_desc(num_queries=q.shape[0], num_seqs=num_seqs, heads=heads, kv_heads=kv_heads,
+                           page_size=page_size, num_pages=k_pool.shape[0] // page_size,
+                           max_pages_per_seq=page_table.shape[1], key_dim=q.shape[2], value_dim=dy.shape[2],
+                           position_dim=0 if qp is None else qp.shape[2], causal=causal, scale=scale)
+
+
+def paged_row_stats(q, k_pool, v_pool, dy, page_table, seq_meta, *, heads, kv_heads, page_size=16, causal=True,
+                    scale=0.0, qp=None, kp_pool=None, workspace=None, stream=None):
+    """lse, delta [Nq, H] (fp32) for CUDA tensors: q [Nq,H,Dk], pools [slots,KVH,D]."""
+    import torch
+    d = _paged_desc_for(q, dy, k_pool, page_table, seq_meta, heads, kv_heads, page_size, causal, scale, qp, kp_pool)
+    lse = torch.empty((q.shape[0], heads), dtype=torch.float32, device=q.device)
+    delta = torch.empty_like(lse)
+    n = attn_bwd_paged_workspace_bytes(d)
+    if workspace is None:
+        workspace = torch.empty(max(n, 256), dtype=torch.uint8, device=q.device)
+    st = attn_paged_row_stats(d, _ptr(q), _ptr(qp), _ptr(k_pool), _ptr(v_pool), _ptr(kp_pool), _ptr(dy),
+                              _ptr(page_table), _ptr(seq_meta), _ptr(lse), _ptr(delta), _ptr(workspace),
+                              workspace.numel(), _stream_handle(stream))
+    _check(st)
+    return lse, delta
+
+
+def paged_backward(q, k_pool, v_pool, dy, page_table, seq_meta, lse, delta, *, heads, kv_heads, page_size=16,
+                   causal=True, scale=0.0, qp=None, kp_pool=None, wrt=None, outputs=None, workspace=None,
+                   stream=None):
+    """Pool gradients (dk_pool, dv_pool) for GQA or (dk_pool, dkp_pool) for MLA."""
+    import torch
+    d = _paged_desc_for(q, dy, k_pool, page_table, seq_meta, heads, kv_heads, page_size, causal, scale, qp, kp_pool)
+    mla = qp is not None
+    if wrt is None:
+        wrt = (ATTN_WRT_DK | ATTN_WRT_DKP) if mla else (ATTN_WRT_DK | ATTN_WRT_DV)
+    if outputs is None:
+        dk = torch.empty_like(k_pool) if wrt & ATTN_WRT_DK else None
+        dv = torch.empty_like(v_pool) if (not mla and wrt & ATTN_WRT_DV) else None
+        dkp = torch.empty_like(kp_pool) if (mla and wrt & ATTN_WRT_DKP) else None
+    else:
+        dk, dv, dkp = outputs
+    n = attn_bwd_paged_workspace_bytes(d)
+    if workspace is None:
+        workspace = torch.empty(max(n, 256), dtype=torch.uint8, device=q.device)
+    st = attn_bwd_paged(d, _ptr(q), _ptr(qp), _ptr(k_pool), _ptr(v_pool), _ptr(kp_pool), _ptr(dy), _ptr(page_table),
+                        _ptr(seq_meta), _ptr(lse), _ptr(delta), _ptr(dk), _ptr(dv), _ptr(dkp), wrt, _ptr(workspace),
+                        workspace.numel(), _stream_handle(stream))
+    _check(st)
+    return (dk, dkp) if mla else (dk, dv)

@@ -11,13 +11,24 @@
 #include <mutex>
 
 #include "../../include/attn_bwd.h"
+#include "api_internal.h"
 #include "dense_launch.h"
 
 namespace {
 
 thread_local char g_msg[512] = "";
+thread_local void* const* g_events = nullptr;
+thread_local int g_event_count = 0;
+thread_local int g_event_next = 0;
 
-attn_status_t fail(attn_status_t st, const char* fmt, ...) {
+// device error word (one per device), set by kernels whose bounded waits expire
+__device__ uint32_t g_device_error;
+
+}  // namespace
+
+namespace attn {
+
+attn_status_t api_fail(attn_status_t st, const char* fmt, ...) {
   va_list ap;
   va_start(ap, fmt);
   vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
@@ -25,15 +36,10 @@ attn_status_t fail(attn_status_t st, const char* fmt, ...) {
   return st;
 }
 
-attn_status_t ok_status() {
+attn_status_t api_ok() {
   g_msg[0] = '\0';
   return ATTN_OK;
 }
-
-// ---------------------------------------------------------------------------
-// device error word (one per device), set by kernels whose bounded waits expire
-// ---------------------------------------------------------------------------
-__device__ uint32_t g_device_error;
 
 uint32_t* device_error_word() {
   static uint32_t* ptrs[64] = {nullptr};
@@ -48,6 +54,32 @@ uint32_t* device_error_word() {
   }
   return ptrs[dev];
 }
+
+void timing_mark_begin(int kernels, cudaStream_t s) {
+  if (g_events && g_event_count < kernels + 1) g_events = nullptr;
+  g_event_next = 0;
+  timing_mark(s);
+}
+
+void timing_mark(cudaStream_t s) {
+  if (g_events && g_event_next < g_event_count)
+    cudaEventRecord(static_cast<cudaEvent_t>(g_events[g_event_next]), s);
+  ++g_event_next;
+}
+
+void timing_mark_end() {
+  g_events = nullptr;
+  g_event_count = 0;
+  g_event_next = 0;
+}
+
+}  // namespace attn
+
+namespace {
+
+using attn::api_fail;
+using attn::api_ok;
+using attn::device_error_word;
 
 // ---------------------------------------------------------------------------
 // TMA descriptor encoding through the driver entry point
@@ -70,18 +102,32 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+}  // namespace
+
+bool attn::encode_tiled(CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base, const uint64_t* dims,
+                        const uint64_t* strides, const uint32_t* box) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || rank < 1 || rank > 5) return false;
+  cuuint64_t gd[5], gs[4];
+  cuuint32_t bx[5], es[5];
+  for (int i = 0; i < rank; ++i) {
+    gd[i] = dims[i];
+    bx[i] = box[i];
+    es[i] = 1;
+    if (i + 1 < rank) gs[i] = strides[i];
+  }
+  return fn(m, dt, cuuint32_t(rank), const_cast<void*>(base), gd, gs, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+namespace {
+
 // 4-D map over a [B, S, H, D]-like tensor addressed as (d, s, h, b).
 bool encode4d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, const uint64_t dims[4],
               const uint64_t strides_bytes[3], uint32_t box0, uint32_t box1) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t gd[4] = {dims[0], dims[1], dims[2], dims[3]};
-  cuuint64_t gs[3] = {strides_bytes[0], strides_bytes[1], strides_bytes[2]};
-  cuuint32_t box[4] = {box0, box1, 1, 1};
-  cuuint32_t es[4] = {1, 1, 1, 1};
-  return fn(m, dt, 4, const_cast<void*>(base), gd, gs, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  const uint32_t box[4] = {box0, box1, 1, 1};
+  return attn::encode_tiled(m, dt, 4, base, dims, strides_bytes, box);
 }
 
 bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb) {
@@ -100,26 +146,26 @@ struct DenseSizes {
 };
 
 attn_status_t check_dense_desc(const attn_dense_desc* d, DenseSizes* z) {
-  if (!d) return fail(ATTN_ERR_INVALID_ARG, "descriptor is NULL");
+  if (!d) return api_fail(ATTN_ERR_INVALID_ARG, "descriptor is NULL");
   if (d->batch < 0 || d->heads < 0 || d->seq_q < 0 || d->seq_k < 0 || d->head_dim <= 0)
-    return fail(ATTN_ERR_INVALID_ARG, "negative size or head_dim <= 0");
+    return api_fail(ATTN_ERR_INVALID_ARG, "negative size or head_dim <= 0");
   if (d->dtype != ATTN_DTYPE_F32 && d->dtype != ATTN_DTYPE_BF16)
-    return fail(ATTN_ERR_INVALID_ARG, "unknown dtype %d", d->dtype);
+    return api_fail(ATTN_ERR_INVALID_ARG, "unknown dtype %d", d->dtype);
   if (d->layout != ATTN_LAYOUT_BSHD && d->layout != ATTN_LAYOUT_BHSD)
-    return fail(ATTN_ERR_INVALID_ARG, "unknown layout %d", d->layout);
-  if (d->mask_flags & ~15u) return fail(ATTN_ERR_INVALID_ARG, "unknown mask flag bits 0x%x", d->mask_flags);
-  if ((d->mask_flags & ATTN_MASK_WINDOW) && d->window < 0) return fail(ATTN_ERR_INVALID_ARG, "window < 0");
-  if (d->reserved != 0) return fail(ATTN_ERR_INVALID_ARG, "reserved field must be 0");
-  if (!std::isfinite(d->mask_neg) || !(d->mask_neg < 0.f)) return fail(ATTN_ERR_INVALID_ARG, "mask_neg must be finite and < 0");
-  if (!std::isfinite(d->mask_thr)) return fail(ATTN_ERR_INVALID_ARG, "mask_thr must be finite");
-  if (!std::isfinite(d->scale) || d->scale < 0.f) return fail(ATTN_ERR_INVALID_ARG, "scale must be finite and >= 0");
+    return api_fail(ATTN_ERR_INVALID_ARG, "unknown layout %d", d->layout);
+  if (d->mask_flags & ~15u) return api_fail(ATTN_ERR_INVALID_ARG, "unknown mask flag bits 0x%x", d->mask_flags);
+  if ((d->mask_flags & ATTN_MASK_WINDOW) && d->window < 0) return api_fail(ATTN_ERR_INVALID_ARG, "window < 0");
+  if (d->reserved != 0) return api_fail(ATTN_ERR_INVALID_ARG, "reserved field must be 0");
+  if (!std::isfinite(d->mask_neg) || !(d->mask_neg < 0.f)) return api_fail(ATTN_ERR_INVALID_ARG, "mask_neg must be finite and < 0");
+  if (!std::isfinite(d->mask_thr)) return api_fail(ATTN_ERR_INVALID_ARG, "mask_thr must be finite");
+  if (!std::isfinite(d->scale) || d->scale < 0.f) return api_fail(ATTN_ERR_INVALID_ARG, "scale must be finite and >= 0");
   const int64_t D = d->head_dim;
   if (D != 16 && D != 32 && D != 64 && D != 128)
-    return fail(ATTN_ERR_UNSUPPORTED, "head_dim %lld not supported (16, 32, 64, 128)", (long long)D);
+    return api_fail(ATTN_ERR_UNSUPPORTED, "head_dim %lld not supported (16, 32, 64, 128)", (long long)D);
   const int64_t lim = int64_t(1) << 31;
   if (d->batch * d->heads >= lim || d->seq_q >= lim || d->seq_k >= lim || d->batch * d->heads * d->seq_q >= lim)
-    return fail(ATTN_ERR_UNSUPPORTED, "sizes exceed 32-bit indexing");
-  if (d->seq_k > 65535LL * 128 || d->seq_q > 65535LL * 128) return fail(ATTN_ERR_UNSUPPORTED, "sequence too long");
+    return api_fail(ATTN_ERR_UNSUPPORTED, "sizes exceed 32-bit indexing");
+  if (d->seq_k > 65535LL * 128 || d->seq_q > 65535LL * 128) return api_fail(ATTN_ERR_UNSUPPORTED, "sequence too long");
   z->es = d->dtype == ATTN_DTYPE_BF16 ? 2 : 4;
   z->q_bytes = size_t(d->batch) * d->heads * d->seq_q * D * z->es;
   z->k_bytes = size_t(d->batch) * d->heads * d->seq_k * D * z->es;
@@ -157,24 +203,24 @@ ATTN_API attn_status_t attn_bwd_dense(const attn_dense_desc* d, const void* q, c
   DenseSizes z;
   attn_status_t st = check_dense_desc(d, &z);
   if (st != ATTN_OK) return st;
-  if (wrt_mask == 0 || (wrt_mask & ~7u)) return fail(ATTN_ERR_INVALID_ARG, "wrt_mask must be a non-empty subset of dQ|dK|dV");
+  if (wrt_mask == 0 || (wrt_mask & ~7u)) return api_fail(ATTN_ERR_INVALID_ARG, "wrt_mask must be a non-empty subset of dQ|dK|dV");
   const bool has_km = (d->mask_flags & ATTN_MASK_KEY) != 0;
   const bool has_bias = (d->mask_flags & ATTN_MASK_BIAS) != 0;
-  if (has_km != (key_mask != nullptr)) return fail(ATTN_ERR_INVALID_ARG, "key_mask must be given iff ATTN_MASK_KEY is set");
-  if (has_bias != (bias != nullptr)) return fail(ATTN_ERR_INVALID_ARG, "bias must be given iff ATTN_MASK_BIAS is set");
-  if ((o == nullptr) != (lse == nullptr)) return fail(ATTN_ERR_INVALID_ARG, "o and lse must be given together");
+  if (has_km != (key_mask != nullptr)) return api_fail(ATTN_ERR_INVALID_ARG, "key_mask must be given iff ATTN_MASK_KEY is set");
+  if (has_bias != (bias != nullptr)) return api_fail(ATTN_ERR_INVALID_ARG, "bias must be given iff ATTN_MASK_BIAS is set");
+  if ((o == nullptr) != (lse == nullptr)) return api_fail(ATTN_ERR_INVALID_ARG, "o and lse must be given together");
   const bool want_dq = wrt_mask & ATTN_WRT_DQ, want_dk = wrt_mask & ATTN_WRT_DK, want_dv = wrt_mask & ATTN_WRT_DV;
   if ((want_dq && !dq && z.q_bytes) || (want_dk && !dk && z.k_bytes) || (want_dv && !dv && z.k_bytes))
-    return fail(ATTN_ERR_INVALID_ARG, "requested gradient pointer is NULL");
+    return api_fail(ATTN_ERR_INVALID_ARG, "requested gradient pointer is NULL");
   const int64_t B = d->batch, H = d->heads, Sq = d->seq_q, Sk = d->seq_k, D = d->head_dim;
   const bool empty_q = B * H * Sq == 0, empty_k = B * H * Sk == 0;
   // required inputs (only when they have elements)
-  if (!empty_q && (!q || !dy)) return fail(ATTN_ERR_INVALID_ARG, "q/dy is NULL");
-  if (!empty_k && (!k || !v)) return fail(ATTN_ERR_INVALID_ARG, "k/v is NULL");
+  if (!empty_q && (!q || !dy)) return api_fail(ATTN_ERR_INVALID_ARG, "q/dy is NULL");
+  if (!empty_k && (!k || !v)) return api_fail(ATTN_ERR_INVALID_ARG, "k/v is NULL");
   const void* ptrs[] = {q, k, v, dy, key_mask, bias, o, lse, dq, dk, dv, workspace};
   for (const void* p : ptrs)
-    if (p && !aligned16(p)) return fail(ATTN_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
-  if (has_bias && (Sk * z.es) % 16 != 0) return fail(ATTN_ERR_UNSUPPORTED, "bias needs Sk * element size to be a multiple of 16");
+    if (p && !aligned16(p)) return api_fail(ATTN_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  if (has_bias && (Sk * z.es) % 16 != 0) return api_fail(ATTN_ERR_UNSUPPORTED, "bias needs Sk * element size to be a multiple of 16");
   // aliasing: no output may overlap an input, the workspace or another output
   struct R { const void* p; size_t n; };
   const R ins[] = {{q, z.q_bytes}, {k, z.k_bytes}, {v, z.k_bytes}, {dy, z.q_bytes}, {key_mask, has_km ? z.mask_bytes : 0},
@@ -183,22 +229,22 @@ ATTN_API attn_status_t attn_bwd_dense(const attn_dense_desc* d, const void* q, c
   const R outs[] = {{want_dq ? dq : nullptr, z.q_bytes}, {want_dk ? dk : nullptr, z.k_bytes}, {want_dv ? dv : nullptr, z.k_bytes}};
   for (int i = 0; i < 3; ++i) {
     for (const R& r : ins)
-      if (ranges_overlap(outs[i].p, outs[i].n, r.p, r.n)) return fail(ATTN_ERR_ALIAS, "output %d overlaps an input or the workspace", i);
+      if (ranges_overlap(outs[i].p, outs[i].n, r.p, r.n)) return api_fail(ATTN_ERR_ALIAS, "output %d overlaps an input or the workspace", i);
     for (int j = i + 1; j < 3; ++j)
-      if (ranges_overlap(outs[i].p, outs[i].n, outs[j].p, outs[j].n)) return fail(ATTN_ERR_ALIAS, "outputs %d and %d overlap", i, j);
+      if (ranges_overlap(outs[i].p, outs[i].n, outs[j].p, outs[j].n)) return api_fail(ATTN_ERR_ALIAS, "outputs %d and %d overlap", i, j);
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // zero-size problems: zero the selected gradients that have elements
   if (empty_q || empty_k) {
-    if (want_dq && z.q_bytes && cudaMemsetAsync(dq, 0, z.q_bytes, s) != cudaSuccess) return fail(ATTN_ERR_CUDA, "memset failed");
-    if (want_dk && z.k_bytes && cudaMemsetAsync(dk, 0, z.k_bytes, s) != cudaSuccess) return fail(ATTN_ERR_CUDA, "memset failed");
-    if (want_dv && z.k_bytes && cudaMemsetAsync(dv, 0, z.k_bytes, s) != cudaSuccess) return fail(ATTN_ERR_CUDA, "memset failed");
-    return ok_status();
+    if (want_dq && z.q_bytes && cudaMemsetAsync(dq, 0, z.q_bytes, s) != cudaSuccess) return api_fail(ATTN_ERR_CUDA, "memset failed");
+    if (want_dk && z.k_bytes && cudaMemsetAsync(dk, 0, z.k_bytes, s) != cudaSuccess) return api_fail(ATTN_ERR_CUDA, "memset failed");
+    if (want_dv && z.k_bytes && cudaMemsetAsync(dv, 0, z.k_bytes, s) != cudaSuccess) return api_fail(ATTN_ERR_CUDA, "memset failed");
+    return api_ok();
   }
   if (!workspace || workspace_bytes < z.ws_bytes)
-    return fail(ATTN_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", z.ws_bytes, workspace_bytes);
-  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return fail(ATTN_ERR_WORKSPACE, "workspace must be 256-byte aligned");
-  if (d->dtype != ATTN_DTYPE_BF16) return fail(ATTN_ERR_UNSUPPORTED, "f32 storage is not available in this build");
+    return api_fail(ATTN_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", z.ws_bytes, workspace_bytes);
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return api_fail(ATTN_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  if (d->dtype != ATTN_DTYPE_BF16) return api_fail(ATTN_ERR_UNSUPPORTED, "f32 storage is not available in this build");
 
   attn::DenseParams p{};
   p.B = int(B); p.H = int(H); p.Sq = int(Sq); p.Sk = int(Sk); p.D = int(D);
@@ -227,7 +273,7 @@ ATTN_API attn_status_t attn_bwd_dense(const attn_dense_desc* d, const void* q, c
   }
   p.wrt = wrt_mask;
   p.err = device_error_word();
-  if (!p.err) return fail(ATTN_ERR_CUDA, "no CUDA device / symbol address unavailable");
+  if (!p.err) return api_fail(ATTN_ERR_CUDA, "no CUDA device / symbol address unavailable");
 
   // TMA descriptors: (d, s, h, b) with byte strides of s, h, b
   const CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -250,19 +296,23 @@ ATTN_API attn_status_t attn_bwd_dense(const attn_dense_desc* d, const void* q, c
     m.bias64 = m.q64;  // unused by the kernels without bias
     m.bias128 = m.q128;
   }
-  if (!enc) return fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed (driver entry point or arguments)");
+  if (!enc) return api_fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed (driver entry point or arguments)");
 
+  const int nk = 1 + (want_dk || want_dv ? 1 : 0) + (want_dq ? 1 : 0);
+  attn::timing_mark_begin(nk, s);
   cudaError_t e = o ? attn::launch_delta_only(p, 1, s) : attn::launch_fwd_stats(m, p, has_bias, s);
-  if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "row-statistics launch failed: %s", cudaGetErrorString(e));
-  if (want_dk || want_dv) {
+  attn::timing_mark(s);
+  if (e == cudaSuccess && (want_dk || want_dv)) {
     e = attn::launch_dkdv(m, p, has_bias, s);
-    if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "dK/dV launch failed: %s", cudaGetErrorString(e));
+    attn::timing_mark(s);
   }
-  if (want_dq) {
+  if (e == cudaSuccess && want_dq) {
     e = attn::launch_dq(m, p, has_bias, s);
-    if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "dQ launch failed: %s", cudaGetErrorString(e));
+    attn::timing_mark(s);
   }
-  return ok_status();
+  attn::timing_mark_end();
+  if (e != cudaSuccess) return api_fail(ATTN_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
+  return api_ok();
 }
 
 ATTN_API const char* attn_last_error(void) { return g_msg; }
@@ -283,15 +333,21 @@ ATTN_API const char* attn_status_string(attn_status_t s) {
 ATTN_API attn_status_t attn_check_device_error(void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaStreamSynchronize(s);
-  if (e != cudaSuccess) return fail(ATTN_ERR_CUDA, "stream failed: %s", cudaGetErrorString(e));
+  if (e != cudaSuccess) return api_fail(ATTN_ERR_CUDA, "stream failed: %s", cudaGetErrorString(e));
   uint32_t* w = device_error_word();
-  if (!w) return fail(ATTN_ERR_CUDA, "no CUDA device");
+  if (!w) return api_fail(ATTN_ERR_CUDA, "no CUDA device");
   uint32_t h = 0;
   if (cudaMemcpy(&h, w, 4, cudaMemcpyDeviceToHost) != cudaSuccess || cudaMemset(w, 0, 4) != cudaSuccess)
-    return fail(ATTN_ERR_CUDA, "reading the device error word failed");
-  if (h & 1u) return fail(ATTN_ERR_TIMEOUT, "a device-side wait timed out (error word 0x%x)", h);
-  if (h) return fail(ATTN_ERR_CUDA, "device error word 0x%x", h);
-  return ok_status();
+    return api_fail(ATTN_ERR_CUDA, "reading the device error word failed");
+  if (h & 1u) return api_fail(ATTN_ERR_TIMEOUT, "a device-side wait timed out (error word 0x%x)", h);
+  if (h) return api_fail(ATTN_ERR_CUDA, "device error word 0x%x", h);
+  return api_ok();
+}
+
+ATTN_API void attn_set_timing_events(void* const* events, int count) {
+  g_events = events;
+  g_event_count = events ? count : 0;
+  g_event_next = 0;
 }
 
 ATTN_API int attn_version(void) { return 100; }

@@ -1,22 +1,122 @@
-// C ABI of the paged-KV history backward (entry points, validation).
+// C ABI of the paged-KV history backward: validation, workspace carving, TMA
+// descriptors and launch order (prep -> zero of unlinked pages -> history).
+#include <cuda.h>
 #include <cuda_runtime.h>
 
-#include <cstdarg>
-#include <cstdio>
+#include <cmath>
+#include <cstring>
 
 #include "../../include/attn_bwd.h"
+#include "api_internal.h"
+#include "paged_launch.h"
 
 namespace {
-// Shares the message buffer of the dense entry points through attn_last_error;
-// the paged calls report through their own thread-local buffer that
-// attn_last_error consults when it is the most recent failure.
+
+using attn::api_fail;
+using attn::api_ok;
+
+struct PagedSizes {
+  size_t q_bytes, qp_bytes, dy_bytes, k_bytes, v_bytes, kp_bytes, table_bytes, meta_bytes, stat_bytes;
+  size_t ws_bytes;
+  size_t off_count, off_off, off_fill, off_links;
+};
+
+size_t a256(size_t x) { return (x + 255) & ~size_t(255); }
+
+attn_status_t check_paged_desc(const attn_paged_desc* d, PagedSizes* z) {
+  if (!d) return api_fail(ATTN_ERR_INVALID_ARG, "descriptor is NULL");
+  if (d->num_queries < 0 || d->num_seqs < 0 || d->heads <= 0 || d->kv_heads <= 0 || d->page_size <= 0 ||
+      d->num_pages < 0 || d->max_pages_per_seq < 0 || d->key_dim <= 0 || d->value_dim <= 0 || d->position_dim < 0)
+    return api_fail(ATTN_ERR_INVALID_ARG, "negative or zero size in the paged descriptor");
+  if (d->reserved != 0) return api_fail(ATTN_ERR_INVALID_ARG, "reserved field must be 0");
+  if (d->heads % d->kv_heads != 0) return api_fail(ATTN_ERR_INVALID_ARG, "heads must be a multiple of kv_heads");
+  if (d->causal != 0 && d->causal != 1) return api_fail(ATTN_ERR_INVALID_ARG, "causal must be 0 or 1");
+  if (!std::isfinite(d->scale) || d->scale < 0.f) return api_fail(ATTN_ERR_INVALID_ARG, "scale must be finite and >= 0");
+  if (d->dtype != ATTN_DTYPE_BF16) return api_fail(ATTN_ERR_UNSUPPORTED, "paged path supports bf16 storage only");
+  if (d->page_size != 16) return api_fail(ATTN_ERR_UNSUPPORTED, "page_size must be 16");
+  const int64_t G = d->heads / d->kv_heads;
+  if (64 % G != 0) return api_fail(ATTN_ERR_UNSUPPORTED, "heads / kv_heads must divide 64");
+  if (d->position_dim != 0) return api_fail(ATTN_ERR_UNSUPPORTED, "MLA (position_dim > 0) is not available in this build");
+  if (d->value_dim != d->key_dim) return api_fail(ATTN_ERR_UNSUPPORTED, "value_dim must equal key_dim");
+  if (d->key_dim != 64 && d->key_dim != 128) return api_fail(ATTN_ERR_UNSUPPORTED, "key_dim must be 64 or 128 (GQA)");
+  const int64_t lim = int64_t(1) << 30;
+  if (d->num_pages * d->page_size >= lim || d->num_queries * d->heads >= lim || d->num_seqs * d->max_pages_per_seq >= lim ||
+      d->num_seqs >= 65535 || d->kv_heads >= 65535)
+    return api_fail(ATTN_ERR_UNSUPPORTED, "sizes exceed the supported index range");
+  const size_t es = 2;
+  const size_t slots = size_t(d->num_pages) * d->page_size;
+  z->q_bytes = size_t(d->num_queries) * d->heads * d->key_dim * es;
+  z->qp_bytes = size_t(d->num_queries) * d->heads * d->position_dim * es;
+  z->dy_bytes = size_t(d->num_queries) * d->heads * d->value_dim * es;
+  z->k_bytes = slots * d->kv_heads * d->key_dim * es;
+  z->v_bytes = slots * d->kv_heads * d->value_dim * es;
+  z->kp_bytes = slots * d->kv_heads * d->position_dim * es;
+  z->table_bytes = size_t(d->num_seqs) * d->max_pages_per_seq * 4;
+  z->meta_bytes = (size_t(d->num_seqs) * 2 + 1 + d->num_queries) * 4;
+  z->stat_bytes = size_t(d->num_queries) * d->heads * 4;
+  z->off_count = 0;
+  z->off_off = z->off_count + a256(size_t(d->num_pages) * 4);
+  z->off_fill = z->off_off + a256(size_t(d->num_pages + 1) * 4);
+  z->off_links = z->off_fill + a256(size_t(d->num_pages) * 4);
+  z->ws_bytes = z->off_links + a256(size_t(d->num_seqs) * d->max_pages_per_seq * 4 + 4);
+  return ATTN_OK;
+}
+
+bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+  if (!a || !b || !na || !nb) return false;
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+attn_status_t fill_params(const attn_paged_desc* d, const PagedSizes& z, const int32_t* page_table,
+                          const int32_t* seq_meta, void* workspace, attn::PagedParams* p) {
+  std::memset(p, 0, sizeof(*p));
+  p->Nq = int(d->num_queries);
+  p->S = int(d->num_seqs);
+  p->H = int(d->heads);
+  p->KVH = int(d->kv_heads);
+  p->G = int(d->heads / d->kv_heads);
+  p->page_size = int(d->page_size);
+  p->num_pages = int(d->num_pages);
+  p->max_pages = int(d->max_pages_per_seq);
+  p->Dk = int(d->key_dim);
+  p->Dv = int(d->value_dim);
+  p->Dp = int(d->position_dim);
+  p->causal = d->causal;
+  p->scale = d->scale > 0.f ? d->scale : float(1.0 / std::sqrt(double(d->key_dim + d->position_dim)));
+  p->scale_log2 = p->scale * 1.4426950408889634f;
+  p->page_table = page_table;
+  p->seq_len = seq_meta;
+  p->q_start = seq_meta + d->num_seqs;
+  p->q_pos = seq_meta + 2 * d->num_seqs + 1;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p->link_count = reinterpret_cast<int32_t*>(ws + z.off_count);
+  p->link_off = reinterpret_cast<int32_t*>(ws + z.off_off);
+  p->link_fill = reinterpret_cast<int32_t*>(ws + z.off_fill);
+  p->links = reinterpret_cast<int32_t*>(ws + z.off_links);
+  p->err = attn::device_error_word();
+  if (!p->err) return api_fail(ATTN_ERR_CUDA, "no CUDA device / symbol address unavailable");
+  return ATTN_OK;
+}
+
+bool encode3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1,
+              uint32_t b2) {
+  const uint64_t dims[3] = {d0, d1, d2};
+  const uint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+  const uint32_t box[3] = {b0, b1, b2};
+  return attn::encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box);
+}
+
 }  // namespace
 
 extern "C" {
 
 ATTN_API size_t attn_bwd_paged_workspace_bytes(const attn_paged_desc* d) {
-  (void)d;
-  return 0;
+  PagedSizes z;
+  if (check_paged_desc(d, &z) != ATTN_OK) return 0;
+  return z.ws_bytes;
 }
 
 ATTN_API attn_status_t attn_bwd_paged(const attn_paged_desc* d, const void* q, const void* qp, const void* k_pool,
@@ -24,10 +124,70 @@ ATTN_API attn_status_t attn_bwd_paged(const attn_paged_desc* d, const void* q, c
                                       const int32_t* page_table, const int32_t* seq_meta, const float* lse,
                                       const float* delta, void* dk_pool, void* dv_pool, void* dkp_pool,
                                       unsigned wrt_mask, void* workspace, size_t workspace_bytes, void* stream) {
-  (void)d; (void)q; (void)qp; (void)k_pool; (void)v_pool; (void)kp_pool; (void)dy; (void)page_table;
-  (void)seq_meta; (void)lse; (void)delta; (void)dk_pool; (void)dv_pool; (void)dkp_pool; (void)wrt_mask;
-  (void)workspace; (void)workspace_bytes; (void)stream;
-  return ATTN_ERR_UNSUPPORTED;
+  PagedSizes z;
+  attn_status_t st = check_paged_desc(d, &z);
+  if (st != ATTN_OK) return st;
+  (void)qp;
+  (void)kp_pool;
+  (void)dkp_pool;
+  if (wrt_mask == 0 || (wrt_mask & ~(ATTN_WRT_DK | ATTN_WRT_DV)))
+    return api_fail(ATTN_ERR_INVALID_ARG, "wrt_mask must be a non-empty subset of dK|dV for GQA");
+  const bool want_dk = wrt_mask & ATTN_WRT_DK, want_dv = wrt_mask & ATTN_WRT_DV;
+  if ((want_dk && !dk_pool && z.k_bytes) || (want_dv && !dv_pool && z.v_bytes))
+    return api_fail(ATTN_ERR_INVALID_ARG, "requested gradient pointer is NULL");
+  if (d->num_seqs > 0 && (!seq_meta || (d->max_pages_per_seq > 0 && !page_table)))
+    return api_fail(ATTN_ERR_INVALID_ARG, "page_table / seq_meta is NULL");
+  if (d->num_queries > 0 && (!q || !dy || !lse || !delta)) return api_fail(ATTN_ERR_INVALID_ARG, "q/dy/lse/delta is NULL");
+  if (d->num_pages > 0 && (!k_pool || !v_pool)) return api_fail(ATTN_ERR_INVALID_ARG, "k_pool/v_pool is NULL");
+  const void* al[] = {q, k_pool, v_pool, dy, dk_pool, dv_pool, lse, delta, page_table, seq_meta, workspace};
+  for (const void* x : al)
+    if (x && !al16(x)) return api_fail(ATTN_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  struct R { const void* p; size_t n; };
+  const R ins[] = {{q, z.q_bytes}, {k_pool, z.k_bytes}, {v_pool, z.v_bytes}, {dy, z.dy_bytes},
+                   {page_table, z.table_bytes}, {seq_meta, z.meta_bytes}, {lse, z.stat_bytes},
+                   {delta, z.stat_bytes}, {workspace, workspace_bytes}};
+  const R outs[] = {{want_dk ? dk_pool : nullptr, z.k_bytes}, {want_dv ? dv_pool : nullptr, z.v_bytes}};
+  for (int i = 0; i < 2; ++i) {
+    for (const R& r : ins)
+      if (overlap(outs[i].p, outs[i].n, r.p, r.n)) return api_fail(ATTN_ERR_ALIAS, "output %d overlaps an input or the workspace", i);
+  }
+  if (overlap(outs[0].p, outs[0].n, outs[1].p, outs[1].n)) return api_fail(ATTN_ERR_ALIAS, "dk_pool and dv_pool overlap");
+  if (d->num_pages == 0) return api_ok();
+  if (!workspace || workspace_bytes < z.ws_bytes)
+    return api_fail(ATTN_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", z.ws_bytes, workspace_bytes);
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return api_fail(ATTN_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+
+  attn::PagedParams p;
+  if ((st = fill_params(d, z, page_table, seq_meta, workspace, &p)) != ATTN_OK) return st;
+  p.lse = lse;
+  p.delta = delta;
+  p.dk_pool = dk_pool;
+  p.dv_pool = dv_pool;
+  p.wrt = wrt_mask;
+  attn::PagedMaps m;
+  std::memset(&m, 0, sizeof(m));
+  const uint64_t slots = uint64_t(d->num_pages) * d->page_size;
+  const uint32_t G = uint32_t(p.G);
+  bool enc = true;
+  if (d->num_queries > 0)
+    enc = encode3d(&m.q, q, d->key_dim, d->heads, d->num_queries, 64, G, 64 / G) &&
+          encode3d(&m.dy, dy, d->value_dim, d->heads, d->num_queries, 64, G, 64 / G);
+  enc = enc && encode3d(&m.k, k_pool, d->key_dim, d->kv_heads, slots, 64, 1, uint32_t(d->page_size)) &&
+        encode3d(&m.v, v_pool, d->value_dim, d->kv_heads, slots, 64, 1, uint32_t(d->page_size));
+  if (!enc) return api_fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+  if (d->num_queries == 0) { m.q = m.k; m.dy = m.v; }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int nk = 6;
+  attn::timing_mark_begin(nk, s);
+  cudaError_t e = attn::launch_paged_prep(p, s);
+  attn::timing_mark(s);
+  if (e == cudaSuccess) e = attn::launch_paged_zero_unlinked(p, s);
+  attn::timing_mark(s);
+  if (e == cudaSuccess && d->num_seqs > 0 && d->max_pages_per_seq > 0) e = attn::launch_paged_history(m, p, s);
+  attn::timing_mark(s);
+  attn::timing_mark_end();
+  if (e != cudaSuccess) return api_fail(ATTN_ERR_CUDA, "paged launch failed: %s", cudaGetErrorString(e));
+  return api_ok();
 }
 
 ATTN_API attn_status_t attn_paged_row_stats(const attn_paged_desc* d, const void* q, const void* qp,
@@ -35,9 +195,48 @@ ATTN_API attn_status_t attn_paged_row_stats(const attn_paged_desc* d, const void
                                             const void* dy, const int32_t* page_table, const int32_t* seq_meta,
                                             float* lse, float* delta, void* workspace, size_t workspace_bytes,
                                             void* stream) {
-  (void)d; (void)q; (void)qp; (void)k_pool; (void)v_pool; (void)kp_pool; (void)dy; (void)page_table;
-  (void)seq_meta; (void)lse; (void)delta; (void)workspace; (void)workspace_bytes; (void)stream;
-  return ATTN_ERR_UNSUPPORTED;
+  PagedSizes z;
+  attn_status_t st = check_paged_desc(d, &z);
+  if (st != ATTN_OK) return st;
+  (void)qp;
+  (void)kp_pool;
+  if (d->num_queries == 0) return api_ok();
+  if (!q || !dy || !lse || !delta || !seq_meta || (d->max_pages_per_seq > 0 && !page_table))
+    return api_fail(ATTN_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (d->num_pages > 0 && (!k_pool || !v_pool)) return api_fail(ATTN_ERR_INVALID_ARG, "k_pool/v_pool is NULL");
+  const void* al[] = {q, k_pool, v_pool, dy, lse, delta, page_table, seq_meta};
+  for (const void* x : al)
+    if (x && !al16(x)) return api_fail(ATTN_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  struct R { const void* p; size_t n; };
+  const R ins[] = {{q, z.q_bytes}, {k_pool, z.k_bytes}, {v_pool, z.v_bytes}, {dy, z.dy_bytes},
+                   {page_table, z.table_bytes}, {seq_meta, z.meta_bytes}, {workspace, workspace_bytes}};
+  for (const R& r : ins)
+    if (overlap(lse, z.stat_bytes, r.p, r.n) || overlap(delta, z.stat_bytes, r.p, r.n))
+      return api_fail(ATTN_ERR_ALIAS, "lse/delta overlap an input or the workspace");
+  if (overlap(lse, z.stat_bytes, delta, z.stat_bytes)) return api_fail(ATTN_ERR_ALIAS, "lse and delta overlap");
+  attn::PagedParams p;
+  if ((st = fill_params(d, z, page_table, seq_meta, workspace, &p)) != ATTN_OK) return st;
+  p.lse_out = lse;
+  p.delta_out = delta;
+  attn::PagedMaps m;
+  std::memset(&m, 0, sizeof(m));
+  const uint64_t slots = uint64_t(d->num_pages) * d->page_size;
+  const uint32_t G = uint32_t(p.G);
+  bool enc = encode3d(&m.q_stats, q, d->key_dim, d->heads, d->num_queries, 64, G, 128 / G) &&
+             encode3d(&m.dy_stats, dy, d->value_dim, d->heads, d->num_queries, 64, G, 128 / G);
+  if (slots > 0)
+    enc = enc && encode3d(&m.k, k_pool, d->key_dim, d->kv_heads, slots, 64, 1, uint32_t(d->page_size)) &&
+          encode3d(&m.v, v_pool, d->value_dim, d->kv_heads, slots, 64, 1, uint32_t(d->page_size));
+  else
+    m.k = m.v = m.q_stats;
+  if (!enc) return api_fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  attn::timing_mark_begin(1, s);
+  cudaError_t e = attn::launch_paged_row_stats(m, p, s);
+  attn::timing_mark(s);
+  attn::timing_mark_end();
+  if (e != cudaSuccess) return api_fail(ATTN_ERR_CUDA, "row-statistics launch failed: %s", cudaGetErrorString(e));
+  return api_ok();
 }
 
 }  // extern "C"

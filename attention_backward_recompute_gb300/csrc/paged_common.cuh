@@ -1,0 +1,62 @@
+// Shared definitions of the paged-KV history kernels.
+//
+// Work decomposition (ruDNN src/paged_attention/ordered_kernel.rs,
+// history_backward: one owner per physical token x KV head, fixed traversal,
+// one final store): a CTA owns 128 consecutive history tokens (eight 16-token
+// pages) of one sequence for one KV head and accumulates their dK/dV in
+// tensor memory.  A physical page referenced by several (sequence, logical
+// page) links is stored only by the CTA of its FIRST link (smallest
+// sequence * max_pages + logical page); that CTA adds the other links'
+// contributions in increasing link order, so the sum is atomic-free and
+// bit-stable.
+#pragma once
+
+#include <cstdint>
+
+namespace attn {
+
+struct PagedParams {
+  int Nq, S, H, KVH, G;        // query rows, sequences, heads, KV heads, heads per KV head
+  int page_size;               // tokens per page (16)
+  int num_pages, max_pages;    // pool pages, page-table row length
+  int Dk, Dv, Dp;              // key, value, position dims (Dp = 0 for GQA)
+  int causal;
+  float scale, scale_log2;
+  const int32_t* page_table;   // [S, max_pages]
+  const int32_t* seq_len;      // [S]
+  const int32_t* q_start;      // [S + 1]
+  const int32_t* q_pos;        // [Nq]
+  const float* lse;            // [Nq, H] natural log (input) or output of the row-stat kernel
+  const float* delta;          // [Nq, H]
+  float* lse_out;              // row-stat kernel outputs
+  float* delta_out;
+  void* dk_pool;               // [slots, KVH, Dk]
+  void* dv_pool;               // [slots, KVH, Dv]
+  void* dkp_pool;              // [slots, KVH, Dp]
+  unsigned wrt;
+  // workspace (link structure of the pool)
+  int32_t* link_count;         // [num_pages]
+  int32_t* link_off;           // [num_pages + 1]
+  int32_t* link_fill;          // [num_pages]
+  int32_t* links;              // [S * max_pages]: link ids s*max_pages+lp grouped by page
+  uint32_t* err;
+};
+
+// device error codes of the paged prep (OR-ed into the error word)
+constexpr uint32_t kErrBadPage = 4u;   // a page-table entry outside [0, num_pages)
+
+__host__ __device__ inline int pages_of(int len, int page_size) { return (len + page_size - 1) / page_size; }
+
+#ifdef __CUDACC__
+// Metadata read through clamps, so that malformed sequence lengths or query
+// ranges can never index outside the caller's arrays.
+__device__ __forceinline__ int seq_len_of(const PagedParams& p, int s) {
+  return min(max(p.seq_len[s], 0), p.max_pages * p.page_size);
+}
+__device__ __forceinline__ int row_begin_of(const PagedParams& p, int s) { return min(max(p.q_start[s], 0), p.Nq); }
+__device__ __forceinline__ int row_end_of(const PagedParams& p, int s) {
+  return min(max(p.q_start[s + 1], row_begin_of(p, s)), p.Nq);
+}
+#endif
+
+}  // namespace attn

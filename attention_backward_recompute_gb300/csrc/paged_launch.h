@@ -1,0 +1,24 @@
+// Host-side launchers of the paged kernels (called from paged_api.cu).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "paged_common.cuh"
+
+namespace attn {
+
+// TMA descriptors of one paged call: q/dy (and qp) as 3-D [Nq, H, D] tensors
+// addressed (d, h, r), pools as 3-D [slots, KVH, D] tensors addressed (d, g, slot).
+struct PagedMaps {
+  CUtensorMap q, dy, qp;         // box (64, G, 64/G) for the history kernel
+  CUtensorMap q_stats, dy_stats; // box (64, G, 128/G) for the row-statistics kernel
+  CUtensorMap k, v, kp;          // box (64, 1, page_size)
+};
+
+cudaError_t launch_paged_prep(const PagedParams& p, cudaStream_t s);
+cudaError_t launch_paged_zero_unlinked(const PagedParams& p, cudaStream_t s);
+cudaError_t launch_paged_history(const PagedMaps& m, const PagedParams& p, cudaStream_t s);
+cudaError_t launch_paged_row_stats(const PagedMaps& m, const PagedParams& p, cudaStream_t s);
+
+}  // namespace attn

@@ -1,0 +1,144 @@
+// Paged prep: the inverse of the page table (links of every physical page in
+// a fixed order) and the zero store of pool rows no valid token owns.
+//
+// ruDNN src/paged_attention/ordered_kernel.rs builds the same inverse on the
+// host (per-page link ranges, link = (sequence, logical page)); here it is
+// built on the device from the caller's page table so the call stays
+// asynchronous:
+//   count  : links per physical page (integer atomics; the counts are exact)
+//   scan   : exclusive prefix sum -> link_off
+//   fill   : each link takes a slot of its page's segment
+//   order  : each segment is sorted by link id, which fixes the traversal
+//            order independently of the atomics above
+// and "inactive pages/tail slots also store zero": pages with no link get
+// zero dK/dV/dKp rows here; tail slots of linked pages get zero from their
+// owner CTA.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "paged_common.cuh"
+#include "paged_launch.h"
+
+namespace attn {
+namespace {
+
+__global__ void count_links_kernel(PagedParams p) {
+  const int64_t n = static_cast<int64_t>(p.S) * p.max_pages;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int s = static_cast<int>(i / p.max_pages), lp = static_cast<int>(i % p.max_pages);
+    if (lp >= pages_of(seq_len_of(p, s), p.page_size)) continue;
+    const int page = p.page_table[i];
+    if (page < 0 || page >= p.num_pages) {
+      atomicOr(p.err, kErrBadPage);
+      continue;
+    }
+    atomicAdd(&p.link_count[page], 1);
+  }
+}
+
+// single-CTA exclusive scan of link_count into link_off[0..num_pages]
+__global__ void __launch_bounds__(1024) scan_links_kernel(PagedParams p) {
+  __shared__ int warp_sums[32];
+  __shared__ int carry;
+  if (threadIdx.x == 0) carry = 0;
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int base = 0; base < p.num_pages; base += 1024) {
+    const int i = base + threadIdx.x;
+    const int v = i < p.num_pages ? p.link_count[i] : 0;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_sums[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+      int w = warp_sums[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += y;
+      }
+      warp_sums[lane] = w;
+    }
+    __syncthreads();
+    const int incl = x + (warp > 0 ? warp_sums[warp - 1] : 0) + carry;
+    if (i < p.num_pages) p.link_off[i] = incl - v;
+    __syncthreads();
+    if (threadIdx.x == 1023) carry = incl;
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) p.link_off[p.num_pages] = carry;
+}
+
+__global__ void fill_links_kernel(PagedParams p) {
+  const int64_t n = static_cast<int64_t>(p.S) * p.max_pages;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int s = static_cast<int>(i / p.max_pages), lp = static_cast<int>(i % p.max_pages);
+    if (lp >= pages_of(seq_len_of(p, s), p.page_size)) continue;
+    const int page = p.page_table[i];
+    if (page < 0 || page >= p.num_pages) continue;
+    const int slot = atomicAdd(&p.link_fill[page], 1);
+    p.links[p.link_off[page] + slot] = static_cast<int32_t>(i);
+  }
+}
+
+// insertion sort of each page's (short) link segment
+__global__ void order_links_kernel(PagedParams p) {
+  for (int page = blockIdx.x * blockDim.x + threadIdx.x; page < p.num_pages; page += gridDim.x * blockDim.x) {
+    const int a = p.link_off[page], b = p.link_off[page + 1];
+    for (int i = a + 1; i < b; ++i) {
+      const int32_t key = p.links[i];
+      int j = i - 1;
+      while (j >= a && p.links[j] > key) {
+        p.links[j + 1] = p.links[j];
+        --j;
+      }
+      p.links[j + 1] = key;
+    }
+  }
+}
+
+// zero rows of pages that no link references: one thread per 16 bytes
+__global__ void zero_unlinked_kernel(PagedParams p, void* pool, int dim) {
+  const int64_t row_vec = dim / 8;  // 16-byte vectors per pool row (bf16)
+  const int64_t per_page = static_cast<int64_t>(p.page_size) * p.KVH * row_vec;
+  const int64_t n = per_page * p.num_pages;
+  const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int page = static_cast<int>(i / per_page);
+    if (p.link_count[page] != 0) continue;
+    reinterpret_cast<uint4*>(pool)[i] = z;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_paged_prep(const PagedParams& p, cudaStream_t s) {
+  cudaError_t e;
+  if ((e = cudaMemsetAsync(p.link_count, 0, sizeof(int32_t) * p.num_pages, s)) != cudaSuccess) return e;
+  if ((e = cudaMemsetAsync(p.link_fill, 0, sizeof(int32_t) * p.num_pages, s)) != cudaSuccess) return e;
+  const int64_t nl = static_cast<int64_t>(p.S) * p.max_pages;
+  const int gl = static_cast<int>((nl + 255) / 256 < 4096 ? (nl + 255) / 256 : 4096);
+  count_links_kernel<<<gl > 0 ? gl : 1, 256, 0, s>>>(p);
+  scan_links_kernel<<<1, 1024, 0, s>>>(p);
+  fill_links_kernel<<<gl > 0 ? gl : 1, 256, 0, s>>>(p);
+  const int gp = (p.num_pages + 255) / 256;
+  order_links_kernel<<<gp > 0 ? gp : 1, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_paged_zero_unlinked(const PagedParams& p, cudaStream_t s) {
+  const int64_t blocks = 152 * 8;
+  if ((p.wrt & 2u) && p.dk_pool) zero_unlinked_kernel<<<blocks, 256, 0, s>>>(p, p.dk_pool, p.Dk);
+  if ((p.wrt & 4u) && p.dv_pool && p.Dp == 0) zero_unlinked_kernel<<<blocks, 256, 0, s>>>(p, p.dv_pool, p.Dv);
+  if ((p.wrt & 8u) && p.dkp_pool && p.Dp > 0) zero_unlinked_kernel<<<blocks, 256, 0, s>>>(p, p.dkp_pool, p.Dp);
+  return cudaGetLastError();
+}
+
+}  // namespace attn

@@ -1,0 +1,354 @@
+#!/usr/bin/env python
+"""Benchmark of the dense attention backward on GB300 (one JSON line).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one call of attn_bwd_dense (C ABI) on the workload
+``dense_bf16_s2048``: bf16 Q, K, V, dY [B=4, S=2048, H=16, D=128] ~ N(0,1)*0.5,
+causal (bottom-right) + custom per-key mask (10% zeros, < 0.5 -> -1e9) +
+additive bias [B,H,Sq,Sk] ~ N(0,1), self-contained mode (the row statistics
+are recomputed from Q, K, V, dY).  The call runs the whole hot path: the
+row-statistics prologue, the dK/dV kernel and the dQ kernel.
+
+Metric: attention-backward TFLOP/s counted as 10 * D * (visible query/key
+pairs) per head (five products of 2*D flops each), visible = allowed by the
+causal mask; custom-masked keys are computed and counted.  Inputs stay resident
+in HBM; the per-step working set (bias 512 MiB + Q, K, V, dY 128 MiB) is larger
+than the 129 MB L2, so no flush is needed between steps.
+
+Under torchrun (N > 1) every rank runs the same workload on its own GPU (weak
+scaling, no data-path collective); the time is the max over ranks.  The
+reference arm (--impl reference) times the CPU oracle on the host cores on a
+bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "attn-bwd TFLOP/s (dQ+dK+dV) on 1 GB300; % of tensor-core dense peak"
+WORKLOAD = "dense_bf16_s2048"
+WORKLOAD_DESC = ("dense SDPA backward, bf16 in / fp32 accumulate, B=4 H=16 Sq=Sk=2048 D=128, [B,S,H,D], "
+                 "N(0,1)*0.5 inputs, causal + custom per-key mask (10% zeros, thr 0.5 -> -1e9) + additive "
+                 "bias [B,H,Sq,Sk] ~ N(0,1) bf16, self-contained (row statistics recomputed)")
+
+
+def visible_pairs(sq: int, sk: int, causal: bool, window) -> int:
+    """Structurally visible (query, key) pairs, bottom-right aligned."""
+    q_off = max(sk - sq, 0)
+    tot = 0
+    for q in range(sq):
+        aq = q + q_off
+        hi = sk - 1
+        lo = 0
+        if causal or window is not None:
+            hi = min(hi, aq)
+        if window is not None:
+            lo = max(0, aq - window)
+        tot += max(0, hi - lo + 1)
+    return tot
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as fh:
+            d = json.load(fh)
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples taken while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as fh:
+            for line in fh:
+                f = [x.strip() for x in line.split(",")]
+                if len(f) < 9:
+                    continue
+                try:
+                    rows.append(dict(sm=float(f[1]), smax=float(f[2]), power=float(f[3]), hw=f[5], hwt=f[6],
+                                     swt=f[7], pcap=f[8]))
+                except ValueError:
+                    continue
+        if not rows:
+            return None
+        # samples under load: the highest-power half
+        pw = sorted(r["power"] for r in rows)
+        cut = pw[len(pw) // 2]
+        load = [r for r in rows if r["power"] >= cut] or rows
+        reasons = set()
+        for r in rows:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in load), "sm_max_mhz": max(r["smax"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows), "power_w_max": max(r["power"] for r in rows)}
+
+
+def cpu_baseline(case, budget_s: float):
+    """The oracle as it stands, on the host cores, on a bounded sample of heads."""
+    import numpy as np  # noqa: F401
+    from oracle import attn_bwd_dense
+    B, H = case.batch, case.heads
+    vp = visible_pairs(case.seq_q, case.seq_k, case.causal, case.window)
+    per_head = 10.0 * case.head_dim * vp
+    order = [(b, h) for b in range(B) for h in range(H)]
+    done = 0
+    t0 = time.perf_counter()
+    while done < len(order):
+        attn_bwd_dense(case.q, case.k, case.v, case.dy, layout=case.layout, causal=case.causal,
+                       window=case.window, key_mask=case.key_mask, bias=case.bias, heads_subset=[order[done]])
+        done += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return {"value": per_head * done / dt / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"{done} of {B * H} (batch, head) pairs of {WORKLOAD}, float64 numpy, {dt:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    """--impl reference: the CPU oracle timed on the host, K steps of one head each."""
+    if rank != 0:
+        return 0
+    from attention_backward_recompute_gb300 import inputs
+    from oracle import attn_bwd_dense
+    case = inputs.dense_config(WORKLOAD)
+    vp = visible_pairs(case.seq_q, case.seq_k, case.causal, case.window)
+    per_head = 10.0 * case.head_dim * vp
+    order = [(b, h) for b in range(case.batch) for h in range(case.heads)]
+
+    def step(i):
+        attn_bwd_dense(case.q, case.k, case.v, case.dy, layout=case.layout, causal=case.causal,
+                       window=case.window, key_mask=case.key_mask, bias=case.bias,
+                       heads_subset=[order[i % len(order)]])
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(i)
+    dt = time.perf_counter() - t0
+    value = per_head * args.steps / dt / 1e12
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD, "description": WORKLOAD_DESC,
+                       "step": "oracle backward of one (batch, head) pair of the workload"},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                             "sample": "one (batch, head) pair per step, float64 numpy"},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    import numpy as np
+    import torch
+    from attention_backward_recompute_gb300 import binding as bd
+    from attention_backward_recompute_gb300 import build, inputs
+
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    build.build()
+    bd.lib()
+
+    case = inputs.dense_config(WORKLOAD)
+    B, H, S, D = case.batch, case.heads, case.seq_q, case.head_dim
+    vp = visible_pairs(case.seq_q, case.seq_k, case.causal, case.window)
+    flops = 10.0 * D * vp * B * H
+    alg = {"prologue": 4.0 * D * vp * B * H, "dkdv": 8.0 * D * vp * B * H, "dq": 6.0 * D * vp * B * H}
+
+    host = {"q": case.q, "k": case.k, "v": case.v, "dy": case.dy, "bias": case.bias}
+    pinned = {n: torch.from_numpy(x).to(torch.bfloat16).pin_memory() for n, x in host.items()}
+    km_host = torch.from_numpy(case.key_mask).pin_memory()
+    dvc = {n: t.to(dev) for n, t in pinned.items()}
+    km = km_host.to(dev)
+    dq, dk, dv = (torch.empty_like(dvc[n]) for n in ("q", "k", "v"))
+    desc = bd.make_dense_desc(batch=B, heads=H, seq_q=S, seq_k=S, head_dim=D, causal=True, key_mask=True,
+                              bias=True)
+    ws_bytes = bd.attn_bwd_dense_workspace_bytes(desc)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = bd.ctypes.c_void_p(stream.cuda_stream)
+    P = bd._ptr
+
+    def call(qq, kk, vv, dyy, kmm, bb, oq, ok_, ov):
+        st = bd.attn_bwd_dense(desc, P(qq), P(kk), P(vv), P(dyy), P(kmm), P(bb), None, None, P(oq), P(ok_), P(ov),
+                               7, P(ws), ws_bytes, sh)
+        if st != bd.ATTN_OK:
+            raise bd.AttnError(st, bd.last_error())
+
+    def step():
+        call(dvc["q"], dvc["k"], dvc["v"], dvc["dy"], km, dvc["bias"], dq, dk, dv)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    bd.check_device_error()
+
+    # per-kernel events for every timed step
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    for row in evs:  # CUDA events are created on first record; create them before the timed region
+        for e in row:
+            e.record(stream)
+    torch.cuda.synchronize(dev)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    sampler.start()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    start.record(stream)
+    for i in range(args.steps):
+        bd.attn_set_timing_events([e.cuda_event for e in evs[i]])
+        step()
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop()
+    bd.check_device_error()
+    ms = start.elapsed_time(end) / args.steps
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    kt = {"prologue": [], "dkdv": [], "dq": []}
+    for e in evs:
+        kt["prologue"].append(e[0].elapsed_time(e[1]))
+        kt["dkdv"].append(e[1].elapsed_time(e[2]))
+        kt["dq"].append(e[2].elapsed_time(e[3]))
+    kmean = {k: sum(v) / len(v) for k, v in kt.items()}
+    dom = max(kmean, key=kmean.get)
+    peaks, peak_src = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    achieved = alg[dom] / (kmean[dom] * 1e-3) / 1e12
+    value = world * flops / (ms * 1e-3) / 1e12
+
+    # end to end through the C ABI with host buffers: H2D of every input and
+    # D2H of every gradient inside the timed region
+    h2d = sum(t.numel() * t.element_size() for t in pinned.values()) + km_host.numel() * 4
+    outs_host = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (dq, dk, dv)]
+    d2h = sum(t.numel() * t.element_size() for t in outs_host)
+    e2e_steps = max(3, args.e2e_steps)
+
+    def e2e_step():
+        for n in pinned:
+            dvc[n].copy_(pinned[n], non_blocking=True)
+        km.copy_(km_host, non_blocking=True)
+        step()
+        for h_, d_ in zip(outs_host, (dq, dk, dv)):
+            h_.copy_(d_, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = t0.elapsed_time(t1) / e2e_steps
+    if dist:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    bd.check_device_error()
+
+    if rank == 0:
+        cpu = cpu_baseline(case, args.cpu_budget) if world == 1 else None
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "description": WORKLOAD_DESC, "counted_flops_per_step": flops,
+                       "visible_pairs_per_head": vp, "l2": "inputs larger than L2 (640 MiB read per step), no flush",
+                       "parallelism": f"replicas x{world} (weak)" if world > 1 else "1 GPU",
+                       "pct_of_peak": 100.0 * value / world / peak,
+                       "kernel_ms": kmean},
+            "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
+                         "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                         "peak_source": f"{peak_src} bf16 (burst)",
+                         "algorithmic": f"{int(alg[dom] / (D * vp * B * H))}*D flops per visible pair"},
+            "cpu_baseline": cpu,
+            "clocks": clocks,
+            "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": 3 * args.steps,
+        }
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -225,6 +225,18 @@ ATTN_API const char* attn_status_string(attn_status_t s);
  */
 ATTN_API attn_status_t attn_check_device_error(void* stream);
 
+/*
+ * Per-kernel timing hook.  When `events` is non-NULL, the next dense or paged
+ * call made on this host thread records events[0] on its stream before its
+ * first kernel and events[i] after its i-th kernel (events are cudaEvent_t
+ * handles created by the caller; `count` must cover every kernel of the call
+ * plus one, else the call records nothing).  The hook applies to ONE call and
+ * is then cleared.  The dense call launches, in order: the row-statistics
+ * prologue, the dK/dV kernel (if dK or dV is requested), the dQ kernel (if dQ
+ * is requested).
+ */
+ATTN_API void attn_set_timing_events(void* const* events, int count);
+
 /* Library version, major * 10000 + minor * 100 + patch. */
 ATTN_API int attn_version(void);
 

@@ -46,16 +46,20 @@ def oracle(c, heads=None):
                           key_mask=c.key_mask, bias=c.bias, heads_subset=heads)
 
 
-def rel_err(got, want):
+def rel_err(got, want, floor=0.0):
     g = got.float().cpu().numpy().astype(np.float64)
-    return np.max(np.abs(g - want)) / max(np.max(np.abs(want)), 1e-30)
+    return np.max(np.abs(g - want)) / max(np.max(np.abs(want)), floor, 1e-30)
 
 
 def assert_close(res, ref, tol=TOL_BF16, names=("dq", "dk", "dv")):
+    # A gradient whose exact value is zero (e.g. dQ with a single key, where
+    # dS = P (dP - delta) cancels exactly) is judged against the scale of the
+    # other gradients of the same call: 1e-3 of their largest magnitude.
+    floor = 1e-3 * max(float(np.max(np.abs(w))) if w.size else 0.0 for w in ref)
     for n, g, w in zip(names, res, ref):
         if g is None:
             continue
-        e = rel_err(g, w)
+        e = rel_err(g, w, floor)
         assert e <= tol, f"{n}: max-abs-err / max|ref| = {e:.3e} > {tol}"
 
 

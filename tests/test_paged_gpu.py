@@ -1,0 +1,129 @@
+"""GPU parity of the paged history backward and the paged row statistics with
+the CPU oracle (dense re-expansion), plus bit stability and the zero store of
+slots no valid token owns.  Tolerance: 2e-2 * max|ref| per output (bf16)."""
+import numpy as np
+import pytest
+
+from attention_backward_recompute_gb300 import inputs
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+TOL = 2e-2
+
+
+@pytest.fixture(scope="module")
+def bd():
+    from attention_backward_recompute_gb300 import binding, build
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build.build()
+    binding.lib()
+    return binding
+
+
+def to_dev(c, bd):
+    t = lambda x: None if x is None else torch.from_numpy(np.ascontiguousarray(x)).cuda().to(torch.bfloat16)
+    dev = dict(q=t(c.q), dy=t(c.dy), k=t(c.k_pool), v=t(c.v_pool), qp=t(c.qp), kp=t(c.kp_pool))
+    dev["table"] = torch.from_numpy(c.page_table).cuda().contiguous()
+    dev["meta"] = bd.seq_meta_tensor(c.seq_len, c.q_start, c.q_pos, "cuda")
+    return dev
+
+
+def gpu_stats(bd, c, dv):
+    return bd.paged_row_stats(dv["q"], dv["k"], dv["v"], dv["dy"], dv["table"], dv["meta"], heads=c.heads,
+                              kv_heads=c.kv_heads, page_size=c.page_size, causal=c.causal)
+
+
+def gpu_bwd(bd, c, dv, lse, delta, outputs=None):
+    return bd.paged_backward(dv["q"], dv["k"], dv["v"], dv["dy"], dv["table"], dv["meta"], lse, delta,
+                             heads=c.heads, kv_heads=c.kv_heads, page_size=c.page_size, causal=c.causal,
+                             outputs=outputs)
+
+
+def oracle(c):
+    from oracle import attn_bwd_paged
+    return attn_bwd_paged(c.q, c.dy, c.k_pool, c.page_table, c.seq_len, c.q_start, c.q_pos,
+                          page_size=c.page_size, kv_heads=c.kv_heads, v_pool=c.v_pool, causal=c.causal,
+                          return_stats=True)
+
+
+def rel(got, want, mask=None):
+    g = got.float().cpu().numpy().astype(np.float64)
+    if mask is not None:
+        g, want = g[mask], want[mask]
+    return np.max(np.abs(g - want)) / max(np.max(np.abs(want)), 1e-30)
+
+
+CASES = [
+    dict(seed=21, num_seqs=5, len_lo=20, len_hi=300, queries_per_seq=40, heads=8, kv_heads=2, key_dim=128,
+         value_dim=128, causal=True),
+    dict(seed=22, num_seqs=4, len_lo=100, len_hi=520, queries_per_seq=64, heads=32, kv_heads=8, key_dim=128,
+         value_dim=128, causal=True),
+    dict(seed=23, num_seqs=3, len_lo=5, len_hi=200, queries_per_seq=20, heads=4, kv_heads=4, key_dim=64,
+         value_dim=64, causal=False),
+    dict(seed=24, num_seqs=4, len_lo=40, len_hi=260, queries_per_seq=24, heads=8, kv_heads=2, key_dim=128,
+         value_dim=128, causal=True, shared_prefix_pages=3),
+]
+
+
+@pytest.mark.parametrize("kw", CASES, ids=lambda k: f"seed{k['seed']}")
+def test_paged_parity(bd, kw):
+    c = inputs.paged_case(name="t", scale=0.5, **kw)
+    dv = to_dev(c, bd)
+    dk_ref, dv_ref, lse_ref, delta_ref = oracle(c)
+    lse, delta = gpu_stats(bd, c, dv)
+    bd.check_device_error()
+    fin = np.isfinite(lse_ref)
+    assert np.max(np.abs(lse.cpu().numpy()[fin] - lse_ref[fin])) < 2e-2
+    assert rel(delta, delta_ref) < TOL
+    dk, dvv = gpu_bwd(bd, c, dv, lse, delta)
+    bd.check_device_error()
+    assert rel(dk, dk_ref) < TOL
+    assert rel(dvv, dv_ref) < TOL
+    # rows of slots no valid token owns are exactly zero (pools are NaN there)
+    valid = np.zeros(c.num_pages * c.page_size, bool)
+    for s in range(c.num_seqs):
+        for t in range(int(c.seq_len[s])):
+            valid[int(c.page_table[s, t // c.page_size]) * c.page_size + t % c.page_size] = True
+    assert torch.all(dk[torch.from_numpy(~valid).cuda()] == 0)
+    assert torch.all(dvv[torch.from_numpy(~valid).cuda()] == 0)
+    assert torch.isfinite(dk).all() and torch.isfinite(dvv).all()
+
+
+def test_paged_bit_stable(bd):
+    c = inputs.paged_case(name="t", seed=31, num_seqs=6, len_lo=50, len_hi=700, queries_per_seq=64, heads=32,
+                          kv_heads=8, key_dim=128, value_dim=128, scale=0.5, shared_prefix_pages=2)
+    dv = to_dev(c, bd)
+    lse, delta = gpu_stats(bd, c, dv)
+    first = gpu_bwd(bd, c, dv, lse, delta)
+    for _ in range(5):
+        again = gpu_bwd(bd, c, dv, lse, delta)
+        for a, b in zip(first, again):
+            assert torch.equal(a, b)
+    bd.check_device_error()
+
+
+def test_paged_full_size_gqa_sampled(bd):
+    """The full GQA configuration (64 sequences, lengths U[128,4096]); the
+    oracle re-expands a sample of sequences and the slots they own are compared."""
+    c = inputs.paged_config("paged_gqa")
+    dv = to_dev(c, bd)
+    lse, delta = gpu_stats(bd, c, dv)
+    dk, dvv = gpu_bwd(bd, c, dv, lse, delta)
+    bd.check_device_error()
+    from oracle import attn_bwd_paged
+    pick = [0, 17, 63]
+    qs = [np.arange(c.q_start[s], c.q_start[s + 1]) for s in pick]
+    rows = np.concatenate(qs)
+    sub_start = np.concatenate([[0], np.cumsum([len(x) for x in qs])]).astype(np.int32)
+    ref_dk, ref_dv, ref_lse, ref_delta = attn_bwd_paged(
+        c.q[rows], c.dy[rows], c.k_pool, c.page_table[pick], c.seq_len[pick], sub_start, c.q_pos[rows],
+        page_size=c.page_size, kv_heads=c.kv_heads, v_pool=c.v_pool, causal=True, return_stats=True)
+    owned = np.zeros(c.num_pages * c.page_size, bool)
+    for s in pick:
+        for t in range(int(c.seq_len[s])):
+            owned[int(c.page_table[s, t // c.page_size]) * c.page_size + t % c.page_size] = True
+    assert rel(dk, ref_dk, owned) < TOL
+    assert rel(dvv, ref_dv, owned) < TOL
+    assert np.max(np.abs(lse.cpu().numpy()[rows] - ref_lse)) < 2e-2
