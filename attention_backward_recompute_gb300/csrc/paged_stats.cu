@@ -264,6 +264,21 @@ __global__ void __launch_bounds__(256, 1)
         }
         tmem_st_wait();
       }
+      // Slots past the sequence's length inside its last page may hold any bit
+      // pattern (NaN included); the tensor core would turn 0 * NaN into NaN in
+      // O += P V, so their V rows are zeroed before the product reads them.
+      if (tk0 + L::BK > len) {
+        // the stage's copies have landed (observed here, not only by the MMA thread)
+        if (!(ok = mbar_wait_warp(&bar_full[s], (t >> 1) & 1, ab))) break;
+        const int row_lo = max(0, len - tk0);
+        const int nvec = (L::BK - row_lo) * L::NCH * 8;
+        uint8_t* vt = sm + L::V_OFF + s * L::KT;
+        for (int i = threadIdx.x - 128; i < nvec; i += 128) {
+          const int rw = row_lo + i / (L::NCH * 8), rem = i % (L::NCH * 8);
+          const int ch = rem >> 3, seg = rem & 7;
+          st_shared_v4(smem_addr(vt + ch * (L::BK * 128) + rw * 128 + seg * 16), 0u, 0u, 0u, 0u);
+        }
+      }
       if (t >= 2 && !(ok = mbar_wait_warp(&bar_p_free[s], ((t - 2) >> 1) & 1, ab))) break;
       const uint32_t sp = smem_addr(sm + L::P_OFF + s * L::PT);
 #pragma unroll

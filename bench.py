@@ -193,6 +193,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--batch", type=int, default=None, help="override B (profiling runs on a smaller case)")
+    ap.add_argument("--heads", type=int, default=None, help="override H (profiling runs on a smaller case)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -216,7 +218,8 @@ def main():
     build.build()
     bd.lib()
 
-    case = inputs.dense_config(WORKLOAD)
+    over = {k: v for k, v in (("batch", args.batch), ("heads", args.heads)) if v is not None}
+    case = inputs.dense_config(WORKLOAD, **over)
     B, H, S, D = case.batch, case.heads, case.seq_q, case.head_dim
     vp = visible_pairs(case.seq_q, case.seq_k, case.causal, case.window)
     flops = 10.0 * D * vp * B * H
@@ -323,12 +326,13 @@ def main():
     bd.check_device_error()
 
     if rank == 0:
-        cpu = cpu_baseline(case, args.cpu_budget) if world == 1 else None
+        cpu = cpu_baseline(case, args.cpu_budget) if world == 1 and args.cpu_budget > 0 else None
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "description": WORKLOAD_DESC, "counted_flops_per_step": flops,
+            "config": {"workload": WORKLOAD if not over else f"{WORKLOAD} with {over}", "description": WORKLOAD_DESC,
+                       "counted_flops_per_step": flops,
                        "visible_pairs_per_head": vp, "l2": "inputs larger than L2 (640 MiB read per step), no flush",
                        "parallelism": f"replicas x{world} (weak)" if world > 1 else "1 GPU",
                        "pct_of_peak": 100.0 * value / world / peak,
