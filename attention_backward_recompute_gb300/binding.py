@@ -69,6 +69,8 @@ _SIG = {
     "attn_bwd_dense_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(attn_dense_desc)]),
     "attn_bwd_dense": (ctypes.c_int32, [ctypes.POINTER(attn_dense_desc), _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                         _P, ctypes.c_uint, _P, ctypes.c_size_t, _P]),
+    "attn_bwd_dense_noalloc": (ctypes.c_int32, [ctypes.POINTER(attn_dense_desc), _P, _P, _P, _P, _P, _P, _P, _P,
+                                                _P, _P, _P, ctypes.c_uint, _P]),
     "attn_bwd_paged_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(attn_paged_desc)]),
     "attn_bwd_paged": (ctypes.c_int32, [ctypes.POINTER(attn_paged_desc), _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                         _P, _P, _P, ctypes.c_uint, _P, ctypes.c_size_t, _P]),
@@ -128,6 +130,12 @@ def attn_bwd_dense(desc, q, k, v, dy, key_mask, bias, o, lse, dq, dk, dv, wrt_ma
                    workspace_bytes, stream) -> int:
     return int(lib().attn_bwd_dense(ctypes.byref(desc), q, k, v, dy, key_mask, bias, o, lse, dq, dk, dv,
                                     wrt_mask, workspace, workspace_bytes, stream))
+
+
+def attn_bwd_dense_noalloc(desc, q, k, v, dy, key_mask, bias, o, lse, dq, dk, dv, wrt_mask, stream) -> int:
+    """Dense backward with the library-owned scratch (no workspace argument)."""
+    return int(lib().attn_bwd_dense_noalloc(ctypes.byref(desc), q, k, v, dy, key_mask, bias, o, lse, dq, dk, dv,
+                                            wrt_mask, stream))
 
 
 def attn_bwd_paged_workspace_bytes(desc: attn_paged_desc) -> int:

@@ -137,6 +137,35 @@ ATTN_API attn_status_t attn_bwd_dense(const attn_dense_desc* d, const void* q, c
                                       void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Dense backward that allocates nothing and takes no workspace.  (The pages
+ * have no counterpart: this entry point exists for callers of this library.)
+ *
+ * Some callers cannot call cudaMalloc: plugin code running inside a host
+ * framework whose device memory belongs to that framework's allocator, or a
+ * serving loop that forbids allocation on its hot path.  For them the row
+ * statistics live in a scratch array owned by the library: a file-scope
+ * device array of ATTN_NOALLOC_MAX_ROWS * 12 bytes (about 12 MiB), which every
+ * GPU that loads the library holds until the process exits.  The caller still
+ * passes every input and output; arguments, layouts and results are those of
+ * attn_bwd_dense, whose outputs this call reproduces.
+ *
+ *   - batch * heads * seq_q above ATTN_NOALLOC_MAX_ROWS is rejected with
+ *     ATTN_ERR_UNSUPPORTED (use attn_bwd_dense with a workspace instead).
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress; it allocates nothing) with that device current;
+ *     make that first call before any stream capture.
+ *   - All calls share the one array and it keeps the last call's contents.
+ *     Calls whose kernels overlap on the GPU (other streams, other host
+ *     threads) race on it: serialise them.
+ *   - No cudaMalloc, cudaFree or allocating library routine is called.
+ */
+#define ATTN_NOALLOC_MAX_ROWS 1048576
+ATTN_API attn_status_t attn_bwd_dense_noalloc(const attn_dense_desc* d, const void* q, const void* k, const void* v,
+                                              const void* dy, const float* key_mask, const void* bias,
+                                              const void* o, const float* lse, void* dq, void* dk, void* dv,
+                                              unsigned wrt_mask, void* stream);
+
+/*
  * Paged KV history.
  *
  * Pools hold `num_pages * page_size` slots; slot = page * page_size + offset,
