@@ -176,7 +176,11 @@ def attn_version() -> int:
 # ---- torch helpers (argument marshalling only) ------------------------------
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors passed to libattnbwd must be contiguous (the ABI takes dense layouts)")
+    return ctypes.c_void_p(t.data_ptr())
 
 
 def _stream_handle(stream):

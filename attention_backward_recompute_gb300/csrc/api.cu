@@ -143,6 +143,7 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct DenseSizes {
   size_t es, q_bytes, k_bytes, bias_bytes, mask_bytes, stat_bytes, ws_bytes;
+  size_t split_off;  // fp32 storage: offset of the hi/lo bf16 copies of q, k, v, dy
 };
 
 attn_status_t check_dense_desc(const attn_dense_desc* d, DenseSizes* z) {
@@ -160,8 +161,8 @@ attn_status_t check_dense_desc(const attn_dense_desc* d, DenseSizes* z) {
   if (!std::isfinite(d->mask_thr)) return api_fail(ATTN_ERR_INVALID_ARG, "mask_thr must be finite");
   if (!std::isfinite(d->scale) || d->scale < 0.f) return api_fail(ATTN_ERR_INVALID_ARG, "scale must be finite and >= 0");
   const int64_t D = d->head_dim;
-  if (D != 16 && D != 32 && D != 64 && D != 128)
-    return api_fail(ATTN_ERR_UNSUPPORTED, "head_dim %lld not supported (16, 32, 64, 128)", (long long)D);
+  if (D != 8 && D != 16 && D != 32 && D != 64 && D != 128)
+    return api_fail(ATTN_ERR_UNSUPPORTED, "head_dim %lld not supported (8, 16, 32, 64, 128)", (long long)D);
   const int64_t lim = int64_t(1) << 31;
   if (d->batch * d->heads >= lim || d->seq_q >= lim || d->seq_k >= lim || d->batch * d->heads * d->seq_q >= lim)
     return api_fail(ATTN_ERR_UNSUPPORTED, "sizes exceed 32-bit indexing");
@@ -172,7 +173,16 @@ attn_status_t check_dense_desc(const attn_dense_desc* d, DenseSizes* z) {
   z->bias_bytes = size_t(d->batch) * d->heads * d->seq_q * d->seq_k * z->es;
   z->mask_bytes = size_t(d->batch) * d->seq_k * 4;
   z->stat_bytes = size_t(d->batch) * d->heads * d->seq_q * 4;
-  z->ws_bytes = 3 * align256(z->stat_bytes);
+  z->split_off = 3 * align256(z->stat_bytes);
+  z->ws_bytes = z->split_off;
+  if (d->dtype == ATTN_DTYPE_F32) {
+    // fp32 storage runs on bf16 tensor cores with every operand split into
+    // hi + lo bf16 copies (three products per GEMM); head_dim <= 64 fits the
+    // doubled tiles in shared memory.
+    if (D > 64) return api_fail(ATTN_ERR_UNSUPPORTED, "fp32 storage supports head_dim <= 64");
+    if (d->mask_flags & ATTN_MASK_BIAS) return api_fail(ATTN_ERR_UNSUPPORTED, "fp32 storage does not take a bias");
+    z->ws_bytes += 4 * align256(z->q_bytes / 2) + 4 * align256(z->k_bytes / 2);
+  }
   if (z->ws_bytes == 0) z->ws_bytes = 256;
   return ATTN_OK;
 }
@@ -244,7 +254,7 @@ ATTN_API attn_status_t attn_bwd_dense(const attn_dense_desc* d, const void* q, c
   if (!workspace || workspace_bytes < z.ws_bytes)
     return api_fail(ATTN_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", z.ws_bytes, workspace_bytes);
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return api_fail(ATTN_ERR_WORKSPACE, "workspace must be 256-byte aligned");
-  if (d->dtype != ATTN_DTYPE_BF16) return api_fail(ATTN_ERR_UNSUPPORTED, "f32 storage is not available in this build");
+  const bool split = d->dtype == ATTN_DTYPE_F32;
 
   attn::DenseParams p{};
   p.B = int(B); p.H = int(H); p.Sq = int(Sq); p.Sk = int(Sk); p.D = int(D);
@@ -275,19 +285,42 @@ ATTN_API attn_status_t attn_bwd_dense(const attn_dense_desc* d, const void* q, c
   p.err = device_error_word();
   if (!p.err) return api_fail(ATTN_ERR_CUDA, "no CUDA device / symbol address unavailable");
 
+  // fp32 storage: the tensor-core operands are hi/lo bf16 copies of q, k, v, dy
+  // (same layout, bf16 elements) made by a split kernel into the workspace.
+  const void *qa = q, *ka = k, *va = v, *dya = dy;
+  const void *ql = q, *kl = k, *vl = v, *dyl = dy;
+  if (split) {
+    uint8_t* c = ws + z.split_off;
+    const size_t qc = align256(z.q_bytes / 2), kc = align256(z.k_bytes / 2);
+    void* parts[8] = {c, c + qc, c + 2 * qc, c + 3 * qc, c + 4 * qc, c + 4 * qc + kc, c + 4 * qc + 2 * kc,
+                      c + 4 * qc + 3 * kc};
+    qa = parts[0]; ql = parts[1]; dya = parts[2]; dyl = parts[3];
+    ka = parts[4]; kl = parts[5]; va = parts[6]; vl = parts[7];
+  }
   // TMA descriptors: (d, s, h, b) with byte strides of s, h, b
   const CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  const uint64_t es = z.es;
+  const uint64_t es = 2;  // the tensor-core operands are always bf16
   const uint64_t qdims[4] = {uint64_t(D), uint64_t(Sq), uint64_t(H), uint64_t(B)};
   const uint64_t kdims[4] = {uint64_t(D), uint64_t(Sk), uint64_t(H), uint64_t(B)};
   const uint64_t qstr[3] = {uint64_t(p.q_ss) * es, uint64_t(p.q_sh) * es, uint64_t(p.q_sb) * es};
   const uint64_t kstr[3] = {uint64_t(p.k_ss) * es, uint64_t(p.k_sh) * es, uint64_t(p.k_sb) * es};
   attn::DenseMaps m;
   std::memset(&m, 0, sizeof(m));
-  bool enc = encode4d(&m.q64, dt, q, qdims, qstr, 64, 64) && encode4d(&m.q128, dt, q, qdims, qstr, 64, 128) &&
-             encode4d(&m.dy64, dt, dy, qdims, qstr, 64, 64) && encode4d(&m.dy128, dt, dy, qdims, qstr, 64, 128) &&
-             encode4d(&m.k64, dt, k, kdims, kstr, 64, 64) && encode4d(&m.k128, dt, k, kdims, kstr, 64, 128) &&
-             encode4d(&m.v64, dt, v, kdims, kstr, 64, 64) && encode4d(&m.v128, dt, v, kdims, kstr, 64, 128);
+  m.split = split;
+  bool enc = encode4d(&m.q64, dt, qa, qdims, qstr, 64, 64) && encode4d(&m.q128, dt, qa, qdims, qstr, 64, 128) &&
+             encode4d(&m.dy64, dt, dya, qdims, qstr, 64, 64) && encode4d(&m.dy128, dt, dya, qdims, qstr, 64, 128) &&
+             encode4d(&m.k64, dt, ka, kdims, kstr, 64, 64) && encode4d(&m.k128, dt, ka, kdims, kstr, 64, 128) &&
+             encode4d(&m.v64, dt, va, kdims, kstr, 64, 64) && encode4d(&m.v128, dt, va, kdims, kstr, 64, 128);
+  if (enc && split) {
+    enc = encode4d(&m.q64_lo, dt, ql, qdims, qstr, 64, 64) && encode4d(&m.q128_lo, dt, ql, qdims, qstr, 64, 128) &&
+          encode4d(&m.dy64_lo, dt, dyl, qdims, qstr, 64, 64) &&
+          encode4d(&m.dy128_lo, dt, dyl, qdims, qstr, 64, 128) && encode4d(&m.k64_lo, dt, kl, kdims, kstr, 64, 64) &&
+          encode4d(&m.k128_lo, dt, kl, kdims, kstr, 64, 128) && encode4d(&m.v64_lo, dt, vl, kdims, kstr, 64, 64) &&
+          encode4d(&m.v128_lo, dt, vl, kdims, kstr, 64, 128);
+  } else if (enc) {
+    m.q64_lo = m.q64; m.q128_lo = m.q128; m.dy64_lo = m.dy64; m.dy128_lo = m.dy128;
+    m.k64_lo = m.k64; m.k128_lo = m.k128; m.v64_lo = m.v64; m.v128_lo = m.v128;
+  }
   if (enc && has_bias) {
     const uint64_t bdims[4] = {uint64_t(Sk), uint64_t(Sq), uint64_t(H), uint64_t(B)};
     const uint64_t bstr[3] = {uint64_t(Sk) * es, uint64_t(Sq * Sk) * es, uint64_t(H * Sq * Sk) * es};
@@ -298,10 +331,24 @@ ATTN_API attn_status_t attn_bwd_dense(const attn_dense_desc* d, const void* q, c
   }
   if (!enc) return api_fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed (driver entry point or arguments)");
 
-  const int nk = 1 + (want_dk || want_dv ? 1 : 0) + (want_dq ? 1 : 0);
+  const int nk = (split ? 4 : 0) + 1 + (want_dk || want_dv ? 1 : 0) + (want_dq ? 1 : 0);
   attn::timing_mark_begin(nk, s);
-  cudaError_t e = o ? attn::launch_delta_only(p, 1, s) : attn::launch_fwd_stats(m, p, has_bias, s);
-  attn::timing_mark(s);
+  cudaError_t e = cudaSuccess;
+  if (split) {
+    const int64_t nq = int64_t(z.q_bytes / 4), nkv = int64_t(z.k_bytes / 4);
+    const float* srcs[4] = {static_cast<const float*>(q), static_cast<const float*>(dy), static_cast<const float*>(k),
+                            static_cast<const float*>(v)};
+    void* his[4] = {const_cast<void*>(qa), const_cast<void*>(dya), const_cast<void*>(ka), const_cast<void*>(va)};
+    void* los[4] = {const_cast<void*>(ql), const_cast<void*>(dyl), const_cast<void*>(kl), const_cast<void*>(vl)};
+    for (int i = 0; i < 4 && e == cudaSuccess; ++i) {
+      e = attn::launch_split_f32(srcs[i], his[i], los[i], i < 2 ? nq : nkv, s);
+      attn::timing_mark(s);
+    }
+  }
+  if (e == cudaSuccess) {
+    e = o ? attn::launch_delta_only(p, split ? 0 : 1, s) : attn::launch_fwd_stats(m, p, has_bias, s);
+    attn::timing_mark(s);
+  }
   if (e == cudaSuccess && (want_dk || want_dv)) {
     e = attn::launch_dkdv(m, p, has_bias, s);
     attn::timing_mark(s);

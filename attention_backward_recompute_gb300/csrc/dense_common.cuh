@@ -105,3 +105,67 @@ __host__ __device__ inline int visible_keys(const DenseParams& p, int q) {
 }
 
 }  // namespace attn
+
+#ifdef __CUDACC__
+#include <cuda_bf16.h>
+
+#include "sm103.cuh"
+
+namespace attn {
+
+// Write 32 values (columns c0..c0+31 of `row`) into a 128-byte-swizzled
+// K-major bf16 tile at shared address `tile`.  With SPLIT the value is stored
+// as two bf16 copies, hi = bf16(x) at `tile` and lo = bf16(x - hi) at
+// `tile + copy_bytes`, so that hi + lo carries about 16 significant bits.
+template <bool SPLIT>
+__device__ __forceinline__ void store_row32(uint32_t tile, uint32_t copy_bytes, int row, int c0, const float* x) {
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    uint32_t hi[4], lo[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float a = x[8 * j + 2 * e], b = x[8 * j + 2 * e + 1];
+      const __nv_bfloat162 h2 = __floats2bfloat162_rn(a, b);
+      hi[e] = *reinterpret_cast<const uint32_t*>(&h2);
+      if (SPLIT) {
+        const __nv_bfloat162 l2 = __floats2bfloat162_rn(a - __low2float(h2), b - __high2float(h2));
+        lo[e] = *reinterpret_cast<const uint32_t*>(&l2);
+      }
+    }
+    const uint32_t off = sm103::sw128_offset(row, (c0 >> 3) + j);
+    sm103::st_shared_v4(tile + off, hi[0], hi[1], hi[2], hi[3]);
+    if (SPLIT) sm103::st_shared_v4(tile + copy_bytes + off, lo[0], lo[1], lo[2], lo[3]);
+  }
+}
+
+// Store 32 fp32 accumulator values (times f) of one output row, columns
+// col0..col0+31 limited to D: bf16 (round to nearest even) or, with SPLIT
+// (fp32 storage), fp32.  `row_off` is the row's element offset.
+template <bool SPLIT>
+__device__ __forceinline__ void store_out32(void* out, int64_t row_off, int col0, int D, const uint32_t (&r)[32],
+                                            float f) {
+  if (SPLIT) {
+    float* o = reinterpret_cast<float*>(out) + row_off + col0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (col0 + 4 * j < D)
+        *reinterpret_cast<float4*>(o + 4 * j) =
+            make_float4(__uint_as_float(r[4 * j]) * f, __uint_as_float(r[4 * j + 1]) * f,
+                        __uint_as_float(r[4 * j + 2]) * f, __uint_as_float(r[4 * j + 3]) * f);
+  } else {
+    __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(out) + row_off + col0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (col0 + 8 * j < D) {
+        uint4 v;
+        v.x = sm103::pack_bf16x2(__uint_as_float(r[8 * j]) * f, __uint_as_float(r[8 * j + 1]) * f);
+        v.y = sm103::pack_bf16x2(__uint_as_float(r[8 * j + 2]) * f, __uint_as_float(r[8 * j + 3]) * f);
+        v.z = sm103::pack_bf16x2(__uint_as_float(r[8 * j + 4]) * f, __uint_as_float(r[8 * j + 5]) * f);
+        v.w = sm103::pack_bf16x2(__uint_as_float(r[8 * j + 6]) * f, __uint_as_float(r[8 * j + 7]) * f);
+        *reinterpret_cast<uint4*>(o + 8 * j) = v;
+      }
+  }
+}
+
+}  // namespace attn
+#endif

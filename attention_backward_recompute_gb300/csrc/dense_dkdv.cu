@@ -23,22 +23,23 @@ using namespace sm103;
 
 namespace {
 
-template <int DP>
+template <int DP, bool SPLIT>
 struct DkdvLayout {
   static constexpr int NCH = DP / 64;          // 128-byte column chunks of a row
+  static constexpr int NSP = SPLIT ? 2 : 1;    // copies of every operand tile (hi, lo)
   static constexpr int BK = 128, BQ = 64;
-  static constexpr int KV = NCH * BK * 128;     // bytes of K (or V) tile
-  static constexpr int QT = NCH * BQ * 128;     // bytes of a Q (or dY) tile
-  static constexpr int BIAS = 2 * BQ * 128;     // two 64-key halves of 64 query rows
+  static constexpr int KV = NCH * BK * 128;     // bytes of one copy of the K (or V) tile
+  static constexpr int QT = NCH * BQ * 128;     // bytes of one copy of a Q (or dY) tile
+  static constexpr int BIAS = SPLIT ? 0 : 2 * BQ * 128;  // two 64-key halves of 64 query rows
   static constexpr int PT = BK * 128;           // P^T / dS^T: 128 keys x 64 queries bf16
   static constexpr int K_OFF = 0;
-  static constexpr int V_OFF = K_OFF + KV;
-  static constexpr int Q_OFF = V_OFF + KV;      // 2 stages
-  static constexpr int DY_OFF = Q_OFF + 2 * QT;  // 2 stages
-  static constexpr int BIAS_OFF = DY_OFF + 2 * QT;  // 2 stages
-  static constexpr int P_OFF = BIAS_OFF + 2 * BIAS;
-  static constexpr int DS_OFF = P_OFF + PT;
-  static constexpr int ST_OFF = DS_OFF + PT;    // 2 stages x {L2, delta, pm} x 64 floats
+  static constexpr int V_OFF = K_OFF + NSP * KV;
+  static constexpr int Q_OFF = V_OFF + NSP * KV;          // 2 stages x NSP copies
+  static constexpr int DY_OFF = Q_OFF + 2 * NSP * QT;      // 2 stages x NSP copies
+  static constexpr int BIAS_OFF = DY_OFF + 2 * NSP * QT;   // 2 stages
+  static constexpr int P_OFF = BIAS_OFF + 2 * BIAS;        // NSP copies
+  static constexpr int DS_OFF = P_OFF + NSP * PT;          // NSP copies
+  static constexpr int ST_OFF = DS_OFF + NSP * PT;         // 2 stages x {L2, delta, pm} x 64 floats
   static constexpr int BYTES = ST_OFF + 2 * 3 * BQ * 4;
   static constexpr int TMEM_COLS = (2 * DP + 128) <= 256 ? 256 : 512;
   // TMEM columns: dV [0, DP), dK [DP, 2DP), S^T [2DP, 2DP+64), dP^T [2DP+64, 2DP+128)
@@ -52,12 +53,14 @@ __device__ __forceinline__ bool drain_wait(uint64_t* bar, uint32_t parity) {
   return true;
 }
 
-template <int DP, bool HAS_BIAS>
+template <int DP, bool HAS_BIAS, bool SPLIT>
 __global__ void __launch_bounds__(384, 1)
     dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_dy,
-                const __grid_constant__ CUtensorMap tm_bias, const DenseParams p) {
-  using L = DkdvLayout<DP>;
+                const __grid_constant__ CUtensorMap tm_bias, const __grid_constant__ CUtensorMap tm_q_lo,
+                const __grid_constant__ CUtensorMap tm_k_lo, const __grid_constant__ CUtensorMap tm_v_lo,
+                const __grid_constant__ CUtensorMap tm_dy_lo, const DenseParams p) {
+  using L = DkdvLayout<DP, SPLIT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ uint64_t bar_kv, bar_full[2], bar_empty[2], bar_s_full, bar_dp_full, bar_p_full, bar_ds_full,
@@ -109,11 +112,12 @@ __global__ void __launch_bounds__(384, 1)
       tma_prefetch_map(&tm_v);
       tma_prefetch_map(&tm_dy);
       if (HAS_BIAS) tma_prefetch_map(&tm_bias);
-      mbar_arrive_expect_tx(&bar_kv, 2 * L::KV);
-      for (int c = 0; c < L::NCH; ++c) {
-        tma_load_4d(sm + L::K_OFF + c * (L::BK * 128), &tm_k, &bar_kv, c * 64, k0, h, b);
-        tma_load_4d(sm + L::V_OFF + c * (L::BK * 128), &tm_v, &bar_kv, c * 64, k0, h, b);
-      }
+      mbar_arrive_expect_tx(&bar_kv, 2 * L::NSP * L::KV);
+      for (int hl = 0; hl < L::NSP; ++hl)
+        for (int c = 0; c < L::NCH; ++c) {
+          tma_load_4d(sm + L::K_OFF + hl * L::KV + c * (L::BK * 128), hl ? &tm_k_lo : &tm_k, &bar_kv, c * 64, k0, h, b);
+          tma_load_4d(sm + L::V_OFF + hl * L::KV + c * (L::BK * 128), hl ? &tm_v_lo : &tm_v, &bar_kv, c * 64, k0, h, b);
+        }
     }
     int last_use[2] = {-1, -1};
     bool ok = true;
@@ -123,12 +127,14 @@ __global__ void __launch_bounds__(384, 1)
       if (!ok) break;
       const int q0 = (i_lo + t) * L::BQ;
       if (lane == 0) {
-        const uint32_t bytes = 2 * L::QT + (HAS_BIAS ? L::BIAS : 0);
+        const uint32_t bytes = 2 * L::NSP * L::QT + (HAS_BIAS ? L::BIAS : 0);
         mbar_arrive_expect_tx(&bar_full[s], bytes);
-        for (int c = 0; c < L::NCH; ++c) {
-          tma_load_4d(sm + L::Q_OFF + s * L::QT + c * (L::BQ * 128), &tm_q, &bar_full[s], c * 64, q0, h, b);
-          tma_load_4d(sm + L::DY_OFF + s * L::QT + c * (L::BQ * 128), &tm_dy, &bar_full[s], c * 64, q0, h, b);
-        }
+        for (int hl = 0; hl < L::NSP; ++hl)
+          for (int c = 0; c < L::NCH; ++c) {
+            const int o = (s * L::NSP + hl) * L::QT + c * (L::BQ * 128);
+            tma_load_4d(sm + L::Q_OFF + o, hl ? &tm_q_lo : &tm_q, &bar_full[s], c * 64, q0, h, b);
+            tma_load_4d(sm + L::DY_OFF + o, hl ? &tm_dy_lo : &tm_dy, &bar_full[s], c * 64, q0, h, b);
+          }
         if (HAS_BIAS) {
           uint8_t* bs = sm + L::BIAS_OFF + s * L::BIAS;
           tma_load_4d(bs, &tm_bias, &bar_full[s], k0, q0, h, b);
@@ -161,25 +167,36 @@ __global__ void __launch_bounds__(384, 1)
       constexpr uint32_t id_acc = idesc_bf16(128, DP, false, true);
       const uint32_t sK = smem_addr(sm + L::K_OFF), sV = smem_addr(sm + L::V_OFF);
       const uint32_t sP = smem_addr(sm + L::P_OFF), sDS = smem_addr(sm + L::DS_OFF);
-      auto q_at = [&](int s) { return smem_addr(sm + L::Q_OFF + s * L::QT); };
-      auto dy_at = [&](int s) { return smem_addr(sm + L::DY_OFF + s * L::QT); };
+      auto q_at = [&](int s) { return smem_addr(sm + L::Q_OFF + s * L::NSP * L::QT); };
+      auto dy_at = [&](int s) { return smem_addr(sm + L::DY_OFF + s * L::NSP * L::QT); };
+      // Split operands: x = hi + lo (two bf16 copies); a product is
+      // hi*hi + hi*lo + lo*hi, all accumulated in fp32.
+      constexpr int NPROD = SPLIT ? 3 : 1;
       // X^T-product: D[128 x 64] = A_tile[128 x DP] * B_tile[64 x DP]^T, both K-major.
       auto issue_xt = [&](uint32_t d, uint32_t a_base, uint32_t b_base) {
 #pragma unroll
-        for (int kk = 0; kk < DP / 16; ++kk) {
-          const int c = kk >> 2, o = (kk & 3) * 32;
-          const uint64_t ad = sdesc_sw128(a_base + c * (L::BK * 128) + o, 16, 1024);
-          const uint64_t bd = sdesc_sw128(b_base + c * (L::BQ * 128) + o, 16, 1024);
-          mma_bf16_ss(d, ad, bd, id_s, kk > 0 ? 1u : 0u);
+        for (int pr = 0; pr < NPROD; ++pr) {
+          const uint32_t a0 = a_base + (pr == 2 ? L::KV : 0), b0 = b_base + (pr == 1 ? L::QT : 0);
+#pragma unroll
+          for (int kk = 0; kk < DP / 16; ++kk) {
+            const int c = kk >> 2, o = (kk & 3) * 32;
+            const uint64_t ad = sdesc_sw128(a0 + c * (L::BK * 128) + o, 16, 1024);
+            const uint64_t bd = sdesc_sw128(b0 + c * (L::BQ * 128) + o, 16, 1024);
+            mma_bf16_ss(d, ad, bd, id_s, (pr > 0 || kk > 0) ? 1u : 0u);
+          }
         }
       };
       // accumulate: D[128 x DP] += A[128 x 64] (K-major) * B[64 x DP] (MN-major)
       auto issue_acc = [&](uint32_t d, uint32_t a_base, uint32_t b_base, bool first) {
 #pragma unroll
-        for (int kk = 0; kk < L::BQ / 16; ++kk) {
-          const uint64_t ad = sdesc_sw128(a_base + kk * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(b_base + kk * 16 * 128, L::BQ * 128, 1024);
-          mma_bf16_ss(d, ad, bd, id_acc, (first && kk == 0) ? 0u : 1u);
+        for (int pr = 0; pr < NPROD; ++pr) {
+          const uint32_t a0 = a_base + (pr == 2 ? L::PT : 0), b0 = b_base + (pr == 1 ? L::QT : 0);
+#pragma unroll
+          for (int kk = 0; kk < L::BQ / 16; ++kk) {
+            const uint64_t ad = sdesc_sw128(a0 + kk * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(b0 + kk * 16 * 128, L::BQ * 128, 1024);
+            mma_bf16_ss(d, ad, bd, id_acc, (first && pr == 0 && kk == 0) ? 0u : 1u);
+          }
         }
       };
       bool ok = mbar_wait(&bar_kv, 0, ab);
@@ -260,11 +277,7 @@ __global__ void __launch_bounds__(384, 1)
           pr[c] = vis ? pv : 0.f;
         }
         if (t > 0 && !(ok = mbar_wait_warp(&bar_p_free, (t - 1) & 1, ab))) break;
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          st_shared_v4(sP + sw128_offset(row, (c0 >> 3) + j), pack_bf16x2(pr[8 * j], pr[8 * j + 1]),
-                       pack_bf16x2(pr[8 * j + 2], pr[8 * j + 3]), pack_bf16x2(pr[8 * j + 4], pr[8 * j + 5]),
-                       pack_bf16x2(pr[8 * j + 6], pr[8 * j + 7]));
+        store_row32<SPLIT>(sP, L::PT, row, c0, pr);
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
@@ -278,11 +291,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
         for (int c = 0; c < 32; ++c) ds[c] = pr[c] * (__uint_as_float(dr[c]) - st[L::BQ + c0 + c]);
         if (t > 0 && !(ok = mbar_wait_warp(&bar_ds_free, (t - 1) & 1, ab))) break;
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          st_shared_v4(sDS + sw128_offset(row, (c0 >> 3) + j), pack_bf16x2(ds[8 * j], ds[8 * j + 1]),
-                       pack_bf16x2(ds[8 * j + 2], ds[8 * j + 3]), pack_bf16x2(ds[8 * j + 4], ds[8 * j + 5]),
-                       pack_bf16x2(ds[8 * j + 6], ds[8 * j + 7]));
+        store_row32<SPLIT>(sDS, L::PT, row, c0, ds);
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
@@ -296,9 +305,9 @@ __global__ void __launch_bounds__(384, 1)
     // a tile no query sees gets zeros.
     const bool want = wg == 0 ? (p.wrt & 4u) != 0 : (p.wrt & 2u) != 0;
     if (want && (ok || n == 0)) {
-      __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(wg == 0 ? p.dv : p.dk) +
-                           static_cast<int64_t>(b) * p.k_sb + static_cast<int64_t>(h) * p.k_sh +
+      const int64_t roff = static_cast<int64_t>(b) * p.k_sb + static_cast<int64_t>(h) * p.k_sh +
                            static_cast<int64_t>(key) * p.k_ss;
+      void* out = wg == 0 ? p.dv : p.dk;
       const float f = wg == 0 ? 1.f : p.scale;
       const uint32_t tacc = (wg == 0 ? t_dv : t_dk) + lane_addr;
 #pragma unroll 1
@@ -311,19 +320,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
           for (int j = 0; j < 32; ++j) r[j] = 0u;
         }
-        if (key < p.Sk) {
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            if (cc * 32 + j * 8 < p.D) {
-              uint4 v;
-              v.x = pack_bf16x2(__uint_as_float(r[8 * j]) * f, __uint_as_float(r[8 * j + 1]) * f);
-              v.y = pack_bf16x2(__uint_as_float(r[8 * j + 2]) * f, __uint_as_float(r[8 * j + 3]) * f);
-              v.z = pack_bf16x2(__uint_as_float(r[8 * j + 4]) * f, __uint_as_float(r[8 * j + 5]) * f);
-              v.w = pack_bf16x2(__uint_as_float(r[8 * j + 6]) * f, __uint_as_float(r[8 * j + 7]) * f);
-              *reinterpret_cast<uint4*>(out + cc * 32 + j * 8) = v;
-            }
-          }
-        }
+        if (key < p.Sk) store_out32<SPLIT>(out, roff, cc * 32, p.D, r, f);
       }
     }
   }
@@ -335,15 +332,15 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
-template <int DP, bool HAS_BIAS>
+template <int DP, bool HAS_BIAS, bool SPLIT>
 cudaError_t launch_dkdv_t(const DenseMaps& m, const DenseParams& p, cudaStream_t s) {
-  using L = DkdvLayout<DP>;
-  auto kern = dkdv_kernel<DP, HAS_BIAS>;
+  using L = DkdvLayout<DP, SPLIT>;
+  auto kern = dkdv_kernel<DP, HAS_BIAS, SPLIT>;
   const int smem = L::BYTES + 1024;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(p.B * p.H, cdiv(p.Sk, L::BK));
-  kern<<<grid, 384, smem, s>>>(m.q64, m.k128, m.v128, m.dy64, m.bias64, p);
+  kern<<<grid, 384, smem, s>>>(m.q64, m.k128, m.v128, m.dy64, m.bias64, m.q64_lo, m.k128_lo, m.v128_lo, m.dy64_lo, p);
   return cudaGetLastError();
 }
 
@@ -351,8 +348,9 @@ cudaError_t launch_dkdv_t(const DenseMaps& m, const DenseParams& p, cudaStream_t
 
 cudaError_t launch_dkdv(const DenseMaps& m, const DenseParams& p, bool bias, cudaStream_t s) {
   const int DP = padded_head_dim(p.D);
-  if (DP == 64) return bias ? launch_dkdv_t<64, true>(m, p, s) : launch_dkdv_t<64, false>(m, p, s);
-  return bias ? launch_dkdv_t<128, true>(m, p, s) : launch_dkdv_t<128, false>(m, p, s);
+  if (m.split) return launch_dkdv_t<64, false, true>(m, p, s);
+  if (DP == 64) return bias ? launch_dkdv_t<64, true, false>(m, p, s) : launch_dkdv_t<64, false, false>(m, p, s);
+  return bias ? launch_dkdv_t<128, true, false>(m, p, s) : launch_dkdv_t<128, false, false>(m, p, s);
 }
 
 }  // namespace attn

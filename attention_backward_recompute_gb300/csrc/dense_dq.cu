@@ -19,21 +19,22 @@ using namespace sm103;
 
 namespace {
 
-template <int DP>
+template <int DP, bool SPLIT>
 struct DqLayout {
   static constexpr int NCH = DP / 64;
+  static constexpr int NSP = SPLIT ? 2 : 1;    // copies of every operand tile (hi, lo)
   static constexpr int BQ = 128, BK = 64;
-  static constexpr int QT = NCH * BQ * 128;    // Q or dY tile (128 rows)
-  static constexpr int KT = NCH * BK * 128;    // K or V tile (64 rows)
-  static constexpr int BIAS = BQ * 128;        // 128 query rows x 64 keys
-  static constexpr int DS = BQ * 128;          // dS: 128 queries x 64 keys bf16
+  static constexpr int QT = NCH * BQ * 128;    // one copy of the Q or dY tile (128 rows)
+  static constexpr int KT = NCH * BK * 128;    // one copy of a K or V tile (64 rows)
+  static constexpr int BIAS = SPLIT ? 0 : BQ * 128;  // 128 query rows x 64 keys
+  static constexpr int DS = BQ * 128;          // one copy of dS: 128 queries x 64 keys bf16
   static constexpr int Q_OFF = 0;
-  static constexpr int DY_OFF = Q_OFF + QT;
-  static constexpr int K_OFF = DY_OFF + QT;          // 2 stages
-  static constexpr int V_OFF = K_OFF + 2 * KT;       // 2 stages
-  static constexpr int BIAS_OFF = V_OFF + 2 * KT;    // 2 stages
-  static constexpr int DS_OFF = BIAS_OFF + 2 * BIAS;
-  static constexpr int BYTES = DS_OFF + DS;
+  static constexpr int DY_OFF = Q_OFF + NSP * QT;
+  static constexpr int K_OFF = DY_OFF + NSP * QT;          // 2 stages x NSP copies
+  static constexpr int V_OFF = K_OFF + 2 * NSP * KT;       // 2 stages x NSP copies
+  static constexpr int BIAS_OFF = V_OFF + 2 * NSP * KT;    // 2 stages
+  static constexpr int DS_OFF = BIAS_OFF + 2 * BIAS;       // NSP copies
+  static constexpr int BYTES = DS_OFF + NSP * DS;
   static constexpr int TMEM_COLS = 256;  // dQ [0, DP), S [DP, DP+64), dP [DP+64, DP+128)
 };
 
@@ -45,12 +46,14 @@ __device__ __forceinline__ bool drain_wait(uint64_t* bar, uint32_t parity) {
   return true;
 }
 
-template <int DP, bool HAS_BIAS>
+template <int DP, bool HAS_BIAS, bool SPLIT>
 __global__ void __launch_bounds__(384, 1)
     dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_dy,
-              const __grid_constant__ CUtensorMap tm_bias, const DenseParams p) {
-  using L = DqLayout<DP>;
+              const __grid_constant__ CUtensorMap tm_bias, const __grid_constant__ CUtensorMap tm_q_lo,
+              const __grid_constant__ CUtensorMap tm_k_lo, const __grid_constant__ CUtensorMap tm_v_lo,
+              const __grid_constant__ CUtensorMap tm_dy_lo, const DenseParams p) {
+  using L = DqLayout<DP, SPLIT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ uint64_t bar_qdy, bar_full[2], bar_empty[2], bar_s_full, bar_s_free, bar_dp_full, bar_ds_full,
@@ -104,22 +107,27 @@ __global__ void __launch_bounds__(384, 1)
       tma_prefetch_map(&tm_v);
       tma_prefetch_map(&tm_dy);
       if (HAS_BIAS) tma_prefetch_map(&tm_bias);
-      mbar_arrive_expect_tx(&bar_qdy, 2 * L::QT);
-      for (int c = 0; c < L::NCH; ++c) {
-        tma_load_4d(sm + L::Q_OFF + c * (L::BQ * 128), &tm_q, &bar_qdy, c * 64, q0, h, b);
-        tma_load_4d(sm + L::DY_OFF + c * (L::BQ * 128), &tm_dy, &bar_qdy, c * 64, q0, h, b);
-      }
+      mbar_arrive_expect_tx(&bar_qdy, 2 * L::NSP * L::QT);
+      for (int hl = 0; hl < L::NSP; ++hl)
+        for (int c = 0; c < L::NCH; ++c) {
+          tma_load_4d(sm + L::Q_OFF + hl * L::QT + c * (L::BQ * 128), hl ? &tm_q_lo : &tm_q, &bar_qdy, c * 64, q0,
+                      h, b);
+          tma_load_4d(sm + L::DY_OFF + hl * L::QT + c * (L::BQ * 128), hl ? &tm_dy_lo : &tm_dy, &bar_qdy, c * 64,
+                      q0, h, b);
+        }
       bool ok = true;
       for (int t = 0; t < n && ok; ++t) {
         const int s = t & 1;
         if (t >= 2) ok = mbar_wait(&bar_empty[s], ((t >> 1) - 1) & 1, ab);
         if (!ok) break;
         const int kk0 = (j_lo + t) * L::BK;
-        mbar_arrive_expect_tx(&bar_full[s], 2 * L::KT + (HAS_BIAS ? L::BIAS : 0));
-        for (int c = 0; c < L::NCH; ++c) {
-          tma_load_4d(sm + L::K_OFF + s * L::KT + c * (L::BK * 128), &tm_k, &bar_full[s], c * 64, kk0, h, b);
-          tma_load_4d(sm + L::V_OFF + s * L::KT + c * (L::BK * 128), &tm_v, &bar_full[s], c * 64, kk0, h, b);
-        }
+        mbar_arrive_expect_tx(&bar_full[s], 2 * L::NSP * L::KT + (HAS_BIAS ? L::BIAS : 0));
+        for (int hl = 0; hl < L::NSP; ++hl)
+          for (int c = 0; c < L::NCH; ++c) {
+            const int o = (s * L::NSP + hl) * L::KT + c * (L::BK * 128);
+            tma_load_4d(sm + L::K_OFF + o, hl ? &tm_k_lo : &tm_k, &bar_full[s], c * 64, kk0, h, b);
+            tma_load_4d(sm + L::V_OFF + o, hl ? &tm_v_lo : &tm_v, &bar_full[s], c * 64, kk0, h, b);
+          }
         if (HAS_BIAS) tma_load_4d(sm + L::BIAS_OFF + s * L::BIAS, &tm_bias, &bar_full[s], kk0, q0, h, b);
         last_use[s] = t;
       }
@@ -135,23 +143,33 @@ __global__ void __launch_bounds__(384, 1)
       constexpr uint32_t id_acc = idesc_bf16(128, DP, false, true);
       const uint32_t sQ = smem_addr(sm + L::Q_OFF), sDY = smem_addr(sm + L::DY_OFF);
       const uint32_t sDS = smem_addr(sm + L::DS_OFF);
-      auto k_at = [&](int s) { return smem_addr(sm + L::K_OFF + s * L::KT); };
-      auto v_at = [&](int s) { return smem_addr(sm + L::V_OFF + s * L::KT); };
+      auto k_at = [&](int s) { return smem_addr(sm + L::K_OFF + s * L::NSP * L::KT); };
+      auto v_at = [&](int s) { return smem_addr(sm + L::V_OFF + s * L::NSP * L::KT); };
+      // split operands: hi*hi + hi*lo + lo*hi
+      constexpr int NPROD = SPLIT ? 3 : 1;
       auto issue_xt = [&](uint32_t d, uint32_t a_base, uint32_t b_base) {
 #pragma unroll
-        for (int kk = 0; kk < DP / 16; ++kk) {
-          const int c = kk >> 2, o = (kk & 3) * 32;
-          const uint64_t ad = sdesc_sw128(a_base + c * (L::BQ * 128) + o, 16, 1024);
-          const uint64_t bd = sdesc_sw128(b_base + c * (L::BK * 128) + o, 16, 1024);
-          mma_bf16_ss(d, ad, bd, id_s, kk > 0 ? 1u : 0u);
+        for (int pr = 0; pr < NPROD; ++pr) {
+          const uint32_t a0 = a_base + (pr == 2 ? L::QT : 0), b0 = b_base + (pr == 1 ? L::KT : 0);
+#pragma unroll
+          for (int kk = 0; kk < DP / 16; ++kk) {
+            const int c = kk >> 2, o = (kk & 3) * 32;
+            const uint64_t ad = sdesc_sw128(a0 + c * (L::BQ * 128) + o, 16, 1024);
+            const uint64_t bd = sdesc_sw128(b0 + c * (L::BK * 128) + o, 16, 1024);
+            mma_bf16_ss(d, ad, bd, id_s, (pr > 0 || kk > 0) ? 1u : 0u);
+          }
         }
       };
       auto issue_dq = [&](int s, bool first) {
 #pragma unroll
-        for (int kk = 0; kk < L::BK / 16; ++kk) {
-          const uint64_t ad = sdesc_sw128(sDS + kk * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(k_at(s) + kk * 16 * 128, L::BK * 128, 1024);
-          mma_bf16_ss(t_dq, ad, bd, id_acc, (first && kk == 0) ? 0u : 1u);
+        for (int pr = 0; pr < NPROD; ++pr) {
+          const uint32_t a0 = sDS + (pr == 2 ? L::DS : 0), b0 = k_at(s) + (pr == 1 ? L::KT : 0);
+#pragma unroll
+          for (int kk = 0; kk < L::BK / 16; ++kk) {
+            const uint64_t ad = sdesc_sw128(a0 + kk * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(b0 + kk * 16 * 128, L::BK * 128, 1024);
+            mma_bf16_ss(t_dq, ad, bd, id_acc, (first && pr == 0 && kk == 0) ? 0u : 1u);
+          }
         }
       };
       bool ok = mbar_wait(&bar_qdy, 0, ab);
@@ -259,11 +277,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
         for (int c = 0; c < 32; ++c) ds[c] = pr[c] * (__uint_as_float(dr[c]) - dlt);
         if (t > 0 && !(ok = mbar_wait_warp(&bar_ds_free, (t - 1) & 1, ab))) break;
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          st_shared_v4(sDS + sw128_offset(row, (c0 >> 3) + j), pack_bf16x2(ds[8 * j], ds[8 * j + 1]),
-                       pack_bf16x2(ds[8 * j + 2], ds[8 * j + 3]), pack_bf16x2(ds[8 * j + 4], ds[8 * j + 5]),
-                       pack_bf16x2(ds[8 * j + 6], ds[8 * j + 7]));
+        store_row32<SPLIT>(sDS, L::DS, row, c0, ds);
         fence_proxy_async_smem();
         tc_fence_before();
         __syncwarp();
@@ -275,8 +289,8 @@ __global__ void __launch_bounds__(384, 1)
     // ------------------------------------------------------------ epilogue
     // each warpgroup writes half of the dQ row (times the softmax scale)
     if ((p.wrt & 1u) && (ok || n == 0)) {
-      __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.dq) + static_cast<int64_t>(b) * p.q_sb +
-                           static_cast<int64_t>(h) * p.q_sh + static_cast<int64_t>(q) * p.q_ss;
+      const int64_t roff = static_cast<int64_t>(b) * p.q_sb + static_cast<int64_t>(h) * p.q_sh +
+                           static_cast<int64_t>(q) * p.q_ss;
       const int half = DP / 2;
 #pragma unroll 1
       for (int cc = wg * half / 32; cc < (wg + 1) * half / 32 && cc * 32 < p.D; ++cc) {
@@ -288,20 +302,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
           for (int j = 0; j < 32; ++j) r[j] = 0u;
         }
-        if (q < p.Sq) {
-          const float f = p.scale;
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            if (cc * 32 + j * 8 < p.D) {
-              uint4 v;
-              v.x = pack_bf16x2(__uint_as_float(r[8 * j]) * f, __uint_as_float(r[8 * j + 1]) * f);
-              v.y = pack_bf16x2(__uint_as_float(r[8 * j + 2]) * f, __uint_as_float(r[8 * j + 3]) * f);
-              v.z = pack_bf16x2(__uint_as_float(r[8 * j + 4]) * f, __uint_as_float(r[8 * j + 5]) * f);
-              v.w = pack_bf16x2(__uint_as_float(r[8 * j + 6]) * f, __uint_as_float(r[8 * j + 7]) * f);
-              *reinterpret_cast<uint4*>(out + cc * 32 + j * 8) = v;
-            }
-          }
-        }
+        if (q < p.Sq) store_out32<SPLIT>(p.dq, roff, cc * 32, p.D, r, p.scale);
       }
     }
   }
@@ -313,15 +314,16 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
-template <int DP, bool HAS_BIAS>
+template <int DP, bool HAS_BIAS, bool SPLIT>
 cudaError_t launch_dq_t(const DenseMaps& m, const DenseParams& p, cudaStream_t s) {
-  using L = DqLayout<DP>;
-  auto kern = dq_kernel<DP, HAS_BIAS>;
+  using L = DqLayout<DP, SPLIT>;
+  auto kern = dq_kernel<DP, HAS_BIAS, SPLIT>;
   const int smem = L::BYTES + 1024;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(p.B * p.H, cdiv(p.Sq, L::BQ));
-  kern<<<grid, 384, smem, s>>>(m.q128, m.k64, m.v64, m.dy128, m.bias128, p);
+  kern<<<grid, 384, smem, s>>>(m.q128, m.k64, m.v64, m.dy128, m.bias128, m.q128_lo, m.k64_lo, m.v64_lo,
+                               m.dy128_lo, p);
   return cudaGetLastError();
 }
 
@@ -329,8 +331,9 @@ cudaError_t launch_dq_t(const DenseMaps& m, const DenseParams& p, cudaStream_t s
 
 cudaError_t launch_dq(const DenseMaps& m, const DenseParams& p, bool bias, cudaStream_t s) {
   const int DP = padded_head_dim(p.D);
-  if (DP == 64) return bias ? launch_dq_t<64, true>(m, p, s) : launch_dq_t<64, false>(m, p, s);
-  return bias ? launch_dq_t<128, true>(m, p, s) : launch_dq_t<128, false>(m, p, s);
+  if (m.split) return launch_dq_t<64, false, true>(m, p, s);
+  if (DP == 64) return bias ? launch_dq_t<64, true, false>(m, p, s) : launch_dq_t<64, false, false>(m, p, s);
+  return bias ? launch_dq_t<128, true, false>(m, p, s) : launch_dq_t<128, false, false>(m, p, s);
 }
 
 }  // namespace attn

@@ -25,21 +25,22 @@ using namespace sm103;
 
 namespace {
 
-template <int DP>
+template <int DP, bool SPLIT>
 struct FwdLayout {
   static constexpr int NCH = DP / 64;
+  static constexpr int NSP = SPLIT ? 2 : 1;        // copies of every operand tile (hi, lo)
   static constexpr int BQ = 128, BK = 64;
   static constexpr int QT = NCH * BQ * 128;
   static constexpr int KT = NCH * BK * 128;
-  static constexpr int BIAS = BQ * 128;
-  static constexpr int PT = BQ * 128;              // P: 128 queries x 64 keys bf16
+  static constexpr int BIAS = SPLIT ? 0 : BQ * 128;
+  static constexpr int PT = BQ * 128;              // P: 128 queries x 64 keys bf16 (one copy)
   static constexpr int Q_OFF = 0;
-  static constexpr int DY_OFF = Q_OFF + QT;
-  static constexpr int K_OFF = DY_OFF + QT;        // 2 stages
-  static constexpr int V_OFF = K_OFF + 2 * KT;     // 2 stages
-  static constexpr int BIAS_OFF = V_OFF + 2 * KT;  // 2 stages
-  static constexpr int P_OFF = BIAS_OFF + 2 * BIAS;  // 2 buffers
-  static constexpr int BYTES = P_OFF + 2 * PT;
+  static constexpr int DY_OFF = Q_OFF + NSP * QT;
+  static constexpr int K_OFF = DY_OFF + NSP * QT;        // 2 stages x NSP copies
+  static constexpr int V_OFF = K_OFF + 2 * NSP * KT;     // 2 stages x NSP copies
+  static constexpr int BIAS_OFF = V_OFF + 2 * NSP * KT;  // 2 stages
+  static constexpr int P_OFF = BIAS_OFF + 2 * BIAS;      // 2 buffers x NSP copies
+  static constexpr int BYTES = P_OFF + 2 * NSP * PT;
   static constexpr int TMEM_COLS = 256;  // O [0, DP), S0 [DP, DP+64), S1 [DP+64, DP+128)
 };
 
@@ -56,12 +57,14 @@ __device__ __forceinline__ bool drain_wait(uint64_t* bar, uint32_t parity) {
   return true;
 }
 
-template <int DP, bool HAS_BIAS>
+template <int DP, bool HAS_BIAS, bool SPLIT>
 __global__ void __launch_bounds__(256, 1)
     fwd_stats_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_dy,
-                     const __grid_constant__ CUtensorMap tm_bias, const DenseParams p) {
-  using L = FwdLayout<DP>;
+                     const __grid_constant__ CUtensorMap tm_bias, const __grid_constant__ CUtensorMap tm_q_lo,
+                     const __grid_constant__ CUtensorMap tm_k_lo, const __grid_constant__ CUtensorMap tm_v_lo,
+                     const __grid_constant__ CUtensorMap tm_dy_lo, const DenseParams p) {
+  using L = FwdLayout<DP, SPLIT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ uint64_t bar_q, bar_dy, bar_full[2], bar_empty[2], bar_s_full[2], bar_p_full[2], bar_p_free[2];
@@ -110,9 +113,11 @@ __global__ void __launch_bounds__(256, 1)
       tma_prefetch_map(&tm_v);
       tma_prefetch_map(&tm_dy);
       if (HAS_BIAS) tma_prefetch_map(&tm_bias);
-      mbar_arrive_expect_tx(&bar_q, L::QT);
-      for (int c = 0; c < L::NCH; ++c)
-        tma_load_4d(sm + L::Q_OFF + c * (L::BQ * 128), &tm_q, &bar_q, c * 64, q0, h, b);
+      mbar_arrive_expect_tx(&bar_q, L::NSP * L::QT);
+      for (int hl = 0; hl < L::NSP; ++hl)
+        for (int c = 0; c < L::NCH; ++c)
+          tma_load_4d(sm + L::Q_OFF + hl * L::QT + c * (L::BQ * 128), hl ? &tm_q_lo : &tm_q, &bar_q, c * 64, q0, h,
+                      b);
       int last_use[2] = {-1, -1};
       bool ok = true;
       for (int t = 0; t < n && ok; ++t) {
@@ -120,17 +125,21 @@ __global__ void __launch_bounds__(256, 1)
         if (t >= 2) ok = mbar_wait(&bar_empty[s], ((t >> 1) - 1) & 1, ab);
         if (!ok) break;
         const int kk0 = (j_lo + t) * L::BK;
-        mbar_arrive_expect_tx(&bar_full[s], 2 * L::KT + (HAS_BIAS ? L::BIAS : 0));
-        for (int c = 0; c < L::NCH; ++c) {
-          tma_load_4d(sm + L::K_OFF + s * L::KT + c * (L::BK * 128), &tm_k, &bar_full[s], c * 64, kk0, h, b);
-          tma_load_4d(sm + L::V_OFF + s * L::KT + c * (L::BK * 128), &tm_v, &bar_full[s], c * 64, kk0, h, b);
-        }
+        mbar_arrive_expect_tx(&bar_full[s], 2 * L::NSP * L::KT + (HAS_BIAS ? L::BIAS : 0));
+        for (int hl = 0; hl < L::NSP; ++hl)
+          for (int c = 0; c < L::NCH; ++c) {
+            const int o = (s * L::NSP + hl) * L::KT + c * (L::BK * 128);
+            tma_load_4d(sm + L::K_OFF + o, hl ? &tm_k_lo : &tm_k, &bar_full[s], c * 64, kk0, h, b);
+            tma_load_4d(sm + L::V_OFF + o, hl ? &tm_v_lo : &tm_v, &bar_full[s], c * 64, kk0, h, b);
+          }
         if (HAS_BIAS) tma_load_4d(sm + L::BIAS_OFF + s * L::BIAS, &tm_bias, &bar_full[s], kk0, q0, h, b);
         last_use[s] = t;
         if (t == 0) {  // dY is only needed at the end; load it behind the first tile
-          mbar_arrive_expect_tx(&bar_dy, L::QT);
-          for (int c = 0; c < L::NCH; ++c)
-            tma_load_4d(sm + L::DY_OFF + c * (L::BQ * 128), &tm_dy, &bar_dy, c * 64, q0, h, b);
+          mbar_arrive_expect_tx(&bar_dy, L::NSP * L::QT);
+          for (int hl = 0; hl < L::NSP; ++hl)
+            for (int c = 0; c < L::NCH; ++c)
+              tma_load_4d(sm + L::DY_OFF + hl * L::QT + c * (L::BQ * 128), hl ? &tm_dy_lo : &tm_dy, &bar_dy, c * 64,
+                          q0, h, b);
         }
       }
       for (int s = 0; s < 2; ++s)
@@ -144,17 +153,22 @@ __global__ void __launch_bounds__(256, 1)
       constexpr uint32_t id_s = idesc_bf16(128, 64, false, false);
       constexpr uint32_t id_o = idesc_bf16(128, DP, false, true);
       const uint32_t sQ = smem_addr(sm + L::Q_OFF);
-      auto k_at = [&](int s) { return smem_addr(sm + L::K_OFF + s * L::KT); };
-      auto v_at = [&](int s) { return smem_addr(sm + L::V_OFF + s * L::KT); };
-      auto p_at = [&](int s) { return smem_addr(sm + L::P_OFF + s * L::PT); };
+      auto k_at = [&](int s) { return smem_addr(sm + L::K_OFF + s * L::NSP * L::KT); };
+      auto v_at = [&](int s) { return smem_addr(sm + L::V_OFF + s * L::NSP * L::KT); };
+      auto p_at = [&](int s) { return smem_addr(sm + L::P_OFF + s * L::NSP * L::PT); };
+      constexpr int NPROD = SPLIT ? 3 : 1;  // hi*hi + hi*lo + lo*hi
       auto issue_s = [&](int t) {
         const int s = t & 1;
 #pragma unroll
-        for (int kk = 0; kk < DP / 16; ++kk) {
-          const int c = kk >> 2, o = (kk & 3) * 32;
-          const uint64_t ad = sdesc_sw128(sQ + c * (L::BQ * 128) + o, 16, 1024);
-          const uint64_t bd = sdesc_sw128(k_at(s) + c * (L::BK * 128) + o, 16, 1024);
-          mma_bf16_ss(t_s0 + s * 64, ad, bd, id_s, kk > 0 ? 1u : 0u);
+        for (int pr = 0; pr < NPROD; ++pr) {
+          const uint32_t a0 = sQ + (pr == 2 ? L::QT : 0), b0 = k_at(s) + (pr == 1 ? L::KT : 0);
+#pragma unroll
+          for (int kk = 0; kk < DP / 16; ++kk) {
+            const int c = kk >> 2, o = (kk & 3) * 32;
+            const uint64_t ad = sdesc_sw128(a0 + c * (L::BQ * 128) + o, 16, 1024);
+            const uint64_t bd = sdesc_sw128(b0 + c * (L::BK * 128) + o, 16, 1024);
+            mma_bf16_ss(t_s0 + s * 64, ad, bd, id_s, (pr > 0 || kk > 0) ? 1u : 0u);
+          }
         }
         mma_commit(&bar_s_full[s]);
       };
@@ -176,10 +190,14 @@ __global__ void __launch_bounds__(256, 1)
         if (!(ok = mbar_wait(&bar_p_full[s], (t >> 1) & 1, ab))) break;
         tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < L::BK / 16; ++kk) {
-          const uint64_t ad = sdesc_sw128(p_at(s) + kk * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(v_at(s) + kk * 16 * 128, L::BK * 128, 1024);
-          mma_bf16_ss(t_o, ad, bd, id_o, (t == 0 && kk == 0) ? 0u : 1u);
+        for (int pr = 0; pr < NPROD; ++pr) {
+          const uint32_t a0 = p_at(s) + (pr == 2 ? L::PT : 0), b0 = v_at(s) + (pr == 1 ? L::KT : 0);
+#pragma unroll
+          for (int kk = 0; kk < L::BK / 16; ++kk) {
+            const uint64_t ad = sdesc_sw128(a0 + kk * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(b0 + kk * 16 * 128, L::BK * 128, 1024);
+            mma_bf16_ss(t_o, ad, bd, id_o, (t == 0 && pr == 0 && kk == 0) ? 0u : 1u);
+          }
         }
         mma_commit(&bar_p_free[s]);
         mma_commit(&bar_empty[s]);
@@ -290,12 +308,9 @@ __global__ void __launch_bounds__(256, 1)
         tmem_st_wait();
       }
       if (t >= 2 && !(ok = mbar_wait_warp(&bar_p_free[s], ((t - 2) >> 1) & 1, ab))) break;
-      const uint32_t sp = smem_addr(sm + L::P_OFF + s * L::PT);
-#pragma unroll
-      for (int j = 0; j < 8; ++j)
-        st_shared_v4(sp + sw128_offset(row, j), pack_bf16x2(pr[8 * j], pr[8 * j + 1]),
-                     pack_bf16x2(pr[8 * j + 2], pr[8 * j + 3]), pack_bf16x2(pr[8 * j + 4], pr[8 * j + 5]),
-                     pack_bf16x2(pr[8 * j + 6], pr[8 * j + 7]));
+      const uint32_t sp = smem_addr(sm + L::P_OFF + s * L::NSP * L::PT);
+      store_row32<SPLIT>(sp, L::PT, row, 0, pr);
+      store_row32<SPLIT>(sp, L::PT, row, 32, pr + 32);
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
@@ -316,17 +331,19 @@ __global__ void __launch_bounds__(256, 1)
           tmem_ld32(t_o + lane_addr + cc * 32, r);
           tmem_ld_wait();
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int col = cc * 32 + j * 8;  // 8 bf16 per 16-byte chunk
-            const uint4 w = *reinterpret_cast<const uint4*>(dys + (col >> 6) * (L::BQ * 128) +
-                                                            sw128_offset(row, (col & 63) >> 3));
-            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+          for (int hl = 0; hl < L::NSP; ++hl)  // dY = hi (+ lo for split fp32 inputs)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              acc = fmaf(__uint_as_float(ws[e] << 16), __uint_as_float(r[8 * j + 2 * e]), acc);
-              acc = fmaf(__uint_as_float(ws[e] & 0xffff0000u), __uint_as_float(r[8 * j + 2 * e + 1]), acc);
+            for (int j = 0; j < 4; ++j) {
+              const int col = cc * 32 + j * 8;  // 8 bf16 per 16-byte chunk
+              const uint4 w = *reinterpret_cast<const uint4*>(dys + hl * L::QT + (col >> 6) * (L::BQ * 128) +
+                                                              sw128_offset(row, (col & 63) >> 3));
+              const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                acc = fmaf(__uint_as_float(ws[e] << 16), __uint_as_float(r[8 * j + 2 * e]), acc);
+                acc = fmaf(__uint_as_float(ws[e] & 0xffff0000u), __uint_as_float(r[8 * j + 2 * e + 1]), acc);
+              }
             }
-          }
         }
         if (l > 0.f) {
           L2 = m2 + __log2f(l);
@@ -350,16 +367,34 @@ __global__ void __launch_bounds__(256, 1)
   }
 }
 
-template <int DP, bool HAS_BIAS>
+template <int DP, bool HAS_BIAS, bool SPLIT>
 cudaError_t launch_fwd_t(const DenseMaps& m, const DenseParams& p, cudaStream_t s) {
-  using L = FwdLayout<DP>;
-  auto kern = fwd_stats_kernel<DP, HAS_BIAS>;
+  using L = FwdLayout<DP, SPLIT>;
+  auto kern = fwd_stats_kernel<DP, HAS_BIAS, SPLIT>;
   const int smem = L::BYTES + 1024;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(p.B * p.H, cdiv(p.Sq, L::BQ));
-  kern<<<grid, 256, smem, s>>>(m.q128, m.k64, m.v64, m.dy128, m.bias128, p);
+  kern<<<grid, 256, smem, s>>>(m.q128, m.k64, m.v64, m.dy128, m.bias128, m.q128_lo, m.k64_lo, m.v64_lo,
+                               m.dy128_lo, p);
   return cudaGetLastError();
+}
+
+// x -> (hi, lo): hi = bf16(x), lo = bf16(x - hi), four elements per thread.
+__global__ void split_f32_kernel(const float* __restrict__ x, __nv_bfloat16* __restrict__ hi,
+                                 __nv_bfloat16* __restrict__ lo, int64_t n) {
+  const int64_t n4 = n / 4;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n4;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const float4 v = reinterpret_cast<const float4*>(x)[i];
+    const __nv_bfloat162 h0 = __floats2bfloat162_rn(v.x, v.y), h1 = __floats2bfloat162_rn(v.z, v.w);
+    const __nv_bfloat162 l0 = __floats2bfloat162_rn(v.x - __low2float(h0), v.y - __high2float(h0));
+    const __nv_bfloat162 l1 = __floats2bfloat162_rn(v.z - __low2float(h1), v.w - __high2float(h1));
+    reinterpret_cast<__nv_bfloat162*>(hi)[2 * i] = h0;
+    reinterpret_cast<__nv_bfloat162*>(hi)[2 * i + 1] = h1;
+    reinterpret_cast<__nv_bfloat162*>(lo)[2 * i] = l0;
+    reinterpret_cast<__nv_bfloat162*>(lo)[2 * i + 1] = l1;
+  }
 }
 
 // One warp per query row: delta = dY . O, L2 from the supplied LSE.
@@ -402,8 +437,17 @@ __global__ void __launch_bounds__(256) delta_only_kernel(const DenseParams p) {
 
 cudaError_t launch_fwd_stats(const DenseMaps& m, const DenseParams& p, bool bias, cudaStream_t s) {
   const int DP = padded_head_dim(p.D);
-  if (DP == 64) return bias ? launch_fwd_t<64, true>(m, p, s) : launch_fwd_t<64, false>(m, p, s);
-  return bias ? launch_fwd_t<128, true>(m, p, s) : launch_fwd_t<128, false>(m, p, s);
+  if (m.split) return launch_fwd_t<64, false, true>(m, p, s);
+  if (DP == 64) return bias ? launch_fwd_t<64, true, false>(m, p, s) : launch_fwd_t<64, false, false>(m, p, s);
+  return bias ? launch_fwd_t<128, true, false>(m, p, s) : launch_fwd_t<128, false, false>(m, p, s);
+}
+
+cudaError_t launch_split_f32(const float* x, void* hi, void* lo, int64_t n, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  const int64_t blocks = (n / 4 + 255) / 256;
+  split_f32_kernel<<<static_cast<int>(blocks < 152 * 16 ? blocks : 152 * 16), 256, 0, s>>>(
+      x, static_cast<__nv_bfloat16*>(hi), static_cast<__nv_bfloat16*>(lo), n);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_delta_only(const DenseParams& p, int dtype_bf16, cudaStream_t s) {

@@ -16,6 +16,11 @@ struct DenseMaps {
   CUtensorMap q64, q128, dy64, dy128;
   CUtensorMap k64, k128, v64, v128;
   CUtensorMap bias64, bias128;
+  // fp32 storage: the maps above address the hi copies (bf16) of the split
+  // inputs and these the lo copies; without split they repeat the maps above.
+  CUtensorMap q64_lo, q128_lo, dy64_lo, dy128_lo;
+  CUtensorMap k64_lo, k128_lo, v64_lo, v128_lo;
+  bool split;
 };
 
 // padded head dim handled by the tensor-core kernels: 64 or 128
@@ -23,6 +28,8 @@ inline int padded_head_dim(int D) { return D <= 64 ? 64 : 128; }
 
 cudaError_t launch_fwd_stats(const DenseMaps& m, const DenseParams& p, bool bias, cudaStream_t s);
 cudaError_t launch_delta_only(const DenseParams& p, int dtype_bf16, cudaStream_t s);
+// Split fp32 tensors into hi/lo bf16 copies: hi = bf16(x), lo = bf16(x - hi).
+cudaError_t launch_split_f32(const float* x, void* hi, void* lo, int64_t n, cudaStream_t s);
 cudaError_t launch_dkdv(const DenseMaps& m, const DenseParams& p, bool bias, cudaStream_t s);
 cudaError_t launch_dq(const DenseMaps& m, const DenseParams& p, bool bias, cudaStream_t s);
 

@@ -49,6 +49,10 @@ extern "C" ATTN_API attn_status_t attn_bwd_dense_noalloc(const attn_dense_desc* 
                                                          void* stream) {
   if (!d) return attn::api_fail(ATTN_ERR_INVALID_ARG, "descriptor is NULL");
   if (d->batch < 0 || d->heads < 0 || d->seq_q < 0) return attn::api_fail(ATTN_ERR_INVALID_ARG, "negative size");
+  if (d->dtype != ATTN_DTYPE_BF16)
+    return attn::api_fail(ATTN_ERR_UNSUPPORTED,
+                          "the library-owned scratch holds row statistics only; fp32 storage also needs split "
+                          "copies of the inputs: use attn_bwd_dense with a workspace");
   const double rows = double(d->batch) * double(d->heads) * double(d->seq_q);
   if (rows > double(kRows))
     return attn::api_fail(ATTN_ERR_UNSUPPORTED,

@@ -35,10 +35,16 @@ attn_status_t check_paged_desc(const attn_paged_desc* d, PagedSizes* z) {
   if (d->dtype != ATTN_DTYPE_BF16) return api_fail(ATTN_ERR_UNSUPPORTED, "paged path supports bf16 storage only");
   if (d->page_size != 16) return api_fail(ATTN_ERR_UNSUPPORTED, "page_size must be 16");
   const int64_t G = d->heads / d->kv_heads;
-  if (64 % G != 0) return api_fail(ATTN_ERR_UNSUPPORTED, "heads / kv_heads must divide 64");
-  if (d->position_dim != 0) return api_fail(ATTN_ERR_UNSUPPORTED, "MLA (position_dim > 0) is not available in this build");
   if (d->value_dim != d->key_dim) return api_fail(ATTN_ERR_UNSUPPORTED, "value_dim must equal key_dim");
-  if (d->key_dim != 64 && d->key_dim != 128) return api_fail(ATTN_ERR_UNSUPPORTED, "key_dim must be 64 or 128 (GQA)");
+  if (d->position_dim != 0) {
+    // MLA: the latent (key_dim) is also the value
+    if (d->key_dim != 512 || d->position_dim != 64)
+      return api_fail(ATTN_ERR_UNSUPPORTED, "MLA needs key_dim 512 and position_dim 64");
+    if (G > 32) return api_fail(ATTN_ERR_UNSUPPORTED, "MLA needs heads / kv_heads <= 32");
+  } else {
+    if (64 % G != 0) return api_fail(ATTN_ERR_UNSUPPORTED, "heads / kv_heads must divide 64");
+    if (d->key_dim != 64 && d->key_dim != 128) return api_fail(ATTN_ERR_UNSUPPORTED, "key_dim must be 64 or 128 (GQA)");
+  }
   const int64_t lim = int64_t(1) << 30;
   if (d->num_pages * d->page_size >= lim || d->num_queries * d->heads >= lim || d->num_seqs * d->max_pages_per_seq >= lim ||
       d->num_seqs >= 65535 || d->kv_heads >= 65535)
@@ -127,31 +133,35 @@ ATTN_API attn_status_t attn_bwd_paged(const attn_paged_desc* d, const void* q, c
   PagedSizes z;
   attn_status_t st = check_paged_desc(d, &z);
   if (st != ATTN_OK) return st;
-  (void)qp;
-  (void)kp_pool;
-  (void)dkp_pool;
-  if (wrt_mask == 0 || (wrt_mask & ~(ATTN_WRT_DK | ATTN_WRT_DV)))
-    return api_fail(ATTN_ERR_INVALID_ARG, "wrt_mask must be a non-empty subset of dK|dV for GQA");
-  const bool want_dk = wrt_mask & ATTN_WRT_DK, want_dv = wrt_mask & ATTN_WRT_DV;
-  if ((want_dk && !dk_pool && z.k_bytes) || (want_dv && !dv_pool && z.v_bytes))
+  const bool mla = d->position_dim > 0;
+  const unsigned allowed = mla ? (ATTN_WRT_DK | ATTN_WRT_DKP) : (ATTN_WRT_DK | ATTN_WRT_DV);
+  if (wrt_mask == 0 || (wrt_mask & ~allowed))
+    return api_fail(ATTN_ERR_INVALID_ARG, "wrt_mask must be a non-empty subset of %s", mla ? "dK|dKp (MLA)" : "dK|dV (GQA)");
+  const bool want_dk = wrt_mask & ATTN_WRT_DK, want_dv = wrt_mask & ATTN_WRT_DV, want_dkp = wrt_mask & ATTN_WRT_DKP;
+  if ((want_dk && !dk_pool && z.k_bytes) || (want_dv && !dv_pool && z.v_bytes) || (want_dkp && !dkp_pool && z.kp_bytes))
     return api_fail(ATTN_ERR_INVALID_ARG, "requested gradient pointer is NULL");
   if (d->num_seqs > 0 && (!seq_meta || (d->max_pages_per_seq > 0 && !page_table)))
     return api_fail(ATTN_ERR_INVALID_ARG, "page_table / seq_meta is NULL");
-  if (d->num_queries > 0 && (!q || !dy || !lse || !delta)) return api_fail(ATTN_ERR_INVALID_ARG, "q/dy/lse/delta is NULL");
-  if (d->num_pages > 0 && (!k_pool || !v_pool)) return api_fail(ATTN_ERR_INVALID_ARG, "k_pool/v_pool is NULL");
-  const void* al[] = {q, k_pool, v_pool, dy, dk_pool, dv_pool, lse, delta, page_table, seq_meta, workspace};
+  if (d->num_queries > 0 && (!q || !dy || !lse || !delta || (mla && !qp)))
+    return api_fail(ATTN_ERR_INVALID_ARG, "q/qp/dy/lse/delta is NULL");
+  if (d->num_pages > 0 && (!k_pool || (mla ? !kp_pool : !v_pool)))
+    return api_fail(ATTN_ERR_INVALID_ARG, "k_pool/v_pool/kp_pool is NULL");
+  const void* al[] = {q, qp, k_pool, v_pool, kp_pool, dy, dk_pool, dv_pool, dkp_pool, lse, delta, page_table,
+                      seq_meta, workspace};
   for (const void* x : al)
     if (x && !al16(x)) return api_fail(ATTN_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
   struct R { const void* p; size_t n; };
-  const R ins[] = {{q, z.q_bytes}, {k_pool, z.k_bytes}, {v_pool, z.v_bytes}, {dy, z.dy_bytes},
-                   {page_table, z.table_bytes}, {seq_meta, z.meta_bytes}, {lse, z.stat_bytes},
-                   {delta, z.stat_bytes}, {workspace, workspace_bytes}};
-  const R outs[] = {{want_dk ? dk_pool : nullptr, z.k_bytes}, {want_dv ? dv_pool : nullptr, z.v_bytes}};
-  for (int i = 0; i < 2; ++i) {
+  const R ins[] = {{q, z.q_bytes}, {qp, mla ? z.qp_bytes : 0}, {k_pool, z.k_bytes}, {v_pool, mla ? 0 : z.v_bytes},
+                   {kp_pool, mla ? z.kp_bytes : 0}, {dy, z.dy_bytes}, {page_table, z.table_bytes},
+                   {seq_meta, z.meta_bytes}, {lse, z.stat_bytes}, {delta, z.stat_bytes}, {workspace, workspace_bytes}};
+  const R outs[] = {{want_dk ? dk_pool : nullptr, z.k_bytes}, {want_dv ? dv_pool : nullptr, z.v_bytes},
+                    {want_dkp ? dkp_pool : nullptr, z.kp_bytes}};
+  for (int i = 0; i < 3; ++i) {
     for (const R& r : ins)
       if (overlap(outs[i].p, outs[i].n, r.p, r.n)) return api_fail(ATTN_ERR_ALIAS, "output %d overlaps an input or the workspace", i);
+    for (int j = i + 1; j < 3; ++j)
+      if (overlap(outs[i].p, outs[i].n, outs[j].p, outs[j].n)) return api_fail(ATTN_ERR_ALIAS, "outputs %d and %d overlap", i, j);
   }
-  if (overlap(outs[0].p, outs[0].n, outs[1].p, outs[1].n)) return api_fail(ATTN_ERR_ALIAS, "dk_pool and dv_pool overlap");
   if (d->num_pages == 0) return api_ok();
   if (!workspace || workspace_bytes < z.ws_bytes)
     return api_fail(ATTN_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", z.ws_bytes, workspace_bytes);
@@ -163,7 +173,21 @@ ATTN_API attn_status_t attn_bwd_paged(const attn_paged_desc* d, const void* q, c
   p.delta = delta;
   p.dk_pool = dk_pool;
   p.dv_pool = dv_pool;
+  p.dkp_pool = dkp_pool;
   p.wrt = wrt_mask;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (mla) {
+    // links, then one owner CTA per physical page (it stores zeros for slots
+    // no link makes valid, so no separate zero store is needed)
+    attn::timing_mark_begin(2, s);
+    cudaError_t e = attn::launch_paged_prep(p, s);
+    attn::timing_mark(s);
+    if (e == cudaSuccess) e = attn::launch_paged_mla_history(p, q, qp, dy, k_pool, kp_pool, s);
+    attn::timing_mark(s);
+    attn::timing_mark_end();
+    if (e != cudaSuccess) return api_fail(ATTN_ERR_CUDA, "paged launch failed: %s", cudaGetErrorString(e));
+    return api_ok();
+  }
   attn::PagedMaps m;
   std::memset(&m, 0, sizeof(m));
   const uint64_t slots = uint64_t(d->num_pages) * d->page_size;
@@ -176,8 +200,7 @@ ATTN_API attn_status_t attn_bwd_paged(const attn_paged_desc* d, const void* q, c
         encode3d(&m.v, v_pool, d->value_dim, d->kv_heads, slots, 64, 1, uint32_t(d->page_size));
   if (!enc) return api_fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed");
   if (d->num_queries == 0) { m.q = m.k; m.dy = m.v; }
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int nk = 6;
+  const int nk = 3;
   attn::timing_mark_begin(nk, s);
   cudaError_t e = attn::launch_paged_prep(p, s);
   attn::timing_mark(s);
@@ -198,18 +221,19 @@ ATTN_API attn_status_t attn_paged_row_stats(const attn_paged_desc* d, const void
   PagedSizes z;
   attn_status_t st = check_paged_desc(d, &z);
   if (st != ATTN_OK) return st;
-  (void)qp;
-  (void)kp_pool;
+  const bool mla = d->position_dim > 0;
   if (d->num_queries == 0) return api_ok();
-  if (!q || !dy || !lse || !delta || !seq_meta || (d->max_pages_per_seq > 0 && !page_table))
+  if (!q || !dy || !lse || !delta || !seq_meta || (d->max_pages_per_seq > 0 && !page_table) || (mla && !qp))
     return api_fail(ATTN_ERR_INVALID_ARG, "a required pointer is NULL");
-  if (d->num_pages > 0 && (!k_pool || !v_pool)) return api_fail(ATTN_ERR_INVALID_ARG, "k_pool/v_pool is NULL");
-  const void* al[] = {q, k_pool, v_pool, dy, lse, delta, page_table, seq_meta};
+  if (d->num_pages > 0 && (!k_pool || (mla ? !kp_pool : !v_pool)))
+    return api_fail(ATTN_ERR_INVALID_ARG, "k_pool/v_pool/kp_pool is NULL");
+  const void* al[] = {q, qp, k_pool, v_pool, kp_pool, dy, lse, delta, page_table, seq_meta};
   for (const void* x : al)
     if (x && !al16(x)) return api_fail(ATTN_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
   struct R { const void* p; size_t n; };
-  const R ins[] = {{q, z.q_bytes}, {k_pool, z.k_bytes}, {v_pool, z.v_bytes}, {dy, z.dy_bytes},
-                   {page_table, z.table_bytes}, {seq_meta, z.meta_bytes}, {workspace, workspace_bytes}};
+  const R ins[] = {{q, z.q_bytes}, {qp, mla ? z.qp_bytes : 0}, {k_pool, z.k_bytes}, {v_pool, mla ? 0 : z.v_bytes},
+                   {kp_pool, mla ? z.kp_bytes : 0}, {dy, z.dy_bytes}, {page_table, z.table_bytes},
+                   {seq_meta, z.meta_bytes}, {workspace, workspace_bytes}};
   for (const R& r : ins)
     if (overlap(lse, z.stat_bytes, r.p, r.n) || overlap(delta, z.stat_bytes, r.p, r.n))
       return api_fail(ATTN_ERR_ALIAS, "lse/delta overlap an input or the workspace");
@@ -218,6 +242,15 @@ ATTN_API attn_status_t attn_paged_row_stats(const attn_paged_desc* d, const void
   if ((st = fill_params(d, z, page_table, seq_meta, workspace, &p)) != ATTN_OK) return st;
   p.lse_out = lse;
   p.delta_out = delta;
+  if (mla) {
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    attn::timing_mark_begin(1, s);
+    cudaError_t e = attn::launch_paged_mla_stats(p, q, qp, dy, k_pool, kp_pool, s);
+    attn::timing_mark(s);
+    attn::timing_mark_end();
+    if (e != cudaSuccess) return api_fail(ATTN_ERR_CUDA, "row-statistics launch failed: %s", cudaGetErrorString(e));
+    return api_ok();
+  }
   attn::PagedMaps m;
   std::memset(&m, 0, sizeof(m));
   const uint64_t slots = uint64_t(d->num_pages) * d->page_size;

@@ -63,7 +63,8 @@ typedef int32_t attn_status_t;
 #define ATTN_ERR_TIMEOUT 6     /* a device-side bounded wait expired */
 
 /* Storage types of q, k, v, dy, o, bias and of the gradients. */
-#define ATTN_DTYPE_F32 0  /* fp32 in and out; products on TF32 tensor cores, 3xTF32 split */
+#define ATTN_DTYPE_F32 0  /* fp32 in and out; every operand split into hi + lo bf16 and each
+                            product taken as hi*hi + hi*lo + lo*hi on bf16 tensor cores */
 #define ATTN_DTYPE_BF16 1 /* bf16 in and out; bf16 tensor cores, fp32 accumulation */
 
 /* Dense layouts (rlx-cpu attention_bwd.rs, fn attention_backward: `bhsd`). */
@@ -87,7 +88,7 @@ typedef struct attn_dense_desc {
   int64_t heads;      /* H  >= 0 */
   int64_t seq_q;      /* Sq >= 0 */
   int64_t seq_k;      /* Sk >= 0 */
-  int64_t head_dim;   /* D: 16, 32, 64 or 128 (head_dim * element size must be a multiple of 16) */
+  int64_t head_dim;   /* D: 8, 16, 32, 64 or 128 for bf16; 8, 16, 32 or 64 for fp32 */
   int32_t dtype;      /* ATTN_DTYPE_* */
   int32_t layout;     /* ATTN_LAYOUT_* */
   uint32_t mask_flags;/* OR of ATTN_MASK_* */
@@ -150,7 +151,8 @@ ATTN_API attn_status_t attn_bwd_dense(const attn_dense_desc* d, const void* q, c
  * attn_bwd_dense, whose outputs this call reproduces.
  *
  *   - batch * heads * seq_q above ATTN_NOALLOC_MAX_ROWS is rejected with
- *     ATTN_ERR_UNSUPPORTED (use attn_bwd_dense with a workspace instead).
+ *     ATTN_ERR_UNSUPPORTED (use attn_bwd_dense with a workspace instead), and
+ *     so is fp32 storage (its split input copies do not fit the scratch).
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress; it allocates nothing) with that device current;
  *     make that first call before any stream capture.
@@ -260,9 +262,11 @@ ATTN_API attn_status_t attn_check_device_error(void* stream);
  * first kernel and events[i] after its i-th kernel (events are cudaEvent_t
  * handles created by the caller; `count` must cover every kernel of the call
  * plus one, else the call records nothing).  The hook applies to ONE call and
- * is then cleared.  The dense call launches, in order: the row-statistics
- * prologue, the dK/dV kernel (if dK or dV is requested), the dQ kernel (if dQ
- * is requested).
+ * is then cleared.  The dense call launches, in order: (fp32 storage only)
+ * four split kernels for q, dy, k, v; the row-statistics prologue; the dK/dV
+ * kernel (if dK or dV is requested); the dQ kernel (if dQ is requested).  The
+ * paged backward launches its link preparation, the zero store of unlinked
+ * pages and the history kernel; the paged row statistics one kernel.
  */
 ATTN_API void attn_set_timing_events(void* const* events, int count);
 

@@ -32,20 +32,21 @@ def to_dev(c, bd):
 
 def gpu_stats(bd, c, dv):
     return bd.paged_row_stats(dv["q"], dv["k"], dv["v"], dv["dy"], dv["table"], dv["meta"], heads=c.heads,
-                              kv_heads=c.kv_heads, page_size=c.page_size, causal=c.causal)
+                              kv_heads=c.kv_heads, page_size=c.page_size, causal=c.causal, qp=dv["qp"],
+                              kp_pool=dv["kp"])
 
 
 def gpu_bwd(bd, c, dv, lse, delta, outputs=None):
     return bd.paged_backward(dv["q"], dv["k"], dv["v"], dv["dy"], dv["table"], dv["meta"], lse, delta,
                              heads=c.heads, kv_heads=c.kv_heads, page_size=c.page_size, causal=c.causal,
-                             outputs=outputs)
+                             outputs=outputs, qp=dv["qp"], kp_pool=dv["kp"])
 
 
 def oracle(c):
     from oracle import attn_bwd_paged
     return attn_bwd_paged(c.q, c.dy, c.k_pool, c.page_table, c.seq_len, c.q_start, c.q_pos,
-                          page_size=c.page_size, kv_heads=c.kv_heads, v_pool=c.v_pool, causal=c.causal,
-                          return_stats=True)
+                          page_size=c.page_size, kv_heads=c.kv_heads, v_pool=c.v_pool, qp=c.qp,
+                          kp_pool=c.kp_pool, causal=c.causal, return_stats=True)
 
 
 def rel(got, want, mask=None):
@@ -64,6 +65,13 @@ CASES = [
          value_dim=64, causal=False),
     dict(seed=24, num_seqs=4, len_lo=40, len_hi=260, queries_per_seq=24, heads=8, kv_heads=2, key_dim=128,
          value_dim=128, causal=True, shared_prefix_pages=3),
+    # MLA: latent 512 (also the value) + position 64
+    dict(seed=25, num_seqs=4, len_lo=20, len_hi=300, queries_per_seq=16, heads=8, kv_heads=1, key_dim=512,
+         value_dim=512, position_dim=64, causal=True),
+    dict(seed=26, num_seqs=3, len_lo=30, len_hi=200, queries_per_seq=12, heads=8, kv_heads=2, key_dim=512,
+         value_dim=512, position_dim=64, causal=False),
+    dict(seed=27, num_seqs=4, len_lo=40, len_hi=200, queries_per_seq=8, heads=32, kv_heads=1, key_dim=512,
+         value_dim=512, position_dim=64, causal=True, shared_prefix_pages=2),
 ]
 
 
@@ -126,4 +134,33 @@ def test_paged_full_size_gqa_sampled(bd):
             owned[int(c.page_table[s, t // c.page_size]) * c.page_size + t % c.page_size] = True
     assert rel(dk, ref_dk, owned) < TOL
     assert rel(dvv, ref_dv, owned) < TOL
+    assert np.max(np.abs(lse.cpu().numpy()[rows] - ref_lse)) < 2e-2
+
+
+def test_paged_full_size_mla_sampled(bd):
+    """The full MLA configuration (latent 512 + position 64, 32 heads, one
+    latent head, the same 64 sequences); sampled sequences against the oracle,
+    and bit stability across two runs."""
+    c = inputs.paged_config("paged_mla")
+    dv = to_dev(c, bd)
+    lse, delta = gpu_stats(bd, c, dv)
+    dk, dkp = gpu_bwd(bd, c, dv, lse, delta)
+    dk2, dkp2 = gpu_bwd(bd, c, dv, lse, delta)
+    bd.check_device_error()
+    assert torch.equal(dk, dk2) and torch.equal(dkp, dkp2)
+    from oracle import attn_bwd_paged
+    pick = [3, 40]
+    qs = [np.arange(c.q_start[s], c.q_start[s + 1]) for s in pick]
+    rows = np.concatenate(qs)
+    sub_start = np.concatenate([[0], np.cumsum([len(x) for x in qs])]).astype(np.int32)
+    ref_dk, ref_dkp, ref_lse, _ = attn_bwd_paged(
+        c.q[rows], c.dy[rows], c.k_pool, c.page_table[pick], c.seq_len[pick], sub_start, c.q_pos[rows],
+        page_size=c.page_size, kv_heads=c.kv_heads, qp=c.qp[rows], kp_pool=c.kp_pool, causal=True,
+        return_stats=True)
+    owned = np.zeros(c.num_pages * c.page_size, bool)
+    for s in pick:
+        for t in range(int(c.seq_len[s])):
+            owned[int(c.page_table[s, t // c.page_size]) * c.page_size + t % c.page_size] = True
+    assert rel(dk, ref_dk, owned) < TOL
+    assert rel(dkp, ref_dkp, owned) < TOL
     assert np.max(np.abs(lse.cpu().numpy()[rows] - ref_lse)) < 2e-2
