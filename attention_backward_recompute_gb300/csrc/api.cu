@@ -350,11 +350,11 @@ ATTN_API attn_status_t attn_bwd_dense(const attn_dense_desc* d, const void* q, c
     attn::timing_mark(s);
   }
   if (e == cudaSuccess && (want_dk || want_dv)) {
-    e = attn::launch_dkdv(m, p, has_bias, s);
+    e = split ? attn::launch_dkdv(m, p, has_bias, s) : attn::launch_dkdv2(m, p, has_bias, s);
     attn::timing_mark(s);
   }
   if (e == cudaSuccess && want_dq) {
-    e = attn::launch_dq(m, p, has_bias, s);
+    e = split ? attn::launch_dq(m, p, has_bias, s) : attn::launch_dq2(m, p, has_bias, s);
     attn::timing_mark(s);
   }
   attn::timing_mark_end();

@@ -1,0 +1,465 @@
+// dK / dV kernel with the softmax and the dS work on separate warpgroups and
+// P, dS kept in tensor memory (bf16 storage path).
+//
+// Same products as rlx-cpu src/attention_bwd.rs (fn backward_dense_head_all),
+// per 128-key tile j and 64-query tile i of one (batch, head):
+//   S^T  = K_j Q_i^T                    tcgen05 (smem x smem), TMEM buffer S[b]
+//   dP^T = V_j dY_i^T                   tcgen05 (smem x smem), TMEM buffer dP[b]
+//   P^T  = exp(S^T*scale + bias - lse)  softmax warpgroup: reads S[b], writes
+//                                       P^T as bf16 over the first half of S[b]
+//   dS^T = P^T * (dP^T - delta)         dS warpgroup: reads dP[b] and P^T,
+//                                       writes dS^T as bf16 over dP[b]
+//   dV_j += P^T dY_i                    tcgen05, A = P^T from tensor memory
+//   dK_j += dS^T Q_i                    tcgen05, A = dS^T from tensor memory
+// S and dP are double-buffered (b = i % 2); each buffer has its own softmax
+// warpgroup, so two tiles are in the softmax at once while the dS warpgroup
+// and the tensor core work on others.  Q, dY, bias and the row statistics come
+// through a 3-stage TMA ring.  Warp 0: TMA producer, warp 1: MMA issuer (one
+// thread), warps 4..7: softmax of even tiles, warps 12..15: softmax of odd
+// tiles, warps 8..11: dS.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "dense_common.cuh"
+#include "dense_launch.h"
+#include "sm103.cuh"
+
+namespace attn {
+using namespace sm103;
+
+namespace {
+
+constexpr int kStages = 3;
+
+template <int DP>
+struct Dkdv2Layout {
+  static constexpr int NCH = DP / 64;
+  static constexpr int BK = 128, BQ = 64;
+  static constexpr int KV = NCH * BK * 128;       // K (or V) tile
+  static constexpr int QT = NCH * BQ * 128;       // Q (or dY) tile
+  static constexpr int BIAS = 2 * BQ * 128;       // two 64-key halves x 64 query rows
+  static constexpr int K_OFF = 0;
+  static constexpr int V_OFF = K_OFF + KV;
+  static constexpr int Q_OFF = V_OFF + KV;                 // kStages
+  static constexpr int DY_OFF = Q_OFF + kStages * QT;      // kStages
+  static constexpr int BIAS_OFF = DY_OFF + kStages * QT;   // kStages
+  static constexpr int ST_OFF = BIAS_OFF + kStages * BIAS; // kStages x {L2, delta, pm} x 64 floats
+  static constexpr int BYTES = ST_OFF + kStages * 3 * BQ * 4;
+  // TMEM: dV [0, DP), dK [DP, 2DP), S[2] and dP[2] 64 columns each after that
+  static constexpr int T_S = 2 * DP, T_DP = 2 * DP + 128;
+  static constexpr int TMEM_COLS = 2 * DP + 256 <= 256 ? 256 : 512;
+};
+
+__device__ __forceinline__ bool drain_wait(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_test(bar, parity)) {
+    if (global_timer_ns() - t0 > ATTN_WAIT_TIMEOUT_NS) return false;
+  }
+  return true;
+}
+
+__device__ __forceinline__ float4 lds_f4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+
+// Registers written by tcgen05.ld are valid only after tcgen05.wait::ld; this
+// empty asm ties every later use of r to a point after the wait.
+__device__ __forceinline__ void reg_fence16(uint32_t (&r)[16]) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) asm volatile("" : "+r"(r[i]));
+}
+
+// 16 queries [c0, c0+16) of the P^T row of one key: exp2(S*scale*log2e +
+// bias*log2e - L2) as 8 bf16 pairs.  CHECK: zero the queries outside [lo, hi]
+// (tile-local range of queries that see this key).  KM: the key is
+// custom-masked; its visible entries take the row's masked-key probability
+// pm instead.
+template <bool HAS_BIAS, bool CHECK>
+__device__ __forceinline__ void p_chunk(const uint32_t (&sr)[16], int c0, const float* st, const uint8_t* bias_s,
+                                        int kc, int kb, float scale_log2, int lo, int hi, bool kmasked,
+                                        uint32_t* pw) {
+#pragma unroll
+  for (int c4 = 0; c4 < 4; ++c4) {
+    const float4 l2 = *reinterpret_cast<const float4*>(st + c0 + 4 * c4);
+    const float l2v[4] = {l2.x, l2.y, l2.z, l2.w};
+    float pv[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int ql = c0 + 4 * c4 + e;
+      float x = fmaf(__uint_as_float(sr[4 * c4 + e]), scale_log2, -l2v[e]);
+      if (HAS_BIAS) {
+        const uint32_t off = ql * 128 + (((kc ^ ql) & 7) << 4) + kb;
+        const uint16_t bbits = *reinterpret_cast<const uint16_t*>(bias_s + off);
+        x = fmaf(__uint_as_float(static_cast<uint32_t>(bbits) << 16), kLog2e, x);
+      }
+      pv[e] = ex2_approx(x);
+    }
+    if (kmasked) {
+      const float4 pm = *reinterpret_cast<const float4*>(st + 128 + c0 + 4 * c4);
+      pv[0] = pm.x;
+      pv[1] = pm.y;
+      pv[2] = pm.z;
+      pv[3] = pm.w;
+    }
+    if (CHECK || kmasked) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int ql = c0 + 4 * c4 + e;
+        pv[e] = (ql >= lo && ql <= hi) ? pv[e] : 0.f;
+      }
+    }
+    pw[2 * c4] = pack_bf16x2(pv[0], pv[1]);
+    pw[2 * c4 + 1] = pack_bf16x2(pv[2], pv[3]);
+  }
+}
+
+// The P^T row over the 64 queries of a tile, S read from tensor memory in
+// four 16-column chunks with the next chunk's load in flight; chunk i's 8 bf16
+// pairs go to columns [8i, 8i+8) of the same buffer, which chunks 0..i have
+// already read.  The caller waits for the stores.
+template <bool HAS_BIAS, bool CHECK>
+__device__ __forceinline__ void p_row(uint32_t tS, const float* st, const uint8_t* bias_s, int kc, int kb,
+                                      float scale_log2, int lo, int hi, bool kmasked) {
+  uint32_t s0[16], s1[16], pw[8];
+  tmem_ld16(tS, s0);
+  tmem_ld_wait();
+  reg_fence16(s0);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint32_t(&cur)[16] = (i & 1) ? s1 : s0;
+    uint32_t(&nxt)[16] = (i & 1) ? s0 : s1;
+    if (i < 3) tmem_ld16(tS + 16 * (i + 1), nxt);
+    p_chunk<HAS_BIAS, CHECK>(cur, 16 * i, st, bias_s, kc, kb, scale_log2, lo, hi, kmasked, pw);
+    tmem_st8(tS + 8 * i, pw);
+    if (i < 3) {
+      tmem_ld_wait();
+      reg_fence16(nxt);
+    }
+  }
+}
+
+template <int DP, bool HAS_BIAS>
+__global__ void __launch_bounds__(512, 1)
+    dkdv2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_dy,
+                 const __grid_constant__ CUtensorMap tm_bias, const DenseParams p) {
+  using L = Dkdv2Layout<DP>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ uint64_t bar_kv, bar_full[kStages], bar_empty[kStages], bar_s_full[2], bar_dp_full[2], bar_p_full[2],
+      bar_p_read[2], bar_ds_full[2], bar_acc;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bh = blockIdx.x;
+  const int b = bh / p.H, h = bh - b * p.H;
+  const int k0 = blockIdx.y * L::BK;
+  const int k1 = imin(k0 + L::BK - 1, p.Sk - 1);
+  int i_lo, i_hi;
+  query_tile_range(p, k0, k1, L::BQ, &i_lo, &i_hi);
+  const int n = i_hi - i_lo;
+  const Abort ab{&abort_flag, p.err};
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&bar_kv, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bar_full[s], 2);  // TMA bytes + statistics written
+      mbar_init(&bar_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bar_s_full[s], 1);
+      mbar_init(&bar_dp_full[s], 1);
+      mbar_init(&bar_p_full[s], 4);
+      mbar_init(&bar_p_read[s], 4);
+      mbar_init(&bar_ds_full[s], 4);
+    }
+    mbar_init(&bar_acc, 1);
+    mbar_fence_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_sh, L::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+  const uint32_t t_dv = tmem, t_dk = tmem + DP;
+
+  if (n > 0 && warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_map(&tm_q);
+      tma_prefetch_map(&tm_k);
+      tma_prefetch_map(&tm_v);
+      tma_prefetch_map(&tm_dy);
+      if (HAS_BIAS) tma_prefetch_map(&tm_bias);
+      mbar_arrive_expect_tx(&bar_kv, 2 * L::KV);
+      for (int c = 0; c < L::NCH; ++c) {
+        tma_load_4d(sm + L::K_OFF + c * (L::BK * 128), &tm_k, &bar_kv, c * 64, k0, h, b);
+        tma_load_4d(sm + L::V_OFF + c * (L::BK * 128), &tm_v, &bar_kv, c * 64, k0, h, b);
+      }
+    }
+    // row statistics (L2, delta, pm) of rows lane and lane + 32 of a tile,
+    // loaded one tile ahead so their latency overlaps the wait for a stage
+    float pre[6];
+    auto load_stats = [&](int t) {
+      const int qb0 = (i_lo + t) * L::BQ;
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int q = qb0 + lane + 32 * i;
+        const bool in = q < p.Sq;
+        const size_t idx = static_cast<size_t>(bh) * p.Sq + (in ? q : 0);
+        pre[3 * i] = in ? p.L2[idx] : __int_as_float(0x7f800000);
+        pre[3 * i + 1] = in ? p.delta[idx] : 0.f;
+        pre[3 * i + 2] = (in && p.has_key_mask) ? p.pm[idx] : 0.f;
+      }
+    };
+    load_stats(0);
+    int last_use[kStages] = {-1, -1, -1};
+    bool ok = true;
+    for (int t = 0; t < n && ok; ++t) {
+      const int s = t % kStages;
+      if (t >= kStages) ok = mbar_wait(&bar_empty[s], ((t / kStages) - 1) & 1, ab);
+      if (!ok) break;
+      const int q0 = (i_lo + t) * L::BQ;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bar_full[s], 2 * L::QT + (HAS_BIAS ? L::BIAS : 0));
+        for (int c = 0; c < L::NCH; ++c) {
+          tma_load_4d(sm + L::Q_OFF + s * L::QT + c * (L::BQ * 128), &tm_q, &bar_full[s], c * 64, q0, h, b);
+          tma_load_4d(sm + L::DY_OFF + s * L::QT + c * (L::BQ * 128), &tm_dy, &bar_full[s], c * 64, q0, h, b);
+        }
+        if (HAS_BIAS) {
+          uint8_t* bs = sm + L::BIAS_OFF + s * L::BIAS;
+          tma_load_4d(bs, &tm_bias, &bar_full[s], k0, q0, h, b);
+          tma_load_4d(bs + L::BQ * 128, &tm_bias, &bar_full[s], k0 + 64, q0, h, b);
+        }
+      }
+      float* st = reinterpret_cast<float*>(sm + L::ST_OFF) + s * 3 * L::BQ;
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        st[lane + 32 * i] = pre[3 * i];
+        st[L::BQ + lane + 32 * i] = pre[3 * i + 1];
+        st[2 * L::BQ + lane + 32 * i] = pre[3 * i + 2];
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_full[s]);
+      last_use[s] = t;
+      if (t + 1 < n) load_stats(t + 1);
+    }
+    if (lane == 0) {
+      for (int s = 0; s < kStages; ++s)
+        if (last_use[s] >= 0) drain_wait(&bar_full[s], (last_use[s] / kStages) & 1);
+      drain_wait(&bar_kv, 0);
+    }
+  } else if (n > 0 && warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_s = idesc_bf16(128, 64, false, false);
+      constexpr uint32_t id_acc = idesc_bf16(128, DP, false, true);
+      const uint32_t sK = smem_addr(sm + L::K_OFF), sV = smem_addr(sm + L::V_OFF);
+      auto q_at = [&](int s) { return smem_addr(sm + L::Q_OFF + s * L::QT); };
+      auto dy_at = [&](int s) { return smem_addr(sm + L::DY_OFF + s * L::QT); };
+      // D[128 x 64] = A[128 x DP] * B[64 x DP]^T, both from shared memory, K-major
+      auto issue_xt = [&](uint32_t d, uint32_t a_base, uint32_t b_base) {
+#pragma unroll
+        for (int kk = 0; kk < DP / 16; ++kk) {
+          const int c = kk >> 2, o = (kk & 3) * 32;
+          mma_bf16_ss(d, sdesc_sw128(a_base + c * (L::BK * 128) + o, 16, 1024),
+                      sdesc_sw128(b_base + c * (L::BQ * 128) + o, 16, 1024), id_s, kk > 0 ? 1u : 0u);
+        }
+      };
+      // D[128 x DP] += A[128 x 64] (tensor memory, bf16 pairs) * B[64 x DP] (MN-major)
+      auto issue_acc = [&](uint32_t d, uint32_t a_tmem, uint32_t b_base, bool first) {
+#pragma unroll
+        for (int kk = 0; kk < L::BQ / 16; ++kk)
+          mma_bf16_ts(d, a_tmem + kk * 8, sdesc_sw128(b_base + kk * 16 * 128, L::BQ * 128, 1024), id_acc,
+                      (first && kk == 0) ? 0u : 1u);
+      };
+      auto issue_s = [&](int t) {  // S(t) into buffer t % 2
+        issue_xt(tmem + L::T_S + (t & 1) * 64, sK, q_at(t % kStages));
+        mma_commit(&bar_s_full[t & 1]);
+      };
+      auto issue_dp = [&](int t) {  // dP(t) into buffer t % 2
+        issue_xt(tmem + L::T_DP + (t & 1) * 64, sV, dy_at(t % kStages));
+        mma_commit(&bar_dp_full[t & 1]);
+      };
+      bool ok = mbar_wait(&bar_kv, 0, ab);
+      for (int t = 0; t < 2 && t < n && ok; ++t) {
+        if (!(ok = mbar_wait(&bar_full[t], 0, ab))) break;
+        tc_fence_after();
+        issue_s(t);
+        issue_dp(t);
+      }
+      // Issue order per tile t: dV(t), S(t+2), dK(t), dP(t+2).  S(t+2) goes
+      // ahead of dK(t) so the softmax of tile t+2 does not wait for dS(t);
+      // it overwrites P(t), which dV(t) (earlier in the same pipe) and the dS
+      // warpgroup (p_read) have consumed.  dP(t+2) overwrites dS(t), read by
+      // dK(t) just before it.
+      for (int t = 0; t < n && ok; ++t) {
+        const int s = t % kStages, bb = t & 1;
+        if (!(ok = mbar_wait(&bar_p_full[bb], (t >> 1) & 1, ab))) break;
+        tc_fence_after();
+        issue_acc(t_dv, tmem + L::T_S + bb * 64, dy_at(s), t == 0);
+        if (t + 2 < n) {
+          if (!(ok = mbar_wait(&bar_full[(t + 2) % kStages], ((t + 2) / kStages) & 1, ab))) break;
+          if (!(ok = mbar_wait(&bar_p_read[bb], (t >> 1) & 1, ab))) break;
+          tc_fence_after();
+          issue_s(t + 2);
+        }
+        if (!(ok = mbar_wait(&bar_ds_full[bb], (t >> 1) & 1, ab))) break;
+        tc_fence_after();
+        issue_acc(t_dk, tmem + L::T_DP + bb * 64, q_at(s), t == 0);
+        mma_commit(&bar_empty[s]);
+        if (t + 2 < n) issue_dp(t + 2);
+      }
+      mma_commit(&bar_acc);
+      drain_wait(&bar_acc, 0);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    const bool softmax_wg = warp < 8 || warp >= 12;  // warps 4..7, 12..15: P; warps 8..11: dS
+    const int sg = warp >= 12 ? 1 : 0;               // softmax group: tiles (and S buffer) of parity sg
+    const int lg = warp & 3;
+    const int row = lg * 32 + lane;  // key row inside the tile == TMEM lane
+    const int key = k0 + row;
+    const uint32_t lane_addr = static_cast<uint32_t>(lg * 32) << 16;
+    bool ok = n > 0;
+    if (n > 0 && softmax_wg) {
+      // ---------------------------------------------------------- softmax: S^T -> P^T
+      bool kmasked = false;
+      if (p.has_key_mask && key < p.Sk) kmasked = p.key_mask[static_cast<size_t>(b) * p.Sk + key] < p.mask_thr;
+      const int half = row >> 6, kc = (row & 63) >> 3, kb = (row & 7) * 2;
+      // queries that see this key: [qa, qb] (causal: q + q_off >= key;
+      // window: q + q_off - window <= key; q < Sq; none when key >= Sk)
+      int qa = -(1 << 30), qb = p.Sq - 1;
+      if (p.causal) qa = key - p.q_off;
+      if (p.window >= 0) qb = imin(qb, key + p.window - p.q_off);
+      if (key >= p.Sk) qa = 1 << 30, qb = -(1 << 30);
+      // Each group waits every phase of its own S buffer.  Of the stage
+      // barrier it skips the phases of the other group's tiles; when it waits
+      // for tile t, the phase of tile t - 3 (same stage, other parity) has
+      // completed, since the tensor core issued S(t - 2) after it.
+      for (int t = sg; t < n && ok; t += 2) {
+        const int s = t % kStages, bb = t & 1;
+        const int q0 = (i_lo + t) * L::BQ;
+        if (!(ok = mbar_wait_warp(&bar_full[s], (t / kStages) & 1, ab))) break;
+        if (!(ok = mbar_wait_warp(&bar_s_full[bb], (t >> 1) & 1, ab))) break;
+        tc_fence_after();
+        const uint32_t tS = tmem + L::T_S + bb * 64 + lane_addr;
+        const float* st = reinterpret_cast<const float*>(sm + L::ST_OFF) + s * 3 * L::BQ;
+        const uint8_t* bias_s = sm + L::BIAS_OFF + s * L::BIAS + half * (L::BQ * 128);
+        const bool full = tile_fully_visible(p, q0, q0 + L::BQ - 1, k0, k0 + L::BK - 1);
+        const int lo = qa - q0, hi = qb - q0;
+        if (full)
+          p_row<HAS_BIAS, false>(tS, st, bias_s, kc, kb, p.scale_log2, lo, hi, kmasked);
+        else
+          p_row<HAS_BIAS, true>(tS, st, bias_s, kc, kb, p.scale_log2, lo, hi, kmasked);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_p_full[bb]);
+      }
+    } else if (n > 0) {
+      // ---------------------------------------------------------- dS: dP^T, P^T -> dS^T
+      for (int t = 0; t < n && ok; ++t) {
+        const int s = t % kStages, bb = t & 1;
+        if (!(ok = mbar_wait_warp(&bar_full[s], (t / kStages) & 1, ab))) break;
+        if (!(ok = mbar_wait_warp(&bar_dp_full[bb], (t >> 1) & 1, ab))) break;
+        if (!(ok = mbar_wait_warp(&bar_p_full[bb], (t >> 1) & 1, ab))) break;
+        tc_fence_after();
+        const uint32_t tDP = tmem + L::T_DP + bb * 64 + lane_addr;
+        const uint32_t tS = tmem + L::T_S + bb * 64 + lane_addr;
+        uint32_t pw[32];
+        tmem_ld32(tS, pw);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_p_read[bb]);
+        const float* dl = reinterpret_cast<const float*>(sm + L::ST_OFF) + s * 3 * L::BQ + L::BQ;
+        // two halves of 32 queries: half hf reads dP columns [32hf, 32hf+32)
+        // and writes dS^T (bf16 pairs) to columns [16hf, 16hf+16), which half
+        // 0 has already read
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t dr[32], dsw[16];
+          tmem_ld32(tDP + 32 * hf, dr);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c4 = 0; c4 < 8; ++c4) {
+            const float4 d4 = lds_f4(dl + 32 * hf + 4 * c4);
+            const uint32_t w0 = pw[16 * hf + 2 * c4], w1 = pw[16 * hf + 2 * c4 + 1];
+            const float p0 = __uint_as_float(w0 << 16), p1 = __uint_as_float(w0 & 0xffff0000u);
+            const float p2 = __uint_as_float(w1 << 16), p3 = __uint_as_float(w1 & 0xffff0000u);
+            dsw[2 * c4] = pack_bf16x2(p0 * (__uint_as_float(dr[4 * c4]) - d4.x),
+                                      p1 * (__uint_as_float(dr[4 * c4 + 1]) - d4.y));
+            dsw[2 * c4 + 1] = pack_bf16x2(p2 * (__uint_as_float(dr[4 * c4 + 2]) - d4.z),
+                                          p3 * (__uint_as_float(dr[4 * c4 + 3]) - d4.w));
+          }
+          tmem_st16(tDP + 16 * hf, dsw);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_ds_full[bb]);
+      }
+    }
+    if (n > 0) {
+      if (ok) ok = mbar_wait_warp(&bar_acc, 0, ab);
+      tc_fence_after();
+    }
+    // ------------------------------------------------------------ epilogue
+    // the softmax warpgroups store dV (half of the columns each), the dS
+    // warpgroup dK (times the softmax scale); a tile no query sees gets zeros
+    const int wg = softmax_wg ? 0 : 1;
+    const bool want = wg == 0 ? (p.wrt & 4u) != 0 : (p.wrt & 2u) != 0;
+    const int c_lo = wg == 0 ? sg * (DP / 64) : 0, c_hi = wg == 0 ? (sg + 1) * (DP / 64) : DP / 32;
+    if (want && (ok || n == 0)) {
+      const int64_t roff = static_cast<int64_t>(b) * p.k_sb + static_cast<int64_t>(h) * p.k_sh +
+                           static_cast<int64_t>(key) * p.k_ss;
+      void* out = wg == 0 ? p.dv : p.dk;
+      const float f = wg == 0 ? 1.f : p.scale;
+      const uint32_t tacc = (wg == 0 ? t_dv : t_dk) + lane_addr;
+#pragma unroll 1
+      for (int cc = c_lo; cc < c_hi && cc * 32 < p.D; ++cc) {
+        uint32_t r[32];
+        if (n > 0) {
+          tmem_ld32(tacc + cc * 32, r);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) r[j] = 0u;
+        }
+        if (key < p.Sk) store_out32<false>(out, roff, cc * 32, p.D, r, f);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, L::TMEM_COLS);
+  }
+}
+
+template <int DP, bool HAS_BIAS>
+cudaError_t launch_t(const DenseMaps& m, const DenseParams& p, cudaStream_t s) {
+  using L = Dkdv2Layout<DP>;
+  auto kern = dkdv2_kernel<DP, HAS_BIAS>;
+  const int smem = L::BYTES + 1024;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(p.B * p.H, cdiv(p.Sk, L::BK));
+  kern<<<grid, 512, smem, s>>>(m.q64, m.k128, m.v128, m.dy64, m.bias64, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_dkdv2(const DenseMaps& m, const DenseParams& p, bool bias, cudaStream_t s) {
+  const int DP = padded_head_dim(p.D);
+  if (DP == 64) return bias ? launch_t<64, true>(m, p, s) : launch_t<64, false>(m, p, s);
+  return bias ? launch_t<128, true>(m, p, s) : launch_t<128, false>(m, p, s);
+}
+
+}  // namespace attn

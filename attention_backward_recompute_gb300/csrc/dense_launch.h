@@ -31,6 +31,10 @@ cudaError_t launch_delta_only(const DenseParams& p, int dtype_bf16, cudaStream_t
 // Split fp32 tensors into hi/lo bf16 copies: hi = bf16(x), lo = bf16(x - hi).
 cudaError_t launch_split_f32(const float* x, void* hi, void* lo, int64_t n, cudaStream_t s);
 cudaError_t launch_dkdv(const DenseMaps& m, const DenseParams& p, bool bias, cudaStream_t s);
+// bf16 storage: softmax and dS on separate warpgroups, P and dS in tensor memory
+cudaError_t launch_dkdv2(const DenseMaps& m, const DenseParams& p, bool bias, cudaStream_t s);
 cudaError_t launch_dq(const DenseMaps& m, const DenseParams& p, bool bias, cudaStream_t s);
+// bf16 storage: softmax and dS on separate warpgroups, P and dS in tensor memory
+cudaError_t launch_dq2(const DenseMaps& m, const DenseParams& p, bool bias, cudaStream_t s);
 
 }  // namespace attn
