@@ -346,7 +346,8 @@ ATTN_API attn_status_t attn_bwd_dense(const attn_dense_desc* d, const void* q, c
     }
   }
   if (e == cudaSuccess) {
-    e = o ? attn::launch_delta_only(p, split ? 0 : 1, s) : attn::launch_fwd_stats(m, p, has_bias, s);
+    e = o ? attn::launch_delta_only(p, split ? 0 : 1, s)
+          : (split ? attn::launch_fwd_stats(m, p, has_bias, s) : attn::launch_stats2(m, p, has_bias, s));
     attn::timing_mark(s);
   }
   if (e == cudaSuccess && (want_dk || want_dv)) {

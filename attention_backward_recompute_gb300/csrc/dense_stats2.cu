@@ -1,0 +1,373 @@
+// Row-statistics prologue of the dense backward, bf16 storage, self-contained
+// mode (no O or LSE from the caller).
+//
+// One CTA per (batch*head, 128-query tile) sweeps the visible 64-key tiles.
+// The tensor core computes, per key tile j,
+//   S  = Q_i K_j^T      (A = Q_i held in tensor memory, B = K_j from a TMA ring)
+//   dP = dY_i V_j^T     (A = dY_i held in tensor memory, B = V_j)
+// and every query row accumulates, with an online maximum m (base-2 units),
+//   l    = sum_j 2^(x_j - m)
+//   dsum = sum_j 2^(x_j - m) * dP_j
+// where x_j = S_j*scale*log2(e) + bias_j*log2(e) for a visible key, the
+// custom-mask value mask_neg*log2(e) for a custom-masked visible key, and no
+// term for a key the structural mask hides.  Then
+//   L2    = m + log2(l)                  (the log-sum-exp in base-2 units)
+//   delta = dsum / l = sum_j P_j dP_j    (= dY_i . O_i, the dS row offset)
+//   pm    = probability of one custom-masked visible key of the row
+// The softmax and the dS offset follow rlx-cpu src/attention_bwd.rs
+// (fn backward_dense_head_all: max-subtracted exponentials, dS = P (dP -
+// rowsum(P dP))); the masks follow fn apply_synthetic_mask there.  Both sums
+// are rescaled by 2^(m_old - m_new) when the maximum grows, which for two
+// scalars costs nothing: no output tile is accumulated or rescaled.
+//
+// Roles: warp 0 TMA producer, warp 1 MMA issuer (one thread), warps 4..7 the
+// key columns 0..31 of every tile, warps 8..11 the columns 32..63; the two
+// column groups keep their own (m, l, dsum) per row and merge at the end.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "dense_common.cuh"
+#include "dense_launch.h"
+#include "sm103.cuh"
+
+namespace attn {
+using namespace sm103;
+
+namespace {
+
+constexpr int kStages = 3;
+
+template <int DP>
+struct Stats2Layout {
+  static constexpr int NCH = DP / 64;
+  static constexpr int BQ = 128, BK = 64;
+  static constexpr int QT = NCH * BQ * 128;  // Q or dY tile (128 rows)
+  static constexpr int KT = NCH * BK * 128;  // K or V tile (64 rows)
+  static constexpr int BIAS = BQ * 128;      // 128 query rows x 64 keys
+  static constexpr int Q_OFF = 0;
+  static constexpr int DY_OFF = Q_OFF + QT;
+  static constexpr int K_OFF = DY_OFF + QT;              // kStages
+  static constexpr int V_OFF = K_OFF + kStages * KT;     // kStages
+  static constexpr int BIAS_OFF = V_OFF + kStages * KT;  // kStages
+  static constexpr int BYTES = BIAS_OFF + kStages * BIAS;
+  // TMEM: S[2] [0, 128), dP[2] [128, 256), Q and dY rows as bf16 pairs after
+  static constexpr int T_S = 0, T_DP = 128, T_QA = 256, T_DYA = 256 + DP / 2;
+  static constexpr int TMEM_COLS = 512;
+  static_assert(T_DYA + DP / 2 <= TMEM_COLS, "tensor memory budget");
+};
+
+// Lazy rescaling threshold (base-2 units): the running maximum is raised only
+// when a score exceeds it by more than this, so every term stays <= 2^8.
+constexpr float kRescaleThreshold = 8.0f;
+
+__device__ __forceinline__ bool drain_wait(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_test(bar, parity)) {
+    if (global_timer_ns() - t0 > ATTN_WAIT_TIMEOUT_NS) return false;
+  }
+  return true;
+}
+
+// Barrier among the 256 threads of warps 4..11 (named barrier 1).
+__device__ __forceinline__ void group_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+template <int DP, bool HAS_BIAS>
+__global__ void __launch_bounds__(384, 1)
+    stats2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_dy,
+                  const __grid_constant__ CUtensorMap tm_bias, const DenseParams p) {
+  using L = Stats2Layout<DP>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ uint64_t bar_qdy, bar_a_ready, bar_full[kStages], bar_empty[kStages], bar_s_full[2], bar_dp_full[2],
+      bar_used[2];
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_flag;
+  __shared__ float mg_m[128], mg_l[128], mg_d[128];
+  __shared__ int mg_any[128];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bh = blockIdx.x;
+  const int b = bh / p.H, h = bh - b * p.H;
+  const int nqt = cdiv(p.Sq, L::BQ);
+  const int it = nqt - 1 - static_cast<int>(blockIdx.y);  // longest rows first under causal masks
+  const int q0 = it * L::BQ;
+  const int q1 = imin(q0 + L::BQ - 1, p.Sq - 1);
+  int j_lo, j_hi;
+  key_tile_range(p, q0, q1, L::BK, &j_lo, &j_hi);
+  const int n = j_hi - j_lo;
+  const Abort ab{&abort_flag, p.err};
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&bar_qdy, 1);
+    mbar_init(&bar_a_ready, 8);  // warps 4..11: Q and dY rows staged in tensor memory
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bar_full[s], 1);
+      mbar_init(&bar_empty[s], 1 + 8);  // MMAs of the tile done + bias read by warps 4..11
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bar_s_full[s], 1);
+      mbar_init(&bar_dp_full[s], 1);
+      mbar_init(&bar_used[s], 8);  // S and dP buffer read by warps 4..11
+    }
+    mbar_fence_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_sh, L::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+
+  if (n > 0 && warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_map(&tm_q);
+      tma_prefetch_map(&tm_k);
+      tma_prefetch_map(&tm_v);
+      tma_prefetch_map(&tm_dy);
+      if (HAS_BIAS) tma_prefetch_map(&tm_bias);
+      mbar_arrive_expect_tx(&bar_qdy, 2 * L::QT);
+      for (int c = 0; c < L::NCH; ++c) {
+        tma_load_4d(sm + L::Q_OFF + c * (L::BQ * 128), &tm_q, &bar_qdy, c * 64, q0, h, b);
+        tma_load_4d(sm + L::DY_OFF + c * (L::BQ * 128), &tm_dy, &bar_qdy, c * 64, q0, h, b);
+      }
+      int last_use[kStages] = {-1, -1, -1};
+      bool ok = true;
+      for (int t = 0; t < n && ok; ++t) {
+        const int s = t % kStages;
+        if (t >= kStages) ok = mbar_wait(&bar_empty[s], ((t / kStages) - 1) & 1, ab);
+        if (!ok) break;
+        const int kk0 = (j_lo + t) * L::BK;
+        mbar_arrive_expect_tx(&bar_full[s], 2 * L::KT + (HAS_BIAS ? L::BIAS : 0));
+        for (int c = 0; c < L::NCH; ++c) {
+          tma_load_4d(sm + L::K_OFF + s * L::KT + c * (L::BK * 128), &tm_k, &bar_full[s], c * 64, kk0, h, b);
+          tma_load_4d(sm + L::V_OFF + s * L::KT + c * (L::BK * 128), &tm_v, &bar_full[s], c * 64, kk0, h, b);
+        }
+        if (HAS_BIAS) tma_load_4d(sm + L::BIAS_OFF + s * L::BIAS, &tm_bias, &bar_full[s], kk0, q0, h, b);
+        last_use[s] = t;
+      }
+      for (int s = 0; s < kStages; ++s)
+        if (last_use[s] >= 0) drain_wait(&bar_full[s], (last_use[s] / kStages) & 1);
+      drain_wait(&bar_qdy, 0);
+    }
+    __syncwarp();
+  } else if (n > 0 && warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_s = idesc_bf16(128, 64, false, false);
+      auto k_at = [&](int s) { return smem_addr(sm + L::K_OFF + s * L::KT); };
+      auto v_at = [&](int s) { return smem_addr(sm + L::V_OFF + s * L::KT); };
+      // D[128 x 64] = A[128 x DP] (tensor memory, bf16 pairs) * B[64 x DP]^T (shared memory, K-major)
+      auto issue_xt = [&](uint32_t d, uint32_t a_tmem, uint32_t b_base) {
+#pragma unroll
+        for (int kk = 0; kk < DP / 16; ++kk) {
+          const int c = kk >> 2, o = (kk & 3) * 32;
+          mma_bf16_ts(d, a_tmem + kk * 8, sdesc_sw128(b_base + c * (L::BK * 128) + o, 16, 1024), id_s,
+                      kk > 0 ? 1u : 0u);
+        }
+      };
+      auto issue_tile = [&](int t) {  // S(t), dP(t) into buffers t % 2; frees stage t % 3 when done
+        const int s = t % kStages, bb = t & 1;
+        issue_xt(tmem + L::T_S + bb * 64, tmem + L::T_QA, k_at(s));
+        mma_commit(&bar_s_full[bb]);
+        issue_xt(tmem + L::T_DP + bb * 64, tmem + L::T_DYA, v_at(s));
+        mma_commit(&bar_dp_full[bb]);
+        mma_commit(&bar_empty[s]);
+      };
+      bool ok = mbar_wait(&bar_a_ready, 0, ab);
+      tc_fence_after();
+      for (int t = 0; t < n && ok; ++t) {
+        if (t >= 2 && !(ok = mbar_wait(&bar_used[t & 1], ((t - 2) >> 1) & 1, ab))) break;
+        if (!(ok = mbar_wait(&bar_full[t % kStages], (t / kStages) & 1, ab))) break;
+        tc_fence_after();
+        issue_tile(t);
+      }
+      // the last commits of each stage arrive before the CTA leaves
+      for (int t = imax(0, n - kStages); t < n; ++t) drain_wait(&bar_empty[t % kStages], (t / kStages) & 1);
+    }
+    __syncwarp();
+  } else if (warp >= 4 && warp < 12) {
+    const int g = (warp - 4) >> 2;  // column group: key columns [32g, 32g + 32) of every tile
+    const int lg = warp & 3;
+    const int row = lg * 32 + lane;  // query row inside the tile == TMEM lane
+    const int q = q0 + row;
+    const uint32_t lane_addr = static_cast<uint32_t>(lg * 32) << 16;
+    const float kInf = __int_as_float(0x7f800000);
+    bool ok = n > 0;
+    if (n > 0) {
+      // stage this row of Q (group 0) or dY (group 1) in tensor memory as bf16
+      // pairs: the A operand of S = Q K^T and dP = dY V^T
+      ok = mbar_wait_warp(&bar_qdy, 0, ab);
+      if (ok) {
+        const uint8_t* src = sm + (g == 0 ? L::Q_OFF : L::DY_OFF);
+        const uint32_t dst = tmem + (g == 0 ? L::T_QA : L::T_DYA) + lane_addr;
+#pragma unroll
+        for (int c = 0; c < L::NCH; ++c) {
+          uint32_t w[32];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint4 v = *reinterpret_cast<const uint4*>(src + c * (L::BQ * 128) + sw128_offset(row, j));
+            w[4 * j] = v.x;
+            w[4 * j + 1] = v.y;
+            w[4 * j + 2] = v.z;
+            w[4 * j + 3] = v.w;
+          }
+          tmem_st32(dst + c * 32, w);
+        }
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_a_ready);
+    }
+    // keys this query sees: [ka, kb] (window: key >= q + q_off - window;
+    // causal: key <= q + q_off; key < Sk; none when q >= Sq)
+    int ka = -(1 << 30), kb = p.Sk - 1;
+    if (p.window >= 0) ka = q + p.q_off - p.window;
+    if (p.causal) kb = imin(kb, q + p.q_off);
+    if (q >= p.Sq) ka = 1 << 30, kb = -(1 << 30);
+    // custom-mask value of this lane's key in the group's columns, one tile ahead
+    const float* km = p.has_key_mask ? p.key_mask + static_cast<size_t>(b) * p.Sk : nullptr;
+    auto km_load = [&](int kk) {
+      const int key = kk + 32 * g + lane;
+      return key < p.Sk ? km[key] : kInf;
+    };
+    float kmv = (p.has_key_mask && n > 0) ? km_load(j_lo * L::BK) : 0.f;
+    float m2 = -kInf, l = 0.f, dsum = 0.f;
+    bool any_unmasked = false;
+    for (int t = 0; t < n && ok; ++t) {
+      const int s = t % kStages, bb = t & 1;
+      const int kk0 = (j_lo + t) * L::BK;
+      uint32_t kbits = 0;
+      if (p.has_key_mask) {
+        kbits = __ballot_sync(0xffffffffu, kmv < p.mask_thr);
+        if (t + 1 < n) kmv = km_load(kk0 + L::BK);
+      }
+      if (!(ok = mbar_wait_warp(&bar_full[s], (t / kStages) & 1, ab))) break;
+      if (!(ok = mbar_wait_warp(&bar_s_full[bb], (t >> 1) & 1, ab))) break;
+      if (!(ok = mbar_wait_warp(&bar_dp_full[bb], (t >> 1) & 1, ab))) break;
+      tc_fence_after();
+      uint32_t sr[32], dr[32];
+      tmem_ld32(tmem + L::T_S + bb * 64 + 32 * g + lane_addr, sr);
+      tmem_ld32(tmem + L::T_DP + bb * 64 + 32 * g + lane_addr, dr);
+      float x[32];
+      if (HAS_BIAS) {
+        const uint8_t* brow = sm + L::BIAS_OFF + s * L::BIAS + row * 128;
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {  // 8 keys per 16-byte bias chunk
+          const int j = 4 * g + jj;
+          const uint4 w4 = *reinterpret_cast<const uint4*>(brow + ((j ^ (row & 7)) << 4));
+          const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            x[8 * jj + 2 * e] = __uint_as_float(w[e] << 16) * kLog2e;
+            x[8 * jj + 2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u) * kLog2e;
+          }
+        }
+      }
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&bar_used[bb]);
+        mbar_arrive(&bar_empty[s]);
+      }
+      const bool full = tile_fully_visible(p, q0, q0 + L::BQ - 1, kk0, kk0 + L::BK - 1);
+      const int lo = ka - kk0 - 32 * g, hi = kb - kk0 - 32 * g;  // group-local visible columns
+      float mt = -kInf;
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const float sc = __uint_as_float(sr[c]) * p.scale_log2;
+        float xc = HAS_BIAS ? x[c] + sc : sc;
+        const bool masked = ((kbits >> c) & 1u) != 0u;
+        const bool vis = full || (c >= lo && c <= hi);
+        if (masked) xc = p.masked_x2;
+        if (!vis) xc = -kInf;
+        any_unmasked |= vis && !masked;
+        x[c] = xc;
+        mt = fmaxf(mt, xc);
+      }
+      if (mt > m2 + kRescaleThreshold || (m2 == -kInf && mt > -kInf)) {
+        if (m2 > -kInf) {
+          const float alpha = ex2_approx(m2 - mt);
+          l *= alpha;
+          dsum *= alpha;
+        }
+        m2 = mt;
+      }
+      if (m2 > -kInf) {
+        float ls = 0.f, ds = 0.f;
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const float e = ex2_approx(x[c] - m2);
+          ls += e;
+          ds = fmaf(e, __uint_as_float(dr[c]), ds);
+        }
+        l += ls;
+        dsum += ds;
+      }
+    }
+    // merge the two column groups: (m, l, dsum) -> (max m, rescaled sums)
+    if (g == 1) {
+      mg_m[row] = m2;
+      mg_l[row] = l;
+      mg_d[row] = dsum;
+      mg_any[row] = any_unmasked ? 1 : 0;
+    }
+    group_sync();
+    if (g == 0 && (ok || n == 0) && q < p.Sq) {
+      const float m1 = mg_m[row], l1 = mg_l[row], d1 = mg_d[row];
+      any_unmasked = any_unmasked || mg_any[row] != 0;
+      const float mm = fmaxf(m2, m1);
+      float lt = 0.f, dt = 0.f;
+      if (mm > -kInf) {
+        const float a0 = m2 > -kInf ? ex2_approx(m2 - mm) : 0.f;
+        const float a1 = m1 > -kInf ? ex2_approx(m1 - mm) : 0.f;
+        lt = l * a0 + l1 * a1;
+        dt = dsum * a0 + d1 * a1;
+      }
+      float L2 = kInf, dl = 0.f, pm = 0.f;
+      if (lt > 0.f) {
+        L2 = mm + __log2f(lt);
+        dl = dt / lt;
+        if (p.has_key_mask) pm = any_unmasked ? ex2_approx(p.masked_x2 - L2) : 1.f / lt;
+      }
+      const size_t idx = static_cast<size_t>(bh) * p.Sq + q;
+      p.L2[idx] = L2;
+      p.delta[idx] = dl;
+      if (p.has_key_mask) p.pm[idx] = pm;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, L::TMEM_COLS);
+  }
+}
+
+template <int DP, bool HAS_BIAS>
+cudaError_t launch_t(const DenseMaps& m, const DenseParams& p, cudaStream_t s) {
+  using L = Stats2Layout<DP>;
+  auto kern = stats2_kernel<DP, HAS_BIAS>;
+  const int smem = L::BYTES + 1024;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(p.B * p.H, cdiv(p.Sq, L::BQ));
+  kern<<<grid, 384, smem, s>>>(m.q128, m.k64, m.v64, m.dy128, m.bias128, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_stats2(const DenseMaps& m, const DenseParams& p, bool bias, cudaStream_t s) {
+  const int DP = padded_head_dim(p.D);
+  if (DP == 64) return bias ? launch_t<64, true>(m, p, s) : launch_t<64, false>(m, p, s);
+  return bias ? launch_t<128, true>(m, p, s) : launch_t<128, false>(m, p, s);
+}
+
+}  // namespace attn
