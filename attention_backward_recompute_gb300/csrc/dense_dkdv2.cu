@@ -254,39 +254,46 @@ __global__ void __launch_bounds__(512, 1)
     }
   } else if (n > 0 && warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // the whole warp runs this role (warp-uniform); elected lanes issue
+    {
       constexpr uint32_t id_s = idesc_bf16(128, 64, false, false);
       constexpr uint32_t id_acc = idesc_bf16(128, DP, false, true);
-      const uint32_t sK = smem_addr(sm + L::K_OFF), sV = smem_addr(sm + L::V_OFF);
-      auto q_at = [&](int s) { return smem_addr(sm + L::Q_OFF + s * L::QT); };
-      auto dy_at = [&](int s) { return smem_addr(sm + L::DY_OFF + s * L::QT); };
+      // descriptors built once; k-slices and stages are constant offsets
+      const uint64_t dK = sdesc_sw128(smem_addr(sm + L::K_OFF), 16, 1024);
+      const uint64_t dV = sdesc_sw128(smem_addr(sm + L::V_OFF), 16, 1024);
+      const uint64_t dQ0 = sdesc_sw128(smem_addr(sm + L::Q_OFF), 16, 1024);
+      const uint64_t dDY0 = sdesc_sw128(smem_addr(sm + L::DY_OFF), 16, 1024);
+      const uint64_t dQm0 = sdesc_sw128(smem_addr(sm + L::Q_OFF), L::BQ * 128, 1024);    // MN-major
+      const uint64_t dDYm0 = sdesc_sw128(smem_addr(sm + L::DY_OFF), L::BQ * 128, 1024);  // MN-major
       // D[128 x 64] = A[128 x DP] * B[64 x DP]^T, both from shared memory, K-major
-      auto issue_xt = [&](uint32_t d, uint32_t a_base, uint32_t b_base) {
+      auto issue_xt = [&](uint32_t d, uint64_t a, uint64_t bq) {
+        mma_ss_w<false>(d, a, bq, id_s);
 #pragma unroll
-        for (int kk = 0; kk < DP / 16; ++kk) {
+        for (int kk = 1; kk < DP / 16; ++kk) {
           const int c = kk >> 2, o = (kk & 3) * 32;
-          mma_bf16_ss(d, sdesc_sw128(a_base + c * (L::BK * 128) + o, 16, 1024),
-                      sdesc_sw128(b_base + c * (L::BQ * 128) + o, 16, 1024), id_s, kk > 0 ? 1u : 0u);
+          mma_ss_w<true>(d, sdesc_add(a, c * (L::BK * 128) + o), sdesc_add(bq, c * (L::BQ * 128) + o), id_s);
         }
       };
-      // D[128 x DP] += A[128 x 64] (tensor memory, bf16 pairs) * B[64 x DP] (MN-major)
-      auto issue_acc = [&](uint32_t d, uint32_t a_tmem, uint32_t b_base, bool first) {
+      // D[128 x DP] (+)= A[128 x 64] (tensor memory, bf16 pairs) * B[64 x DP] (MN-major)
+      auto issue_acc = [&](uint32_t d, uint32_t a_tmem, uint64_t bm, bool first) {
+        if (first)
+          mma_ts_w<false>(d, a_tmem, bm, id_acc);
+        else
+          mma_ts_w<true>(d, a_tmem, bm, id_acc);
 #pragma unroll
-        for (int kk = 0; kk < L::BQ / 16; ++kk)
-          mma_bf16_ts(d, a_tmem + kk * 8, sdesc_sw128(b_base + kk * 16 * 128, L::BQ * 128, 1024), id_acc,
-                      (first && kk == 0) ? 0u : 1u);
+        for (int kk = 1; kk < L::BQ / 16; ++kk) mma_ts_w<true>(d, a_tmem + kk * 8, sdesc_add(bm, kk * 16 * 128), id_acc);
       };
       auto issue_s = [&](int t) {  // S(t) into buffer t % 2
-        issue_xt(tmem + L::T_S + (t & 1) * 64, sK, q_at(t % kStages));
-        mma_commit(&bar_s_full[t & 1]);
+        issue_xt(tmem + L::T_S + (t & 1) * 64, dK, sdesc_add(dQ0, (t % kStages) * L::QT));
+        mma_commit_w(&bar_s_full[t & 1]);
       };
       auto issue_dp = [&](int t) {  // dP(t) into buffer t % 2
-        issue_xt(tmem + L::T_DP + (t & 1) * 64, sV, dy_at(t % kStages));
-        mma_commit(&bar_dp_full[t & 1]);
+        issue_xt(tmem + L::T_DP + (t & 1) * 64, dV, sdesc_add(dDY0, (t % kStages) * L::QT));
+        mma_commit_w(&bar_dp_full[t & 1]);
       };
-      bool ok = mbar_wait(&bar_kv, 0, ab);
+      bool ok = mbar_wait_warp(&bar_kv, 0, ab);
       for (int t = 0; t < 2 && t < n && ok; ++t) {
-        if (!(ok = mbar_wait(&bar_full[t], 0, ab))) break;
+        if (!(ok = mbar_wait_warp(&bar_full[t], 0, ab))) break;
         tc_fence_after();
         issue_s(t);
         issue_dp(t);
@@ -298,22 +305,22 @@ __global__ void __launch_bounds__(512, 1)
       // dK(t) just before it.
       for (int t = 0; t < n && ok; ++t) {
         const int s = t % kStages, bb = t & 1;
-        if (!(ok = mbar_wait(&bar_p_full[bb], (t >> 1) & 1, ab))) break;
+        if (!(ok = mbar_wait_warp(&bar_p_full[bb], (t >> 1) & 1, ab))) break;
         tc_fence_after();
-        issue_acc(t_dv, tmem + L::T_S + bb * 64, dy_at(s), t == 0);
+        issue_acc(t_dv, tmem + L::T_S + bb * 64, sdesc_add(dDYm0, s * L::QT), t == 0);
         if (t + 2 < n) {
-          if (!(ok = mbar_wait(&bar_full[(t + 2) % kStages], ((t + 2) / kStages) & 1, ab))) break;
-          if (!(ok = mbar_wait(&bar_p_read[bb], (t >> 1) & 1, ab))) break;
+          if (!(ok = mbar_wait_warp(&bar_full[(t + 2) % kStages], ((t + 2) / kStages) & 1, ab))) break;
+          if (!(ok = mbar_wait_warp(&bar_p_read[bb], (t >> 1) & 1, ab))) break;
           tc_fence_after();
           issue_s(t + 2);
         }
-        if (!(ok = mbar_wait(&bar_ds_full[bb], (t >> 1) & 1, ab))) break;
+        if (!(ok = mbar_wait_warp(&bar_ds_full[bb], (t >> 1) & 1, ab))) break;
         tc_fence_after();
-        issue_acc(t_dk, tmem + L::T_DP + bb * 64, q_at(s), t == 0);
-        mma_commit(&bar_empty[s]);
+        issue_acc(t_dk, tmem + L::T_DP + bb * 64, sdesc_add(dQm0, s * L::QT), t == 0);
+        mma_commit_w(&bar_empty[s]);
         if (t + 2 < n) issue_dp(t + 2);
       }
-      mma_commit(&bar_acc);
+      mma_commit_w(&bar_acc);
       drain_wait(&bar_acc, 0);
     }
     __syncwarp();

@@ -217,32 +217,35 @@ __global__ void __launch_bounds__(512, 1)
     __syncwarp();
   } else if (n > 0 && warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // the whole warp runs this role (warp-uniform); elected lanes issue
+    {
       constexpr uint32_t id_s = idesc_bf16(128, 64, false, false);
       constexpr uint32_t id_acc = idesc_bf16(128, DP, false, true);
-      auto k_at = [&](int s) { return smem_addr(sm + L::K_OFF + s * L::KT); };
-      auto v_at = [&](int s) { return smem_addr(sm + L::V_OFF + s * L::KT); };
+      // descriptors built once; k-slices and stages are constant offsets
+      const uint64_t dK0 = sdesc_sw128(smem_addr(sm + L::K_OFF), 16, 1024);
+      const uint64_t dV0 = sdesc_sw128(smem_addr(sm + L::V_OFF), 16, 1024);
+      const uint64_t dKm0 = sdesc_sw128(smem_addr(sm + L::K_OFF), L::BK * 128, 1024);  // MN-major
       // D[128 x 64] = A[128 x DP] (tensor memory, bf16 pairs) * B[64 x DP]^T (shared memory, K-major)
-      auto issue_xt = [&](uint32_t d, uint32_t a_tmem, uint32_t b_base) {
+      auto issue_xt = [&](uint32_t d, uint32_t a_tmem, uint64_t bk) {
+        mma_ts_w<false>(d, a_tmem, bk, id_s);
 #pragma unroll
-        for (int kk = 0; kk < DP / 16; ++kk) {
+        for (int kk = 1; kk < DP / 16; ++kk) {
           const int c = kk >> 2, o = (kk & 3) * 32;
-          mma_bf16_ts(d, a_tmem + kk * 8, sdesc_sw128(b_base + c * (L::BK * 128) + o, 16, 1024), id_s,
-                      kk > 0 ? 1u : 0u);
+          mma_ts_w<true>(d, a_tmem + kk * 8, sdesc_add(bk, c * (L::BK * 128) + o), id_s);
         }
       };
       auto issue_s = [&](int t) {  // S(t) = Q K^T into buffer t % 2
-        issue_xt(tmem + L::T_S + (t & 1) * 64, tmem + L::T_QA, k_at(t % kStages));
-        mma_commit(&bar_s_full[t & 1]);
+        issue_xt(tmem + L::T_S + (t & 1) * 64, tmem + L::T_QA, sdesc_add(dK0, (t % kStages) * L::KT));
+        mma_commit_w(&bar_s_full[t & 1]);
       };
       auto issue_dp = [&](int t) {  // dP(t) = dY V^T into buffer t % 2
-        issue_xt(tmem + L::T_DP + (t & 1) * 64, tmem + L::T_DYA, v_at(t % kStages));
-        mma_commit(&bar_dp_full[t & 1]);
+        issue_xt(tmem + L::T_DP + (t & 1) * 64, tmem + L::T_DYA, sdesc_add(dV0, (t % kStages) * L::KT));
+        mma_commit_w(&bar_dp_full[t & 1]);
       };
-      bool ok = mbar_wait(&bar_a_ready, 0, ab);
+      bool ok = mbar_wait_warp(&bar_a_ready, 0, ab);
       tc_fence_after();
       for (int t = 0; t < 2 && t < n && ok; ++t) {
-        if (!(ok = mbar_wait(&bar_full[t], 0, ab))) break;
+        if (!(ok = mbar_wait_warp(&bar_full[t], 0, ab))) break;
         tc_fence_after();
         issue_s(t);
         issue_dp(t);
@@ -253,21 +256,27 @@ __global__ void __launch_bounds__(512, 1)
       for (int t = 0; t < n && ok; ++t) {
         const int s = t % kStages, bb = t & 1;
         if (t + 2 < n) {
-          if (!(ok = mbar_wait(&bar_full[(t + 2) % kStages], ((t + 2) / kStages) & 1, ab))) break;
-          if (!(ok = mbar_wait(&bar_p_read[bb], (t >> 1) & 1, ab))) break;
+          if (!(ok = mbar_wait_warp(&bar_full[(t + 2) % kStages], ((t + 2) / kStages) & 1, ab))) break;
+          if (!(ok = mbar_wait_warp(&bar_p_read[bb], (t >> 1) & 1, ab))) break;
           tc_fence_after();
           issue_s(t + 2);
         }
-        if (!(ok = mbar_wait(&bar_ds_full[bb], (t >> 1) & 1, ab))) break;
+        if (!(ok = mbar_wait_warp(&bar_ds_full[bb], (t >> 1) & 1, ab))) break;
         tc_fence_after();
+        {
+          const uint64_t bm = sdesc_add(dKm0, s * L::KT);
+          const uint32_t a = tmem + L::T_DP + bb * 64;
+          if (t == 0)
+            mma_ts_w<false>(t_dq, a, bm, id_acc);
+          else
+            mma_ts_w<true>(t_dq, a, bm, id_acc);
 #pragma unroll
-        for (int kk = 0; kk < L::BK / 16; ++kk)
-          mma_bf16_ts(t_dq, tmem + L::T_DP + bb * 64 + kk * 8,
-                      sdesc_sw128(k_at(s) + kk * 16 * 128, L::BK * 128, 1024), id_acc, (t == 0 && kk == 0) ? 0u : 1u);
-        mma_commit(&bar_empty[s]);
+          for (int kk = 1; kk < L::BK / 16; ++kk) mma_ts_w<true>(t_dq, a + kk * 8, sdesc_add(bm, kk * 16 * 128), id_acc);
+        }
+        mma_commit_w(&bar_empty[s]);
         if (t + 2 < n) issue_dp(t + 2);
       }
-      mma_commit(&bar_acc);
+      mma_commit_w(&bar_acc);
       drain_wait(&bar_acc, 0);
     }
     __syncwarp();

@@ -20,9 +20,10 @@
 // are rescaled by 2^(m_old - m_new) when the maximum grows, which for two
 // scalars costs nothing: no output tile is accumulated or rescaled.
 //
-// Roles: warp 0 TMA producer, warp 1 MMA issuer (one thread), warps 4..7 the
-// key columns 0..31 of every tile, warps 8..11 the columns 32..63; the two
-// column groups keep their own (m, l, dsum) per row and merge at the end.
+// Roles: warp 0 TMA producer, warp 1 MMA issuer (one thread), warps 2..17
+// four column groups of four warps, group g owning key columns [16g, 16g+16)
+// of every tile; the groups keep their own (m, l, dsum) per row and merge at
+// the end.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -49,7 +50,13 @@ struct Stats2Layout {
   static constexpr int K_OFF = DY_OFF + QT;              // kStages
   static constexpr int V_OFF = K_OFF + kStages * KT;     // kStages
   static constexpr int BIAS_OFF = V_OFF + kStages * KT;  // kStages
-  static constexpr int BYTES = BIAS_OFF + kStages * BIAS;
+  // per key column of a tile: sk = scale*log2(e), kb = log2(e), off = 0 for a
+  // key the custom mask keeps; sk = kb = 0, off = mask_neg*log2(e) for a
+  // custom-masked key (so x = S*sk + bias*kb + off); then the 64-bit set of
+  // custom-masked columns
+  static constexpr int COL = 3 * BK * 4 + 16;
+  static constexpr int COL_OFF = BIAS_OFF + kStages * BIAS;  // kStages
+  static constexpr int BYTES = COL_OFF + kStages * COL;
   // TMEM: S[2] [0, 128), dP[2] [128, 256), Q and dY rows as bf16 pairs after
   static constexpr int T_S = 0, T_DP = 128, T_QA = 256, T_DYA = 256 + DP / 2;
   static constexpr int TMEM_COLS = 512;
@@ -68,23 +75,25 @@ __device__ __forceinline__ bool drain_wait(uint64_t* bar, uint32_t parity) {
   return true;
 }
 
-// Barrier among the 256 threads of warps 4..11 (named barrier 1).
-__device__ __forceinline__ void group_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+// Column groups (warps 2..17, four warps each) and the barrier among them
+// (named barrier 1, 512 threads).
+constexpr int kGroups = 4;
+__device__ __forceinline__ void group_sync() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
 
 template <int DP, bool HAS_BIAS>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(576, 1)
     stats2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_dy,
                   const __grid_constant__ CUtensorMap tm_bias, const DenseParams p) {
   using L = Stats2Layout<DP>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t bar_qdy, bar_a_ready, bar_full[kStages], bar_empty[kStages], bar_s_full[2], bar_dp_full[2],
+  __shared__ uint64_t bar_qdy, bar_a_ready, bar_full[kStages], bar_empty[kStages], bar_dp_full[2],
       bar_used[2];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
-  __shared__ float mg_m[128], mg_l[128], mg_d[128];
-  __shared__ int mg_any[128];
+  __shared__ float mg_m[kGroups - 1][128], mg_l[kGroups - 1][128], mg_d[kGroups - 1][128];
+  __shared__ int mg_any[kGroups - 1][128];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bh = blockIdx.x;
@@ -101,15 +110,14 @@ __global__ void __launch_bounds__(384, 1)
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(&bar_qdy, 1);
-    mbar_init(&bar_a_ready, 8);  // warps 4..11: Q and dY rows staged in tensor memory
+    mbar_init(&bar_a_ready, 8);  // warps 2..9: Q and dY rows staged in tensor memory
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&bar_full[s], 1);
-      mbar_init(&bar_empty[s], 1 + 8);  // MMAs of the tile done + bias read by warps 4..11
+      mbar_init(&bar_full[s], 2);        // TMA bytes + key-column constants written
+      mbar_init(&bar_empty[s], 1 + 4 * kGroups);  // MMAs of the tile done + bias read by warps 2..17
     }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&bar_s_full[s], 1);
-      mbar_init(&bar_dp_full[s], 1);
-      mbar_init(&bar_used[s], 8);  // S and dP buffer read by warps 4..11
+      mbar_init(&bar_dp_full[s], 1);  // S(t) and dP(t) done
+      mbar_init(&bar_used[s], 4 * kGroups);  // S and dP buffer read by warps 2..17
     }
     mbar_fence_init();
   }
@@ -135,21 +143,53 @@ __global__ void __launch_bounds__(384, 1)
         tma_load_4d(sm + L::Q_OFF + c * (L::BQ * 128), &tm_q, &bar_qdy, c * 64, q0, h, b);
         tma_load_4d(sm + L::DY_OFF + c * (L::BQ * 128), &tm_dy, &bar_qdy, c * 64, q0, h, b);
       }
-      int last_use[kStages] = {-1, -1, -1};
-      bool ok = true;
-      for (int t = 0; t < n && ok; ++t) {
-        const int s = t % kStages;
-        if (t >= kStages) ok = mbar_wait(&bar_empty[s], ((t / kStages) - 1) & 1, ab);
-        if (!ok) break;
-        const int kk0 = (j_lo + t) * L::BK;
+    }
+    // custom-mask values of keys lane and lane + 32 of a tile, one tile ahead
+    const float* km = p.has_key_mask ? p.key_mask + static_cast<size_t>(b) * p.Sk : nullptr;
+    float kmv[2] = {0.f, 0.f};
+    auto km_load = [&](int t) {
+      const int kk0 = (j_lo + t) * L::BK;
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int key = kk0 + lane + 32 * i;
+        kmv[i] = key < p.Sk ? km[key] : 1.f;
+      }
+    };
+    if (p.has_key_mask) km_load(0);
+    int last_use[kStages] = {-1, -1, -1};
+    bool ok = true;
+    for (int t = 0; t < n && ok; ++t) {
+      const int s = t % kStages;
+      if (t >= kStages) ok = mbar_wait_warp(&bar_empty[s], ((t / kStages) - 1) & 1, ab);
+      if (!ok) break;
+      const int kk0 = (j_lo + t) * L::BK;
+      if (lane == 0) {
         mbar_arrive_expect_tx(&bar_full[s], 2 * L::KT + (HAS_BIAS ? L::BIAS : 0));
         for (int c = 0; c < L::NCH; ++c) {
           tma_load_4d(sm + L::K_OFF + s * L::KT + c * (L::BK * 128), &tm_k, &bar_full[s], c * 64, kk0, h, b);
           tma_load_4d(sm + L::V_OFF + s * L::KT + c * (L::BK * 128), &tm_v, &bar_full[s], c * 64, kk0, h, b);
         }
         if (HAS_BIAS) tma_load_4d(sm + L::BIAS_OFF + s * L::BIAS, &tm_bias, &bar_full[s], kk0, q0, h, b);
-        last_use[s] = t;
       }
+      if (p.has_key_mask) {
+        float* col = reinterpret_cast<float*>(sm + L::COL_OFF + s * L::COL);
+        uint32_t* bits = reinterpret_cast<uint32_t*>(col + 3 * L::BK);
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const bool masked = kmv[i] < p.mask_thr;
+          col[lane + 32 * i] = masked ? 0.f : p.scale_log2;
+          col[L::BK + lane + 32 * i] = masked ? 0.f : kLog2e;
+          col[2 * L::BK + lane + 32 * i] = masked ? p.masked_x2 : 0.f;
+          const uint32_t w = __ballot_sync(0xffffffffu, masked);
+          if (lane == 0) bits[i] = w;
+        }
+        if (t + 1 < n) km_load(t + 1);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_full[s]);
+      last_use[s] = t;
+    }
+    if (lane == 0) {
       for (int s = 0; s < kStages; ++s)
         if (last_use[s] >= 0) drain_wait(&bar_full[s], (last_use[s] / kStages) & 1);
       drain_wait(&bar_qdy, 0);
@@ -157,32 +197,33 @@ __global__ void __launch_bounds__(384, 1)
     __syncwarp();
   } else if (n > 0 && warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    // the whole warp runs this role (warp-uniform); elected lanes issue
+    {
       constexpr uint32_t id_s = idesc_bf16(128, 64, false, false);
-      auto k_at = [&](int s) { return smem_addr(sm + L::K_OFF + s * L::KT); };
-      auto v_at = [&](int s) { return smem_addr(sm + L::V_OFF + s * L::KT); };
+      // descriptors built once; k-slices and stages are constant offsets
+      const uint64_t dK0 = sdesc_sw128(smem_addr(sm + L::K_OFF), 16, 1024);
+      const uint64_t dV0 = sdesc_sw128(smem_addr(sm + L::V_OFF), 16, 1024);
       // D[128 x 64] = A[128 x DP] (tensor memory, bf16 pairs) * B[64 x DP]^T (shared memory, K-major)
-      auto issue_xt = [&](uint32_t d, uint32_t a_tmem, uint32_t b_base) {
+      auto issue_xt = [&](uint32_t d, uint32_t a_tmem, uint64_t bk) {
+        mma_ts_w<false>(d, a_tmem, bk, id_s);
 #pragma unroll
-        for (int kk = 0; kk < DP / 16; ++kk) {
+        for (int kk = 1; kk < DP / 16; ++kk) {
           const int c = kk >> 2, o = (kk & 3) * 32;
-          mma_bf16_ts(d, a_tmem + kk * 8, sdesc_sw128(b_base + c * (L::BK * 128) + o, 16, 1024), id_s,
-                      kk > 0 ? 1u : 0u);
+          mma_ts_w<true>(d, a_tmem + kk * 8, sdesc_add(bk, c * (L::BK * 128) + o), id_s);
         }
       };
       auto issue_tile = [&](int t) {  // S(t), dP(t) into buffers t % 2; frees stage t % 3 when done
         const int s = t % kStages, bb = t & 1;
-        issue_xt(tmem + L::T_S + bb * 64, tmem + L::T_QA, k_at(s));
-        mma_commit(&bar_s_full[bb]);
-        issue_xt(tmem + L::T_DP + bb * 64, tmem + L::T_DYA, v_at(s));
-        mma_commit(&bar_dp_full[bb]);
-        mma_commit(&bar_empty[s]);
+        issue_xt(tmem + L::T_S + bb * 64, tmem + L::T_QA, sdesc_add(dK0, s * L::KT));
+        issue_xt(tmem + L::T_DP + bb * 64, tmem + L::T_DYA, sdesc_add(dV0, s * L::KT));
+        mma_commit_w(&bar_dp_full[bb]);
+        mma_commit_w(&bar_empty[s]);
       };
-      bool ok = mbar_wait(&bar_a_ready, 0, ab);
+      bool ok = mbar_wait_warp(&bar_a_ready, 0, ab);
       tc_fence_after();
       for (int t = 0; t < n && ok; ++t) {
-        if (t >= 2 && !(ok = mbar_wait(&bar_used[t & 1], ((t - 2) >> 1) & 1, ab))) break;
-        if (!(ok = mbar_wait(&bar_full[t % kStages], (t / kStages) & 1, ab))) break;
+        if (t >= 2 && !(ok = mbar_wait_warp(&bar_used[t & 1], ((t - 2) >> 1) & 1, ab))) break;
+        if (!(ok = mbar_wait_warp(&bar_full[t % kStages], (t / kStages) & 1, ab))) break;
         tc_fence_after();
         issue_tile(t);
       }
@@ -190,15 +231,15 @@ __global__ void __launch_bounds__(384, 1)
       for (int t = imax(0, n - kStages); t < n; ++t) drain_wait(&bar_empty[t % kStages], (t / kStages) & 1);
     }
     __syncwarp();
-  } else if (warp >= 4 && warp < 12) {
-    const int g = (warp - 4) >> 2;  // column group: key columns [32g, 32g + 32) of every tile
+  } else if (warp >= 2) {
+    const int g = (warp - 2) >> 2;  // column group: key columns [16g, 16g + 16) of every tile
     const int lg = warp & 3;
     const int row = lg * 32 + lane;  // query row inside the tile == TMEM lane
     const int q = q0 + row;
     const uint32_t lane_addr = static_cast<uint32_t>(lg * 32) << 16;
     const float kInf = __int_as_float(0x7f800000);
     bool ok = n > 0;
-    if (n > 0) {
+    if (n > 0 && g < 2) {
       // stage this row of Q (group 0) or dY (group 1) in tensor memory as bf16
       // pairs: the A operand of S = Q K^T and dP = dY V^T
       ok = mbar_wait_warp(&bar_qdy, 0, ab);
@@ -230,67 +271,90 @@ __global__ void __launch_bounds__(384, 1)
     if (p.window >= 0) ka = q + p.q_off - p.window;
     if (p.causal) kb = imin(kb, q + p.q_off);
     if (q >= p.Sq) ka = 1 << 30, kb = -(1 << 30);
-    // custom-mask value of this lane's key in the group's columns, one tile ahead
-    const float* km = p.has_key_mask ? p.key_mask + static_cast<size_t>(b) * p.Sk : nullptr;
-    auto km_load = [&](int kk) {
-      const int key = kk + 32 * g + lane;
-      return key < p.Sk ? km[key] : kInf;
-    };
-    float kmv = (p.has_key_mask && n > 0) ? km_load(j_lo * L::BK) : 0.f;
     float m2 = -kInf, l = 0.f, dsum = 0.f;
     bool any_unmasked = false;
     for (int t = 0; t < n && ok; ++t) {
       const int s = t % kStages, bb = t & 1;
       const int kk0 = (j_lo + t) * L::BK;
-      uint32_t kbits = 0;
-      if (p.has_key_mask) {
-        kbits = __ballot_sync(0xffffffffu, kmv < p.mask_thr);
-        if (t + 1 < n) kmv = km_load(kk0 + L::BK);
-      }
       if (!(ok = mbar_wait_warp(&bar_full[s], (t / kStages) & 1, ab))) break;
-      if (!(ok = mbar_wait_warp(&bar_s_full[bb], (t >> 1) & 1, ab))) break;
-      if (!(ok = mbar_wait_warp(&bar_dp_full[bb], (t >> 1) & 1, ab))) break;
-      tc_fence_after();
-      uint32_t sr[32], dr[32];
-      tmem_ld32(tmem + L::T_S + bb * 64 + 32 * g + lane_addr, sr);
-      tmem_ld32(tmem + L::T_DP + bb * 64 + 32 * g + lane_addr, dr);
-      float x[32];
-      if (HAS_BIAS) {
-        const uint8_t* brow = sm + L::BIAS_OFF + s * L::BIAS + row * 128;
+      // bias and custom-mask terms of the group's 16 columns while the tensor
+      // core works: x = bias*kb + off, S*sk added below
+      const float* col = reinterpret_cast<const float*>(sm + L::COL_OFF + s * L::COL) + 16 * g;
+      const uint32_t kbits =
+          p.has_key_mask
+              ? (reinterpret_cast<const uint32_t*>(col - 16 * g + 3 * L::BK)[g >> 1] >> (16 * (g & 1))) & 0xffffu
+              : 0u;
+      const uint8_t* brow = sm + L::BIAS_OFF + s * L::BIAS + row * 128;
+      float x[16], skv[16];
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {  // 8 keys per 16-byte bias chunk
-          const int j = 4 * g + jj;
-          const uint4 w4 = *reinterpret_cast<const uint4*>(brow + ((j ^ (row & 7)) << 4));
+      for (int jj = 0; jj < 2; ++jj) {  // 8 keys per 16-byte bias chunk
+        float bv[8];
+        if (HAS_BIAS) {
+          const uint4 w4 = *reinterpret_cast<const uint4*>(brow + (((2 * g + jj) ^ (row & 7)) << 4));
           const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            x[8 * jj + 2 * e] = __uint_as_float(w[e] << 16) * kLog2e;
-            x[8 * jj + 2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u) * kLog2e;
+            bv[2 * e] = __uint_as_float(w[e] << 16);
+            bv[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
+          }
+        }
+        if (p.has_key_mask) {
+#pragma unroll
+          for (int h4 = 0; h4 < 2; ++h4) {
+            const int c = 8 * jj + 4 * h4;
+            const float4 sk4 = *reinterpret_cast<const float4*>(col + c);
+            const float4 kb4 = *reinterpret_cast<const float4*>(col + L::BK + c);
+            const float4 of4 = *reinterpret_cast<const float4*>(col + 2 * L::BK + c);
+            const float kbv[4] = {kb4.x, kb4.y, kb4.z, kb4.w}, ofv[4] = {of4.x, of4.y, of4.z, of4.w};
+            skv[c] = sk4.x;
+            skv[c + 1] = sk4.y;
+            skv[c + 2] = sk4.z;
+            skv[c + 3] = sk4.w;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) x[c + e] = HAS_BIAS ? fmaf(bv[4 * h4 + e], kbv[e], ofv[e]) : ofv[e];
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            x[8 * jj + e] = HAS_BIAS ? bv[e] * kLog2e : 0.f;
+            skv[8 * jj + e] = p.scale_log2;
           }
         }
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_empty[s]);  // bias and column constants read
+      // the dP commit follows the S MMAs of the tile, so it covers both
+      if (!(ok = mbar_wait_warp(&bar_dp_full[bb], (t >> 1) & 1, ab))) break;
+      tc_fence_after();
+      uint32_t sr[16], dr[16];
+      tmem_ld16(tmem + L::T_S + bb * 64 + 16 * g + lane_addr, sr);
+      tmem_ld16(tmem + L::T_DP + bb * 64 + 16 * g + lane_addr, dr);
       tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&bar_used[bb]);
-        mbar_arrive(&bar_empty[s]);
-      }
+      if (lane == 0) mbar_arrive(&bar_used[bb]);
       const bool full = tile_fully_visible(p, q0, q0 + L::BQ - 1, kk0, kk0 + L::BK - 1);
-      const int lo = ka - kk0 - 32 * g, hi = kb - kk0 - 32 * g;  // group-local visible columns
+      // visible columns of this row among the group's 16: [lo, hi]
+      uint32_t vb = 0xffffu;
+      if (!full) {
+        const int lo = ka - kk0 - 16 * g, hi = kb - kk0 - 16 * g;
+        vb = 0u;
+        if (lo <= 15 && hi >= 0 && lo <= hi) {
+          const uint32_t up = hi >= 15 ? 0xffffu : ((1u << (hi + 1)) - 1u);
+          const uint32_t dn = lo <= 0 ? 0xffffu : (0xffffu & ~((1u << lo) - 1u));
+          vb = up & dn;
+        }
+      }
+      any_unmasked |= (vb & ~kbits) != 0u;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) x[c] = fmaf(__uint_as_float(sr[c]), skv[c], x[c]);
+      if (!full) {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) x[c] = ((vb >> c) & 1u) ? x[c] : -kInf;
+      }
       float mt = -kInf;
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const float sc = __uint_as_float(sr[c]) * p.scale_log2;
-        float xc = HAS_BIAS ? x[c] + sc : sc;
-        const bool masked = ((kbits >> c) & 1u) != 0u;
-        const bool vis = full || (c >= lo && c <= hi);
-        if (masked) xc = p.masked_x2;
-        if (!vis) xc = -kInf;
-        any_unmasked |= vis && !masked;
-        x[c] = xc;
-        mt = fmaxf(mt, xc);
-      }
+      for (int c = 0; c < 16; ++c) mt = fmaxf(mt, x[c]);
       if (mt > m2 + kRescaleThreshold || (m2 == -kInf && mt > -kInf)) {
         if (m2 > -kInf) {
           const float alpha = ex2_approx(m2 - mt);
@@ -302,7 +366,7 @@ __global__ void __launch_bounds__(384, 1)
       if (m2 > -kInf) {
         float ls = 0.f, ds = 0.f;
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
+        for (int c = 0; c < 16; ++c) {
           const float e = ex2_approx(x[c] - m2);
           ls += e;
           ds = fmaf(e, __uint_as_float(dr[c]), ds);
@@ -311,24 +375,33 @@ __global__ void __launch_bounds__(384, 1)
         dsum += ds;
       }
     }
-    // merge the two column groups: (m, l, dsum) -> (max m, rescaled sums)
-    if (g == 1) {
-      mg_m[row] = m2;
-      mg_l[row] = l;
-      mg_d[row] = dsum;
-      mg_any[row] = any_unmasked ? 1 : 0;
+    // merge the four column groups: (m, l, dsum) -> (max m, rescaled sums)
+    if (g > 0) {
+      mg_m[g - 1][row] = m2;
+      mg_l[g - 1][row] = l;
+      mg_d[g - 1][row] = dsum;
+      mg_any[g - 1][row] = any_unmasked ? 1 : 0;
     }
     group_sync();
     if (g == 0 && (ok || n == 0) && q < p.Sq) {
-      const float m1 = mg_m[row], l1 = mg_l[row], d1 = mg_d[row];
-      any_unmasked = any_unmasked || mg_any[row] != 0;
-      const float mm = fmaxf(m2, m1);
+      float mm = m2;
+#pragma unroll
+      for (int i = 0; i < kGroups - 1; ++i) {
+        mm = fmaxf(mm, mg_m[i][row]);
+        any_unmasked = any_unmasked || mg_any[i][row] != 0;
+      }
       float lt = 0.f, dt = 0.f;
       if (mm > -kInf) {
         const float a0 = m2 > -kInf ? ex2_approx(m2 - mm) : 0.f;
-        const float a1 = m1 > -kInf ? ex2_approx(m1 - mm) : 0.f;
-        lt = l * a0 + l1 * a1;
-        dt = dsum * a0 + d1 * a1;
+        lt = l * a0;
+        dt = dsum * a0;
+#pragma unroll
+        for (int i = 0; i < kGroups - 1; ++i) {
+          const float mi = mg_m[i][row];
+          const float ai = mi > -kInf ? ex2_approx(mi - mm) : 0.f;
+          lt = fmaf(mg_l[i][row], ai, lt);
+          dt = fmaf(mg_d[i][row], ai, dt);
+        }
       }
       float L2 = kInf, dl = 0.f, pm = 0.f;
       if (lt > 0.f) {
@@ -358,7 +431,7 @@ cudaError_t launch_t(const DenseMaps& m, const DenseParams& p, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(p.B * p.H, cdiv(p.Sq, L::BQ));
-  kern<<<grid, 384, smem, s>>>(m.q128, m.k64, m.v64, m.dy128, m.bias128, p);
+  kern<<<grid, 576, smem, s>>>(m.q128, m.k64, m.v64, m.dy128, m.bias128, p);
   return cudaGetLastError();
 }
 
