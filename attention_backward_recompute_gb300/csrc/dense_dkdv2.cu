@@ -216,7 +216,8 @@ __global__ void __launch_bounds__(512, 1)
       }
     };
     load_stats(0);
-    int last_use[kStages] = {-1, -1, -1};
+    int last_use[kStages];
+    for (int i = 0; i < kStages; ++i) last_use[i] = -1;
     bool ok = true;
     for (int t = 0; t < n && ok; ++t) {
       const int s = t % kStages;

@@ -10,7 +10,7 @@
 //   dQ_i += dS K_j                     tcgen05, A = dS from tensor memory
 // with the softmax scale applied to dQ at the end.  Q_i and dY_i are copied
 // once into tensor memory (bf16 pairs), so the tensor core reads only the K
-// and V tiles from shared memory; K, V and bias tiles come through a 3-stage
+// and V tiles from shared memory; K, V and bias tiles come through a 4-stage
 // TMA ring.  S and dP are double-buffered (b = j % 2) and each S buffer has
 // its own softmax warpgroup.  Warp 0: TMA producer, warp 1: MMA issuer,
 // warps 4..7: softmax of even tiles, warps 12..15: softmax of odd tiles,
@@ -27,7 +27,7 @@ using namespace sm103;
 
 namespace {
 
-constexpr int kStages = 3;
+constexpr int kStages = 4;
 
 template <int DP>
 struct Dq2Layout {
@@ -36,12 +36,16 @@ struct Dq2Layout {
   static constexpr int QT = NCH * BQ * 128;      // Q or dY tile (128 rows)
   static constexpr int KT = NCH * BK * 128;      // K or V tile (64 rows)
   static constexpr int BIAS = BQ * 128;          // 128 query rows x 64 keys
-  static constexpr int Q_OFF = 0;
-  static constexpr int DY_OFF = Q_OFF + QT;
-  static constexpr int K_OFF = DY_OFF + QT;                 // kStages
+  static constexpr int K_OFF = 0;                           // kStages
   static constexpr int V_OFF = K_OFF + kStages * KT;        // kStages
   static constexpr int BIAS_OFF = V_OFF + kStages * KT;     // kStages
   static constexpr int BYTES = BIAS_OFF + kStages * BIAS;
+  // Q and dY are needed in shared memory only until they are staged into
+  // tensor memory: they occupy the K and V slots of stages 2 and 3, which the
+  // producer fills only after that staging
+  static constexpr int Q_OFF = K_OFF + 2 * KT;
+  static constexpr int DY_OFF = V_OFF + 2 * KT;
+  static_assert(QT == 2 * KT && kStages >= 4, "Q / dY alias two ring slots");
   // TMEM: dQ [0, DP), S[2] and dP[2] 64 columns each after that, then the
   // Q and dY rows as bf16 pairs (DP/2 columns each)
   static constexpr int T_S = DP, T_DP = DP + 128;
@@ -195,11 +199,13 @@ __global__ void __launch_bounds__(512, 1)
         tma_load_4d(sm + L::Q_OFF + c * (L::BQ * 128), &tm_q, &bar_qdy, c * 64, q0, h, b);
         tma_load_4d(sm + L::DY_OFF + c * (L::BQ * 128), &tm_dy, &bar_qdy, c * 64, q0, h, b);
       }
-      int last_use[kStages] = {-1, -1, -1};
+      int last_use[kStages];
+      for (int i = 0; i < kStages; ++i) last_use[i] = -1;
       bool ok = true;
       for (int t = 0; t < n && ok; ++t) {
         const int s = t % kStages;
         if (t >= kStages) ok = mbar_wait(&bar_empty[s], ((t / kStages) - 1) & 1, ab);
+        if (t == 2 && ok) ok = mbar_wait(&bar_a_ready, 0, ab);  // Q, dY slots free
         if (!ok) break;
         const int kk0 = (j_lo + t) * L::BK;
         mbar_arrive_expect_tx(&bar_full[s], 2 * L::KT + (HAS_BIAS ? L::BIAS : 0));
@@ -341,8 +347,8 @@ __global__ void __launch_bounds__(512, 1)
       if (p.has_key_mask && sg < n) km_load((j_lo + sg) * L::BK, kmv);
       // Each group waits every phase of its own S buffer.  Of the stage
       // barrier it skips the phases of the other group's tiles; when it waits
-      // for tile t, the phase of tile t - 3 (same stage) has completed, since
-      // the tensor core issued S(t - 2) after it.
+      // for tile t, the phase of tile t - kStages (same stage) has completed,
+      // since the tensor core issued S(t - 2) after it.
       for (int t = sg; t < n && ok; t += 2) {
         const int s = t % kStages, bb = t & 1;
         const int kk0 = (j_lo + t) * L::BK;

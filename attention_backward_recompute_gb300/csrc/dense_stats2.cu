@@ -36,7 +36,7 @@ using namespace sm103;
 
 namespace {
 
-constexpr int kStages = 3;
+constexpr int kStages = 4;
 
 template <int DP>
 struct Stats2Layout {
@@ -45,11 +45,15 @@ struct Stats2Layout {
   static constexpr int QT = NCH * BQ * 128;  // Q or dY tile (128 rows)
   static constexpr int KT = NCH * BK * 128;  // K or V tile (64 rows)
   static constexpr int BIAS = BQ * 128;      // 128 query rows x 64 keys
-  static constexpr int Q_OFF = 0;
-  static constexpr int DY_OFF = Q_OFF + QT;
-  static constexpr int K_OFF = DY_OFF + QT;              // kStages
+  static constexpr int K_OFF = 0;                        // kStages
   static constexpr int V_OFF = K_OFF + kStages * KT;     // kStages
   static constexpr int BIAS_OFF = V_OFF + kStages * KT;  // kStages
+  // Q and dY are needed in shared memory only until they are staged into
+  // tensor memory: they occupy the K and V slots of stages 2 and 3, which the
+  // producer fills only after that staging
+  static constexpr int Q_OFF = K_OFF + 2 * KT;
+  static constexpr int DY_OFF = V_OFF + 2 * KT;
+  static_assert(QT == 2 * KT && kStages >= 4, "Q / dY alias two ring slots");
   // per key column of a tile: sk = scale*log2(e), kb = log2(e), off = 0 for a
   // key the custom mask keeps; sk = kb = 0, off = mask_neg*log2(e) for a
   // custom-masked key (so x = S*sk + bias*kb + off); then the 64-bit set of
@@ -156,11 +160,13 @@ __global__ void __launch_bounds__(576, 1)
       }
     };
     if (p.has_key_mask) km_load(0);
-    int last_use[kStages] = {-1, -1, -1};
+    int last_use[kStages];
+    for (int i = 0; i < kStages; ++i) last_use[i] = -1;
     bool ok = true;
     for (int t = 0; t < n && ok; ++t) {
       const int s = t % kStages;
       if (t >= kStages) ok = mbar_wait_warp(&bar_empty[s], ((t / kStages) - 1) & 1, ab);
+      if (t == 2 && ok) ok = mbar_wait_warp(&bar_a_ready, 0, ab);  // Q, dY slots free
       if (!ok) break;
       const int kk0 = (j_lo + t) * L::BK;
       if (lane == 0) {
