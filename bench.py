@@ -126,6 +126,35 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(rows), "power_w_max": max(r["power"] for r in rows)}
 
 
+# DRAM bytes per launch of the dominant kernel, from the committed ncu summary,
+# scaled from the captured case to this launch by the number of (batch, head)
+# pairs; None when the kernel sources changed since the capture.
+TRAFFIC_PROFILES = {
+    "dkdv": ("profiles/dkdv2_kernel_dense_bf16_b2h8.md",
+             ["dense_dkdv2.cu", "sm103.cuh", "dense_common.cuh", "dense_launch.h"]),
+}
+
+
+def recorded_traffic(kernel: str, units: int):
+    import hashlib
+    import re
+    if kernel not in TRAFFIC_PROFILES:
+        return None
+    prof, files = TRAFFIC_PROFILES[kernel]
+    try:
+        text = open(os.path.join(ROOT, prof)).read()
+        h = hashlib.sha256()
+        for f in files:
+            with open(os.path.join(ROOT, "attention_backward_recompute_gb300", "csrc", f), "rb") as fh:
+                h.update(fh.read())
+    except OSError:
+        return None
+    fields = dict(re.findall(r"^\s*(dram_bytes_per_launch|units_per_launch|sources_sha256):\s*(\S+)", text, re.M))
+    if len(fields) != 3 or fields["sources_sha256"] != h.hexdigest():
+        return None
+    return float(fields["dram_bytes_per_launch"]) * units / float(fields["units_per_launch"])
+
+
 def cpu_baseline(case, budget_s: float):
     """The oracle as it stands, on the host cores, on a bounded sample of heads."""
     import numpy as np  # noqa: F401
@@ -327,6 +356,7 @@ def main():
 
     if rank == 0:
         cpu = cpu_baseline(case, args.cpu_budget) if world == 1 and args.cpu_budget > 0 else None
+        traffic = recorded_traffic(dom, B * H)
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -338,7 +368,7 @@ def main():
                        "pct_of_peak": 100.0 * value / world / peak,
                        "kernel_ms": kmean},
             "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
-                         "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                         "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
                          "peak_source": f"{peak_src} bf16 (burst)",
                          "algorithmic": f"{int(alg[dom] / (D * vp * B * H))}*D flops per visible pair"},
             "cpu_baseline": cpu,
