@@ -79,6 +79,7 @@ _SIG = {
     "attn_last_error": (ctypes.c_char_p, []),
     "attn_status_string": (ctypes.c_char_p, [ctypes.c_int32]),
     "attn_check_device_error": (ctypes.c_int32, [_P]),
+    "attn_selftest_wait_timeout": (ctypes.c_int32, [_P]),
     "attn_version": (ctypes.c_int, []),
     "attn_set_timing_events": (None, [ctypes.POINTER(ctypes.c_void_p), ctypes.c_int]),
 }
@@ -157,6 +158,10 @@ def attn_paged_row_stats(desc, q, qp, k_pool, v_pool, kp_pool, dy, page_table, s
 
 def attn_check_device_error(stream) -> int:
     return int(lib().attn_check_device_error(stream))
+
+
+def attn_selftest_wait_timeout(stream) -> int:
+    return int(lib().attn_selftest_wait_timeout(stream))
 
 
 def attn_set_timing_events(events) -> None:

@@ -257,6 +257,17 @@ ATTN_API const char* attn_status_string(attn_status_t s);
 ATTN_API attn_status_t attn_check_device_error(void* stream);
 
 /*
+ * Self-test of the failure detection above (no counterpart on the pages: it
+ * checks this library's own bounded waits).  Launches on `stream` one warp
+ * that waits on an mbarrier nothing ever arrives on; the wait gives up after
+ * the library's bounded-wait limit (one second), sets the device error word
+ * and the kernel returns.  A following attn_check_device_error(stream) must
+ * report ATTN_ERR_TIMEOUT (and clear the word); the CUDA context stays usable.
+ * Returns ATTN_ERR_CUDA if the launch fails, else ATTN_OK.
+ */
+ATTN_API attn_status_t attn_selftest_wait_timeout(void* stream);
+
+/*
  * Per-kernel timing hook.  When `events` is non-NULL, the next dense or paged
  * call made on this host thread records events[0] on its stream before its
  * first kernel and events[i] after its i-th kernel (events are cudaEvent_t
