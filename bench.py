@@ -214,6 +214,151 @@ def run_reference(args, rank, world):
     return 0
 
 
+def sweep(args) -> int:
+    """Every configuration once (not the bench contract line): GPU time (CUDA
+    events, median of reps), counted TFLOP/s or GB/s, % of the measured peak,
+    max error against the oracle on a sample, and the oracle's own time on that
+    sample with the extrapolation to the whole configuration labelled as such.
+    One JSON line per configuration."""
+    import numpy as np
+    import torch
+    from attention_backward_recompute_gb300 import binding as bd
+    from attention_backward_recompute_gb300 import build, inputs
+    from oracle import attn_bwd_dense, attn_bwd_paged, attn_fwd_dense
+    build.build()
+    bd.lib()
+    peaks, src = load_peaks()
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+
+    def timed(fn, reps):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        bd.check_device_error()
+        return statistics.median(ts), min(ts)
+
+    def rel(got, want, mask=None):
+        g = got.float().cpu().numpy().astype(np.float64)
+        if mask is not None:
+            g, want = g[mask], want[mask]
+        return float(np.max(np.abs(g - want)) / max(np.max(np.abs(want)), 1e-30))
+
+    def emit(d):
+        print(json.dumps(d), flush=True)
+
+    dense = [("C1", "dense_small_f32", {}), ("C2c", "dense_f32_causal", {}), ("C2w", "dense_f32_window", {}),
+             ("C3", "dense_bf16_s2048", {}), ("C3 O+LSE supplied", "dense_bf16_s2048", {"supplied": True}),
+             ("C4", "dense_bf16_cross", {})]
+    for tag, name, opt in dense:
+        c = inputs.dense_config(name)
+        dt = torch.float32 if c.dtype == "f32" else torch.bfloat16
+        t = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda().to(dt)
+        q, k, v, dy = t(c.q), t(c.k), t(c.v), t(c.dy)
+        km = None if c.key_mask is None else torch.from_numpy(c.key_mask).cuda()
+        bias = None if c.bias is None else t(c.bias)
+        o = lse = None
+        if opt.get("supplied"):
+            o_np, lse_np = attn_fwd_dense(c.q, c.k, c.v, layout=c.layout, causal=c.causal, window=c.window,
+                                          key_mask=c.key_mask, bias=c.bias)
+            o = t(o_np)
+            lse = torch.from_numpy(lse_np.astype(np.float32)).cuda()
+        outs = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
+        call = lambda: bd.dense_backward(q, k, v, dy, layout=c.layout, causal=c.causal, window=c.window,
+                                         key_mask=km, bias=bias, o=o, lse=lse, outputs=outs)
+        ms, ms_min = timed(call, 20 if c.seq_q * c.seq_k * c.batch * c.heads > 1e7 else 50)
+        vp = visible_pairs(c.seq_q, c.seq_k, c.causal, c.window)
+        flops = 10.0 * c.head_dim * vp * c.batch * c.heads
+        heads = [(b, h) for b in range(c.batch) for h in range(c.heads)]
+        sample = heads if len(heads) <= 16 else [heads[0], heads[len(heads) // 2], heads[-1]]
+        t0 = time.perf_counter()
+        ref = attn_bwd_dense(c.q, c.k, c.v, c.dy, layout=c.layout, causal=c.causal, window=c.window,
+                             key_mask=c.key_mask, bias=c.bias, heads_subset=sample)
+        t_or = time.perf_counter() - t0
+        res = call()
+        torch.cuda.synchronize()
+        errs = []
+        for g, w in zip(res, ref):
+            gh = g.float().cpu().numpy().astype(np.float64)
+            if c.layout == "bshd":
+                gs = np.stack([gh[b, :, h] for b, h in sample]); ws = np.stack([w[b, :, h] for b, h in sample])
+            else:
+                gs = np.stack([gh[b, h] for b, h in sample]); ws = np.stack([w[b, h] for b, h in sample])
+            errs.append(float(np.max(np.abs(gs - ws)) / max(np.max(np.abs(ws)), 1e-30)))
+        tflops = flops / (ms * 1e-3) / 1e12
+        emit({"config": tag, "workload": name, "gpu_ms_median": ms, "gpu_ms_min": ms_min,
+              "counted_tflops": tflops, "pct_of_bf16_peak": 100.0 * tflops / peaks["bf16_tflops"],
+              "max_err_rel": max(errs), "tolerance": 2e-4 if c.dtype == "f32" else 2e-2,
+              "oracle_s_sample": t_or, "oracle_sample": f"{len(sample)} of {len(heads)} (batch, head) pairs",
+              "oracle_s_extrapolated": t_or * len(heads) / len(sample), "host_cores": cores,
+              "peak_source": src})
+
+    for tag, name in (("C5g", "paged_gqa"), ("C5m", "paged_mla")):
+        c = inputs.paged_config(name)
+        tb = lambda x: None if x is None else torch.from_numpy(np.ascontiguousarray(x)).cuda().to(torch.bfloat16)
+        dv = dict(q=tb(c.q), dy=tb(c.dy), k=tb(c.k_pool), v=tb(c.v_pool), qp=tb(c.qp), kp=tb(c.kp_pool))
+        table = torch.from_numpy(c.page_table).cuda().contiguous()
+        meta = bd.seq_meta_tensor(c.seq_len, c.q_start, c.q_pos, "cuda")
+        lse, delta = bd.paged_row_stats(dv["q"], dv["k"], dv["v"], dv["dy"], table, meta, heads=c.heads,
+                                        kv_heads=c.kv_heads, page_size=c.page_size, causal=c.causal,
+                                        qp=dv["qp"], kp_pool=dv["kp"])
+        first = bd.paged_backward(dv["q"], dv["k"], dv["v"], dv["dy"], table, meta, lse, delta, heads=c.heads,
+                                  kv_heads=c.kv_heads, page_size=c.page_size, causal=c.causal, qp=dv["qp"],
+                                  kp_pool=dv["kp"])
+        buf = tuple(torch.empty_like(x) for x in first)
+        outs = (buf[0], None, buf[1]) if c.position_dim else (buf[0], buf[1], None)
+        call = lambda: bd.paged_backward(dv["q"], dv["k"], dv["v"], dv["dy"], table, meta, lse, delta,
+                                         heads=c.heads, kv_heads=c.kv_heads, page_size=c.page_size,
+                                         causal=c.causal, outputs=outs, qp=dv["qp"], kp_pool=dv["kp"])
+        ms, ms_min = timed(call, 20)
+        stable = all(torch.equal(a, b) for a, b in zip(first, call()))
+        for _ in range(3):
+            stable = stable and all(torch.equal(a, b) for a, b in zip(first, call()))
+        triples = int(sum(int(p) + 1 for p in c.q_pos)) * c.heads if c.causal else None
+        kvh, dk_, dvv = c.kv_heads, c.key_dim, c.value_dim
+        valid = int(np.sum(c.seq_len))
+        slots = c.num_pages * c.page_size
+        if c.position_dim:
+            flops = (2 * (dk_ + c.position_dim) + 2 * dvv + 4 * dvv + 2 * c.position_dim) * triples
+            alg_bytes = (valid * kvh * (dk_ + c.position_dim) * 2 + slots * kvh * (dk_ + c.position_dim) * 2 +
+                         c.q.shape[0] * c.heads * (dk_ + c.position_dim + dvv) * 2)
+        else:
+            flops = 1024 * triples * dk_ // 128
+            alg_bytes = (valid * kvh * (dk_ + dvv) * 2 + slots * kvh * (dk_ + dvv) * 2 +
+                         c.q.shape[0] * c.heads * (dk_ + dvv) * 2)
+        pick = [0, c.num_seqs // 2]
+        qs = [np.arange(c.q_start[s], c.q_start[s + 1]) for s in pick]
+        rows = np.concatenate(qs)
+        sub = np.concatenate([[0], np.cumsum([len(x) for x in qs])]).astype(np.int32)
+        t0 = time.perf_counter()
+        ref = attn_bwd_paged(c.q[rows], c.dy[rows], c.k_pool, c.page_table[pick], c.seq_len[pick], sub,
+                             c.q_pos[rows], page_size=c.page_size, kv_heads=c.kv_heads, v_pool=c.v_pool,
+                             qp=None if c.qp is None else c.qp[rows], kp_pool=c.kp_pool, causal=c.causal)
+        t_or = time.perf_counter() - t0
+        owned = np.zeros(slots, bool)
+        for s_ in pick:
+            for tok in range(int(c.seq_len[s_])):
+                owned[int(c.page_table[s_, tok // c.page_size]) * c.page_size + tok % c.page_size] = True
+        err = max(rel(g, w, owned) for g, w in zip(first, ref))
+        emit({"config": tag, "workload": name, "gpu_ms_median": ms, "gpu_ms_min": ms_min,
+              "counted_tflops": flops / (ms * 1e-3) / 1e12,
+              "pct_of_bf16_peak": 100.0 * flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
+              "algorithmic_gbs": alg_bytes / (ms * 1e-3) / 1e9,
+              "pct_of_hbm_peak": 100.0 * alg_bytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+              "max_err_rel": err, "tolerance": 2e-2, "bit_stable_5_runs": bool(stable),
+              "oracle_s_sample": t_or, "oracle_sample": f"{len(pick)} of {c.num_seqs} sequences",
+              "oracle_s_extrapolated": t_or * c.num_seqs / len(pick), "host_cores": cores,
+              "peak_source": src})
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -224,7 +369,11 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--batch", type=int, default=None, help="override B (profiling runs on a smaller case)")
     ap.add_argument("--heads", type=int, default=None, help="override H (profiling runs on a smaller case)")
+    ap.add_argument("--sweep", action="store_true",
+                    help="time every configuration once against its oracle sample (one JSON line each)")
     args = ap.parse_args()
+    if args.sweep:
+        return sweep(args)
     args.warmup = max(args.warmup, 3)
 
     rank = int(os.environ.get("RANK", "0"))
