@@ -235,6 +235,17 @@ __global__ void __launch_bounds__(512, 1)
           tma_load_4d(bs, &tm_bias, &bar_full[s], k0, q0, h, b);
           tma_load_4d(bs + L::BQ * 128, &tm_bias, &bar_full[s], k0 + 64, q0, h, b);
         }
+        if (t + kStages < n) {  // the tile that will reuse this stage, into L2
+          const int qn = (i_lo + t + kStages) * L::BQ;
+          for (int c = 0; c < L::NCH; ++c) {
+            tma_prefetch_l2_4d(&tm_q, c * 64, qn, h, b);
+            tma_prefetch_l2_4d(&tm_dy, c * 64, qn, h, b);
+          }
+          if (HAS_BIAS) {
+            tma_prefetch_l2_4d(&tm_bias, k0, qn, h, b);
+            tma_prefetch_l2_4d(&tm_bias, k0 + 64, qn, h, b);
+          }
+        }
       }
       float* st = reinterpret_cast<float*>(sm + L::ST_OFF) + s * 3 * L::BQ;
 #pragma unroll

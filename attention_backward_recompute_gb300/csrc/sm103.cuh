@@ -137,6 +137,17 @@ __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
+// Prefetch a tile into L2 (no shared memory, no barrier): issued a few
+// tiles ahead of the tile's real load, so that the load finds its data in L2.
+// The same coordinate rules as tma_load_4d apply; out-of-range parts are
+// simply not fetched.
+__device__ __forceinline__ void tma_prefetch_l2_4d(const CUtensorMap* map, int c0, int c1, int c2, int c3) {
+  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+               : "memory");
+}
+
 // Generic-proxy writes to shared memory (st.shared) become visible to the
 // async proxy (tensor cores, TMA) only after this fence.
 __device__ __forceinline__ void fence_proxy_async_smem() {
