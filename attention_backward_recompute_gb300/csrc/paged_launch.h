@@ -23,6 +23,14 @@ cudaError_t launch_paged_row_stats(const PagedMaps& m, const PagedParams& p, cud
 // MLA (key_dim 512 latent + position_dim 64; the latent is also the value)
 cudaError_t launch_paged_mla_history(const PagedParams& p, const void* q, const void* qp, const void* dy,
                                      const void* k_pool, const void* kp_pool, cudaStream_t s);
+// MLA on the warp-level tensor path: q, qp, dy as [Nq, H, D] addressed
+// (d, h, r) with box (64, G, 32/G); latent and position pools as [slots, KVH, D]
+// with box (64, 1, 16).
+struct PagedMlaMaps {
+  CUtensorMap q, qp, dy, k, kp;
+};
+bool mla_mma_supported(const PagedParams& p);
+cudaError_t launch_paged_mla_mma(const PagedMlaMaps& m, const PagedParams& p, cudaStream_t s);
 cudaError_t launch_paged_mla_stats(const PagedParams& p, const void* q, const void* qp, const void* dy,
                                    const void* k_pool, const void* kp_pool, cudaStream_t s);
 

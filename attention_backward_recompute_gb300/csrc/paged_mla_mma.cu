@@ -1,0 +1,391 @@
+// Paged MLA history backward on the warp-level tensor path (mma.sync bf16).
+//
+// ruDNN src/paged_attention/ordered_kernel.rs (history_backward with `mla`):
+// for query row r, head h and history token t,
+//   s = scale * (q[r,h] . k_lat[t] + qp[r,h] . k_pos[t]),  p = exp(s - lse[r,h])
+//   ds = p * (dY[r,h] . k_lat[t] - delta[r,h]) * scale
+//   dK_lat[t] += ds * q[r,h] + p * dY[r,h]      (the latent is key and value)
+//   dKp[t]    += ds * qp[r,h]
+// summed over the links of the token's page (link order), the visible rows of
+// each linked sequence (t <= pos(r) when causal) and the heads of the group.
+//
+// Why mma.sync and not tcgen05: the accumulator of one 64-token block is
+// 64 x 576 fp32 (144 KiB); with the score and dP tiles it does not fit the
+// 512 tensor-memory columns, while 16 warps hold it in registers (72 per
+// thread).  The warp-level tensor path runs at about a quarter of tcgen05's
+// rate on this GPU, which is still far above CUDA-core FMA.
+//
+// One CTA owns 64 tokens (four 16-token pages) of one sequence and one KV head
+// and walks the same passes as the GQA kernel: its own sequence, then for
+// every page it stores that other links share, those links in link order.
+// A column is one (query row, head of the group) pair; a tile is 32 columns
+// (32 / G rows).  Per tile:
+//   phase A  warp (token tile tt, column octet n8): S^T and dP^T (16 x 8) with
+//            one k-loop over the 512 latent dims (K fragments shared by both)
+//            plus the 64 position dims for S^T; P^T and dS^T in registers,
+//            stored to shared memory as bf16
+//   phase B  warp (token tile tt, dim quarter dr): dK_lat[., 128 dr ..+128)
+//            += dS^T Q + P^T dY and dKp[., 16 dr ..+16) += dS^T Qp
+// The K tile (latent + position, 9 chunks of 64 dims) stays in shared memory;
+// Q, Qp and dY tiles arrive by TMA in 128-byte-swizzled 64-dim chunks,
+// double-buffered.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "paged_common.cuh"
+#include "paged_launch.h"
+#include "sm103.cuh"
+
+namespace attn {
+using namespace sm103;
+
+namespace {
+
+constexpr int kLat = 512, kPos = 64;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr int BT = 64;                      // tokens per CTA (4 pages of 16)
+constexpr int BC = 32;                      // columns per tile
+constexpr int kThreads = 512;
+constexpr int CH = BT * 128;                // K chunk: [64 tokens][64 dims]
+constexpr int K_OFF = 0;                    // 8 latent chunks + 1 position chunk
+constexpr int CQ = BC * 128;                // column chunk: [32 columns][64 dims]
+constexpr int STAGE = 17 * CQ;              // Q (8 chunks), Qp (1), dY (8)
+constexpr int ST_OFF = K_OFF + 9 * CH;      // 2 stages
+constexpr int PS_STRIDE = BC * 2 + 16;      // P^T / dS^T rows: 32 bf16 + 16 bytes of padding
+constexpr int PS = BT * PS_STRIDE;
+constexpr int P_OFF = ST_OFF + 2 * STAGE;   // P^T then dS^T
+constexpr int BYTES = P_OFF + 2 * PS;
+static_assert(ST_OFF % 1024 == 0 && STAGE % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+
+struct MPageInfo {
+  int phys[4];    // physical page (or -1)
+  int off[4];     // first index of the page's link segment
+  int cnt[4];     // links of the page
+  int store[4];   // this CTA stores the page
+};
+
+// The passes of a CTA: its own sequence over all 64 tokens, then for every
+// page j it stores, the other links of that page with only its 16 tokens live.
+struct MPass {
+  const PagedParams* p;
+  const MPageInfo* pi;
+  int s0, tb;
+  int j, li;
+  int seq, tbase, ra, rb, r_begin, r_end, tile, ntiles;
+
+  __device__ void load(int sq, int tbs, int a, int b, int rt) {
+    seq = sq;
+    tbase = tbs;
+    ra = a;
+    rb = b;
+    r_begin = row_begin_of(*p, sq);
+    r_end = row_end_of(*p, sq);
+    tile = 0;
+    ntiles = (r_end - r_begin + rt - 1) / rt;
+  }
+  __device__ bool next_pass(int rt) {
+    while (true) {
+      if (j < 0) {
+        j = 0;
+        li = 1;
+      } else {
+        ++li;
+      }
+      while (j < 4 && !(pi->store[j] && li < pi->cnt[j])) {
+        ++j;
+        li = 1;
+      }
+      if (j >= 4) return false;
+      const int link = p->links[pi->off[j] + li];
+      const int s2 = link / p->max_pages, lp2 = link - s2 * p->max_pages;
+      load(s2, lp2 * p->page_size - 16 * j, 16 * j, 16 * j + 16, rt);
+      if (ntiles > 0) return true;
+    }
+  }
+  __device__ bool begin(int rt) {
+    j = -1;
+    li = 0;
+    load(s0, tb * BT, 0, BT, rt);
+    if (ntiles > 0) return true;
+    return next_pass(rt);
+  }
+  __device__ bool advance(int rt) {
+    if (++tile < ntiles) return true;
+    return next_pass(rt);
+  }
+};
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr) : "memory");
+}
+// D (16x8 fp32) += A (16x16 bf16, row) * B (16x8 bf16, col)
+__device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// address of the 16-byte piece `piece` (0..7) of row `row` in a 128-byte-swizzled chunk
+__device__ __forceinline__ uint32_t swz(uint32_t base, int row, int piece) {
+  return base + row * 128 + (((piece ^ row) & 7) << 4);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    mla_mma_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_qp,
+                   const __grid_constant__ CUtensorMap tm_dy, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_kp, const PagedParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ uint64_t bar_k, bar_full[2];
+  __shared__ int abort_flag;
+  __shared__ MPageInfo pinfo;
+  __shared__ int n_tiles_sh;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tb = blockIdx.x, s0 = blockIdx.y, gkv = blockIdx.z;
+  const int npg = pages_of(seq_len_of(p, s0), p.page_size);
+  if (tb * 4 >= npg) return;  // no token of this sequence in the block (uniform exit)
+  const int G = p.G, RT = BC / G;
+  const Abort ab{&abort_flag, p.err};
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&bar_k, 1);
+    mbar_init(&bar_full[0], 1);
+    mbar_init(&bar_full[1], 1);
+    mbar_fence_init();
+    for (int j = 0; j < 4; ++j) {
+      const int lp = tb * 4 + j;
+      int ph = -1, off = 0, cnt = 0, st = 0;
+      if (lp < npg) {
+        ph = p.page_table[static_cast<int64_t>(s0) * p.max_pages + lp];
+        if (ph >= 0 && ph < p.num_pages) {
+          off = p.link_off[ph];
+          cnt = p.link_off[ph + 1] - off;
+          st = cnt > 0 && p.links[off] == s0 * p.max_pages + lp;
+        } else {
+          ph = -1;
+        }
+      }
+      pinfo.phys[j] = ph;
+      pinfo.off[j] = off;
+      pinfo.cnt[j] = cnt;
+      pinfo.store[j] = st;
+    }
+    MPass it{&p, &pinfo, s0, tb};
+    int n = 0;
+    if (it.begin(RT)) {
+      do ++n;
+      while (it.advance(RT));
+    }
+    n_tiles_sh = n;
+  }
+  __syncthreads();
+  const int n = n_tiles_sh;
+  const uint32_t sbase = smem_addr(sm);
+  const int oob_slot = p.num_pages * p.page_size;  // out-of-range coordinate: TMA fills zeros
+
+  // thread 0 issues the copies; the pass iterator runs one tile ahead of use
+  MPass pf{&p, &pinfo, s0, tb};
+  bool pf_live = false;
+  auto issue_tile = [&](int stage) {
+    const int r0 = pf.r_begin + pf.tile * RT;
+    uint64_t* bar = &bar_full[stage];
+    mbar_arrive_expect_tx(bar, STAGE);
+    uint8_t* st = sm + ST_OFF + stage * STAGE;
+    for (int c = 0; c < 8; ++c) {
+      tma_load_3d(st + c * CQ, &tm_q, bar, c * 64, gkv * G, r0);
+      tma_load_3d(st + (9 + c) * CQ, &tm_dy, bar, c * 64, gkv * G, r0);
+    }
+    tma_load_3d(st + 8 * CQ, &tm_qp, bar, 0, gkv * G, r0);
+  };
+  if (threadIdx.x == 0 && n > 0) {
+    tma_prefetch_map(&tm_q);
+    tma_prefetch_map(&tm_qp);
+    tma_prefetch_map(&tm_dy);
+    tma_prefetch_map(&tm_k);
+    tma_prefetch_map(&tm_kp);
+    mbar_arrive_expect_tx(&bar_k, 9 * CH);
+    for (int j = 0; j < 4; ++j) {
+      const int slot = pinfo.phys[j] >= 0 ? pinfo.phys[j] * p.page_size : oob_slot;
+      for (int c = 0; c < 8; ++c) tma_load_3d(sm + K_OFF + c * CH + j * 16 * 128, &tm_k, &bar_k, c * 64, gkv, slot);
+      tma_load_3d(sm + K_OFF + 8 * CH + j * 16 * 128, &tm_kp, &bar_k, 0, gkv, slot);
+    }
+    pf_live = pf.begin(RT);
+    for (int t = 0; t < 2 && t < n && pf_live; ++t) {
+      issue_tile(t);
+      pf_live = pf.advance(RT);
+    }
+  }
+
+  const int tt = warp & 3;        // token tile (16 tokens, = page tt of the block)
+  const int n8 = warp >> 2;       // phase A: column octet
+  const int dr = warp >> 2;       // phase B: dim quarter
+  const int g8 = lane >> 2, t4 = lane & 3;
+  float acc[16][4], accp[2][4];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) accp[i][0] = accp[i][1] = accp[i][2] = accp[i][3] = 0.f;
+
+  MPass it{&p, &pinfo, s0, tb};
+  bool live = n > 0 && it.begin(RT);
+  bool ok = n > 0 ? mbar_wait_warp(&bar_k, 0, ab) : true;
+  const float kInf = __int_as_float(0x7f800000);
+  const uint32_t p_base = sbase + P_OFF, ds_base = sbase + P_OFF + PS;
+  for (int t = 0; t < n; ++t) {
+    const int stage = t & 1;
+    const uint32_t stb = sbase + ST_OFF + stage * STAGE;
+    // column data of this thread's two phase-A columns
+    const int r0 = it.r_begin + it.tile * RT;
+    float lse_c[2], dl_c[2];
+    int pos_c[2];
+    bool col_ok[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int c = n8 * 8 + 2 * t4 + e;
+      const int r = r0 + c / G, hh = gkv * G + c % G;
+      col_ok[e] = r < it.r_end;
+      const size_t si = static_cast<size_t>(col_ok[e] ? r : 0) * p.H + hh;
+      lse_c[e] = col_ok[e] ? p.lse[si] * kLog2e : kInf;
+      dl_c[e] = col_ok[e] ? p.delta[si] : 0.f;
+      pos_c[e] = col_ok[e] ? (p.causal ? p.q_pos[r] : 0x7fffffff) : -1;
+    }
+    if (ok) ok = mbar_wait_warp(&bar_full[stage], (t >> 1) & 1, ab);
+    if (ok) {
+      // ---------------------------------------------------------------- phase A
+      float sacc[4] = {0.f, 0.f, 0.f, 0.f}, dpacc[4] = {0.f, 0.f, 0.f, 0.f};
+      const int arow = tt * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
+      const int ahalf = lane >> 4;
+      const int brow = n8 * 8 + (lane & 7);
+      const int bm = lane >> 3;  // matrix of the x4 B load: 0,1 Q (k halves), 2,3 dY
+#pragma unroll 2
+      for (int kc = 0; kc < 8; ++kc) {
+#pragma unroll
+        for (int kp = 0; kp < 4; ++kp) {
+          uint32_t a[4], bq[4];
+          ldsm_x4(swz(sbase + K_OFF + kc * CH, arow, 2 * kp + ahalf), a);
+          const uint32_t bchunk = stb + ((bm >> 1) ? (9 + kc) : kc) * CQ;
+          ldsm_x4(swz(bchunk, brow, 2 * kp + (bm & 1)), bq);
+          mma_16816(sacc, a, bq[0], bq[1]);
+          mma_16816(dpacc, a, bq[2], bq[3]);
+        }
+      }
+#pragma unroll
+      for (int kp = 0; kp < 4; ++kp) {
+        uint32_t a[4], b0, b1;
+        ldsm_x4(swz(sbase + K_OFF + 8 * CH, arow, 2 * kp + ahalf), a);
+        ldsm_x2(swz(stb + 8 * CQ, brow, 2 * kp + (bm & 1)), b0, b1);
+        mma_16816(sacc, a, b0, b1);
+      }
+      // P^T and dS^T of this warp's 16 tokens x 8 columns
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+        const int i = tt * 16 + g8 + 8 * hr;  // block-local token
+        const int tok = it.tbase + i;
+        const bool tok_ok = i >= it.ra && i < it.rb && tok < seq_len_of(p, it.seq);
+        float pv[2], dsv[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const bool vis = tok_ok && col_ok[e] && tok <= pos_c[e] && lse_c[e] > -kInf;
+          const float pe = ex2_approx(fmaf(sacc[2 * hr + e], p.scale_log2, -lse_c[e]));
+          // select, not multiply: dP of a tail or unowned slot may be NaN
+          pv[e] = vis ? pe : 0.f;
+          dsv[e] = vis ? pe * (dpacc[2 * hr + e] - dl_c[e]) * p.scale : 0.f;
+        }
+        const int c = n8 * 8 + 2 * t4;
+        *reinterpret_cast<uint32_t*>(sm + P_OFF + i * PS_STRIDE + c * 2) = pack_bf16x2(pv[0], pv[1]);
+        *reinterpret_cast<uint32_t*>(sm + P_OFF + PS + i * PS_STRIDE + c * 2) = pack_bf16x2(dsv[0], dsv[1]);
+      }
+    }
+    __syncthreads();
+    if (ok && !abort_flag) {
+      // ---------------------------------------------------------------- phase B
+      const int arow = tt * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
+      const int bm = lane >> 3;
+#pragma unroll
+      for (int ks = 0; ks < 2; ++ks) {
+        uint32_t ads[4], ap[4];
+        const uint32_t aoff = arow * PS_STRIDE + (ks * 16 + 8 * (lane >> 4)) * 2;
+        ldsm_x4(ds_base + aoff, ads);
+        ldsm_x4(p_base + aoff, ap);
+        const int krow = ks * 16 + (lane & 7) + 8 * (bm & 1);  // column index = B row
+#pragma unroll
+        for (int np = 0; np < 8; ++np) {  // pairs of 8-dim tiles: dims 128 dr + 16 np
+          const int chunk = 2 * dr + (np >> 2);
+          const int piece = 2 * (np & 3) + (bm >> 1);
+          uint32_t bq[4], bd[4];
+          ldsm_x4_t(swz(stb + chunk * CQ, krow, piece), bq);
+          ldsm_x4_t(swz(stb + (9 + chunk) * CQ, krow, piece), bd);
+          mma_16816(acc[2 * np], ads, bq[0], bq[1]);
+          mma_16816(acc[2 * np + 1], ads, bq[2], bq[3]);
+          mma_16816(acc[2 * np], ap, bd[0], bd[1]);
+          mma_16816(acc[2 * np + 1], ap, bd[2], bd[3]);
+        }
+        uint32_t bqp[4];
+        ldsm_x4_t(swz(stb + 8 * CQ, krow, 2 * dr + (bm >> 1)), bqp);
+        mma_16816(accp[0], ads, bqp[0], bqp[1]);
+        mma_16816(accp[1], ads, bqp[2], bqp[3]);
+      }
+    }
+    __syncthreads();  // stage and P^T/dS^T buffers free
+    if (threadIdx.x == 0 && pf_live && !abort_flag) {
+      issue_tile(stage);  // tile t + 2 into the stage just freed
+      pf_live = pf.advance(RT);
+    }
+    live = it.advance(RT);
+  }
+  (void)live;
+  // every issued copy was consumed (each tile waited for its stage); store the
+  // pages this CTA owns, one row per token, zeros where nothing was added
+  if (n > 0 && (!ok || abort_flag)) return;
+  if (!pinfo.store[tt]) return;
+  const int slot_base = pinfo.phys[tt] * p.page_size;
+#pragma unroll
+  for (int hr = 0; hr < 2; ++hr) {
+    const int64_t prow = static_cast<int64_t>(slot_base + g8 + 8 * hr) * p.KVH + gkv;
+    if (p.wrt & 2u) {
+      __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.dk_pool) + prow * kLat + 128 * dr + 2 * t4;
+#pragma unroll
+      for (int nt = 0; nt < 16; ++nt)
+        *reinterpret_cast<uint32_t*>(o + nt * 8) = pack_bf16x2(acc[nt][2 * hr], acc[nt][2 * hr + 1]);
+    }
+    if (p.wrt & 8u) {
+      __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.dkp_pool) + prow * kPos + 16 * dr + 2 * t4;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+        *reinterpret_cast<uint32_t*>(o + nt * 8) = pack_bf16x2(accp[nt][2 * hr], accp[nt][2 * hr + 1]);
+    }
+  }
+}
+
+}  // namespace
+
+bool mla_mma_supported(const PagedParams& p) {
+  return p.Dk == kLat && p.Dp == kPos && p.page_size == 16 && (p.G == 4 || p.G == 8 || p.G == 16 || p.G == 32);
+}
+
+cudaError_t launch_paged_mla_mma(const PagedMlaMaps& m, const PagedParams& p, cudaStream_t s) {
+  if (p.num_pages == 0 || p.S == 0 || p.max_pages == 0) return cudaSuccess;
+  const int smem = BYTES + 1024;
+  cudaError_t e = cudaFuncSetAttribute(mla_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((p.max_pages + 3) / 4, p.S, p.KVH);
+  mla_mma_kernel<<<grid, kThreads, smem, s>>>(m.q, m.qp, m.dy, m.k, m.kp, p);
+  return cudaGetLastError();
+}
+
+}  // namespace attn
