@@ -269,6 +269,28 @@ ATTN_API attn_status_t attn_paged_row_stats(const attn_paged_desc* d, const void
   if ((st = fill_params(d, z, page_table, seq_meta, workspace, &p)) != ATTN_OK) return st;
   p.lse_out = lse;
   p.delta_out = delta;
+  if (mla && attn::mla_mma_supported(p)) {
+    attn::PagedMlaMaps mm;
+    std::memset(&mm, 0, sizeof(mm));
+    const uint64_t slots = uint64_t(d->num_pages) * d->page_size;
+    const uint32_t G = uint32_t(p.G), RT2 = 64u / G;
+    bool enc = encode3d(&mm.q, q, d->key_dim, d->heads, d->num_queries, 64, G, RT2) &&
+               encode3d(&mm.qp, qp, d->position_dim, d->heads, d->num_queries, 64, G, RT2) &&
+               encode3d(&mm.dy, dy, d->value_dim, d->heads, d->num_queries, 64, G, RT2);
+    if (slots > 0)
+      enc = enc && encode3d(&mm.k, k_pool, d->key_dim, d->kv_heads, slots, 64, 1, uint32_t(d->page_size)) &&
+            encode3d(&mm.kp, kp_pool, d->position_dim, d->kv_heads, slots, 64, 1, uint32_t(d->page_size));
+    else
+      mm.k = mm.kp = mm.q;
+    if (!enc) return api_fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    attn::timing_mark_begin(1, s);
+    cudaError_t e = attn::launch_paged_mla_stats_mma(mm, p, s);
+    attn::timing_mark(s);
+    attn::timing_mark_end();
+    if (e != cudaSuccess) return api_fail(ATTN_ERR_CUDA, "row-statistics launch failed: %s", cudaGetErrorString(e));
+    return api_ok();
+  }
   if (mla) {
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     attn::timing_mark_begin(1, s);

@@ -31,6 +31,8 @@ struct PagedMlaMaps {
 };
 bool mla_mma_supported(const PagedParams& p);
 cudaError_t launch_paged_mla_mma(const PagedMlaMaps& m, const PagedParams& p, cudaStream_t s);
+// MLA row statistics on the same path; q, qp, dy maps with box (64, G, 64/G)
+cudaError_t launch_paged_mla_stats_mma(const PagedMlaMaps& m, const PagedParams& p, cudaStream_t s);
 cudaError_t launch_paged_mla_stats(const PagedParams& p, const void* q, const void* qp, const void* dy,
                                    const void* k_pool, const void* kp_pool, cudaStream_t s);
 

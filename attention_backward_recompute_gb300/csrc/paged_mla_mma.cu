@@ -372,10 +372,242 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Row statistics (lse, delta) of the MLA history on the same tensor path.
+// One CTA owns 64 columns (64 / G query rows of one sequence, the G heads of
+// one KV head) with their q, qp and dY resident in shared memory, and streams
+// the sequence's keys in 32-token tiles (latent + position, double-buffered).
+// Warp (token tile tt of 16, column octet n8) computes S^T and dP^T for
+// 16 tokens x 8 columns per tile; each thread keeps, for its two columns, the
+// online maximum m, l = sum 2^(x - m) and dsum = sum 2^(x - m) dP over its
+// tokens (x = S * scale * log2 e); the partial triples are merged across lanes
+// and warps at the end:  lse = (m + log2 l) * ln 2,  delta = dsum / l
+// (= rowsum(P dP) = dY . O, the dS row offset of the page's backward).
+// ---------------------------------------------------------------------------
+constexpr int SBT = 32;                   // tokens per step (2 pages)
+constexpr int SBC = 64;                   // columns per CTA
+constexpr int SKC = SBT * 128;            // key chunk: [32 tokens][64 dims]
+constexpr int SK_STAGE = 9 * SKC;         // 8 latent chunks + 1 position chunk
+constexpr int SQC = SBC * 128;            // column chunk: [64 columns][64 dims]
+constexpr int SQ_OFF = 0;                 // q (8 chunks), qp (1), dY (8)
+constexpr int SK_OFF = SQ_OFF + 17 * SQC; // 2 stages
+constexpr int S_BYTES = SK_OFF + 2 * SK_STAGE;
+static_assert(SK_OFF % 1024 == 0 && SK_STAGE % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+
+// merge two online-softmax partials (base-2 maxima)
+__device__ __forceinline__ void merge_stat(float& m, float& l, float& d, float m2, float l2, float d2) {
+  const float kNegInf = -__int_as_float(0x7f800000);
+  const float mm = fmaxf(m, m2);
+  if (mm == kNegInf) return;
+  const float a = m > kNegInf ? ex2_approx(m - mm) : 0.f, b = m2 > kNegInf ? ex2_approx(m2 - mm) : 0.f;
+  l = l * a + l2 * b;
+  d = d * a + d2 * b;
+  m = mm;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    mla_stats_mma_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_qp,
+                         const __grid_constant__ CUtensorMap tm_dy, const __grid_constant__ CUtensorMap tm_k,
+                         const __grid_constant__ CUtensorMap tm_kp, const PagedParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ uint64_t bar_q, bar_k[2];
+  __shared__ int abort_flag, ntok_sh, seq_sh, r0_sh;
+  __shared__ float mg[3][SBC];  // the second token tile's partials: (m, l, dsum) per column
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gkv = blockIdx.x;
+  const int G = p.G, RT2 = SBC / G;
+  // this CTA's (sequence, row tile): the row tiles of every sequence, in order
+  if (threadIdx.x == 0) {
+    int idx = blockIdx.y, sq = -1, r0 = 0;
+    for (int q = 0; q < p.S; ++q) {
+      const int tiles = (row_end_of(p, q) - row_begin_of(p, q) + RT2 - 1) / RT2;
+      if (idx < tiles) {
+        sq = q;
+        r0 = row_begin_of(p, q) + idx * RT2;
+        break;
+      }
+      idx -= tiles;
+    }
+    seq_sh = sq;
+    r0_sh = r0;
+  }
+  __syncthreads();
+  const int s = seq_sh, r0 = r0_sh;
+  if (s < 0) return;  // past the last row tile (uniform exit)
+  const int re = row_end_of(p, s);
+  const int len = seq_len_of(p, s);
+  const int npg = pages_of(len, p.page_size);
+  const Abort ab{&abort_flag, p.err};
+  const int oob_slot = p.num_pages * p.page_size;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&bar_q, 1);
+    mbar_init(&bar_k[0], 1);
+    mbar_init(&bar_k[1], 1);
+    mbar_fence_init();
+    int ntok = len;
+    if (p.causal) {  // tokens past the largest position of the CTA's rows are never visible
+      int mp = -1;
+      for (int r = r0; r < r0 + RT2 && r < re; ++r) mp = max(mp, p.q_pos[r]);
+      ntok = min(len, mp + 1);
+    }
+    ntok_sh = max(ntok, 0);
+  }
+  __syncthreads();
+  const int nt = (ntok_sh + SBT - 1) / SBT;
+  auto issue_keys = [&](int t, int stage) {
+    uint64_t* bar = &bar_k[stage];
+    mbar_arrive_expect_tx(bar, SK_STAGE);
+    uint8_t* dst = sm + SK_OFF + stage * SK_STAGE;
+    for (int j = 0; j < 2; ++j) {
+      const int lp = 2 * t + j;
+      int slot = oob_slot;
+      if (lp < npg) {
+        const int ph = p.page_table[static_cast<int64_t>(s) * p.max_pages + lp];
+        if (ph >= 0 && ph < p.num_pages) slot = ph * p.page_size;
+      }
+      for (int c = 0; c < 8; ++c) tma_load_3d(dst + c * SKC + j * 16 * 128, &tm_k, bar, c * 64, gkv, slot);
+      tma_load_3d(dst + 8 * SKC + j * 16 * 128, &tm_kp, bar, 0, gkv, slot);
+    }
+  };
+  if (threadIdx.x == 0) {
+    mbar_arrive_expect_tx(&bar_q, 17 * SQC);
+    for (int c = 0; c < 8; ++c) {
+      tma_load_3d(sm + SQ_OFF + c * SQC, &tm_q, &bar_q, c * 64, gkv * G, r0);
+      tma_load_3d(sm + SQ_OFF + (9 + c) * SQC, &tm_dy, &bar_q, c * 64, gkv * G, r0);
+    }
+    tma_load_3d(sm + SQ_OFF + 8 * SQC, &tm_qp, &bar_q, 0, gkv * G, r0);
+    for (int t = 0; t < 2 && t < nt; ++t) issue_keys(t, t);
+  }
+
+  const int tt = warp & 1, n8 = warp >> 1;  // 2 token tiles x 8 column octets
+  const int g8 = lane >> 2, t4 = lane & 3;
+  const float kNegInf = -__int_as_float(0x7f800000);
+  int pos_c[2], r_c[2];
+  bool col_ok[2];
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    const int c = n8 * 8 + 2 * t4 + e;
+    r_c[e] = r0 + c / G;
+    col_ok[e] = r_c[e] < re;
+    pos_c[e] = col_ok[e] ? (p.causal ? p.q_pos[r_c[e]] : 0x7fffffff) : -1;
+  }
+  float m[2] = {kNegInf, kNegInf}, l[2] = {0.f, 0.f}, ds[2] = {0.f, 0.f};
+  const uint32_t sbase = smem_addr(sm);
+  bool ok = nt > 0 ? mbar_wait_warp(&bar_q, 0, ab) : true;
+  for (int t = 0; t < nt; ++t) {
+    const int stage = t & 1;
+    const uint32_t kb = sbase + SK_OFF + stage * SK_STAGE;
+    if (ok) ok = mbar_wait_warp(&bar_k[stage], (t >> 1) & 1, ab);
+    if (ok) {
+      float sacc[4] = {0.f, 0.f, 0.f, 0.f}, dpacc[4] = {0.f, 0.f, 0.f, 0.f};
+      const int arow = tt * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
+      const int ahalf = lane >> 4;
+      const int brow = n8 * 8 + (lane & 7);
+      const int bm = lane >> 3;
+#pragma unroll 2
+      for (int kc = 0; kc < 8; ++kc) {
+#pragma unroll
+        for (int kp = 0; kp < 4; ++kp) {
+          uint32_t a[4], bq[4];
+          ldsm_x4(swz(kb + kc * SKC, arow, 2 * kp + ahalf), a);
+          ldsm_x4(swz(sbase + SQ_OFF + ((bm >> 1) ? (9 + kc) : kc) * SQC, brow, 2 * kp + (bm & 1)), bq);
+          mma_16816(sacc, a, bq[0], bq[1]);
+          mma_16816(dpacc, a, bq[2], bq[3]);
+        }
+      }
+#pragma unroll
+      for (int kp = 0; kp < 4; ++kp) {
+        uint32_t a[4], b0, b1;
+        ldsm_x4(swz(kb + 8 * SKC, arow, 2 * kp + ahalf), a);
+        ldsm_x2(swz(sbase + SQ_OFF + 8 * SQC, brow, 2 * kp + (bm & 1)), b0, b1);
+        mma_16816(sacc, a, b0, b1);
+      }
+      // online update of this thread's two columns over its two tokens
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        float x[2];
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+          const int tok = t * SBT + tt * 16 + g8 + 8 * hr;
+          const bool vis = col_ok[e] && tok < len && tok <= pos_c[e];
+          x[hr] = vis ? sacc[2 * hr + e] * p.scale_log2 : kNegInf;
+        }
+        const float mt = fmaxf(x[0], x[1]);
+        if (mt > m[e]) {
+          const float a = m[e] > kNegInf ? ex2_approx(m[e] - mt) : 0.f;
+          l[e] *= a;
+          ds[e] *= a;
+          m[e] = mt;
+        }
+        if (m[e] > kNegInf) {
+#pragma unroll
+          for (int hr = 0; hr < 2; ++hr) {
+            const float pe = x[hr] > kNegInf ? ex2_approx(x[hr] - m[e]) : 0.f;
+            l[e] += pe;
+            ds[e] = x[hr] > kNegInf ? fmaf(pe, dpacc[2 * hr + e], ds[e]) : ds[e];
+          }
+        }
+      }
+    }
+    __syncthreads();  // stage free
+    if (threadIdx.x == 0 && t + 2 < nt && ok && !abort_flag) issue_keys(t + 2, stage);
+  }
+  // merge over the 8 lanes that share a column pair (different tokens) ...
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, m[e], o);
+      const float l2 = __shfl_xor_sync(0xffffffffu, l[e], o);
+      const float d2 = __shfl_xor_sync(0xffffffffu, ds[e], o);
+      merge_stat(m[e], l[e], ds[e], m2, l2, d2);
+    }
+  }
+  // ... and over the two token tiles
+  if (tt == 1 && g8 == 0) {
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int c = n8 * 8 + 2 * t4 + e;
+      mg[0][c] = m[e];
+      mg[1][c] = l[e];
+      mg[2][c] = ds[e];
+    }
+  }
+  __syncthreads();
+  if (nt > 0 && (!ok || abort_flag)) return;
+  if (tt == 0 && g8 == 0) {
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int c = n8 * 8 + 2 * t4 + e;
+      merge_stat(m[e], l[e], ds[e], mg[0][c], mg[1][c], mg[2][c]);
+      if (col_ok[e]) {
+        const size_t idx = static_cast<size_t>(r_c[e]) * p.H + gkv * G + c % G;
+        p.lse_out[idx] = l[e] > 0.f ? (m[e] + __log2f(l[e])) * 0.6931471805599453f : kNegInf;
+        p.delta_out[idx] = l[e] > 0.f ? ds[e] / l[e] : 0.f;
+      }
+    }
+  }
+}
+
 }  // namespace
 
 bool mla_mma_supported(const PagedParams& p) {
   return p.Dk == kLat && p.Dp == kPos && p.page_size == 16 && (p.G == 4 || p.G == 8 || p.G == 16 || p.G == 32);
+}
+
+cudaError_t launch_paged_mla_stats_mma(const PagedMlaMaps& m, const PagedParams& p, cudaStream_t s) {
+  if (p.Nq == 0 || p.S == 0) return cudaSuccess;
+  const int smem = S_BYTES + 1024;
+  cudaError_t e = cudaFuncSetAttribute(mla_stats_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  // an upper bound on the row tiles of all sequences; each CTA finds its own
+  const int RT2 = SBC / p.G;
+  dim3 grid(p.KVH, p.Nq / RT2 + p.S + 1, 1);
+  mla_stats_mma_kernel<<<grid, kThreads, smem, s>>>(m.q, m.qp, m.dy, m.k, m.kp, p);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_paged_mla_mma(const PagedMlaMaps& m, const PagedParams& p, cudaStream_t s) {

@@ -318,6 +318,10 @@ def sweep(args) -> int:
                                          heads=c.heads, kv_heads=c.kv_heads, page_size=c.page_size,
                                          causal=c.causal, outputs=outs, qp=dv["qp"], kp_pool=dv["kp"])
         ms, ms_min = timed(call, 20)
+        stats_call = lambda: bd.paged_row_stats(dv["q"], dv["k"], dv["v"], dv["dy"], table, meta, heads=c.heads,
+                                                kv_heads=c.kv_heads, page_size=c.page_size, causal=c.causal,
+                                                qp=dv["qp"], kp_pool=dv["kp"])
+        stats_ms, _ = timed(stats_call, 10)
         stable = all(torch.equal(a, b) for a, b in zip(first, call()))
         for _ in range(3):
             stable = stable and all(torch.equal(a, b) for a, b in zip(first, call()))
@@ -352,6 +356,7 @@ def sweep(args) -> int:
               "pct_of_bf16_peak": 100.0 * flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
               "algorithmic_gbs": alg_bytes / (ms * 1e-3) / 1e9,
               "pct_of_hbm_peak": 100.0 * alg_bytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+              "row_stats_ms": stats_ms,
               "max_err_rel": err, "tolerance": 2e-2, "bit_stable_5_runs": bool(stable),
               "oracle_s_sample": t_or, "oracle_sample": f"{len(pick)} of {c.num_seqs} sequences",
               "oracle_s_extrapolated": t_or * c.num_seqs / len(pick), "host_cores": cores,
