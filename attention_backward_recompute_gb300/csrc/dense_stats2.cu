@@ -20,10 +20,11 @@
 // are rescaled by 2^(m_old - m_new) when the maximum grows, which for two
 // scalars costs nothing: no output tile is accumulated or rescaled.
 //
-// Roles: warp 0 TMA producer, warp 1 MMA issuer (one thread), warps 2..17
-// four column groups of four warps, group g owning key columns [16g, 16g+16)
-// of every tile; the groups keep their own (m, l, dsum) per row and merge at
-// the end.
+// Tiles are 128 queries x 128 keys (N = 128 MMAs).  Roles: warp 0 TMA
+// producer, warp 1 MMA issuer (whole warp, elect.sync), warps 2..17 four
+// column groups of four warps, group g owning key columns [32g, 32g+32) of
+// every tile; the groups keep their own (m, l, dsum) per row and merge at the
+// end.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -36,33 +37,33 @@ using namespace sm103;
 
 namespace {
 
-constexpr int kStages = 4;
+constexpr int kStages = 2;
 
 template <int DP>
 struct Stats2Layout {
   static constexpr int NCH = DP / 64;
-  static constexpr int BQ = 128, BK = 64;
+  static constexpr int BQ = 128, BK = 128;
   static constexpr int QT = NCH * BQ * 128;  // Q or dY tile (128 rows)
-  static constexpr int KT = NCH * BK * 128;  // K or V tile (64 rows)
-  static constexpr int BIAS = BQ * 128;      // 128 query rows x 64 keys
+  static constexpr int KT = NCH * BK * 128;  // K or V tile (128 rows)
+  static constexpr int BIAS = 2 * BQ * 128;  // two 64-key halves x 128 query rows
   static constexpr int K_OFF = 0;                        // kStages
   static constexpr int V_OFF = K_OFF + kStages * KT;     // kStages
   static constexpr int BIAS_OFF = V_OFF + kStages * KT;  // kStages
   // Q and dY are needed in shared memory only until they are staged into
-  // tensor memory: they occupy the K and V slots of stages 2 and 3, which the
+  // tensor memory: they occupy the K and V slots of stage 1, which the
   // producer fills only after that staging
-  static constexpr int Q_OFF = K_OFF + 2 * KT;
-  static constexpr int DY_OFF = V_OFF + 2 * KT;
-  static_assert(QT == 2 * KT && kStages >= 4, "Q / dY alias two ring slots");
+  static constexpr int Q_OFF = K_OFF + KT;
+  static constexpr int DY_OFF = V_OFF + KT;
+  static_assert(QT == KT, "Q / dY alias one ring slot");
   // per key column of a tile: sk = scale*log2(e), kb = log2(e), off = 0 for a
   // key the custom mask keeps; sk = kb = 0, off = mask_neg*log2(e) for a
-  // custom-masked key (so x = S*sk + bias*kb + off); then the 64-bit set of
+  // custom-masked key (so x = S*sk + bias*kb + off); then the 128-bit set of
   // custom-masked columns
   static constexpr int COL = 3 * BK * 4 + 16;
   static constexpr int COL_OFF = BIAS_OFF + kStages * BIAS;  // kStages
   static constexpr int BYTES = COL_OFF + kStages * COL;
-  // TMEM: S[2] [0, 128), dP[2] [128, 256), Q and dY rows as bf16 pairs after
-  static constexpr int T_S = 0, T_DP = 128, T_QA = 256, T_DYA = 256 + DP / 2;
+  // TMEM: S[2] [0, 256), dP [256, 384), Q and dY rows as bf16 pairs after
+  static constexpr int T_S = 0, T_DP = 256, T_QA = 384, T_DYA = 384 + DP / 2;
   static constexpr int TMEM_COLS = 512;
   static_assert(T_DYA + DP / 2 <= TMEM_COLS, "tensor memory budget");
 };
@@ -92,8 +93,7 @@ __global__ void __launch_bounds__(576, 1)
   using L = Stats2Layout<DP>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t bar_qdy, bar_a_ready, bar_full[kStages], bar_empty[kStages], bar_dp_full[2],
-      bar_used[2];
+  __shared__ uint64_t bar_qdy, bar_a_ready, bar_full[kStages], bar_empty[kStages], bar_dp_full, bar_used[2];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
   __shared__ float mg_m[kGroups - 1][128], mg_l[kGroups - 1][128], mg_d[kGroups - 1][128];
@@ -116,13 +116,11 @@ __global__ void __launch_bounds__(576, 1)
     mbar_init(&bar_qdy, 1);
     mbar_init(&bar_a_ready, 8);  // warps 2..9: Q and dY rows staged in tensor memory
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&bar_full[s], 2);        // TMA bytes + key-column constants written
-      mbar_init(&bar_empty[s], 1 + 4 * kGroups);  // MMAs of the tile done + bias read by warps 2..17
+      mbar_init(&bar_full[s], 2);                 // TMA bytes + key-column constants written
+      mbar_init(&bar_empty[s], 1 + 4 * kGroups);  // MMAs of the tile done + stage read by warps 2..17
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&bar_dp_full[s], 1);  // S(t) and dP(t) done
-      mbar_init(&bar_used[s], 4 * kGroups);  // S and dP buffer read by warps 2..17
-    }
+    mbar_init(&bar_dp_full, 1);  // S(t) and dP(t) done
+    for (int s = 0; s < 2; ++s) mbar_init(&bar_used[s], 4 * kGroups);  // S(t), dP(t) read, t = s mod 2
     mbar_fence_init();
   }
   if (warp == 1) {
@@ -148,13 +146,13 @@ __global__ void __launch_bounds__(576, 1)
         tma_load_4d(sm + L::DY_OFF + c * (L::BQ * 128), &tm_dy, &bar_qdy, c * 64, q0, h, b);
       }
     }
-    // custom-mask values of keys lane and lane + 32 of a tile, one tile ahead
+    // custom-mask values of keys lane + 32 i of a tile, one tile ahead
     const float* km = p.has_key_mask ? p.key_mask + static_cast<size_t>(b) * p.Sk : nullptr;
-    float kmv[2] = {0.f, 0.f};
+    float kmv[4] = {0.f, 0.f, 0.f, 0.f};
     auto km_load = [&](int t) {
       const int kk0 = (j_lo + t) * L::BK;
 #pragma unroll
-      for (int i = 0; i < 2; ++i) {
+      for (int i = 0; i < 4; ++i) {
         const int key = kk0 + lane + 32 * i;
         kmv[i] = key < p.Sk ? km[key] : 1.f;
       }
@@ -166,7 +164,7 @@ __global__ void __launch_bounds__(576, 1)
     for (int t = 0; t < n && ok; ++t) {
       const int s = t % kStages;
       if (t >= kStages) ok = mbar_wait_warp(&bar_empty[s], ((t / kStages) - 1) & 1, ab);
-      if (t == 2 && ok) ok = mbar_wait_warp(&bar_a_ready, 0, ab);  // Q, dY slots free
+      if (t == 1 && ok) ok = mbar_wait_warp(&bar_a_ready, 0, ab);  // Q, dY slots free
       if (!ok) break;
       const int kk0 = (j_lo + t) * L::BK;
       if (lane == 0) {
@@ -175,13 +173,17 @@ __global__ void __launch_bounds__(576, 1)
           tma_load_4d(sm + L::K_OFF + s * L::KT + c * (L::BK * 128), &tm_k, &bar_full[s], c * 64, kk0, h, b);
           tma_load_4d(sm + L::V_OFF + s * L::KT + c * (L::BK * 128), &tm_v, &bar_full[s], c * 64, kk0, h, b);
         }
-        if (HAS_BIAS) tma_load_4d(sm + L::BIAS_OFF + s * L::BIAS, &tm_bias, &bar_full[s], kk0, q0, h, b);
+        if (HAS_BIAS) {
+          uint8_t* bs = sm + L::BIAS_OFF + s * L::BIAS;
+          tma_load_4d(bs, &tm_bias, &bar_full[s], kk0, q0, h, b);
+          tma_load_4d(bs + L::BQ * 128, &tm_bias, &bar_full[s], kk0 + 64, q0, h, b);
+        }
       }
       if (p.has_key_mask) {
         float* col = reinterpret_cast<float*>(sm + L::COL_OFF + s * L::COL);
         uint32_t* bits = reinterpret_cast<uint32_t*>(col + 3 * L::BK);
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < 4; ++i) {
           const bool masked = kmv[i] < p.mask_thr;
           col[lane + 32 * i] = masked ? 0.f : p.scale_log2;
           col[L::BK + lane + 32 * i] = masked ? 0.f : kLog2e;
@@ -205,11 +207,11 @@ __global__ void __launch_bounds__(576, 1)
     // ------------------------------------------------------------ MMA issuer
     // the whole warp runs this role (warp-uniform); elected lanes issue
     {
-      constexpr uint32_t id_s = idesc_bf16(128, 64, false, false);
+      constexpr uint32_t id_s = idesc_bf16(128, 128, false, false);
       // descriptors built once; k-slices and stages are constant offsets
       const uint64_t dK0 = sdesc_sw128(smem_addr(sm + L::K_OFF), 16, 1024);
       const uint64_t dV0 = sdesc_sw128(smem_addr(sm + L::V_OFF), 16, 1024);
-      // D[128 x 64] = A[128 x DP] (tensor memory, bf16 pairs) * B[64 x DP]^T (shared memory, K-major)
+      // D[128 x 128] = A[128 x DP] (tensor memory, bf16 pairs) * B[128 x DP]^T (shared memory, K-major)
       auto issue_xt = [&](uint32_t d, uint32_t a_tmem, uint64_t bk) {
         mma_ts_w<false>(d, a_tmem, bk, id_s);
 #pragma unroll
@@ -218,27 +220,29 @@ __global__ void __launch_bounds__(576, 1)
           mma_ts_w<true>(d, a_tmem + kk * 8, sdesc_add(bk, c * (L::BK * 128) + o), id_s);
         }
       };
-      auto issue_tile = [&](int t) {  // S(t), dP(t) into buffers t % 2; frees stage t % 3 when done
-        const int s = t % kStages, bb = t & 1;
-        issue_xt(tmem + L::T_S + bb * 64, tmem + L::T_QA, sdesc_add(dK0, s * L::KT));
-        issue_xt(tmem + L::T_DP + bb * 64, tmem + L::T_DYA, sdesc_add(dV0, s * L::KT));
-        mma_commit_w(&bar_dp_full[bb]);
-        mma_commit_w(&bar_empty[s]);
-      };
       bool ok = mbar_wait_warp(&bar_a_ready, 0, ab);
       tc_fence_after();
+      // S(t) may go as soon as its buffer's previous tile (t - 2) was read;
+      // dP(t) (single buffer) once tile t - 1 was read.  Each of the two
+      // barriers is awaited at most one phase behind its current one.
       for (int t = 0; t < n && ok; ++t) {
-        if (t >= 2 && !(ok = mbar_wait_warp(&bar_used[t & 1], ((t - 2) >> 1) & 1, ab))) break;
-        if (!(ok = mbar_wait_warp(&bar_full[t % kStages], (t / kStages) & 1, ab))) break;
+        const int s = t % kStages, bb = t & 1;
+        if (!(ok = mbar_wait_warp(&bar_full[s], (t / kStages) & 1, ab))) break;
+        if (t >= 2 && !(ok = mbar_wait_warp(&bar_used[bb], ((t - 2) >> 1) & 1, ab))) break;
         tc_fence_after();
-        issue_tile(t);
+        issue_xt(tmem + L::T_S + bb * 128, tmem + L::T_QA, sdesc_add(dK0, s * L::KT));
+        if (t >= 1 && !(ok = mbar_wait_warp(&bar_used[bb ^ 1], ((t - 1) >> 1) & 1, ab))) break;
+        tc_fence_after();
+        issue_xt(tmem + L::T_DP, tmem + L::T_DYA, sdesc_add(dV0, s * L::KT));
+        mma_commit_w(&bar_dp_full);
+        mma_commit_w(&bar_empty[s]);
       }
       // the last commits of each stage arrive before the CTA leaves
       for (int t = imax(0, n - kStages); t < n; ++t) drain_wait(&bar_empty[t % kStages], (t / kStages) & 1);
     }
     __syncwarp();
   } else if (warp >= 2) {
-    const int g = (warp - 2) >> 2;  // column group: key columns [16g, 16g + 16) of every tile
+    const int g = (warp - 2) >> 2;  // column group: key columns [32g, 32g + 32) of every tile
     const int lg = warp & 3;
     const int row = lg * 32 + lane;  // query row inside the tile == TMEM lane
     const int q = q0 + row;
@@ -283,20 +287,18 @@ __global__ void __launch_bounds__(576, 1)
       const int s = t % kStages, bb = t & 1;
       const int kk0 = (j_lo + t) * L::BK;
       if (!(ok = mbar_wait_warp(&bar_full[s], (t / kStages) & 1, ab))) break;
-      // bias and custom-mask terms of the group's 16 columns while the tensor
-      // core works: x = bias*kb + off, S*sk added below
-      const float* col = reinterpret_cast<const float*>(sm + L::COL_OFF + s * L::COL) + 16 * g;
-      const uint32_t kbits =
-          p.has_key_mask
-              ? (reinterpret_cast<const uint32_t*>(col - 16 * g + 3 * L::BK)[g >> 1] >> (16 * (g & 1))) & 0xffffu
-              : 0u;
-      const uint8_t* brow = sm + L::BIAS_OFF + s * L::BIAS + row * 128;
-      float x[16], skv[16];
+      // bias and custom-mask terms of the group's 32 columns while the tensor
+      // core works: x = bias*kb + off (S*sk added once S is in)
+      const float* col = reinterpret_cast<const float*>(sm + L::COL_OFF + s * L::COL) + 32 * g;
+      const uint32_t kbits = p.has_key_mask ? reinterpret_cast<const uint32_t*>(col - 32 * g + 3 * L::BK)[g] : 0u;
+      // bias half (64 keys) g >> 1, 16-byte chunks 4 (g & 1) .. + 3 of this row
+      const uint8_t* brow = sm + L::BIAS_OFF + s * L::BIAS + (g >> 1) * (L::BQ * 128) + row * 128;
+      float x[32];
 #pragma unroll
-      for (int jj = 0; jj < 2; ++jj) {  // 8 keys per 16-byte bias chunk
+      for (int jj = 0; jj < 4; ++jj) {  // 8 keys per 16-byte bias chunk
         float bv[8];
         if (HAS_BIAS) {
-          const uint4 w4 = *reinterpret_cast<const uint4*>(brow + (((2 * g + jj) ^ (row & 7)) << 4));
+          const uint4 w4 = *reinterpret_cast<const uint4*>(brow + (((4 * (g & 1) + jj) ^ (row & 7)) << 4));
           const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -308,59 +310,64 @@ __global__ void __launch_bounds__(576, 1)
 #pragma unroll
           for (int h4 = 0; h4 < 2; ++h4) {
             const int c = 8 * jj + 4 * h4;
-            const float4 sk4 = *reinterpret_cast<const float4*>(col + c);
             const float4 kb4 = *reinterpret_cast<const float4*>(col + L::BK + c);
             const float4 of4 = *reinterpret_cast<const float4*>(col + 2 * L::BK + c);
             const float kbv[4] = {kb4.x, kb4.y, kb4.z, kb4.w}, ofv[4] = {of4.x, of4.y, of4.z, of4.w};
-            skv[c] = sk4.x;
-            skv[c + 1] = sk4.y;
-            skv[c + 2] = sk4.z;
-            skv[c + 3] = sk4.w;
 #pragma unroll
             for (int e = 0; e < 4; ++e) x[c + e] = HAS_BIAS ? fmaf(bv[4 * h4 + e], kbv[e], ofv[e]) : ofv[e];
           }
         } else {
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            x[8 * jj + e] = HAS_BIAS ? bv[e] * kLog2e : 0.f;
-            skv[8 * jj + e] = p.scale_log2;
-          }
+          for (int e = 0; e < 8; ++e) x[8 * jj + e] = HAS_BIAS ? bv[e] * kLog2e : 0.f;
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar_empty[s]);  // bias and column constants read
       // the dP commit follows the S MMAs of the tile, so it covers both
-      if (!(ok = mbar_wait_warp(&bar_dp_full[bb], (t >> 1) & 1, ab))) break;
+      if (!(ok = mbar_wait_warp(&bar_dp_full, t & 1, ab))) break;
       tc_fence_after();
-      uint32_t sr[16], dr[16];
-      tmem_ld16(tmem + L::T_S + bb * 64 + 16 * g + lane_addr, sr);
-      tmem_ld16(tmem + L::T_DP + bb * 64 + 16 * g + lane_addr, dr);
+      {
+        uint32_t sr[32];
+        tmem_ld32(tmem + L::T_S + bb * 128 + 32 * g + lane_addr, sr);
+        tmem_ld_wait();
+        if (p.has_key_mask) {
+#pragma unroll
+          for (int c4 = 0; c4 < 8; ++c4) {
+            const float4 sk4 = *reinterpret_cast<const float4*>(col + 4 * c4);
+            const float skv[4] = {sk4.x, sk4.y, sk4.z, sk4.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) x[4 * c4 + e] = fmaf(__uint_as_float(sr[4 * c4 + e]), skv[e], x[4 * c4 + e]);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) x[c] = fmaf(__uint_as_float(sr[c]), p.scale_log2, x[c]);
+        }
+      }
+      uint32_t dr[32];
+      tmem_ld32(tmem + L::T_DP + 32 * g + lane_addr, dr);
       tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bar_used[bb]);
+      if (lane == 0) {
+        mbar_arrive(&bar_used[bb]);
+        mbar_arrive(&bar_empty[s]);  // bias and column constants read
+      }
       const bool full = tile_fully_visible(p, q0, q0 + L::BQ - 1, kk0, kk0 + L::BK - 1);
-      // visible columns of this row among the group's 16: [lo, hi]
-      uint32_t vb = 0xffffu;
+      // visible columns of this row among the group's 32: [lo, hi]
+      uint32_t vb = 0xffffffffu;
       if (!full) {
-        const int lo = ka - kk0 - 16 * g, hi = kb - kk0 - 16 * g;
+        const int lo = ka - kk0 - 32 * g, hi = kb - kk0 - 32 * g;
         vb = 0u;
-        if (lo <= 15 && hi >= 0 && lo <= hi) {
-          const uint32_t up = hi >= 15 ? 0xffffu : ((1u << (hi + 1)) - 1u);
-          const uint32_t dn = lo <= 0 ? 0xffffu : (0xffffu & ~((1u << lo) - 1u));
+        if (lo <= 31 && hi >= 0 && lo <= hi) {
+          const uint32_t up = hi >= 31 ? 0xffffffffu : ((1u << (hi + 1)) - 1u);
+          const uint32_t dn = lo <= 0 ? 0xffffffffu : ~((1u << lo) - 1u);
           vb = up & dn;
         }
+#pragma unroll
+        for (int c = 0; c < 32; ++c) x[c] = ((vb >> c) & 1u) ? x[c] : -kInf;
       }
       any_unmasked |= (vb & ~kbits) != 0u;
-#pragma unroll
-      for (int c = 0; c < 16; ++c) x[c] = fmaf(__uint_as_float(sr[c]), skv[c], x[c]);
-      if (!full) {
-#pragma unroll
-        for (int c = 0; c < 16; ++c) x[c] = ((vb >> c) & 1u) ? x[c] : -kInf;
-      }
       float mt = -kInf;
 #pragma unroll
-      for (int c = 0; c < 16; ++c) mt = fmaxf(mt, x[c]);
+      for (int c = 0; c < 32; ++c) mt = fmaxf(mt, x[c]);
       if (mt > m2 + kRescaleThreshold || (m2 == -kInf && mt > -kInf)) {
         if (m2 > -kInf) {
           const float alpha = ex2_approx(m2 - mt);
@@ -372,7 +379,7 @@ __global__ void __launch_bounds__(576, 1)
       if (m2 > -kInf) {
         float ls = 0.f, ds = 0.f;
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
+        for (int c = 0; c < 32; ++c) {
           const float e = ex2_approx(x[c] - m2);
           ls += e;
           ds = fmaf(e, __uint_as_float(dr[c]), ds);
@@ -437,7 +444,7 @@ cudaError_t launch_t(const DenseMaps& m, const DenseParams& p, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(p.B * p.H, cdiv(p.Sq, L::BQ));
-  kern<<<grid, 576, smem, s>>>(m.q128, m.k64, m.v64, m.dy128, m.bias128, p);
+  kern<<<grid, 576, smem, s>>>(m.q128, m.k128, m.v128, m.dy128, m.bias128, p);
   return cudaGetLastError();
 }
 
