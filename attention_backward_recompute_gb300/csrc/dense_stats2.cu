@@ -1,7 +1,7 @@
 // Row-statistics prologue of the dense backward, bf16 storage, self-contained
 // mode (no O or LSE from the caller).
 //
-// One CTA per (batch*head, 128-query tile) sweeps the visible 64-key tiles.
+// One CTA per (batch*head, 128-query tile) sweeps the visible 128-key tiles.
 // The tensor core computes, per key tile j,
 //   S  = Q_i K_j^T      (A = Q_i held in tensor memory, B = K_j from a TMA ring)
 //   dP = dY_i V_j^T     (A = dY_i held in tensor memory, B = V_j)
@@ -19,6 +19,14 @@
 // rowsum(P dP))); the masks follow fn apply_synthetic_mask there.  Both sums
 // are rescaled by 2^(m_old - m_new) when the maximum grows, which for two
 // scalars costs nothing: no output tile is accumulated or rescaled.
+//
+// A custom-masked key enters through a per-tile bit set, not through its
+// score: its term 2^(mask_neg*log2(e) - m) underflows to exactly zero as soon
+// as the row has a visible unmasked key (whose x exceeds the masked value by
+// far more than 150), so such keys are left out of the sums; a row whose
+// visible keys are all custom-masked has equal x = mask_neg*log2(e) on every
+// one of them, so its statistics are the count of those keys and the plain
+// sum of their dP, kept on the side until an unmasked key shows up.
 //
 // Tiles are 128 queries x 128 keys (N = 128 MMAs).  Roles: warp 0 TMA
 // producer, warp 1 MMA issuer (whole warp, elect.sync), warps 2..17 four
@@ -55,11 +63,8 @@ struct Stats2Layout {
   static constexpr int Q_OFF = K_OFF + KT;
   static constexpr int DY_OFF = V_OFF + KT;
   static_assert(QT == KT, "Q / dY alias one ring slot");
-  // per key column of a tile: sk = scale*log2(e), kb = log2(e), off = 0 for a
-  // key the custom mask keeps; sk = kb = 0, off = mask_neg*log2(e) for a
-  // custom-masked key (so x = S*sk + bias*kb + off); then the 128-bit set of
-  // custom-masked columns
-  static constexpr int COL = 3 * BK * 4 + 16;
+  // the 128-bit set of the tile's custom-masked key columns
+  static constexpr int COL = 16;
   static constexpr int COL_OFF = BIAS_OFF + kStages * BIAS;  // kStages
   static constexpr int BYTES = COL_OFF + kStages * COL;
   // TMEM: S[2] [0, 256), dP [256, 384), Q and dY rows as bf16 pairs after
@@ -98,6 +103,7 @@ __global__ void __launch_bounds__(576, 1)
   __shared__ int abort_flag;
   __shared__ float mg_m[kGroups - 1][128], mg_l[kGroups - 1][128], mg_d[kGroups - 1][128];
   __shared__ int mg_any[kGroups - 1][128];
+  __shared__ float mg_c[kGroups - 1][128], mg_md[kGroups - 1][128];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bh = blockIdx.x;
@@ -180,15 +186,10 @@ __global__ void __launch_bounds__(576, 1)
         }
       }
       if (p.has_key_mask) {
-        float* col = reinterpret_cast<float*>(sm + L::COL_OFF + s * L::COL);
-        uint32_t* bits = reinterpret_cast<uint32_t*>(col + 3 * L::BK);
+        uint32_t* bits = reinterpret_cast<uint32_t*>(sm + L::COL_OFF + s * L::COL);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-          const bool masked = kmv[i] < p.mask_thr;
-          col[lane + 32 * i] = masked ? 0.f : p.scale_log2;
-          col[L::BK + lane + 32 * i] = masked ? 0.f : kLog2e;
-          col[2 * L::BK + lane + 32 * i] = masked ? p.masked_x2 : 0.f;
-          const uint32_t w = __ballot_sync(0xffffffffu, masked);
+          const uint32_t w = __ballot_sync(0xffffffffu, kmv[i] < p.mask_thr);
           if (lane == 0) bits[i] = w;
         }
         if (t + 1 < n) km_load(t + 1);
@@ -282,43 +283,28 @@ __global__ void __launch_bounds__(576, 1)
     if (p.causal) kb = imin(kb, q + p.q_off);
     if (q >= p.Sq) ka = 1 << 30, kb = -(1 << 30);
     float m2 = -kInf, l = 0.f, dsum = 0.f;
+    float mcnt = 0.f, mdsum = 0.f;  // visible custom-masked keys while no unmasked one is seen
     bool any_unmasked = false;
     for (int t = 0; t < n && ok; ++t) {
       const int s = t % kStages, bb = t & 1;
       const int kk0 = (j_lo + t) * L::BK;
       if (!(ok = mbar_wait_warp(&bar_full[s], (t / kStages) & 1, ab))) break;
-      // bias and custom-mask terms of the group's 32 columns while the tensor
-      // core works: x = bias*kb + off (S*sk added once S is in)
-      const float* col = reinterpret_cast<const float*>(sm + L::COL_OFF + s * L::COL) + 32 * g;
-      const uint32_t kbits = p.has_key_mask ? reinterpret_cast<const uint32_t*>(col - 32 * g + 3 * L::BK)[g] : 0u;
+      // bias term of the group's 32 columns while the tensor core works:
+      // x = bias*log2(e), as 16 packed pairs of adjacent columns
+      const uint32_t kbits =
+          p.has_key_mask ? reinterpret_cast<const uint32_t*>(sm + L::COL_OFF + s * L::COL)[g] : 0u;
       // bias half (64 keys) g >> 1, 16-byte chunks 4 (g & 1) .. + 3 of this row
       const uint8_t* brow = sm + L::BIAS_OFF + s * L::BIAS + (g >> 1) * (L::BQ * 128) + row * 128;
-      float x[32];
+      uint64_t x[16];
+      if (HAS_BIAS) {
+        const uint64_t l2e = f2_pack(kLog2e, kLog2e);
 #pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {  // 8 keys per 16-byte bias chunk
-        float bv[8];
-        if (HAS_BIAS) {
+        for (int jj = 0; jj < 4; ++jj) {  // 8 keys per 16-byte bias chunk
           const uint4 w4 = *reinterpret_cast<const uint4*>(brow + (((4 * (g & 1) + jj) ^ (row & 7)) << 4));
-          const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            bv[2 * e] = __uint_as_float(w[e] << 16);
-            bv[2 * e + 1] = __uint_as_float(w[e] & 0xffff0000u);
-          }
-        }
-        if (p.has_key_mask) {
-#pragma unroll
-          for (int h4 = 0; h4 < 2; ++h4) {
-            const int c = 8 * jj + 4 * h4;
-            const float4 kb4 = *reinterpret_cast<const float4*>(col + L::BK + c);
-            const float4 of4 = *reinterpret_cast<const float4*>(col + 2 * L::BK + c);
-            const float kbv[4] = {kb4.x, kb4.y, kb4.z, kb4.w}, ofv[4] = {of4.x, of4.y, of4.z, of4.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) x[c + e] = HAS_BIAS ? fmaf(bv[4 * h4 + e], kbv[e], ofv[e]) : ofv[e];
-          }
-        } else {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) x[8 * jj + e] = HAS_BIAS ? bv[e] * kLog2e : 0.f;
+          x[4 * jj] = f2_mul(f2_from_bf16x2(w4.x), l2e);
+          x[4 * jj + 1] = f2_mul(f2_from_bf16x2(w4.y), l2e);
+          x[4 * jj + 2] = f2_mul(f2_from_bf16x2(w4.z), l2e);
+          x[4 * jj + 3] = f2_mul(f2_from_bf16x2(w4.w), l2e);
         }
       }
       // the dP commit follows the S MMAs of the tile, so it covers both
@@ -328,19 +314,13 @@ __global__ void __launch_bounds__(576, 1)
         uint32_t sr[32];
         tmem_ld32(tmem + L::T_S + bb * 128 + 32 * g + lane_addr, sr);
         tmem_ld_wait();
-        if (p.has_key_mask) {
+        const uint64_t sl2 = f2_pack(p.scale_log2, p.scale_log2);
 #pragma unroll
-          for (int c4 = 0; c4 < 8; ++c4) {
-            const float4 sk4 = *reinterpret_cast<const float4*>(col + 4 * c4);
-            const float skv[4] = {sk4.x, sk4.y, sk4.z, sk4.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) x[4 * c4 + e] = fmaf(__uint_as_float(sr[4 * c4 + e]), skv[e], x[4 * c4 + e]);
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < 32; ++c) x[c] = fmaf(__uint_as_float(sr[c]), p.scale_log2, x[c]);
-        }
+        for (int i = 0; i < 16; ++i)
+          x[i] = HAS_BIAS ? f2_fma(f2_pack_u(sr[2 * i], sr[2 * i + 1]), sl2, x[i])
+                          : f2_mul(f2_pack_u(sr[2 * i], sr[2 * i + 1]), sl2);
       }
+      // dP of the same columns; then both buffers go back to the tensor core
       uint32_t dr[32];
       tmem_ld32(tmem + L::T_DP + 32 * g + lane_addr, dr);
       tmem_ld_wait();
@@ -348,7 +328,7 @@ __global__ void __launch_bounds__(576, 1)
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&bar_used[bb]);
-        mbar_arrive(&bar_empty[s]);  // bias and column constants read
+        mbar_arrive(&bar_empty[s]);  // bias and mask bits read
       }
       const bool full = tile_fully_visible(p, q0, q0 + L::BQ - 1, kk0, kk0 + L::BK - 1);
       // visible columns of this row among the group's 32: [lo, hi]
@@ -361,13 +341,27 @@ __global__ void __launch_bounds__(576, 1)
           const uint32_t dn = lo <= 0 ? 0xffffffffu : ~((1u << lo) - 1u);
           vb = up & dn;
         }
-#pragma unroll
-        for (int c = 0; c < 32; ++c) x[c] = ((vb >> c) & 1u) ? x[c] : -kInf;
       }
-      any_unmasked |= (vb & ~kbits) != 0u;
+      // visible and not custom-masked
+      const uint32_t vis = vb & ~kbits;
+      if (vis != 0xffffffffu) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          float a0, a1;
+          f2_split(x[i], a0, a1);
+          a0 = ((vis >> (2 * i)) & 1u) ? a0 : -kInf;
+          a1 = ((vis >> (2 * i + 1)) & 1u) ? a1 : -kInf;
+          x[i] = f2_pack(a0, a1);
+        }
+      }
+      any_unmasked |= vis != 0u;
       float mt = -kInf;
 #pragma unroll
-      for (int c = 0; c < 32; ++c) mt = fmaxf(mt, x[c]);
+      for (int i = 0; i < 16; ++i) {
+        float a0, a1;
+        f2_split(x[i], a0, a1);
+        mt = fmax3(mt, a0, a1);
+      }
       if (mt > m2 + kRescaleThreshold || (m2 == -kInf && mt > -kInf)) {
         if (m2 > -kInf) {
           const float alpha = ex2_approx(m2 - mt);
@@ -377,15 +371,30 @@ __global__ void __launch_bounds__(576, 1)
         m2 = mt;
       }
       if (m2 > -kInf) {
-        float ls = 0.f, ds = 0.f;
+        const uint64_t negm = f2_pack(-m2, -m2);
+        uint64_t ls = 0ull, ds = 0ull;
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const float e = ex2_approx(x[c] - m2);
-          ls += e;
-          ds = fmaf(e, __uint_as_float(dr[c]), ds);
+        for (int i = 0; i < 16; ++i) {
+          float d0, d1;
+          f2_split(f2_add(x[i], negm), d0, d1);
+          const uint64_t e = f2_pack(ex2_approx(d0), ex2_approx(d1));
+          ls = f2_add(ls, e);
+          ds = f2_fma(e, f2_pack_u(dr[2 * i], dr[2 * i + 1]), ds);
         }
-        l += ls;
-        dsum += ds;
+        float l0, l1, d0, d1;
+        f2_split(ls, l0, l1);
+        f2_split(ds, d0, d1);
+        l += l0 + l1;
+        dsum += d0 + d1;
+      } else {
+        // no visible unmasked key so far: the row's terms are those of its
+        // visible custom-masked keys, each with weight 2^0
+        const uint32_t mv = vb & kbits;
+        if (mv != 0u) {
+          mcnt += static_cast<float>(__popc(mv));
+#pragma unroll
+          for (int c = 0; c < 32; ++c) mdsum += ((mv >> c) & 1u) ? __uint_as_float(dr[c]) : 0.f;
+        }
       }
     }
     // merge the four column groups: (m, l, dsum) -> (max m, rescaled sums)
@@ -394,6 +403,8 @@ __global__ void __launch_bounds__(576, 1)
       mg_l[g - 1][row] = l;
       mg_d[g - 1][row] = dsum;
       mg_any[g - 1][row] = any_unmasked ? 1 : 0;
+      mg_c[g - 1][row] = mcnt;
+      mg_md[g - 1][row] = mdsum;
     }
     group_sync();
     if (g == 0 && (ok || n == 0) && q < p.Sq) {
@@ -415,6 +426,16 @@ __global__ void __launch_bounds__(576, 1)
           lt = fmaf(mg_l[i][row], ai, lt);
           dt = fmaf(mg_d[i][row], ai, dt);
         }
+      } else if (p.has_key_mask) {
+        // every visible key of the row is custom-masked: all carry the same x
+        lt = mcnt;
+        dt = mdsum;
+#pragma unroll
+        for (int i = 0; i < kGroups - 1; ++i) {
+          lt += mg_c[i][row];
+          dt += mg_md[i][row];
+        }
+        mm = p.masked_x2;
       }
       float L2 = kInf, dl = 0.f, pm = 0.f;
       if (lt > 0.f) {

@@ -137,12 +137,15 @@ def test_o_lse_supplied_mode(bd):
     assert_close(run_gpu(bd, c, o=o_t, lse=lse_t), oracle(c))
 
 
-def test_fully_custom_masked_rows(bd):
+@pytest.mark.parametrize("n_masked,bias", [(5, False), (40, True), (130, True)])
+def test_fully_custom_masked_rows(bd, n_masked, bias):
     """The first keys are custom-masked, so under the causal mask the first
-    rows see only masked keys: their softmax is uniform over the visible keys."""
+    rows see only masked keys: their softmax is uniform over the visible keys
+    (whatever the bias).  40 and 130 masked keys span several column groups
+    and a whole 128-key tile."""
     c = inputs.dense_inputs(batch=1, heads=2, seq_q=256, seq_k=256, head_dim=128, dtype="bf16", seed=41,
-                            scale=0.5, causal=True, key_mask_zero_frac=0.0)
-    c.key_mask[0, :5] = 0.0
+                            scale=0.5, causal=True, key_mask_zero_frac=0.0, bias=bias)
+    c.key_mask[0, :n_masked] = 0.0
     assert_close(run_gpu(bd, c), oracle(c))
 
 
