@@ -122,16 +122,19 @@ __device__ __forceinline__ void p_row(uint32_t tS, const float* st, const uint8_
   tmem_ld16(tS, s0);
   tmem_ld_wait();
   reg_fence16(s0);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    uint32_t(&cur)[16] = (i & 1) ? s1 : s0;
-    uint32_t(&nxt)[16] = (i & 1) ? s0 : s1;
-    if (i < 3) tmem_ld16(tS + 16 * (i + 1), nxt);
-    p_chunk<HAS_BIAS, CHECK>(cur, 16 * i, st, bias_s, kc, kb, scale_log2, lo, hi, kmasked, pw);
+#pragma unroll 1
+  for (int i = 0; i < 4; i += 2) {
+    tmem_ld16(tS + 16 * (i + 1), s1);
+    p_chunk<HAS_BIAS, CHECK>(s0, 16 * i, st, bias_s, kc, kb, scale_log2, lo, hi, kmasked, pw);
     tmem_st8(tS + 8 * i, pw);
-    if (i < 3) {
+    tmem_ld_wait();
+    reg_fence16(s1);
+    if (i + 2 < 4) tmem_ld16(tS + 16 * (i + 2), s0);
+    p_chunk<HAS_BIAS, CHECK>(s1, 16 * (i + 1), st, bias_s, kc, kb, scale_log2, lo, hi, kmasked, pw);
+    tmem_st8(tS + 8 * (i + 1), pw);
+    if (i + 2 < 4) {
       tmem_ld_wait();
-      reg_fence16(nxt);
+      reg_fence16(s0);
     }
   }
 }
