@@ -25,4 +25,4 @@ formulas: central finite differences of the loss, invariants, closed forms and
 brute force on tiny inputs.
 """
 from .dense import attn_bwd_dense, attn_fwd_dense, head_backward, visibility  # noqa: F401
-from .paged import attn_bwd_paged, paged_row_stats  # noqa: F401
+from .paged import attn_bwd_paged, paged_query_backward, paged_row_stats  # noqa: F401

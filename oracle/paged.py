@@ -11,6 +11,11 @@ over all (sequence, logical page) links that map to it, over the visible query
 rows and over the query heads of its group.  Slots that no valid token owns,
 and tail slots past a sequence's length, get zero.
 
+The query side (the "query kernel" the page names, which computes the row
+statistics once): dQ[r, h] = scale * sum_t dS_t k_t over the row's visible
+tokens, and for MLA dQp[r, h] = scale * sum_t dS_t kp_t; a row that belongs to
+no sequence, or sees no token, gets zero.
+
 MLA (``position_dim > 0``): the score is q.k_latent + qp.k_position; the latent
 is both key and value, so dK_latent = dS^T Q + P^T dY and dKp = dS^T Qp, with
 no separate dV.  Here this is the dense backward on Q' = [q | qp],
@@ -32,11 +37,12 @@ def _slots_of(page_table_row, length, page_size):
 
 def attn_bwd_paged(q, dy, k_pool, page_table, seq_len, q_start, q_pos, *, page_size, kv_heads,
                    v_pool=None, qp=None, kp_pool=None, causal=True, scale=None,
-                   return_stats=False):
+                   return_stats=False, return_dq=False):
     """q: [Nq, H, Dk]; dy: [Nq, H, Dv]; pools: [slots, kv_heads, dim].
 
     Returns float64 (dk_pool, dv_pool) for GQA or (dk_pool, dkp_pool) for MLA,
-    plus lse, delta [Nq, H] when ``return_stats``."""
+    plus lse, delta [Nq, H] when ``return_stats``, plus dq [Nq, H, Dk] (and
+    dqp [Nq, H, Dp] for MLA) when ``return_dq``."""
     q = np.asarray(q, dtype=np.float64)
     dy = np.asarray(dy, dtype=np.float64)
     Nq, H, Dk = q.shape
@@ -53,6 +59,8 @@ def attn_bwd_paged(q, dy, k_pool, page_table, seq_len, q_start, q_pos, *, page_s
         dv_pool = np.zeros((slots, kv_heads, v_pool.shape[2]))
     lse = np.full((Nq, H), -np.inf)
     delta = np.zeros((Nq, H))
+    dq = np.zeros((Nq, H, Dk))
+    dqp = np.zeros((Nq, H, qp.shape[2])) if mla else None
     for s in range(len(seq_len)):
         L = int(seq_len[s])
         r0, r1 = int(q_start[s]), int(q_start[s + 1])
@@ -71,16 +79,21 @@ def attn_bwd_paged(q, dy, k_pool, page_table, seq_len, q_start, q_pos, *, page_s
                 r = head_backward(Qc, Kc, K, dy[r0:r1, h], vis, scale)
                 np.add.at(dk_pool[:, g], sl, r["dk"][:, :Dk] + r["dv"])
                 np.add.at(dkp_pool[:, g], sl, r["dk"][:, Dk:])
+                dq[r0:r1, h] = r["dq"][:, :Dk]
+                dqp[r0:r1, h] = r["dq"][:, Dk:]
             else:
                 V = np.asarray(v_pool[sl, g], dtype=np.float64)
                 r = head_backward(q[r0:r1, h], K, V, dy[r0:r1, h], vis, scale)
                 np.add.at(dk_pool[:, g], sl, r["dk"])
                 np.add.at(dv_pool[:, g], sl, r["dv"])
+                dq[r0:r1, h] = r["dq"]
             lse[r0:r1, h] = r["lse"]
             delta[r0:r1, h] = r["delta"]
     out = (dk_pool, dkp_pool) if mla else (dk_pool, dv_pool)
     if return_stats:
-        return out + (lse, delta)
+        out = out + (lse, delta)
+    if return_dq:
+        out = out + ((dq, dqp) if mla else (dq,))
     return out
 
 
@@ -92,3 +105,14 @@ def paged_row_stats(q, dy, k_pool, page_table, seq_len, q_start, q_pos, *, page_
                        kv_heads=kv_heads, v_pool=v_pool, qp=qp, kp_pool=kp_pool, causal=causal,
                        scale=scale, return_stats=True)
     return r[-2], r[-1]
+
+
+def paged_query_backward(q, dy, k_pool, page_table, seq_len, q_start, q_pos, *, page_size, kv_heads,
+                         v_pool=None, qp=None, kp_pool=None, causal=True, scale=None):
+    """Query side of the paged backward, float64: (lse, delta, dq) for GQA or
+    (lse, delta, dq, dqp) for MLA; lse, delta [Nq, H], dq [Nq, H, Dk],
+    dqp [Nq, H, Dp]."""
+    r = attn_bwd_paged(q, dy, k_pool, page_table, seq_len, q_start, q_pos, page_size=page_size,
+                       kv_heads=kv_heads, v_pool=v_pool, qp=qp, kp_pool=kp_pool, causal=causal,
+                       scale=scale, return_stats=True, return_dq=True)
+    return r[2:]

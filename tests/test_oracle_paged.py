@@ -5,7 +5,9 @@
   explicit per-row loops), compared with the oracle's dense re-expansion;
 * finite differences of the loss with respect to the pool entries, for GQA and
   for MLA (where the latent is both key and value);
-* unowned and tail slots come out exactly zero.
+* unowned and tail slots come out exactly zero;
+* the query side (dQ, and dQp for MLA): per-(row, head) loops over the visible
+  tokens, and finite differences of the loss with respect to q and qp.
 """
 import math
 
@@ -13,7 +15,7 @@ import numpy as np
 import pytest
 
 from attention_backward_recompute_gb300 import inputs
-from oracle import attn_bwd_paged
+from oracle import attn_bwd_paged, paged_query_backward
 
 
 def tiny_case(mla=False, shared=0, seed=11, causal=True):
@@ -196,4 +198,86 @@ def test_paged_fd(mla):
                         checked += 1
             if s > 0:
                 break
+    assert checked > 0
+
+
+def brute_force_dq(c):
+    """dQ (and dQp) by loops over each row's visible tokens, with the row
+    statistics of the slot brute force."""
+    _, _, lse, delta = brute_force(c)
+    H, group = c.heads, c.heads // c.kv_heads
+    q = c.q.astype(np.float64)
+    dy = c.dy.astype(np.float64)
+    dq = np.zeros(q.shape)
+    dqp = None if c.qp is None else np.zeros(c.qp.shape)
+    for s in range(c.num_seqs):
+        for row in range(int(c.q_start[s]), int(c.q_start[s + 1])):
+            for h in range(H):
+                g = h // group
+                for t in range(int(c.seq_len[s])):
+                    if c.causal and t > int(c.q_pos[row]):
+                        continue
+                    slot = int(c.page_table[s, t // c.page_size]) * c.page_size + t % c.page_size
+                    k = c.k_pool[slot, g].astype(np.float64)
+                    a = float(q[row, h] @ k)
+                    if c.mla:
+                        a += float(c.qp[row, h].astype(np.float64) @ c.kp_pool[slot, g].astype(np.float64))
+                    p = math.exp(a * c.scale - lse[row, h])
+                    v = k if c.mla else c.v_pool[slot, g].astype(np.float64)
+                    ds = p * (float(dy[row, h] @ v) - delta[row, h]) * c.scale
+                    dq[row, h] += ds * k
+                    if c.mla:
+                        dqp[row, h] += ds * c.kp_pool[slot, g].astype(np.float64)
+    return dq, dqp, lse, delta
+
+
+def run_query_oracle(c):
+    return paged_query_backward(c.q, c.dy, c.k_pool, c.page_table, c.seq_len, c.q_start, c.q_pos,
+                                page_size=c.page_size, kv_heads=c.kv_heads, v_pool=c.v_pool, qp=c.qp,
+                                kp_pool=c.kp_pool, causal=c.causal)
+
+
+@pytest.mark.parametrize("mla", [False, True])
+@pytest.mark.parametrize("causal", [True, False])
+def test_paged_query_oracle_matches_brute_force(mla, causal):
+    c = tiny_case(mla=mla, shared=1, causal=causal)
+    got = run_query_oracle(c)
+    want_dq, want_dqp, want_lse, want_delta = brute_force_dq(c)
+    np.testing.assert_allclose(got[0], want_lse, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(got[1], want_delta, rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(got[2], want_dq, rtol=1e-10, atol=1e-12)
+    if mla:
+        np.testing.assert_allclose(got[3], want_dqp, rtol=1e-10, atol=1e-12)
+
+
+@pytest.mark.parametrize("mla", [False, True])
+def test_paged_query_fd(mla):
+    c = tiny_case(mla=mla, seed=17)
+    kpool = np.nan_to_num(c.k_pool.astype(np.float64))
+    vpool = None if c.v_pool is None else np.nan_to_num(c.v_pool.astype(np.float64))
+    kppool = None if c.kp_pool is None else np.nan_to_num(c.kp_pool.astype(np.float64))
+    c.q = c.q.astype(np.float64)
+    c.dy = c.dy.astype(np.float64)
+    if c.qp is not None:
+        c.qp = c.qp.astype(np.float64)
+    r = paged_query_backward(c.q, c.dy, kpool, c.page_table, c.seq_len, c.q_start, c.q_pos,
+                             page_size=c.page_size, kv_heads=c.kv_heads, v_pool=vpool, qp=c.qp,
+                             kp_pool=kppool, causal=c.causal)
+    f = lambda: _paged_loss(c, kpool, vpool, kppool)
+    h = 1e-6
+    checked = 0
+    targets = [(c.q, r[2])] + ([(c.qp, r[3])] if mla else [])
+    for x, grad in targets:
+        for row in (0, int(c.q_start[1]), c.num_queries - 1):
+            for hh in range(c.heads):
+                for d in range(x.shape[2]):
+                    old = x[row, hh, d]
+                    x[row, hh, d] = old + h
+                    fp = f()
+                    x[row, hh, d] = old - h
+                    fm = f()
+                    x[row, hh, d] = old
+                    num = (fp - fm) / (2 * h)
+                    assert abs(num - grad[row, hh, d]) <= 1e-6 * max(1.0, abs(num)), (row, hh, d)
+                    checked += 1
     assert checked > 0
