@@ -76,6 +76,8 @@ _SIG = {
                                         _P, _P, _P, ctypes.c_uint, _P, ctypes.c_size_t, _P]),
     "attn_paged_row_stats": (ctypes.c_int32, [ctypes.POINTER(attn_paged_desc), _P, _P, _P, _P, _P, _P, _P, _P,
                                               _P, _P, _P, ctypes.c_size_t, _P]),
+    "attn_bwd_paged_query": (ctypes.c_int32, [ctypes.POINTER(attn_paged_desc), _P, _P, _P, _P, _P, _P, _P, _P,
+                                              _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "attn_last_error": (ctypes.c_char_p, []),
     "attn_status_string": (ctypes.c_char_p, [ctypes.c_int32]),
     "attn_check_device_error": (ctypes.c_int32, [_P]),
@@ -154,6 +156,12 @@ def attn_paged_row_stats(desc, q, qp, k_pool, v_pool, kp_pool, dy, page_table, s
                          workspace_bytes, stream) -> int:
     return int(lib().attn_paged_row_stats(ctypes.byref(desc), q, qp, k_pool, v_pool, kp_pool, dy, page_table,
                                           seq_meta, lse, delta, workspace, workspace_bytes, stream))
+
+
+def attn_bwd_paged_query(desc, q, qp, k_pool, v_pool, kp_pool, dy, page_table, seq_meta, lse, delta, dq, dqp,
+                         workspace, workspace_bytes, stream) -> int:
+    return int(lib().attn_bwd_paged_query(ctypes.byref(desc), q, qp, k_pool, v_pool, kp_pool, dy, page_table,
+                                          seq_meta, lse, delta, dq, dqp, workspace, workspace_bytes, stream))
 
 
 def attn_check_device_error(stream) -> int:
@@ -307,6 +315,28 @@ def paged_row_stats(q, k_pool, v_pool, dy, page_table, seq_meta, *, heads, kv_he
                               workspace.numel(), _stream_handle(stream))
     _check(st)
     return lse, delta
+
+
+def paged_query_backward(q, k_pool, v_pool, dy, page_table, seq_meta, *, heads, kv_heads, page_size=16,
+                         causal=True, scale=0.0, outputs=None, workspace=None, stream=None):
+    """Query side (GQA): (lse, delta, dq) for CUDA tensors, lse/delta [Nq, H]
+    fp32 and dq shaped like q."""
+    import torch
+    d = _paged_desc_for(q, dy, k_pool, page_table, seq_meta, heads, kv_heads, page_size, causal, scale, None, None)
+    if outputs is None:
+        lse = torch.empty((q.shape[0], heads), dtype=torch.float32, device=q.device)
+        delta = torch.empty_like(lse)
+        dq = torch.empty_like(q)
+    else:
+        lse, delta, dq = outputs
+    n = attn_bwd_paged_workspace_bytes(d)
+    if workspace is None:
+        workspace = torch.empty(max(n, 256), dtype=torch.uint8, device=q.device)
+    st = attn_bwd_paged_query(d, _ptr(q), None, _ptr(k_pool), _ptr(v_pool), None, _ptr(dy), _ptr(page_table),
+                              _ptr(seq_meta), _ptr(lse), _ptr(delta), _ptr(dq), None, _ptr(workspace),
+                              workspace.numel(), _stream_handle(stream))
+    _check(st)
+    return lse, delta, dq
 
 
 def paged_backward(q, k_pool, v_pool, dy, page_table, seq_meta, lse, delta, *, heads, kv_heads, page_size=16,

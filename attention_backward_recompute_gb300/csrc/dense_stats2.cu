@@ -461,7 +461,7 @@ template <int DP, bool HAS_BIAS>
 cudaError_t launch_t(const DenseMaps& m, const DenseParams& p, cudaStream_t s) {
   using L = Stats2Layout<DP>;
   auto kern = stats2_kernel<DP, HAS_BIAS>;
-  const int smem = L::BYTES + 1024;
+  const int smem = max(L::BYTES + 1024, kSmemOneCtaPerSm);  // all 512 TMEM columns: one CTA per SM
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(p.B * p.H, cdiv(p.Sq, L::BQ));

@@ -321,4 +321,60 @@ ATTN_API attn_status_t attn_paged_row_stats(const attn_paged_desc* d, const void
   return api_ok();
 }
 
+ATTN_API attn_status_t attn_bwd_paged_query(const attn_paged_desc* d, const void* q, const void* qp,
+                                            const void* k_pool, const void* v_pool, const void* kp_pool,
+                                            const void* dy, const int32_t* page_table, const int32_t* seq_meta,
+                                            float* lse, float* delta, void* dq, void* dqp, void* workspace,
+                                            size_t workspace_bytes, void* stream) {
+  PagedSizes z;
+  attn_status_t st = check_paged_desc(d, &z);
+  if (st != ATTN_OK) return st;
+  const bool mla = d->position_dim > 0;
+  if (mla) return api_fail(ATTN_ERR_UNSUPPORTED, "the query side of MLA (dQ, dQp) is not built; GQA only");
+  (void)qp;
+  (void)kp_pool;
+  (void)dqp;
+  if (d->num_queries == 0) return api_ok();
+  if (!q || !dy || !lse || !delta || !dq || !seq_meta || (d->max_pages_per_seq > 0 && !page_table))
+    return api_fail(ATTN_ERR_INVALID_ARG, "a required pointer is NULL");
+  if (d->num_pages > 0 && (!k_pool || !v_pool)) return api_fail(ATTN_ERR_INVALID_ARG, "k_pool/v_pool is NULL");
+  const void* al[] = {q, k_pool, v_pool, dy, lse, delta, dq, page_table, seq_meta};
+  for (const void* x : al)
+    if (x && !al16(x)) return api_fail(ATTN_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  struct R { const void* p; size_t n; };
+  const R ins[] = {{q, z.q_bytes}, {k_pool, z.k_bytes}, {v_pool, z.v_bytes}, {dy, z.dy_bytes},
+                   {page_table, z.table_bytes}, {seq_meta, z.meta_bytes}, {workspace, workspace_bytes}};
+  const R outs[] = {{lse, z.stat_bytes}, {delta, z.stat_bytes}, {dq, z.q_bytes}};
+  for (const R& o : outs)
+    for (const R& r : ins)
+      if (overlap(o.p, o.n, r.p, r.n)) return api_fail(ATTN_ERR_ALIAS, "an output overlaps an input or the workspace");
+  for (int i = 0; i < 3; ++i)
+    for (int j = i + 1; j < 3; ++j)
+      if (overlap(outs[i].p, outs[i].n, outs[j].p, outs[j].n)) return api_fail(ATTN_ERR_ALIAS, "outputs overlap");
+  attn::PagedParams p;
+  if ((st = fill_params(d, z, page_table, seq_meta, workspace, &p)) != ATTN_OK) return st;
+  p.lse_out = lse;
+  p.delta_out = delta;
+  p.dq = dq;
+  attn::PagedMaps m;
+  std::memset(&m, 0, sizeof(m));
+  const uint64_t slots = uint64_t(d->num_pages) * d->page_size;
+  const uint32_t G = uint32_t(p.G);
+  bool enc = encode3d(&m.q_stats, q, d->key_dim, d->heads, d->num_queries, 64, G, 128 / G) &&
+             encode3d(&m.dy_stats, dy, d->value_dim, d->heads, d->num_queries, 64, G, 128 / G);
+  if (slots > 0)
+    enc = enc && encode3d(&m.k, k_pool, d->key_dim, d->kv_heads, slots, 64, 1, uint32_t(d->page_size)) &&
+          encode3d(&m.v, v_pool, d->value_dim, d->kv_heads, slots, 64, 1, uint32_t(d->page_size));
+  else
+    m.k = m.v = m.q_stats;
+  if (!enc) return api_fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  attn::timing_mark_begin(1, s);
+  cudaError_t e = attn::launch_paged_query(m, p, s);
+  attn::timing_mark(s);
+  attn::timing_mark_end();
+  if (e != cudaSuccess) return api_fail(ATTN_ERR_CUDA, "query-side launch failed: %s", cudaGetErrorString(e));
+  return api_ok();
+}
+
 }  // extern "C"

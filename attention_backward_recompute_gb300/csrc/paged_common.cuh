@@ -33,6 +33,8 @@ struct PagedParams {
   void* dk_pool;               // [slots, KVH, Dk]
   void* dv_pool;               // [slots, KVH, Dv]
   void* dkp_pool;              // [slots, KVH, Dp]
+  void* dq;                    // query side: [Nq, H, Dk]
+  void* dqp;                   // query side, MLA: [Nq, H, Dp]
   unsigned wrt;
   // workspace (link structure of the pool)
   int32_t* link_count;         // [num_pages]

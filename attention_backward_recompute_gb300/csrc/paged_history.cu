@@ -525,7 +525,7 @@ template <int DP>
 cudaError_t launch_hist_t(const PagedMaps& m, const PagedParams& p, cudaStream_t s) {
   using L = HistLayout<DP>;
   auto kern = paged_history_kernel<DP>;
-  const int smem = L::BYTES + 1024;
+  const int smem = max(L::BYTES + 1024, kSmemOneCtaPerSm);  // all 512 TMEM columns: one CTA per SM
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int nblk = (p.max_pages * p.page_size + 127) / 128;

@@ -20,6 +20,8 @@ cudaError_t launch_paged_prep(const PagedParams& p, cudaStream_t s);
 cudaError_t launch_paged_zero_unlinked(const PagedParams& p, cudaStream_t s);
 cudaError_t launch_paged_history(const PagedMaps& m, const PagedParams& p, cudaStream_t s);
 cudaError_t launch_paged_row_stats(const PagedMaps& m, const PagedParams& p, cudaStream_t s);
+// query side (GQA): row statistics and dQ in one kernel; q_stats/dy_stats maps
+cudaError_t launch_paged_query(const PagedMaps& m, const PagedParams& p, cudaStream_t s);
 // MLA (key_dim 512 latent + position_dim 64; the latent is also the value)
 cudaError_t launch_paged_mla_history(const PagedParams& p, const void* q, const void* qp, const void* dy,
                                      const void* k_pool, const void* kp_pool, cudaStream_t s);

@@ -159,6 +159,13 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 // ----------------------------------------------------------------------------
 // Allocate `ncols` (power of two, >= 32) tensor-memory columns; the base address
 // is written to `*dst_smem`.  Executed by one full warp.
+// A kernel that allocates all 512 tensor-memory columns must run one CTA per
+// SM: a second resident CTA blocks in tcgen05.alloc until the first frees its
+// columns, and the two can wait on each other.  Requesting at least this much
+// dynamic shared memory per CTA keeps two of them from sharing an SM (the SM
+// has 228 KiB).
+constexpr int kSmemOneCtaPerSm = 120 * 1024;
+
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(dst_smem)),
                "r"(ncols)

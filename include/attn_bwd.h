@@ -241,6 +241,29 @@ ATTN_API attn_status_t attn_paged_row_stats(const attn_paged_desc* d, const void
                                             float* lse, float* delta, void* workspace, size_t workspace_bytes,
                                             void* stream);
 
+/*
+ * Query side of the paged backward: the row statistics and the query
+ * gradient of every packed query row in one call.  ruDNN
+ * src/paged_attention/ordered_kernel.rs (history_backward) reads per (row,
+ * head) statistics "computed once by the query kernel"; this is that kernel,
+ * with dQ added.  Same arguments as attn_paged_row_stats, plus
+ *   dq [Nq, H, key_dim] (storage dtype): output,
+ *   dq[r, h] = scale * sum_t dS_rt k_t over the row's visible tokens t, with
+ *   dS = P (dP - delta) and P, dP, delta as in attn_bwd_paged;
+ *   dqp [Nq, H, position_dim] (MLA): output of the position part.
+ * lse and delta (fp32 [Nq, H]) are written as by attn_paged_row_stats.  Every
+ * row is written exactly once: a row with no visible token, or outside every
+ * sequence's query range, gets dq = 0, lse = -inf and delta = 0.  Tokens are
+ * visited in a fixed order, so the result is bit-identical from run to run.
+ * GQA only: MLA (position_dim > 0) returns ATTN_ERR_UNSUPPORTED.  The
+ * workspace is that of attn_bwd_paged (it may be NULL when its size is 0).
+ */
+ATTN_API attn_status_t attn_bwd_paged_query(const attn_paged_desc* d, const void* q, const void* qp,
+                                            const void* k_pool, const void* v_pool, const void* kp_pool,
+                                            const void* dy, const int32_t* page_table, const int32_t* seq_meta,
+                                            float* lse, float* delta, void* dq, void* dqp, void* workspace,
+                                            size_t workspace_bytes, void* stream);
+
 /* Reason for the last non-OK status on this host thread ("" if none). */
 ATTN_API const char* attn_last_error(void);
 
