@@ -21,13 +21,15 @@ import math
 import numpy as np
 
 
-def visibility(seq_q: int, seq_k: int, causal: bool, window: int | None) -> np.ndarray:
+def visibility(seq_q: int, seq_k: int, causal: bool, window: int | None, top_left: bool = False) -> np.ndarray:
     """Structurally visible (query, key) pairs, bottom-right aligned.
 
     rlx-cpu attention_bwd.rs, ``apply_synthetic_mask``: q_offset = Sk - Sq
     (saturating at 0), abs_q = q_offset + qi; causal excludes ki > abs_q; the
-    sliding window w excludes ki < abs_q - w (saturating) or ki > abs_q."""
-    q_off = max(seq_k - seq_q, 0)
+    sliding window w excludes ki < abs_q - w (saturating) or ki > abs_q.
+    ``top_left``: the alignment of rlx-wgpu attention_bwd.wgsl ``mask_score``
+    (causal hides ki > qi), i.e. q_offset = 0."""
+    q_off = 0 if top_left else max(seq_k - seq_q, 0)
     abs_q = q_off + np.arange(seq_q)[:, None]
     ki = np.arange(seq_k)[None, :]
     vis = np.ones((seq_q, seq_k), dtype=bool)
@@ -93,12 +95,13 @@ def _heads(x, layout):
 
 def attn_bwd_dense(q, k, v, dy, *, layout="bshd", causal=False, window=None, key_mask=None,
                    bias=None, mask_thr=0.5, mask_neg=-1e9, scale=None, heads_subset=None,
-                   return_stats=False):
+                   return_stats=False, top_left=False):
     """Full-tensor dense backward (rlx-cpu attention_bwd.rs, ``attention_backward_all``).
 
     q, dy: [B,Sq,H,D] ('bshd') or [B,H,Sq,D] ('bhsd'); k, v likewise with Sk.
     key_mask: [B, Sk] (masked where value < mask_thr); bias: [B, H, Sq, Sk].
     ``heads_subset``: optional list of (b, h) to evaluate (others stay zero).
+    ``top_left``: causal / window masks aligned top-left (see ``visibility``).
     Returns float64 dq, dk, dv in the input layout (and lse, delta [B,H,Sq]
     when ``return_stats``)."""
     qh, kh, vh, dyh = (_heads(np.asarray(x), layout) for x in (q, k, v, dy))
@@ -106,7 +109,7 @@ def attn_bwd_dense(q, k, v, dy, *, layout="bshd", causal=False, window=None, key
     Sk = kh.shape[2]
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    vis = visibility(Sq, Sk, causal, window)
+    vis = visibility(Sq, Sk, causal, window, top_left)
     dq = np.zeros((B, H, Sq, D))
     dk = np.zeros((B, H, Sk, D))
     dv = np.zeros((B, H, Sk, D))

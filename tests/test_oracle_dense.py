@@ -319,3 +319,47 @@ def test_forward_output_by_loops():
         assert abs(np.sum(dy * o) - loop_loss(q, k, v, dy, True, None, km, bias)) < 1e-12
     # lse: exp(lse) is the softmax normaliser, so sum_k exp(s - lse) = 1 per row
     assert np.all(np.isfinite(lse))
+
+
+# ---------------------------------------------------------------------------
+# top-left alignment (rlx-wgpu attention_bwd.wgsl, mask_score: causal hides
+# ki > qi): each row is plain attention over a key prefix
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("sq,sk", [(5, 9), (9, 5), (6, 6)])
+def test_top_left_causal_is_prefix_attention(sq, sk):
+    """With top-left causal alignment row q sees keys 0..min(q, Sk-1); its
+    gradients equal those of an unmasked single-row problem on that key
+    prefix, summed over rows for dK and dV."""
+    rng = np.random.default_rng(71)
+    D = 4
+    q, k, v, dy = (rng.standard_normal(s) for s in ((1, sq, 1, D), (1, sk, 1, D), (1, sk, 1, D), (1, sq, 1, D)))
+    dq, dk, dv = attn_bwd_dense(q, k, v, dy, causal=True, top_left=True)
+    want_dq = np.zeros_like(dq)
+    want_dk = np.zeros_like(dk)
+    want_dv = np.zeros_like(dv)
+    for qi in range(sq):
+        n = min(qi, sk - 1) + 1
+        r = attn_bwd_dense(q[:, qi:qi + 1], k[:, :n], v[:, :n], dy[:, qi:qi + 1], causal=False,
+                           scale=1.0 / math.sqrt(D))
+        want_dq[:, qi] = r[0][:, 0]
+        want_dk[:, :n] += r[1]
+        want_dv[:, :n] += r[2]
+    np.testing.assert_allclose(dq, want_dq, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(dk, want_dk, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(dv, want_dv, rtol=1e-12, atol=1e-12)
+    if sq < sk:  # differs from the bottom-right default there
+        assert not np.allclose(dq, attn_bwd_dense(q, k, v, dy, causal=True)[0])
+
+
+def test_top_left_window_is_band_attention():
+    """Top-left window w: row q sees keys max(q - w, 0)..q (a band of plain
+    attention over that key range)."""
+    rng = np.random.default_rng(72)
+    sq, sk, D, w = 7, 11, 4, 2
+    q, k, v, dy = (rng.standard_normal(s) for s in ((1, sq, 1, D), (1, sk, 1, D), (1, sk, 1, D), (1, sq, 1, D)))
+    dq = attn_bwd_dense(q, k, v, dy, window=w, top_left=True)[0]
+    for qi in range(sq):
+        lo, hi = max(qi - w, 0), qi + 1
+        r = attn_bwd_dense(q[:, qi:qi + 1], k[:, lo:hi], v[:, lo:hi], dy[:, qi:qi + 1], scale=1.0 / math.sqrt(D))
+        np.testing.assert_allclose(dq[:, qi], r[0][:, 0], rtol=1e-12, atol=1e-12)
