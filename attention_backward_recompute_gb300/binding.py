@@ -34,6 +34,7 @@ ATTN_MASK_CAUSAL = 1
 ATTN_MASK_WINDOW = 2
 ATTN_MASK_KEY = 4
 ATTN_MASK_BIAS = 8
+ATTN_MASK_TOP_LEFT = 16
 ATTN_WRT_DQ = 1
 ATTN_WRT_DK = 2
 ATTN_WRT_DV = 4
@@ -218,7 +219,7 @@ def _dtype_code(t):
 
 def make_dense_desc(*, batch, heads, seq_q, seq_k, head_dim, dtype=ATTN_DTYPE_BF16, layout=ATTN_LAYOUT_BSHD,
                     causal=False, window=None, key_mask=False, bias=False, mask_thr=0.5, mask_neg=-1e9,
-                    scale=0.0) -> attn_dense_desc:
+                    scale=0.0, top_left=False) -> attn_dense_desc:
     d = attn_dense_desc()
     attn_dense_desc_init(d)
     d.batch, d.heads, d.seq_q, d.seq_k, d.head_dim = batch, heads, seq_q, seq_k, head_dim
@@ -233,6 +234,8 @@ def make_dense_desc(*, batch, heads, seq_q, seq_k, head_dim, dtype=ATTN_DTYPE_BF
         flags |= ATTN_MASK_KEY
     if bias:
         flags |= ATTN_MASK_BIAS
+    if top_left:
+        flags |= ATTN_MASK_TOP_LEFT
     d.mask_flags = flags
     d.mask_thr, d.mask_neg, d.scale = mask_thr, mask_neg, scale
     return d
@@ -240,7 +243,7 @@ def make_dense_desc(*, batch, heads, seq_q, seq_k, head_dim, dtype=ATTN_DTYPE_BF
 
 def dense_backward(q, k, v, dy, *, layout="bshd", causal=False, window=None, key_mask=None, bias=None, o=None,
                    lse=None, wrt=ATTN_WRT_DQ | ATTN_WRT_DK | ATTN_WRT_DV, scale=0.0, mask_thr=0.5, mask_neg=-1e9,
-                   outputs=None, workspace=None, stream=None):
+                   outputs=None, workspace=None, stream=None, top_left=False):
     """dQ, dK, dV for CUDA tensors q, k, v, dy ([B,S,H,D] or [B,H,S,D]).
 
     Returns (dq, dk, dv) with None for gradients not selected in ``wrt``."""
@@ -254,7 +257,7 @@ def dense_backward(q, k, v, dy, *, layout="bshd", causal=False, window=None, key
         Sk = k.shape[2]
     desc = make_dense_desc(batch=B, heads=H, seq_q=Sq, seq_k=Sk, head_dim=D, dtype=_dtype_code(q), layout=lay,
                            causal=causal, window=window, key_mask=key_mask is not None, bias=bias is not None,
-                           mask_thr=mask_thr, mask_neg=mask_neg, scale=scale)
+                           mask_thr=mask_thr, mask_neg=mask_neg, scale=scale, top_left=top_left)
     if outputs is None:
         dq = torch.empty_like(q) if wrt & ATTN_WRT_DQ else None
         dk = torch.empty_like(k) if wrt & ATTN_WRT_DK else None

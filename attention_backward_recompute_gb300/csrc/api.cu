@@ -154,7 +154,7 @@ attn_status_t check_dense_desc(const attn_dense_desc* d, DenseSizes* z) {
     return api_fail(ATTN_ERR_INVALID_ARG, "unknown dtype %d", d->dtype);
   if (d->layout != ATTN_LAYOUT_BSHD && d->layout != ATTN_LAYOUT_BHSD)
     return api_fail(ATTN_ERR_INVALID_ARG, "unknown layout %d", d->layout);
-  if (d->mask_flags & ~15u) return api_fail(ATTN_ERR_INVALID_ARG, "unknown mask flag bits 0x%x", d->mask_flags);
+  if (d->mask_flags & ~31u) return api_fail(ATTN_ERR_INVALID_ARG, "unknown mask flag bits 0x%x", d->mask_flags);
   if ((d->mask_flags & ATTN_MASK_WINDOW) && d->window < 0) return api_fail(ATTN_ERR_INVALID_ARG, "window < 0");
   if (d->reserved != 0) return api_fail(ATTN_ERR_INVALID_ARG, "reserved field must be 0");
   if (!std::isfinite(d->mask_neg) || !(d->mask_neg < 0.f)) return api_fail(ATTN_ERR_INVALID_ARG, "mask_neg must be finite and < 0");
@@ -258,7 +258,7 @@ ATTN_API attn_status_t attn_bwd_dense(const attn_dense_desc* d, const void* q, c
 
   attn::DenseParams p{};
   p.B = int(B); p.H = int(H); p.Sq = int(Sq); p.Sk = int(Sk); p.D = int(D);
-  p.q_off = Sk > Sq ? int(Sk - Sq) : 0;
+  p.q_off = (Sk > Sq && !(d->mask_flags & ATTN_MASK_TOP_LEFT)) ? int(Sk - Sq) : 0;
   p.causal = (d->mask_flags & (ATTN_MASK_CAUSAL | ATTN_MASK_WINDOW)) ? 1 : 0;
   p.window = (d->mask_flags & ATTN_MASK_WINDOW) ? d->window : -1;
   p.has_key_mask = has_km ? 1 : 0;

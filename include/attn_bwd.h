@@ -10,7 +10,8 @@
  *   S   = scale * Q K^T                                    [Sq, Sk]
  *   S  += bias[b,h]                          (ATTN_MASK_BIAS)
  *   S[:, k] = mask_neg where key_mask[b,k] < mask_thr      (ATTN_MASK_KEY)
- *   structural masks, bottom-right aligned, q_off = max(Sk - Sq, 0),
+ *   structural masks, bottom-right aligned, q_off = max(Sk - Sq, 0) (0 with
+ *   ATTN_MASK_TOP_LEFT),
  *   abs_q = q_off + q:   causal hides k > abs_q;  window w hides
  *   k < abs_q - w (saturating at 0) or k > abs_q.  Hidden entries get P = 0.
  *   P   = softmax over the visible keys of each row        (a row with no
@@ -76,6 +77,9 @@ typedef int32_t attn_status_t;
 #define ATTN_MASK_WINDOW 2u /* hide k < abs_q - window and k > abs_q */
 #define ATTN_MASK_KEY 4u    /* custom per-key mask key_mask[B, Sk] (fp32) */
 #define ATTN_MASK_BIAS 8u   /* additive bias[B, H, Sq, Sk] in the storage type */
+/* align the causal and window masks top-left instead: abs_q = q (q_off = 0),
+ * as rlx-wgpu attention_bwd.wgsl mask_score does (causal hides k > q) */
+#define ATTN_MASK_TOP_LEFT 16u
 
 /* Gradient selection (enum order of the pages: Query = 0, Key = 1, Value = 2). */
 #define ATTN_WRT_DQ 1u

@@ -192,3 +192,23 @@ def test_error_word_clear_after_normal_runs(bd):
     c = inputs.dense_inputs(batch=1, heads=1, seq_q=64, seq_k=64, head_dim=64, dtype="bf16", seed=3)
     run_gpu(bd, c)
     assert bd.attn_check_device_error(None) == bd.ATTN_OK
+
+
+@pytest.mark.parametrize("sq,sk,causal,window,dim", [(200, 456, True, None, 128), (330, 200, True, None, 128),
+                                                       (190, 296, False, 40, 64)])
+def test_top_left_alignment(bd, sq, sk, causal, window, dim):
+    """ATTN_MASK_TOP_LEFT: causal / window masks aligned top-left (row q sees
+    keys <= q); Sq < Sk leaves keys that no query sees, whose dK, dV are 0."""
+    from oracle import attn_bwd_dense
+    c = inputs.dense_inputs(batch=2, heads=2, seq_q=sq, seq_k=sk, head_dim=dim, dtype="bf16", seed=81,
+                            scale=0.5, causal=causal, window=window, key_mask_zero_frac=0.1, bias=True)
+    q, k, v, dy = (_dev(x) for x in (c.q, c.k, c.v, c.dy))
+    km = torch.from_numpy(c.key_mask).cuda()
+    res = bd.dense_backward(q, k, v, dy, layout=c.layout, causal=causal, window=window, key_mask=km,
+                            bias=_dev(c.bias), top_left=True)
+    bd.check_device_error()
+    ref = attn_bwd_dense(c.q, c.k, c.v, c.dy, layout=c.layout, causal=causal, window=window,
+                         key_mask=c.key_mask, bias=c.bias, top_left=True)
+    assert_close(res, ref)
+    if sq < sk and window is None:
+        assert torch.all(res[1][:, sq:] == 0) and torch.all(res[2][:, sq:] == 0)
