@@ -131,18 +131,18 @@ def attn_bwd_dense(q, k, v, dy, *, layout="bshd", causal=False, window=None, key
 
 
 def attn_fwd_dense(q, k, v, *, layout="bshd", causal=False, window=None, key_mask=None, bias=None,
-                   mask_thr=0.5, mask_neg=-1e9, scale=None):
+                   mask_thr=0.5, mask_neg=-1e9, scale=None, top_left=False):
     """Forward output O = P V and lse = log-sum-exp of the masked scores, float64.
 
     The probabilities are those of the backward (same masks, same softmax); a
     row with no visible key has O = 0 and lse = -inf.  Returns (o in the input
-    layout, lse [B, H, Sq])."""
+    layout, lse [B, H, Sq]).  ``top_left`` as for ``attn_bwd_dense``."""
     qh, kh, vh = (_heads(np.asarray(x), layout) for x in (q, k, v))
     B, H, Sq, D = qh.shape
     Sk = kh.shape[2]
     if scale is None:
         scale = 1.0 / math.sqrt(D)
-    vis = visibility(Sq, Sk, causal, window)
+    vis = visibility(Sq, Sk, causal, window, top_left)
     o = np.zeros((B, H, Sq, vh.shape[3]))
     lse = np.full((B, H, Sq), -np.inf)
     for b in range(B):
