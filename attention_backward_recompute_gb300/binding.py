@@ -72,6 +72,8 @@ _SIG = {
                                         _P, ctypes.c_uint, _P, ctypes.c_size_t, _P]),
     "attn_bwd_dense_noalloc": (ctypes.c_int32, [ctypes.POINTER(attn_dense_desc), _P, _P, _P, _P, _P, _P, _P, _P,
                                                 _P, _P, _P, ctypes.c_uint, _P]),
+    "attn_fwd_dense": (ctypes.c_int32, [ctypes.POINTER(attn_dense_desc), _P, _P, _P, _P, _P, _P, _P, _P,
+                                        ctypes.c_size_t, _P]),
     "attn_bwd_paged_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(attn_paged_desc)]),
     "attn_bwd_paged": (ctypes.c_int32, [ctypes.POINTER(attn_paged_desc), _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                         _P, _P, _P, ctypes.c_uint, _P, ctypes.c_size_t, _P]),
@@ -272,6 +274,40 @@ def dense_backward(q, k, v, dy, *, layout="bshd", causal=False, window=None, key
                         _stream_handle(stream))
     _check(st)
     return dq, dk, dv
+
+
+def attn_fwd_dense(desc, q, k, v, key_mask, bias, o, lse, workspace, workspace_bytes, stream) -> int:
+    return int(lib().attn_fwd_dense(ctypes.byref(desc), q, k, v, key_mask, bias, o, lse, workspace, workspace_bytes,
+                                    stream))
+
+
+def dense_forward(q, k, v, *, layout="bshd", causal=False, window=None, key_mask=None, bias=None, scale=0.0,
+                  mask_thr=0.5, mask_neg=-1e9, top_left=False, outputs=None, workspace=None, stream=None):
+    """(o, lse) for CUDA tensors q, k, v ([B,S,H,D] or [B,H,S,D]): o like q,
+    lse fp32 [B, H, Sq] (natural log)."""
+    import torch
+    lay = {"bshd": ATTN_LAYOUT_BSHD, "bhsd": ATTN_LAYOUT_BHSD}[layout]
+    if lay == ATTN_LAYOUT_BSHD:
+        B, Sq, H, D = q.shape
+        Sk = k.shape[1]
+    else:
+        B, H, Sq, D = q.shape
+        Sk = k.shape[2]
+    desc = make_dense_desc(batch=B, heads=H, seq_q=Sq, seq_k=Sk, head_dim=D, dtype=_dtype_code(q), layout=lay,
+                           causal=causal, window=window, key_mask=key_mask is not None, bias=bias is not None,
+                           mask_thr=mask_thr, mask_neg=mask_neg, scale=scale, top_left=top_left)
+    if outputs is None:
+        o = torch.empty_like(q)
+        lse = torch.empty((B, H, Sq), dtype=torch.float32, device=q.device)
+    else:
+        o, lse = outputs
+    nbytes = attn_bwd_dense_workspace_bytes(desc)
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=q.device)
+    st = attn_fwd_dense(desc, _ptr(q), _ptr(k), _ptr(v), _ptr(key_mask), _ptr(bias), _ptr(o), _ptr(lse),
+                        _ptr(workspace), workspace.numel(), _stream_handle(stream))
+    _check(st)
+    return o, lse
 
 
 def check_device_error(stream=None) -> None:

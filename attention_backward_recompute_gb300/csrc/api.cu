@@ -8,6 +8,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <limits>
 #include <mutex>
 
 #include "../../include/attn_bwd.h"
@@ -187,6 +188,100 @@ attn_status_t check_dense_desc(const attn_dense_desc* d, DenseSizes* z) {
   return ATTN_OK;
 }
 
+// Kernel parameters, the hi/lo copy buffers of fp32 storage and the TMA
+// descriptors shared by the backward and the forward export.  dy may be NULL
+// (forward): its maps and copies then alias those of q.  split_hi / split_lo
+// receive the copy buffers of q, dy, k, v (fp32 storage; else the inputs).
+attn_status_t prepare_dense(const attn_dense_desc* d, const DenseSizes& z, const void* q, const void* k,
+                            const void* v, const void* dy, const float* key_mask, const void* bias, const void* o,
+                            const float* lse, void* dq, void* dk, void* dv, void* workspace, attn::DenseParams* pp,
+                            attn::DenseMaps* mp, void* split_hi[4], void* split_lo[4]) {
+  const int64_t B = d->batch, H = d->heads, Sq = d->seq_q, Sk = d->seq_k, D = d->head_dim;
+  const bool has_km = (d->mask_flags & ATTN_MASK_KEY) != 0;
+  const bool has_bias = (d->mask_flags & ATTN_MASK_BIAS) != 0;
+  const bool split = d->dtype == ATTN_DTYPE_F32;
+  attn::DenseParams& p = *pp;
+  p = attn::DenseParams{};
+  p.B = int(B); p.H = int(H); p.Sq = int(Sq); p.Sk = int(Sk); p.D = int(D);
+  p.q_off = (Sk > Sq && !(d->mask_flags & ATTN_MASK_TOP_LEFT)) ? int(Sk - Sq) : 0;
+  p.causal = (d->mask_flags & (ATTN_MASK_CAUSAL | ATTN_MASK_WINDOW)) ? 1 : 0;
+  p.window = (d->mask_flags & ATTN_MASK_WINDOW) ? d->window : -1;
+  p.has_key_mask = has_km ? 1 : 0;
+  p.scale = d->scale > 0.f ? d->scale : float(1.0 / std::sqrt(double(D)));
+  p.scale_log2 = p.scale * attn::kLog2e;
+  p.masked_x2 = d->mask_neg * attn::kLog2e;
+  p.mask_thr = d->mask_thr;
+  p.mask_neg = d->mask_neg;
+  p.key_mask = key_mask;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  p.L2 = reinterpret_cast<float*>(ws);
+  p.delta = reinterpret_cast<float*>(ws + align256(z.stat_bytes));
+  p.pm = reinterpret_cast<float*>(ws + 2 * align256(z.stat_bytes));
+  p.o = o; p.lse = lse; p.dy = dy;
+  p.dq = dq; p.dk = dk; p.dv = dv;
+  if (d->layout == ATTN_LAYOUT_BSHD) {
+    p.q_ss = H * D; p.q_sh = D; p.q_sb = Sq * H * D;
+    p.k_ss = H * D; p.k_sh = D; p.k_sb = Sk * H * D;
+  } else {
+    p.q_ss = D; p.q_sh = Sq * D; p.q_sb = H * Sq * D;
+    p.k_ss = D; p.k_sh = Sk * D; p.k_sb = H * Sk * D;
+  }
+  p.err = device_error_word();
+  if (!p.err) return api_fail(ATTN_ERR_CUDA, "no CUDA device / symbol address unavailable");
+
+  // fp32 storage: the tensor-core operands are hi/lo bf16 copies of q, k, v, dy
+  // (same layout, bf16 elements) made by a split kernel into the workspace.
+  const void *qa = q, *ka = k, *va = v, *dya = dy ? dy : q;
+  const void *ql = q, *kl = k, *vl = v, *dyl = dy ? dy : q;
+  if (split) {
+    uint8_t* c = ws + z.split_off;
+    const size_t qc = align256(z.q_bytes / 2), kc = align256(z.k_bytes / 2);
+    void* parts[8] = {c, c + qc, c + 2 * qc, c + 3 * qc, c + 4 * qc, c + 4 * qc + kc, c + 4 * qc + 2 * kc,
+                      c + 4 * qc + 3 * kc};
+    qa = parts[0]; ql = parts[1]; dya = parts[2]; dyl = parts[3];
+    ka = parts[4]; kl = parts[5]; va = parts[6]; vl = parts[7];
+    if (!dy) dya = qa, dyl = ql;
+  }
+  split_hi[0] = const_cast<void*>(qa); split_lo[0] = const_cast<void*>(ql);
+  split_hi[1] = const_cast<void*>(dya); split_lo[1] = const_cast<void*>(dyl);
+  split_hi[2] = const_cast<void*>(ka); split_lo[2] = const_cast<void*>(kl);
+  split_hi[3] = const_cast<void*>(va); split_lo[3] = const_cast<void*>(vl);
+  // TMA descriptors: (d, s, h, b) with byte strides of s, h, b
+  const CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const uint64_t es = 2;  // the tensor-core operands are always bf16
+  const uint64_t qdims[4] = {uint64_t(D), uint64_t(Sq), uint64_t(H), uint64_t(B)};
+  const uint64_t kdims[4] = {uint64_t(D), uint64_t(Sk), uint64_t(H), uint64_t(B)};
+  const uint64_t qstr[3] = {uint64_t(p.q_ss) * es, uint64_t(p.q_sh) * es, uint64_t(p.q_sb) * es};
+  const uint64_t kstr[3] = {uint64_t(p.k_ss) * es, uint64_t(p.k_sh) * es, uint64_t(p.k_sb) * es};
+  attn::DenseMaps& m = *mp;
+  std::memset(&m, 0, sizeof(m));
+  m.split = split;
+  bool enc = encode4d(&m.q64, dt, qa, qdims, qstr, 64, 64) && encode4d(&m.q128, dt, qa, qdims, qstr, 64, 128) &&
+             encode4d(&m.dy64, dt, dya, qdims, qstr, 64, 64) && encode4d(&m.dy128, dt, dya, qdims, qstr, 64, 128) &&
+             encode4d(&m.k64, dt, ka, kdims, kstr, 64, 64) && encode4d(&m.k128, dt, ka, kdims, kstr, 64, 128) &&
+             encode4d(&m.v64, dt, va, kdims, kstr, 64, 64) && encode4d(&m.v128, dt, va, kdims, kstr, 64, 128);
+  if (enc && split) {
+    enc = encode4d(&m.q64_lo, dt, ql, qdims, qstr, 64, 64) && encode4d(&m.q128_lo, dt, ql, qdims, qstr, 64, 128) &&
+          encode4d(&m.dy64_lo, dt, dyl, qdims, qstr, 64, 64) &&
+          encode4d(&m.dy128_lo, dt, dyl, qdims, qstr, 64, 128) && encode4d(&m.k64_lo, dt, kl, kdims, kstr, 64, 64) &&
+          encode4d(&m.k128_lo, dt, kl, kdims, kstr, 64, 128) && encode4d(&m.v64_lo, dt, vl, kdims, kstr, 64, 64) &&
+          encode4d(&m.v128_lo, dt, vl, kdims, kstr, 64, 128);
+  } else if (enc) {
+    m.q64_lo = m.q64; m.q128_lo = m.q128; m.dy64_lo = m.dy64; m.dy128_lo = m.dy128;
+    m.k64_lo = m.k64; m.k128_lo = m.k128; m.v64_lo = m.v64; m.v128_lo = m.v128;
+  }
+  if (enc && has_bias) {
+    const uint64_t bdims[4] = {uint64_t(Sk), uint64_t(Sq), uint64_t(H), uint64_t(B)};
+    const uint64_t bstr[3] = {uint64_t(Sk) * es, uint64_t(Sq * Sk) * es, uint64_t(H * Sq * Sk) * es};
+    enc = encode4d(&m.bias64, dt, bias, bdims, bstr, 64, 64) && encode4d(&m.bias128, dt, bias, bdims, bstr, 64, 128);
+  } else if (enc) {
+    m.bias64 = m.q64;  // unused by the kernels without bias
+    m.bias128 = m.q128;
+  }
+  if (!enc) return api_fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed (driver entry point or arguments)");
+  return ATTN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -222,7 +317,7 @@ ATTN_API attn_status_t attn_bwd_dense(const attn_dense_desc* d, const void* q, c
   const bool want_dq = wrt_mask & ATTN_WRT_DQ, want_dk = wrt_mask & ATTN_WRT_DK, want_dv = wrt_mask & ATTN_WRT_DV;
   if ((want_dq && !dq && z.q_bytes) || (want_dk && !dk && z.k_bytes) || (want_dv && !dv && z.k_bytes))
     return api_fail(ATTN_ERR_INVALID_ARG, "requested gradient pointer is NULL");
-  const int64_t B = d->batch, H = d->heads, Sq = d->seq_q, Sk = d->seq_k, D = d->head_dim;
+  const int64_t B = d->batch, H = d->heads, Sq = d->seq_q, Sk = d->seq_k;
   const bool empty_q = B * H * Sq == 0, empty_k = B * H * Sk == 0;
   // required inputs (only when they have elements)
   if (!empty_q && (!q || !dy)) return api_fail(ATTN_ERR_INVALID_ARG, "q/dy is NULL");
@@ -256,80 +351,14 @@ ATTN_API attn_status_t attn_bwd_dense(const attn_dense_desc* d, const void* q, c
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return api_fail(ATTN_ERR_WORKSPACE, "workspace must be 256-byte aligned");
   const bool split = d->dtype == ATTN_DTYPE_F32;
 
-  attn::DenseParams p{};
-  p.B = int(B); p.H = int(H); p.Sq = int(Sq); p.Sk = int(Sk); p.D = int(D);
-  p.q_off = (Sk > Sq && !(d->mask_flags & ATTN_MASK_TOP_LEFT)) ? int(Sk - Sq) : 0;
-  p.causal = (d->mask_flags & (ATTN_MASK_CAUSAL | ATTN_MASK_WINDOW)) ? 1 : 0;
-  p.window = (d->mask_flags & ATTN_MASK_WINDOW) ? d->window : -1;
-  p.has_key_mask = has_km ? 1 : 0;
-  p.scale = d->scale > 0.f ? d->scale : float(1.0 / std::sqrt(double(D)));
-  p.scale_log2 = p.scale * attn::kLog2e;
-  p.masked_x2 = d->mask_neg * attn::kLog2e;
-  p.mask_thr = d->mask_thr;
-  p.mask_neg = d->mask_neg;
-  p.key_mask = key_mask;
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  p.L2 = reinterpret_cast<float*>(ws);
-  p.delta = reinterpret_cast<float*>(ws + align256(z.stat_bytes));
-  p.pm = reinterpret_cast<float*>(ws + 2 * align256(z.stat_bytes));
-  p.o = o; p.lse = lse; p.dy = dy;
-  p.dq = dq; p.dk = dk; p.dv = dv;
-  if (d->layout == ATTN_LAYOUT_BSHD) {
-    p.q_ss = H * D; p.q_sh = D; p.q_sb = Sq * H * D;
-    p.k_ss = H * D; p.k_sh = D; p.k_sb = Sk * H * D;
-  } else {
-    p.q_ss = D; p.q_sh = Sq * D; p.q_sb = H * Sq * D;
-    p.k_ss = D; p.k_sh = Sk * D; p.k_sb = H * Sk * D;
-  }
-  p.wrt = wrt_mask;
-  p.err = device_error_word();
-  if (!p.err) return api_fail(ATTN_ERR_CUDA, "no CUDA device / symbol address unavailable");
-
-  // fp32 storage: the tensor-core operands are hi/lo bf16 copies of q, k, v, dy
-  // (same layout, bf16 elements) made by a split kernel into the workspace.
-  const void *qa = q, *ka = k, *va = v, *dya = dy;
-  const void *ql = q, *kl = k, *vl = v, *dyl = dy;
-  if (split) {
-    uint8_t* c = ws + z.split_off;
-    const size_t qc = align256(z.q_bytes / 2), kc = align256(z.k_bytes / 2);
-    void* parts[8] = {c, c + qc, c + 2 * qc, c + 3 * qc, c + 4 * qc, c + 4 * qc + kc, c + 4 * qc + 2 * kc,
-                      c + 4 * qc + 3 * kc};
-    qa = parts[0]; ql = parts[1]; dya = parts[2]; dyl = parts[3];
-    ka = parts[4]; kl = parts[5]; va = parts[6]; vl = parts[7];
-  }
-  // TMA descriptors: (d, s, h, b) with byte strides of s, h, b
-  const CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  const uint64_t es = 2;  // the tensor-core operands are always bf16
-  const uint64_t qdims[4] = {uint64_t(D), uint64_t(Sq), uint64_t(H), uint64_t(B)};
-  const uint64_t kdims[4] = {uint64_t(D), uint64_t(Sk), uint64_t(H), uint64_t(B)};
-  const uint64_t qstr[3] = {uint64_t(p.q_ss) * es, uint64_t(p.q_sh) * es, uint64_t(p.q_sb) * es};
-  const uint64_t kstr[3] = {uint64_t(p.k_ss) * es, uint64_t(p.k_sh) * es, uint64_t(p.k_sb) * es};
+  attn::DenseParams p;
   attn::DenseMaps m;
-  std::memset(&m, 0, sizeof(m));
-  m.split = split;
-  bool enc = encode4d(&m.q64, dt, qa, qdims, qstr, 64, 64) && encode4d(&m.q128, dt, qa, qdims, qstr, 64, 128) &&
-             encode4d(&m.dy64, dt, dya, qdims, qstr, 64, 64) && encode4d(&m.dy128, dt, dya, qdims, qstr, 64, 128) &&
-             encode4d(&m.k64, dt, ka, kdims, kstr, 64, 64) && encode4d(&m.k128, dt, ka, kdims, kstr, 64, 128) &&
-             encode4d(&m.v64, dt, va, kdims, kstr, 64, 64) && encode4d(&m.v128, dt, va, kdims, kstr, 64, 128);
-  if (enc && split) {
-    enc = encode4d(&m.q64_lo, dt, ql, qdims, qstr, 64, 64) && encode4d(&m.q128_lo, dt, ql, qdims, qstr, 64, 128) &&
-          encode4d(&m.dy64_lo, dt, dyl, qdims, qstr, 64, 64) &&
-          encode4d(&m.dy128_lo, dt, dyl, qdims, qstr, 64, 128) && encode4d(&m.k64_lo, dt, kl, kdims, kstr, 64, 64) &&
-          encode4d(&m.k128_lo, dt, kl, kdims, kstr, 64, 128) && encode4d(&m.v64_lo, dt, vl, kdims, kstr, 64, 64) &&
-          encode4d(&m.v128_lo, dt, vl, kdims, kstr, 64, 128);
-  } else if (enc) {
-    m.q64_lo = m.q64; m.q128_lo = m.q128; m.dy64_lo = m.dy64; m.dy128_lo = m.dy128;
-    m.k64_lo = m.k64; m.k128_lo = m.k128; m.v64_lo = m.v64; m.v128_lo = m.v128;
-  }
-  if (enc && has_bias) {
-    const uint64_t bdims[4] = {uint64_t(Sk), uint64_t(Sq), uint64_t(H), uint64_t(B)};
-    const uint64_t bstr[3] = {uint64_t(Sk) * es, uint64_t(Sq * Sk) * es, uint64_t(H * Sq * Sk) * es};
-    enc = encode4d(&m.bias64, dt, bias, bdims, bstr, 64, 64) && encode4d(&m.bias128, dt, bias, bdims, bstr, 64, 128);
-  } else if (enc) {
-    m.bias64 = m.q64;  // unused by the kernels without bias
-    m.bias128 = m.q128;
-  }
-  if (!enc) return api_fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed (driver entry point or arguments)");
+  void* his[4];
+  void* los[4];
+  if ((st = prepare_dense(d, z, q, k, v, dy, key_mask, bias, o, lse, dq, dk, dv, workspace, &p, &m, his, los)) !=
+      ATTN_OK)
+    return st;
+  p.wrt = wrt_mask;
 
   const int nk = (split ? 4 : 0) + 1 + (want_dk || want_dv ? 1 : 0) + (want_dq ? 1 : 0);
   attn::timing_mark_begin(nk, s);
@@ -338,8 +367,6 @@ ATTN_API attn_status_t attn_bwd_dense(const attn_dense_desc* d, const void* q, c
     const int64_t nq = int64_t(z.q_bytes / 4), nkv = int64_t(z.k_bytes / 4);
     const float* srcs[4] = {static_cast<const float*>(q), static_cast<const float*>(dy), static_cast<const float*>(k),
                             static_cast<const float*>(v)};
-    void* his[4] = {const_cast<void*>(qa), const_cast<void*>(dya), const_cast<void*>(ka), const_cast<void*>(va)};
-    void* los[4] = {const_cast<void*>(ql), const_cast<void*>(dyl), const_cast<void*>(kl), const_cast<void*>(vl)};
     for (int i = 0; i < 4 && e == cudaSuccess; ++i) {
       e = attn::launch_split_f32(srcs[i], his[i], los[i], i < 2 ? nq : nkv, s);
       attn::timing_mark(s);
@@ -356,6 +383,75 @@ ATTN_API attn_status_t attn_bwd_dense(const attn_dense_desc* d, const void* q, c
   }
   if (e == cudaSuccess && want_dq) {
     e = split ? attn::launch_dq(m, p, has_bias, s) : attn::launch_dq2(m, p, has_bias, s);
+    attn::timing_mark(s);
+  }
+  attn::timing_mark_end();
+  if (e != cudaSuccess) return api_fail(ATTN_ERR_CUDA, "kernel launch failed: %s", cudaGetErrorString(e));
+  return api_ok();
+}
+
+ATTN_API attn_status_t attn_fwd_dense(const attn_dense_desc* d, const void* q, const void* k, const void* v,
+                                      const float* key_mask, const void* bias, void* o, float* lse, void* workspace,
+                                      size_t workspace_bytes, void* stream) {
+  DenseSizes z;
+  attn_status_t st = check_dense_desc(d, &z);
+  if (st != ATTN_OK) return st;
+  const bool has_km = (d->mask_flags & ATTN_MASK_KEY) != 0;
+  const bool has_bias = (d->mask_flags & ATTN_MASK_BIAS) != 0;
+  if (has_km != (key_mask != nullptr)) return api_fail(ATTN_ERR_INVALID_ARG, "key_mask must be given iff ATTN_MASK_KEY is set");
+  if (has_bias != (bias != nullptr)) return api_fail(ATTN_ERR_INVALID_ARG, "bias must be given iff ATTN_MASK_BIAS is set");
+  const int64_t B = d->batch, H = d->heads, Sq = d->seq_q, Sk = d->seq_k;
+  const bool empty_q = B * H * Sq == 0, empty_k = B * H * Sk == 0;
+  if (!empty_q && (!q || !o || !lse)) return api_fail(ATTN_ERR_INVALID_ARG, "q/o/lse is NULL");
+  if (!empty_k && (!k || !v)) return api_fail(ATTN_ERR_INVALID_ARG, "k/v is NULL");
+  const void* ptrs[] = {q, k, v, key_mask, bias, o, lse, workspace};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return api_fail(ATTN_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  if (has_bias && (Sk * z.es) % 16 != 0) return api_fail(ATTN_ERR_UNSUPPORTED, "bias needs Sk * element size to be a multiple of 16");
+  struct R { const void* p; size_t n; };
+  const R ins[] = {{q, z.q_bytes}, {k, z.k_bytes}, {v, z.k_bytes}, {key_mask, has_km ? z.mask_bytes : 0},
+                   {bias, has_bias ? z.bias_bytes : 0}, {workspace, workspace_bytes}};
+  const R outs[] = {{o, z.q_bytes}, {lse, z.stat_bytes}};
+  for (const R& w : outs)
+    for (const R& r : ins)
+      if (ranges_overlap(w.p, w.n, r.p, r.n)) return api_fail(ATTN_ERR_ALIAS, "an output overlaps an input or the workspace");
+  if (ranges_overlap(o, z.q_bytes, lse, z.stat_bytes)) return api_fail(ATTN_ERR_ALIAS, "o and lse overlap");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (empty_q) return api_ok();
+  if (empty_k) {  // no key: O = 0, lse = -inf
+    if (cudaMemsetAsync(o, 0, z.q_bytes, s) != cudaSuccess) return api_fail(ATTN_ERR_CUDA, "memset failed");
+    cudaError_t e = attn::launch_fill_f32(lse, -std::numeric_limits<float>::infinity(), int64_t(z.stat_bytes / 4), s);
+    if (e != cudaSuccess) return api_fail(ATTN_ERR_CUDA, "fill failed: %s", cudaGetErrorString(e));
+    return api_ok();
+  }
+  if (!workspace || workspace_bytes < z.ws_bytes)
+    return api_fail(ATTN_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", z.ws_bytes, workspace_bytes);
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return api_fail(ATTN_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+  const bool split = d->dtype == ATTN_DTYPE_F32;
+  attn::DenseParams p;
+  attn::DenseMaps m;
+  void* his[4];
+  void* los[4];
+  if ((st = prepare_dense(d, z, q, k, v, nullptr, key_mask, bias, nullptr, nullptr, nullptr, nullptr, nullptr,
+                          workspace, &p, &m, his, los)) != ATTN_OK)
+    return st;
+  p.fwd_only = 1;
+  p.o_out = o;
+  p.lse_out = lse;
+  attn::timing_mark_begin(split ? 4 : 1, s);
+  cudaError_t e = cudaSuccess;
+  if (split) {
+    const int64_t nq = int64_t(z.q_bytes / 4), nkv = int64_t(z.k_bytes / 4);
+    const float* srcs[4] = {static_cast<const float*>(q), nullptr, static_cast<const float*>(k),
+                            static_cast<const float*>(v)};
+    for (int i = 0; i < 4 && e == cudaSuccess; ++i) {
+      if (i == 1) continue;  // no dY in a forward pass
+      e = attn::launch_split_f32(srcs[i], his[i], los[i], i < 2 ? nq : nkv, s);
+      attn::timing_mark(s);
+    }
+  }
+  if (e == cudaSuccess) {
+    e = attn::launch_fwd_stats(m, p, has_bias, s);
     attn::timing_mark(s);
   }
   attn::timing_mark_end();

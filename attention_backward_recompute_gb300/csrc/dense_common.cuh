@@ -37,6 +37,12 @@ struct DenseParams {
   int64_t q_ss, q_sh, q_sb;   // strides of q / dy / o / dq
   int64_t k_ss, k_sh, k_sb;   // strides of k / v / dk / dv
   unsigned wrt;               // ATTN_WRT_* bits
+  // Forward export (the row-statistics sweep run as a forward pass): when
+  // fwd_only is set there is no dY and no delta; o_out (q's layout and dtype)
+  // and lse_out ([B, H, Sq], natural log) receive O and the LSE.
+  int fwd_only;
+  void* o_out;
+  float* lse_out;
   uint32_t* err;              // device error word
 };
 

@@ -134,7 +134,7 @@ __global__ void __launch_bounds__(256, 1)
           }
         if (HAS_BIAS) tma_load_4d(sm + L::BIAS_OFF + s * L::BIAS, &tm_bias, &bar_full[s], kk0, q0, h, b);
         last_use[s] = t;
-        if (t == 0) {  // dY is only needed at the end; load it behind the first tile
+        if (t == 0 && !p.fwd_only) {  // dY is only needed at the end; load it behind the first tile
           mbar_arrive_expect_tx(&bar_dy, L::NSP * L::QT);
           for (int hl = 0; hl < L::NSP; ++hl)
             for (int c = 0; c < L::NCH; ++c)
@@ -145,7 +145,7 @@ __global__ void __launch_bounds__(256, 1)
       for (int s = 0; s < 2; ++s)
         if (last_use[s] >= 0) drain_wait(&bar_full[s], (last_use[s] >> 1) & 1);
       drain_wait(&bar_q, 0);
-      if (last_use[0] >= 0) drain_wait(&bar_dy, 0);
+      if (last_use[0] >= 0 && !p.fwd_only) drain_wait(&bar_dy, 0);
     }
     __syncwarp();
   } else if (n > 0 && warp == 1) {
@@ -317,19 +317,25 @@ __global__ void __launch_bounds__(256, 1)
       if (lane == 0) mbar_arrive(&bar_p_full[s]);
     }
     float L2 = kInf, dl = 0.f, pm = 0.f;
+    // forward export: O / l in the storage dtype (rows of the tile that exist)
+    const int64_t o_row = static_cast<int64_t>(b) * p.q_sb + static_cast<int64_t>(h) * p.q_sh +
+                          static_cast<int64_t>(q) * p.q_ss;
     if (ok && n > 0) {
       ok = mbar_wait_warp(&bar_p_free[(n - 1) & 1], ((n - 1) >> 1) & 1, ab);
-      if (ok) ok = mbar_wait_warp(&bar_dy, 0, ab);
+      if (ok && !p.fwd_only) ok = mbar_wait_warp(&bar_dy, 0, ab);
       tc_fence_after();
       if (ok) {
         // delta = dY . O / l, O read back from TMEM, dY from the swizzled tile
         float acc = 0.f;
         const uint8_t* dys = sm + L::DY_OFF;
+        const float inv_l = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll 1
         for (int cc = 0; cc < DP / 32; ++cc) {
           uint32_t r[32];
           tmem_ld32(t_o + lane_addr + cc * 32, r);
           tmem_ld_wait();
+          if (p.o_out && q < p.Sq) store_out32<SPLIT>(p.o_out, o_row, cc * 32, p.D, r, inv_l);
+          if (p.fwd_only) continue;
 #pragma unroll
           for (int hl = 0; hl < L::NSP; ++hl)  // dY = hi (+ lo for split fp32 inputs)
 #pragma unroll
@@ -357,6 +363,13 @@ __global__ void __launch_bounds__(256, 1)
       p.L2[idx] = L2;
       p.delta[idx] = dl;
       if (p.has_key_mask) p.pm[idx] = pm;
+      if (p.lse_out) p.lse_out[idx] = L2 < __int_as_float(0x7f800000) ? L2 * 0.6931471805599453f : -L2;
+      if (p.o_out && n == 0) {
+        uint32_t z[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) z[j] = 0u;
+        for (int cc = 0; cc * 32 < p.D; ++cc) store_out32<SPLIT>(p.o_out, o_row, cc * 32, p.D, z, 0.f);
+      }
     }
   }
   tc_fence_before();
@@ -447,6 +460,21 @@ cudaError_t launch_split_f32(const float* x, void* hi, void* lo, int64_t n, cuda
   const int64_t blocks = (n / 4 + 255) / 256;
   split_f32_kernel<<<static_cast<int>(blocks < 152 * 16 ? blocks : 152 * 16), 256, 0, s>>>(
       x, static_cast<__nv_bfloat16*>(hi), static_cast<__nv_bfloat16*>(lo), n);
+  return cudaGetLastError();
+}
+
+namespace {
+__global__ void fill_f32_kernel(float* x, float value, int64_t n) {
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    x[i] = value;
+}
+}  // namespace
+
+cudaError_t launch_fill_f32(float* x, float value, int64_t n, cudaStream_t s) {
+  if (n <= 0) return cudaSuccess;
+  const int64_t blocks = (n + 255) / 256;
+  fill_f32_kernel<<<static_cast<int>(blocks < 152 * 8 ? blocks : 152 * 8), 256, 0, s>>>(x, value, n);
   return cudaGetLastError();
 }
 

@@ -29,6 +29,8 @@ inline int padded_head_dim(int D) { return D <= 64 ? 64 : 128; }
 cudaError_t launch_fwd_stats(const DenseMaps& m, const DenseParams& p, bool bias, cudaStream_t s);
 // bf16 storage: row statistics from S and dP (no O accumulator), Q and dY in tensor memory
 cudaError_t launch_stats2(const DenseMaps& m, const DenseParams& p, bool bias, cudaStream_t s);
+// x[0, n) = value
+cudaError_t launch_fill_f32(float* x, float value, int64_t n, cudaStream_t s);
 cudaError_t launch_delta_only(const DenseParams& p, int dtype_bf16, cudaStream_t s);
 // Split fp32 tensors into hi/lo bf16 copies: hi = bf16(x), lo = bf16(x - hi).
 cudaError_t launch_split_f32(const float* x, void* hi, void* lo, int64_t n, cudaStream_t s);

@@ -246,6 +246,26 @@ ATTN_API attn_status_t attn_paged_row_stats(const attn_paged_desc* d, const void
                                             void* stream);
 
 /*
+ * Dense forward export: O and the LSE of the same attention the backward
+ * differentiates (same descriptor, masks and bias), by the forward sweep of
+ * the backward's row-statistics prologue (rlx-cpu src/attention_bwd.rs,
+ * backward_dense_head_all: scores, masks and max-subtracted softmax; O = P V).
+ *   q [.., Sq, .., D], k, v [.., Sk, .., D] in the descriptor's layout and
+ *   dtype; key_mask / bias as for attn_bwd_dense (required iff flagged);
+ *   o: output shaped and typed like q, O = softmax(S) V (0 for a row with no
+ *   visible key);
+ *   lse: fp32 [B, H, Sq] output, natural-log log-sum-exp of the row's scores
+ *   (-inf for a row with no visible key).
+ * The pair (o, lse) is what attn_bwd_dense takes in its O-and-LSE mode.
+ * Workspace as attn_bwd_dense (attn_bwd_dense_workspace_bytes).  Errors as
+ * attn_bwd_dense; an output overlapping an input or the workspace gives
+ * ATTN_ERR_ALIAS.  Asynchronous on `stream`.
+ */
+ATTN_API attn_status_t attn_fwd_dense(const attn_dense_desc* d, const void* q, const void* k, const void* v,
+                                      const float* key_mask, const void* bias, void* o, float* lse, void* workspace,
+                                      size_t workspace_bytes, void* stream);
+
+/*
  * Query side of the paged backward: the row statistics and the query
  * gradient of every packed query row in one call.  ruDNN
  * src/paged_attention/ordered_kernel.rs (history_backward) reads per (row,
