@@ -300,6 +300,34 @@ def sweep(args) -> int:
               "oracle_s_extrapolated": t_or * len(heads) / len(sample), "host_cores": cores,
               "peak_source": src})
 
+    # forward export (O and LSE) on the headline shape
+    c = inputs.dense_config("dense_bf16_s2048")
+    t = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda().to(torch.bfloat16)
+    q, k, v = t(c.q), t(c.k), t(c.v)
+    km = torch.from_numpy(c.key_mask).cuda()
+    bias = t(c.bias)
+    fo = (torch.empty_like(q), torch.empty((c.batch, c.heads, c.seq_q), dtype=torch.float32, device="cuda"))
+    fcall = lambda: bd.dense_forward(q, k, v, layout=c.layout, causal=c.causal, window=c.window, key_mask=km,
+                                     bias=bias, outputs=fo)
+    fms, fms_min = timed(fcall, 20)
+    vp = visible_pairs(c.seq_q, c.seq_k, c.causal, c.window)
+    fflops = 4.0 * c.head_dim * vp * c.batch * c.heads
+    sample = [(0, 0), (3, 15)]
+    from oracle import attn_fwd_dense as fwd_oracle
+    t0 = time.perf_counter()
+    o_ref, lse_ref = fwd_oracle(c.q, c.k, c.v, layout=c.layout, causal=c.causal, window=c.window,
+                                key_mask=c.key_mask, bias=c.bias)
+    ft_or = time.perf_counter() - t0
+    g = fo[0].float().cpu().numpy()
+    ferr = max(float(np.max(np.abs(g[b_, :, h_] - o_ref[b_, :, h_])) / np.max(np.abs(o_ref[b_, :, h_])))
+               for b_, h_ in sample)
+    emit({"config": "C3 forward export (O, LSE)", "workload": "dense_bf16_s2048", "gpu_ms_median": fms,
+          "gpu_ms_min": fms_min, "counted_tflops": fflops / (fms * 1e-3) / 1e12,
+          "pct_of_bf16_peak": 100.0 * fflops / (fms * 1e-3) / 1e12 / peaks["bf16_tflops"],
+          "flops_counted": "4*D per visible pair (S = Q K^T, O = P V)", "max_err_rel_o": ferr, "tolerance": 2e-2,
+          "oracle_s": ft_or, "oracle_sample": "all 64 (batch, head) pairs, error on 2", "host_cores": cores,
+          "peak_source": src})
+
     for tag, name in (("C5g", "paged_gqa"), ("C5m", "paged_mla")):
         c = inputs.paged_config(name)
         tb = lambda x: None if x is None else torch.from_numpy(np.ascontiguousarray(x)).cuda().to(torch.bfloat16)
