@@ -357,25 +357,29 @@ def paged_row_stats(q, k_pool, v_pool, dy, page_table, seq_meta, *, heads, kv_he
 
 
 def paged_query_backward(q, k_pool, v_pool, dy, page_table, seq_meta, *, heads, kv_heads, page_size=16,
-                         causal=True, scale=0.0, outputs=None, workspace=None, stream=None):
-    """Query side (GQA): (lse, delta, dq) for CUDA tensors, lse/delta [Nq, H]
-    fp32 and dq shaped like q."""
+                         causal=True, scale=0.0, qp=None, kp_pool=None, outputs=None, workspace=None, stream=None):
+    """Query side: (lse, delta, dq) for GQA or (lse, delta, dq, dqp) for MLA
+    (qp, kp_pool given), for CUDA tensors; lse/delta [Nq, H] fp32, dq shaped
+    like q, dqp like qp."""
     import torch
-    d = _paged_desc_for(q, dy, k_pool, page_table, seq_meta, heads, kv_heads, page_size, causal, scale, None, None)
+    d = _paged_desc_for(q, dy, k_pool, page_table, seq_meta, heads, kv_heads, page_size, causal, scale, qp, kp_pool)
+    mla = qp is not None
     if outputs is None:
         lse = torch.empty((q.shape[0], heads), dtype=torch.float32, device=q.device)
         delta = torch.empty_like(lse)
         dq = torch.empty_like(q)
+        dqp = torch.empty_like(qp) if mla else None
     else:
-        lse, delta, dq = outputs
+        lse, delta, dq = outputs[:3]
+        dqp = outputs[3] if mla else None
     n = attn_bwd_paged_workspace_bytes(d)
     if workspace is None:
         workspace = torch.empty(max(n, 256), dtype=torch.uint8, device=q.device)
-    st = attn_bwd_paged_query(d, _ptr(q), None, _ptr(k_pool), _ptr(v_pool), None, _ptr(dy), _ptr(page_table),
-                              _ptr(seq_meta), _ptr(lse), _ptr(delta), _ptr(dq), None, _ptr(workspace),
-                              workspace.numel(), _stream_handle(stream))
+    st = attn_bwd_paged_query(d, _ptr(q), _ptr(qp), _ptr(k_pool), _ptr(v_pool), _ptr(kp_pool), _ptr(dy),
+                              _ptr(page_table), _ptr(seq_meta), _ptr(lse), _ptr(delta), _ptr(dq), _ptr(dqp),
+                              _ptr(workspace), workspace.numel(), _stream_handle(stream))
     _check(st)
-    return lse, delta, dq
+    return (lse, delta, dq, dqp) if mla else (lse, delta, dq)
 
 
 def paged_backward(q, k_pool, v_pool, dy, page_table, seq_meta, lse, delta, *, heads, kv_heads, page_size=16,

@@ -330,32 +330,64 @@ ATTN_API attn_status_t attn_bwd_paged_query(const attn_paged_desc* d, const void
   attn_status_t st = check_paged_desc(d, &z);
   if (st != ATTN_OK) return st;
   const bool mla = d->position_dim > 0;
-  if (mla) return api_fail(ATTN_ERR_UNSUPPORTED, "the query side of MLA (dQ, dQp) is not built; GQA only");
-  (void)qp;
-  (void)kp_pool;
-  (void)dqp;
   if (d->num_queries == 0) return api_ok();
-  if (!q || !dy || !lse || !delta || !dq || !seq_meta || (d->max_pages_per_seq > 0 && !page_table))
+  if (!q || !dy || !lse || !delta || !dq || !seq_meta || (d->max_pages_per_seq > 0 && !page_table) ||
+      (mla && (!qp || !dqp)))
     return api_fail(ATTN_ERR_INVALID_ARG, "a required pointer is NULL");
-  if (d->num_pages > 0 && (!k_pool || !v_pool)) return api_fail(ATTN_ERR_INVALID_ARG, "k_pool/v_pool is NULL");
-  const void* al[] = {q, k_pool, v_pool, dy, lse, delta, dq, page_table, seq_meta};
+  if (d->num_pages > 0 && (!k_pool || (mla ? !kp_pool : !v_pool)))
+    return api_fail(ATTN_ERR_INVALID_ARG, "k_pool/v_pool/kp_pool is NULL");
+  const void* al[] = {q, qp, k_pool, v_pool, kp_pool, dy, lse, delta, dq, dqp, page_table, seq_meta};
   for (const void* x : al)
     if (x && !al16(x)) return api_fail(ATTN_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
+  const size_t dqp_bytes = mla ? z.qp_bytes : 0;
   struct R { const void* p; size_t n; };
-  const R ins[] = {{q, z.q_bytes}, {k_pool, z.k_bytes}, {v_pool, z.v_bytes}, {dy, z.dy_bytes},
-                   {page_table, z.table_bytes}, {seq_meta, z.meta_bytes}, {workspace, workspace_bytes}};
-  const R outs[] = {{lse, z.stat_bytes}, {delta, z.stat_bytes}, {dq, z.q_bytes}};
+  const R ins[] = {{q, z.q_bytes}, {qp, dqp_bytes}, {k_pool, z.k_bytes}, {v_pool, mla ? 0 : z.v_bytes},
+                   {kp_pool, mla ? z.kp_bytes : 0}, {dy, z.dy_bytes}, {page_table, z.table_bytes},
+                   {seq_meta, z.meta_bytes}, {workspace, workspace_bytes}};
+  const R outs[] = {{lse, z.stat_bytes}, {delta, z.stat_bytes}, {dq, z.q_bytes}, {mla ? dqp : nullptr, dqp_bytes}};
   for (const R& o : outs)
     for (const R& r : ins)
       if (overlap(o.p, o.n, r.p, r.n)) return api_fail(ATTN_ERR_ALIAS, "an output overlaps an input or the workspace");
-  for (int i = 0; i < 3; ++i)
-    for (int j = i + 1; j < 3; ++j)
+  for (int i = 0; i < 4; ++i)
+    for (int j = i + 1; j < 4; ++j)
       if (overlap(outs[i].p, outs[i].n, outs[j].p, outs[j].n)) return api_fail(ATTN_ERR_ALIAS, "outputs overlap");
   attn::PagedParams p;
   if ((st = fill_params(d, z, page_table, seq_meta, workspace, &p)) != ATTN_OK) return st;
   p.lse_out = lse;
   p.delta_out = delta;
   p.dq = dq;
+  if (mla) {
+    // row statistics, then dQ / dQp from them, on the warp-level tensor path
+    if (!attn::mla_mma_supported(p))
+      return api_fail(ATTN_ERR_UNSUPPORTED, "MLA query side needs heads / kv_heads in {4, 8, 16, 32} and page 16");
+    p.dqp = dqp;
+    p.lse = lse;
+    p.delta = delta;
+    attn::PagedMlaMaps mm;
+    std::memset(&mm, 0, sizeof(mm));
+    const uint64_t slots = uint64_t(d->num_pages) * d->page_size;
+    const uint32_t G = uint32_t(p.G), RT2 = 64u / G;
+    bool enc = encode3d(&mm.q, q, d->key_dim, d->heads, d->num_queries, 64, G, RT2) &&
+               encode3d(&mm.qp, qp, d->position_dim, d->heads, d->num_queries, 64, G, RT2) &&
+               encode3d(&mm.dy, dy, d->value_dim, d->heads, d->num_queries, 64, G, RT2);
+    if (slots > 0)
+      enc = enc && encode3d(&mm.k, k_pool, d->key_dim, d->kv_heads, slots, 64, 1, uint32_t(d->page_size)) &&
+            encode3d(&mm.kp, kp_pool, d->position_dim, d->kv_heads, slots, 64, 1, uint32_t(d->page_size));
+    else
+      mm.k = mm.kp = mm.q;
+    if (!enc) return api_fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    attn::timing_mark_begin(3, s);
+    cudaError_t e = attn::launch_paged_mla_stats_mma(mm, p, s);
+    attn::timing_mark(s);
+    if (e == cudaSuccess) e = attn::launch_paged_mla_query_mma(mm, p, s);
+    attn::timing_mark(s);
+    if (e == cudaSuccess) e = attn::launch_paged_query_outside(p, s);
+    attn::timing_mark(s);
+    attn::timing_mark_end();
+    if (e != cudaSuccess) return api_fail(ATTN_ERR_CUDA, "query-side launch failed: %s", cudaGetErrorString(e));
+    return api_ok();
+  }
   attn::PagedMaps m;
   std::memset(&m, 0, sizeof(m));
   const uint64_t slots = uint64_t(d->num_pages) * d->page_size;

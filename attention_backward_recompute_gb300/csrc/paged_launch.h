@@ -22,6 +22,8 @@ cudaError_t launch_paged_history(const PagedMaps& m, const PagedParams& p, cudaS
 cudaError_t launch_paged_row_stats(const PagedMaps& m, const PagedParams& p, cudaStream_t s);
 // query side (GQA): row statistics and dQ in one kernel; q_stats/dy_stats maps
 cudaError_t launch_paged_query(const PagedMaps& m, const PagedParams& p, cudaStream_t s);
+// rows outside every sequence's range: dq (and dqp) = 0, lse = -inf, delta = 0
+cudaError_t launch_paged_query_outside(const PagedParams& p, cudaStream_t s);
 // MLA (key_dim 512 latent + position_dim 64; the latent is also the value)
 cudaError_t launch_paged_mla_history(const PagedParams& p, const void* q, const void* qp, const void* dy,
                                      const void* k_pool, const void* kp_pool, cudaStream_t s);
@@ -35,6 +37,8 @@ bool mla_mma_supported(const PagedParams& p);
 cudaError_t launch_paged_mla_mma(const PagedMlaMaps& m, const PagedParams& p, cudaStream_t s);
 // MLA row statistics on the same path; q, qp, dy maps with box (64, G, 64/G)
 cudaError_t launch_paged_mla_stats_mma(const PagedMlaMaps& m, const PagedParams& p, cudaStream_t s);
+// MLA query side (dQ, dQp) on the same path, from lse / delta; maps as for the statistics
+cudaError_t launch_paged_mla_query_mma(const PagedMlaMaps& m, const PagedParams& p, cudaStream_t s);
 cudaError_t launch_paged_mla_stats(const PagedParams& p, const void* q, const void* qp, const void* dy,
                                    const void* k_pool, const void* kp_pool, cudaStream_t s);
 

@@ -592,6 +592,227 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// Query side of the MLA backward: dQ (latent, 512) and dQp (position, 64) per
+// (query row, head), from the row statistics lse and delta of the same rows.
+// Same CTA decomposition as the row statistics (64 columns resident, keys in
+// 32-token tiles, double-buffered) and the same phase A; then per tile
+//   dS^T of the warp's 16 tokens x 8 columns -> shared memory as dS[col][token]
+//   phase B  warp (column tile mt of 16, dim quarter dq): dQ[., 128 dq ..+128)
+//            += dS K_lat and dQp[., 16 dq ..+16) += dS K_pos  (K as B operand,
+//            token-major, read with transposing ldmatrix)
+// with the fp32 accumulators (16 x 144 per warp) in registers, stored once.
+// ---------------------------------------------------------------------------
+constexpr int QDS_STRIDE = SBT * 2 + 16;       // dS rows: 32 bf16 + 16 bytes of padding
+constexpr int QDS_OFF = S_BYTES;
+constexpr int Q_BYTES = QDS_OFF + SBC * QDS_STRIDE;
+
+__global__ void __launch_bounds__(kThreads, 1)
+    mla_query_mma_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_qp,
+                         const __grid_constant__ CUtensorMap tm_dy, const __grid_constant__ CUtensorMap tm_k,
+                         const __grid_constant__ CUtensorMap tm_kp, const PagedParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ uint64_t bar_q, bar_k[2];
+  __shared__ int abort_flag, ntok_sh, seq_sh, r0_sh;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gkv = blockIdx.x;
+  const int G = p.G, RT2 = SBC / G;
+  if (threadIdx.x == 0) {
+    int idx = blockIdx.y, sq = -1, r0 = 0;
+    for (int q = 0; q < p.S; ++q) {
+      const int tiles = (row_end_of(p, q) - row_begin_of(p, q) + RT2 - 1) / RT2;
+      if (idx < tiles) {
+        sq = q;
+        r0 = row_begin_of(p, q) + idx * RT2;
+        break;
+      }
+      idx -= tiles;
+    }
+    seq_sh = sq;
+    r0_sh = r0;
+  }
+  __syncthreads();
+  const int s = seq_sh, r0 = r0_sh;
+  if (s < 0) return;  // past the last row tile (uniform exit)
+  const int re = row_end_of(p, s);
+  const int len = seq_len_of(p, s);
+  const int npg = pages_of(len, p.page_size);
+  const Abort ab{&abort_flag, p.err};
+  const int oob_slot = p.num_pages * p.page_size;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&bar_q, 1);
+    mbar_init(&bar_k[0], 1);
+    mbar_init(&bar_k[1], 1);
+    mbar_fence_init();
+    int ntok = len;
+    if (p.causal) {
+      int mp = -1;
+      for (int r = r0; r < r0 + RT2 && r < re; ++r) mp = max(mp, p.q_pos[r]);
+      ntok = min(len, mp + 1);
+    }
+    ntok_sh = max(ntok, 0);
+  }
+  __syncthreads();
+  const int nt = (ntok_sh + SBT - 1) / SBT;
+  auto issue_keys = [&](int t, int stage) {
+    uint64_t* bar = &bar_k[stage];
+    mbar_arrive_expect_tx(bar, SK_STAGE);
+    uint8_t* dst = sm + SK_OFF + stage * SK_STAGE;
+    for (int j = 0; j < 2; ++j) {
+      const int lp = 2 * t + j;
+      int slot = oob_slot;
+      if (lp < npg) {
+        const int ph = p.page_table[static_cast<int64_t>(s) * p.max_pages + lp];
+        if (ph >= 0 && ph < p.num_pages) slot = ph * p.page_size;
+      }
+      for (int c = 0; c < 8; ++c) tma_load_3d(dst + c * SKC + j * 16 * 128, &tm_k, bar, c * 64, gkv, slot);
+      tma_load_3d(dst + 8 * SKC + j * 16 * 128, &tm_kp, bar, 0, gkv, slot);
+    }
+  };
+  if (threadIdx.x == 0) {
+    mbar_arrive_expect_tx(&bar_q, 17 * SQC);
+    for (int c = 0; c < 8; ++c) {
+      tma_load_3d(sm + SQ_OFF + c * SQC, &tm_q, &bar_q, c * 64, gkv * G, r0);
+      tma_load_3d(sm + SQ_OFF + (9 + c) * SQC, &tm_dy, &bar_q, c * 64, gkv * G, r0);
+    }
+    tma_load_3d(sm + SQ_OFF + 8 * SQC, &tm_qp, &bar_q, 0, gkv * G, r0);
+    for (int t = 0; t < 2 && t < nt; ++t) issue_keys(t, t);
+  }
+
+  const int tt = warp & 1, n8 = warp >> 1;  // phase A: 2 token tiles x 8 column octets
+  const int mt = warp & 3, dq = warp >> 2;  // phase B: 4 column tiles x 4 dim quarters
+  const int g8 = lane >> 2, t4 = lane & 3;
+  const float kInf = __int_as_float(0x7f800000);
+  // phase-A columns of this thread: statistics, position
+  float lse_c[2], dl_c[2];
+  int pos_c[2];
+  bool col_ok[2];
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    const int c = n8 * 8 + 2 * t4 + e;
+    const int r = r0 + c / G, hh = gkv * G + c % G;
+    col_ok[e] = r < re;
+    const size_t si = static_cast<size_t>(col_ok[e] ? r : 0) * p.H + hh;
+    lse_c[e] = col_ok[e] ? p.lse[si] * kLog2e : kInf;
+    dl_c[e] = col_ok[e] ? p.delta[si] : 0.f;
+    pos_c[e] = col_ok[e] ? (p.causal ? p.q_pos[r] : 0x7fffffff) : -1;
+  }
+  float acc[16][4], accp[2][4];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) accp[i][0] = accp[i][1] = accp[i][2] = accp[i][3] = 0.f;
+  const uint32_t sbase = smem_addr(sm);
+  const uint32_t ds_base = sbase + QDS_OFF;
+  bool ok = nt > 0 ? mbar_wait_warp(&bar_q, 0, ab) : true;
+  for (int t = 0; t < nt; ++t) {
+    const int stage = t & 1;
+    const uint32_t kb = sbase + SK_OFF + stage * SK_STAGE;
+    if (ok) ok = mbar_wait_warp(&bar_k[stage], (t >> 1) & 1, ab);
+    if (ok) {
+      // ---------------------------------------------------------------- phase A
+      float sacc[4] = {0.f, 0.f, 0.f, 0.f}, dpacc[4] = {0.f, 0.f, 0.f, 0.f};
+      const int arow = tt * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
+      const int ahalf = lane >> 4;
+      const int brow = n8 * 8 + (lane & 7);
+      const int bm = lane >> 3;
+#pragma unroll 2
+      for (int kc = 0; kc < 8; ++kc) {
+#pragma unroll
+        for (int kp = 0; kp < 4; ++kp) {
+          uint32_t a[4], bq[4];
+          ldsm_x4(swz(kb + kc * SKC, arow, 2 * kp + ahalf), a);
+          ldsm_x4(swz(sbase + SQ_OFF + ((bm >> 1) ? (9 + kc) : kc) * SQC, brow, 2 * kp + (bm & 1)), bq);
+          mma_16816(sacc, a, bq[0], bq[1]);
+          mma_16816(dpacc, a, bq[2], bq[3]);
+        }
+      }
+#pragma unroll
+      for (int kp = 0; kp < 4; ++kp) {
+        uint32_t a[4], b0, b1;
+        ldsm_x4(swz(kb + 8 * SKC, arow, 2 * kp + ahalf), a);
+        ldsm_x2(swz(sbase + SQ_OFF + 8 * SQC, brow, 2 * kp + (bm & 1)), b0, b1);
+        mma_16816(sacc, a, b0, b1);
+      }
+      // dS of this warp's 16 tokens x 8 columns, stored column-major for phase B
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+        const int i = tt * 16 + g8 + 8 * hr;  // tile-local token
+        const int tok = t * SBT + i;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const bool vis = col_ok[e] && tok < len && tok <= pos_c[e] && lse_c[e] < kInf;
+          const float pe = ex2_approx(fmaf(sacc[2 * hr + e], p.scale_log2, -lse_c[e]));
+          // select, not multiply: S and dP of a tail slot may be NaN
+          const float dsv = vis ? pe * (dpacc[2 * hr + e] - dl_c[e]) * p.scale : 0.f;
+          const int c = n8 * 8 + 2 * t4 + e;
+          *reinterpret_cast<__nv_bfloat16*>(sm + QDS_OFF + c * QDS_STRIDE + i * 2) = __float2bfloat16_rn(dsv);
+        }
+      }
+    }
+    __syncthreads();
+    if (t * SBT + SBT > len) {  // uniform: the barrier below is reached by every thread
+      // key rows of tokens past the length inside the last page may hold any
+      // bit pattern; phase B multiplies them by dS = 0, so they are zeroed
+      if (ok) {
+        const int row_lo = max(0, len - t * SBT);
+        const int nvec = (SBT - row_lo) * 9 * 8;
+        for (int i = threadIdx.x; i < nvec; i += kThreads) {
+          const int rw = row_lo + i / 72, rem = i % 72;
+          st_shared_v4(kb + (rem >> 3) * SKC + rw * 128 + (rem & 7) * 16, 0u, 0u, 0u, 0u);
+        }
+      }
+      __syncthreads();
+    }
+    if (ok && !abort_flag) {
+      // ---------------------------------------------------------------- phase B
+      const int arow = mt * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
+      const int bm = lane >> 3;
+#pragma unroll
+      for (int ks = 0; ks < 2; ++ks) {
+        uint32_t ads[4];
+        ldsm_x4(ds_base + arow * QDS_STRIDE + (ks * 16 + 8 * (lane >> 4)) * 2, ads);
+        const int krow = ks * 16 + (lane & 7) + 8 * (bm & 1);  // token index = B row
+#pragma unroll
+        for (int np = 0; np < 8; ++np) {  // pairs of 8-dim tiles: dims 128 dq + 16 np
+          const int chunk = 2 * dq + (np >> 2);
+          const int piece = 2 * (np & 3) + (bm >> 1);
+          uint32_t bk[4];
+          ldsm_x4_t(swz(kb + chunk * SKC, krow, piece), bk);
+          mma_16816(acc[2 * np], ads, bk[0], bk[1]);
+          mma_16816(acc[2 * np + 1], ads, bk[2], bk[3]);
+        }
+        uint32_t bkp[4];
+        ldsm_x4_t(swz(kb + 8 * SKC, krow, 2 * dq + (bm >> 1)), bkp);
+        mma_16816(accp[0], ads, bkp[0], bkp[1]);
+        mma_16816(accp[1], ads, bkp[2], bkp[3]);
+      }
+    }
+    __syncthreads();  // stage and dS buffer free
+    if (threadIdx.x == 0 && t + 2 < nt && ok && !abort_flag) issue_keys(t + 2, stage);
+  }
+  if (nt > 0 && (!ok || abort_flag)) return;
+  // one store per (row, head): zeros for a column that saw no token
+#pragma unroll
+  for (int hr = 0; hr < 2; ++hr) {
+    const int c = mt * 16 + g8 + 8 * hr;
+    const int r = r0 + c / G, hh = gkv * G + c % G;
+    if (r >= re) continue;
+    const int64_t row = static_cast<int64_t>(r) * p.H + hh;
+    __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.dq) + row * kLat + 128 * dq + 2 * t4;
+#pragma unroll
+    for (int n = 0; n < 16; ++n)
+      *reinterpret_cast<uint32_t*>(o + n * 8) = pack_bf16x2(acc[n][2 * hr], acc[n][2 * hr + 1]);
+    __nv_bfloat16* op = static_cast<__nv_bfloat16*>(p.dqp) + row * kPos + 16 * dq + 2 * t4;
+#pragma unroll
+    for (int n = 0; n < 2; ++n)
+      *reinterpret_cast<uint32_t*>(op + n * 8) = pack_bf16x2(accp[n][2 * hr], accp[n][2 * hr + 1]);
+  }
+}
+
 }  // namespace
 
 bool mla_mma_supported(const PagedParams& p) {
@@ -617,6 +838,21 @@ cudaError_t launch_paged_mla_mma(const PagedMlaMaps& m, const PagedParams& p, cu
   if (e != cudaSuccess) return e;
   dim3 grid((p.max_pages + 3) / 4, p.S, p.KVH);
   mla_mma_kernel<<<grid, kThreads, smem, s>>>(m.q, m.qp, m.dy, m.k, m.kp, p);
+  return cudaGetLastError();
+}
+
+}  // namespace attn
+
+namespace attn {
+
+cudaError_t launch_paged_mla_query_mma(const PagedMlaMaps& m, const PagedParams& p, cudaStream_t s) {
+  if (p.Nq == 0 || p.S == 0) return cudaSuccess;
+  const int smem = Q_BYTES + 1024;
+  cudaError_t e = cudaFuncSetAttribute(mla_query_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const int RT2 = SBC / p.G;
+  dim3 grid(p.KVH, p.Nq / RT2 + p.S + 1, 1);
+  mla_query_mma_kernel<<<grid, kThreads, smem, s>>>(m.q, m.qp, m.dy, m.k, m.kp, p);
   return cudaGetLastError();
 }
 

@@ -450,6 +450,8 @@ __global__ void paged_query_outside_kernel(const PagedParams p) {
     p.lse_out[i] = -__int_as_float(0x7f800000);
     p.delta_out[i] = 0.f;
     for (int d = 0; d < p.Dk; ++d) dq[i * p.Dk + d] = __float2bfloat16(0.f);
+    if (p.dqp)
+      for (int d = 0; d < p.Dp; ++d) static_cast<__nv_bfloat16*>(p.dqp)[i * p.Dp + d] = __float2bfloat16(0.f);
   }
 }
 
@@ -469,6 +471,12 @@ cudaError_t launch_query_t(const PagedMaps& m, const PagedParams& p, cudaStream_
 }
 
 }  // namespace
+
+cudaError_t launch_paged_query_outside(const PagedParams& p, cudaStream_t s) {
+  if (p.Nq == 0) return cudaSuccess;
+  paged_query_outside_kernel<<<64, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_paged_query(const PagedMaps& m, const PagedParams& p, cudaStream_t s) {
   if (p.Nq == 0) return cudaSuccess;

@@ -1,5 +1,5 @@
-"""GPU parity of the query side of the paged backward (row statistics and dQ
-in one call, GQA) with the CPU oracle (dense re-expansion), plus bit
+"""GPU parity of the query side of the paged backward (row statistics and dQ,
+plus dQp for MLA, in one call) with the CPU oracle (dense re-expansion), plus bit
 stability, rows outside every sequence and the full GQA configuration on
 sampled sequences.  Tolerance: 2e-2 * max|ref| (bf16 dQ), 2e-2 absolute on
 the LSE."""
@@ -134,24 +134,74 @@ def test_paged_query_bit_stable(bd):
     bd.check_device_error()
 
 
-def test_paged_query_mla_unsupported(bd):
-    c = inputs.paged_case(name="t", seed=49, num_seqs=2, len_lo=20, len_hi=60, queries_per_seq=4, heads=8,
-                          kv_heads=1, key_dim=512, value_dim=512, position_dim=64, scale=0.5)
+MLA_CASES = [
+    dict(seed=51, num_seqs=4, len_lo=20, len_hi=300, queries_per_seq=16, heads=8, kv_heads=1, causal=True),
+    dict(seed=52, num_seqs=3, len_lo=30, len_hi=200, queries_per_seq=12, heads=8, kv_heads=2, causal=False),
+    dict(seed=53, num_seqs=4, len_lo=40, len_hi=200, queries_per_seq=8, heads=32, kv_heads=1, causal=True,
+         shared_prefix_pages=2),
+    dict(seed=54, num_seqs=5, len_lo=9, len_hi=45, queries_per_seq=5, heads=16, kv_heads=1, causal=True),
+]
+
+
+def mla_dev(c, bd):
     t = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda().to(torch.bfloat16)
-    q, qp, dy, k, kp = t(c.q), t(c.qp), t(c.dy), t(c.k_pool), t(c.kp_pool)
-    table = torch.from_numpy(c.page_table).cuda().contiguous()
-    meta = bd.seq_meta_tensor(c.seq_len, c.q_start, c.q_pos, "cuda")
-    d = bd.make_paged_desc(num_queries=q.shape[0], num_seqs=c.num_seqs, heads=c.heads, kv_heads=c.kv_heads,
-                           page_size=c.page_size, num_pages=k.shape[0] // c.page_size,
-                           max_pages_per_seq=table.shape[1], key_dim=512, value_dim=512, position_dim=64)
-    lse = torch.empty((q.shape[0], c.heads), dtype=torch.float32, device="cuda")
-    delta = torch.empty_like(lse)
-    dq, dqp = torch.empty_like(q), torch.empty_like(qp)
-    ws = torch.empty(max(bd.attn_bwd_paged_workspace_bytes(d), 256), dtype=torch.uint8, device="cuda")
-    p = lambda x: x.data_ptr()
-    st = bd.attn_bwd_paged_query(d, p(q), p(qp), p(k), None, p(kp), p(dy), p(table), p(meta), p(lse), p(delta),
-                                 p(dq), p(dqp), p(ws), ws.numel(), None)
-    assert st == bd.ATTN_ERR_UNSUPPORTED
+    dev = dict(q=t(c.q), qp=t(c.qp), dy=t(c.dy), k=t(c.k_pool), kp=t(c.kp_pool))
+    dev["table"] = torch.from_numpy(c.page_table).cuda().contiguous()
+    dev["meta"] = bd.seq_meta_tensor(c.seq_len, c.q_start, c.q_pos, "cuda")
+    return dev
+
+
+@pytest.mark.parametrize("kw", MLA_CASES, ids=lambda k: f"seed{k['seed']}")
+def test_paged_query_mla_parity(bd, kw):
+    from oracle import paged_query_backward
+    c = inputs.paged_case(name="t", scale=0.5, key_dim=512, value_dim=512, position_dim=64, **kw)
+    dv = mla_dev(c, bd)
+    lse, delta, dq, dqp = bd.paged_query_backward(dv["q"], dv["k"], None, dv["dy"], dv["table"], dv["meta"],
+                                                  heads=c.heads, kv_heads=c.kv_heads, page_size=c.page_size,
+                                                  causal=c.causal, qp=dv["qp"], kp_pool=dv["kp"])
+    bd.check_device_error()
+    ref = paged_query_backward(c.q, c.dy, c.k_pool, c.page_table, c.seq_len, c.q_start, c.q_pos,
+                               page_size=c.page_size, kv_heads=c.kv_heads, qp=c.qp, kp_pool=c.kp_pool,
+                               causal=c.causal)
+    check(lse, delta, dq, ref[:3])
+    assert rel(dqp, ref[3]) < TOL
+    assert torch.isfinite(dqp).all()
+    again = bd.paged_query_backward(dv["q"], dv["k"], None, dv["dy"], dv["table"], dv["meta"], heads=c.heads,
+                                    kv_heads=c.kv_heads, page_size=c.page_size, causal=c.causal, qp=dv["qp"],
+                                    kp_pool=dv["kp"])
+    for a, b in zip((lse, delta, dq, dqp), again):
+        assert torch.equal(a, b)
+
+
+def test_paged_query_mla_unsupported_group(bd):
+    """MLA head groups outside {4, 8, 16, 32} are refused, not computed."""
+    c = inputs.paged_case(name="t", seed=49, num_seqs=2, len_lo=20, len_hi=60, queries_per_seq=4, heads=6,
+                          kv_heads=1, key_dim=512, value_dim=512, position_dim=64, scale=0.5)
+    dv = mla_dev(c, bd)
+    with pytest.raises(bd.AttnError):
+        bd.paged_query_backward(dv["q"], dv["k"], None, dv["dy"], dv["table"], dv["meta"], heads=c.heads,
+                                kv_heads=c.kv_heads, page_size=c.page_size, causal=c.causal, qp=dv["qp"],
+                                kp_pool=dv["kp"])
+
+
+def test_paged_query_full_size_mla_sampled(bd):
+    """The full MLA configuration; sampled sequences against the oracle."""
+    c = inputs.paged_config("paged_mla")
+    dv = mla_dev(c, bd)
+    lse, delta, dq, dqp = bd.paged_query_backward(dv["q"], dv["k"], None, dv["dy"], dv["table"], dv["meta"],
+                                                  heads=c.heads, kv_heads=c.kv_heads, page_size=c.page_size,
+                                                  causal=True, qp=dv["qp"], kp_pool=dv["kp"])
+    bd.check_device_error()
+    from oracle import paged_query_backward
+    pick = [5, 50]
+    qs = [np.arange(c.q_start[s], c.q_start[s + 1]) for s in pick]
+    rows = np.concatenate(qs)
+    sub_start = np.concatenate([[0], np.cumsum([len(x) for x in qs])]).astype(np.int32)
+    ref = paged_query_backward(c.q[rows], c.dy[rows], c.k_pool, c.page_table[pick], c.seq_len[pick], sub_start,
+                               c.q_pos[rows], page_size=c.page_size, kv_heads=c.kv_heads, qp=c.qp[rows],
+                               kp_pool=c.kp_pool, causal=True)
+    check(lse[rows], delta[rows], dq[rows], ref[:3])
+    assert rel(dqp[rows], ref[3]) < TOL
 
 
 def test_paged_query_full_size_gqa_sampled(bd):
