@@ -279,8 +279,9 @@ ATTN_API attn_status_t attn_fwd_dense(const attn_dense_desc* d, const void* q, c
  * row is written exactly once: a row with no visible token, or outside every
  * sequence's query range, gets dq = 0, lse = -inf and delta = 0.  Tokens are
  * visited in a fixed order, so the result is bit-identical from run to run.
- * GQA only: MLA (position_dim > 0) returns ATTN_ERR_UNSUPPORTED.  The
- * workspace is that of attn_bwd_paged (it may be NULL when its size is 0).
+ * MLA (position_dim > 0) needs heads / kv_heads in {4, 8, 16, 32} and page
+ * size 16 (else ATTN_ERR_UNSUPPORTED); qp, kp_pool and dqp are then required.
+ * The workspace is that of attn_bwd_paged.
  */
 ATTN_API attn_status_t attn_bwd_paged_query(const attn_paged_desc* d, const void* q, const void* qp,
                                             const void* k_pool, const void* v_pool, const void* kp_pool,
