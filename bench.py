@@ -389,33 +389,43 @@ def sweep(args) -> int:
               "oracle_s_sample": t_or, "oracle_sample": f"{len(pick)} of {c.num_seqs} sequences",
               "oracle_s_extrapolated": t_or * c.num_seqs / len(pick), "host_cores": cores,
               "peak_source": src})
-        if c.position_dim:
-            continue
-        # query side (row statistics and dQ in one call)
+        # query side (row statistics and dQ, dQp for MLA, in one call)
+        mla = bool(c.position_dim)
         qouts = (torch.empty((c.q.shape[0], c.heads), dtype=torch.float32, device="cuda"),
                  torch.empty((c.q.shape[0], c.heads), dtype=torch.float32, device="cuda"), torch.empty_like(dv["q"]))
+        if mla:
+            qouts = qouts + (torch.empty_like(dv["qp"]),)
         qcall = lambda: bd.paged_query_backward(dv["q"], dv["k"], dv["v"], dv["dy"], table, meta, heads=c.heads,
                                                 kv_heads=c.kv_heads, page_size=c.page_size, causal=c.causal,
-                                                outputs=qouts)
+                                                qp=dv["qp"], kp_pool=dv["kp"], outputs=qouts)
         qcall()
         qfirst = tuple(x.clone() for x in qouts)
         qms, qms_min = timed(qcall, 20)
         qstable = all(torch.equal(a, b) for a, b in zip(qfirst, qouts))
-        qflops = (6 * dk_ + 4 * dvv) * triples  # S twice, O += P V, dP, dQ += dS K
-        qbytes = valid * kvh * (dk_ + dvv) * 2 + c.q.shape[0] * c.heads * (2 * dk_ + dvv) * 2
+        if mla:  # statistics: S (576), dP (512); query: S, dP again, dQ and dQp (576)
+            qflops = (2 * (dk_ + c.position_dim) + 2 * dvv) * 2 * triples + 2 * (dk_ + c.position_dim) * triples
+            qbytes = valid * kvh * (dk_ + c.position_dim) * 2 + c.q.shape[0] * c.heads * (
+                2 * (dk_ + c.position_dim) + dvv) * 2
+            qdesc = "per visible (row, head, token): S and dP twice (576 + 512), dQ and dQp (576)"
+        else:
+            qflops = (6 * dk_ + 4 * dvv) * triples  # S twice, O += P V, dP, dQ += dS K
+            qbytes = valid * kvh * (dk_ + dvv) * 2 + c.q.shape[0] * c.heads * (2 * dk_ + dvv) * 2
+            qdesc = "10*D per visible (row, head, token): S twice, O += P V, dP, dQ += dS K"
         t0 = time.perf_counter()
         qref = paged_query_backward(c.q[rows], c.dy[rows], c.k_pool, c.page_table[pick], c.seq_len[pick], sub,
                                     c.q_pos[rows], page_size=c.page_size, kv_heads=c.kv_heads, v_pool=c.v_pool,
-                                    causal=c.causal)
+                                    qp=None if c.qp is None else c.qp[rows], kp_pool=c.kp_pool, causal=c.causal)
         qt_or = time.perf_counter() - t0
         rsel = torch.from_numpy(rows).cuda()
         qerr = rel(qouts[2].index_select(0, rsel), qref[2])
+        if mla:
+            qerr = max(qerr, rel(qouts[3].index_select(0, rsel), qref[3]))
         emit({"config": tag + " query side", "workload": name, "gpu_ms_median": qms, "gpu_ms_min": qms_min,
               "executed_tflops": qflops / (qms * 1e-3) / 1e12,
               "pct_of_bf16_peak": 100.0 * qflops / (qms * 1e-3) / 1e12 / peaks["bf16_tflops"],
               "algorithmic_gbs": qbytes / (qms * 1e-3) / 1e9,
               "pct_of_hbm_peak": 100.0 * qbytes / (qms * 1e-3) / 1e9 / peaks["hbm_gbs"],
-              "flops_counted": "10*D per visible (row, head, token): S twice, O += P V, dP, dQ += dS K",
+              "flops_counted": qdesc,
               "max_err_rel_dq": qerr, "tolerance": 2e-2, "bit_stable": bool(qstable),
               "oracle_s_sample": qt_or, "oracle_sample": f"{len(pick)} of {c.num_seqs} sequences",
               "host_cores": cores, "peak_source": src})
