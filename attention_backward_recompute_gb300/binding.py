@@ -55,6 +55,14 @@ class attn_dense_desc(ctypes.Structure):
                 ("reserved", ctypes.c_int32)]
 
 
+class attn_strides3(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int64), ("seq", ctypes.c_int64), ("head", ctypes.c_int64)]
+
+
+class attn_dense_strides(ctypes.Structure):
+    _fields_ = [(n, attn_strides3) for n in ("q", "k", "v", "dy", "o", "dq", "dk", "dv")]
+
+
 class attn_paged_desc(ctypes.Structure):
     _fields_ = [("num_queries", ctypes.c_int64), ("num_seqs", ctypes.c_int64), ("heads", ctypes.c_int64),
                 ("kv_heads", ctypes.c_int64), ("page_size", ctypes.c_int64), ("num_pages", ctypes.c_int64),
@@ -72,6 +80,12 @@ _SIG = {
                                         _P, ctypes.c_uint, _P, ctypes.c_size_t, _P]),
     "attn_bwd_dense_noalloc": (ctypes.c_int32, [ctypes.POINTER(attn_dense_desc), _P, _P, _P, _P, _P, _P, _P, _P,
                                                 _P, _P, _P, ctypes.c_uint, _P]),
+    "attn_dense_strides_from_layout": (None, [ctypes.POINTER(attn_dense_desc), ctypes.POINTER(attn_dense_strides)]),
+    "attn_bwd_dense_strided": (ctypes.c_int32, [ctypes.POINTER(attn_dense_desc), ctypes.POINTER(attn_dense_strides),
+                                                _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_uint, _P,
+                                                ctypes.c_size_t, _P]),
+    "attn_fwd_dense_strided": (ctypes.c_int32, [ctypes.POINTER(attn_dense_desc), ctypes.POINTER(attn_dense_strides),
+                                                _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
     "attn_fwd_dense": (ctypes.c_int32, [ctypes.POINTER(attn_dense_desc), _P, _P, _P, _P, _P, _P, _P, _P,
                                         ctypes.c_size_t, _P]),
     "attn_bwd_paged_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(attn_paged_desc)]),
@@ -199,6 +213,11 @@ def _ptr(t):
     return ctypes.c_void_p(t.data_ptr())
 
 
+def _vptr(t):
+    """Pointer of a tensor whose strides are passed alongside (views allowed)."""
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
 def _stream_handle(stream):
     import torch
     s = stream if stream is not None else torch.cuda.current_stream()
@@ -269,11 +288,37 @@ def dense_backward(q, k, v, dy, *, layout="bshd", causal=False, window=None, key
     nbytes = attn_bwd_dense_workspace_bytes(desc)
     if workspace is None:
         workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=q.device)
-    st = attn_bwd_dense(desc, _ptr(q), _ptr(k), _ptr(v), _ptr(dy), _ptr(key_mask), _ptr(bias), _ptr(o), _ptr(lse),
-                        _ptr(dq), _ptr(dk), _ptr(dv), wrt, _ptr(workspace), workspace.numel(),
-                        _stream_handle(stream))
+    tensors = dict(q=q, k=k, v=v, dy=dy, o=o, dq=dq, dk=dk, dv=dv)
+    if all(t is None or t.is_contiguous() for t in tensors.values()):
+        st = attn_bwd_dense(desc, _ptr(q), _ptr(k), _ptr(v), _ptr(dy), _ptr(key_mask), _ptr(bias), _ptr(o),
+                            _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), wrt, _ptr(workspace), workspace.numel(),
+                            _stream_handle(stream))
+    else:  # non-contiguous views: pass their strides
+        sts = _dense_strides(desc, layout, tensors)
+        st = int(lib().attn_bwd_dense_strided(ctypes.byref(desc), ctypes.byref(sts), _vptr(q), _vptr(k), _vptr(v),
+                                              _vptr(dy), _ptr(key_mask), _ptr(bias), _vptr(o), _ptr(lse), _vptr(dq),
+                                              _vptr(dk), _vptr(dv), wrt, _ptr(workspace), workspace.numel(),
+                                              _stream_handle(stream)))
     _check(st)
     return dq, dk, dv
+
+
+def _dense_strides(desc, layout, tensors):
+    """attn_dense_strides from torch tensors' strides (the layout's own for a
+    tensor that is None)."""
+    sts = attn_dense_strides()
+    lib().attn_dense_strides_from_layout(ctypes.byref(desc), ctypes.byref(sts))
+    for name, t in tensors.items():
+        if t is None:
+            continue
+        if t.stride(3) != 1:
+            raise ValueError(f"{name}: the head_dim dimension must be contiguous")
+        st3 = getattr(sts, name)
+        if layout == "bshd":
+            st3.batch, st3.seq, st3.head = t.stride(0), t.stride(1), t.stride(2)
+        else:
+            st3.batch, st3.head, st3.seq = t.stride(0), t.stride(1), t.stride(2)
+    return sts
 
 
 def attn_fwd_dense(desc, q, k, v, key_mask, bias, o, lse, workspace, workspace_bytes, stream) -> int:
@@ -304,8 +349,15 @@ def dense_forward(q, k, v, *, layout="bshd", causal=False, window=None, key_mask
     nbytes = attn_bwd_dense_workspace_bytes(desc)
     if workspace is None:
         workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=q.device)
-    st = attn_fwd_dense(desc, _ptr(q), _ptr(k), _ptr(v), _ptr(key_mask), _ptr(bias), _ptr(o), _ptr(lse),
-                        _ptr(workspace), workspace.numel(), _stream_handle(stream))
+    tensors = dict(q=q, k=k, v=v, o=o)
+    if all(t.is_contiguous() for t in tensors.values()):
+        st = attn_fwd_dense(desc, _ptr(q), _ptr(k), _ptr(v), _ptr(key_mask), _ptr(bias), _ptr(o), _ptr(lse),
+                            _ptr(workspace), workspace.numel(), _stream_handle(stream))
+    else:
+        sts = _dense_strides(desc, layout, tensors)
+        st = int(lib().attn_fwd_dense_strided(ctypes.byref(desc), ctypes.byref(sts), _vptr(q), _vptr(k), _vptr(v),
+                                              _ptr(key_mask), _ptr(bias), _vptr(o), _ptr(lse), _ptr(workspace),
+                                              workspace.numel(), _stream_handle(stream)))
     _check(st)
     return o, lse
 

@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -188,14 +189,100 @@ attn_status_t check_dense_desc(const attn_dense_desc* d, DenseSizes* z) {
   return ATTN_OK;
 }
 
+// Strides of the descriptor's layout ([B,S,H,D] or [B,H,S,D], contiguous).
+void layout_strides(const attn_dense_desc* d, attn_dense_strides* st) {
+  const int64_t H = d->heads, Sq = d->seq_q, Sk = d->seq_k, D = d->head_dim;
+  attn_strides3 q, k;
+  if (d->layout == ATTN_LAYOUT_BSHD) {
+    q = attn_strides3{Sq * H * D, H * D, D};
+    k = attn_strides3{Sk * H * D, H * D, D};
+  } else {
+    q = attn_strides3{H * Sq * D, D, Sq * D};
+    k = attn_strides3{H * Sk * D, D, Sk * D};
+  }
+  st->q = st->dy = st->o = st->dq = q;
+  st->k = st->v = st->dk = st->dv = k;
+}
+
+bool same3(const attn_strides3& a, const attn_strides3& b) {
+  return a.batch == b.batch && a.seq == b.seq && a.head == b.head;
+}
+
+// Bytes from a tensor's base to one past its last element.
+size_t extent_bytes(const attn_strides3& x, int64_t B, int64_t S, int64_t H, int64_t D, size_t es) {
+  if (B == 0 || S == 0 || H == 0 || D == 0) return 0;
+  return size_t((B - 1) * x.batch + (S - 1) * x.seq + (H - 1) * x.head + D) * es;
+}
+
+// Non-negative strides in multiples of 16 bytes (TMA and vector stores need
+// that); for an output also no two (batch, seq, head) rows may share bytes.
+attn_status_t check_strides3(const attn_strides3& x, int64_t B, int64_t S, int64_t H, int64_t D, size_t es,
+                             bool output, const char* name) {
+  const int64_t st[3] = {x.batch, x.seq, x.head}, ex[3] = {B, S, H};
+  for (int i = 0; i < 3; ++i) {
+    if (st[i] < 0) return api_fail(ATTN_ERR_INVALID_ARG, "%s: negative stride", name);
+    if (ex[i] > 1 && (size_t(st[i]) * es) % 16 != 0)
+      return api_fail(ATTN_ERR_UNSUPPORTED, "%s: strides must be multiples of 16 bytes", name);
+  }
+  if (!output) return ATTN_OK;
+  // sorted by stride, each dimension must step past the whole span of the smaller ones
+  int o[3] = {0, 1, 2};
+  for (int i = 0; i < 3; ++i)
+    for (int j = i + 1; j < 3; ++j)
+      if (st[o[j]] < st[o[i]]) std::swap(o[i], o[j]);
+  int64_t span = D;
+  for (int i = 0; i < 3; ++i) {
+    if (ex[o[i]] <= 1) continue;
+    if (st[o[i]] < span) return api_fail(ATTN_ERR_INVALID_ARG, "%s: strides make rows overlap", name);
+    span = st[o[i]] * ex[o[i]];
+  }
+  return ATTN_OK;
+}
+
+// Whether two strided [B, S, H, D] tensors share a byte.  Disjoint byte
+// ranges never do; two views with the same strides (e.g. q, k, v slices of
+// one fused tensor) are tested exactly: they overlap when the distance of
+// their bases is within D elements of some difference of row offsets
+// sum_i k_i * stride_i, |k_i| < extent_i, which for strides that each step
+// past the smaller dimensions' span is found by trying the two nearest k at
+// every dimension from the largest stride down.  Other pairs count as
+// overlapping when their byte ranges do.
+bool strided_overlap(const void* a, const attn_strides3& sa, size_t xa, const void* b, const attn_strides3& sb,
+                     size_t xb, int64_t B, int64_t S, int64_t H, int64_t D, size_t es) {
+  if (!ranges_overlap(a, xa, b, xb)) return false;
+  if (!same3(sa, sb)) return true;
+  const int64_t diff = int64_t(reinterpret_cast<uintptr_t>(b)) - int64_t(reinterpret_cast<uintptr_t>(a));
+  if (diff % int64_t(es) != 0) return true;
+  int64_t st[3] = {sa.batch, sa.seq, sa.head}, n[3] = {B, S, H};
+  for (int i = 0; i < 3; ++i)
+    for (int j = i + 1; j < 3; ++j)
+      if (st[j] > st[i]) std::swap(st[i], st[j]), std::swap(n[i], n[j]);
+  struct F {
+    const int64_t *st, *n;
+    int64_t D;
+    bool go(int i, int64_t rem) const {
+      if (i == 3) return rem > -D && rem < D;
+      if (n[i] <= 1 || st[i] == 0) return go(i + 1, rem);
+      int64_t k = rem >= 0 ? rem / st[i] : -((-rem + st[i] - 1) / st[i]);
+      for (int64_t kk = k; kk <= k + 1; ++kk) {
+        const int64_t kc = std::max(-(n[i] - 1), std::min(n[i] - 1, kk));
+        if (go(i + 1, rem - kc * st[i])) return true;
+      }
+      return false;
+    }
+  } f{st, n, D};
+  return f.go(0, diff / int64_t(es));
+}
+
 // Kernel parameters, the hi/lo copy buffers of fp32 storage and the TMA
 // descriptors shared by the backward and the forward export.  dy may be NULL
 // (forward): its maps and copies then alias those of q.  split_hi / split_lo
 // receive the copy buffers of q, dy, k, v (fp32 storage; else the inputs).
-attn_status_t prepare_dense(const attn_dense_desc* d, const DenseSizes& z, const void* q, const void* k,
-                            const void* v, const void* dy, const float* key_mask, const void* bias, const void* o,
-                            const float* lse, void* dq, void* dk, void* dv, void* workspace, attn::DenseParams* pp,
-                            attn::DenseMaps* mp, void* split_hi[4], void* split_lo[4]) {
+attn_status_t prepare_dense(const attn_dense_desc* d, const attn_dense_strides& st, const DenseSizes& z,
+                            const void* q, const void* k, const void* v, const void* dy, const float* key_mask,
+                            const void* bias, const void* o, const float* lse, void* dq, void* dk, void* dv,
+                            void* workspace, attn::DenseParams* pp, attn::DenseMaps* mp, void* split_hi[4],
+                            void* split_lo[4]) {
   const int64_t B = d->batch, H = d->heads, Sq = d->seq_q, Sk = d->seq_k, D = d->head_dim;
   const bool has_km = (d->mask_flags & ATTN_MASK_KEY) != 0;
   const bool has_bias = (d->mask_flags & ATTN_MASK_BIAS) != 0;
@@ -219,13 +306,18 @@ attn_status_t prepare_dense(const attn_dense_desc* d, const DenseSizes& z, const
   p.pm = reinterpret_cast<float*>(ws + 2 * align256(z.stat_bytes));
   p.o = o; p.lse = lse; p.dy = dy;
   p.dq = dq; p.dk = dk; p.dv = dv;
-  if (d->layout == ATTN_LAYOUT_BSHD) {
-    p.q_ss = H * D; p.q_sh = D; p.q_sb = Sq * H * D;
-    p.k_ss = H * D; p.k_sh = D; p.k_sb = Sk * H * D;
-  } else {
-    p.q_ss = D; p.q_sh = Sq * D; p.q_sb = H * Sq * D;
-    p.k_ss = D; p.k_sh = Sk * D; p.k_sb = H * Sk * D;
-  }
+  p.q_ss = st.q.seq; p.q_sh = st.q.head; p.q_sb = st.q.batch;
+  p.k_ss = st.k.seq; p.k_sh = st.k.head; p.k_sb = st.k.batch;
+  auto put = [](int64_t (&dst)[3], const attn_strides3& x) {
+    dst[0] = x.seq;
+    dst[1] = x.head;
+    dst[2] = x.batch;
+  };
+  put(p.s_dy, st.dy);
+  put(p.s_o, st.o);
+  put(p.s_dq, st.dq);
+  put(p.s_dk, st.dk);
+  put(p.s_dv, st.dv);
   p.err = device_error_word();
   if (!p.err) return api_fail(ATTN_ERR_CUDA, "no CUDA device / symbol address unavailable");
 
@@ -251,21 +343,26 @@ attn_status_t prepare_dense(const attn_dense_desc* d, const DenseSizes& z, const
   const uint64_t es = 2;  // the tensor-core operands are always bf16
   const uint64_t qdims[4] = {uint64_t(D), uint64_t(Sq), uint64_t(H), uint64_t(B)};
   const uint64_t kdims[4] = {uint64_t(D), uint64_t(Sk), uint64_t(H), uint64_t(B)};
-  const uint64_t qstr[3] = {uint64_t(p.q_ss) * es, uint64_t(p.q_sh) * es, uint64_t(p.q_sb) * es};
-  const uint64_t kstr[3] = {uint64_t(p.k_ss) * es, uint64_t(p.k_sh) * es, uint64_t(p.k_sb) * es};
+  // (the hi/lo copies of fp32 storage keep the inputs' strides: those are
+  // the layout's own there)
+  const uint64_t qstr[3] = {uint64_t(st.q.seq) * es, uint64_t(st.q.head) * es, uint64_t(st.q.batch) * es};
+  const uint64_t kstr[3] = {uint64_t(st.k.seq) * es, uint64_t(st.k.head) * es, uint64_t(st.k.batch) * es};
+  const uint64_t vstr[3] = {uint64_t(st.v.seq) * es, uint64_t(st.v.head) * es, uint64_t(st.v.batch) * es};
+  const attn_strides3& dys = dy ? st.dy : st.q;
+  const uint64_t dystr[3] = {uint64_t(dys.seq) * es, uint64_t(dys.head) * es, uint64_t(dys.batch) * es};
   attn::DenseMaps& m = *mp;
   std::memset(&m, 0, sizeof(m));
   m.split = split;
   bool enc = encode4d(&m.q64, dt, qa, qdims, qstr, 64, 64) && encode4d(&m.q128, dt, qa, qdims, qstr, 64, 128) &&
-             encode4d(&m.dy64, dt, dya, qdims, qstr, 64, 64) && encode4d(&m.dy128, dt, dya, qdims, qstr, 64, 128) &&
+             encode4d(&m.dy64, dt, dya, qdims, dystr, 64, 64) && encode4d(&m.dy128, dt, dya, qdims, dystr, 64, 128) &&
              encode4d(&m.k64, dt, ka, kdims, kstr, 64, 64) && encode4d(&m.k128, dt, ka, kdims, kstr, 64, 128) &&
-             encode4d(&m.v64, dt, va, kdims, kstr, 64, 64) && encode4d(&m.v128, dt, va, kdims, kstr, 64, 128);
+             encode4d(&m.v64, dt, va, kdims, vstr, 64, 64) && encode4d(&m.v128, dt, va, kdims, vstr, 64, 128);
   if (enc && split) {
     enc = encode4d(&m.q64_lo, dt, ql, qdims, qstr, 64, 64) && encode4d(&m.q128_lo, dt, ql, qdims, qstr, 64, 128) &&
-          encode4d(&m.dy64_lo, dt, dyl, qdims, qstr, 64, 64) &&
-          encode4d(&m.dy128_lo, dt, dyl, qdims, qstr, 64, 128) && encode4d(&m.k64_lo, dt, kl, kdims, kstr, 64, 64) &&
-          encode4d(&m.k128_lo, dt, kl, kdims, kstr, 64, 128) && encode4d(&m.v64_lo, dt, vl, kdims, kstr, 64, 64) &&
-          encode4d(&m.v128_lo, dt, vl, kdims, kstr, 64, 128);
+          encode4d(&m.dy64_lo, dt, dyl, qdims, dystr, 64, 64) &&
+          encode4d(&m.dy128_lo, dt, dyl, qdims, dystr, 64, 128) && encode4d(&m.k64_lo, dt, kl, kdims, kstr, 64, 64) &&
+          encode4d(&m.k128_lo, dt, kl, kdims, kstr, 64, 128) && encode4d(&m.v64_lo, dt, vl, kdims, vstr, 64, 64) &&
+          encode4d(&m.v128_lo, dt, vl, kdims, vstr, 64, 128);
   } else if (enc) {
     m.q64_lo = m.q64; m.q128_lo = m.q128; m.dy64_lo = m.dy64; m.dy128_lo = m.dy128;
     m.k64_lo = m.k64; m.k128_lo = m.k128; m.v64_lo = m.v64; m.v128_lo = m.v128;
@@ -301,13 +398,31 @@ ATTN_API size_t attn_bwd_dense_workspace_bytes(const attn_dense_desc* d) {
   return z.ws_bytes;
 }
 
+ATTN_API void attn_dense_strides_from_layout(const attn_dense_desc* d, attn_dense_strides* st) {
+  if (d && st) layout_strides(d, st);
+}
+
 ATTN_API attn_status_t attn_bwd_dense(const attn_dense_desc* d, const void* q, const void* k, const void* v,
                                       const void* dy, const float* key_mask, const void* bias, const void* o,
                                       const float* lse, void* dq, void* dk, void* dv, unsigned wrt_mask,
                                       void* workspace, size_t workspace_bytes, void* stream) {
+  if (!d) return api_fail(ATTN_ERR_INVALID_ARG, "descriptor is NULL");
+  attn_dense_strides sts;
+  layout_strides(d, &sts);
+  return attn_bwd_dense_strided(d, &sts, q, k, v, dy, key_mask, bias, o, lse, dq, dk, dv, wrt_mask, workspace,
+                                workspace_bytes, stream);
+}
+
+ATTN_API attn_status_t attn_bwd_dense_strided(const attn_dense_desc* d, const attn_dense_strides* sts, const void* q,
+                                              const void* k, const void* v, const void* dy, const float* key_mask,
+                                              const void* bias, const void* o, const float* lse, void* dq, void* dk,
+                                              void* dv, unsigned wrt_mask, void* workspace, size_t workspace_bytes,
+                                              void* stream) {
   DenseSizes z;
   attn_status_t st = check_dense_desc(d, &z);
   if (st != ATTN_OK) return st;
+  if (!sts) return api_fail(ATTN_ERR_INVALID_ARG, "strides are NULL");
+  const attn_dense_strides& S3 = *sts;
   if (wrt_mask == 0 || (wrt_mask & ~7u)) return api_fail(ATTN_ERR_INVALID_ARG, "wrt_mask must be a non-empty subset of dQ|dK|dV");
   const bool has_km = (d->mask_flags & ATTN_MASK_KEY) != 0;
   const bool has_bias = (d->mask_flags & ATTN_MASK_BIAS) != 0;
@@ -317,8 +432,24 @@ ATTN_API attn_status_t attn_bwd_dense(const attn_dense_desc* d, const void* q, c
   const bool want_dq = wrt_mask & ATTN_WRT_DQ, want_dk = wrt_mask & ATTN_WRT_DK, want_dv = wrt_mask & ATTN_WRT_DV;
   if ((want_dq && !dq && z.q_bytes) || (want_dk && !dk && z.k_bytes) || (want_dv && !dv && z.k_bytes))
     return api_fail(ATTN_ERR_INVALID_ARG, "requested gradient pointer is NULL");
-  const int64_t B = d->batch, H = d->heads, Sq = d->seq_q, Sk = d->seq_k;
+  const int64_t B = d->batch, H = d->heads, Sq = d->seq_q, Sk = d->seq_k, D = d->head_dim;
   const bool empty_q = B * H * Sq == 0, empty_k = B * H * Sk == 0;
+  {
+    const struct { const attn_strides3* x; int64_t S; bool out; const char* n; } chk[] = {
+        {&S3.q, Sq, false, "q"}, {&S3.k, Sk, false, "k"}, {&S3.v, Sk, false, "v"}, {&S3.dy, Sq, false, "dy"},
+        {&S3.o, Sq, false, "o"}, {&S3.dq, Sq, true, "dq"}, {&S3.dk, Sk, true, "dk"}, {&S3.dv, Sk, true, "dv"}};
+    for (const auto& c : chk)
+      if ((st = check_strides3(*c.x, B, c.S, H, D, z.es, c.out, c.n)) != ATTN_OK) return st;
+    attn_dense_strides lay;
+    layout_strides(d, &lay);
+    if (d->dtype == ATTN_DTYPE_F32 &&
+        !(same3(S3.q, lay.q) && same3(S3.k, lay.k) && same3(S3.v, lay.v) && same3(S3.dy, lay.dy)))
+      return api_fail(ATTN_ERR_UNSUPPORTED, "fp32 storage needs q, k, v, dy in the descriptor's layout");
+  }
+  const size_t xq = extent_bytes(S3.q, B, Sq, H, D, z.es), xk = extent_bytes(S3.k, B, Sk, H, D, z.es),
+               xv = extent_bytes(S3.v, B, Sk, H, D, z.es), xdy = extent_bytes(S3.dy, B, Sq, H, D, z.es),
+               xo = extent_bytes(S3.o, B, Sq, H, D, z.es), xdq = extent_bytes(S3.dq, B, Sq, H, D, z.es),
+               xdk = extent_bytes(S3.dk, B, Sk, H, D, z.es), xdv = extent_bytes(S3.dv, B, Sk, H, D, z.es);
   // required inputs (only when they have elements)
   if (!empty_q && (!q || !dy)) return api_fail(ATTN_ERR_INVALID_ARG, "q/dy is NULL");
   if (!empty_k && (!k || !v)) return api_fail(ATTN_ERR_INVALID_ARG, "k/v is NULL");
@@ -328,22 +459,37 @@ ATTN_API attn_status_t attn_bwd_dense(const attn_dense_desc* d, const void* q, c
   if (has_bias && (Sk * z.es) % 16 != 0) return api_fail(ATTN_ERR_UNSUPPORTED, "bias needs Sk * element size to be a multiple of 16");
   // aliasing: no output may overlap an input, the workspace or another output
   struct R { const void* p; size_t n; };
-  const R ins[] = {{q, z.q_bytes}, {k, z.k_bytes}, {v, z.k_bytes}, {dy, z.q_bytes}, {key_mask, has_km ? z.mask_bytes : 0},
-                   {bias, has_bias ? z.bias_bytes : 0}, {o, o ? z.q_bytes : 0}, {lse, lse ? z.stat_bytes : 0},
-                   {workspace, workspace_bytes}};
-  const R outs[] = {{want_dq ? dq : nullptr, z.q_bytes}, {want_dk ? dk : nullptr, z.k_bytes}, {want_dv ? dv : nullptr, z.k_bytes}};
+  // plain inputs (contiguous) by byte range; strided tensors against each other exactly
+  const R ins[] = {{key_mask, has_km ? z.mask_bytes : 0}, {bias, has_bias ? z.bias_bytes : 0},
+                   {lse, lse ? z.stat_bytes : 0}, {workspace, workspace_bytes}};
+  struct T { const void* p; const attn_strides3* s; size_t n; int64_t S; };
+  const T tin[] = {{q, &S3.q, xq, Sq}, {k, &S3.k, xk, Sk}, {v, &S3.v, xv, Sk}, {dy, &S3.dy, xdy, Sq},
+                   {o, &S3.o, o ? xo : 0, Sq}};
+  const T tout[] = {{want_dq ? dq : nullptr, &S3.dq, xdq, Sq}, {want_dk ? dk : nullptr, &S3.dk, xdk, Sk},
+                    {want_dv ? dv : nullptr, &S3.dv, xdv, Sk}};
   for (int i = 0; i < 3; ++i) {
+    const T& w = tout[i];
     for (const R& r : ins)
-      if (ranges_overlap(outs[i].p, outs[i].n, r.p, r.n)) return api_fail(ATTN_ERR_ALIAS, "output %d overlaps an input or the workspace", i);
-    for (int j = i + 1; j < 3; ++j)
-      if (ranges_overlap(outs[i].p, outs[i].n, outs[j].p, outs[j].n)) return api_fail(ATTN_ERR_ALIAS, "outputs %d and %d overlap", i, j);
+      if (ranges_overlap(w.p, w.n, r.p, r.n)) return api_fail(ATTN_ERR_ALIAS, "output %d overlaps an input or the workspace", i);
+    for (const T& r : tin)  // (S differs between the q- and k-shaped tensors: the byte test then decides)
+      if (r.S == w.S ? strided_overlap(w.p, *w.s, w.n, r.p, *r.s, r.n, B, w.S, H, D, z.es)
+                     : ranges_overlap(w.p, w.n, r.p, r.n))
+        return api_fail(ATTN_ERR_ALIAS, "output %d overlaps an input", i);
+    for (int j = i + 1; j < 3; ++j) {
+      const T& u = tout[j];
+      if (u.S == w.S ? strided_overlap(w.p, *w.s, w.n, u.p, *u.s, u.n, B, w.S, H, D, z.es)
+                     : ranges_overlap(w.p, w.n, u.p, u.n))
+        return api_fail(ATTN_ERR_ALIAS, "outputs %d and %d overlap", i, j);
+    }
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // zero-size problems: zero the selected gradients that have elements
   if (empty_q || empty_k) {
-    if (want_dq && z.q_bytes && cudaMemsetAsync(dq, 0, z.q_bytes, s) != cudaSuccess) return api_fail(ATTN_ERR_CUDA, "memset failed");
-    if (want_dk && z.k_bytes && cudaMemsetAsync(dk, 0, z.k_bytes, s) != cudaSuccess) return api_fail(ATTN_ERR_CUDA, "memset failed");
-    if (want_dv && z.k_bytes && cudaMemsetAsync(dv, 0, z.k_bytes, s) != cudaSuccess) return api_fail(ATTN_ERR_CUDA, "memset failed");
+    cudaError_t e = cudaSuccess;
+    if (want_dq && e == cudaSuccess) e = attn::launch_zero_rows(dq, S3.dq.batch, S3.dq.seq, S3.dq.head, B, Sq, H, D, z.es, s);
+    if (want_dk && e == cudaSuccess) e = attn::launch_zero_rows(dk, S3.dk.batch, S3.dk.seq, S3.dk.head, B, Sk, H, D, z.es, s);
+    if (want_dv && e == cudaSuccess) e = attn::launch_zero_rows(dv, S3.dv.batch, S3.dv.seq, S3.dv.head, B, Sk, H, D, z.es, s);
+    if (e != cudaSuccess) return api_fail(ATTN_ERR_CUDA, "zero fill failed: %s", cudaGetErrorString(e));
     return api_ok();
   }
   if (!workspace || workspace_bytes < z.ws_bytes)
@@ -355,7 +501,7 @@ ATTN_API attn_status_t attn_bwd_dense(const attn_dense_desc* d, const void* q, c
   attn::DenseMaps m;
   void* his[4];
   void* los[4];
-  if ((st = prepare_dense(d, z, q, k, v, dy, key_mask, bias, o, lse, dq, dk, dv, workspace, &p, &m, his, los)) !=
+  if ((st = prepare_dense(d, S3, z, q, k, v, dy, key_mask, bias, o, lse, dq, dk, dv, workspace, &p, &m, his, los)) !=
       ATTN_OK)
     return st;
   p.wrt = wrt_mask;
@@ -393,15 +539,39 @@ ATTN_API attn_status_t attn_bwd_dense(const attn_dense_desc* d, const void* q, c
 ATTN_API attn_status_t attn_fwd_dense(const attn_dense_desc* d, const void* q, const void* k, const void* v,
                                       const float* key_mask, const void* bias, void* o, float* lse, void* workspace,
                                       size_t workspace_bytes, void* stream) {
+  if (!d) return api_fail(ATTN_ERR_INVALID_ARG, "descriptor is NULL");
+  attn_dense_strides sts;
+  layout_strides(d, &sts);
+  return attn_fwd_dense_strided(d, &sts, q, k, v, key_mask, bias, o, lse, workspace, workspace_bytes, stream);
+}
+
+ATTN_API attn_status_t attn_fwd_dense_strided(const attn_dense_desc* d, const attn_dense_strides* sts, const void* q,
+                                              const void* k, const void* v, const float* key_mask, const void* bias,
+                                              void* o, float* lse, void* workspace, size_t workspace_bytes,
+                                              void* stream) {
   DenseSizes z;
   attn_status_t st = check_dense_desc(d, &z);
   if (st != ATTN_OK) return st;
+  if (!sts) return api_fail(ATTN_ERR_INVALID_ARG, "strides are NULL");
+  const attn_dense_strides& S3 = *sts;
   const bool has_km = (d->mask_flags & ATTN_MASK_KEY) != 0;
   const bool has_bias = (d->mask_flags & ATTN_MASK_BIAS) != 0;
   if (has_km != (key_mask != nullptr)) return api_fail(ATTN_ERR_INVALID_ARG, "key_mask must be given iff ATTN_MASK_KEY is set");
   if (has_bias != (bias != nullptr)) return api_fail(ATTN_ERR_INVALID_ARG, "bias must be given iff ATTN_MASK_BIAS is set");
-  const int64_t B = d->batch, H = d->heads, Sq = d->seq_q, Sk = d->seq_k;
+  const int64_t B = d->batch, H = d->heads, Sq = d->seq_q, Sk = d->seq_k, D = d->head_dim;
   const bool empty_q = B * H * Sq == 0, empty_k = B * H * Sk == 0;
+  {
+    const struct { const attn_strides3* x; int64_t S; bool out; const char* n; } chk[] = {
+        {&S3.q, Sq, false, "q"}, {&S3.k, Sk, false, "k"}, {&S3.v, Sk, false, "v"}, {&S3.o, Sq, true, "o"}};
+    for (const auto& c : chk)
+      if ((st = check_strides3(*c.x, B, c.S, H, D, z.es, c.out, c.n)) != ATTN_OK) return st;
+    attn_dense_strides lay;
+    layout_strides(d, &lay);
+    if (d->dtype == ATTN_DTYPE_F32 && !(same3(S3.q, lay.q) && same3(S3.k, lay.k) && same3(S3.v, lay.v)))
+      return api_fail(ATTN_ERR_UNSUPPORTED, "fp32 storage needs q, k, v in the descriptor's layout");
+  }
+  const size_t xq = extent_bytes(S3.q, B, Sq, H, D, z.es), xk = extent_bytes(S3.k, B, Sk, H, D, z.es),
+               xv = extent_bytes(S3.v, B, Sk, H, D, z.es), xo = extent_bytes(S3.o, B, Sq, H, D, z.es);
   if (!empty_q && (!q || !o || !lse)) return api_fail(ATTN_ERR_INVALID_ARG, "q/o/lse is NULL");
   if (!empty_k && (!k || !v)) return api_fail(ATTN_ERR_INVALID_ARG, "k/v is NULL");
   const void* ptrs[] = {q, k, v, key_mask, bias, o, lse, workspace};
@@ -409,18 +579,19 @@ ATTN_API attn_status_t attn_fwd_dense(const attn_dense_desc* d, const void* q, c
     if (p && !aligned16(p)) return api_fail(ATTN_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
   if (has_bias && (Sk * z.es) % 16 != 0) return api_fail(ATTN_ERR_UNSUPPORTED, "bias needs Sk * element size to be a multiple of 16");
   struct R { const void* p; size_t n; };
-  const R ins[] = {{q, z.q_bytes}, {k, z.k_bytes}, {v, z.k_bytes}, {key_mask, has_km ? z.mask_bytes : 0},
+  const R ins[] = {{q, xq}, {k, xk}, {v, xv}, {key_mask, has_km ? z.mask_bytes : 0},
                    {bias, has_bias ? z.bias_bytes : 0}, {workspace, workspace_bytes}};
-  const R outs[] = {{o, z.q_bytes}, {lse, z.stat_bytes}};
+  const R outs[] = {{o, xo}, {lse, z.stat_bytes}};
   for (const R& w : outs)
     for (const R& r : ins)
       if (ranges_overlap(w.p, w.n, r.p, r.n)) return api_fail(ATTN_ERR_ALIAS, "an output overlaps an input or the workspace");
-  if (ranges_overlap(o, z.q_bytes, lse, z.stat_bytes)) return api_fail(ATTN_ERR_ALIAS, "o and lse overlap");
+  if (ranges_overlap(o, xo, lse, z.stat_bytes)) return api_fail(ATTN_ERR_ALIAS, "o and lse overlap");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (empty_q) return api_ok();
   if (empty_k) {  // no key: O = 0, lse = -inf
-    if (cudaMemsetAsync(o, 0, z.q_bytes, s) != cudaSuccess) return api_fail(ATTN_ERR_CUDA, "memset failed");
-    cudaError_t e = attn::launch_fill_f32(lse, -std::numeric_limits<float>::infinity(), int64_t(z.stat_bytes / 4), s);
+    cudaError_t e = attn::launch_zero_rows(o, S3.o.batch, S3.o.seq, S3.o.head, B, Sq, H, D, z.es, s);
+    if (e == cudaSuccess)
+      e = attn::launch_fill_f32(lse, -std::numeric_limits<float>::infinity(), int64_t(z.stat_bytes / 4), s);
     if (e != cudaSuccess) return api_fail(ATTN_ERR_CUDA, "fill failed: %s", cudaGetErrorString(e));
     return api_ok();
   }
@@ -432,7 +603,7 @@ ATTN_API attn_status_t attn_fwd_dense(const attn_dense_desc* d, const void* q, c
   attn::DenseMaps m;
   void* his[4];
   void* los[4];
-  if ((st = prepare_dense(d, z, q, k, v, nullptr, key_mask, bias, nullptr, nullptr, nullptr, nullptr, nullptr,
+  if ((st = prepare_dense(d, S3, z, q, k, v, nullptr, key_mask, bias, nullptr, nullptr, nullptr, nullptr, nullptr,
                           workspace, &p, &m, his, los)) != ATTN_OK)
     return st;
   p.fwd_only = 1;

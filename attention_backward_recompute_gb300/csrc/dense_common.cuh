@@ -34,8 +34,10 @@ struct DenseParams {
   void* dq;
   void* dk;
   void* dv;
-  int64_t q_ss, q_sh, q_sb;   // strides of q / dy / o / dq
-  int64_t k_ss, k_sh, k_sb;   // strides of k / v / dk / dv
+  int64_t q_ss, q_sh, q_sb;   // element strides (sequence, head, batch) of q
+  int64_t k_ss, k_sh, k_sb;   // ... of k
+  // ... of the other tensors the kernels address directly, {s, h, b} each
+  int64_t s_dy[3], s_o[3], s_dq[3], s_dk[3], s_dv[3];
   unsigned wrt;               // ATTN_WRT_* bits
   // Forward export (the row-statistics sweep run as a forward pass): when
   // fwd_only is set there is no dY and no delta; o_out (q's layout and dtype)

@@ -305,8 +305,9 @@ __global__ void __launch_bounds__(384, 1)
     // a tile no query sees gets zeros.
     const bool want = wg == 0 ? (p.wrt & 4u) != 0 : (p.wrt & 2u) != 0;
     if (want && (ok || n == 0)) {
-      const int64_t roff = static_cast<int64_t>(b) * p.k_sb + static_cast<int64_t>(h) * p.k_sh +
-                           static_cast<int64_t>(key) * p.k_ss;
+      const int64_t* so = wg == 0 ? p.s_dv : p.s_dk;
+      const int64_t roff = static_cast<int64_t>(b) * so[2] + static_cast<int64_t>(h) * so[1] +
+                           static_cast<int64_t>(key) * so[0];
       void* out = wg == 0 ? p.dv : p.dk;
       const float f = wg == 0 ? 1.f : p.scale;
       const uint32_t tacc = (wg == 0 ? t_dv : t_dk) + lane_addr;

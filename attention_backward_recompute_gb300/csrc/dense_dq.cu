@@ -289,8 +289,8 @@ __global__ void __launch_bounds__(384, 1)
     // ------------------------------------------------------------ epilogue
     // each warpgroup writes half of the dQ row (times the softmax scale)
     if ((p.wrt & 1u) && (ok || n == 0)) {
-      const int64_t roff = static_cast<int64_t>(b) * p.q_sb + static_cast<int64_t>(h) * p.q_sh +
-                           static_cast<int64_t>(q) * p.q_ss;
+      const int64_t roff = static_cast<int64_t>(b) * p.s_dq[2] + static_cast<int64_t>(h) * p.s_dq[1] +
+                           static_cast<int64_t>(q) * p.s_dq[0];
       const int half = DP / 2;
 #pragma unroll 1
       for (int cc = wg * half / 32; cc < (wg + 1) * half / 32 && cc * 32 < p.D; ++cc) {

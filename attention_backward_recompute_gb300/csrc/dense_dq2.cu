@@ -418,8 +418,8 @@ __global__ void __launch_bounds__(512, 1)
     // ------------------------------------------------------------ epilogue
     // each softmax group stores half of the dQ row (times the softmax scale)
     if (softmax_wg && (p.wrt & 1u) && (ok || n == 0)) {
-      const int64_t roff = static_cast<int64_t>(b) * p.q_sb + static_cast<int64_t>(h) * p.q_sh +
-                           static_cast<int64_t>(q) * p.q_ss;
+      const int64_t roff = static_cast<int64_t>(b) * p.s_dq[2] + static_cast<int64_t>(h) * p.s_dq[1] +
+                           static_cast<int64_t>(q) * p.s_dq[0];
 #pragma unroll 1
       for (int cc = sg * (DP / 64); cc < (sg + 1) * (DP / 64) && cc * 32 < p.D; ++cc) {
         uint32_t r[32];

@@ -318,8 +318,8 @@ __global__ void __launch_bounds__(256, 1)
     }
     float L2 = kInf, dl = 0.f, pm = 0.f;
     // forward export: O / l in the storage dtype (rows of the tile that exist)
-    const int64_t o_row = static_cast<int64_t>(b) * p.q_sb + static_cast<int64_t>(h) * p.q_sh +
-                          static_cast<int64_t>(q) * p.q_ss;
+    const int64_t o_row = static_cast<int64_t>(b) * p.s_o[2] + static_cast<int64_t>(h) * p.s_o[1] +
+                          static_cast<int64_t>(q) * p.s_o[0];
     if (ok && n > 0) {
       ok = mbar_wait_warp(&bar_p_free[(n - 1) & 1], ((n - 1) >> 1) & 1, ab);
       if (ok && !p.fwd_only) ok = mbar_wait_warp(&bar_dy, 0, ab);
@@ -422,9 +422,8 @@ __global__ void __launch_bounds__(256) delta_only_kernel(const DenseParams p) {
     const int q = static_cast<int>(r % p.Sq);
     const int64_t bh = r / p.Sq;
     const int h = static_cast<int>(bh % p.H), b = static_cast<int>(bh / p.H);
-    const int64_t off = b * p.q_sb + h * p.q_sh + static_cast<int64_t>(q) * p.q_ss;
-    const T* dy = reinterpret_cast<const T*>(p.dy) + off;
-    const T* o = reinterpret_cast<const T*>(p.o) + off;
+    const T* dy = reinterpret_cast<const T*>(p.dy) + b * p.s_dy[2] + h * p.s_dy[1] + static_cast<int64_t>(q) * p.s_dy[0];
+    const T* o = reinterpret_cast<const T*>(p.o) + b * p.s_o[2] + h * p.s_o[1] + static_cast<int64_t>(q) * p.s_o[0];
     float acc = 0.f;
     for (int d = lane; d < p.D; d += 32) acc = fmaf(static_cast<float>(dy[d]), static_cast<float>(o[d]), acc);
 #pragma unroll
@@ -470,6 +469,27 @@ __global__ void fill_f32_kernel(float* x, float value, int64_t n) {
     x[i] = value;
 }
 }  // namespace
+
+namespace {
+// zero D elements of es bytes at every (b, s, h) row of a strided tensor
+__global__ void zero_rows_kernel(uint8_t* x, int64_t sb, int64_t ss, int64_t sh, int64_t B, int64_t S, int64_t H,
+                                 int64_t D, int64_t es) {
+  const int64_t rows = B * S * H, row_bytes = D * es;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < rows * row_bytes;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t r = i / row_bytes, byte = i - r * row_bytes;
+    const int64_t h = r % H, sq = (r / H) % S, b = r / (H * S);
+    x[(b * sb + sq * ss + h * sh) * es + byte] = 0;
+  }
+}
+}  // namespace
+
+cudaError_t launch_zero_rows(void* x, int64_t sb, int64_t ss, int64_t sh, int64_t B, int64_t S, int64_t H, int64_t D,
+                             size_t es, cudaStream_t s) {
+  if (!x || B * S * H * D == 0) return cudaSuccess;
+  zero_rows_kernel<<<152 * 4, 256, 0, s>>>(static_cast<uint8_t*>(x), sb, ss, sh, B, S, H, D, int64_t(es));
+  return cudaGetLastError();
+}
 
 cudaError_t launch_fill_f32(float* x, float value, int64_t n, cudaStream_t s) {
   if (n <= 0) return cudaSuccess;

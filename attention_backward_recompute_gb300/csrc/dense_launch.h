@@ -31,6 +31,9 @@ cudaError_t launch_fwd_stats(const DenseMaps& m, const DenseParams& p, bool bias
 cudaError_t launch_stats2(const DenseMaps& m, const DenseParams& p, bool bias, cudaStream_t s);
 // x[0, n) = value
 cudaError_t launch_fill_f32(float* x, float value, int64_t n, cudaStream_t s);
+// zero the D elements (es bytes each) of every (b, s, h) row of a strided tensor
+cudaError_t launch_zero_rows(void* x, int64_t sb, int64_t ss, int64_t sh, int64_t B, int64_t S, int64_t H, int64_t D,
+                             size_t es, cudaStream_t s);
 cudaError_t launch_delta_only(const DenseParams& p, int dtype_bf16, cudaStream_t s);
 // Split fp32 tensors into hi/lo bf16 copies: hi = bf16(x), lo = bf16(x - hi).
 cudaError_t launch_split_f32(const float* x, void* hi, void* lo, int64_t n, cudaStream_t s);

@@ -246,6 +246,43 @@ ATTN_API attn_status_t attn_paged_row_stats(const attn_paged_desc* d, const void
                                             void* stream);
 
 /*
+ * General strides.  Element strides of the batch, sequence and head
+ * dimensions of one [B, S, H, D] tensor (any order in memory); its head_dim
+ * dimension is contiguous.  Strides are non-negative multiples of 16 bytes;
+ * an output's strides must not make two (batch, seq, head) rows share bytes
+ * (an input's may, e.g. a key tensor shared by all heads with head stride 0).
+ * rlx-wgpu attention_bwd.wgsl passes per-tensor batch, head and sequence
+ * strides in its Params block; this is the same freedom.
+ */
+typedef struct attn_strides3 {
+  int64_t batch, seq, head;
+} attn_strides3;
+
+typedef struct attn_dense_strides {
+  attn_strides3 q, k, v, dy, o, dq, dk, dv;  /* o: the O input (backward) or output (forward) */
+} attn_dense_strides;
+
+/* The strides of the descriptor's layout (what attn_bwd_dense uses). */
+ATTN_API void attn_dense_strides_from_layout(const attn_dense_desc* d, attn_dense_strides* st);
+
+/*
+ * attn_bwd_dense and attn_fwd_dense with explicit strides (the descriptor's
+ * layout field is then ignored for addressing).  fp32 storage needs q, k, v
+ * and dy in the descriptor's layout (ATTN_ERR_UNSUPPORTED otherwise); bf16
+ * takes any valid strides.  Results are bit-identical to the layout call on
+ * the same values.
+ */
+ATTN_API attn_status_t attn_bwd_dense_strided(const attn_dense_desc* d, const attn_dense_strides* st, const void* q,
+                                              const void* k, const void* v, const void* dy, const float* key_mask,
+                                              const void* bias, const void* o, const float* lse, void* dq, void* dk,
+                                              void* dv, unsigned wrt_mask, void* workspace, size_t workspace_bytes,
+                                              void* stream);
+ATTN_API attn_status_t attn_fwd_dense_strided(const attn_dense_desc* d, const attn_dense_strides* st, const void* q,
+                                              const void* k, const void* v, const float* key_mask, const void* bias,
+                                              void* o, float* lse, void* workspace, size_t workspace_bytes,
+                                              void* stream);
+
+/*
  * Dense forward export: O and the LSE of the same attention the backward
  * differentiates (same descriptor, masks and bias), by the forward sweep of
  * the backward's row-statistics prologue (rlx-cpu src/attention_bwd.rs,

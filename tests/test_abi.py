@@ -98,3 +98,36 @@ def test_workspace_errors(lib):
     d = _desc()
     assert _call(d, ws_bytes=16) == bd.ATTN_ERR_WORKSPACE
     assert _call(d, ws=FAKE + 28 * MB + 16) == bd.ATTN_ERR_WORKSPACE
+
+
+def _strided_call(desc, sts, q, k, v, dy, dq, dk, dv):
+    return int(bd.lib().attn_bwd_dense_strided(ctypes.byref(desc), ctypes.byref(sts), ctypes.c_void_p(q),
+                                               ctypes.c_void_p(k), ctypes.c_void_p(v), ctypes.c_void_p(dy), None,
+                                               None, None, None, ctypes.c_void_p(dq), ctypes.c_void_p(dk),
+                                               ctypes.c_void_p(dv), 7, None, 0, None))
+
+
+def test_strided_fused_views(lib):
+    """q, k, v and dq, dk, dv as interleaved views of fused [B, S, 3, H, D]
+    tensors pass the overlap checks (the call stops at the missing workspace);
+    the same views with one gradient aliasing another are refused."""
+    B, S, H, D = 2, 64, 2, 128
+    desc = _desc(batch=B, heads=H, seq_q=S, seq_k=S, head_dim=D)
+    sts = bd.attn_dense_strides()
+    bd.lib().attn_dense_strides_from_layout(ctypes.byref(desc), ctypes.byref(sts))
+    fused = bd.attn_strides3(S * 3 * H * D, 3 * H * D, D)
+    for n in ("q", "k", "v", "dq", "dk", "dv"):
+        setattr(sts, n, fused)
+    es = 2
+    x, g = FAKE, FAKE + 64 * MB
+    st = _strided_call(desc, sts, x, x + H * D * es, x + 2 * H * D * es, FAKE + 32 * MB,
+                       g, g + H * D * es, g + 2 * H * D * es)
+    assert st == bd.ATTN_ERR_WORKSPACE
+    st = _strided_call(desc, sts, x, x + H * D * es, x + 2 * H * D * es, FAKE + 32 * MB,
+                       g, g + H * D * es, g + H * D * es + 64)
+    assert st == bd.ATTN_ERR_ALIAS
+    # an output whose own rows overlap (sequence stride below the head span)
+    sts.dq = bd.attn_strides3(S * H * D, D, D)
+    st = _strided_call(desc, sts, x, x + H * D * es, x + 2 * H * D * es, FAKE + 32 * MB,
+                       g, g + H * D * es, g + 2 * H * D * es)
+    assert st == bd.ATTN_ERR_INVALID_ARG

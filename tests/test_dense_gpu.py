@@ -212,3 +212,56 @@ def test_top_left_alignment(bd, sq, sk, causal, window, dim):
     assert_close(res, ref)
     if sq < sk and window is None:
         assert torch.all(res[1][:, sq:] == 0) and torch.all(res[2][:, sq:] == 0)
+
+
+def test_strided_views_match_contiguous(bd):
+    """q, k, v as views of one fused [B, S, 3, H, D] tensor and dq, dk, dv
+    written into one fused gradient tensor give bit-identical results to the
+    contiguous call (attn_bwd_dense_strided)."""
+    c = inputs.dense_inputs(batch=2, heads=3, seq_q=320, seq_k=320, head_dim=128, dtype="bf16", seed=91,
+                            scale=0.5, causal=True, key_mask_zero_frac=0.1, bias=True)
+    qkv = torch.stack([_dev(c.q), _dev(c.k), _dev(c.v)], dim=2)  # [B, S, 3, H, D]
+    q, k, v = qkv[:, :, 0], qkv[:, :, 1], qkv[:, :, 2]
+    assert not q.is_contiguous()
+    dy = _dev(c.dy)
+    km = torch.from_numpy(c.key_mask).cuda()
+    bias = _dev(c.bias)
+    grads = torch.full_like(qkv, float("nan"))
+    outs = (grads[:, :, 0], grads[:, :, 1], grads[:, :, 2])
+    bd.dense_backward(q, k, v, dy, causal=True, key_mask=km, bias=bias, outputs=outs)
+    ref = bd.dense_backward(q.contiguous(), k.contiguous(), v.contiguous(), dy, causal=True, key_mask=km, bias=bias)
+    bd.check_device_error()
+    for a, b in zip(outs, ref):
+        assert torch.equal(a, b)
+    # the forward export through the same views, O into a strided slice
+    obuf = torch.full((2, 320, 2, 3, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    o, lse = bd.dense_forward(q, k, v, causal=True, key_mask=km, bias=bias,
+                              outputs=(obuf[:, :, 1], torch.empty(2, 3, 320, device="cuda")))
+    o2, lse2 = bd.dense_forward(q.contiguous(), k.contiguous(), v.contiguous(), causal=True, key_mask=km, bias=bias)
+    bd.check_device_error()
+    assert torch.equal(o, o2) and torch.equal(lse, lse2)
+    assert torch.isnan(obuf[:, :, 0]).all()  # the other slice is untouched
+
+
+def test_strided_head_broadcast_keys(bd):
+    """One key/value head shared by all query heads through a head stride of 0
+    (inputs may overlap), against the materialised copy."""
+    c = inputs.dense_inputs(batch=1, heads=4, seq_q=256, seq_k=384, head_dim=64, dtype="bf16", seed=92,
+                            scale=0.5, causal=True)
+    q, dy = _dev(c.q), _dev(c.dy)
+    k1, v1 = _dev(c.k[:, :, :1]), _dev(c.v[:, :, :1])
+    k, v = k1.expand(-1, -1, 4, -1), v1.expand(-1, -1, 4, -1)
+    assert k.stride(2) == 0
+    a = bd.dense_backward(q, k, v, dy, causal=True)
+    b = bd.dense_backward(q, k.contiguous(), v.contiguous(), dy, causal=True)
+    bd.check_device_error()
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+
+
+def test_strided_overlapping_output_refused(bd):
+    c = inputs.dense_inputs(batch=1, heads=2, seq_q=64, seq_k=64, head_dim=64, dtype="bf16", seed=93, scale=0.5)
+    q, k, v, dy = (_dev(x) for x in (c.q, c.k, c.v, c.dy))
+    dq = torch.empty(1, 1, 2, 64, dtype=torch.bfloat16, device="cuda").expand(1, 64, 2, 64)  # seq stride 0
+    with pytest.raises(bd.AttnError):
+        bd.dense_backward(q, k, v, dy, outputs=(dq, torch.empty_like(k), torch.empty_like(v)))
