@@ -41,14 +41,16 @@ def visibility(seq_q: int, seq_k: int, causal: bool, window: int | None, top_lef
     return vis
 
 
-def head_backward(q, k, v, dy, vis, scale, key_masked=None, bias=None, mask_neg=-1e9):
+def head_backward(q, k, v, dy, vis, scale, key_masked=None, bias=None, mask_neg=-1e9, elem_masked=None):
     """Backward of one head.  q, dy: [Sq, D]; k, v: [Sk, D]; vis: [Sq, Sk] bool;
-    key_masked: [Sk] bool (custom mask hit) or None; bias: [Sq, Sk] or None.
+    key_masked: [Sk] bool (custom mask hit) or None; bias: [Sq, Sk] or None;
+    elem_masked: [Sq, Sk] bool (per-element custom mask hit, rlx-wgpu
+    attention_bwd.wgsl ``mask_score`` kind 2) or None.
 
     Steps (rlx-cpu attention_bwd.rs, ``backward_dense_head_all``):
       S  = scale * Q K^T            (score product)
       S += bias                     (additive bias mask)
-      S[:, masked keys] = mask_neg  (custom mask)
+      S[:, masked keys] = mask_neg  (custom mask; per element likewise)
       P  = softmax over visible keys, max-subtracted
       dV = P^T dY
       dP = dY V^T
@@ -65,6 +67,8 @@ def head_backward(q, k, v, dy, vis, scale, key_masked=None, bias=None, mask_neg=
         s = s + np.asarray(bias, dtype=np.float64)
     if key_masked is not None:
         s[:, np.asarray(key_masked, dtype=bool)] = mask_neg
+    if elem_masked is not None:
+        s = np.where(np.asarray(elem_masked, dtype=bool), mask_neg, s)
     s = np.where(vis, s, -np.inf)
     m = s.max(axis=1, initial=-np.inf)
     has = np.isfinite(m)
@@ -95,13 +99,15 @@ def _heads(x, layout):
 
 def attn_bwd_dense(q, k, v, dy, *, layout="bshd", causal=False, window=None, key_mask=None,
                    bias=None, mask_thr=0.5, mask_neg=-1e9, scale=None, heads_subset=None,
-                   return_stats=False, top_left=False):
+                   return_stats=False, top_left=False, elem_mask=None):
     """Full-tensor dense backward (rlx-cpu attention_bwd.rs, ``attention_backward_all``).
 
     q, dy: [B,Sq,H,D] ('bshd') or [B,H,Sq,D] ('bhsd'); k, v likewise with Sk.
     key_mask: [B, Sk] (masked where value < mask_thr); bias: [B, H, Sq, Sk].
     ``heads_subset``: optional list of (b, h) to evaluate (others stay zero).
     ``top_left``: causal / window masks aligned top-left (see ``visibility``).
+    ``elem_mask``: [B, H, Sq, Sk] per-element custom mask (masked where value
+    < mask_thr), alone or together with ``key_mask``.
     Returns float64 dq, dk, dv in the input layout (and lse, delta [B,H,Sq]
     when ``return_stats``)."""
     qh, kh, vh, dyh = (_heads(np.asarray(x), layout) for x in (q, k, v, dy))
@@ -119,8 +125,9 @@ def attn_bwd_dense(q, k, v, dy, *, layout="bshd", causal=False, window=None, key
     for b, h in pairs:
         km = None if key_mask is None else (np.asarray(key_mask[b]) < mask_thr)
         bi = None if bias is None else bias[b, h]
+        em = None if elem_mask is None else (np.asarray(elem_mask[b, h]) < mask_thr)
         r = head_backward(qh[b, h], kh[b, h], vh[b, h], dyh[b, h], vis, scale,
-                          key_masked=km, bias=bi, mask_neg=mask_neg)
+                          key_masked=km, bias=bi, mask_neg=mask_neg, elem_masked=em)
         dq[b, h], dk[b, h], dv[b, h] = r["dq"], r["dk"], r["dv"]
         lse[b, h], delta[b, h] = r["lse"], r["delta"]
     if layout == "bshd":
@@ -131,7 +138,7 @@ def attn_bwd_dense(q, k, v, dy, *, layout="bshd", causal=False, window=None, key
 
 
 def attn_fwd_dense(q, k, v, *, layout="bshd", causal=False, window=None, key_mask=None, bias=None,
-                   mask_thr=0.5, mask_neg=-1e9, scale=None, top_left=False):
+                   mask_thr=0.5, mask_neg=-1e9, scale=None, top_left=False, elem_mask=None):
     """Forward output O = P V and lse = log-sum-exp of the masked scores, float64.
 
     The probabilities are those of the backward (same masks, same softmax); a
@@ -149,9 +156,10 @@ def attn_fwd_dense(q, k, v, *, layout="bshd", causal=False, window=None, key_mas
         for h in range(H):
             km = None if key_mask is None else (np.asarray(key_mask[b]) < mask_thr)
             bi = None if bias is None else bias[b, h]
+            em = None if elem_mask is None else (np.asarray(elem_mask[b, h]) < mask_thr)
             # the backward's P with a zero upstream gradient
             r = head_backward(qh[b, h], kh[b, h], vh[b, h], np.zeros((Sq, vh.shape[3])), vis, scale,
-                              key_masked=km, bias=bi, mask_neg=mask_neg)
+                              key_masked=km, bias=bi, mask_neg=mask_neg, elem_masked=em)
             o[b, h] = r["p"] @ np.asarray(vh[b, h], dtype=np.float64)
             lse[b, h] = r["lse"]
     if layout == "bshd":

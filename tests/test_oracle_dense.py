@@ -37,7 +37,7 @@ def _loop_visible(qi, ki, sq, sk, causal, window):
 
 
 def loop_loss(q, k, v, dy, causal=False, window=None, key_mask=None, bias=None, thr=0.5,
-              neg=-1e9, layout="bshd"):
+              neg=-1e9, layout="bshd", elem_mask=None):
     """L = sum over b,h,q,d of dY * O with O the attention output (loops)."""
     if layout == "bshd":
         B, Sq, H, D = q.shape
@@ -60,6 +60,8 @@ def loop_loss(q, k, v, dy, causal=False, window=None, key_mask=None, bias=None, 
                     if bias is not None:
                         s += float(bias[b, h, qi, ki])
                     if key_mask is not None and key_mask[b, ki] < thr:
+                        s = neg
+                    if elem_mask is not None and elem_mask[b, h, qi, ki] < thr:
                         s = neg
                     scores.append((ki, s))
                 if not scores:
@@ -363,3 +365,38 @@ def test_top_left_window_is_band_attention():
         lo, hi = max(qi - w, 0), qi + 1
         r = attn_bwd_dense(q[:, qi:qi + 1], k[:, lo:hi], v[:, lo:hi], dy[:, qi:qi + 1], scale=1.0 / math.sqrt(D))
         np.testing.assert_allclose(dq[:, qi], r[0][:, 0], rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# per-element custom mask (rlx-wgpu attention_bwd.wgsl, mask_score kind 2)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("causal,use_bias", [(False, False), (True, True)])
+def test_fd_element_mask(causal, use_bias):
+    """Finite differences of the looped loss with a per-element mask (each row
+    keeps an unmasked visible key)."""
+    rng = np.random.default_rng(91)
+    B, H, sq, sk, D = 1, 2, 5, 6, 4
+    q, k, v, dy = (rng.standard_normal(x) for x in ((B, sq, H, D), (B, sk, H, D), (B, sk, H, D), (B, sq, H, D)))
+    em = (rng.random((B, H, sq, sk)) > 0.3).astype(np.float64)
+    em[..., 0] = 1.0  # key 0 is visible to every row under either mask
+    bias = rng.standard_normal((B, H, sq, sk)) if use_bias else None
+    dq, dk, dv = attn_bwd_dense(q, k, v, dy, causal=causal, bias=bias, elem_mask=em)
+    f = lambda: loop_loss(q, k, v, dy, causal, None, None, bias, elem_mask=em)
+    for x, g in ((q, dq), (k, dk), (v, dv)):
+        assert _rel(g, fd_grad(f, x)) < 1e-6
+
+
+def test_element_mask_repeating_a_key_mask_is_the_key_mask():
+    """An element mask equal to a key mask on every row gives the key mask's
+    gradients (and statistics), including rows whose keys are all masked."""
+    rng = np.random.default_rng(92)
+    B, H, sq, sk, D = 2, 2, 6, 7, 4
+    q, k, v, dy = (rng.standard_normal(x) for x in ((B, sq, H, D), (B, sk, H, D), (B, sk, H, D), (B, sq, H, D)))
+    km = (rng.random((B, sk)) > 0.4).astype(np.float64)
+    km[:, 0] = 0.0  # under causal alignment the first row sees only masked keys
+    em = np.broadcast_to(km[:, None, None, :], (B, H, sq, sk)).copy()
+    a = attn_bwd_dense(q, k, v, dy, causal=True, key_mask=km, return_stats=True)
+    b = attn_bwd_dense(q, k, v, dy, causal=True, elem_mask=em, return_stats=True)
+    for x, y in zip(a, b):
+        np.testing.assert_array_equal(x, y)
