@@ -35,6 +35,7 @@ ATTN_MASK_WINDOW = 2
 ATTN_MASK_KEY = 4
 ATTN_MASK_BIAS = 8
 ATTN_MASK_TOP_LEFT = 16
+ATTN_MASK_ELEM = 32
 ATTN_WRT_DQ = 1
 ATTN_WRT_DK = 2
 ATTN_WRT_DV = 4
@@ -82,7 +83,7 @@ _SIG = {
                                                 _P, _P, _P, ctypes.c_uint, _P]),
     "attn_dense_strides_from_layout": (None, [ctypes.POINTER(attn_dense_desc), ctypes.POINTER(attn_dense_strides)]),
     "attn_bwd_dense_strided": (ctypes.c_int32, [ctypes.POINTER(attn_dense_desc), ctypes.POINTER(attn_dense_strides),
-                                                _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_uint, _P,
+                                                _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_uint, _P,
                                                 ctypes.c_size_t, _P]),
     "attn_fwd_dense_strided": (ctypes.c_int32, [ctypes.POINTER(attn_dense_desc), ctypes.POINTER(attn_dense_strides),
                                                 _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]),
@@ -240,7 +241,7 @@ def _dtype_code(t):
 
 def make_dense_desc(*, batch, heads, seq_q, seq_k, head_dim, dtype=ATTN_DTYPE_BF16, layout=ATTN_LAYOUT_BSHD,
                     causal=False, window=None, key_mask=False, bias=False, mask_thr=0.5, mask_neg=-1e9,
-                    scale=0.0, top_left=False) -> attn_dense_desc:
+                    scale=0.0, top_left=False, elem_mask=False) -> attn_dense_desc:
     d = attn_dense_desc()
     attn_dense_desc_init(d)
     d.batch, d.heads, d.seq_q, d.seq_k, d.head_dim = batch, heads, seq_q, seq_k, head_dim
@@ -257,6 +258,8 @@ def make_dense_desc(*, batch, heads, seq_q, seq_k, head_dim, dtype=ATTN_DTYPE_BF
         flags |= ATTN_MASK_BIAS
     if top_left:
         flags |= ATTN_MASK_TOP_LEFT
+    if elem_mask:
+        flags |= ATTN_MASK_ELEM
     d.mask_flags = flags
     d.mask_thr, d.mask_neg, d.scale = mask_thr, mask_neg, scale
     return d
@@ -264,9 +267,11 @@ def make_dense_desc(*, batch, heads, seq_q, seq_k, head_dim, dtype=ATTN_DTYPE_BF
 
 def dense_backward(q, k, v, dy, *, layout="bshd", causal=False, window=None, key_mask=None, bias=None, o=None,
                    lse=None, wrt=ATTN_WRT_DQ | ATTN_WRT_DK | ATTN_WRT_DV, scale=0.0, mask_thr=0.5, mask_neg=-1e9,
-                   outputs=None, workspace=None, stream=None, top_left=False):
+                   outputs=None, workspace=None, stream=None, top_left=False, elem_mask=None):
     """dQ, dK, dV for CUDA tensors q, k, v, dy ([B,S,H,D] or [B,H,S,D]).
 
+    ``elem_mask`` is the optional per-element mask [B, H, Sq, Sk] (fp32,
+    contiguous; a pair below ``mask_thr`` is masked).
     Returns (dq, dk, dv) with None for gradients not selected in ``wrt``."""
     import torch
     lay = {"bshd": ATTN_LAYOUT_BSHD, "bhsd": ATTN_LAYOUT_BHSD}[layout]
@@ -278,7 +283,10 @@ def dense_backward(q, k, v, dy, *, layout="bshd", causal=False, window=None, key
         Sk = k.shape[2]
     desc = make_dense_desc(batch=B, heads=H, seq_q=Sq, seq_k=Sk, head_dim=D, dtype=_dtype_code(q), layout=lay,
                            causal=causal, window=window, key_mask=key_mask is not None, bias=bias is not None,
-                           mask_thr=mask_thr, mask_neg=mask_neg, scale=scale, top_left=top_left)
+                           mask_thr=mask_thr, mask_neg=mask_neg, scale=scale, top_left=top_left,
+                           elem_mask=elem_mask is not None)
+    if elem_mask is not None and not elem_mask.is_contiguous():
+        raise ValueError("elem_mask must be contiguous")
     if outputs is None:
         dq = torch.empty_like(q) if wrt & ATTN_WRT_DQ else None
         dk = torch.empty_like(k) if wrt & ATTN_WRT_DK else None
@@ -289,14 +297,15 @@ def dense_backward(q, k, v, dy, *, layout="bshd", causal=False, window=None, key
     if workspace is None:
         workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=q.device)
     tensors = dict(q=q, k=k, v=v, dy=dy, o=o, dq=dq, dk=dk, dv=dv)
-    if all(t is None or t.is_contiguous() for t in tensors.values()):
+    if elem_mask is None and all(t is None or t.is_contiguous() for t in tensors.values()):
         st = attn_bwd_dense(desc, _ptr(q), _ptr(k), _ptr(v), _ptr(dy), _ptr(key_mask), _ptr(bias), _ptr(o),
                             _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), wrt, _ptr(workspace), workspace.numel(),
                             _stream_handle(stream))
-    else:  # non-contiguous views: pass their strides
+    else:  # non-contiguous views or a per-element mask: the strided entry point
         sts = _dense_strides(desc, layout, tensors)
         st = int(lib().attn_bwd_dense_strided(ctypes.byref(desc), ctypes.byref(sts), _vptr(q), _vptr(k), _vptr(v),
-                                              _vptr(dy), _ptr(key_mask), _ptr(bias), _vptr(o), _ptr(lse), _vptr(dq),
+                                              _vptr(dy), _ptr(key_mask), _ptr(elem_mask), _ptr(bias), _vptr(o),
+                                              _ptr(lse), _vptr(dq),
                                               _vptr(dk), _vptr(dv), wrt, _ptr(workspace), workspace.numel(),
                                               _stream_handle(stream)))
     _check(st)

@@ -146,6 +146,8 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 struct DenseSizes {
   size_t es, q_bytes, k_bytes, bias_bytes, mask_bytes, stat_bytes, ws_bytes;
   size_t split_off;  // fp32 storage: offset of the hi/lo bf16 copies of q, k, v, dy
+  size_t elem_off;   // per-element mask: offset of its row and column bits
+  int ew_q, ew_k;    // 32-bit words per query row / key column of those bits (even)
 };
 
 attn_status_t check_dense_desc(const attn_dense_desc* d, DenseSizes* z) {
@@ -156,7 +158,7 @@ attn_status_t check_dense_desc(const attn_dense_desc* d, DenseSizes* z) {
     return api_fail(ATTN_ERR_INVALID_ARG, "unknown dtype %d", d->dtype);
   if (d->layout != ATTN_LAYOUT_BSHD && d->layout != ATTN_LAYOUT_BHSD)
     return api_fail(ATTN_ERR_INVALID_ARG, "unknown layout %d", d->layout);
-  if (d->mask_flags & ~31u) return api_fail(ATTN_ERR_INVALID_ARG, "unknown mask flag bits 0x%x", d->mask_flags);
+  if (d->mask_flags & ~63u) return api_fail(ATTN_ERR_INVALID_ARG, "unknown mask flag bits 0x%x", d->mask_flags);
   if ((d->mask_flags & ATTN_MASK_WINDOW) && d->window < 0) return api_fail(ATTN_ERR_INVALID_ARG, "window < 0");
   if (d->reserved != 0) return api_fail(ATTN_ERR_INVALID_ARG, "reserved field must be 0");
   if (!std::isfinite(d->mask_neg) || !(d->mask_neg < 0.f)) return api_fail(ATTN_ERR_INVALID_ARG, "mask_neg must be finite and < 0");
@@ -183,7 +185,18 @@ attn_status_t check_dense_desc(const attn_dense_desc* d, DenseSizes* z) {
     // doubled tiles in shared memory.
     if (D > 64) return api_fail(ATTN_ERR_UNSUPPORTED, "fp32 storage supports head_dim <= 64");
     if (d->mask_flags & ATTN_MASK_BIAS) return api_fail(ATTN_ERR_UNSUPPORTED, "fp32 storage does not take a bias");
+    if (d->mask_flags & ATTN_MASK_ELEM) return api_fail(ATTN_ERR_UNSUPPORTED, "fp32 storage does not take a per-element mask");
     z->ws_bytes += 4 * align256(z->q_bytes / 2) + 4 * align256(z->k_bytes / 2);
+  }
+  z->elem_off = z->ws_bytes;
+  z->ew_q = z->ew_k = 0;
+  if (d->mask_flags & ATTN_MASK_ELEM) {
+    // bits of the mask, rows [BH, Sq, ew_q] and columns [BH, Sk, ew_k]; even
+    // widths so the kernels read 64-bit words
+    z->ew_q = int(((d->seq_k + 31) / 32 + 1) & ~int64_t(1));
+    z->ew_k = int(((d->seq_q + 31) / 32 + 1) & ~int64_t(1));
+    const size_t bh = size_t(d->batch) * d->heads;
+    z->ws_bytes += align256(bh * d->seq_q * z->ew_q * 4) + align256(bh * d->seq_k * z->ew_k * 4);
   }
   if (z->ws_bytes == 0) z->ws_bytes = 256;
   return ATTN_OK;
@@ -294,6 +307,7 @@ attn_status_t prepare_dense(const attn_dense_desc* d, const attn_dense_strides& 
   p.causal = (d->mask_flags & (ATTN_MASK_CAUSAL | ATTN_MASK_WINDOW)) ? 1 : 0;
   p.window = (d->mask_flags & ATTN_MASK_WINDOW) ? d->window : -1;
   p.has_key_mask = has_km ? 1 : 0;
+  p.has_custom = (has_km || (d->mask_flags & ATTN_MASK_ELEM)) ? 1 : 0;
   p.scale = d->scale > 0.f ? d->scale : float(1.0 / std::sqrt(double(D)));
   p.scale_log2 = p.scale * attn::kLog2e;
   p.masked_x2 = d->mask_neg * attn::kLog2e;
@@ -318,6 +332,12 @@ attn_status_t prepare_dense(const attn_dense_desc* d, const attn_dense_strides& 
   put(p.s_dq, st.dq);
   put(p.s_dk, st.dk);
   put(p.s_dv, st.dv);
+  if (z.ew_q) {
+    p.elem_rows = reinterpret_cast<const uint32_t*>(ws + z.elem_off);
+    p.elem_cols = reinterpret_cast<const uint32_t*>(ws + z.elem_off + align256(size_t(B * H * Sq) * z.ew_q * 4));
+    p.ew_q = z.ew_q;
+    p.ew_k = z.ew_k;
+  }
   p.err = device_error_word();
   if (!p.err) return api_fail(ATTN_ERR_CUDA, "no CUDA device / symbol address unavailable");
 
@@ -409,25 +429,29 @@ ATTN_API attn_status_t attn_bwd_dense(const attn_dense_desc* d, const void* q, c
   if (!d) return api_fail(ATTN_ERR_INVALID_ARG, "descriptor is NULL");
   attn_dense_strides sts;
   layout_strides(d, &sts);
-  return attn_bwd_dense_strided(d, &sts, q, k, v, dy, key_mask, bias, o, lse, dq, dk, dv, wrt_mask, workspace,
-                                workspace_bytes, stream);
+  return attn_bwd_dense_strided(d, &sts, q, k, v, dy, key_mask, nullptr, bias, o, lse, dq, dk, dv, wrt_mask,
+                                workspace, workspace_bytes, stream);
 }
 
 ATTN_API attn_status_t attn_bwd_dense_strided(const attn_dense_desc* d, const attn_dense_strides* sts, const void* q,
                                               const void* k, const void* v, const void* dy, const float* key_mask,
-                                              const void* bias, const void* o, const float* lse, void* dq, void* dk,
-                                              void* dv, unsigned wrt_mask, void* workspace, size_t workspace_bytes,
-                                              void* stream) {
+                                              const float* elem_mask, const void* bias, const void* o,
+                                              const float* lse, void* dq, void* dk, void* dv, unsigned wrt_mask,
+                                              void* workspace, size_t workspace_bytes, void* stream) {
   DenseSizes z;
   attn_status_t st = check_dense_desc(d, &z);
   if (st != ATTN_OK) return st;
-  if (!sts) return api_fail(ATTN_ERR_INVALID_ARG, "strides are NULL");
-  const attn_dense_strides& S3 = *sts;
+  attn_dense_strides lay_st;
+  if (!sts) layout_strides(d, &lay_st);
+  const attn_dense_strides& S3 = sts ? *sts : lay_st;
   if (wrt_mask == 0 || (wrt_mask & ~7u)) return api_fail(ATTN_ERR_INVALID_ARG, "wrt_mask must be a non-empty subset of dQ|dK|dV");
   const bool has_km = (d->mask_flags & ATTN_MASK_KEY) != 0;
   const bool has_bias = (d->mask_flags & ATTN_MASK_BIAS) != 0;
   if (has_km != (key_mask != nullptr)) return api_fail(ATTN_ERR_INVALID_ARG, "key_mask must be given iff ATTN_MASK_KEY is set");
   if (has_bias != (bias != nullptr)) return api_fail(ATTN_ERR_INVALID_ARG, "bias must be given iff ATTN_MASK_BIAS is set");
+  const bool has_elem = (d->mask_flags & ATTN_MASK_ELEM) != 0;
+  if (has_elem != (elem_mask != nullptr))
+    return api_fail(ATTN_ERR_INVALID_ARG, "elem_mask must be given iff ATTN_MASK_ELEM is set");
   if ((o == nullptr) != (lse == nullptr)) return api_fail(ATTN_ERR_INVALID_ARG, "o and lse must be given together");
   const bool want_dq = wrt_mask & ATTN_WRT_DQ, want_dk = wrt_mask & ATTN_WRT_DK, want_dv = wrt_mask & ATTN_WRT_DV;
   if ((want_dq && !dq && z.q_bytes) || (want_dk && !dk && z.k_bytes) || (want_dv && !dv && z.k_bytes))
@@ -453,7 +477,7 @@ ATTN_API attn_status_t attn_bwd_dense_strided(const attn_dense_desc* d, const at
   // required inputs (only when they have elements)
   if (!empty_q && (!q || !dy)) return api_fail(ATTN_ERR_INVALID_ARG, "q/dy is NULL");
   if (!empty_k && (!k || !v)) return api_fail(ATTN_ERR_INVALID_ARG, "k/v is NULL");
-  const void* ptrs[] = {q, k, v, dy, key_mask, bias, o, lse, dq, dk, dv, workspace};
+  const void* ptrs[] = {q, k, v, dy, key_mask, elem_mask, bias, o, lse, dq, dk, dv, workspace};
   for (const void* p : ptrs)
     if (p && !aligned16(p)) return api_fail(ATTN_ERR_INVALID_ARG, "tensor pointers must be 16-byte aligned");
   if (has_bias && (Sk * z.es) % 16 != 0) return api_fail(ATTN_ERR_UNSUPPORTED, "bias needs Sk * element size to be a multiple of 16");
@@ -461,7 +485,8 @@ ATTN_API attn_status_t attn_bwd_dense_strided(const attn_dense_desc* d, const at
   struct R { const void* p; size_t n; };
   // plain inputs (contiguous) by byte range; strided tensors against each other exactly
   const R ins[] = {{key_mask, has_km ? z.mask_bytes : 0}, {bias, has_bias ? z.bias_bytes : 0},
-                   {lse, lse ? z.stat_bytes : 0}, {workspace, workspace_bytes}};
+                   {elem_mask, has_elem ? z.bias_bytes / z.es * 4 : 0}, {lse, lse ? z.stat_bytes : 0},
+                   {workspace, workspace_bytes}};
   struct T { const void* p; const attn_strides3* s; size_t n; int64_t S; };
   const T tin[] = {{q, &S3.q, xq, Sq}, {k, &S3.k, xk, Sk}, {v, &S3.v, xv, Sk}, {dy, &S3.dy, xdy, Sq},
                    {o, &S3.o, o ? xo : 0, Sq}};
@@ -506,9 +531,14 @@ ATTN_API attn_status_t attn_bwd_dense_strided(const attn_dense_desc* d, const at
     return st;
   p.wrt = wrt_mask;
 
-  const int nk = (split ? 4 : 0) + 1 + (want_dk || want_dv ? 1 : 0) + (want_dq ? 1 : 0);
+  const int nk = (split ? 4 : 0) + (has_elem ? 1 : 0) + 1 + (want_dk || want_dv ? 1 : 0) + (want_dq ? 1 : 0);
   attn::timing_mark_begin(nk, s);
   cudaError_t e = cudaSuccess;
+  if (has_elem) {
+    e = attn::launch_pack_elem_mask(elem_mask, d->mask_thr, B * H, int(Sq), int(Sk), const_cast<uint32_t*>(p.elem_rows),
+                                    const_cast<uint32_t*>(p.elem_cols), z.ew_q, z.ew_k, s);
+    attn::timing_mark(s);
+  }
   if (split) {
     const int64_t nq = int64_t(z.q_bytes / 4), nkv = int64_t(z.k_bytes / 4);
     const float* srcs[4] = {static_cast<const float*>(q), static_cast<const float*>(dy), static_cast<const float*>(k),
@@ -552,8 +582,11 @@ ATTN_API attn_status_t attn_fwd_dense_strided(const attn_dense_desc* d, const at
   DenseSizes z;
   attn_status_t st = check_dense_desc(d, &z);
   if (st != ATTN_OK) return st;
-  if (!sts) return api_fail(ATTN_ERR_INVALID_ARG, "strides are NULL");
-  const attn_dense_strides& S3 = *sts;
+  if (d->mask_flags & ATTN_MASK_ELEM)
+    return api_fail(ATTN_ERR_UNSUPPORTED, "the forward export does not take a per-element mask");
+  attn_dense_strides lay_st;
+  if (!sts) layout_strides(d, &lay_st);
+  const attn_dense_strides& S3 = sts ? *sts : lay_st;
   const bool has_km = (d->mask_flags & ATTN_MASK_KEY) != 0;
   const bool has_bias = (d->mask_flags & ATTN_MASK_BIAS) != 0;
   if (has_km != (key_mask != nullptr)) return api_fail(ATTN_ERR_INVALID_ARG, "key_mask must be given iff ATTN_MASK_KEY is set");

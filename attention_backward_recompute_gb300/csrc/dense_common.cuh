@@ -16,6 +16,7 @@ struct DenseParams {
   int causal;            // 1 when keys k > abs_q are hidden (causal or window)
   int window;            // window w, or -1 when there is no lower bound
   int has_key_mask;      // custom per-key mask present
+  int has_custom;        // a custom mask (per-key or per-element) present: pm is live
   float scale;           // softmax scale
   float scale_log2;      // scale * log2(e)
   float masked_x2;       // mask_neg * log2(e): a custom-masked score in base-2 units
@@ -45,6 +46,12 @@ struct DenseParams {
   int fwd_only;
   void* o_out;
   float* lse_out;
+  // Per-element custom mask as bits (workspace): elem_rows[(bh*Sq + q)*ew_q + k/32]
+  // bit k%32 and elem_cols[(bh*Sk + k)*ew_k + q/32] bit q%32 are set for a
+  // masked pair; null without the mask.  ew_q, ew_k are even.
+  const uint32_t* elem_rows;
+  const uint32_t* elem_cols;
+  int ew_q, ew_k;
   uint32_t* err;              // device error word
 };
 

@@ -72,10 +72,10 @@ __device__ __forceinline__ void reg_fence16(uint32_t (&r)[16]) {
 // (tile-local range of queries that see this key).  KM: the key is
 // custom-masked; its visible entries take the row's masked-key probability
 // pm instead.
-template <bool HAS_BIAS, bool CHECK>
+template <bool HAS_BIAS, bool CHECK, bool ELEM>
 __device__ __forceinline__ void p_chunk(const uint32_t (&sr)[16], int c0, const float* st, const uint8_t* bias_s,
                                         int kc, int kb, float scale_log2, int lo, int hi, bool kmasked,
-                                        uint32_t* pw) {
+                                        uint32_t ebits, uint32_t* pw) {
 #pragma unroll
   for (int c4 = 0; c4 < 4; ++c4) {
     const float4 l2 = *reinterpret_cast<const float4*>(st + c0 + 4 * c4);
@@ -92,14 +92,15 @@ __device__ __forceinline__ void p_chunk(const uint32_t (&sr)[16], int c0, const 
       }
       pv[e] = ex2_approx(x);
     }
-    if (kmasked) {
+    // per-element mask bits of these 4 queries
+    const uint32_t e4 = ELEM ? (ebits >> (4 * c4)) & 0xfu : 0u;
+    if (kmasked || e4) {
       const float4 pm = *reinterpret_cast<const float4*>(st + 128 + c0 + 4 * c4);
-      pv[0] = pm.x;
-      pv[1] = pm.y;
-      pv[2] = pm.z;
-      pv[3] = pm.w;
+      const float pmv[4] = {pm.x, pm.y, pm.z, pm.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) pv[e] = (kmasked || ((e4 >> e) & 1u)) ? pmv[e] : pv[e];
     }
-    if (CHECK || kmasked) {
+    if (CHECK || kmasked || e4) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int ql = c0 + 4 * c4 + e;
@@ -115,9 +116,9 @@ __device__ __forceinline__ void p_chunk(const uint32_t (&sr)[16], int c0, const 
 // four 16-column chunks with the next chunk's load in flight; chunk i's 8 bf16
 // pairs go to columns [8i, 8i+8) of the same buffer, which chunks 0..i have
 // already read.  The caller waits for the stores.
-template <bool HAS_BIAS, bool CHECK>
+template <bool HAS_BIAS, bool CHECK, bool ELEM>
 __device__ __forceinline__ void p_row(uint32_t tS, const float* st, const uint8_t* bias_s, int kc, int kb,
-                                      float scale_log2, int lo, int hi, bool kmasked) {
+                                      float scale_log2, int lo, int hi, bool kmasked, uint2 eb) {
   uint32_t s0[16], s1[16], pw[8];
   tmem_ld16(tS, s0);
   tmem_ld_wait();
@@ -125,12 +126,14 @@ __device__ __forceinline__ void p_row(uint32_t tS, const float* st, const uint8_
 #pragma unroll 1
   for (int i = 0; i < 4; i += 2) {
     tmem_ld16(tS + 16 * (i + 1), s1);
-    p_chunk<HAS_BIAS, CHECK>(s0, 16 * i, st, bias_s, kc, kb, scale_log2, lo, hi, kmasked, pw);
+    p_chunk<HAS_BIAS, CHECK, ELEM>(s0, 16 * i, st, bias_s, kc, kb, scale_log2, lo, hi, kmasked,
+                                   i < 2 ? eb.x : eb.y, pw);
     tmem_st8(tS + 8 * i, pw);
     tmem_ld_wait();
     reg_fence16(s1);
     if (i + 2 < 4) tmem_ld16(tS + 16 * (i + 2), s0);
-    p_chunk<HAS_BIAS, CHECK>(s1, 16 * (i + 1), st, bias_s, kc, kb, scale_log2, lo, hi, kmasked, pw);
+    p_chunk<HAS_BIAS, CHECK, ELEM>(s1, 16 * (i + 1), st, bias_s, kc, kb, scale_log2, lo, hi, kmasked,
+                                   (i < 2 ? eb.x : eb.y) >> 16, pw);
     tmem_st8(tS + 8 * (i + 1), pw);
     if (i + 2 < 4) {
       tmem_ld_wait();
@@ -139,7 +142,7 @@ __device__ __forceinline__ void p_row(uint32_t tS, const float* st, const uint8_
   }
 }
 
-template <int DP, bool HAS_BIAS>
+template <int DP, bool HAS_BIAS, bool ELEM>
 __global__ void __launch_bounds__(512, 1)
     dkdv2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_dy,
@@ -215,7 +218,7 @@ __global__ void __launch_bounds__(512, 1)
         const size_t idx = static_cast<size_t>(bh) * p.Sq + (in ? q : 0);
         pre[3 * i] = in ? p.L2[idx] : __int_as_float(0x7f800000);
         pre[3 * i + 1] = in ? p.delta[idx] : 0.f;
-        pre[3 * i + 2] = (in && p.has_key_mask) ? p.pm[idx] : 0.f;
+        pre[3 * i + 2] = (in && p.has_custom) ? p.pm[idx] : 0.f;
       }
     };
     load_stats(0);
@@ -373,10 +376,14 @@ __global__ void __launch_bounds__(512, 1)
         const uint8_t* bias_s = sm + L::BIAS_OFF + s * L::BIAS + half * (L::BQ * 128);
         const bool full = tile_fully_visible(p, q0, q0 + L::BQ - 1, k0, k0 + L::BK - 1);
         const int lo = qa - q0, hi = qb - q0;
+        uint2 eb = make_uint2(0u, 0u);  // per-element mask: this key's bits of the tile's 64 queries
+        if (ELEM && key < p.Sk)
+          eb = *reinterpret_cast<const uint2*>(p.elem_cols + (static_cast<size_t>(bh) * p.Sk + key) * p.ew_k +
+                                               (q0 >> 5));
         if (full)
-          p_row<HAS_BIAS, false>(tS, st, bias_s, kc, kb, p.scale_log2, lo, hi, kmasked);
+          p_row<HAS_BIAS, false, ELEM>(tS, st, bias_s, kc, kb, p.scale_log2, lo, hi, kmasked, eb);
         else
-          p_row<HAS_BIAS, true>(tS, st, bias_s, kc, kb, p.scale_log2, lo, hi, kmasked);
+          p_row<HAS_BIAS, true, ELEM>(tS, st, bias_s, kc, kb, p.scale_log2, lo, hi, kmasked, eb);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
@@ -465,10 +472,10 @@ __global__ void __launch_bounds__(512, 1)
   }
 }
 
-template <int DP, bool HAS_BIAS>
+template <int DP, bool HAS_BIAS, bool ELEM>
 cudaError_t launch_t(const DenseMaps& m, const DenseParams& p, cudaStream_t s) {
   using L = Dkdv2Layout<DP>;
-  auto kern = dkdv2_kernel<DP, HAS_BIAS>;
+  auto kern = dkdv2_kernel<DP, HAS_BIAS, ELEM>;
   const int smem = max(L::BYTES + 1024, kSmemOneCtaPerSm);  // all 512 TMEM columns: one CTA per SM
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -481,8 +488,12 @@ cudaError_t launch_t(const DenseMaps& m, const DenseParams& p, cudaStream_t s) {
 
 cudaError_t launch_dkdv2(const DenseMaps& m, const DenseParams& p, bool bias, cudaStream_t s) {
   const int DP = padded_head_dim(p.D);
-  if (DP == 64) return bias ? launch_t<64, true>(m, p, s) : launch_t<64, false>(m, p, s);
-  return bias ? launch_t<128, true>(m, p, s) : launch_t<128, false>(m, p, s);
+  if (p.elem_rows) {  // per-element custom mask
+    if (DP == 64) return bias ? launch_t<64, true, true>(m, p, s) : launch_t<64, false, true>(m, p, s);
+    return bias ? launch_t<128, true, true>(m, p, s) : launch_t<128, false, true>(m, p, s);
+  }
+  if (DP == 64) return bias ? launch_t<64, true, false>(m, p, s) : launch_t<64, false, false>(m, p, s);
+  return bias ? launch_t<128, true, false>(m, p, s) : launch_t<128, false, false>(m, p, s);
 }
 
 }  // namespace attn

@@ -133,7 +133,7 @@ __device__ __forceinline__ void p_row(uint32_t tS, const uint8_t* bias_row, int 
   }
 }
 
-template <int DP, bool HAS_BIAS>
+template <int DP, bool HAS_BIAS, bool ELEM>
 __global__ void __launch_bounds__(512, 1)
     dq2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_dy,
@@ -299,7 +299,7 @@ __global__ void __launch_bounds__(512, 1)
       const size_t idx = static_cast<size_t>(bh) * p.Sq + q;
       L2q = p.L2[idx];
       dlt = p.delta[idx];
-      if (p.has_key_mask) pmq = p.pm[idx];
+      if (p.has_custom) pmq = p.pm[idx];
     }
     if (n > 0 && warp < 12) {
       // stage this row of Q (warps 4..7) or dY (warps 8..11) in tensor memory
@@ -358,6 +358,12 @@ __global__ void __launch_bounds__(512, 1)
           kb1 = __ballot_sync(0xffffffffu, kmv[1] < p.mask_thr);
           if (t + 2 < n) km_load(kk0 + 2 * L::BK, kmv);
         }
+        if (ELEM && q < p.Sq) {  // per-element mask: this row's bits of the tile's 64 keys
+          const uint2 w = *reinterpret_cast<const uint2*>(p.elem_rows + (static_cast<size_t>(bh) * p.Sq + q) * p.ew_q +
+                                                           (kk0 >> 5));
+          kb0 |= w.x;
+          kb1 |= w.y;
+        }
         if (!(ok = mbar_wait_warp(&bar_full[s], (t / kStages) & 1, ab))) break;
         if (!(ok = mbar_wait_warp(&bar_s_full[bb], (t >> 1) & 1, ab))) break;
         tc_fence_after();
@@ -365,7 +371,7 @@ __global__ void __launch_bounds__(512, 1)
         const bool full = tile_fully_visible(p, q0, q0 + L::BQ - 1, kk0, kk0 + L::BK - 1);
         const uint8_t* bias_row = sm + L::BIAS_OFF + s * L::BIAS + row * 128;
         const int lo = ka - kk0, hi = kb - kk0;
-        if (full && !p.has_key_mask)
+        if (full && !p.has_key_mask && !ELEM)
           p_row<HAS_BIAS, false>(tS, bias_row, row, p.scale_log2, L2q, pmq, kb0, kb1, lo, hi);
         else
           p_row<HAS_BIAS, true>(tS, bias_row, row, p.scale_log2, L2q, pmq, kb0, kb1, lo, hi);
@@ -442,10 +448,10 @@ __global__ void __launch_bounds__(512, 1)
   }
 }
 
-template <int DP, bool HAS_BIAS>
+template <int DP, bool HAS_BIAS, bool ELEM>
 cudaError_t launch_t(const DenseMaps& m, const DenseParams& p, cudaStream_t s) {
   using L = Dq2Layout<DP>;
-  auto kern = dq2_kernel<DP, HAS_BIAS>;
+  auto kern = dq2_kernel<DP, HAS_BIAS, ELEM>;
   const int smem = max(L::BYTES + 1024, kSmemOneCtaPerSm);  // all 512 TMEM columns: one CTA per SM
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -458,8 +464,12 @@ cudaError_t launch_t(const DenseMaps& m, const DenseParams& p, cudaStream_t s) {
 
 cudaError_t launch_dq2(const DenseMaps& m, const DenseParams& p, bool bias, cudaStream_t s) {
   const int DP = padded_head_dim(p.D);
-  if (DP == 64) return bias ? launch_t<64, true>(m, p, s) : launch_t<64, false>(m, p, s);
-  return bias ? launch_t<128, true>(m, p, s) : launch_t<128, false>(m, p, s);
+  if (p.elem_rows) {  // per-element custom mask
+    if (DP == 64) return bias ? launch_t<64, true, true>(m, p, s) : launch_t<64, false, true>(m, p, s);
+    return bias ? launch_t<128, true, true>(m, p, s) : launch_t<128, false, true>(m, p, s);
+  }
+  if (DP == 64) return bias ? launch_t<64, true, false>(m, p, s) : launch_t<64, false, false>(m, p, s);
+  return bias ? launch_t<128, true, false>(m, p, s) : launch_t<128, false, false>(m, p, s);
 }
 
 }  // namespace attn

@@ -434,7 +434,7 @@ __global__ void __launch_bounds__(256) delta_only_kernel(const DenseParams p) {
       const bool empty = nvis == 0 || lse == -kInf;
       p.L2[r] = empty ? kInf : lse * kLog2e;
       p.delta[r] = empty ? 0.f : acc;
-      if (p.has_key_mask) {
+      if (p.has_custom) {
         // a row whose visible keys are all custom-masked has LSE = mask_neg +
         // log(n), which rounds to mask_neg when |mask_neg| is large
         float pm = 0.f;
@@ -488,6 +488,47 @@ cudaError_t launch_zero_rows(void* x, int64_t sb, int64_t ss, int64_t sh, int64_
                              size_t es, cudaStream_t s) {
   if (!x || B * S * H * D == 0) return cudaSuccess;
   zero_rows_kernel<<<152 * 4, 256, 0, s>>>(static_cast<uint8_t*>(x), sb, ss, sh, B, S, H, D, int64_t(es));
+  return cudaGetLastError();
+}
+
+namespace {
+// The per-element mask as bits, in both orientations: one warp per 32 x 32
+// block of (query, key) pairs, lane = key; the ballot over a query row gives
+// its row word, and each lane gathers its key's column word over the rows.
+__global__ void pack_elem_mask_kernel(const float* __restrict__ m, float thr, int64_t BH, int Sq, int Sk,
+                                      uint32_t* rows, uint32_t* cols, int ew_q, int ew_k) {
+  const int lane = threadIdx.x & 31;
+  const int nqt = (Sq + 31) / 32, nkt = (Sk + 31) / 32;
+  const int64_t blocks = BH * nqt * nkt;
+  for (int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; w < blocks;
+       w += (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5) {
+    const int kt = static_cast<int>(w % nkt), qt = static_cast<int>((w / nkt) % nqt);
+    const int64_t bh = w / (static_cast<int64_t>(nkt) * nqt);
+    const int k = kt * 32 + lane;
+    uint32_t colword = 0u;
+    for (int i = 0; i < 32; ++i) {
+      const int q = qt * 32 + i;
+      const bool in = q < Sq && k < Sk;
+      const bool masked = in && m[(bh * Sq + q) * Sk + k] < thr;
+      const uint32_t rowword = __ballot_sync(0xffffffffu, masked);
+      if (lane == 0 && q < Sq) {
+        rows[(bh * Sq + q) * ew_q + kt] = rowword;
+        if (kt == nkt - 1 && nkt < ew_q) rows[(bh * Sq + q) * ew_q + kt + 1] = 0u;  // even-width padding
+      }
+      colword |= (masked ? 1u : 0u) << i;
+    }
+    if (k < Sk) {
+      cols[(bh * Sk + k) * ew_k + qt] = colword;
+      if (qt == nqt - 1 && nqt < ew_k) cols[(bh * Sk + k) * ew_k + qt + 1] = 0u;
+    }
+  }
+}
+}  // namespace
+
+cudaError_t launch_pack_elem_mask(const float* m, float thr, int64_t BH, int Sq, int Sk, uint32_t* rows,
+                                  uint32_t* cols, int ew_q, int ew_k, cudaStream_t s) {
+  if (BH == 0 || Sq == 0 || Sk == 0) return cudaSuccess;
+  pack_elem_mask_kernel<<<152 * 8, 256, 0, s>>>(m, thr, BH, Sq, Sk, rows, cols, ew_q, ew_k);
   return cudaGetLastError();
 }
 

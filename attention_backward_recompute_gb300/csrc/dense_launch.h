@@ -31,6 +31,9 @@ cudaError_t launch_fwd_stats(const DenseMaps& m, const DenseParams& p, bool bias
 cudaError_t launch_stats2(const DenseMaps& m, const DenseParams& p, bool bias, cudaStream_t s);
 // x[0, n) = value
 cudaError_t launch_fill_f32(float* x, float value, int64_t n, cudaStream_t s);
+// per-element mask [BH, Sq, Sk] fp32 -> row and column bit sets (see DenseParams)
+cudaError_t launch_pack_elem_mask(const float* m, float thr, int64_t BH, int Sq, int Sk, uint32_t* rows,
+                                  uint32_t* cols, int ew_q, int ew_k, cudaStream_t s);
 // zero the D elements (es bytes each) of every (b, s, h) row of a strided tensor
 cudaError_t launch_zero_rows(void* x, int64_t sb, int64_t ss, int64_t sh, int64_t B, int64_t S, int64_t H, int64_t D,
                              size_t es, cudaStream_t s);

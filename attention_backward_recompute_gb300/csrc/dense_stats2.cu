@@ -90,7 +90,7 @@ __device__ __forceinline__ bool drain_wait(uint64_t* bar, uint32_t parity) {
 constexpr int kGroups = 4;
 __device__ __forceinline__ void group_sync() { asm volatile("bar.sync 1, 512;" ::: "memory"); }
 
-template <int DP, bool HAS_BIAS>
+template <int DP, bool HAS_BIAS, bool ELEM>
 __global__ void __launch_bounds__(576, 1)
     stats2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_dy,
@@ -288,11 +288,14 @@ __global__ void __launch_bounds__(576, 1)
     for (int t = 0; t < n && ok; ++t) {
       const int s = t % kStages, bb = t & 1;
       const int kk0 = (j_lo + t) * L::BK;
+      // per-element mask bits of this row's 32 columns (loaded before the wait)
+      uint32_t ebits = 0u;
+      if (ELEM && q < p.Sq && kk0 + 32 * g < p.Sk) ebits = p.elem_rows[(static_cast<size_t>(bh) * p.Sq + q) * p.ew_q + (kk0 >> 5) + g];
       if (!(ok = mbar_wait_warp(&bar_full[s], (t / kStages) & 1, ab))) break;
       // bias term of the group's 32 columns while the tensor core works:
       // x = bias*log2(e), as 16 packed pairs of adjacent columns
       const uint32_t kbits =
-          p.has_key_mask ? reinterpret_cast<const uint32_t*>(sm + L::COL_OFF + s * L::COL)[g] : 0u;
+          (p.has_key_mask ? reinterpret_cast<const uint32_t*>(sm + L::COL_OFF + s * L::COL)[g] : 0u) | ebits;
       // bias half (64 keys) g >> 1, 16-byte chunks 4 (g & 1) .. + 3 of this row
       const uint8_t* brow = sm + L::BIAS_OFF + s * L::BIAS + (g >> 1) * (L::BQ * 128) + row * 128;
       uint64_t x[16];
@@ -426,7 +429,7 @@ __global__ void __launch_bounds__(576, 1)
           lt = fmaf(mg_l[i][row], ai, lt);
           dt = fmaf(mg_d[i][row], ai, dt);
         }
-      } else if (p.has_key_mask) {
+      } else if (p.has_custom) {
         // every visible key of the row is custom-masked: all carry the same x
         lt = mcnt;
         dt = mdsum;
@@ -441,12 +444,12 @@ __global__ void __launch_bounds__(576, 1)
       if (lt > 0.f) {
         L2 = mm + __log2f(lt);
         dl = dt / lt;
-        if (p.has_key_mask) pm = any_unmasked ? ex2_approx(p.masked_x2 - L2) : 1.f / lt;
+        if (p.has_custom) pm = any_unmasked ? ex2_approx(p.masked_x2 - L2) : 1.f / lt;
       }
       const size_t idx = static_cast<size_t>(bh) * p.Sq + q;
       p.L2[idx] = L2;
       p.delta[idx] = dl;
-      if (p.has_key_mask) p.pm[idx] = pm;
+      if (p.has_custom) p.pm[idx] = pm;
     }
   }
   tc_fence_before();
@@ -457,10 +460,10 @@ __global__ void __launch_bounds__(576, 1)
   }
 }
 
-template <int DP, bool HAS_BIAS>
+template <int DP, bool HAS_BIAS, bool ELEM>
 cudaError_t launch_t(const DenseMaps& m, const DenseParams& p, cudaStream_t s) {
   using L = Stats2Layout<DP>;
-  auto kern = stats2_kernel<DP, HAS_BIAS>;
+  auto kern = stats2_kernel<DP, HAS_BIAS, ELEM>;
   const int smem = max(L::BYTES + 1024, kSmemOneCtaPerSm);  // all 512 TMEM columns: one CTA per SM
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -473,8 +476,12 @@ cudaError_t launch_t(const DenseMaps& m, const DenseParams& p, cudaStream_t s) {
 
 cudaError_t launch_stats2(const DenseMaps& m, const DenseParams& p, bool bias, cudaStream_t s) {
   const int DP = padded_head_dim(p.D);
-  if (DP == 64) return bias ? launch_t<64, true>(m, p, s) : launch_t<64, false>(m, p, s);
-  return bias ? launch_t<128, true>(m, p, s) : launch_t<128, false>(m, p, s);
+  if (p.elem_rows) {  // per-element custom mask
+    if (DP == 64) return bias ? launch_t<64, true, true>(m, p, s) : launch_t<64, false, true>(m, p, s);
+    return bias ? launch_t<128, true, true>(m, p, s) : launch_t<128, false, true>(m, p, s);
+  }
+  if (DP == 64) return bias ? launch_t<64, true, false>(m, p, s) : launch_t<64, false, false>(m, p, s);
+  return bias ? launch_t<128, true, false>(m, p, s) : launch_t<128, false, false>(m, p, s);
 }
 
 }  // namespace attn

@@ -116,6 +116,43 @@ def dense_inputs(*, name="custom", batch, heads, seq_q, seq_k, head_dim, dtype="
                      window=window, q=q, k=k, v=v, dy=dy, key_mask=km, bias=b)
 
 
+def elem_mask_inputs(*, batch, heads, seq_q, seq_k, seed=0, kind="random", masked_frac=0.3, doc_lo=16,
+                     doc_hi=160, full_rows=0, full_cols=0) -> np.ndarray:
+    """A per-element custom mask [B, H, Sq, Sk] (float32; a pair whose value is
+    below 0.5 is masked).
+
+    kind 'random': uniform values in [0, 1) shifted so that a pair is masked
+    with probability ``masked_frac``.  kind 'docs': queries and keys are cut
+    into documents of lengths drawn uniformly in [doc_lo, doc_hi] (the same
+    cut positions for both sides, per batch), and a pair across documents is
+    masked (values 0 / 1).  Then ``full_rows`` query rows and ``full_cols``
+    key columns per head are masked entirely (value 0)."""
+    rng = np.random.default_rng(seed)
+    shape = (batch, heads, seq_q, seq_k)
+    if kind == "random":
+        m = rng.random(size=shape, dtype=np.float64) + (0.5 - masked_frac)
+    elif kind == "docs":
+        m = np.zeros(shape)
+        n = max(seq_q, seq_k)
+        for b in range(batch):
+            doc = np.empty(n, dtype=np.int64)
+            pos, d = 0, 0
+            while pos < n:
+                ln = int(rng.integers(doc_lo, doc_hi + 1))
+                doc[pos:pos + ln] = d
+                pos, d = pos + ln, d + 1
+            m[b] = (doc[:seq_q, None] == doc[None, :seq_k])
+    else:
+        raise ValueError(kind)
+    for b in range(batch):
+        for h in range(heads):
+            if full_rows and seq_q:
+                m[b, h, rng.choice(seq_q, size=min(full_rows, seq_q), replace=False), :] = 0.0
+            if full_cols and seq_k:
+                m[b, h, :, rng.choice(seq_k, size=min(full_cols, seq_k), replace=False)] = 0.0
+    return m.astype(np.float32)
+
+
 # The five measured configurations (dense part), by name.  Seeds follow the
 # configuration order (1..5).
 DENSE_CONFIGS = {

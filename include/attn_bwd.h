@@ -80,6 +80,13 @@ typedef int32_t attn_status_t;
 /* align the causal and window masks top-left instead: abs_q = q (q_off = 0),
  * as rlx-wgpu attention_bwd.wgsl mask_score does (causal hides k > q) */
 #define ATTN_MASK_TOP_LEFT 16u
+/* per-element custom mask elem_mask[B, H, Sq, Sk] (fp32, contiguous): the
+ * score of a pair whose value is < mask_thr is replaced by mask_neg, as
+ * rlx-wgpu attention_bwd.wgsl mask_score does for its mask kind 2; combines
+ * with ATTN_MASK_KEY.  Taken by attn_bwd_dense_strided (bf16 storage);
+ * attn_bwd_dense has no argument for it (ATTN_ERR_INVALID_ARG) and the
+ * forward export returns ATTN_ERR_UNSUPPORTED */
+#define ATTN_MASK_ELEM 32u
 
 /* Gradient selection (enum order of the pages: Query = 0, Key = 1, Value = 2). */
 #define ATTN_WRT_DQ 1u
@@ -267,16 +274,20 @@ ATTN_API void attn_dense_strides_from_layout(const attn_dense_desc* d, attn_dens
 
 /*
  * attn_bwd_dense and attn_fwd_dense with explicit strides (the descriptor's
- * layout field is then ignored for addressing).  fp32 storage needs q, k, v
+ * layout field is then ignored for addressing; st NULL means the layout's
+ * strides).  attn_bwd_dense_strided also takes the per-element mask
+ * (ATTN_MASK_ELEM; NULL otherwise): bf16 storage only, and the workspace
+ * then also holds the mask as bits (attn_bwd_dense_workspace_bytes counts
+ * it when the flag is set).  fp32 storage needs q, k, v
  * and dy in the descriptor's layout (ATTN_ERR_UNSUPPORTED otherwise); bf16
  * takes any valid strides.  Results are bit-identical to the layout call on
  * the same values.
  */
 ATTN_API attn_status_t attn_bwd_dense_strided(const attn_dense_desc* d, const attn_dense_strides* st, const void* q,
                                               const void* k, const void* v, const void* dy, const float* key_mask,
-                                              const void* bias, const void* o, const float* lse, void* dq, void* dk,
-                                              void* dv, unsigned wrt_mask, void* workspace, size_t workspace_bytes,
-                                              void* stream);
+                                              const float* elem_mask, const void* bias, const void* o,
+                                              const float* lse, void* dq, void* dk, void* dv, unsigned wrt_mask,
+                                              void* workspace, size_t workspace_bytes, void* stream);
 ATTN_API attn_status_t attn_fwd_dense_strided(const attn_dense_desc* d, const attn_dense_strides* st, const void* q,
                                               const void* k, const void* v, const float* key_mask, const void* bias,
                                               void* o, float* lse, void* workspace, size_t workspace_bytes,

@@ -100,11 +100,45 @@ def test_workspace_errors(lib):
     assert _call(d, ws=FAKE + 28 * MB + 16) == bd.ATTN_ERR_WORKSPACE
 
 
-def _strided_call(desc, sts, q, k, v, dy, dq, dk, dv):
-    return int(bd.lib().attn_bwd_dense_strided(ctypes.byref(desc), ctypes.byref(sts), ctypes.c_void_p(q),
-                                               ctypes.c_void_p(k), ctypes.c_void_p(v), ctypes.c_void_p(dy), None,
-                                               None, None, None, ctypes.c_void_p(dq), ctypes.c_void_p(dk),
-                                               ctypes.c_void_p(dv), 7, None, 0, None))
+def _strided_call(desc, sts, q, k, v, dy, dq, dk, dv, elem=None, ws=None, ws_bytes=0):
+    return int(bd.lib().attn_bwd_dense_strided(ctypes.byref(desc), sts if sts is None else ctypes.byref(sts),
+                                               ctypes.c_void_p(q), ctypes.c_void_p(k), ctypes.c_void_p(v),
+                                               ctypes.c_void_p(dy), None, elem and ctypes.c_void_p(elem), None,
+                                               None, None, ctypes.c_void_p(dq), ctypes.c_void_p(dk),
+                                               ctypes.c_void_p(dv), 7, ws and ctypes.c_void_p(ws), ws_bytes, None))
+
+
+def test_elem_mask_checks(lib):
+    """The per-element mask: flag and pointer go together, fp32 storage and the
+    forward export refuse it, and the workspace grows by its row and column
+    bits (Sk and Sq rounded up to 64 bits per row/column)."""
+    B, H, Sq, Sk, D = 2, 3, 100, 130, 64
+    d = _desc(batch=B, heads=H, seq_q=Sq, seq_k=Sk, head_dim=D)
+    base = bd.attn_bwd_dense_workspace_bytes(d)
+    de = _desc(batch=B, heads=H, seq_q=Sq, seq_k=Sk, head_dim=D)
+    de.mask_flags |= bd.ATTN_MASK_ELEM
+    ew_q, ew_k = 6, 4  # ceil(130/32) = 5 -> 6 words, ceil(100/32) = 4
+    a256 = lambda x: (x + 255) // 256 * 256
+    assert bd.attn_bwd_dense_workspace_bytes(de) == base + a256(B * H * Sq * ew_q * 4) + a256(B * H * Sk * ew_k * 4)
+    qb, kb = FAKE, FAKE + 8 * MB
+    args = (qb, kb, kb + 2 * MB, qb + 2 * MB, FAKE + 16 * MB, FAKE + 18 * MB, FAKE + 20 * MB)
+    # flag without the pointer, pointer without the flag
+    assert _strided_call(de, None, *args) == bd.ATTN_ERR_INVALID_ARG
+    assert _strided_call(d, None, *args, elem=FAKE + 32 * MB) == bd.ATTN_ERR_INVALID_ARG
+    # with both the call reaches the workspace check
+    assert _strided_call(de, None, *args, elem=FAKE + 32 * MB) == bd.ATTN_ERR_WORKSPACE
+    # an output on the mask is refused
+    assert _strided_call(de, None, *args[:4], FAKE + 32 * MB, args[5], args[6],
+                         elem=FAKE + 32 * MB) == bd.ATTN_ERR_ALIAS
+    df = _desc(batch=B, heads=H, seq_q=Sq, seq_k=Sk, head_dim=D, dtype=bd.ATTN_DTYPE_F32)
+    df.mask_flags |= bd.ATTN_MASK_ELEM
+    assert bd.attn_bwd_dense_workspace_bytes(df) == 0
+    assert _strided_call(df, None, *args, elem=FAKE + 32 * MB) == bd.ATTN_ERR_UNSUPPORTED
+    st = bd.attn_fwd_dense(de, ctypes.c_void_p(qb), ctypes.c_void_p(kb), ctypes.c_void_p(kb + 2 * MB), None, None,
+                           ctypes.c_void_p(FAKE + 16 * MB), ctypes.c_void_p(FAKE + 18 * MB), None, 0, None)
+    assert st == bd.ATTN_ERR_UNSUPPORTED
+    # the layout call has no argument for it
+    assert _call(de) == bd.ATTN_ERR_INVALID_ARG
 
 
 def test_strided_fused_views(lib):
