@@ -15,9 +15,10 @@
 // where a column c is one (query row, head of the group) pair.  The K/V tile is
 // gathered page by page with TMA (3-D map over [slots, KVH, D]); pages past the
 // sequence are fetched at an out-of-range coordinate, i.e. read as zeros
-// without touching memory.  Passes: the CTA's own sequence first, then, for
-// every page it stores that other links share, those links in increasing link
-// order (only that page's 16 rows are live in such a pass).
+// without touching memory.  Passes: the CTA's own sequence first, then the
+// other links of the pages it stores, by link index; consecutive pages linked
+// from consecutive logical pages of one sequence share a pass (a shared prefix
+// costs one pass per (sequence, block), not one per page).
 //
 // Roles (512 threads): warp 0 TMA producer (K/V pages once, then Q/dY column
 // tiles through a 4-stage ring with the columns' statistics), warp 1 MMA
@@ -63,12 +64,16 @@ struct PageInfo {
 };
 
 // One pass = one (sequence, token mapping, live row range); the passes of a CTA
-// are enumerated identically by every role.
+// are enumerated identically by every role.  After the own pass come, for link
+// index li = 1, 2, ..., the li-th links of the pages this CTA stores; a run of
+// consecutive stored pages whose li-th links are consecutive logical pages of
+// one sequence (a shared prefix) is one pass with all their rows live.  Every
+// page still sees its links in increasing order.
 struct PassIter {
   const PagedParams* p;
   const PageInfo* pi;
   int s0, tb;
-  int j, li;                         // j = -1: own pass; else page j, link index li
+  int j, jn, li, lmax;               // j = -1: own pass; else pages [j, jn) at link index li
   int seq, tbase, ra, rb, r_begin, r_end, tile, ntiles;
 
   __device__ void load(int sq, int tbs, int a, int b, int rt) {
@@ -88,22 +93,31 @@ struct PassIter {
         j = 0;
         li = 1;
       } else {
-        ++li;
+        j = jn;
       }
-      while (j < 8 && !(pi->store[j] && li < pi->cnt[j])) {
-        ++j;
-        li = 1;
+      while (true) {
+        while (j < 8 && !(pi->store[j] && li < pi->cnt[j])) ++j;
+        if (j < 8) break;
+        if (++li >= lmax) return false;
+        j = 0;
       }
-      if (j >= 8) return false;
       const int link = p->links[pi->off[j] + li];
       const int s2 = link / p->max_pages, lp2 = link - s2 * p->max_pages;
-      load(s2, lp2 * p->page_size - 16 * j, 16 * j, 16 * j + 16, rt);
+      jn = j + 1;
+      while (jn < 8 && pi->store[jn] && li < pi->cnt[jn] && lp2 + (jn - j) < p->max_pages &&
+             p->links[pi->off[jn] + li] == link + (jn - j))
+        ++jn;
+      load(s2, lp2 * p->page_size - 16 * j, 16 * j, 16 * jn, rt);
       if (ntiles > 0) return true;
     }
   }
   __device__ bool begin(int rt) {
     j = -1;
+    jn = 0;
     li = 0;
+    lmax = 0;
+    for (int k = 0; k < 8; ++k)
+      if (pi->store[k] && pi->cnt[k] > lmax) lmax = pi->cnt[k];
     load(s0, tb * 128, 0, 128, rt);
     if (ntiles > 0) return true;
     return next_pass(rt);
@@ -183,7 +197,7 @@ __global__ void __launch_bounds__(512, 1)
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
   __shared__ PageInfo pinfo;
-  __shared__ int n_steps_sh;
+  __shared__ int n_steps_sh, any_store_sh;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // the KV heads of one token block are neighbours in the grid: together they
@@ -229,6 +243,9 @@ __global__ void __launch_bounds__(512, 1)
       pinfo.cnt[j] = cnt;
       pinfo.store[j] = st;
     }
+    int any = 0;
+    for (int j = 0; j < 8; ++j) any |= pinfo.store[j];
+    any_store_sh = any;
     // number of steps over all passes
     PassIter it{&p, &pinfo, s0, tb};
     int n = 0;
@@ -238,6 +255,10 @@ __global__ void __launch_bounds__(512, 1)
     }
     n_steps_sh = n;
   }
+  __syncthreads();
+  // a block whose pages are all stored by other CTAs (their owners) has
+  // nothing to write: leave before taking tensor memory (uniform exit)
+  if (!any_store_sh) return;
   if (warp == 1) {
     tmem_alloc(&tmem_base_sh, L::TMEM_COLS);
     tmem_relinquish();

@@ -16,8 +16,9 @@
 // rate on this GPU, which is still far above CUDA-core FMA.
 //
 // One CTA owns 64 tokens (four 16-token pages) of one sequence and one KV head
-// and walks the same passes as the GQA kernel: its own sequence, then for
-// every page it stores that other links share, those links in link order.
+// and walks the same passes as the GQA kernel: its own sequence, then the
+// other links of the pages it stores, in link order, consecutive pages of a
+// shared prefix in one pass.
 // A column is one (query row, head of the group) pair; a tile is 32 columns
 // (32 / G rows).  Per tile:
 //   phase A  warp (token tile tt, column octet n8): S^T and dP^T (16 x 8) with
@@ -64,13 +65,15 @@ struct MPageInfo {
   int store[4];   // this CTA stores the page
 };
 
-// The passes of a CTA: its own sequence over all 64 tokens, then for every
-// page j it stores, the other links of that page with only its 16 tokens live.
+// The passes of a CTA: its own sequence over all 64 tokens, then for link
+// index li = 1, 2, ... the li-th links of the pages it stores; consecutive
+// pages whose li-th links are consecutive logical pages of one sequence share
+// one pass (their rows all live), so every page still sees its links in order.
 struct MPass {
   const PagedParams* p;
   const MPageInfo* pi;
   int s0, tb;
-  int j, li;
+  int j, jn, li, lmax;
   int seq, tbase, ra, rb, r_begin, r_end, tile, ntiles;
 
   __device__ void load(int sq, int tbs, int a, int b, int rt) {
@@ -89,22 +92,31 @@ struct MPass {
         j = 0;
         li = 1;
       } else {
-        ++li;
+        j = jn;
       }
-      while (j < 4 && !(pi->store[j] && li < pi->cnt[j])) {
-        ++j;
-        li = 1;
+      while (true) {
+        while (j < 4 && !(pi->store[j] && li < pi->cnt[j])) ++j;
+        if (j < 4) break;
+        if (++li >= lmax) return false;
+        j = 0;
       }
-      if (j >= 4) return false;
       const int link = p->links[pi->off[j] + li];
       const int s2 = link / p->max_pages, lp2 = link - s2 * p->max_pages;
-      load(s2, lp2 * p->page_size - 16 * j, 16 * j, 16 * j + 16, rt);
+      jn = j + 1;
+      while (jn < 4 && pi->store[jn] && li < pi->cnt[jn] && lp2 + (jn - j) < p->max_pages &&
+             p->links[pi->off[jn] + li] == link + (jn - j))
+        ++jn;
+      load(s2, lp2 * p->page_size - 16 * j, 16 * j, 16 * jn, rt);
       if (ntiles > 0) return true;
     }
   }
   __device__ bool begin(int rt) {
     j = -1;
+    jn = 0;
     li = 0;
+    lmax = 0;
+    for (int k = 0; k < 4; ++k)
+      if (pi->store[k] && pi->cnt[k] > lmax) lmax = pi->cnt[k];
     load(s0, tb * BT, 0, BT, rt);
     if (ntiles > 0) return true;
     return next_pass(rt);
@@ -152,7 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ uint64_t bar_k, bar_full[2];
   __shared__ int abort_flag;
   __shared__ MPageInfo pinfo;
-  __shared__ int n_tiles_sh;
+  __shared__ int n_tiles_sh, any_store_sh;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tb = blockIdx.x, s0 = blockIdx.y, gkv = blockIdx.z;
@@ -185,6 +197,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       pinfo.cnt[j] = cnt;
       pinfo.store[j] = st;
     }
+    any_store_sh = pinfo.store[0] | pinfo.store[1] | pinfo.store[2] | pinfo.store[3];
     MPass it{&p, &pinfo, s0, tb};
     int n = 0;
     if (it.begin(RT)) {
@@ -194,12 +207,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     n_tiles_sh = n;
   }
   __syncthreads();
+  // pages all stored by their owners elsewhere: nothing to write (uniform exit)
+  if (!any_store_sh) return;
   const int n = n_tiles_sh;
   const uint32_t sbase = smem_addr(sm);
   const int oob_slot = p.num_pages * p.page_size;  // out-of-range coordinate: TMA fills zeros
 
   // thread 0 issues the copies; the pass iterator runs one tile ahead of use
-  MPass pf{&p, &pinfo, s0, tb};
+  // (the copy iterator lives in shared memory: only thread 0 uses it, and in
+  // registers it would be held by every thread)
+  __shared__ MPass pf;
   bool pf_live = false;
   auto issue_tile = [&](int stage) {
     const int r0 = pf.r_begin + pf.tile * RT;
@@ -224,6 +241,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int c = 0; c < 8; ++c) tma_load_3d(sm + K_OFF + c * CH + j * 16 * 128, &tm_k, &bar_k, c * 64, gkv, slot);
       tma_load_3d(sm + K_OFF + 8 * CH + j * 16 * 128, &tm_kp, &bar_k, 0, gkv, slot);
     }
+    pf.p = &p;
+    pf.pi = &pinfo;
+    pf.s0 = s0;
+    pf.tb = tb;
     pf_live = pf.begin(RT);
     for (int t = 0; t < 2 && t < n && pf_live; ++t) {
       issue_tile(t);

@@ -27,6 +27,7 @@ import argparse
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -254,10 +255,17 @@ def sweep(args) -> int:
     def emit(d):
         print(json.dumps(d), flush=True)
 
+    only = re.compile(args.only) if args.only else None
+
+    def want(tag):
+        return only is None or only.search(tag) is not None
+
     dense = [("C1", "dense_small_f32", {}), ("C2c", "dense_f32_causal", {}), ("C2w", "dense_f32_window", {}),
              ("C3", "dense_bf16_s2048", {}), ("C3 O+LSE supplied", "dense_bf16_s2048", {"supplied": True}),
              ("C4", "dense_bf16_cross", {})]
     for tag, name, opt in dense:
+        if not want(tag):
+            continue
         c = inputs.dense_config(name)
         dt = torch.float32 if c.dtype == "f32" else torch.bfloat16
         t = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda().to(dt)
@@ -301,35 +309,42 @@ def sweep(args) -> int:
               "peak_source": src})
 
     # forward export (O and LSE) on the headline shape
-    c = inputs.dense_config("dense_bf16_s2048")
-    t = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda().to(torch.bfloat16)
-    q, k, v = t(c.q), t(c.k), t(c.v)
-    km = torch.from_numpy(c.key_mask).cuda()
-    bias = t(c.bias)
-    fo = (torch.empty_like(q), torch.empty((c.batch, c.heads, c.seq_q), dtype=torch.float32, device="cuda"))
-    fcall = lambda: bd.dense_forward(q, k, v, layout=c.layout, causal=c.causal, window=c.window, key_mask=km,
-                                     bias=bias, outputs=fo)
-    fms, fms_min = timed(fcall, 20)
-    vp = visible_pairs(c.seq_q, c.seq_k, c.causal, c.window)
-    fflops = 4.0 * c.head_dim * vp * c.batch * c.heads
-    sample = [(0, 0), (3, 15)]
-    from oracle import attn_fwd_dense as fwd_oracle
-    t0 = time.perf_counter()
-    o_ref, lse_ref = fwd_oracle(c.q, c.k, c.v, layout=c.layout, causal=c.causal, window=c.window,
-                                key_mask=c.key_mask, bias=c.bias)
-    ft_or = time.perf_counter() - t0
-    g = fo[0].float().cpu().numpy()
-    ferr = max(float(np.max(np.abs(g[b_, :, h_] - o_ref[b_, :, h_])) / np.max(np.abs(o_ref[b_, :, h_])))
-               for b_, h_ in sample)
-    emit({"config": "C3 forward export (O, LSE)", "workload": "dense_bf16_s2048", "gpu_ms_median": fms,
-          "gpu_ms_min": fms_min, "counted_tflops": fflops / (fms * 1e-3) / 1e12,
-          "pct_of_bf16_peak": 100.0 * fflops / (fms * 1e-3) / 1e12 / peaks["bf16_tflops"],
-          "flops_counted": "4*D per visible pair (S = Q K^T, O = P V)", "max_err_rel_o": ferr, "tolerance": 2e-2,
-          "oracle_s": ft_or, "oracle_sample": "all 64 (batch, head) pairs, error on 2", "host_cores": cores,
-          "peak_source": src})
+    if want("C3 forward export"):
+        c = inputs.dense_config("dense_bf16_s2048")
+        t = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda().to(torch.bfloat16)
+        q, k, v = t(c.q), t(c.k), t(c.v)
+        km = torch.from_numpy(c.key_mask).cuda()
+        bias = t(c.bias)
+        fo = (torch.empty_like(q), torch.empty((c.batch, c.heads, c.seq_q), dtype=torch.float32, device="cuda"))
+        fcall = lambda: bd.dense_forward(q, k, v, layout=c.layout, causal=c.causal, window=c.window, key_mask=km,
+                                         bias=bias, outputs=fo)
+        fms, fms_min = timed(fcall, 20)
+        vp = visible_pairs(c.seq_q, c.seq_k, c.causal, c.window)
+        fflops = 4.0 * c.head_dim * vp * c.batch * c.heads
+        sample = [(0, 0), (3, 15)]
+        from oracle import attn_fwd_dense as fwd_oracle
+        t0 = time.perf_counter()
+        o_ref, lse_ref = fwd_oracle(c.q, c.k, c.v, layout=c.layout, causal=c.causal, window=c.window,
+                                    key_mask=c.key_mask, bias=c.bias)
+        ft_or = time.perf_counter() - t0
+        g = fo[0].float().cpu().numpy()
+        ferr = max(float(np.max(np.abs(g[b_, :, h_] - o_ref[b_, :, h_])) / np.max(np.abs(o_ref[b_, :, h_])))
+                   for b_, h_ in sample)
+        emit({"config": "C3 forward export (O, LSE)", "workload": "dense_bf16_s2048", "gpu_ms_median": fms,
+              "gpu_ms_min": fms_min, "counted_tflops": fflops / (fms * 1e-3) / 1e12,
+              "pct_of_bf16_peak": 100.0 * fflops / (fms * 1e-3) / 1e12 / peaks["bf16_tflops"],
+              "flops_counted": "4*D per visible pair (S = Q K^T, O = P V)", "max_err_rel_o": ferr, "tolerance": 2e-2,
+              "oracle_s": ft_or, "oracle_sample": "all 64 (batch, head) pairs, error on 2", "host_cores": cores,
+              "peak_source": src})
 
-    for tag, name in (("C5g", "paged_gqa"), ("C5m", "paged_mla")):
-        c = inputs.paged_config(name)
+    # the two paged workloads, then the same with a 1024-token prefix (64
+    # pages) shared by every sequence
+    for tag, name, ov in (("C5g", "paged_gqa", {}), ("C5m", "paged_mla", {}),
+                          ("C5g prefix1024", "paged_gqa", {"shared_prefix_pages": 64}),
+                          ("C5m prefix1024", "paged_mla", {"shared_prefix_pages": 64})):
+        if not want(tag):
+            continue
+        c = inputs.paged_config(name, **ov)
         tb = lambda x: None if x is None else torch.from_numpy(np.ascontiguousarray(x)).cuda().to(torch.bfloat16)
         dv = dict(q=tb(c.q), dy=tb(c.dy), k=tb(c.k_pool), v=tb(c.v_pool), qp=tb(c.qp), kp=tb(c.kp_pool))
         table = torch.from_numpy(c.page_table).cuda().contiguous()
@@ -374,12 +389,18 @@ def sweep(args) -> int:
                              c.q_pos[rows], page_size=c.page_size, kv_heads=c.kv_heads, v_pool=c.v_pool,
                              qp=None if c.qp is None else c.qp[rows], kp_pool=c.kp_pool, causal=c.causal)
         t_or = time.perf_counter() - t0
+        # compare the slots of pages that only the sampled sequences map
         owned = np.zeros(slots, bool)
         for s_ in pick:
             for tok in range(int(c.seq_len[s_])):
                 owned[int(c.page_table[s_, tok // c.page_size]) * c.page_size + tok % c.page_size] = True
+        for s_ in set(range(c.num_seqs)) - set(pick):
+            for lp in range((int(c.seq_len[s_]) + c.page_size - 1) // c.page_size):
+                ph = int(c.page_table[s_, lp])
+                owned[ph * c.page_size:(ph + 1) * c.page_size] = False
         err = max(rel(g, w, owned) for g, w in zip(first, ref))
-        emit({"config": tag, "workload": name, "gpu_ms_median": ms, "gpu_ms_min": ms_min,
+        emit({"config": tag, "workload": name, **({"shared_prefix_pages": ov["shared_prefix_pages"]} if ov else {}),
+              "gpu_ms_median": ms, "gpu_ms_min": ms_min,
               "counted_tflops": flops / (ms * 1e-3) / 1e12,
               "pct_of_bf16_peak": 100.0 * flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
               "algorithmic_gbs": alg_bytes / (ms * 1e-3) / 1e9,
@@ -444,6 +465,7 @@ def main():
     ap.add_argument("--heads", type=int, default=None, help="override H (profiling runs on a smaller case)")
     ap.add_argument("--sweep", action="store_true",
                     help="time every configuration once against its oracle sample (one JSON line each)")
+    ap.add_argument("--only", default=None, help="--sweep: only the configurations whose tag matches this regex")
     args = ap.parse_args()
     if args.sweep:
         return sweep(args)

@@ -72,6 +72,12 @@ CASES = [
          value_dim=512, position_dim=64, causal=False),
     dict(seed=27, num_seqs=4, len_lo=40, len_hi=200, queries_per_seq=8, heads=32, kv_heads=1, key_dim=512,
          value_dim=512, position_dim=64, causal=True, shared_prefix_pages=2),
+    # long shared prefixes: 20 pages (2.5 blocks of 8 pages) and 9 pages (2.25
+    # MLA blocks of 4 pages) shared by every sequence
+    dict(seed=28, num_seqs=12, len_lo=330, len_hi=700, queries_per_seq=32, heads=16, kv_heads=4, key_dim=128,
+         value_dim=128, causal=True, shared_prefix_pages=20),
+    dict(seed=29, num_seqs=10, len_lo=150, len_hi=400, queries_per_seq=6, heads=16, kv_heads=1, key_dim=512,
+         value_dim=512, position_dim=64, causal=True, shared_prefix_pages=9),
 ]
 
 
@@ -97,6 +103,41 @@ def test_paged_parity(bd, kw):
     assert torch.all(dk[torch.from_numpy(~valid).cuda()] == 0)
     assert torch.all(dvv[torch.from_numpy(~valid).cuda()] == 0)
     assert torch.isfinite(dk).all() and torch.isfinite(dvv).all()
+
+
+@pytest.mark.parametrize("mla", [False, True], ids=["gqa", "mla"])
+def test_paged_shared_at_offsets(bd, mla):
+    """Shared pages at other logical positions: sequence 2 maps its logical
+    pages 0..P-2 to sequence 0's physical pages 1..P-1 (links that follow one
+    another at an offset) and its page P-1 to a free page; sequence 3 swaps two
+    of its shared pages (links that do not follow one another)."""
+    P = 11
+    kw = dict(seed=41 + int(mla), num_seqs=5, len_lo=240, len_hi=420, causal=True, shared_prefix_pages=P)
+    if mla:
+        kw.update(queries_per_seq=6, heads=16, kv_heads=1, key_dim=512, value_dim=512, position_dim=64)
+    else:
+        kw.update(queries_per_seq=24, heads=8, kv_heads=2, key_dim=128, value_dim=128)
+    c = inputs.paged_case(name="t", scale=0.5, **kw)
+    t = c.page_table.copy()
+    used = {int(t[s, lp]) for s in range(c.num_seqs) for lp in range(-(-int(c.seq_len[s]) // c.page_size))}
+    free = [q for q in range(c.num_pages) if q not in used]
+    t[2, :P - 1] = c.page_table[0, 1:P]
+    t[2, P - 1] = free[0]
+    t[3, [1, 3]] = t[3, [3, 1]]
+    c.page_table = t
+    src, ps = int(c.page_table[0, 0]), c.page_size  # the free page's rows: finite values of another page
+    for pool in (c.k_pool, c.v_pool, c.kp_pool):
+        if pool is not None:
+            pool[free[0] * ps:(free[0] + 1) * ps] = pool[src * ps:(src + 1) * ps]
+    dv = to_dev(c, bd)
+    dk_ref, dv_ref, lse_ref, delta_ref = oracle(c)
+    lse, delta = gpu_stats(bd, c, dv)
+    dk, dvv = gpu_bwd(bd, c, dv, lse, delta)
+    bd.check_device_error()
+    assert rel(dk, dk_ref) < TOL
+    assert rel(dvv, dv_ref) < TOL
+    again = gpu_bwd(bd, c, dv, lse, delta)
+    assert all(torch.equal(a, b) for a, b in zip((dk, dvv), again))
 
 
 def test_paged_bit_stable(bd):
