@@ -18,7 +18,7 @@ using attn::api_ok;
 struct PagedSizes {
   size_t q_bytes, qp_bytes, dy_bytes, k_bytes, v_bytes, kp_bytes, table_bytes, meta_bytes, stat_bytes;
   size_t ws_bytes;
-  size_t off_count, off_off, off_fill, off_links;
+  size_t off_count, off_off, off_fill, off_links, off_heavy;
 };
 
 size_t a256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -64,7 +64,8 @@ attn_status_t check_paged_desc(const attn_paged_desc* d, PagedSizes* z) {
   z->off_off = z->off_count + a256(size_t(d->num_pages) * 4);
   z->off_fill = z->off_off + a256(size_t(d->num_pages + 1) * 4);
   z->off_links = z->off_fill + a256(size_t(d->num_pages) * 4);
-  z->ws_bytes = z->off_links + a256(size_t(d->num_seqs) * d->max_pages_per_seq * 4 + 4);
+  z->off_heavy = z->off_links + a256(size_t(d->num_seqs) * d->max_pages_per_seq * 4 + 4);
+  z->ws_bytes = z->off_heavy + a256(size_t(d->num_seqs) * ((d->max_pages_per_seq + 3) / 4) * d->kv_heads * 4 + 4);
   return ATTN_OK;
 }
 
@@ -102,6 +103,7 @@ attn_status_t fill_params(const attn_paged_desc* d, const PagedSizes& z, const i
   p->link_off = reinterpret_cast<int32_t*>(ws + z.off_off);
   p->link_fill = reinterpret_cast<int32_t*>(ws + z.off_fill);
   p->links = reinterpret_cast<int32_t*>(ws + z.off_links);
+  p->heavy = reinterpret_cast<int32_t*>(ws + z.off_heavy);
   p->err = attn::device_error_word();
   if (!p->err) return api_fail(ATTN_ERR_CUDA, "no CUDA device / symbol address unavailable");
   return ATTN_OK;
@@ -192,12 +194,15 @@ ATTN_API attn_status_t attn_bwd_paged(const attn_paged_desc* d, const void* q, c
     else
       mm.q = mm.qp = mm.dy = mm.k;
     if (!enc) return api_fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed");
-    attn::timing_mark_begin(3, s);
+    attn::timing_mark_begin(4, s);
     cudaError_t e = attn::launch_paged_prep(p, s);
     attn::timing_mark(s);
     if (e == cudaSuccess) e = attn::launch_paged_zero_unlinked(p, s);
     attn::timing_mark(s);
     if (e == cudaSuccess) e = attn::launch_paged_mla_mma(mm, p, s);
+    attn::timing_mark(s);
+    // blocks whose shared pages carry many links: split over clusters
+    if (e == cudaSuccess) e = attn::launch_paged_mla_mma_split(mm, p, s);
     attn::timing_mark(s);
     attn::timing_mark_end();
     if (e != cudaSuccess) return api_fail(ATTN_ERR_CUDA, "paged launch failed: %s", cudaGetErrorString(e));

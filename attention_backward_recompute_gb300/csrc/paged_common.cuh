@@ -41,6 +41,7 @@ struct PagedParams {
   int32_t* link_off;           // [num_pages + 1]
   int32_t* link_fill;          // [num_pages]
   int32_t* links;              // [S * max_pages]: link ids s*max_pages+lp grouped by page
+  int32_t* heavy;              // [S, ceil(max_pages / 4), KVH]: MLA blocks left to the split kernel
   uint32_t* err;
 };
 

@@ -35,6 +35,8 @@ struct PagedMlaMaps {
 };
 bool mla_mma_supported(const PagedParams& p);
 cudaError_t launch_paged_mla_mma(const PagedMlaMaps& m, const PagedParams& p, cudaStream_t s);
+// the blocks launch_paged_mla_mma flagged as heavy, by clusters of CTAs
+cudaError_t launch_paged_mla_mma_split(const PagedMlaMaps& m, const PagedParams& p, cudaStream_t s);
 // MLA row statistics on the same path; q, qp, dy maps with box (64, G, 64/G)
 cudaError_t launch_paged_mla_stats_mma(const PagedMlaMaps& m, const PagedParams& p, cudaStream_t s);
 // MLA query side (dQ, dQp) on the same path, from lse / delta; maps as for the statistics

@@ -155,6 +155,64 @@ __device__ __forceinline__ uint32_t swz(uint32_t base, int row, int piece) {
   return base + row * 128 + (((piece ^ row) & 7) << 4);
 }
 
+// Cluster primitives of the split kernel.
+__device__ __forceinline__ int cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return static_cast<int>(r);
+}
+__device__ __forceinline__ int cluster_index() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return static_cast<int>(r);
+}
+__device__ __forceinline__ int cluster_count() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return static_cast<int>(r);
+}
+// All threads of all CTAs of the cluster: shared-memory writes before it are
+// visible to the other CTAs' reads after it.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+// the same shared-memory offset in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t map_rank(uint32_t addr, int rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float4 ld_cluster_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+// bounded wait for copies still in flight (after an abort)
+__device__ __forceinline__ void drain(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_test(bar, parity))
+    if (global_timer_ns() - t0 > ATTN_WAIT_TIMEOUT_NS) return;
+}
+
+// A block whose link passes (shared pages) exceed this many tiles is left to
+// the split kernel: its owner alone would serialise the other sequences' work.
+constexpr int kHeavyLinkTiles = 128;
+constexpr int kCL = 8;                       // CTAs of a split cluster; CTA r sums tokens [8r, 8r + 8)
+constexpr int RED_STRIDE = kLat + kPos + 8;  // floats per token row of a partial (+8: bank spread)
+static_assert(BT * RED_STRIDE * 4 <= BYTES, "a partial fits the tiles' shared memory");
+static_assert(BT % kCL == 0, "tokens split evenly over the cluster");
+
+// SPLIT = false: one CTA per (64-token block, sequence, KV head); a block it
+// stores is finished here unless its link passes are heavy, which it flags.
+// SPLIT = true: persistent clusters of kCL CTAs take the flagged blocks (heavy
+// block k to cluster k mod clusters); CTA r of a cluster runs the block's
+// tiles r, r + kCL, ..., the partial sums meet in shared memory and each CTA
+// adds its 8 tokens' partials over the cluster in rank order (a fixed order:
+// the result does not depend on the number of clusters or on timing).
+template <bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     mla_mma_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_qp,
                    const __grid_constant__ CUtensorMap tm_dy, const __grid_constant__ CUtensorMap tm_k,
@@ -164,232 +222,361 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ uint64_t bar_k, bar_full[2];
   __shared__ int abort_flag;
   __shared__ MPageInfo pinfo;
-  __shared__ int n_tiles_sh, any_store_sh;
+  __shared__ int n_tiles_sh, any_store_sh, heavy_sh;
+  // (the copy iterator lives in shared memory: only thread 0 uses it, and in
+  // registers it would be held by every thread)
+  __shared__ MPass pf;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int tb = blockIdx.x, s0 = blockIdx.y, gkv = blockIdx.z;
-  const int npg = pages_of(seq_len_of(p, s0), p.page_size);
-  if (tb * 4 >= npg) return;  // no token of this sequence in the block (uniform exit)
   const int G = p.G, RT = BC / G;
+  const int nblk = (p.max_pages + 3) / 4;
+  const int rank = SPLIT ? cluster_rank() : 0;
+  const int ncta = SPLIT ? kCL : 1;  // CTAs sharing one block's tiles
   const Abort ab{&abort_flag, p.err};
+  const uint32_t sbase = smem_addr(sm);
+  const int oob_slot = p.num_pages * p.page_size;  // out-of-range coordinate: TMA fills zeros
+  const int tt = warp & 3;        // token tile (16 tokens, = page tt of the block)
+  const int n8 = warp >> 2;       // phase A: column octet
+  const int dr = warp >> 2;       // phase B: dim quarter
+  const int g8 = lane >> 2, t4 = lane & 3;
+  const float kInf = __int_as_float(0x7f800000);
+  const uint32_t p_base = sbase + P_OFF, ds_base = sbase + P_OFF + PS;
 
+  if (!SPLIT) {
+    const int tb = blockIdx.x, s0 = blockIdx.y;
+    if (tb * 4 >= pages_of(seq_len_of(p, s0), p.page_size)) {  // no token of the sequence here (uniform)
+      if (threadIdx.x == 0) p.heavy[(s0 * nblk + tb) * p.KVH + blockIdx.z] = 0;
+      return;
+    }
+  }
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(&bar_k, 1);
     mbar_init(&bar_full[0], 1);
     mbar_init(&bar_full[1], 1);
     mbar_fence_init();
-    for (int j = 0; j < 4; ++j) {
-      const int lp = tb * 4 + j;
-      int ph = -1, off = 0, cnt = 0, st = 0;
-      if (lp < npg) {
-        ph = p.page_table[static_cast<int64_t>(s0) * p.max_pages + lp];
-        if (ph >= 0 && ph < p.num_pages) {
-          off = p.link_off[ph];
-          cnt = p.link_off[ph + 1] - off;
-          st = cnt > 0 && p.links[off] == s0 * p.max_pages + lp;
-        } else {
-          ph = -1;
-        }
-      }
-      pinfo.phys[j] = ph;
-      pinfo.off[j] = off;
-      pinfo.cnt[j] = cnt;
-      pinfo.store[j] = st;
-    }
-    any_store_sh = pinfo.store[0] | pinfo.store[1] | pinfo.store[2] | pinfo.store[3];
-    MPass it{&p, &pinfo, s0, tb};
-    int n = 0;
-    if (it.begin(RT)) {
-      do ++n;
-      while (it.advance(RT));
-    }
-    n_tiles_sh = n;
   }
-  __syncthreads();
-  // pages all stored by their owners elsewhere: nothing to write (uniform exit)
-  if (!any_store_sh) return;
-  const int n = n_tiles_sh;
-  const uint32_t sbase = smem_addr(sm);
-  const int oob_slot = p.num_pages * p.page_size;  // out-of-range coordinate: TMA fills zeros
+  // thread 0's copy bookkeeping (split: running over the blocks of a persistent CTA)
+  int issued[2] = {0, 0}, k_issued = 0;
+  int tc = 0;       // tiles this CTA consumed: tile u uses stage u & 1, phase u >> 1
+  int k_phase = 0;  // blocks this CTA loaded keys for
 
-  // thread 0 issues the copies; the pass iterator runs one tile ahead of use
-  // (the copy iterator lives in shared memory: only thread 0 uses it, and in
-  // registers it would be held by every thread)
-  __shared__ MPass pf;
-  bool pf_live = false;
-  auto issue_tile = [&](int stage) {
-    const int r0 = pf.r_begin + pf.tile * RT;
-    uint64_t* bar = &bar_full[stage];
-    mbar_arrive_expect_tx(bar, STAGE);
-    uint8_t* st = sm + ST_OFF + stage * STAGE;
-    for (int c = 0; c < 8; ++c) {
-      tma_load_3d(st + c * CQ, &tm_q, bar, c * 64, gkv * G, r0);
-      tma_load_3d(st + (9 + c) * CQ, &tm_dy, bar, c * 64, gkv * G, r0);
-    }
-    tma_load_3d(st + 8 * CQ, &tm_qp, bar, 0, gkv * G, r0);
-  };
-  if (threadIdx.x == 0 && n > 0) {
-    tma_prefetch_map(&tm_q);
-    tma_prefetch_map(&tm_qp);
-    tma_prefetch_map(&tm_dy);
-    tma_prefetch_map(&tm_k);
-    tma_prefetch_map(&tm_kp);
-    mbar_arrive_expect_tx(&bar_k, 9 * CH);
-    for (int j = 0; j < 4; ++j) {
-      const int slot = pinfo.phys[j] >= 0 ? pinfo.phys[j] * p.page_size : oob_slot;
-      for (int c = 0; c < 8; ++c) tma_load_3d(sm + K_OFF + c * CH + j * 16 * 128, &tm_k, &bar_k, c * 64, gkv, slot);
-      tma_load_3d(sm + K_OFF + 8 * CH + j * 16 * 128, &tm_kp, &bar_k, 0, gkv, slot);
-    }
-    pf.p = &p;
-    pf.pi = &pinfo;
-    pf.s0 = s0;
-    pf.tb = tb;
-    pf_live = pf.begin(RT);
-    for (int t = 0; t < 2 && t < n && pf_live; ++t) {
-      issue_tile(t);
-      pf_live = pf.advance(RT);
-    }
-  }
-
-  const int tt = warp & 3;        // token tile (16 tokens, = page tt of the block)
-  const int n8 = warp >> 2;       // phase A: column octet
-  const int dr = warp >> 2;       // phase B: dim quarter
-  const int g8 = lane >> 2, t4 = lane & 3;
-  float acc[16][4], accp[2][4];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-#pragma unroll
-  for (int i = 0; i < 2; ++i) accp[i][0] = accp[i][1] = accp[i][2] = accp[i][3] = 0.f;
-
-  MPass it{&p, &pinfo, s0, tb};
-  bool live = n > 0 && it.begin(RT);
-  bool ok = n > 0 ? mbar_wait_warp(&bar_k, 0, ab) : true;
-  const float kInf = __int_as_float(0x7f800000);
-  const uint32_t p_base = sbase + P_OFF, ds_base = sbase + P_OFF + PS;
-  for (int t = 0; t < n; ++t) {
-    const int stage = t & 1;
-    const uint32_t stb = sbase + ST_OFF + stage * STAGE;
-    // column data of this thread's two phase-A columns
-    const int r0 = it.r_begin + it.tile * RT;
-    float lse_c[2], dl_c[2];
-    int pos_c[2];
-    bool col_ok[2];
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int c = n8 * 8 + 2 * t4 + e;
-      const int r = r0 + c / G, hh = gkv * G + c % G;
-      col_ok[e] = r < it.r_end;
-      const size_t si = static_cast<size_t>(col_ok[e] ? r : 0) * p.H + hh;
-      lse_c[e] = col_ok[e] ? p.lse[si] * kLog2e : kInf;
-      dl_c[e] = col_ok[e] ? p.delta[si] : 0.f;
-      pos_c[e] = col_ok[e] ? (p.causal ? p.q_pos[r] : 0x7fffffff) : -1;
-    }
-    if (ok) ok = mbar_wait_warp(&bar_full[stage], (t >> 1) & 1, ab);
-    if (ok) {
-      // ---------------------------------------------------------------- phase A
-      float sacc[4] = {0.f, 0.f, 0.f, 0.f}, dpacc[4] = {0.f, 0.f, 0.f, 0.f};
-      const int arow = tt * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
-      const int ahalf = lane >> 4;
-      const int brow = n8 * 8 + (lane & 7);
-      const int bm = lane >> 3;  // matrix of the x4 B load: 0,1 Q (k halves), 2,3 dY
-#pragma unroll 2
-      for (int kc = 0; kc < 8; ++kc) {
-#pragma unroll
-        for (int kp = 0; kp < 4; ++kp) {
-          uint32_t a[4], bq[4];
-          ldsm_x4(swz(sbase + K_OFF + kc * CH, arow, 2 * kp + ahalf), a);
-          const uint32_t bchunk = stb + ((bm >> 1) ? (9 + kc) : kc) * CQ;
-          ldsm_x4(swz(bchunk, brow, 2 * kp + (bm & 1)), bq);
-          mma_16816(sacc, a, bq[0], bq[1]);
-          mma_16816(dpacc, a, bq[2], bq[3]);
+  auto run_block = [&](int tb, int s0, int gkv, int item) {
+    __syncthreads();  // the previous block's readers of pinfo are done
+    if (threadIdx.x == 0) {
+      const int npg = pages_of(seq_len_of(p, s0), p.page_size);
+      for (int j = 0; j < 4; ++j) {
+        const int lp = tb * 4 + j;
+        int ph = -1, off = 0, cnt = 0, st = 0;
+        if (lp < npg) {
+          ph = p.page_table[static_cast<int64_t>(s0) * p.max_pages + lp];
+          if (ph >= 0 && ph < p.num_pages) {
+            off = p.link_off[ph];
+            cnt = p.link_off[ph + 1] - off;
+            st = cnt > 0 && p.links[off] == s0 * p.max_pages + lp;
+          } else {
+            ph = -1;
+          }
         }
+        pinfo.phys[j] = ph;
+        pinfo.off[j] = off;
+        pinfo.cnt[j] = cnt;
+        pinfo.store[j] = st;
       }
-#pragma unroll
-      for (int kp = 0; kp < 4; ++kp) {
-        uint32_t a[4], b0, b1;
-        ldsm_x4(swz(sbase + K_OFF + 8 * CH, arow, 2 * kp + ahalf), a);
-        ldsm_x2(swz(stb + 8 * CQ, brow, 2 * kp + (bm & 1)), b0, b1);
-        mma_16816(sacc, a, b0, b1);
+      const int any = pinfo.store[0] | pinfo.store[1] | pinfo.store[2] | pinfo.store[3];
+      MPass it{&p, &pinfo, s0, tb};
+      int n_all = 0, n_own = 0;
+      if (any && it.begin(RT)) {
+        do {
+          ++n_all;
+          n_own += it.j < 0 ? 1 : 0;
+        } while (it.advance(RT));
       }
-      // P^T and dS^T of this warp's 16 tokens x 8 columns
-#pragma unroll
-      for (int hr = 0; hr < 2; ++hr) {
-        const int i = tt * 16 + g8 + 8 * hr;  // block-local token
-        const int tok = it.tbase + i;
-        const bool tok_ok = i >= it.ra && i < it.rb && tok < seq_len_of(p, it.seq);
-        float pv[2], dsv[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const bool vis = tok_ok && col_ok[e] && tok <= pos_c[e] && lse_c[e] > -kInf;
-          const float pe = ex2_approx(fmaf(sacc[2 * hr + e], p.scale_log2, -lse_c[e]));
-          // select, not multiply: dP of a tail or unowned slot may be NaN
-          pv[e] = vis ? pe : 0.f;
-          dsv[e] = vis ? pe * (dpacc[2 * hr + e] - dl_c[e]) * p.scale : 0.f;
-        }
-        const int c = n8 * 8 + 2 * t4;
-        *reinterpret_cast<uint32_t*>(sm + P_OFF + i * PS_STRIDE + c * 2) = pack_bf16x2(pv[0], pv[1]);
-        *reinterpret_cast<uint32_t*>(sm + P_OFF + PS + i * PS_STRIDE + c * 2) = pack_bf16x2(dsv[0], dsv[1]);
-      }
+      const int heavy = !SPLIT && any && n_all - n_own > kHeavyLinkTiles;
+      if (!SPLIT) p.heavy[item] = heavy;
+      any_store_sh = any;
+      heavy_sh = heavy;
+      n_tiles_sh = n_all > rank ? (n_all - rank + ncta - 1) / ncta : 0;  // tiles rank, rank + ncta, ...
     }
     __syncthreads();
-    if (ok && !abort_flag) {
-      // ---------------------------------------------------------------- phase B
-      const int arow = tt * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
-      const int bm = lane >> 3;
-#pragma unroll
-      for (int ks = 0; ks < 2; ++ks) {
-        uint32_t ads[4], ap[4];
-        const uint32_t aoff = arow * PS_STRIDE + (ks * 16 + 8 * (lane >> 4)) * 2;
-        ldsm_x4(ds_base + aoff, ads);
-        ldsm_x4(p_base + aoff, ap);
-        const int krow = ks * 16 + (lane & 7) + 8 * (bm & 1);  // column index = B row
-#pragma unroll
-        for (int np = 0; np < 8; ++np) {  // pairs of 8-dim tiles: dims 128 dr + 16 np
-          const int chunk = 2 * dr + (np >> 2);
-          const int piece = 2 * (np & 3) + (bm >> 1);
-          uint32_t bq[4], bd[4];
-          ldsm_x4_t(swz(stb + chunk * CQ, krow, piece), bq);
-          ldsm_x4_t(swz(stb + (9 + chunk) * CQ, krow, piece), bd);
-          mma_16816(acc[2 * np], ads, bq[0], bq[1]);
-          mma_16816(acc[2 * np + 1], ads, bq[2], bq[3]);
-          mma_16816(acc[2 * np], ap, bd[0], bd[1]);
-          mma_16816(acc[2 * np + 1], ap, bd[2], bd[3]);
-        }
-        uint32_t bqp[4];
-        ldsm_x4_t(swz(stb + 8 * CQ, krow, 2 * dr + (bm >> 1)), bqp);
-        mma_16816(accp[0], ads, bqp[0], bqp[1]);
-        mma_16816(accp[1], ads, bqp[2], bqp[3]);
+    // pages all stored by their owners elsewhere, or a heavy block: nothing to
+    // do here (uniform over the CTA, and over the cluster: same block)
+    if (!any_store_sh || heavy_sh) return;
+    const int n = n_tiles_sh;
+    const int tc0 = tc;
+
+    bool pf_live = false;
+    auto issue_tile = [&](int u) {
+      const int stage = u & 1;
+      const int r0 = pf.r_begin + pf.tile * RT;
+      uint64_t* bar = &bar_full[stage];
+      mbar_arrive_expect_tx(bar, STAGE);
+      uint8_t* st = sm + ST_OFF + stage * STAGE;
+      for (int c = 0; c < 8; ++c) {
+        tma_load_3d(st + c * CQ, &tm_q, bar, c * 64, gkv * G, r0);
+        tma_load_3d(st + (9 + c) * CQ, &tm_dy, bar, c * 64, gkv * G, r0);
+      }
+      tma_load_3d(st + 8 * CQ, &tm_qp, bar, 0, gkv * G, r0);
+      if (SPLIT) ++issued[stage];
+    };
+    auto pf_next = [&]() -> bool {  // the next tile this CTA owns
+      for (int k = 0; k < ncta; ++k)
+        if (!pf.advance(RT)) return false;
+      return true;
+    };
+    if (threadIdx.x == 0 && n > 0 && !abort_flag) {
+      tma_prefetch_map(&tm_q);
+      tma_prefetch_map(&tm_qp);
+      tma_prefetch_map(&tm_dy);
+      tma_prefetch_map(&tm_k);
+      tma_prefetch_map(&tm_kp);
+      mbar_arrive_expect_tx(&bar_k, 9 * CH);
+      if (SPLIT) ++k_issued;
+      for (int j = 0; j < 4; ++j) {
+        const int slot = pinfo.phys[j] >= 0 ? pinfo.phys[j] * p.page_size : oob_slot;
+        for (int c = 0; c < 8; ++c) tma_load_3d(sm + K_OFF + c * CH + j * 16 * 128, &tm_k, &bar_k, c * 64, gkv, slot);
+        tma_load_3d(sm + K_OFF + 8 * CH + j * 16 * 128, &tm_kp, &bar_k, 0, gkv, slot);
+      }
+      pf.p = &p;
+      pf.pi = &pinfo;
+      pf.s0 = s0;
+      pf.tb = tb;
+      pf_live = pf.begin(RT);
+      for (int k = 0; k < rank && pf_live; ++k) pf_live = pf.advance(RT);
+      for (int t = 0; t < 2 && t < n && pf_live; ++t) {
+        issue_tile(tc0 + t);
+        pf_live = pf_next();
       }
     }
-    __syncthreads();  // stage and P^T/dS^T buffers free
-    if (threadIdx.x == 0 && pf_live && !abort_flag) {
-      issue_tile(stage);  // tile t + 2 into the stage just freed
-      pf_live = pf.advance(RT);
-    }
-    live = it.advance(RT);
-  }
-  (void)live;
-  // every issued copy was consumed (each tile waited for its stage); store the
-  // pages this CTA owns, one row per token, zeros where nothing was added
-  if (n > 0 && (!ok || abort_flag)) return;
-  if (!pinfo.store[tt]) return;
-  const int slot_base = pinfo.phys[tt] * p.page_size;
+
+    float acc[16][4], accp[2][4];
 #pragma unroll
-  for (int hr = 0; hr < 2; ++hr) {
-    const int64_t prow = static_cast<int64_t>(slot_base + g8 + 8 * hr) * p.KVH + gkv;
-    if (p.wrt & 2u) {
-      __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.dk_pool) + prow * kLat + 128 * dr + 2 * t4;
+    for (int i = 0; i < 16; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) accp[i][0] = accp[i][1] = accp[i][2] = accp[i][3] = 0.f;
+
+    MPass it{&p, &pinfo, s0, tb};
+    bool live = n > 0 && it.begin(RT);
+    for (int k = 0; k < rank && live; ++k) live = it.advance(RT);
+    bool ok = true;
+    if (n > 0) {
+      ok = mbar_wait_warp(&bar_k, k_phase & 1, ab);
+      ++k_phase;
+    }
+    for (int t = 0; t < n; ++t) {
+      const int u = tc0 + t, stage = u & 1;  // running tile number of this CTA
+      const uint32_t stb = sbase + ST_OFF + stage * STAGE;
+      // column data of this thread's two phase-A columns
+      const int r0 = it.r_begin + it.tile * RT;
+      float lse_c[2], dl_c[2];
+      int pos_c[2];
+      bool col_ok[2];
+  #pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int c = n8 * 8 + 2 * t4 + e;
+        const int r = r0 + c / G, hh = gkv * G + c % G;
+        col_ok[e] = r < it.r_end;
+        const size_t si = static_cast<size_t>(col_ok[e] ? r : 0) * p.H + hh;
+        lse_c[e] = col_ok[e] ? p.lse[si] * kLog2e : kInf;
+        dl_c[e] = col_ok[e] ? p.delta[si] : 0.f;
+        pos_c[e] = col_ok[e] ? (p.causal ? p.q_pos[r] : 0x7fffffff) : -1;
+      }
+      if (ok) ok = mbar_wait_warp(&bar_full[stage], (u >> 1) & 1, ab);
+      if (ok) {
+        // ---------------------------------------------------------------- phase A
+        float sacc[4] = {0.f, 0.f, 0.f, 0.f}, dpacc[4] = {0.f, 0.f, 0.f, 0.f};
+        const int arow = tt * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
+        const int ahalf = lane >> 4;
+        const int brow = n8 * 8 + (lane & 7);
+        const int bm = lane >> 3;  // matrix of the x4 B load: 0,1 Q (k halves), 2,3 dY
+  #pragma unroll 2
+        for (int kc = 0; kc < 8; ++kc) {
+  #pragma unroll
+          for (int kp = 0; kp < 4; ++kp) {
+            uint32_t a[4], bq[4];
+            ldsm_x4(swz(sbase + K_OFF + kc * CH, arow, 2 * kp + ahalf), a);
+            const uint32_t bchunk = stb + ((bm >> 1) ? (9 + kc) : kc) * CQ;
+            ldsm_x4(swz(bchunk, brow, 2 * kp + (bm & 1)), bq);
+            mma_16816(sacc, a, bq[0], bq[1]);
+            mma_16816(dpacc, a, bq[2], bq[3]);
+          }
+        }
+  #pragma unroll
+        for (int kp = 0; kp < 4; ++kp) {
+          uint32_t a[4], b0, b1;
+          ldsm_x4(swz(sbase + K_OFF + 8 * CH, arow, 2 * kp + ahalf), a);
+          ldsm_x2(swz(stb + 8 * CQ, brow, 2 * kp + (bm & 1)), b0, b1);
+          mma_16816(sacc, a, b0, b1);
+        }
+        // P^T and dS^T of this warp's 16 tokens x 8 columns
+  #pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+          const int i = tt * 16 + g8 + 8 * hr;  // block-local token
+          const int tok = it.tbase + i;
+          const bool tok_ok = i >= it.ra && i < it.rb && tok < seq_len_of(p, it.seq);
+          float pv[2], dsv[2];
+  #pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const bool vis = tok_ok && col_ok[e] && tok <= pos_c[e] && lse_c[e] > -kInf;
+            const float pe = ex2_approx(fmaf(sacc[2 * hr + e], p.scale_log2, -lse_c[e]));
+            // select, not multiply: dP of a tail or unowned slot may be NaN
+            pv[e] = vis ? pe : 0.f;
+            dsv[e] = vis ? pe * (dpacc[2 * hr + e] - dl_c[e]) * p.scale : 0.f;
+          }
+          const int c = n8 * 8 + 2 * t4;
+          *reinterpret_cast<uint32_t*>(sm + P_OFF + i * PS_STRIDE + c * 2) = pack_bf16x2(pv[0], pv[1]);
+          *reinterpret_cast<uint32_t*>(sm + P_OFF + PS + i * PS_STRIDE + c * 2) = pack_bf16x2(dsv[0], dsv[1]);
+        }
+      }
+      __syncthreads();
+      if (ok && !abort_flag) {
+        // ---------------------------------------------------------------- phase B
+        const int arow = tt * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
+        const int bm = lane >> 3;
+  #pragma unroll
+        for (int ks = 0; ks < 2; ++ks) {
+          uint32_t ads[4], ap[4];
+          const uint32_t aoff = arow * PS_STRIDE + (ks * 16 + 8 * (lane >> 4)) * 2;
+          ldsm_x4(ds_base + aoff, ads);
+          ldsm_x4(p_base + aoff, ap);
+          const int krow = ks * 16 + (lane & 7) + 8 * (bm & 1);  // column index = B row
+  #pragma unroll
+          for (int np = 0; np < 8; ++np) {  // pairs of 8-dim tiles: dims 128 dr + 16 np
+            const int chunk = 2 * dr + (np >> 2);
+            const int piece = 2 * (np & 3) + (bm >> 1);
+            uint32_t bq[4], bd[4];
+            ldsm_x4_t(swz(stb + chunk * CQ, krow, piece), bq);
+            ldsm_x4_t(swz(stb + (9 + chunk) * CQ, krow, piece), bd);
+            mma_16816(acc[2 * np], ads, bq[0], bq[1]);
+            mma_16816(acc[2 * np + 1], ads, bq[2], bq[3]);
+            mma_16816(acc[2 * np], ap, bd[0], bd[1]);
+            mma_16816(acc[2 * np + 1], ap, bd[2], bd[3]);
+          }
+          uint32_t bqp[4];
+          ldsm_x4_t(swz(stb + 8 * CQ, krow, 2 * dr + (bm >> 1)), bqp);
+          mma_16816(accp[0], ads, bqp[0], bqp[1]);
+          mma_16816(accp[1], ads, bqp[2], bqp[3]);
+        }
+      }
+      __syncthreads();  // stage and P^T/dS^T buffers free
+      if (threadIdx.x == 0 && pf_live && !abort_flag) {
+        issue_tile(u + 2);  // owned tile t + 2, into the stage just freed
+        pf_live = pf_next();
+      }
+      for (int k = 0; k < ncta && live; ++k) live = it.advance(RT);
+    }
+    (void)live;
+    tc = tc0 + n;
+    if (!SPLIT) {
+      // every issued copy was consumed (each tile waited for its stage); store
+      // the pages this CTA owns, one row per token, zeros where nothing was added
+      if (n > 0 && (!ok || abort_flag)) return;
+      if (!pinfo.store[tt]) return;
+      const int slot_base = pinfo.phys[tt] * p.page_size;
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr) {
+        const int64_t prow = static_cast<int64_t>(slot_base + g8 + 8 * hr) * p.KVH + gkv;
+        if (p.wrt & 2u) {
+          __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.dk_pool) + prow * kLat + 128 * dr + 2 * t4;
+#pragma unroll
+          for (int nt = 0; nt < 16; ++nt)
+            *reinterpret_cast<uint32_t*>(o + nt * 8) = pack_bf16x2(acc[nt][2 * hr], acc[nt][2 * hr + 1]);
+        }
+        if (p.wrt & 8u) {
+          __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.dkp_pool) + prow * kPos + 16 * dr + 2 * t4;
+#pragma unroll
+          for (int nt = 0; nt < 2; ++nt)
+            *reinterpret_cast<uint32_t*>(o + nt * 8) = pack_bf16x2(accp[nt][2 * hr], accp[nt][2 * hr + 1]);
+        }
+      }
+      return;
+    }
+    // split: this CTA's partial sums to shared memory as [64 tokens][576 dims]
+    // (the tiles' buffers are free: the loop ended on a barrier after the last
+    // copy was consumed)
+    float* red = reinterpret_cast<float*>(sm);
+#pragma unroll
+    for (int hr = 0; hr < 2; ++hr) {
+      float* row = red + (tt * 16 + g8 + 8 * hr) * RED_STRIDE;
 #pragma unroll
       for (int nt = 0; nt < 16; ++nt)
-        *reinterpret_cast<uint32_t*>(o + nt * 8) = pack_bf16x2(acc[nt][2 * hr], acc[nt][2 * hr + 1]);
-    }
-    if (p.wrt & 8u) {
-      __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.dkp_pool) + prow * kPos + 16 * dr + 2 * t4;
+        *reinterpret_cast<float2*>(row + 128 * dr + 8 * nt + 2 * t4) = make_float2(acc[nt][2 * hr], acc[nt][2 * hr + 1]);
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt)
-        *reinterpret_cast<uint32_t*>(o + nt * 8) = pack_bf16x2(accp[nt][2 * hr], accp[nt][2 * hr + 1]);
+        *reinterpret_cast<float2*>(row + kLat + 16 * dr + 8 * nt + 2 * t4) =
+            make_float2(accp[nt][2 * hr], accp[nt][2 * hr + 1]);
     }
+    cluster_sync();
+    // tokens [8 rank, 8 rank + 8): the partials of CTAs 0..kCL-1 added in that order
+    constexpr int kQuads = (kLat + kPos) / 4;
+    const bool good = !abort_flag;
+    for (int idx = threadIdx.x; idx < (BT / kCL) * kQuads; idx += kThreads) {
+      const int i = (BT / kCL) * rank + idx / kQuads, d = 4 * (idx % kQuads);
+      const uint32_t a = smem_addr(red + i * RED_STRIDE + d);
+      float4 sum = ld_cluster_f4(map_rank(a, 0));
+#pragma unroll
+      for (int r = 1; r < kCL; ++r) {
+        const float4 v = ld_cluster_f4(map_rank(a, r));
+        sum.x += v.x;
+        sum.y += v.y;
+        sum.z += v.z;
+        sum.w += v.w;
+      }
+      const int j = i >> 4;
+      if (good && pinfo.store[j]) {
+        const int64_t prow = (static_cast<int64_t>(pinfo.phys[j]) * p.page_size + (i & 15)) * p.KVH + gkv;
+        const uint2 w = make_uint2(pack_bf16x2(sum.x, sum.y), pack_bf16x2(sum.z, sum.w));
+        if (d < kLat) {
+          if (p.wrt & 2u) *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.dk_pool) + prow * kLat + d) = w;
+        } else if (p.wrt & 8u) {
+          *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.dkp_pool) + prow * kPos + (d - kLat)) = w;
+        }
+      }
+    }
+    cluster_sync();  // the other CTAs have read this CTA's partial
+  };
+
+  if (!SPLIT) {
+    run_block(blockIdx.x, blockIdx.y, blockIdx.z, (blockIdx.y * nblk + blockIdx.x) * p.KVH + blockIdx.z);
+    return;
+  }
+  // split: the flagged blocks in flag order, heavy block k to cluster k mod clusters
+  __shared__ int items_sh[kThreads];
+  __shared__ int warp_cnt[kThreads / 32];
+  const int cid = cluster_index(), ncl = cluster_count();
+  const int nitems = p.S * nblk * p.KVH;
+  int base = 0;
+  for (int c0 = 0; c0 < nitems; c0 += kThreads) {
+    const int i = c0 + threadIdx.x;
+    const bool f = i < nitems && p.heavy[i] != 0;
+    const uint32_t bal = __ballot_sync(0xffffffffu, f);
+    if (lane == 0) warp_cnt[warp] = __popc(bal);
+    __syncthreads();
+    int before = 0, total = 0;
+    for (int w = 0; w < kThreads / 32; ++w) {
+      const int c = warp_cnt[w];
+      before += w < warp ? c : 0;
+      total += c;
+    }
+    const int k = base + before + __popc(bal & ((1u << lane) - 1u));
+    // this cluster's heavy indices in [base, base + total): cid + ncl * m, m in [m0, m1)
+    const int m0 = base > cid ? (base - cid + ncl - 1) / ncl : 0;
+    const int m1 = base + total > cid ? (base + total - cid + ncl - 1) / ncl : 0;
+    if (f && k % ncl == cid) items_sh[k / ncl - m0] = i;
+    __syncthreads();
+    for (int m = 0; m < m1 - m0; ++m) {
+      const int item = items_sh[m];
+      const int gkv = item % p.KVH, rest = item / p.KVH;
+      run_block(rest % nblk, rest / nblk, gkv, item);
+    }
+    base += total;
+    __syncthreads();  // items_sh and warp_cnt are rewritten next
+  }
+  // copies still in flight after an abort land before the CTA exits
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < 2; ++st)
+      if (issued[st] > 0) drain(&bar_full[st], static_cast<uint32_t>((issued[st] - 1) & 1));
+    if (k_issued > 0) drain(&bar_k, static_cast<uint32_t>((k_issued - 1) & 1));
   }
 }
 
@@ -855,11 +1042,44 @@ cudaError_t launch_paged_mla_stats_mma(const PagedMlaMaps& m, const PagedParams&
 cudaError_t launch_paged_mla_mma(const PagedMlaMaps& m, const PagedParams& p, cudaStream_t s) {
   if (p.num_pages == 0 || p.S == 0 || p.max_pages == 0) return cudaSuccess;
   const int smem = BYTES + 1024;
-  cudaError_t e = cudaFuncSetAttribute(mla_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  auto kern = mla_mma_kernel<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid((p.max_pages + 3) / 4, p.S, p.KVH);
-  mla_mma_kernel<<<grid, kThreads, smem, s>>>(m.q, m.qp, m.dy, m.k, m.kp, p);
+  kern<<<grid, kThreads, smem, s>>>(m.q, m.qp, m.dy, m.k, m.kp, p);
   return cudaGetLastError();
+}
+
+cudaError_t launch_paged_mla_mma_split(const PagedMlaMaps& m, const PagedParams& p, cudaStream_t s) {
+  if (p.num_pages == 0 || p.S == 0 || p.max_pages == 0) return cudaSuccess;
+  const int smem = BYTES + 1024;
+  auto kern = mla_mma_kernel<true>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = kCL;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  // as many clusters as fit the GPU at once (one CTA per SM), cached per device
+  static int clusters[64] = {0};
+  int dev = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  int ncl = dev < 64 ? clusters[dev] : 0;
+  if (ncl == 0) {
+    cfg.gridDim = dim3(kCL, 1, 1);
+    if ((e = cudaOccupancyMaxActiveClusters(&ncl, kern, &cfg)) != cudaSuccess) return e;
+    if (ncl < 1) return cudaErrorInvalidConfiguration;
+    if (dev < 64) clusters[dev] = ncl;
+  }
+  cfg.gridDim = dim3(ncl * kCL, 1, 1);
+  return cudaLaunchKernelEx(&cfg, kern, m.q, m.qp, m.dy, m.k, m.kp, p);
 }
 
 }  // namespace attn

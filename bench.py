@@ -361,6 +361,13 @@ def sweep(args) -> int:
                                          heads=c.heads, kv_heads=c.kv_heads, page_size=c.page_size,
                                          causal=c.causal, outputs=outs, qp=dv["qp"], kp_pool=dv["kp"])
         ms, ms_min = timed(call, 20)
+        # per-kernel split of one call: links, zero store, history (MLA: + the cluster-split kernel)
+        names = ["links", "zero_unlinked", "history"] + (["history_split"] if c.position_dim else [])
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
+        bd.attn_set_timing_events([e.cuda_event for e in evs])
+        call()
+        torch.cuda.synchronize()
+        kernel_ms = {n: evs[i].elapsed_time(evs[i + 1]) for i, n in enumerate(names)}
         stats_call = lambda: bd.paged_row_stats(dv["q"], dv["k"], dv["v"], dv["dy"], table, meta, heads=c.heads,
                                                 kv_heads=c.kv_heads, page_size=c.page_size, causal=c.causal,
                                                 qp=dv["qp"], kp_pool=dv["kp"])
@@ -405,7 +412,7 @@ def sweep(args) -> int:
               "pct_of_bf16_peak": 100.0 * flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
               "algorithmic_gbs": alg_bytes / (ms * 1e-3) / 1e9,
               "pct_of_hbm_peak": 100.0 * alg_bytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
-              "row_stats_ms": stats_ms,
+              "row_stats_ms": stats_ms, "kernel_ms": kernel_ms,
               "max_err_rel": err, "tolerance": 2e-2, "bit_stable_5_runs": bool(stable),
               "oracle_s_sample": t_or, "oracle_sample": f"{len(pick)} of {c.num_seqs} sequences",
               "oracle_s_extrapolated": t_or * c.num_seqs / len(pick), "host_cores": cores,

@@ -78,6 +78,12 @@ CASES = [
          value_dim=128, causal=True, shared_prefix_pages=20),
     dict(seed=29, num_seqs=10, len_lo=150, len_hi=400, queries_per_seq=6, heads=16, kv_heads=1, key_dim=512,
          value_dim=512, position_dim=64, causal=True, shared_prefix_pages=9),
+    # MLA blocks whose shared pages carry more than 128 link tiles go to the
+    # cluster-split kernel: 11 other sequences x 24 (resp. 12) tiles each
+    dict(seed=30, num_seqs=12, len_lo=150, len_hi=300, queries_per_seq=24, heads=32, kv_heads=1, key_dim=512,
+         value_dim=512, position_dim=64, causal=True, shared_prefix_pages=9),
+    dict(seed=32, num_seqs=12, len_lo=150, len_hi=300, queries_per_seq=24, heads=32, kv_heads=2, key_dim=512,
+         value_dim=512, position_dim=64, causal=False, shared_prefix_pages=5),
 ]
 
 
@@ -138,6 +144,20 @@ def test_paged_shared_at_offsets(bd, mla):
     assert rel(dvv, dv_ref) < TOL
     again = gpu_bwd(bd, c, dv, lse, delta)
     assert all(torch.equal(a, b) for a, b in zip((dk, dvv), again))
+
+
+def test_paged_mla_split_bit_stable(bd):
+    """The cluster-split MLA blocks sum their partials in a fixed order."""
+    c = inputs.paged_case(name="t", seed=33, num_seqs=12, len_lo=150, len_hi=300, queries_per_seq=24, heads=32,
+                          kv_heads=1, key_dim=512, value_dim=512, position_dim=64, scale=0.5, shared_prefix_pages=6)
+    dv = to_dev(c, bd)
+    lse, delta = gpu_stats(bd, c, dv)
+    first = gpu_bwd(bd, c, dv, lse, delta)
+    for _ in range(3):
+        again = gpu_bwd(bd, c, dv, lse, delta)
+        for a, b in zip(first, again):
+            assert torch.equal(a, b)
+    bd.check_device_error()
 
 
 def test_paged_bit_stable(bd):
