@@ -200,7 +200,7 @@ __device__ __forceinline__ void drain(uint64_t* bar, uint32_t parity) {
 // A block whose link passes (shared pages) exceed this many tiles is left to
 // the split kernel: its owner alone would serialise the other sequences' work.
 constexpr int kHeavyLinkTiles = 128;
-constexpr int kCL = 8;                       // CTAs of a split cluster; CTA r sums tokens [8r, 8r + 8)
+constexpr int kCL = 16;                      // CTAs of a split cluster; CTA r sums tokens [4r, 4r + 4)
 constexpr int RED_STRIDE = kLat + kPos + 8;  // floats per token row of a partial (+8: bank spread)
 static_assert(BT * RED_STRIDE * 4 <= BYTES, "a partial fits the tiles' shared memory");
 static_assert(BT % kCL == 0, "tokens split evenly over the cluster");
@@ -210,7 +210,7 @@ static_assert(BT % kCL == 0, "tokens split evenly over the cluster");
 // SPLIT = true: persistent clusters of kCL CTAs take the flagged blocks (heavy
 // block k to cluster k mod clusters); CTA r of a cluster runs the block's
 // tiles r, r + kCL, ..., the partial sums meet in shared memory and each CTA
-// adds its 8 tokens' partials over the cluster in rank order (a fixed order:
+// adds its BT / kCL tokens' partials over the cluster in rank order (a fixed order:
 // the result does not depend on the number of clusters or on timing).
 template <bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -507,7 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             make_float2(accp[nt][2 * hr], accp[nt][2 * hr + 1]);
     }
     cluster_sync();
-    // tokens [8 rank, 8 rank + 8): the partials of CTAs 0..kCL-1 added in that order
+    // tokens [4 rank, 4 rank + 4): the partials of CTAs 0..kCL-1 added in that order
     constexpr int kQuads = (kLat + kPos) / 4;
     const bool good = !abort_flag;
     for (int idx = threadIdx.x; idx < (BT / kCL) * kQuads; idx += kThreads) {
@@ -1056,6 +1056,8 @@ cudaError_t launch_paged_mla_mma_split(const PagedMlaMaps& m, const PagedParams&
   auto kern = mla_mma_kernel<true>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
+  // 16 CTAs per cluster is above the portable 8
+  if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) != cudaSuccess) return e;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeClusterDimension;
   at[0].val.clusterDim.x = kCL;

@@ -364,6 +364,9 @@ def sweep(args) -> int:
         # per-kernel split of one call: links, zero store, history (MLA: + the cluster-split kernel)
         names = ["links", "zero_unlinked", "history"] + (["history_split"] if c.position_dim else [])
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
+        for e in evs:  # CUDA events are created on first record
+            e.record()
+        torch.cuda.synchronize()
         bd.attn_set_timing_events([e.cuda_event for e in evs])
         call()
         torch.cuda.synchronize()
