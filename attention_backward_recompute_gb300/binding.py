@@ -92,6 +92,9 @@ _SIG = {
     "attn_bwd_paged_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(attn_paged_desc)]),
     "attn_bwd_paged": (ctypes.c_int32, [ctypes.POINTER(attn_paged_desc), _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                         _P, _P, _P, ctypes.c_uint, _P, ctypes.c_size_t, _P]),
+    "attn_bwd_paged_compact": (ctypes.c_int32, [ctypes.POINTER(attn_paged_desc), _P, _P, _P, _P, _P, _P, _P, _P,
+                                                _P, _P, _P, ctypes.c_int64, _P, _P, _P, ctypes.c_uint, _P,
+                                                ctypes.c_size_t, _P]),
     "attn_paged_row_stats": (ctypes.c_int32, [ctypes.POINTER(attn_paged_desc), _P, _P, _P, _P, _P, _P, _P, _P,
                                               _P, _P, _P, ctypes.c_size_t, _P]),
     "attn_bwd_paged_query": (ctypes.c_int32, [ctypes.POINTER(attn_paged_desc), _P, _P, _P, _P, _P, _P, _P, _P,
@@ -445,8 +448,12 @@ def paged_query_backward(q, k_pool, v_pool, dy, page_table, seq_meta, *, heads, 
 
 def paged_backward(q, k_pool, v_pool, dy, page_table, seq_meta, lse, delta, *, heads, kv_heads, page_size=16,
                    causal=True, scale=0.0, qp=None, kp_pool=None, wrt=None, outputs=None, workspace=None,
-                   stream=None):
-    """Pool gradients (dk_pool, dv_pool) for GQA or (dk_pool, dkp_pool) for MLA."""
+                   stream=None, history_pages=None):
+    """Pool gradients (dk_pool, dv_pool) for GQA or (dk_pool, dkp_pool) for MLA.
+
+    ``history_pages`` (int32 CUDA tensor of physical page indices) selects the
+    compact history call: only the listed pages' rows are computed and
+    written, the others are left as they are in ``outputs``."""
     import torch
     d = _paged_desc_for(q, dy, k_pool, page_table, seq_meta, heads, kv_heads, page_size, causal, scale, qp, kp_pool)
     mla = qp is not None
@@ -461,8 +468,17 @@ def paged_backward(q, k_pool, v_pool, dy, page_table, seq_meta, lse, delta, *, h
     n = attn_bwd_paged_workspace_bytes(d)
     if workspace is None:
         workspace = torch.empty(max(n, 256), dtype=torch.uint8, device=q.device)
-    st = attn_bwd_paged(d, _ptr(q), _ptr(qp), _ptr(k_pool), _ptr(v_pool), _ptr(kp_pool), _ptr(dy), _ptr(page_table),
-                        _ptr(seq_meta), _ptr(lse), _ptr(delta), _ptr(dk), _ptr(dv), _ptr(dkp), wrt, _ptr(workspace),
-                        workspace.numel(), _stream_handle(stream))
+    if history_pages is None:
+        st = attn_bwd_paged(d, _ptr(q), _ptr(qp), _ptr(k_pool), _ptr(v_pool), _ptr(kp_pool), _ptr(dy),
+                            _ptr(page_table), _ptr(seq_meta), _ptr(lse), _ptr(delta), _ptr(dk), _ptr(dv), _ptr(dkp),
+                            wrt, _ptr(workspace), workspace.numel(), _stream_handle(stream))
+    else:
+        if history_pages.dtype != torch.int32 or not history_pages.is_contiguous():
+            raise ValueError("history_pages must be a contiguous int32 tensor")
+        st = int(lib().attn_bwd_paged_compact(ctypes.byref(d), _ptr(q), _ptr(qp), _ptr(k_pool), _ptr(v_pool),
+                                              _ptr(kp_pool), _ptr(dy), _ptr(page_table), _ptr(seq_meta), _ptr(lse),
+                                              _ptr(delta), _ptr(history_pages), history_pages.numel(), _ptr(dk),
+                                              _ptr(dv), _ptr(dkp), wrt, _ptr(workspace), workspace.numel(),
+                                              _stream_handle(stream)))
     _check(st)
     return (dk, dkp) if mla else (dk, dv)

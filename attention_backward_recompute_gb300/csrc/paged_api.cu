@@ -18,7 +18,7 @@ using attn::api_ok;
 struct PagedSizes {
   size_t q_bytes, qp_bytes, dy_bytes, k_bytes, v_bytes, kp_bytes, table_bytes, meta_bytes, stat_bytes;
   size_t ws_bytes;
-  size_t off_count, off_off, off_fill, off_links, off_heavy;
+  size_t off_count, off_off, off_fill, off_links, off_heavy, off_listed;
 };
 
 size_t a256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -65,7 +65,8 @@ attn_status_t check_paged_desc(const attn_paged_desc* d, PagedSizes* z) {
   z->off_fill = z->off_off + a256(size_t(d->num_pages + 1) * 4);
   z->off_links = z->off_fill + a256(size_t(d->num_pages) * 4);
   z->off_heavy = z->off_links + a256(size_t(d->num_seqs) * d->max_pages_per_seq * 4 + 4);
-  z->ws_bytes = z->off_heavy + a256(size_t(d->num_seqs) * ((d->max_pages_per_seq + 3) / 4) * d->kv_heads * 4 + 4);
+  z->off_listed = z->off_heavy + a256(size_t(d->num_seqs) * ((d->max_pages_per_seq + 3) / 4) * d->kv_heads * 4 + 4);
+  z->ws_bytes = z->off_listed + a256(size_t(d->num_pages) + 4);
   return ATTN_OK;
 }
 
@@ -104,6 +105,7 @@ attn_status_t fill_params(const attn_paged_desc* d, const PagedSizes& z, const i
   p->link_fill = reinterpret_cast<int32_t*>(ws + z.off_fill);
   p->links = reinterpret_cast<int32_t*>(ws + z.off_links);
   p->heavy = reinterpret_cast<int32_t*>(ws + z.off_heavy);
+  p->listed = nullptr;  // every page (the compact call points it at its map)
   p->err = attn::device_error_word();
   if (!p->err) return api_fail(ATTN_ERR_CUDA, "no CUDA device / symbol address unavailable");
   return ATTN_OK;
@@ -132,9 +134,29 @@ ATTN_API attn_status_t attn_bwd_paged(const attn_paged_desc* d, const void* q, c
                                       const int32_t* page_table, const int32_t* seq_meta, const float* lse,
                                       const float* delta, void* dk_pool, void* dv_pool, void* dkp_pool,
                                       unsigned wrt_mask, void* workspace, size_t workspace_bytes, void* stream) {
+  return attn_bwd_paged_compact(d, q, qp, k_pool, v_pool, kp_pool, dy, page_table, seq_meta, lse, delta, nullptr, -1,
+                                dk_pool, dv_pool, dkp_pool, wrt_mask, workspace, workspace_bytes, stream);
+}
+
+ATTN_API attn_status_t attn_bwd_paged_compact(const attn_paged_desc* d, const void* q, const void* qp,
+                                              const void* k_pool, const void* v_pool, const void* kp_pool,
+                                              const void* dy, const int32_t* page_table, const int32_t* seq_meta,
+                                              const float* lse, const float* delta, const int32_t* history_pages,
+                                              int64_t num_history_pages, void* dk_pool, void* dv_pool,
+                                              void* dkp_pool, unsigned wrt_mask, void* workspace,
+                                              size_t workspace_bytes, void* stream) {
   PagedSizes z;
   attn_status_t st = check_paged_desc(d, &z);
   if (st != ATTN_OK) return st;
+  // num_history_pages < 0 (the full call): every page; else the listed ones
+  const bool compact = num_history_pages >= 0;
+  if (compact && num_history_pages > 0 && !history_pages)
+    return api_fail(ATTN_ERR_INVALID_ARG, "history_pages is NULL");
+  if (compact && num_history_pages >= (int64_t(1) << 31))
+    return api_fail(ATTN_ERR_UNSUPPORTED, "too many history pages");
+  if (reinterpret_cast<uintptr_t>(history_pages) & 3u)
+    return api_fail(ATTN_ERR_INVALID_ARG, "history_pages must be 4-byte aligned");
+  const size_t hist_bytes = compact ? size_t(num_history_pages) * 4 : 0;
   const bool mla = d->position_dim > 0;
   const unsigned allowed = mla ? (ATTN_WRT_DK | ATTN_WRT_DKP) : (ATTN_WRT_DK | ATTN_WRT_DV);
   if (wrt_mask == 0 || (wrt_mask & ~allowed))
@@ -155,7 +177,8 @@ ATTN_API attn_status_t attn_bwd_paged(const attn_paged_desc* d, const void* q, c
   struct R { const void* p; size_t n; };
   const R ins[] = {{q, z.q_bytes}, {qp, mla ? z.qp_bytes : 0}, {k_pool, z.k_bytes}, {v_pool, mla ? 0 : z.v_bytes},
                    {kp_pool, mla ? z.kp_bytes : 0}, {dy, z.dy_bytes}, {page_table, z.table_bytes},
-                   {seq_meta, z.meta_bytes}, {lse, z.stat_bytes}, {delta, z.stat_bytes}, {workspace, workspace_bytes}};
+                   {seq_meta, z.meta_bytes}, {lse, z.stat_bytes}, {delta, z.stat_bytes}, {workspace, workspace_bytes},
+                   {history_pages, hist_bytes}};
   const R outs[] = {{want_dk ? dk_pool : nullptr, z.k_bytes}, {want_dv ? dv_pool : nullptr, z.v_bytes},
                     {want_dkp ? dkp_pool : nullptr, z.kp_bytes}};
   for (int i = 0; i < 3; ++i) {
@@ -164,7 +187,7 @@ ATTN_API attn_status_t attn_bwd_paged(const attn_paged_desc* d, const void* q, c
     for (int j = i + 1; j < 3; ++j)
       if (overlap(outs[i].p, outs[i].n, outs[j].p, outs[j].n)) return api_fail(ATTN_ERR_ALIAS, "outputs %d and %d overlap", i, j);
   }
-  if (d->num_pages == 0) return api_ok();
+  if (d->num_pages == 0 || (compact && num_history_pages == 0)) return api_ok();
   if (!workspace || workspace_bytes < z.ws_bytes)
     return api_fail(ATTN_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", z.ws_bytes, workspace_bytes);
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return api_fail(ATTN_ERR_WORKSPACE, "workspace must be 256-byte aligned");
@@ -178,6 +201,12 @@ ATTN_API attn_status_t attn_bwd_paged(const attn_paged_desc* d, const void* q, c
   p.dkp_pool = dkp_pool;
   p.wrt = wrt_mask;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (compact) {
+    // the map of listed pages, ahead of the kernels that read it
+    p.listed = static_cast<uint8_t*>(workspace) + z.off_listed;
+    const cudaError_t e = attn::launch_paged_listed(p, history_pages, num_history_pages, s);
+    if (e != cudaSuccess) return api_fail(ATTN_ERR_CUDA, "paged launch failed: %s", cudaGetErrorString(e));
+  }
   if (mla && attn::mla_mma_supported(p)) {
     // links, zeros for pages no link references, then one CTA per 64-token
     // block of every sequence (warp-level tensor path)

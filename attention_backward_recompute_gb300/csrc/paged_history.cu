@@ -233,7 +233,7 @@ __global__ void __launch_bounds__(512, 1)
         if (ph >= 0 && ph < p.num_pages) {
           off = p.link_off[ph];
           cnt = p.link_off[ph + 1] - off;
-          st = cnt > 0 && p.links[off] == s0 * p.max_pages + lp;
+          st = cnt > 0 && p.links[off] == s0 * p.max_pages + lp && (!p.listed || p.listed[ph]);
         } else {
           ph = -1;
         }

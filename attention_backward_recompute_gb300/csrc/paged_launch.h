@@ -35,6 +35,8 @@ struct PagedMlaMaps {
 };
 bool mla_mma_supported(const PagedParams& p);
 cudaError_t launch_paged_mla_mma(const PagedMlaMaps& m, const PagedParams& p, cudaStream_t s);
+// compact history: p.listed[page] = 1 for the n listed pages (zero otherwise)
+cudaError_t launch_paged_listed(const PagedParams& p, const int32_t* pages, int64_t n, cudaStream_t s);
 // the blocks launch_paged_mla_mma flagged as heavy, by clusters of CTAs
 cudaError_t launch_paged_mla_mma_split(const PagedMlaMaps& m, const PagedParams& p, cudaStream_t s);
 // MLA row statistics on the same path; q, qp, dy maps with box (64, G, 64/G)

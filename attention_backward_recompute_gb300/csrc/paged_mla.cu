@@ -86,6 +86,7 @@ __global__ void __launch_bounds__(512, 1) mla_history_kernel(const __nv_bfloat16
   const uint32_t q_bytes = G * kLat * 2, qp_bytes = G * kPos * 2, dy_bytes = G * kLat * 2;
   const uint32_t stage_bytes = q_bytes + qp_bytes + dy_bytes;
   const Abort ab{&abort_flag, p.err};
+  if (p.listed && !p.listed[page]) return;  // compact history: a page not asked for (uniform)
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(&bar_full[0], 1);

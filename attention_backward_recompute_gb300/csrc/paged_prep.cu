@@ -112,12 +112,35 @@ __global__ void zero_unlinked_kernel(PagedParams p, void* pool, int dim) {
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int page = static_cast<int>(i / per_page);
-    if (p.link_count[page] != 0) continue;
+    if (p.link_count[page] != 0 || (p.listed && !p.listed[page])) continue;
     reinterpret_cast<uint4*>(pool)[i] = z;
   }
 }
 
+// compact history: mark the listed pages (an entry outside the pool raises
+// kErrBadPage and is skipped)
+__global__ void mark_listed_kernel(PagedParams p, const int32_t* pages, int64_t n) {
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int page = pages[i];
+    if (page < 0 || page >= p.num_pages) {
+      atomicOr(p.err, kErrBadPage);
+      continue;
+    }
+    p.listed[page] = 1;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_paged_listed(const PagedParams& p, const int32_t* pages, int64_t n, cudaStream_t s) {
+  cudaError_t e;
+  if ((e = cudaMemsetAsync(p.listed, 0, p.num_pages, s)) != cudaSuccess) return e;
+  if (n <= 0) return cudaSuccess;
+  const int64_t blocks = (n + 255) / 256 < 1024 ? (n + 255) / 256 : 1024;
+  mark_listed_kernel<<<static_cast<int>(blocks), 256, 0, s>>>(p, pages, n);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_paged_prep(const PagedParams& p, cudaStream_t s) {
   cudaError_t e;

@@ -371,6 +371,19 @@ def sweep(args) -> int:
         call()
         torch.cuda.synchronize()
         kernel_ms = {n: evs[i].elapsed_time(evs[i + 1]) for i, n in enumerate(names)}
+        compact = None
+        if not ov:
+            # compact history listing the referenced pages only: the zero store
+            # of the unreferenced pool pages is skipped
+            ref_pages = np.unique(np.concatenate([c.page_table[s_, :(int(c.seq_len[s_]) + c.page_size - 1) // c.page_size]
+                                                  for s_ in range(c.num_seqs)])).astype(np.int32)
+            hist = torch.from_numpy(ref_pages).cuda()
+            ccall = lambda: bd.paged_backward(dv["q"], dv["k"], dv["v"], dv["dy"], table, meta, lse, delta,
+                                              heads=c.heads, kv_heads=c.kv_heads, page_size=c.page_size,
+                                              causal=c.causal, outputs=outs, qp=dv["qp"], kp_pool=dv["kp"],
+                                              history_pages=hist)
+            cms, _ = timed(ccall, 20)
+            compact = {"gpu_ms_median": cms, "listed_pages": int(ref_pages.size), "pool_pages": int(c.num_pages)}
         stats_call = lambda: bd.paged_row_stats(dv["q"], dv["k"], dv["v"], dv["dy"], table, meta, heads=c.heads,
                                                 kv_heads=c.kv_heads, page_size=c.page_size, causal=c.causal,
                                                 qp=dv["qp"], kp_pool=dv["kp"])
@@ -415,7 +428,7 @@ def sweep(args) -> int:
               "pct_of_bf16_peak": 100.0 * flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
               "algorithmic_gbs": alg_bytes / (ms * 1e-3) / 1e9,
               "pct_of_hbm_peak": 100.0 * alg_bytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
-              "row_stats_ms": stats_ms, "kernel_ms": kernel_ms,
+              "row_stats_ms": stats_ms, "kernel_ms": kernel_ms, "compact_history_referenced_pages": compact,
               "max_err_rel": err, "tolerance": 2e-2, "bit_stable_5_runs": bool(stable),
               "oracle_s_sample": t_or, "oracle_sample": f"{len(pick)} of {c.num_seqs} sequences",
               "oracle_s_extrapolated": t_or * c.num_seqs / len(pick), "host_cores": cores,

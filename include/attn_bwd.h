@@ -241,6 +241,31 @@ ATTN_API attn_status_t attn_bwd_paged(const attn_paged_desc* d, const void* q, c
                                       unsigned wrt_mask, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Compact history: attn_bwd_paged restricted to the physical pages listed in
+ * history_pages (int32 [num_history_pages], any order, repeats allowed), as
+ * ruDNN src/paged_attention/ordered_kernel.rs does when its compact_history
+ * flag maps the launch grid through a history_pages list.  Every pool row of
+ * a listed page is written exactly once, with the same values as the full
+ * call (zeros for slots no valid token owns; bit-identical except in MLA
+ * blocks split over a cluster, whose partial sums may group differently when
+ * pages of the block are not listed); rows of pages not listed are
+ * not written, and the work of the pages not listed (their link passes and
+ * the zero store of unreferenced ones) is skipped.  An entry outside
+ * [0, num_pages) is skipped and reported by attn_check_device_error
+ * (ATTN_ERR_CUDA).  num_history_pages = 0 writes nothing; a negative count
+ * means every page (attn_bwd_paged).  history_pages is read on the device
+ * (4-byte aligned) and may not overlap an output.  The page map lives in the
+ * workspace (attn_bwd_paged_workspace_bytes covers it).
+ */
+ATTN_API attn_status_t attn_bwd_paged_compact(const attn_paged_desc* d, const void* q, const void* qp,
+                                              const void* k_pool, const void* v_pool, const void* kp_pool,
+                                              const void* dy, const int32_t* page_table, const int32_t* seq_meta,
+                                              const float* lse, const float* delta, const int32_t* history_pages,
+                                              int64_t num_history_pages, void* dk_pool, void* dv_pool,
+                                              void* dkp_pool, unsigned wrt_mask, void* workspace,
+                                              size_t workspace_bytes, void* stream);
+
+/*
  * Row statistics for the paged path by a forward sweep over each sequence's
  * pages: lse[r, h] = log sum_t exp(s_rt) over visible tokens (-inf if none)
  * and delta[r, h] = rowsum(P * dP) = dY . O.  Same arguments as
@@ -374,8 +399,8 @@ ATTN_API attn_status_t attn_selftest_wait_timeout(void* stream);
  * kernel (if dK or dV is requested); the dQ kernel (if dQ is requested).  The
  * paged backward launches its link preparation, the zero store of unlinked
  * pages and the history kernel (MLA: then the cluster-split history kernel of
- * the blocks whose shared pages carry many links); the paged row statistics
- * one kernel.
+ * the blocks whose shared pages carry many links; the compact call marks its
+ * page list before events[0]); the paged row statistics one kernel.
  */
 ATTN_API void attn_set_timing_events(void* const* events, int count);
 

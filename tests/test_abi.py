@@ -165,3 +165,32 @@ def test_strided_fused_views(lib):
     st = _strided_call(desc, sts, x, x + H * D * es, x + 2 * H * D * es, FAKE + 32 * MB,
                        g, g + H * D * es, g + 2 * H * D * es)
     assert st == bd.ATTN_ERR_INVALID_ARG
+
+
+def _compact_call(d, hist, n, dk=FAKE + 40 * MB, ws=None, ws_bytes=0):
+    return int(bd.lib().attn_bwd_paged_compact(
+        ctypes.byref(d), ctypes.c_void_p(FAKE), None, ctypes.c_void_p(FAKE + 8 * MB), ctypes.c_void_p(FAKE + 16 * MB),
+        None, ctypes.c_void_p(FAKE + 24 * MB), ctypes.c_void_p(FAKE + 30 * MB), ctypes.c_void_p(FAKE + 31 * MB),
+        ctypes.c_void_p(FAKE + 32 * MB), ctypes.c_void_p(FAKE + 33 * MB), hist and ctypes.c_void_p(hist), n,
+        ctypes.c_void_p(dk), ctypes.c_void_p(FAKE + 48 * MB), None, bd.ATTN_WRT_DK | bd.ATTN_WRT_DV,
+        ws and ctypes.c_void_p(ws), ws_bytes, None))
+
+
+def test_paged_compact_checks(lib):
+    """Compact history: a list pointer is needed when pages are listed, it is
+    4-byte aligned and no output may overlap it; an empty list writes nothing
+    (the call returns before any device work); the workspace covers the page
+    map (one byte per pool page)."""
+    d = bd.make_paged_desc(num_queries=64, num_seqs=4, heads=8, kv_heads=2, page_size=16, num_pages=100,
+                           max_pages_per_seq=10, key_dim=128, value_dim=128)
+    d0 = bd.make_paged_desc(num_queries=64, num_seqs=4, heads=8, kv_heads=2, page_size=16, num_pages=0,
+                            max_pages_per_seq=10, key_dim=128, value_dim=128)
+    assert bd.attn_bwd_paged_workspace_bytes(d) >= 100 + (4 + 101 + 100 + 40) * 4
+    assert _compact_call(d, None, 5) == bd.ATTN_ERR_INVALID_ARG
+    assert _compact_call(d, FAKE + 34 * MB + 2, 5) == bd.ATTN_ERR_INVALID_ARG
+    assert _compact_call(d, FAKE + 40 * MB, 5) == bd.ATTN_ERR_ALIAS
+    assert _compact_call(d, FAKE + 34 * MB, 0) == bd.ATTN_OK
+    assert _compact_call(d, None, 0) == bd.ATTN_OK
+    # a list with pages needs the workspace
+    assert _compact_call(d, FAKE + 34 * MB, 5) == bd.ATTN_ERR_WORKSPACE
+    assert _compact_call(d0, FAKE + 34 * MB, 5) == bd.ATTN_OK

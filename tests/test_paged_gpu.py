@@ -160,6 +160,39 @@ def test_paged_mla_split_bit_stable(bd):
     bd.check_device_error()
 
 
+@pytest.mark.parametrize("mla", [False, True], ids=["gqa", "mla"])
+def test_paged_compact_history(bd, mla):
+    """Compact history: listed pages (owned, shared, unreferenced, repeated,
+    in any order) get exactly the full call's rows; the other rows keep the
+    caller's values."""
+    kw = dict(seed=51 + int(mla), num_seqs=6, len_lo=60, len_hi=500, causal=True, shared_prefix_pages=3)
+    if mla:
+        kw.update(queries_per_seq=8, heads=16, kv_heads=1, key_dim=512, value_dim=512, position_dim=64)
+    else:
+        kw.update(queries_per_seq=32, heads=8, kv_heads=2, key_dim=128, value_dim=128)
+    c = inputs.paged_case(name="t", scale=0.5, **kw)
+    dv = to_dev(c, bd)
+    lse, delta = gpu_stats(bd, c, dv)
+    full = gpu_bwd(bd, c, dv, lse, delta)
+    rng = np.random.default_rng(7)
+    pages = rng.permutation(c.num_pages)[: c.num_pages // 2].astype(np.int32)
+    pages = np.concatenate([pages, pages[:3], [int(c.page_table[0, 0])]]).astype(np.int32)  # repeats, a shared page
+    hist = torch.from_numpy(pages).cuda()
+    outs = tuple(torch.full_like(x, 3.0) for x in full)
+    res = bd.paged_backward(dv["q"], dv["k"], dv["v"], dv["dy"], dv["table"], dv["meta"], lse, delta,
+                            heads=c.heads, kv_heads=c.kv_heads, page_size=c.page_size, causal=c.causal,
+                            qp=dv["qp"], kp_pool=dv["kp"], history_pages=hist,
+                            outputs=(outs[0], None, outs[1]) if mla else (outs[0], outs[1], None))
+    bd.check_device_error()
+    listed = np.zeros(c.num_pages * c.page_size, bool)
+    for pg in set(int(x) for x in pages):
+        listed[pg * c.page_size:(pg + 1) * c.page_size] = True
+    sel = torch.from_numpy(listed).cuda()
+    for a, b in zip(res, full):
+        assert torch.equal(a[sel], b[sel])
+        assert torch.all(a[~sel] == 3.0)
+
+
 def test_paged_bit_stable(bd):
     c = inputs.paged_case(name="t", seed=31, num_seqs=6, len_lo=50, len_hi=700, queries_per_seq=64, heads=32,
                           kv_heads=8, key_dim=128, value_dim=128, scale=0.5, shared_prefix_pages=2)
