@@ -36,6 +36,7 @@ ATTN_MASK_KEY = 4
 ATTN_MASK_BIAS = 8
 ATTN_MASK_TOP_LEFT = 16
 ATTN_MASK_ELEM = 32
+ATTN_OPT_STORE_DS = 1
 ATTN_WRT_DQ = 1
 ATTN_WRT_DK = 2
 ATTN_WRT_DV = 4
@@ -53,7 +54,7 @@ class attn_dense_desc(ctypes.Structure):
                 ("seq_k", ctypes.c_int64), ("head_dim", ctypes.c_int64), ("dtype", ctypes.c_int32),
                 ("layout", ctypes.c_int32), ("mask_flags", ctypes.c_uint32), ("window", ctypes.c_int32),
                 ("mask_thr", ctypes.c_float), ("mask_neg", ctypes.c_float), ("scale", ctypes.c_float),
-                ("reserved", ctypes.c_int32)]
+                ("options", ctypes.c_uint32)]
 
 
 class attn_strides3(ctypes.Structure):
@@ -244,7 +245,7 @@ def _dtype_code(t):
 
 def make_dense_desc(*, batch, heads, seq_q, seq_k, head_dim, dtype=ATTN_DTYPE_BF16, layout=ATTN_LAYOUT_BSHD,
                     causal=False, window=None, key_mask=False, bias=False, mask_thr=0.5, mask_neg=-1e9,
-                    scale=0.0, top_left=False, elem_mask=False) -> attn_dense_desc:
+                    scale=0.0, top_left=False, elem_mask=False, store_ds=False) -> attn_dense_desc:
     d = attn_dense_desc()
     attn_dense_desc_init(d)
     d.batch, d.heads, d.seq_q, d.seq_k, d.head_dim = batch, heads, seq_q, seq_k, head_dim
@@ -265,16 +266,18 @@ def make_dense_desc(*, batch, heads, seq_q, seq_k, head_dim, dtype=ATTN_DTYPE_BF
         flags |= ATTN_MASK_ELEM
     d.mask_flags = flags
     d.mask_thr, d.mask_neg, d.scale = mask_thr, mask_neg, scale
+    d.options = ATTN_OPT_STORE_DS if store_ds else 0
     return d
 
 
 def dense_backward(q, k, v, dy, *, layout="bshd", causal=False, window=None, key_mask=None, bias=None, o=None,
                    lse=None, wrt=ATTN_WRT_DQ | ATTN_WRT_DK | ATTN_WRT_DV, scale=0.0, mask_thr=0.5, mask_neg=-1e9,
-                   outputs=None, workspace=None, stream=None, top_left=False, elem_mask=None):
+                   outputs=None, workspace=None, stream=None, top_left=False, elem_mask=None, store_ds=False):
     """dQ, dK, dV for CUDA tensors q, k, v, dy ([B,S,H,D] or [B,H,S,D]).
 
     ``elem_mask`` is the optional per-element mask [B, H, Sq, Sk] (fp32,
-    contiguous; a pair below ``mask_thr`` is masked).
+    contiguous; a pair below ``mask_thr`` is masked).  ``store_ds`` selects
+    ATTN_OPT_STORE_DS (dQ from the stored dS tiles; larger workspace).
     Returns (dq, dk, dv) with None for gradients not selected in ``wrt``."""
     import torch
     lay = {"bshd": ATTN_LAYOUT_BSHD, "bhsd": ATTN_LAYOUT_BHSD}[layout]
@@ -287,7 +290,7 @@ def dense_backward(q, k, v, dy, *, layout="bshd", causal=False, window=None, key
     desc = make_dense_desc(batch=B, heads=H, seq_q=Sq, seq_k=Sk, head_dim=D, dtype=_dtype_code(q), layout=lay,
                            causal=causal, window=window, key_mask=key_mask is not None, bias=bias is not None,
                            mask_thr=mask_thr, mask_neg=mask_neg, scale=scale, top_left=top_left,
-                           elem_mask=elem_mask is not None)
+                           elem_mask=elem_mask is not None, store_ds=store_ds)
     if elem_mask is not None and not elem_mask.is_contiguous():
         raise ValueError("elem_mask must be contiguous")
     if outputs is None:

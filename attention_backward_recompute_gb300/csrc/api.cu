@@ -147,6 +147,7 @@ struct DenseSizes {
   size_t es, q_bytes, k_bytes, bias_bytes, mask_bytes, stat_bytes, ws_bytes;
   size_t split_off;  // fp32 storage: offset of the hi/lo bf16 copies of q, k, v, dy
   size_t elem_off;   // per-element mask: offset of its row and column bits
+  size_t ds_off;     // ATTN_OPT_STORE_DS: offset of the stored dS tiles
   int ew_q, ew_k;    // 32-bit words per query row / key column of those bits (even)
 };
 
@@ -160,7 +161,7 @@ attn_status_t check_dense_desc(const attn_dense_desc* d, DenseSizes* z) {
     return api_fail(ATTN_ERR_INVALID_ARG, "unknown layout %d", d->layout);
   if (d->mask_flags & ~63u) return api_fail(ATTN_ERR_INVALID_ARG, "unknown mask flag bits 0x%x", d->mask_flags);
   if ((d->mask_flags & ATTN_MASK_WINDOW) && d->window < 0) return api_fail(ATTN_ERR_INVALID_ARG, "window < 0");
-  if (d->reserved != 0) return api_fail(ATTN_ERR_INVALID_ARG, "reserved field must be 0");
+  if (d->options & ~ATTN_OPT_STORE_DS) return api_fail(ATTN_ERR_INVALID_ARG, "unknown option bits 0x%x", d->options);
   if (!std::isfinite(d->mask_neg) || !(d->mask_neg < 0.f)) return api_fail(ATTN_ERR_INVALID_ARG, "mask_neg must be finite and < 0");
   if (!std::isfinite(d->mask_thr)) return api_fail(ATTN_ERR_INVALID_ARG, "mask_thr must be finite");
   if (!std::isfinite(d->scale) || d->scale < 0.f) return api_fail(ATTN_ERR_INVALID_ARG, "scale must be finite and >= 0");
@@ -186,6 +187,7 @@ attn_status_t check_dense_desc(const attn_dense_desc* d, DenseSizes* z) {
     if (D > 64) return api_fail(ATTN_ERR_UNSUPPORTED, "fp32 storage supports head_dim <= 64");
     if (d->mask_flags & ATTN_MASK_BIAS) return api_fail(ATTN_ERR_UNSUPPORTED, "fp32 storage does not take a bias");
     if (d->mask_flags & ATTN_MASK_ELEM) return api_fail(ATTN_ERR_UNSUPPORTED, "fp32 storage does not take a per-element mask");
+    if (d->options & ATTN_OPT_STORE_DS) return api_fail(ATTN_ERR_UNSUPPORTED, "fp32 storage does not store dS");
     z->ws_bytes += 4 * align256(z->q_bytes / 2) + 4 * align256(z->k_bytes / 2);
   }
   z->elem_off = z->ws_bytes;
@@ -198,6 +200,9 @@ attn_status_t check_dense_desc(const attn_dense_desc* d, DenseSizes* z) {
     const size_t bh = size_t(d->batch) * d->heads;
     z->ws_bytes += align256(bh * d->seq_q * z->ew_q * 4) + align256(bh * d->seq_k * z->ew_k * 4);
   }
+  z->ds_off = z->ws_bytes;
+  if (d->options & ATTN_OPT_STORE_DS)  // dS^T tiles of 128 keys x 64 queries, bf16
+    z->ws_bytes += align256(size_t(d->batch) * d->heads * ((d->seq_k + 127) / 128) * ((d->seq_q + 63) / 64) * 16384);
   if (z->ws_bytes == 0) z->ws_bytes = 256;
   return ATTN_OK;
 }
@@ -332,6 +337,7 @@ attn_status_t prepare_dense(const attn_dense_desc* d, const attn_dense_strides& 
   put(p.s_dq, st.dq);
   put(p.s_dk, st.dk);
   put(p.s_dv, st.dv);
+  if (d->options & ATTN_OPT_STORE_DS) p.ds_store = ws + z.ds_off;
   if (z.ew_q) {
     p.elem_rows = reinterpret_cast<const uint32_t*>(ws + z.elem_off);
     p.elem_cols = reinterpret_cast<const uint32_t*>(ws + z.elem_off + align256(size_t(B * H * Sq) * z.ew_q * 4));
@@ -530,8 +536,11 @@ ATTN_API attn_status_t attn_bwd_dense_strided(const attn_dense_desc* d, const at
       ATTN_OK)
     return st;
   p.wrt = wrt_mask;
+  const bool store_ds = p.ds_store && want_dq;  // dQ from the dS tiles the dK/dV kernel stores
+  if (!want_dq) p.ds_store = nullptr;
+  const bool run_dkdv = want_dk || want_dv || store_ds;
 
-  const int nk = (split ? 4 : 0) + (has_elem ? 1 : 0) + 1 + (want_dk || want_dv ? 1 : 0) + (want_dq ? 1 : 0);
+  const int nk = (split ? 4 : 0) + (has_elem ? 1 : 0) + 1 + (run_dkdv ? 1 : 0) + (want_dq ? 1 : 0);
   attn::timing_mark_begin(nk, s);
   cudaError_t e = cudaSuccess;
   if (has_elem) {
@@ -553,12 +562,14 @@ ATTN_API attn_status_t attn_bwd_dense_strided(const attn_dense_desc* d, const at
           : (split ? attn::launch_fwd_stats(m, p, has_bias, s) : attn::launch_stats2(m, p, has_bias, s));
     attn::timing_mark(s);
   }
-  if (e == cudaSuccess && (want_dk || want_dv)) {
+  if (e == cudaSuccess && run_dkdv) {
     e = split ? attn::launch_dkdv(m, p, has_bias, s) : attn::launch_dkdv2(m, p, has_bias, s);
     attn::timing_mark(s);
   }
   if (e == cudaSuccess && want_dq) {
-    e = split ? attn::launch_dq(m, p, has_bias, s) : attn::launch_dq2(m, p, has_bias, s);
+    e = split      ? attn::launch_dq(m, p, has_bias, s)
+        : store_ds ? attn::launch_dq3(m, p, s)
+                   : attn::launch_dq2(m, p, has_bias, s);
     attn::timing_mark(s);
   }
   attn::timing_mark_end();

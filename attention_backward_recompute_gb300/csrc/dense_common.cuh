@@ -52,6 +52,12 @@ struct DenseParams {
   const uint32_t* elem_rows;
   const uint32_t* elem_cols;
   int ew_q, ew_k;
+  // Stored dS (ATTN_OPT_STORE_DS, workspace): the dK/dV kernel writes tile
+  // (bh, key tile kt of 128, query tile qt of 64) of dS^T, unscaled bf16, at
+  // ds_store + ((bh * ceil(Sk/128) + kt) * ceil(Sq/64) + qt) * 16384 as 128
+  // rows (keys) of 64 queries, 16-byte chunks swizzled by (row % 8); the dQ
+  // kernel reads it as the MN-major A operand.  Null: dQ by recomputation.
+  uint8_t* ds_store;
   uint32_t* err;              // device error word
 };
 

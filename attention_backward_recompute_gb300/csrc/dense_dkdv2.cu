@@ -142,7 +142,7 @@ __device__ __forceinline__ void p_row(uint32_t tS, const float* st, const uint8_
   }
 }
 
-template <int DP, bool HAS_BIAS, bool ELEM>
+template <int DP, bool HAS_BIAS, bool ELEM, bool DS>
 __global__ void __launch_bounds__(512, 1)
     dkdv2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_dy,
@@ -406,6 +406,12 @@ __global__ void __launch_bounds__(512, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar_p_read[bb]);
         const float* dl = reinterpret_cast<const float*>(sm + L::ST_OFF) + s * 3 * L::BQ + L::BQ;
+        // stored dS: this key's row of tile (key tile, query tile i_lo + t)
+        uint4* ds_row = nullptr;
+        if (DS) {
+          const size_t blob = (static_cast<size_t>(bh) * gridDim.y + blockIdx.y) * cdiv(p.Sq, L::BQ) + i_lo + t;
+          ds_row = reinterpret_cast<uint4*>(p.ds_store + blob * (L::BK * 128) + row * 128);
+        }
         // two halves of 32 queries: half hf reads dP columns [32hf, 32hf+32)
         // and writes dS^T (bf16 pairs) to columns [16hf, 16hf+16), which half
         // 0 has already read
@@ -426,6 +432,11 @@ __global__ void __launch_bounds__(512, 1)
                                           p3 * (__uint_as_float(dr[4 * c4 + 3]) - d4.w));
           }
           tmem_st16(tDP + 16 * hf, dsw);
+          if (DS) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              ds_row[(4 * hf + j) ^ (row & 7)] = make_uint4(dsw[4 * j], dsw[4 * j + 1], dsw[4 * j + 2], dsw[4 * j + 3]);
+          }
         }
         tmem_st_wait();
         tc_fence_before();
@@ -472,10 +483,10 @@ __global__ void __launch_bounds__(512, 1)
   }
 }
 
-template <int DP, bool HAS_BIAS, bool ELEM>
+template <int DP, bool HAS_BIAS, bool ELEM, bool DS>
 cudaError_t launch_t(const DenseMaps& m, const DenseParams& p, cudaStream_t s) {
   using L = Dkdv2Layout<DP>;
-  auto kern = dkdv2_kernel<DP, HAS_BIAS, ELEM>;
+  auto kern = dkdv2_kernel<DP, HAS_BIAS, ELEM, DS>;
   const int smem = max(L::BYTES + 1024, kSmemOneCtaPerSm);  // all 512 TMEM columns: one CTA per SM
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
@@ -484,16 +495,19 @@ cudaError_t launch_t(const DenseMaps& m, const DenseParams& p, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+template <bool ELEM, bool DS>
+cudaError_t launch_dp(const DenseMaps& m, const DenseParams& p, bool bias, cudaStream_t s) {
+  if (padded_head_dim(p.D) == 64)
+    return bias ? launch_t<64, true, ELEM, DS>(m, p, s) : launch_t<64, false, ELEM, DS>(m, p, s);
+  return bias ? launch_t<128, true, ELEM, DS>(m, p, s) : launch_t<128, false, ELEM, DS>(m, p, s);
+}
+
 }  // namespace
 
 cudaError_t launch_dkdv2(const DenseMaps& m, const DenseParams& p, bool bias, cudaStream_t s) {
-  const int DP = padded_head_dim(p.D);
-  if (p.elem_rows) {  // per-element custom mask
-    if (DP == 64) return bias ? launch_t<64, true, true>(m, p, s) : launch_t<64, false, true>(m, p, s);
-    return bias ? launch_t<128, true, true>(m, p, s) : launch_t<128, false, true>(m, p, s);
-  }
-  if (DP == 64) return bias ? launch_t<64, true, false>(m, p, s) : launch_t<64, false, false>(m, p, s);
-  return bias ? launch_t<128, true, false>(m, p, s) : launch_t<128, false, false>(m, p, s);
+  // per-element custom mask (ELEM) and stored dS (DS) are separate instances
+  if (p.elem_rows) return p.ds_store ? launch_dp<true, true>(m, p, bias, s) : launch_dp<true, false>(m, p, bias, s);
+  return p.ds_store ? launch_dp<false, true>(m, p, bias, s) : launch_dp<false, false>(m, p, bias, s);
 }
 
 }  // namespace attn

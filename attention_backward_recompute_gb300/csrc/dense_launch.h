@@ -46,5 +46,7 @@ cudaError_t launch_dkdv2(const DenseMaps& m, const DenseParams& p, bool bias, cu
 cudaError_t launch_dq(const DenseMaps& m, const DenseParams& p, bool bias, cudaStream_t s);
 // bf16 storage: softmax and dS on separate warpgroups, P and dS in tensor memory
 cudaError_t launch_dq2(const DenseMaps& m, const DenseParams& p, bool bias, cudaStream_t s);
+// bf16 storage with p.ds_store: dQ = scale * dS K from the dS tiles the dK/dV kernel stored
+cudaError_t launch_dq3(const DenseMaps& m, const DenseParams& p, cudaStream_t s);
 
 }  // namespace attn

@@ -53,6 +53,9 @@ extern "C" ATTN_API attn_status_t attn_bwd_dense_noalloc(const attn_dense_desc* 
     return attn::api_fail(ATTN_ERR_UNSUPPORTED,
                           "the library-owned scratch holds row statistics only; fp32 storage also needs split "
                           "copies of the inputs: use attn_bwd_dense with a workspace");
+  if (d->options & ATTN_OPT_STORE_DS)
+    return attn::api_fail(ATTN_ERR_UNSUPPORTED,
+                          "stored dS does not fit the library-owned scratch: use attn_bwd_dense with a workspace");
   const double rows = double(d->batch) * double(d->heads) * double(d->seq_q);
   if (rows > double(kRows))
     return attn::api_fail(ATTN_ERR_UNSUPPORTED,

@@ -262,7 +262,9 @@ def sweep(args) -> int:
 
     dense = [("C1", "dense_small_f32", {}), ("C2c", "dense_f32_causal", {}), ("C2w", "dense_f32_window", {}),
              ("C3", "dense_bf16_s2048", {}), ("C3 O+LSE supplied", "dense_bf16_s2048", {"supplied": True}),
-             ("C4", "dense_bf16_cross", {})]
+             ("C4", "dense_bf16_cross", {}),
+             ("C3 stored dS", "dense_bf16_s2048", {"store_ds": True}),
+             ("C4 stored dS", "dense_bf16_cross", {"store_ds": True})]
     for tag, name, opt in dense:
         if not want(tag):
             continue
@@ -280,7 +282,8 @@ def sweep(args) -> int:
             lse = torch.from_numpy(lse_np.astype(np.float32)).cuda()
         outs = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v))
         call = lambda: bd.dense_backward(q, k, v, dy, layout=c.layout, causal=c.causal, window=c.window,
-                                         key_mask=km, bias=bias, o=o, lse=lse, outputs=outs)
+                                         key_mask=km, bias=bias, o=o, lse=lse, outputs=outs,
+                                         store_ds=bool(opt.get("store_ds")))
         ms, ms_min = timed(call, 20 if c.seq_q * c.seq_k * c.batch * c.heads > 1e7 else 50)
         vp = visible_pairs(c.seq_q, c.seq_k, c.causal, c.window)
         flops = 10.0 * c.head_dim * vp * c.batch * c.heads

@@ -107,15 +107,30 @@ typedef struct attn_dense_desc {
   float mask_thr;     /* key masked when key_mask[b,k] < mask_thr (default 0.5) */
   float mask_neg;     /* masked score value, finite and < 0 (default -1e9) */
   float scale;        /* softmax scale; 0 means 1/sqrt(head_dim) */
-  int32_t reserved;   /* must be 0 */
+  uint32_t options;   /* OR of ATTN_OPT_* (0: none) */
 } attn_dense_desc;
+
+/*
+ * Backward option: store dS once instead of recomputing it for dQ.  The dK/dV
+ * kernel writes every dS tile it forms (bf16) to the workspace and dQ is one
+ * product, dQ = scale * dS K, over those tiles: 14 * D flops per visible pair
+ * instead of 18 * D, for a workspace larger by
+ * 16384 * batch * heads * ceil(seq_k / 128) * ceil(seq_q / 64) bytes
+ * (attn_bwd_dense_workspace_bytes counts it).  Results stay deterministic:
+ * dK and dV are bit-identical to the call without the option; dQ differs
+ * only by rounding (dS enters it as the same bf16 values the dK product
+ * uses).  bf16 storage only (fp32: ATTN_ERR_UNSUPPORTED); ignored by the
+ * forward export; refused by attn_bwd_dense_noalloc.
+ */
+#define ATTN_OPT_STORE_DS 1u
 
 /* Fill `d` with defaults: zeros, BSHD, bf16, mask_thr 0.5, mask_neg -1e9. */
 ATTN_API void attn_dense_desc_init(attn_dense_desc* d);
 
 /* Bytes of workspace attn_bwd_dense needs for `d` (row statistics: three fp32
- * values per (b, h, query row), each array 256-byte aligned).  Returns 0 for an
- * invalid descriptor. */
+ * values per (b, h, query row), each array 256-byte aligned; plus the split
+ * copies of fp32 storage, the bits of a per-element mask and the stored dS of
+ * ATTN_OPT_STORE_DS when those apply).  Returns 0 for an invalid descriptor. */
 ATTN_API size_t attn_bwd_dense_workspace_bytes(const attn_dense_desc* d);
 
 /*

@@ -194,3 +194,27 @@ def test_paged_compact_checks(lib):
     # a list with pages needs the workspace
     assert _compact_call(d, FAKE + 34 * MB, 5) == bd.ATTN_ERR_WORKSPACE
     assert _compact_call(d0, FAKE + 34 * MB, 5) == bd.ATTN_OK
+
+
+def test_store_ds_option_checks(lib):
+    """ATTN_OPT_STORE_DS grows the workspace by one 128 x 64 bf16 dS tile per
+    (batch, head, key tile of 128, query tile of 64); fp32 storage and unknown
+    option bits are refused; the no-allocation entry point refuses it."""
+    d = _desc(batch=2, heads=3, seq_q=200, seq_k=300, head_dim=128)
+    base = bd.attn_bwd_dense_workspace_bytes(d)
+    d.options = bd.ATTN_OPT_STORE_DS
+    a256 = lambda x: (x + 255) // 256 * 256
+    assert bd.attn_bwd_dense_workspace_bytes(d) == base + a256(2 * 3 * 3 * 4 * 16384)
+    d.options = 2
+    assert bd.attn_bwd_dense_workspace_bytes(d) == 0
+    assert _call(d) == bd.ATTN_ERR_INVALID_ARG
+    df = _desc(dtype=bd.ATTN_DTYPE_F32, head_dim=64)
+    df.options = bd.ATTN_OPT_STORE_DS
+    assert _call(df) == bd.ATTN_ERR_UNSUPPORTED
+    d.options = bd.ATTN_OPT_STORE_DS
+    st = int(bd.lib().attn_bwd_dense_noalloc(ctypes.byref(d), ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE + 4 * MB),
+                                             ctypes.c_void_p(FAKE + 8 * MB), ctypes.c_void_p(FAKE + 12 * MB), None,
+                                             None, None, None, ctypes.c_void_p(FAKE + 16 * MB),
+                                             ctypes.c_void_p(FAKE + 20 * MB), ctypes.c_void_p(FAKE + 24 * MB), 7,
+                                             None))
+    assert st == bd.ATTN_ERR_UNSUPPORTED
