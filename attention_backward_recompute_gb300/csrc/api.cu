@@ -201,8 +201,11 @@ attn_status_t check_dense_desc(const attn_dense_desc* d, DenseSizes* z) {
     z->ws_bytes += align256(bh * d->seq_q * z->ew_q * 4) + align256(bh * d->seq_k * z->ew_k * 4);
   }
   z->ds_off = z->ws_bytes;
-  if (d->options & ATTN_OPT_STORE_DS)  // dS^T tiles of 128 keys x 64 queries, bf16
-    z->ws_bytes += align256(size_t(d->batch) * d->heads * ((d->seq_k + 127) / 128) * ((d->seq_q + 63) / 64) * 16384);
+  if (d->options & ATTN_OPT_STORE_DS) {  // dS^T tiles of 128 keys x 64 queries, bf16
+    const int64_t tiles = d->batch * d->heads * ((d->seq_k + 127) / 128) * ((d->seq_q + 63) / 64);
+    if (tiles >= lim) return api_fail(ATTN_ERR_UNSUPPORTED, "too many dS tiles to store (%lld)", (long long)tiles);
+    z->ws_bytes += align256(size_t(tiles) * 16384);
+  }
   if (z->ws_bytes == 0) z->ws_bytes = 256;
   return ATTN_OK;
 }

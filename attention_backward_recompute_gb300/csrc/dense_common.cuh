@@ -54,9 +54,12 @@ struct DenseParams {
   int ew_q, ew_k;
   // Stored dS (ATTN_OPT_STORE_DS, workspace): the dK/dV kernel writes tile
   // (bh, key tile kt of 128, query tile qt of 64) of dS^T, unscaled bf16, at
-  // ds_store + ((bh * ceil(Sk/128) + kt) * ceil(Sq/64) + qt) * 16384 as 128
-  // rows (keys) of 64 queries, 16-byte chunks swizzled by (row % 8); the dQ
-  // kernel reads it as the MN-major A operand.  Null: dQ by recomputation.
+  // ds_store + ((bh * ceil(Sk/128) + kt) * ceil(Sq/64) + qt) * 16384: chunk c
+  // (queries 8c..8c+7, 16 bytes) of key k at byte c * 2048 + k * 16, so that
+  // one warp store instruction writes 512 contiguous bytes.  Read as is, this
+  // is the unswizzled MN-major operand layout (8-key x 16-byte core matrices,
+  // 128 bytes apart along the keys, 2048 along the queries) the dQ kernel
+  // gives the tensor core.  Null: dQ by recomputation.
   uint8_t* ds_store;
   uint32_t* err;              // device error word
 };

@@ -406,11 +406,12 @@ __global__ void __launch_bounds__(512, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar_p_read[bb]);
         const float* dl = reinterpret_cast<const float*>(sm + L::ST_OFF) + s * 3 * L::BQ + L::BQ;
-        // stored dS: this key's row of tile (key tile, query tile i_lo + t)
+        // stored dS of tile (key tile, query tile i_lo + t): chunk c of this
+        // key at c * 2048 + row * 16
         uint4* ds_row = nullptr;
         if (DS) {
           const size_t blob = (static_cast<size_t>(bh) * gridDim.y + blockIdx.y) * cdiv(p.Sq, L::BQ) + i_lo + t;
-          ds_row = reinterpret_cast<uint4*>(p.ds_store + blob * (L::BK * 128) + row * 128);
+          ds_row = reinterpret_cast<uint4*>(p.ds_store + blob * (L::BK * 128)) + row;
         }
         // two halves of 32 queries: half hf reads dP columns [32hf, 32hf+32)
         // and writes dS^T (bf16 pairs) to columns [16hf, 16hf+16), which half
@@ -435,7 +436,7 @@ __global__ void __launch_bounds__(512, 1)
           if (DS) {
 #pragma unroll
             for (int j = 0; j < 4; ++j)
-              ds_row[(4 * hf + j) ^ (row & 7)] = make_uint4(dsw[4 * j], dsw[4 * j + 1], dsw[4 * j + 2], dsw[4 * j + 3]);
+              ds_row[(4 * hf + j) * L::BK] = make_uint4(dsw[4 * j], dsw[4 * j + 1], dsw[4 * j + 2], dsw[4 * j + 3]);
           }
         }
         tmem_st_wait();

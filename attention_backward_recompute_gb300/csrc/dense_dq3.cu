@@ -3,8 +3,10 @@
 // rlx-cpu src/attention_bwd.rs (fn backward_dense_head_all) forms, per query
 // row, dQ = scale * sum_k dS[q, k] K[k] with dS = P * (dP - delta).  The dK/dV
 // kernel already computes every dS tile; with this option it also writes each
-// 128-key x 64-query tile dS^T once to the workspace (bf16, rows of 64 queries
-// laid out as the 128-byte-swizzled MN-major operand), and this kernel forms
+// 128-key x 64-query tile dS^T once to the workspace (bf16, 16-byte chunks of
+// 8 queries stored key after key, so that each warp stores 512 contiguous
+// bytes; that order is the unswizzled MN-major operand layout), and this
+// kernel forms
 //   dQ_i = scale * sum_j dS_ij K_j      (M = 128 queries, N = head dim, K = 128 keys per tile)
 // on tcgen05 with both operands MN-major in shared memory: A = the two 64-query
 // dS^T tiles of query tile i, B = the key tile [128 keys][head dim].  No S or
@@ -69,7 +71,8 @@ __global__ void __launch_bounds__(256, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bh = blockIdx.x;
   const int b = bh / p.H, h = bh - b * p.H;
-  const int q0 = blockIdx.y * L::BQ;
+  const int it = static_cast<int>(gridDim.y - 1 - blockIdx.y);  // longest rows first under causal masks
+  const int q0 = it * L::BQ;
   const int q1 = imin(q0 + L::BQ - 1, p.Sq - 1);
   int j_lo, j_hi;
   key_tile_range(p, q0, q1, L::BK, &j_lo, &j_hi);
@@ -114,7 +117,7 @@ __global__ void __launch_bounds__(256, 1)
       uint32_t bytes = L::KT;
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
-        const int qt = 2 * blockIdx.y + hf;
+        const int qt = 2 * it + hf;
         have[hf] = qt >= i_lo && qt < i_hi && qt < nqt;
         if (have[hf]) {
           bytes += kDsTile;
@@ -130,7 +133,7 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf)
           if (have[hf]) {
-            const size_t blob = (static_cast<size_t>(bh) * nkt + kt) * nqt + 2 * blockIdx.y + hf;
+            const size_t blob = (static_cast<size_t>(bh) * nkt + kt) * nqt + 2 * it + hf;
             bulk_g2s(st + hf * kDsTile, p.ds_store + blob * kDsTile, kDsTile, &bar_full[s]);
           }
         for (int c = 0; c < L::NCH; ++c)
@@ -145,7 +148,9 @@ __global__ void __launch_bounds__(256, 1)
   } else if (n > 0 && warp == 1) {
     // ------------------------------------------------------------ MMA issuer (whole warp, elected lane)
     constexpr uint32_t id = idesc_bf16(128, DP, true, true);
-    const uint64_t dA = sdesc_sw128(smem_addr(sm), kDsTile, 1024);            // MN-major: 64-query halves LBO apart
+    // A: the stored dS as is, unswizzled MN-major (core matrices 2048 bytes
+    // apart along the 128 queries of the two halves, 128 along the keys)
+    const uint64_t dA = sdesc_none(smem_addr(sm), 128, 2048);
     const uint64_t dB = sdesc_sw128(smem_addr(sm + L::DS), L::BK * 128, 1024);  // MN-major: 64-dim chunks
     bool ok = true;
     for (int t = 0; t < n && ok; ++t) {
@@ -158,8 +163,8 @@ __global__ void __launch_bounds__(256, 1)
       else
         mma_ss_w<true>(tmem, a, bdesc, id);
 #pragma unroll
-      for (int kk = 1; kk < L::BK / 16; ++kk)
-        mma_ss_w<true>(tmem, sdesc_add(a, kk * 16 * 128), sdesc_add(bdesc, kk * 16 * 128), id);
+      for (int kk = 1; kk < L::BK / 16; ++kk)  // 16 keys: two core matrices of A, 16 swizzled rows of B
+        mma_ss_w<true>(tmem, sdesc_add(a, kk * 256), sdesc_add(bdesc, kk * 16 * 128), id);
       mma_commit_w(&bar_empty[s]);
     }
     mma_commit_w(&bar_acc);

@@ -202,6 +202,16 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
          (static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
+// The same descriptor for an operand without swizzle, in the canonical layout
+// of 8-row x 16-byte core matrices (each 128 contiguous bytes).  MN-major:
+// a core matrix holds 8 K-rows of 8 bf16 of M/N; LBO = bytes between core
+// matrices adjacent along K, SBO = bytes between core matrices adjacent
+// along M/N (the reverse of the swizzled MN-major form).
+__device__ __forceinline__ uint64_t sdesc_none(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16) |
+         (static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32) | (1ull << 46);
+}
+
 // Instruction descriptor for kind::f16 (bf16 x bf16 -> f32) and kind::tf32.
 //   bits 4-5 D format (1 = f32); 7-9 A format; 10-12 B format (f16 kind:
 //   1 = bf16; tf32 kind: 2 = tf32); 15 A MN-major; 16 B MN-major;

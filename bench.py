@@ -8,7 +8,9 @@ One step = one call of attn_bwd_dense (C ABI) on the workload
 causal (bottom-right) + custom per-key mask (10% zeros, < 0.5 -> -1e9) +
 additive bias [B,H,Sq,Sk] ~ N(0,1), self-contained mode (the row statistics
 are recomputed from Q, K, V, dY).  The call runs the whole hot path: the
-row-statistics prologue, the dK/dV kernel and the dQ kernel.
+row-statistics prologue, the dK/dV kernel (which also stores every dS tile,
+ATTN_OPT_STORE_DS) and the dQ kernel (dQ = scale * dS K over those tiles);
+--recompute-dq times the default dQ kernel, which recomputes S and dP.
 
 Metric: attention-backward TFLOP/s counted as 10 * D * (visible query/key
 pairs) per head (five products of 2*D flops each), visible = allowed by the
@@ -491,6 +493,8 @@ def main():
     ap.add_argument("--heads", type=int, default=None, help="override H (profiling runs on a smaller case)")
     ap.add_argument("--sweep", action="store_true",
                     help="time every configuration once against its oracle sample (one JSON line each)")
+    ap.add_argument("--recompute-dq", action="store_true",
+                    help="time the default dQ path (S and dP recomputed) instead of ATTN_OPT_STORE_DS")
     ap.add_argument("--only", default=None, help="--sweep: only the configurations whose tag matches this regex")
     args = ap.parse_args()
     if args.sweep:
@@ -522,7 +526,11 @@ def main():
     B, H, S, D = case.batch, case.heads, case.seq_q, case.head_dim
     vp = visible_pairs(case.seq_q, case.seq_k, case.causal, case.window)
     flops = 10.0 * D * vp * B * H
-    alg = {"prologue": 4.0 * D * vp * B * H, "dkdv": 8.0 * D * vp * B * H, "dq": 6.0 * D * vp * B * H}
+    # dQ from the dS tiles the dK/dV kernel stores (ATTN_OPT_STORE_DS, one
+    # product: 2*D per pair) unless --recompute-dq (S, dP and dS K: 6*D)
+    store_ds = not args.recompute_dq
+    alg = {"prologue": 4.0 * D * vp * B * H, "dkdv": 8.0 * D * vp * B * H,
+           "dq": (2.0 if store_ds else 6.0) * D * vp * B * H}
 
     host = {"q": case.q, "k": case.k, "v": case.v, "dy": case.dy, "bias": case.bias}
     pinned = {n: torch.from_numpy(x).to(torch.bfloat16).pin_memory() for n, x in host.items()}
@@ -531,7 +539,7 @@ def main():
     km = km_host.to(dev)
     dq, dk, dv = (torch.empty_like(dvc[n]) for n in ("q", "k", "v"))
     desc = bd.make_dense_desc(batch=B, heads=H, seq_q=S, seq_k=S, head_dim=D, causal=True, key_mask=True,
-                              bias=True)
+                              bias=True, store_ds=store_ds)
     ws_bytes = bd.attn_bwd_dense_workspace_bytes(desc)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -636,6 +644,7 @@ def main():
                        "visible_pairs_per_head": vp, "l2": "inputs larger than L2 (640 MiB read per step), no flush",
                        "parallelism": f"replicas x{world} (weak)" if world > 1 else "1 GPU",
                        "pct_of_peak": 100.0 * value / world / peak,
+                       "dq_path": "stored dS (ATTN_OPT_STORE_DS)" if store_ds else "recomputed S, dP",
                        "kernel_ms": kmean},
             "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak,
                          "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic,
