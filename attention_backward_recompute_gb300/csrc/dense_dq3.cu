@@ -12,9 +12,10 @@
 // dS^T tiles of query tile i, B = the key tile [128 keys][head dim].  No S or
 // dP is recomputed, and every dQ element still has one writer (no atomics).
 //
-// Roles (256 threads): warp 0 copies (dS tiles by bulk copy, K by TMA, zeros
-// for a 64-query half the dK/dV kernel never visited), warp 1 issues the
-// MMAs, warps 4..7 store dQ (tensor-memory lane = query row of the tile).
+// Roles (256 threads, one persistent CTA per SM over the 128-query tiles):
+// warp 0 copies (dS tiles by bulk copy, K by TMA, zeros for a 64-query half
+// the dK/dV kernel never visited), warp 1 issues the MMAs, warps 4..7 store
+// dQ (tensor-memory lane = query row of the tile).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -38,7 +39,7 @@ struct Dq3Layout {
   static constexpr int KT = NCH * BK * 128;        // key tile as NCH chunks [128 keys][64 dims]
   static constexpr int STAGE = DS + KT;
   static constexpr int BYTES = kStages * STAGE;
-  static constexpr int TMEM_COLS = DP;             // the dQ accumulator
+  static constexpr int TMEM_COLS = 2 * DP;         // two dQ accumulators (alternating items)
 };
 
 // 1-D bulk copy global -> shared, completion counted on `bar` (bytes % 16 == 0,
@@ -58,27 +59,37 @@ __device__ __forceinline__ bool drain_wait(uint64_t* bar, uint32_t parity) {
   return true;
 }
 
+// Query tile of work item w: longest rows first under causal masks (query
+// tile nqt - 1 - w / BH of head w % BH).
+__device__ __forceinline__ void dq3_item(const DenseParams& p, int w, int nqt128, int* bh, int* it) {
+  const int BH = p.B * p.H;
+  *bh = w % BH;
+  *it = nqt128 - 1 - w / BH;
+}
+
+// Persistent: CTA c takes work items c, c + gridDim.x, ...; the copy ring and
+// its phases run on across items, and the two dQ accumulators alternate, so
+// one item's epilogue overlaps the next item's copies and products.
 template <int DP>
 __global__ void __launch_bounds__(256, 1)
     dq3_kernel(const __grid_constant__ CUtensorMap tm_k, const DenseParams p) {
   using L = Dq3Layout<DP>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t bar_full[kStages], bar_empty[kStages], bar_acc;
+  __shared__ uint64_t bar_full[kStages], bar_empty[kStages], bar_acc_full[2], bar_acc_empty[2], bar_fin;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bh = blockIdx.x;
-  const int b = bh / p.H, h = bh - b * p.H;
-  const int it = static_cast<int>(gridDim.y - 1 - blockIdx.y);  // longest rows first under causal masks
-  const int q0 = it * L::BQ;
-  const int q1 = imin(q0 + L::BQ - 1, p.Sq - 1);
-  int j_lo, j_hi;
-  key_tile_range(p, q0, q1, L::BK, &j_lo, &j_hi);
-  const int n = j_hi - j_lo;
+  const int nqt128 = cdiv(p.Sq, L::BQ);
+  const int items = p.B * p.H * nqt128;
   const int nkt = cdiv(p.Sk, L::BK), nqt = cdiv(p.Sq, 64);
   const Abort ab{&abort_flag, p.err};
+  // key tiles [j_lo, j_hi) of an item
+  auto tiles_of = [&](int it, int* j_lo, int* j_hi) {
+    const int q0 = it * L::BQ;
+    key_tile_range(p, q0, imin(q0 + L::BQ - 1, p.Sq - 1), L::BK, j_lo, j_hi);
+  };
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
@@ -86,7 +97,11 @@ __global__ void __launch_bounds__(256, 1)
       mbar_init(&bar_full[s], 1);
       mbar_init(&bar_empty[s], 1);
     }
-    mbar_init(&bar_acc, 1);
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&bar_acc_full[a], 1);
+      mbar_init(&bar_acc_empty[a], 4);  // one arrival per epilogue warp
+    }
+    mbar_init(&bar_fin, 1);
     mbar_fence_init();
   }
   if (warp == 1) {
@@ -98,54 +113,61 @@ __global__ void __launch_bounds__(256, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
 
-  if (n > 0 && warp == 0) {
+  if (warp == 0) {
     // ------------------------------------------------------------ copies
     if (lane == 0) tma_prefetch_map(&tm_k);
     int last_use[kStages];
     for (int i = 0; i < kStages; ++i) last_use[i] = -1;
     bool ok = true;
-    for (int t = 0; t < n && ok; ++t) {
-      const int s = t % kStages, kt = j_lo + t;
-      if (t >= kStages) ok = mbar_wait_warp(&bar_empty[s], ((t / kStages) - 1) & 1, ab);
-      if (!ok) break;
-      uint8_t* st = sm + s * L::STAGE;
-      // the dK/dV kernel visited query tiles [i_lo, i_hi) of key tile kt; a
-      // half outside that range holds no stored tile and reads as zeros
-      int i_lo, i_hi;
-      query_tile_range(p, kt * L::BK, imin(kt * L::BK + L::BK - 1, p.Sk - 1), 64, &i_lo, &i_hi);
-      bool have[2];
-      uint32_t bytes = L::KT;
+    int g = 0;  // running tile number of this CTA
+    for (int w = blockIdx.x; w < items && ok; w += gridDim.x) {
+      int bh, it, j_lo, j_hi;
+      dq3_item(p, w, nqt128, &bh, &it);
+      tiles_of(it, &j_lo, &j_hi);
+      const int b = bh / p.H, h = bh - b * p.H;
+      for (int kt = j_lo; kt < j_hi && ok; ++kt, ++g) {
+        const int s = g % kStages;
+        if (g >= kStages) ok = mbar_wait_warp(&bar_empty[s], ((g / kStages) - 1) & 1, ab);
+        if (!ok) break;
+        uint8_t* st = sm + s * L::STAGE;
+        // the dK/dV kernel visited query tiles [i_lo, i_hi) of key tile kt; a
+        // half outside that range holds no stored tile and reads as zeros
+        int i_lo, i_hi;
+        query_tile_range(p, kt * L::BK, imin(kt * L::BK + L::BK - 1, p.Sk - 1), 64, &i_lo, &i_hi);
+        bool have[2];
+        uint32_t bytes = L::KT;
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        const int qt = 2 * it + hf;
-        have[hf] = qt >= i_lo && qt < i_hi && qt < nqt;
-        if (have[hf]) {
-          bytes += kDsTile;
-        } else {
-          uint4* z = reinterpret_cast<uint4*>(st + hf * kDsTile);
-          for (int i = lane; i < kDsTile / 16; i += 32) z[i] = make_uint4(0u, 0u, 0u, 0u);
-        }
-      }
-      if (!have[0] || !have[1]) fence_proxy_async_smem();  // zeros visible to the tensor core
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&bar_full[s], bytes);
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf)
+        for (int hf = 0; hf < 2; ++hf) {
+          const int qt = 2 * it + hf;
+          have[hf] = qt >= i_lo && qt < i_hi && qt < nqt;
           if (have[hf]) {
-            const size_t blob = (static_cast<size_t>(bh) * nkt + kt) * nqt + 2 * it + hf;
-            bulk_g2s(st + hf * kDsTile, p.ds_store + blob * kDsTile, kDsTile, &bar_full[s]);
+            bytes += kDsTile;
+          } else {
+            uint4* z = reinterpret_cast<uint4*>(st + hf * kDsTile);
+            for (int i = lane; i < kDsTile / 16; i += 32) z[i] = make_uint4(0u, 0u, 0u, 0u);
           }
-        for (int c = 0; c < L::NCH; ++c)
-          tma_load_4d(st + L::DS + c * (L::BK * 128), &tm_k, &bar_full[s], c * 64, kt * L::BK, h, b);
+        }
+        if (!have[0] || !have[1]) fence_proxy_async_smem();  // zeros visible to the tensor core
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bar_full[s], bytes);
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf)
+            if (have[hf]) {
+              const size_t blob = (static_cast<size_t>(bh) * nkt + kt) * nqt + 2 * it + hf;
+              bulk_g2s(st + hf * kDsTile, p.ds_store + blob * kDsTile, kDsTile, &bar_full[s]);
+            }
+          for (int c = 0; c < L::NCH; ++c)
+            tma_load_4d(st + L::DS + c * (L::BK * 128), &tm_k, &bar_full[s], c * 64, kt * L::BK, h, b);
+        }
+        last_use[s] = g;
       }
-      last_use[s] = t;
     }
     if (lane == 0) {
       for (int s = 0; s < kStages; ++s)
         if (last_use[s] >= 0) drain_wait(&bar_full[s], (last_use[s] / kStages) & 1);
     }
-  } else if (n > 0 && warp == 1) {
+  } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (whole warp, elected lane)
     constexpr uint32_t id = idesc_bf16(128, DP, true, true);
     // A: the stored dS as is, unswizzled MN-major (core matrices 2048 bytes
@@ -153,41 +175,57 @@ __global__ void __launch_bounds__(256, 1)
     const uint64_t dA = sdesc_none(smem_addr(sm), 128, 2048);
     const uint64_t dB = sdesc_sw128(smem_addr(sm + L::DS), L::BK * 128, 1024);  // MN-major: 64-dim chunks
     bool ok = true;
-    for (int t = 0; t < n && ok; ++t) {
-      const int s = t % kStages;
-      if (!(ok = mbar_wait_warp(&bar_full[s], (t / kStages) & 1, ab))) break;
+    int g = 0, li = 0;
+    for (int w = blockIdx.x; w < items && ok; w += gridDim.x, ++li) {
+      int bh, it, j_lo, j_hi;
+      dq3_item(p, w, nqt128, &bh, &it);
+      tiles_of(it, &j_lo, &j_hi);
+      const int a = li & 1;
+      // the epilogue has read this accumulator's previous item
+      if (li >= 2 && !(ok = mbar_wait_warp(&bar_acc_empty[a], ((li >> 1) - 1) & 1, ab))) break;
       tc_fence_after();
-      const uint64_t a = sdesc_add(dA, s * L::STAGE), bdesc = sdesc_add(dB, s * L::STAGE);
-      if (t == 0)
-        mma_ss_w<false>(tmem, a, bdesc, id);
-      else
-        mma_ss_w<true>(tmem, a, bdesc, id);
+      const uint32_t acc = tmem + a * DP;
+      for (int kt = j_lo; kt < j_hi && ok; ++kt, ++g) {
+        const int s = g % kStages;
+        if (!(ok = mbar_wait_warp(&bar_full[s], (g / kStages) & 1, ab))) break;
+        tc_fence_after();
+        const uint64_t ad = sdesc_add(dA, s * L::STAGE), bdesc = sdesc_add(dB, s * L::STAGE);
+        if (kt == j_lo)
+          mma_ss_w<false>(acc, ad, bdesc, id);
+        else
+          mma_ss_w<true>(acc, ad, bdesc, id);
 #pragma unroll
-      for (int kk = 1; kk < L::BK / 16; ++kk)  // 16 keys: two core matrices of A, 16 swizzled rows of B
-        mma_ss_w<true>(tmem, sdesc_add(a, kk * 256), sdesc_add(bdesc, kk * 16 * 128), id);
-      mma_commit_w(&bar_empty[s]);
+        for (int kk = 1; kk < L::BK / 16; ++kk)  // 16 keys: two core matrices of A, 16 swizzled rows of B
+          mma_ss_w<true>(acc, sdesc_add(ad, kk * 256), sdesc_add(bdesc, kk * 16 * 128), id);
+        mma_commit_w(&bar_empty[s]);
+      }
+      if (ok) mma_commit_w(&bar_acc_full[a]);  // also for an item without key tiles (stores zeros)
     }
-    mma_commit_w(&bar_acc);
-    drain_wait(&bar_acc, 0);
+    mma_commit_w(&bar_fin);
+    drain_wait(&bar_fin, 0);
     __syncwarp();
   } else if (warp >= 4) {
     // ------------------------------------------------------------ epilogue
     const int row = (warp & 3) * 32 + lane;  // query row of the tile == tensor-memory lane
-    const int q = q0 + row;
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
     bool ok = true;
-    if (n > 0) {
-      ok = mbar_wait_warp(&bar_acc, 0, ab);
+    int li = 0;
+    for (int w = blockIdx.x; w < items && ok; w += gridDim.x, ++li) {
+      int bh, it, j_lo, j_hi;
+      dq3_item(p, w, nqt128, &bh, &it);
+      tiles_of(it, &j_lo, &j_hi);
+      const int b = bh / p.H, h = bh - b * p.H;
+      const int a = li & 1;
+      if (!(ok = mbar_wait_warp(&bar_acc_full[a], (li >> 1) & 1, ab))) break;
       tc_fence_after();
-    }
-    if (ok) {  // warp-uniform: the tensor-memory loads are warp-collective
+      const int q = it * L::BQ + row;
       const int64_t roff = static_cast<int64_t>(b) * p.s_dq[2] + static_cast<int64_t>(h) * p.s_dq[1] +
                            static_cast<int64_t>(q) * p.s_dq[0];
 #pragma unroll 1
-      for (int cc = 0; cc < DP / 32 && cc * 32 < p.D; ++cc) {
+      for (int cc = 0; cc < DP / 32 && cc * 32 < p.D; ++cc) {  // warp-uniform: tensor-memory loads are collective
         uint32_t r[32];
-        if (n > 0) {
-          tmem_ld32(tmem + lane_addr + cc * 32, r);
+        if (j_hi > j_lo) {
+          tmem_ld32(tmem + a * DP + lane_addr + cc * 32, r);
           tmem_ld_wait();
         } else {
 #pragma unroll
@@ -195,6 +233,9 @@ __global__ void __launch_bounds__(256, 1)
         }
         if (q < p.Sq) store_out32<false>(p.dq, roff, cc * 32, p.D, r, p.scale);
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_acc_empty[a]);
     }
   }
   tc_fence_before();
@@ -212,7 +253,11 @@ cudaError_t launch_t(const DenseMaps& m, const DenseParams& p, cudaStream_t s) {
   const int smem = L::BYTES + 1024;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(p.B * p.H, cdiv(p.Sq, L::BQ));
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  const int items = p.B * p.H * cdiv(p.Sq, L::BQ);
+  const int grid = imin(items, imax(sms, 1));  // one CTA per SM (shared memory)
   kern<<<grid, 256, smem, s>>>(m.k128, p);
   return cudaGetLastError();
 }
