@@ -180,6 +180,17 @@ def cpu_baseline(case, budget_s: float):
             "sample": f"{done} of {B * H} (batch, head) pairs of {WORKLOAD}, float64 numpy, {dt:.1f} s"}
 
 
+def rank_max(x: float, dist, device) -> float:
+    """The largest x over the ranks (x itself without a process group): the
+    timing rule of the multi-GPU line is the slowest rank's time."""
+    if not dist:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def run_reference(args, rank, world):
     """--impl reference: the CPU oracle timed on the host, K steps of one head each."""
     if rank != 0:
@@ -583,10 +594,7 @@ def main():
     clocks = sampler.stop()
     bd.check_device_error()
     ms = start.elapsed_time(end) / args.steps
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = rank_max(ms, dist, dev)
     kt = {"prologue": [], "dkdv": [], "dq": []}
     for e in evs:
         kt["prologue"].append(e[0].elapsed_time(e[1]))
@@ -626,10 +634,7 @@ def main():
     t1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = t0.elapsed_time(t1) / e2e_steps
-    if dist:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = rank_max(e2e_ms, dist, dev)
     bd.check_device_error()
 
     if rank == 0:
