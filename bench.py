@@ -277,6 +277,7 @@ def sweep(args) -> int:
              ("C3", "dense_bf16_s2048", {}), ("C3 O+LSE supplied", "dense_bf16_s2048", {"supplied": True}),
              ("C4", "dense_bf16_cross", {}),
              ("C3 stored dS", "dense_bf16_s2048", {"store_ds": True}),
+             ("C3 O+LSE supplied, stored dS", "dense_bf16_s2048", {"supplied": True, "store_ds": True}),
              ("C4 stored dS", "dense_bf16_cross", {"store_ds": True})]
     for tag, name, opt in dense:
         if not want(tag):
