@@ -109,3 +109,29 @@ def test_store_ds_full_size_sampled(bd):
         _close([x[b, :, h] for x in res], [x[b, :, h] for x in ref])
     again = _run(bd, c, False, True)
     assert all(torch.equal(x, y) for x, y in zip(res, again))
+
+
+def test_store_ds_with_o_lse_and_strided_views(bd):
+    """O and LSE supplied (delta from dY . O) with stored dS, and the same call
+    on q, k, v and dq, dk, dv as interleaved views of fused [B, S, 3, H, D]
+    tensors: the strided call matches the contiguous one bit for bit, and both
+    match the oracle."""
+    from oracle import attn_bwd_dense, attn_fwd_dense
+    c = inputs.dense_inputs(batch=2, heads=2, seq_q=256, seq_k=256, head_dim=128, seed=840, scale=0.5, causal=True,
+                            key_mask_zero_frac=0.1, bias=True)
+    o, lse = attn_fwd_dense(c.q, c.k, c.v, causal=True, key_mask=c.key_mask, bias=c.bias)
+    q, k, v, dy = (_dev(x) for x in (c.q, c.k, c.v, c.dy))
+    km = torch.from_numpy(c.key_mask).cuda()
+    bi = _dev(c.bias)
+    o_t = _dev(o.astype(np.float32))
+    lse_t = torch.from_numpy(lse.astype(np.float32)).cuda().contiguous()
+    a = bd.dense_backward(q, k, v, dy, causal=True, key_mask=km, bias=bi, o=o_t, lse=lse_t, store_ds=True)
+    fused = torch.stack([q, k, v], dim=2).contiguous()  # [B, S, 3, H, D]
+    grads = torch.empty_like(fused)
+    outs = (grads[:, :, 0], grads[:, :, 1], grads[:, :, 2])
+    b = bd.dense_backward(fused[:, :, 0], fused[:, :, 1], fused[:, :, 2], dy, causal=True, key_mask=km, bias=bi,
+                          o=o_t, lse=lse_t, store_ds=True, outputs=outs)
+    bd.check_device_error()
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+    _close(a, attn_bwd_dense(c.q, c.k, c.v, c.dy, causal=True, key_mask=c.key_mask, bias=c.bias))
