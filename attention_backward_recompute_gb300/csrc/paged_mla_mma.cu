@@ -33,6 +33,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "paged_common.cuh"
 #include "paged_launch.h"
 #include "sm103.cuh"
@@ -1069,16 +1071,17 @@ cudaError_t launch_paged_mla_mma_split(const PagedMlaMaps& m, const PagedParams&
   cfg.stream = s;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  // as many clusters as fit the GPU at once (one CTA per SM), cached per device
-  static int clusters[64] = {0};
+  // as many clusters as fit the GPU at once (one CTA per SM), cached per
+  // device (host threads may race to fill an entry: they store the same value)
+  static std::atomic<int> clusters[64];
   int dev = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-  int ncl = dev < 64 ? clusters[dev] : 0;
+  int ncl = dev < 64 ? clusters[dev].load(std::memory_order_relaxed) : 0;
   if (ncl == 0) {
     cfg.gridDim = dim3(kCL, 1, 1);
     if ((e = cudaOccupancyMaxActiveClusters(&ncl, kern, &cfg)) != cudaSuccess) return e;
     if (ncl < 1) return cudaErrorInvalidConfiguration;
-    if (dev < 64) clusters[dev] = ncl;
+    if (dev < 64) clusters[dev].store(ncl, std::memory_order_relaxed);
   }
   cfg.gridDim = dim3(ncl * kCL, 1, 1);
   return cudaLaunchKernelEx(&cfg, kern, m.q, m.qp, m.dy, m.k, m.kp, p);
