@@ -226,7 +226,7 @@ ATTN_API attn_status_t attn_bwd_paged_compact(const attn_paged_desc* d, const vo
     attn::timing_mark_begin(4, s);
     cudaError_t e = attn::launch_paged_prep(p, s);
     attn::timing_mark(s);
-    if (e == cudaSuccess) e = attn::launch_paged_zero_unlinked(p, s);
+    if (e == cudaSuccess) e = attn::launch_paged_zero_unlinked(p, compact ? history_pages : nullptr, num_history_pages, s);
     attn::timing_mark(s);
     if (e == cudaSuccess) e = attn::launch_paged_mla_mma(mm, p, s);
     attn::timing_mark(s);
@@ -265,7 +265,7 @@ ATTN_API attn_status_t attn_bwd_paged_compact(const attn_paged_desc* d, const vo
   attn::timing_mark_begin(nk, s);
   cudaError_t e = attn::launch_paged_prep(p, s);
   attn::timing_mark(s);
-  if (e == cudaSuccess) e = attn::launch_paged_zero_unlinked(p, s);
+  if (e == cudaSuccess) e = attn::launch_paged_zero_unlinked(p, compact ? history_pages : nullptr, num_history_pages, s);
   attn::timing_mark(s);
   if (e == cudaSuccess && d->num_seqs > 0 && d->max_pages_per_seq > 0) e = attn::launch_paged_history(m, p, s);
   attn::timing_mark(s);

@@ -17,7 +17,9 @@ struct PagedMaps {
 };
 
 cudaError_t launch_paged_prep(const PagedParams& p, cudaStream_t s);
-cudaError_t launch_paged_zero_unlinked(const PagedParams& p, cudaStream_t s);
+// zero the pool rows of pages no link references: every page (list null) or
+// the n listed ones (compact history)
+cudaError_t launch_paged_zero_unlinked(const PagedParams& p, const int32_t* list, int64_t n, cudaStream_t s);
 cudaError_t launch_paged_history(const PagedMaps& m, const PagedParams& p, cudaStream_t s);
 cudaError_t launch_paged_row_stats(const PagedMaps& m, const PagedParams& p, cudaStream_t s);
 // query side (GQA): row statistics and dQ in one kernel; q_stats/dy_stats maps

@@ -103,17 +103,17 @@ __global__ void order_links_kernel(PagedParams p) {
   }
 }
 
-// zero rows of pages that no link references: one thread per 16 bytes
-__global__ void zero_unlinked_kernel(PagedParams p, void* pool, int dim) {
-  const int64_t row_vec = dim / 8;  // 16-byte vectors per pool row (bf16)
-  const int64_t per_page = static_cast<int64_t>(p.page_size) * p.KVH * row_vec;
-  const int64_t n = per_page * p.num_pages;
+// zero the rows of pages that no link references: one block per page (of
+// the pool, or of the compact-history list), 16 bytes per thread
+__global__ void zero_unlinked_kernel(PagedParams p, void* pool, int dim, const int32_t* list, int nlist) {
+  const int per_page = p.page_size * p.KVH * (dim / 8);  // 16-byte vectors per page (bf16 rows)
+  const int npg = list ? nlist : p.num_pages;
   const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int page = static_cast<int>(i / per_page);
-    if (p.link_count[page] != 0 || (p.listed && !p.listed[page])) continue;
-    reinterpret_cast<uint4*>(pool)[i] = z;
+  for (int i = blockIdx.x; i < npg; i += gridDim.x) {
+    const int page = list ? list[i] : i;
+    if (page < 0 || page >= p.num_pages || p.link_count[page] != 0) continue;  // uniform over the block
+    uint4* dst = reinterpret_cast<uint4*>(pool) + static_cast<int64_t>(page) * per_page;
+    for (int v = threadIdx.x; v < per_page; v += blockDim.x) dst[v] = z;
   }
 }
 
@@ -156,11 +156,14 @@ cudaError_t launch_paged_prep(const PagedParams& p, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_paged_zero_unlinked(const PagedParams& p, cudaStream_t s) {
-  const int64_t blocks = 152 * 8;
-  if ((p.wrt & 2u) && p.dk_pool) zero_unlinked_kernel<<<blocks, 256, 0, s>>>(p, p.dk_pool, p.Dk);
-  if ((p.wrt & 4u) && p.dv_pool && p.Dp == 0) zero_unlinked_kernel<<<blocks, 256, 0, s>>>(p, p.dv_pool, p.Dv);
-  if ((p.wrt & 8u) && p.dkp_pool && p.Dp > 0) zero_unlinked_kernel<<<blocks, 256, 0, s>>>(p, p.dkp_pool, p.Dp);
+cudaError_t launch_paged_zero_unlinked(const PagedParams& p, const int32_t* list, int64_t nlist, cudaStream_t s) {
+  const int64_t npg = list ? nlist : p.num_pages;
+  if (npg <= 0) return cudaSuccess;
+  const int blocks = static_cast<int>(npg < 152 * 8 ? npg : 152 * 8);
+  const int n = static_cast<int>(npg);
+  if ((p.wrt & 2u) && p.dk_pool) zero_unlinked_kernel<<<blocks, 256, 0, s>>>(p, p.dk_pool, p.Dk, list, n);
+  if ((p.wrt & 4u) && p.dv_pool && p.Dp == 0) zero_unlinked_kernel<<<blocks, 256, 0, s>>>(p, p.dv_pool, p.Dv, list, n);
+  if ((p.wrt & 8u) && p.dkp_pool && p.Dp > 0) zero_unlinked_kernel<<<blocks, 256, 0, s>>>(p, p.dkp_pool, p.Dp, list, n);
   return cudaGetLastError();
 }
 
