@@ -127,6 +127,19 @@ struct MPass {
     if (++tile < ntiles) return true;
     return next_pass(rt);
   }
+  // k tiles further on, a pass at a time
+  __device__ bool skip(int k, int rt) {
+    while (k > 0) {
+      const int left = ntiles - 1 - tile;  // tiles after the current one in this pass
+      if (k <= left) {
+        tile += k;
+        return true;
+      }
+      k -= left + 1;
+      if (!next_pass(rt)) return false;  // tile 0 of the next pass that has tiles
+    }
+    return true;
+  }
 };
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
@@ -211,9 +224,10 @@ static_assert(BT % kCL == 0, "tokens split evenly over the cluster");
 // stores is finished here unless its link passes are heavy, which it flags.
 // SPLIT = true: persistent clusters of kCL CTAs take the flagged blocks (heavy
 // block k to cluster k mod clusters); CTA r of a cluster runs the block's
-// tiles r, r + kCL, ..., the partial sums meet in shared memory and each CTA
-// adds its BT / kCL tokens' partials over the cluster in rank order (a fixed order:
-// the result does not depend on the number of clusters or on timing).
+// tiles [r n / kCL, (r + 1) n / kCL) of its n, the partial sums meet in
+// shared memory and each CTA adds its BT / kCL tokens' partials over the
+// cluster in rank order (a fixed order: the result does not depend on the
+// number of clusters or on timing).
 template <bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     mla_mma_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_qp,
@@ -224,7 +238,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ uint64_t bar_k, bar_full[2];
   __shared__ int abort_flag;
   __shared__ MPageInfo pinfo;
-  __shared__ int n_tiles_sh, any_store_sh, heavy_sh;
+  __shared__ int n_tiles_sh, tile0_sh, any_store_sh, heavy_sh;
   // (the copy iterator lives in shared memory: only thread 0 uses it, and in
   // registers it would be held by every thread)
   __shared__ MPass pf;
@@ -298,7 +312,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!SPLIT) p.heavy[item] = heavy;
       any_store_sh = any;
       heavy_sh = heavy;
-      n_tiles_sh = n_all > rank ? (n_all - rank + ncta - 1) / ncta : 0;  // tiles rank, rank + ncta, ...
+      // this CTA's share of the block's tiles: [t0, t1), contiguous
+      const int t0 = rank * n_all / ncta, t1 = (rank + 1) * n_all / ncta;
+      tile0_sh = t0;
+      n_tiles_sh = t1 - t0;
     }
     __syncthreads();
     // pages all stored by their owners elsewhere, or a heavy block: nothing to
@@ -321,11 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_load_3d(st + 8 * CQ, &tm_qp, bar, 0, gkv * G, r0);
       if (SPLIT) ++issued[stage];
     };
-    auto pf_next = [&]() -> bool {  // the next tile this CTA owns
-      for (int k = 0; k < ncta; ++k)
-        if (!pf.advance(RT)) return false;
-      return true;
-    };
+    auto pf_next = [&]() -> bool { return pf.advance(RT); };
     if (threadIdx.x == 0 && n > 0 && !abort_flag) {
       tma_prefetch_map(&tm_q);
       tma_prefetch_map(&tm_qp);
@@ -344,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       pf.s0 = s0;
       pf.tb = tb;
       pf_live = pf.begin(RT);
-      for (int k = 0; k < rank && pf_live; ++k) pf_live = pf.advance(RT);
+      if (pf_live) pf_live = pf.skip(tile0_sh, RT);
       for (int t = 0; t < 2 && t < n && pf_live; ++t) {
         issue_tile(tc0 + t);
         pf_live = pf_next();
@@ -359,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     MPass it{&p, &pinfo, s0, tb};
     bool live = n > 0 && it.begin(RT);
-    for (int k = 0; k < rank && live; ++k) live = it.advance(RT);
+    if (live) live = it.skip(tile0_sh, RT);
     bool ok = true;
     if (n > 0) {
       ok = mbar_wait_warp(&bar_k, k_phase & 1, ab);
@@ -461,11 +474,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       __syncthreads();  // stage and P^T/dS^T buffers free
-      if (threadIdx.x == 0 && pf_live && !abort_flag) {
+      // (the copy iterator runs on past this CTA's share of the tiles: stop at n)
+      if (threadIdx.x == 0 && pf_live && t + 2 < n && !abort_flag) {
         issue_tile(u + 2);  // owned tile t + 2, into the stage just freed
         pf_live = pf_next();
       }
-      for (int k = 0; k < ncta && live; ++k) live = it.advance(RT);
+      if (live) live = it.advance(RT);
     }
     (void)live;
     tc = tc0 + n;
