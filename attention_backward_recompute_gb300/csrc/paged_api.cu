@@ -223,15 +223,18 @@ ATTN_API attn_status_t attn_bwd_paged_compact(const attn_paged_desc* d, const vo
     else
       mm.q = mm.qp = mm.dy = mm.k;
     if (!enc) return api_fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed");
-    attn::timing_mark_begin(4, s);
+    attn::timing_mark_begin(5, s);
     cudaError_t e = attn::launch_paged_prep(p, s);
     attn::timing_mark(s);
     if (e == cudaSuccess) e = attn::launch_paged_zero_unlinked(p, compact ? history_pages : nullptr, num_history_pages, s);
     attn::timing_mark(s);
-    if (e == cudaSuccess) e = attn::launch_paged_mla_mma(mm, p, s);
+    // blocks whose shared pages carry many links: flagged, then split over
+    // clusters, with the other blocks' kernel starting on the SMs left free
+    if (e == cudaSuccess) e = attn::launch_paged_mla_plan(p, s);
     attn::timing_mark(s);
-    // blocks whose shared pages carry many links: split over clusters
     if (e == cudaSuccess) e = attn::launch_paged_mla_mma_split(mm, p, s);
+    attn::timing_mark(s);
+    if (e == cudaSuccess) e = attn::launch_paged_mla_mma(mm, p, s);
     attn::timing_mark(s);
     attn::timing_mark_end();
     if (e != cudaSuccess) return api_fail(ATTN_ERR_CUDA, "paged launch failed: %s", cudaGetErrorString(e));

@@ -39,7 +39,10 @@ bool mla_mma_supported(const PagedParams& p);
 cudaError_t launch_paged_mla_mma(const PagedMlaMaps& m, const PagedParams& p, cudaStream_t s);
 // compact history: p.listed[page] = 1 for the n listed pages (zero otherwise)
 cudaError_t launch_paged_listed(const PagedParams& p, const int32_t* pages, int64_t n, cudaStream_t s);
-// the blocks launch_paged_mla_mma flagged as heavy, by clusters of CTAs
+// flags the MLA history blocks whose shared pages carry many link tiles (p.heavy)
+cudaError_t launch_paged_mla_plan(const PagedParams& p, cudaStream_t s);
+// the flagged blocks, by clusters of CTAs; launched before launch_paged_mla_mma,
+// which then runs as its programmatic dependent on the SMs the clusters leave
 cudaError_t launch_paged_mla_mma_split(const PagedMlaMaps& m, const PagedParams& p, cudaStream_t s);
 // MLA row statistics on the same path; q, qp, dy maps with box (64, G, 64/G)
 cudaError_t launch_paged_mla_stats_mma(const PagedMlaMaps& m, const PagedParams& p, cudaStream_t s);

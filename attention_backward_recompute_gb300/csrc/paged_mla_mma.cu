@@ -170,6 +170,31 @@ __device__ __forceinline__ uint32_t swz(uint32_t base, int row, int piece) {
   return base + row * 128 + (((piece ^ row) & 7) << 4);
 }
 
+// Pages of block tb (4 pages) of sequence s0: physical page, link segment,
+// and whether this block stores the page (it is the page's first link and,
+// in compact history, the page is listed).
+__device__ __forceinline__ void block_info(const PagedParams& p, int s0, int tb, MPageInfo* pi) {
+  const int npg = pages_of(seq_len_of(p, s0), p.page_size);
+  for (int j = 0; j < 4; ++j) {
+    const int lp = tb * 4 + j;
+    int ph = -1, off = 0, cnt = 0, st = 0;
+    if (lp < npg) {
+      ph = p.page_table[static_cast<int64_t>(s0) * p.max_pages + lp];
+      if (ph >= 0 && ph < p.num_pages) {
+        off = p.link_off[ph];
+        cnt = p.link_off[ph + 1] - off;
+        st = cnt > 0 && p.links[off] == s0 * p.max_pages + lp && (!p.listed || p.listed[ph]);
+      } else {
+        ph = -1;
+      }
+    }
+    pi->phys[j] = ph;
+    pi->off[j] = off;
+    pi->cnt[j] = cnt;
+    pi->store[j] = st;
+  }
+}
+
 // Cluster primitives of the split kernel.
 __device__ __forceinline__ int cluster_rank() {
   uint32_t r;
@@ -220,8 +245,35 @@ constexpr int RED_STRIDE = kLat + kPos + 8;  // floats per token row of a partia
 static_assert(BT * RED_STRIDE * 4 <= BYTES, "a partial fits the tiles' shared memory");
 static_assert(BT % kCL == 0, "tokens split evenly over the cluster");
 
+// Plan of the MLA history: heavy[(s0 * nblk + tb) * KVH + g] = 1 when the
+// pages block tb of sequence s0 stores carry more than kHeavyLinkTiles tiles of
+// other links (counting stops there), else 0; one thread per block.
+__global__ void mla_plan_kernel(const PagedParams p) {
+  const int nblk = (p.max_pages + 3) / 4;
+  const int n = p.S * nblk;
+  const int RT = BC / p.G;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+    const int s0 = i / nblk, tb = i - s0 * nblk;
+    int heavy = 0;
+    if (tb * 4 < pages_of(seq_len_of(p, s0), p.page_size)) {
+      MPageInfo pi;
+      block_info(p, s0, tb, &pi);
+      if (pi.store[0] | pi.store[1] | pi.store[2] | pi.store[3]) {
+        MPass it{&p, &pi, s0, tb};
+        int n_link = 0;
+        if (it.begin(RT)) {
+          do n_link += it.j >= 0 ? 1 : 0;
+          while (n_link <= kHeavyLinkTiles && it.advance(RT));
+        }
+        heavy = n_link > kHeavyLinkTiles;
+      }
+    }
+    for (int g = 0; g < p.KVH; ++g) p.heavy[static_cast<int64_t>(i) * p.KVH + g] = heavy;
+  }
+}
+
 // SPLIT = false: one CTA per (64-token block, sequence, KV head); a block it
-// stores is finished here unless its link passes are heavy, which it flags.
+// stores is finished here unless the plan flagged its link passes as heavy.
 // SPLIT = true: persistent clusters of kCL CTAs take the flagged blocks (heavy
 // block k to cluster k mod clusters); CTA r of a cluster runs the block's
 // tiles [r n / kCL, (r + 1) n / kCL) of its n, the partial sums meet in
@@ -258,12 +310,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   const float kInf = __int_as_float(0x7f800000);
   const uint32_t p_base = sbase + P_OFF, ds_base = sbase + P_OFF + PS;
 
-  if (!SPLIT) {
+  if (SPLIT) {
+    // the main kernel may start on the SMs these clusters leave free
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  } else {
+    // launched as the split kernel's programmatic dependent: the last CTA
+    // waits for the split grid, so this grid completes after it and later
+    // work in the stream sees both
+    if (blockIdx.x == gridDim.x - 1 && blockIdx.y == gridDim.y - 1 && blockIdx.z == gridDim.z - 1)
+      asm volatile("griddepcontrol.wait;" ::: "memory");
     const int tb = blockIdx.x, s0 = blockIdx.y;
-    if (tb * 4 >= pages_of(seq_len_of(p, s0), p.page_size)) {  // no token of the sequence here (uniform)
-      if (threadIdx.x == 0) p.heavy[(s0 * nblk + tb) * p.KVH + blockIdx.z] = 0;
-      return;
-    }
+    if (tb * 4 >= pages_of(seq_len_of(p, s0), p.page_size)) return;  // no token of the sequence here (uniform)
   }
   if (threadIdx.x == 0) {
     abort_flag = 0;
@@ -280,36 +337,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto run_block = [&](int tb, int s0, int gkv, int item) {
     __syncthreads();  // the previous block's readers of pinfo are done
     if (threadIdx.x == 0) {
-      const int npg = pages_of(seq_len_of(p, s0), p.page_size);
-      for (int j = 0; j < 4; ++j) {
-        const int lp = tb * 4 + j;
-        int ph = -1, off = 0, cnt = 0, st = 0;
-        if (lp < npg) {
-          ph = p.page_table[static_cast<int64_t>(s0) * p.max_pages + lp];
-          if (ph >= 0 && ph < p.num_pages) {
-            off = p.link_off[ph];
-            cnt = p.link_off[ph + 1] - off;
-            st = cnt > 0 && p.links[off] == s0 * p.max_pages + lp && (!p.listed || p.listed[ph]);
-          } else {
-            ph = -1;
-          }
-        }
-        pinfo.phys[j] = ph;
-        pinfo.off[j] = off;
-        pinfo.cnt[j] = cnt;
-        pinfo.store[j] = st;
-      }
+      block_info(p, s0, tb, &pinfo);
       const int any = pinfo.store[0] | pinfo.store[1] | pinfo.store[2] | pinfo.store[3];
       MPass it{&p, &pinfo, s0, tb};
-      int n_all = 0, n_own = 0;
+      int n_all = 0;
       if (any && it.begin(RT)) {
-        do {
-          ++n_all;
-          n_own += it.j < 0 ? 1 : 0;
-        } while (it.advance(RT));
+        do ++n_all;
+        while (it.advance(RT));
       }
-      const int heavy = !SPLIT && any && n_all - n_own > kHeavyLinkTiles;
-      if (!SPLIT) p.heavy[item] = heavy;
+      // heavy blocks (flagged by the plan kernel) belong to the split kernel
+      const int heavy = !SPLIT && any && p.heavy[item] != 0;
       any_store_sh = any;
       heavy_sh = heavy;
       // this CTA's share of the block's tiles: [t0, t1), contiguous
@@ -1061,8 +1098,26 @@ cudaError_t launch_paged_mla_mma(const PagedMlaMaps& m, const PagedParams& p, cu
   auto kern = mla_mma_kernel<false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  dim3 grid((p.max_pages + 3) / 4, p.S, p.KVH);
-  kern<<<grid, kThreads, smem, s>>>(m.q, m.qp, m.dy, m.k, m.kp, p);
+  // programmatic dependent of the split kernel launched just before it: it
+  // may start while the split clusters run (it reads none of their results)
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((p.max_pages + 3) / 4, p.S, p.KVH);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, m.q, m.qp, m.dy, m.k, m.kp, p);
+}
+
+cudaError_t launch_paged_mla_plan(const PagedParams& p, cudaStream_t s) {
+  const int64_t n = static_cast<int64_t>(p.S) * ((p.max_pages + 3) / 4);
+  if (n == 0 || p.num_pages == 0) return cudaSuccess;
+  const int blocks = static_cast<int>((n + 127) / 128 < 1024 ? (n + 127) / 128 : 1024);
+  mla_plan_kernel<<<blocks, 128, 0, s>>>(p);
   return cudaGetLastError();
 }
 

@@ -378,8 +378,10 @@ def sweep(args) -> int:
                                          heads=c.heads, kv_heads=c.kv_heads, page_size=c.page_size,
                                          causal=c.causal, outputs=outs, qp=dv["qp"], kp_pool=dv["kp"])
         ms, ms_min = timed(call, 20)
-        # per-kernel split of one call: links, zero store, history (MLA: + the cluster-split kernel)
-        names = ["links", "zero_unlinked", "history"] + (["history_split"] if c.position_dim else [])
+        # per-kernel split of one call: links, zero store, history (MLA: plan, the cluster-split kernel,
+        # then the history kernel; the recorded events keep these two from overlapping in this one call)
+        names = (["links", "zero_unlinked", "plan", "history_split", "history"] if c.position_dim
+                 else ["links", "zero_unlinked", "history"])
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
         for e in evs:  # CUDA events are created on first record
             e.record()

@@ -413,9 +413,10 @@ ATTN_API attn_status_t attn_selftest_wait_timeout(void* stream);
  * four split kernels for q, dy, k, v; the row-statistics prologue; the dK/dV
  * kernel (if dK or dV is requested); the dQ kernel (if dQ is requested).  The
  * paged backward launches its link preparation, the zero store of unlinked
- * pages and the history kernel (MLA: then the cluster-split history kernel of
- * the blocks whose shared pages carry many links; the compact call marks its
- * page list before events[0]); the paged row statistics one kernel.
+ * pages and the history kernel (MLA: a plan kernel that flags the blocks whose
+ * shared pages carry many links, the cluster-split kernel of those blocks,
+ * then the history kernel of the others; the compact call marks its page list
+ * before events[0]); the paged row statistics one kernel.
  */
 ATTN_API void attn_set_timing_events(void* const* events, int count);
 
