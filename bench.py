@@ -79,7 +79,10 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+        # raw samples: $BENCH_CLOCKS_DIR/clocks_rank<i>.csv if set, else a temporary file
+        import tempfile
+        d = os.environ.get("BENCH_CLOCKS_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(d, f"clocks_rank{index}.csv")
 
     def start(self):
         try:
