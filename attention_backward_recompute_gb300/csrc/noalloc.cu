@@ -25,7 +25,10 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
 // Device address of the scratch array for the current device.  In host code
 // the array's name is only a host-side stand-in, so the address comes from
-// cudaGetSymbolAddress, once per device, with that device current.
+// cudaGetSymbolAddress, once per device, with that device current.  The
+// cached address belongs to the device's primary context: after
+// cudaDeviceReset (which tears that context down) it is stale, and this entry
+// point must not be used again in the process.
 void* scratch_address() {
   static void* addr[64] = {nullptr};
   static std::mutex mu;
@@ -53,6 +56,10 @@ extern "C" ATTN_API attn_status_t attn_bwd_dense_noalloc(const attn_dense_desc* 
     return attn::api_fail(ATTN_ERR_UNSUPPORTED,
                           "the library-owned scratch holds row statistics only; fp32 storage also needs split "
                           "copies of the inputs: use attn_bwd_dense with a workspace");
+  if (d->mask_flags & ATTN_MASK_ELEM)
+    return attn::api_fail(ATTN_ERR_UNSUPPORTED,
+                          "the per-element mask's packed bits do not fit the library-owned scratch: use "
+                          "attn_bwd_dense_strided with a workspace");
   if (d->options & ATTN_OPT_STORE_DS)
     return attn::api_fail(ATTN_ERR_UNSUPPORTED,
                           "stored dS does not fit the library-owned scratch: use attn_bwd_dense with a workspace");

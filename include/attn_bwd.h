@@ -178,10 +178,14 @@ ATTN_API attn_status_t attn_bwd_dense(const attn_dense_desc* d, const void* q, c
  *
  *   - batch * heads * seq_q above ATTN_NOALLOC_MAX_ROWS is rejected with
  *     ATTN_ERR_UNSUPPORTED (use attn_bwd_dense with a workspace instead), and
- *     so is fp32 storage (its split input copies do not fit the scratch).
+ *     so are fp32 storage (its split input copies do not fit the scratch),
+ *     ATTN_OPT_STORE_DS (the stored dS tiles do not fit either) and
+ *     ATTN_MASK_ELEM (the packed mask bits do not fit either).
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress; it allocates nothing) with that device current;
- *     make that first call before any stream capture.
+ *     make that first call before any stream capture.  The address is cached
+ *     for the life of the process: after cudaDeviceReset on a device, do not
+ *     call this entry point on that device again.
  *   - All calls share the one array and it keeps the last call's contents.
  *     Calls whose kernels overlap on the GPU (other streams, other host
  *     threads) race on it: serialise them.

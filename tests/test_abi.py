@@ -218,3 +218,17 @@ def test_store_ds_option_checks(lib):
                                              ctypes.c_void_p(FAKE + 20 * MB), ctypes.c_void_p(FAKE + 24 * MB), 7,
                                              None))
     assert st == bd.ATTN_ERR_UNSUPPORTED
+
+
+def test_noalloc_refuses_elem_mask(lib):
+    """The no-allocation entry point refuses the per-element mask by name (its
+    packed bits would need workspace) before touching any pointer."""
+    d = _desc(batch=1, heads=2, seq_q=64, seq_k=64, head_dim=64)
+    d.mask_flags |= bd.ATTN_MASK_ELEM
+    st = int(bd.lib().attn_bwd_dense_noalloc(ctypes.byref(d), ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE + 4 * MB),
+                                             ctypes.c_void_p(FAKE + 8 * MB), ctypes.c_void_p(FAKE + 12 * MB), None,
+                                             None, None, None, ctypes.c_void_p(FAKE + 16 * MB),
+                                             ctypes.c_void_p(FAKE + 20 * MB), ctypes.c_void_p(FAKE + 24 * MB), 7,
+                                             None))
+    assert st == bd.ATTN_ERR_UNSUPPORTED
+    assert "per-element" in bd.last_error()
