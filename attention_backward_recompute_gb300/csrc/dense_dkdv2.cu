@@ -1,22 +1,23 @@
-// dK / dV kernel with the softmax and the dS work on separate warpgroups and
-// P, dS kept in tensor memory (bf16 storage path).
+// dK / dV kernel, bf16 storage: the tensor core forms the score and dP tiles
+// of one tile while two groups of compute warps turn earlier tiles into P and
+// dS, kept in tensor memory.
 //
 // Same products as rlx-cpu src/attention_bwd.rs (fn backward_dense_head_all),
 // per 128-key tile j and 64-query tile i of one (batch, head):
 //   S^T  = K_j Q_i^T                    tcgen05 (smem x smem), TMEM buffer S[b]
 //   dP^T = V_j dY_i^T                   tcgen05 (smem x smem), TMEM buffer dP[b]
-//   P^T  = exp(S^T*scale + bias - lse)  softmax warpgroup: reads S[b], writes
-//                                       P^T as bf16 over the first half of S[b]
-//   dS^T = P^T * (dP^T - delta)         dS warpgroup: reads dP[b] and P^T,
-//                                       writes dS^T as bf16 over dP[b]
+//   P^T  = exp(S^T*scale + bias - lse)  written as bf16 over the first half of S[b]
+//   dS^T = P^T * (dP^T - delta)         written as bf16 over the first half of dP[b]
 //   dV_j += P^T dY_i                    tcgen05, A = P^T from tensor memory
 //   dK_j += dS^T Q_i                    tcgen05, A = dS^T from tensor memory
-// S and dP are double-buffered (b = i % 2); each buffer has its own softmax
-// warpgroup, so two tiles are in the softmax at once while the dS warpgroup
-// and the tensor core work on others.  Q, dY, bias and the row statistics come
-// through a 3-stage TMA ring.  Warp 0: TMA producer, warp 1: MMA issuer (one
-// thread), warps 4..7: softmax of even tiles, warps 12..15: softmax of odd
-// tiles, warps 8..11: dS.
+// S and dP are double-buffered (b = i % 2).  Compute group b (four warps, one
+// TMEM lane quarter each) owns the tiles of parity b: it forms P^T(i), hands
+// it to the tensor core, then forms dS^T(i) from the P^T values it still holds
+// in registers and dP^T(i).  Once P^T(i) is handed over, nothing reads S[b]
+// any more, so the score tile of i + 2 can be formed while the group works on
+// dS^T(i).  Q, dY, bias and the row statistics come through a 3-stage TMA
+// ring.  Warp 0: TMA producer, warp 1: MMA issuer (whole warp, elect.sync),
+// warps 4..7: group 0, warps 8..11: group 1.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -43,7 +44,7 @@ struct Dkdv2Layout {
   static constexpr int Q_OFF = V_OFF + KV;                 // kStages
   static constexpr int DY_OFF = Q_OFF + kStages * QT;      // kStages
   static constexpr int BIAS_OFF = DY_OFF + kStages * QT;   // kStages
-  static constexpr int ST_OFF = BIAS_OFF + kStages * BIAS; // kStages x {L2, delta, pm} x 64 floats
+  static constexpr int ST_OFF = BIAS_OFF + kStages * BIAS; // kStages x {-L2, delta, pm} x 64 floats
   static constexpr int BYTES = ST_OFF + kStages * 3 * BQ * 4;
   // TMEM: dV [0, DP), dK [DP, 2DP), S[2] and dP[2] 64 columns each after that
   static constexpr int T_S = 2 * DP, T_DP = 2 * DP + 128;
@@ -68,34 +69,42 @@ __device__ __forceinline__ void reg_fence16(uint32_t (&r)[16]) {
 }
 
 // 16 queries [c0, c0+16) of the P^T row of one key: exp2(S*scale*log2e +
-// bias*log2e - L2) as 8 bf16 pairs.  CHECK: zero the queries outside [lo, hi]
-// (tile-local range of queries that see this key).  KM: the key is
-// custom-masked; its visible entries take the row's masked-key probability
-// pm instead.
+// bias*log2e - L2) as 8 bf16 pairs, the arithmetic on fp32 pairs.  st holds
+// -L2 per query.  bq[m] points at this key's bias of query m (m < 8) of the
+// chunk; query m + 8 is 8 rows further on.  CHECK: zero the queries outside
+// [lo, hi] (tile-local range of queries that see this key).  kmasked: the key
+// is custom-masked; its visible entries take the row's masked-key
+// probability pm instead.
 template <bool HAS_BIAS, bool CHECK, bool ELEM>
-__device__ __forceinline__ void p_chunk(const uint32_t (&sr)[16], int c0, const float* st, const uint8_t* bias_s,
-                                        int kc, int kb, float scale_log2, int lo, int hi, bool kmasked,
-                                        uint32_t ebits, uint32_t* pw) {
+__device__ __forceinline__ void p_chunk(const uint32_t (&sr)[16], int c0, const float* st, const uint8_t* const* bq,
+                                        float scale_log2, int lo, int hi, bool kmasked, uint32_t ebits,
+                                        uint32_t* pw) {
+  const uint64_t sl2 = f2_pack(scale_log2, scale_log2);
+  const uint64_t l2e = f2_pack(kLog2e, kLog2e);
 #pragma unroll
   for (int c4 = 0; c4 < 4; ++c4) {
-    const float4 l2 = *reinterpret_cast<const float4*>(st + c0 + 4 * c4);
-    const float l2v[4] = {l2.x, l2.y, l2.z, l2.w};
-    float pv[4];
+    const float4 nl = lds_f4(st + c0 + 4 * c4);
+    uint64_t x[2];
+    x[0] = f2_fma(f2_pack_u(sr[4 * c4], sr[4 * c4 + 1]), sl2, f2_pack(nl.x, nl.y));
+    x[1] = f2_fma(f2_pack_u(sr[4 * c4 + 2], sr[4 * c4 + 3]), sl2, f2_pack(nl.z, nl.w));
+    if (HAS_BIAS) {
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int ql = c0 + 4 * c4 + e;
-      float x = fmaf(__uint_as_float(sr[4 * c4 + e]), scale_log2, -l2v[e]);
-      if (HAS_BIAS) {
-        const uint32_t off = ql * 128 + (((kc ^ ql) & 7) << 4) + kb;
-        const uint16_t bbits = *reinterpret_cast<const uint16_t*>(bias_s + off);
-        x = fmaf(__uint_as_float(static_cast<uint32_t>(bbits) << 16), kLog2e, x);
+      for (int h2 = 0; h2 < 2; ++h2) {
+        const int m0 = 4 * c4 + 2 * h2;  // query of the chunk, 0..15
+        const uint32_t b0 = *reinterpret_cast<const uint16_t*>(bq[m0 & 7] + (m0 >> 3) * 1024);
+        const uint32_t b1 = *reinterpret_cast<const uint16_t*>(bq[(m0 + 1) & 7] + ((m0 + 1) >> 3) * 1024);
+        x[h2] = f2_fma(f2_pack_u(b0 << 16, b1 << 16), l2e, x[h2]);
       }
-      pv[e] = ex2_approx(x);
     }
+    float pv[4];
+    f2_split(x[0], pv[0], pv[1]);
+    f2_split(x[1], pv[2], pv[3]);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) pv[e] = ex2_approx(pv[e]);
     // per-element mask bits of these 4 queries
     const uint32_t e4 = ELEM ? (ebits >> (4 * c4)) & 0xfu : 0u;
     if (kmasked || e4) {
-      const float4 pm = *reinterpret_cast<const float4*>(st + 128 + c0 + 4 * c4);
+      const float4 pm = lds_f4(st + 128 + c0 + 4 * c4);
       const float pmv[4] = {pm.x, pm.y, pm.z, pm.w};
 #pragma unroll
       for (int e = 0; e < 4; ++e) pv[e] = (kmasked || ((e4 >> e) & 1u)) ? pmv[e] : pv[e];
@@ -112,29 +121,39 @@ __device__ __forceinline__ void p_chunk(const uint32_t (&sr)[16], int c0, const 
   }
 }
 
-// The P^T row over the 64 queries of a tile, S read from tensor memory in
-// four 16-column chunks with the next chunk's load in flight; chunk i's 8 bf16
-// pairs go to columns [8i, 8i+8) of the same buffer, which chunks 0..i have
-// already read.  The caller waits for the stores.
+// The P^T row over the 64 queries of a tile into pw (32 bf16 pairs, kept for
+// dS), S read from tensor memory in four 16-column chunks with the next
+// chunk's load in flight; chunk i's 8 pairs also go to columns [8i, 8i+8) of
+// the same buffer, which chunks 0..i have already read.  bias_row points at
+// this key's bias column in the tile (query 0).  The caller waits for the
+// stores.
 template <bool HAS_BIAS, bool CHECK, bool ELEM>
-__device__ __forceinline__ void p_row(uint32_t tS, const float* st, const uint8_t* bias_s, int kc, int kb,
-                                      float scale_log2, int lo, int hi, bool kmasked, uint2 eb) {
-  uint32_t s0[16], s1[16], pw[8];
+__device__ __forceinline__ void p_row(uint32_t tS, const float* st, const uint8_t* bias_row, int kc,
+                                      float scale_log2, int lo, int hi, bool kmasked, uint2 eb, uint32_t (&pw)[32]) {
+  // the 128-byte swizzle moves query m's 16-byte chunk to chunk kc ^ (m % 8)
+  const uint8_t* bq[8];
+#pragma unroll
+  for (int m = 0; m < 8; ++m) bq[m] = bias_row + m * 128 + (((kc ^ m) & 7) << 4);
+  uint32_t s0[16], s1[16];
   tmem_ld16(tS, s0);
   tmem_ld_wait();
   reg_fence16(s0);
-#pragma unroll 1
+#pragma unroll
   for (int i = 0; i < 4; i += 2) {
     tmem_ld16(tS + 16 * (i + 1), s1);
-    p_chunk<HAS_BIAS, CHECK, ELEM>(s0, 16 * i, st, bias_s, kc, kb, scale_log2, lo, hi, kmasked,
-                                   i < 2 ? eb.x : eb.y, pw);
-    tmem_st8(tS + 8 * i, pw);
+    p_chunk<HAS_BIAS, CHECK, ELEM>(s0, 16 * i, st, bq, scale_log2, lo, hi, kmasked, i < 2 ? eb.x : eb.y,
+                                   pw + 8 * i);
+    tmem_st8(tS + 8 * i, pw + 8 * i);
+#pragma unroll
+    for (int m = 0; m < 8; ++m) bq[m] += 16 * 128;
     tmem_ld_wait();
     reg_fence16(s1);
     if (i + 2 < 4) tmem_ld16(tS + 16 * (i + 2), s0);
-    p_chunk<HAS_BIAS, CHECK, ELEM>(s1, 16 * (i + 1), st, bias_s, kc, kb, scale_log2, lo, hi, kmasked,
-                                   (i < 2 ? eb.x : eb.y) >> 16, pw);
-    tmem_st8(tS + 8 * (i + 1), pw);
+    p_chunk<HAS_BIAS, CHECK, ELEM>(s1, 16 * (i + 1), st, bq, scale_log2, lo, hi, kmasked,
+                                   (i < 2 ? eb.x : eb.y) >> 16, pw + 8 * (i + 1));
+    tmem_st8(tS + 8 * (i + 1), pw + 8 * (i + 1));
+#pragma unroll
+    for (int m = 0; m < 8; ++m) bq[m] += 16 * 128;
     if (i + 2 < 4) {
       tmem_ld_wait();
       reg_fence16(s0);
@@ -143,7 +162,7 @@ __device__ __forceinline__ void p_row(uint32_t tS, const float* st, const uint8_
 }
 
 template <int DP, bool HAS_BIAS, bool ELEM, bool DS>
-__global__ void __launch_bounds__(512, 1)
+__global__ void __launch_bounds__(384, 1)
     dkdv2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_dy,
                  const __grid_constant__ CUtensorMap tm_bias, const DenseParams p) {
@@ -151,7 +170,7 @@ __global__ void __launch_bounds__(512, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ uint64_t bar_kv, bar_full[kStages], bar_empty[kStages], bar_s_full[2], bar_dp_full[2], bar_p_full[2],
-      bar_p_read[2], bar_ds_full[2], bar_acc;
+      bar_ds_full[2], bar_acc;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
 
@@ -176,7 +195,6 @@ __global__ void __launch_bounds__(512, 1)
       mbar_init(&bar_s_full[s], 1);
       mbar_init(&bar_dp_full[s], 1);
       mbar_init(&bar_p_full[s], 4);
-      mbar_init(&bar_p_read[s], 4);
       mbar_init(&bar_ds_full[s], 4);
     }
     mbar_init(&bar_acc, 1);
@@ -206,7 +224,7 @@ __global__ void __launch_bounds__(512, 1)
         tma_load_4d(sm + L::V_OFF + c * (L::BK * 128), &tm_v, &bar_kv, c * 64, k0, h, b);
       }
     }
-    // row statistics (L2, delta, pm) of rows lane and lane + 32 of a tile,
+    // row statistics (-L2, delta, pm) of rows lane and lane + 32 of a tile,
     // loaded one tile ahead so their latency overlaps the wait for a stage
     float pre[6];
     auto load_stats = [&](int t) {
@@ -216,7 +234,7 @@ __global__ void __launch_bounds__(512, 1)
         const int q = qb0 + lane + 32 * i;
         const bool in = q < p.Sq;
         const size_t idx = static_cast<size_t>(bh) * p.Sq + (in ? q : 0);
-        pre[3 * i] = in ? p.L2[idx] : __int_as_float(0x7f800000);
+        pre[3 * i] = in ? -p.L2[idx] : -__int_as_float(0x7f800000);
         pre[3 * i + 1] = in ? p.delta[idx] : 0.f;
         pre[3 * i + 2] = (in && p.has_custom) ? p.pm[idx] : 0.f;
       }
@@ -316,26 +334,35 @@ __global__ void __launch_bounds__(512, 1)
         issue_s(t);
         issue_dp(t);
       }
-      // Issue order per tile t: dV(t), S(t+2), dK(t), dP(t+2).  S(t+2) goes
-      // ahead of dK(t) so the softmax of tile t+2 does not wait for dS(t);
-      // it overwrites P(t), which dV(t) (earlier in the same pipe) and the dS
-      // warpgroup (p_read) have consumed.  dP(t+2) overwrites dS(t), read by
-      // dK(t) just before it.
+      // Per tile t: dV(t) once P(t) is in; then S(t+2) and dK(t) in whichever
+      // order their inputs arrive; then dP(t+2).  S(t+2) overwrites P(t),
+      // which dV(t) (earlier in the same pipe) consumes, and S(t), which the
+      // group finished reading before it handed P(t) over; dP(t+2) overwrites
+      // dS(t) and dP(t), read by dK(t) and by the group before dS(t) was
+      // handed over.  Issuing dK(t) as soon as dS(t) is ready releases tile
+      // t's stage early: the copies of tile t+3 wait on that release.
       for (int t = 0; t < n && ok; ++t) {
         const int s = t % kStages, bb = t & 1;
         if (!(ok = mbar_wait_warp(&bar_p_full[bb], (t >> 1) & 1, ab))) break;
         tc_fence_after();
         issue_acc(t_dv, tmem + L::T_S + bb * 64, sdesc_add(dDYm0, s * L::QT), t == 0);
-        if (t + 2 < n) {
-          if (!(ok = mbar_wait_warp(&bar_full[(t + 2) % kStages], ((t + 2) / kStages) & 1, ab))) break;
-          if (!(ok = mbar_wait_warp(&bar_p_read[bb], (t >> 1) & 1, ab))) break;
-          tc_fence_after();
-          issue_s(t + 2);
+        bool s_next = t + 2 < n, k_now = true;
+        PollBudget pb;
+        while (s_next || k_now) {
+          if (s_next && mbar_test_warp(&bar_full[(t + 2) % kStages], ((t + 2) / kStages) & 1)) {
+            tc_fence_after();
+            issue_s(t + 2);
+            s_next = false;
+          }
+          if (k_now && mbar_test_warp(&bar_ds_full[bb], (t >> 1) & 1)) {
+            tc_fence_after();
+            issue_acc(t_dk, tmem + L::T_DP + bb * 64, sdesc_add(dQm0, s * L::QT), t == 0);
+            mma_commit_w(&bar_empty[s]);
+            k_now = false;
+          }
+          if ((s_next || k_now) && !(ok = pb.check(ab))) break;
         }
-        if (!(ok = mbar_wait_warp(&bar_ds_full[bb], (t >> 1) & 1, ab))) break;
-        tc_fence_after();
-        issue_acc(t_dk, tmem + L::T_DP + bb * 64, sdesc_add(dQm0, s * L::QT), t == 0);
-        mma_commit_w(&bar_empty[s]);
+        if (!ok) break;
         if (t + 2 < n) issue_dp(t + 2);
       }
       mma_commit_w(&bar_acc);
@@ -343,15 +370,13 @@ __global__ void __launch_bounds__(512, 1)
     }
     __syncwarp();
   } else if (warp >= 4) {
-    const bool softmax_wg = warp < 8 || warp >= 12;  // warps 4..7, 12..15: P; warps 8..11: dS
-    const int sg = warp >= 12 ? 1 : 0;               // softmax group: tiles (and S buffer) of parity sg
+    const int sg = (warp - 4) >> 2;  // compute group: tiles (and S/dP buffers) of parity sg
     const int lg = warp & 3;
     const int row = lg * 32 + lane;  // key row inside the tile == TMEM lane
     const int key = k0 + row;
     const uint32_t lane_addr = static_cast<uint32_t>(lg * 32) << 16;
     bool ok = n > 0;
-    if (n > 0 && softmax_wg) {
-      // ---------------------------------------------------------- softmax: S^T -> P^T
+    if (n > 0) {
       bool kmasked = false;
       if (p.has_key_mask && key < p.Sk) kmasked = p.key_mask[static_cast<size_t>(b) * p.Sk + key] < p.mask_thr;
       const int half = row >> 6, kc = (row & 63) >> 3, kb = (row & 7) * 2;
@@ -361,51 +386,40 @@ __global__ void __launch_bounds__(512, 1)
       if (p.causal) qa = key - p.q_off;
       if (p.window >= 0) qb = imin(qb, key + p.window - p.q_off);
       if (key >= p.Sk) qa = 1 << 30, qb = -(1 << 30);
-      // Each group waits every phase of its own S buffer.  Of the stage
-      // barrier it skips the phases of the other group's tiles; when it waits
-      // for tile t, the phase of tile t - 3 (same stage, other parity) has
-      // completed, since the tensor core issued S(t - 2) after it.
+      // Each group waits every phase of its own S and dP buffers.  Of the
+      // stage barrier it skips the phases of the other group's tiles; when it
+      // waits for tile t, the phase of tile t - 3 (same stage, other parity)
+      // has completed, since the tensor core issued S(t - 2) after it.
       for (int t = sg; t < n && ok; t += 2) {
         const int s = t % kStages, bb = t & 1;
         const int q0 = (i_lo + t) * L::BQ;
-        if (!(ok = mbar_wait_warp(&bar_full[s], (t / kStages) & 1, ab))) break;
-        if (!(ok = mbar_wait_warp(&bar_s_full[bb], (t >> 1) & 1, ab))) break;
-        tc_fence_after();
-        const uint32_t tS = tmem + L::T_S + bb * 64 + lane_addr;
-        const float* st = reinterpret_cast<const float*>(sm + L::ST_OFF) + s * 3 * L::BQ;
-        const uint8_t* bias_s = sm + L::BIAS_OFF + s * L::BIAS + half * (L::BQ * 128);
-        const bool full = tile_fully_visible(p, q0, q0 + L::BQ - 1, k0, k0 + L::BK - 1);
-        const int lo = qa - q0, hi = qb - q0;
         uint2 eb = make_uint2(0u, 0u);  // per-element mask: this key's bits of the tile's 64 queries
         if (ELEM && key < p.Sk)
           eb = *reinterpret_cast<const uint2*>(p.elem_cols + (static_cast<size_t>(bh) * p.Sk + key) * p.ew_k +
                                                (q0 >> 5));
+        if (!(ok = mbar_wait_warp(&bar_full[s], (t / kStages) & 1, ab))) break;
+        if (!(ok = mbar_wait_warp(&bar_s_full[bb], (t >> 1) & 1, ab))) break;
+        tc_fence_after();
+        // ---------------------------------------------------- S^T -> P^T
+        const uint32_t tS = tmem + L::T_S + bb * 64 + lane_addr;
+        const float* st = reinterpret_cast<const float*>(sm + L::ST_OFF) + s * 3 * L::BQ;
+        const uint8_t* bias_row = sm + L::BIAS_OFF + s * L::BIAS + half * (L::BQ * 128) + kb;
+        const bool full = tile_fully_visible(p, q0, q0 + L::BQ - 1, k0, k0 + L::BK - 1);
+        const int lo = qa - q0, hi = qb - q0;
+        uint32_t pw[32];
         if (full)
-          p_row<HAS_BIAS, false, ELEM>(tS, st, bias_s, kc, kb, p.scale_log2, lo, hi, kmasked, eb);
+          p_row<HAS_BIAS, false, ELEM>(tS, st, bias_row, kc, p.scale_log2, lo, hi, kmasked, eb, pw);
         else
-          p_row<HAS_BIAS, true, ELEM>(tS, st, bias_s, kc, kb, p.scale_log2, lo, hi, kmasked, eb);
+          p_row<HAS_BIAS, true, ELEM>(tS, st, bias_row, kc, p.scale_log2, lo, hi, kmasked, eb, pw);
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar_p_full[bb]);
-      }
-    } else if (n > 0) {
-      // ---------------------------------------------------------- dS: dP^T, P^T -> dS^T
-      for (int t = 0; t < n && ok; ++t) {
-        const int s = t % kStages, bb = t & 1;
-        if (!(ok = mbar_wait_warp(&bar_full[s], (t / kStages) & 1, ab))) break;
+        // ---------------------------------------------------- dP^T, P^T -> dS^T
         if (!(ok = mbar_wait_warp(&bar_dp_full[bb], (t >> 1) & 1, ab))) break;
-        if (!(ok = mbar_wait_warp(&bar_p_full[bb], (t >> 1) & 1, ab))) break;
         tc_fence_after();
         const uint32_t tDP = tmem + L::T_DP + bb * 64 + lane_addr;
-        const uint32_t tS = tmem + L::T_S + bb * 64 + lane_addr;
-        uint32_t pw[32];
-        tmem_ld32(tS, pw);
-        tmem_ld_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bar_p_read[bb]);
-        const float* dl = reinterpret_cast<const float*>(sm + L::ST_OFF) + s * 3 * L::BQ + L::BQ;
+        const float* dl = st + L::BQ;
         // stored dS of tile (key tile, query tile i_lo + t): chunk c of this
         // key at c * 2048 + row * 16
         uint4* ds_row = nullptr;
@@ -425,12 +439,13 @@ __global__ void __launch_bounds__(512, 1)
           for (int c4 = 0; c4 < 8; ++c4) {
             const float4 d4 = lds_f4(dl + 32 * hf + 4 * c4);
             const uint32_t w0 = pw[16 * hf + 2 * c4], w1 = pw[16 * hf + 2 * c4 + 1];
-            const float p0 = __uint_as_float(w0 << 16), p1 = __uint_as_float(w0 & 0xffff0000u);
-            const float p2 = __uint_as_float(w1 << 16), p3 = __uint_as_float(w1 & 0xffff0000u);
-            dsw[2 * c4] = pack_bf16x2(p0 * (__uint_as_float(dr[4 * c4]) - d4.x),
-                                      p1 * (__uint_as_float(dr[4 * c4 + 1]) - d4.y));
-            dsw[2 * c4 + 1] = pack_bf16x2(p2 * (__uint_as_float(dr[4 * c4 + 2]) - d4.z),
-                                          p3 * (__uint_as_float(dr[4 * c4 + 3]) - d4.w));
+            const uint64_t dp01 = f2_add(f2_pack_u(dr[4 * c4], dr[4 * c4 + 1]), f2_pack(-d4.x, -d4.y));
+            const uint64_t dp23 = f2_add(f2_pack_u(dr[4 * c4 + 2], dr[4 * c4 + 3]), f2_pack(-d4.z, -d4.w));
+            float a0, a1, a2, a3;
+            f2_split(f2_mul(f2_from_bf16x2(w0), dp01), a0, a1);
+            f2_split(f2_mul(f2_from_bf16x2(w1), dp23), a2, a3);
+            dsw[2 * c4] = pack_bf16x2(a0, a1);
+            dsw[2 * c4 + 1] = pack_bf16x2(a2, a3);
           }
           tmem_st16(tDP + 16 * hf, dsw);
           if (DS) {
@@ -450,20 +465,18 @@ __global__ void __launch_bounds__(512, 1)
       tc_fence_after();
     }
     // ------------------------------------------------------------ epilogue
-    // the softmax warpgroups store dV (half of the columns each), the dS
-    // warpgroup dK (times the softmax scale); a tile no query sees gets zeros
-    const int wg = softmax_wg ? 0 : 1;
-    const bool want = wg == 0 ? (p.wrt & 4u) != 0 : (p.wrt & 2u) != 0;
-    const int c_lo = wg == 0 ? sg * (DP / 64) : 0, c_hi = wg == 0 ? (sg + 1) * (DP / 64) : DP / 32;
+    // group 0 stores dV, group 1 dK (times the softmax scale); a tile no
+    // query sees gets zeros
+    const bool want = sg == 0 ? (p.wrt & 4u) != 0 : (p.wrt & 2u) != 0;
     if (want && (ok || n == 0)) {
-      const int64_t* so = wg == 0 ? p.s_dv : p.s_dk;
+      const int64_t* so = sg == 0 ? p.s_dv : p.s_dk;
       const int64_t roff = static_cast<int64_t>(b) * so[2] + static_cast<int64_t>(h) * so[1] +
                            static_cast<int64_t>(key) * so[0];
-      void* out = wg == 0 ? p.dv : p.dk;
-      const float f = wg == 0 ? 1.f : p.scale;
-      const uint32_t tacc = (wg == 0 ? t_dv : t_dk) + lane_addr;
+      void* out = sg == 0 ? p.dv : p.dk;
+      const float f = sg == 0 ? 1.f : p.scale;
+      const uint32_t tacc = (sg == 0 ? t_dv : t_dk) + lane_addr;
 #pragma unroll 1
-      for (int cc = c_lo; cc < c_hi && cc * 32 < p.D; ++cc) {
+      for (int cc = 0; cc < DP / 32 && cc * 32 < p.D; ++cc) {
         uint32_t r[32];
         if (n > 0) {
           tmem_ld32(tacc + cc * 32, r);
@@ -492,7 +505,7 @@ cudaError_t launch_t(const DenseMaps& m, const DenseParams& p, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(p.B * p.H, cdiv(p.Sk, L::BK));
-  kern<<<grid, 512, smem, s>>>(m.q64, m.k128, m.v128, m.dy64, m.bias64, p);
+  kern<<<grid, 384, smem, s>>>(m.q64, m.k128, m.v128, m.dy64, m.bias64, p);
   return cudaGetLastError();
 }
 

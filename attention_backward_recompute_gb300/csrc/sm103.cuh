@@ -104,6 +104,48 @@ __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, c
   return __all_sync(0xffffffffu, ok);
 }
 
+// Non-blocking test (mbarrier.test_wait never suspends the thread, unlike
+// try_wait, which may park it until the phase completes or a time limit).
+__device__ __forceinline__ bool mbar_test_now(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Non-blocking warp-collective test: true when every lane sees the phase
+// complete (completion is monotonic, so a false is retried by the caller).
+// Used by a warp that polls several barriers, so that one incomplete phase
+// does not hold it while another is ready.
+__device__ __forceinline__ bool mbar_test_warp(uint64_t* bar, uint32_t parity) {
+  return __all_sync(0xffffffffu, mbar_test_now(bar, parity));
+}
+
+// Bounded polling loop state for a warp that waits on several barriers at
+// once: check() returns false (warp-uniformly) once the CTA is aborting or
+// ATTN_WAIT_TIMEOUT_NS has passed since the loop began (raising
+// DEV_ERR_TIMEOUT in the second case).
+struct PollBudget {
+  uint64_t t0;
+  uint32_t n;
+  __device__ __forceinline__ PollBudget() : t0(global_timer_ns()), n(0) {}
+  __device__ __forceinline__ bool check(const Abort& a) {
+    if (__any_sync(0xffffffffu, *a.flag != 0)) return false;
+    if ((++n & 63u) == 0u) {
+      if (__any_sync(0xffffffffu, global_timer_ns() - t0 > ATTN_WAIT_TIMEOUT_NS)) {
+        raise_error(a, DEV_ERR_TIMEOUT);
+        return false;
+      }
+    }
+    return true;
+  }
+};
+
 // ----------------------------------------------------------------------------
 // TMA (tiled bulk tensor copies, global -> shared)
 // ----------------------------------------------------------------------------
