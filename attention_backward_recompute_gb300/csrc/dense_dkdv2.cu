@@ -161,6 +161,44 @@ __device__ __forceinline__ void p_row(uint32_t tS, const float* st, const uint8_
   }
 }
 
+// One work item = one (batch*head, 128-key tile): the visible 64-query tiles
+// [i_lo, i_lo + n) of that key tile.
+struct Item {
+  int bh, kt, i_lo, n;
+};
+
+__device__ __forceinline__ Item item_at(const DenseParams& p, int idx) {
+  const int BH = p.B * p.H;
+  Item it;
+  it.kt = idx / BH;
+  it.bh = idx - it.kt * BH;
+  const int k0 = it.kt * 128;
+  int lo, hi;
+  query_tile_range(p, k0, imin(k0 + 127, p.Sk - 1), 64, &lo, &hi);
+  it.i_lo = lo;
+  it.n = hi - lo;
+  return it;
+}
+
+// Items of this CTA: item indices run key tile major (longest first under a
+// causal mask); round r gives CTA c the index r*G + c, or r*G + G-1-c in odd
+// rounds (a snake order that evens out the per-CTA totals).
+struct ItemIter {
+  int r, c, G, total;
+  __device__ __forceinline__ bool next(int* idx) {
+    while (true) {
+      const int base = r * G;
+      if (base >= total) return false;
+      const int i = base + ((r & 1) ? G - 1 - c : c);
+      ++r;
+      if (i < total) {
+        *idx = i;
+        return true;
+      }
+    }
+  }
+};
+
 template <int DP, bool HAS_BIAS, bool ELEM, bool DS>
 __global__ void __launch_bounds__(384, 1)
     dkdv2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -169,24 +207,24 @@ __global__ void __launch_bounds__(384, 1)
   using L = Dkdv2Layout<DP>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t bar_kv, bar_full[kStages], bar_empty[kStages], bar_s_full[2], bar_dp_full[2], bar_p_full[2],
-      bar_ds_full[2], bar_acc;
+  // bar_kv: K/V of a live item loaded; bar_kv_free: every S/dP product of
+  // the item done (K/V slots free); bar_acc: every product of the item done;
+  // bar_acc_free: the epilogue has read dV and dK out of tensor memory.
+  // Their phases count live items (items with at least one query tile).
+  __shared__ uint64_t bar_kv, bar_kv_free, bar_full[kStages], bar_empty[kStages], bar_s_full[2], bar_dp_full[2],
+      bar_p_full[2], bar_ds_full[2], bar_acc, bar_acc_free;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bh = blockIdx.x;
-  const int b = bh / p.H, h = bh - b * p.H;
-  const int k0 = blockIdx.y * L::BK;
-  const int k1 = imin(k0 + L::BK - 1, p.Sk - 1);
-  int i_lo, i_hi;
-  query_tile_range(p, k0, k1, L::BQ, &i_lo, &i_hi);
-  const int n = i_hi - i_lo;
+  const int nkt = cdiv(p.Sk, L::BK);
+  const int total = p.B * p.H * nkt;
   const Abort ab{&abort_flag, p.err};
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(&bar_kv, 1);
+    mbar_init(&bar_kv_free, 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bar_full[s], 2);  // TMA bytes + statistics written
       mbar_init(&bar_empty[s], 1);
@@ -198,6 +236,7 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&bar_ds_full[s], 4);
     }
     mbar_init(&bar_acc, 1);
+    mbar_init(&bar_acc_free, 8);
     mbar_fence_init();
   }
   if (warp == 1) {
@@ -209,8 +248,9 @@ __global__ void __launch_bounds__(384, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
   const uint32_t t_dv = tmem, t_dk = tmem + DP;
+  ItemIter iter{0, static_cast<int>(blockIdx.x), static_cast<int>(gridDim.x), total};
 
-  if (n > 0 && warp == 0) {
+  if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_map(&tm_q);
@@ -218,17 +258,12 @@ __global__ void __launch_bounds__(384, 1)
       tma_prefetch_map(&tm_v);
       tma_prefetch_map(&tm_dy);
       if (HAS_BIAS) tma_prefetch_map(&tm_bias);
-      mbar_arrive_expect_tx(&bar_kv, 2 * L::KV);
-      for (int c = 0; c < L::NCH; ++c) {
-        tma_load_4d(sm + L::K_OFF + c * (L::BK * 128), &tm_k, &bar_kv, c * 64, k0, h, b);
-        tma_load_4d(sm + L::V_OFF + c * (L::BK * 128), &tm_v, &bar_kv, c * 64, k0, h, b);
-      }
     }
     // row statistics (-L2, delta, pm) of rows lane and lane + 32 of a tile,
-    // loaded one tile ahead so their latency overlaps the wait for a stage
+    // loaded one tile ahead within an item so their latency overlaps the
+    // wait for a stage
     float pre[6];
-    auto load_stats = [&](int t) {
-      const int qb0 = (i_lo + t) * L::BQ;
+    auto load_stats = [&](int bh, int qb0) {
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
         const int q = qb0 + lane + 32 * i;
@@ -239,122 +274,148 @@ __global__ void __launch_bounds__(384, 1)
         pre[3 * i + 2] = (in && p.has_custom) ? p.pm[idx] : 0.f;
       }
     };
-    load_stats(0);
     int last_use[kStages];
     for (int i = 0; i < kStages; ++i) last_use[i] = -1;
     bool ok = true;
-    for (int t = 0; t < n && ok; ++t) {
-      const int s = t % kStages;
-      if (t >= kStages) ok = mbar_wait(&bar_empty[s], ((t / kStages) - 1) & 1, ab);
-      if (!ok) break;
-      const int q0 = (i_lo + t) * L::BQ;
+    int g0 = 0, lv = 0, idx;
+    while (ok && iter.next(&idx)) {
+      const Item it = item_at(p, idx);
+      if (it.n == 0) continue;
+      const int b = it.bh / p.H, h = it.bh - b * p.H, k0 = it.kt * L::BK;
+      if (lv > 0 && !(ok = mbar_wait(&bar_kv_free, (lv - 1) & 1, ab))) break;
       if (lane == 0) {
-        mbar_arrive_expect_tx(&bar_full[s], 2 * L::QT + (HAS_BIAS ? L::BIAS : 0));
+        mbar_arrive_expect_tx(&bar_kv, 2 * L::KV);
         for (int c = 0; c < L::NCH; ++c) {
-          tma_load_4d(sm + L::Q_OFF + s * L::QT + c * (L::BQ * 128), &tm_q, &bar_full[s], c * 64, q0, h, b);
-          tma_load_4d(sm + L::DY_OFF + s * L::QT + c * (L::BQ * 128), &tm_dy, &bar_full[s], c * 64, q0, h, b);
+          tma_load_4d(sm + L::K_OFF + c * (L::BK * 128), &tm_k, &bar_kv, c * 64, k0, h, b);
+          tma_load_4d(sm + L::V_OFF + c * (L::BK * 128), &tm_v, &bar_kv, c * 64, k0, h, b);
         }
-        if (HAS_BIAS) {
-          uint8_t* bs = sm + L::BIAS_OFF + s * L::BIAS;
-          tma_load_4d(bs, &tm_bias, &bar_full[s], k0, q0, h, b);
-          tma_load_4d(bs + L::BQ * 128, &tm_bias, &bar_full[s], k0 + 64, q0, h, b);
-        }
-        if (t + kStages < n) {  // the tile that will reuse this stage, into L2
-          const int qn = (i_lo + t + kStages) * L::BQ;
+      }
+      load_stats(it.bh, it.i_lo * L::BQ);
+      for (int t = 0; t < it.n && ok; ++t) {
+        const int g = g0 + t, s = g % kStages;
+        if (g >= kStages && !(ok = mbar_wait(&bar_empty[s], ((g / kStages) - 1) & 1, ab))) break;
+        const int q0 = (it.i_lo + t) * L::BQ;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bar_full[s], 2 * L::QT + (HAS_BIAS ? L::BIAS : 0));
           for (int c = 0; c < L::NCH; ++c) {
-            tma_prefetch_l2_4d(&tm_q, c * 64, qn, h, b);
-            tma_prefetch_l2_4d(&tm_dy, c * 64, qn, h, b);
+            tma_load_4d(sm + L::Q_OFF + s * L::QT + c * (L::BQ * 128), &tm_q, &bar_full[s], c * 64, q0, h, b);
+            tma_load_4d(sm + L::DY_OFF + s * L::QT + c * (L::BQ * 128), &tm_dy, &bar_full[s], c * 64, q0, h, b);
           }
           if (HAS_BIAS) {
-            tma_prefetch_l2_4d(&tm_bias, k0, qn, h, b);
-            tma_prefetch_l2_4d(&tm_bias, k0 + 64, qn, h, b);
+            uint8_t* bs = sm + L::BIAS_OFF + s * L::BIAS;
+            tma_load_4d(bs, &tm_bias, &bar_full[s], k0, q0, h, b);
+            tma_load_4d(bs + L::BQ * 128, &tm_bias, &bar_full[s], k0 + 64, q0, h, b);
+          }
+          if (t + kStages < it.n) {  // the tile that will reuse this stage, into L2
+            const int qn = (it.i_lo + t + kStages) * L::BQ;
+            for (int c = 0; c < L::NCH; ++c) {
+              tma_prefetch_l2_4d(&tm_q, c * 64, qn, h, b);
+              tma_prefetch_l2_4d(&tm_dy, c * 64, qn, h, b);
+            }
+            if (HAS_BIAS) {
+              tma_prefetch_l2_4d(&tm_bias, k0, qn, h, b);
+              tma_prefetch_l2_4d(&tm_bias, k0 + 64, qn, h, b);
+            }
           }
         }
-      }
-      float* st = reinterpret_cast<float*>(sm + L::ST_OFF) + s * 3 * L::BQ;
+        float* st = reinterpret_cast<float*>(sm + L::ST_OFF) + s * 3 * L::BQ;
 #pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        st[lane + 32 * i] = pre[3 * i];
-        st[L::BQ + lane + 32 * i] = pre[3 * i + 1];
-        st[2 * L::BQ + lane + 32 * i] = pre[3 * i + 2];
+        for (int i = 0; i < 2; ++i) {
+          st[lane + 32 * i] = pre[3 * i];
+          st[L::BQ + lane + 32 * i] = pre[3 * i + 1];
+          st[2 * L::BQ + lane + 32 * i] = pre[3 * i + 2];
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_full[s]);
+        last_use[s] = g;
+        if (t + 1 < it.n) load_stats(it.bh, q0 + L::BQ);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar_full[s]);
-      last_use[s] = t;
-      if (t + 1 < n) load_stats(t + 1);
+      g0 += it.n;
+      ++lv;
     }
     if (lane == 0) {
       for (int s = 0; s < kStages; ++s)
         if (last_use[s] >= 0) drain_wait(&bar_full[s], (last_use[s] / kStages) & 1);
-      drain_wait(&bar_kv, 0);
+      if (lv > 0) drain_wait(&bar_kv, (lv - 1) & 1);
     }
-  } else if (n > 0 && warp == 1) {
+  } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     // the whole warp runs this role (warp-uniform); elected lanes issue
-    {
-      constexpr uint32_t id_s = idesc_bf16(128, 64, false, false);
-      constexpr uint32_t id_acc = idesc_bf16(128, DP, false, true);
-      // descriptors built once; k-slices and stages are constant offsets
-      const uint64_t dK = sdesc_sw128(smem_addr(sm + L::K_OFF), 16, 1024);
-      const uint64_t dV = sdesc_sw128(smem_addr(sm + L::V_OFF), 16, 1024);
-      const uint64_t dQ0 = sdesc_sw128(smem_addr(sm + L::Q_OFF), 16, 1024);
-      const uint64_t dDY0 = sdesc_sw128(smem_addr(sm + L::DY_OFF), 16, 1024);
-      const uint64_t dQm0 = sdesc_sw128(smem_addr(sm + L::Q_OFF), L::BQ * 128, 1024);    // MN-major
-      const uint64_t dDYm0 = sdesc_sw128(smem_addr(sm + L::DY_OFF), L::BQ * 128, 1024);  // MN-major
-      // D[128 x 64] = A[128 x DP] * B[64 x DP]^T, both from shared memory, K-major
-      auto issue_xt = [&](uint32_t d, uint64_t a, uint64_t bq) {
-        mma_ss_w<false>(d, a, bq, id_s);
+    constexpr uint32_t id_s = idesc_bf16(128, 64, false, false);
+    constexpr uint32_t id_acc = idesc_bf16(128, DP, false, true);
+    // descriptors built once; k-slices and stages are constant offsets
+    const uint64_t dK = sdesc_sw128(smem_addr(sm + L::K_OFF), 16, 1024);
+    const uint64_t dV = sdesc_sw128(smem_addr(sm + L::V_OFF), 16, 1024);
+    const uint64_t dQ0 = sdesc_sw128(smem_addr(sm + L::Q_OFF), 16, 1024);
+    const uint64_t dDY0 = sdesc_sw128(smem_addr(sm + L::DY_OFF), 16, 1024);
+    const uint64_t dQm0 = sdesc_sw128(smem_addr(sm + L::Q_OFF), L::BQ * 128, 1024);    // MN-major
+    const uint64_t dDYm0 = sdesc_sw128(smem_addr(sm + L::DY_OFF), L::BQ * 128, 1024);  // MN-major
+    // D[128 x 64] = A[128 x DP] * B[64 x DP]^T, both from shared memory, K-major
+    auto issue_xt = [&](uint32_t d, uint64_t a, uint64_t bq) {
+      mma_ss_w<false>(d, a, bq, id_s);
 #pragma unroll
-        for (int kk = 1; kk < DP / 16; ++kk) {
-          const int c = kk >> 2, o = (kk & 3) * 32;
-          mma_ss_w<true>(d, sdesc_add(a, c * (L::BK * 128) + o), sdesc_add(bq, c * (L::BQ * 128) + o), id_s);
-        }
-      };
-      // D[128 x DP] (+)= A[128 x 64] (tensor memory, bf16 pairs) * B[64 x DP] (MN-major)
-      auto issue_acc = [&](uint32_t d, uint32_t a_tmem, uint64_t bm, bool first) {
-        if (first)
-          mma_ts_w<false>(d, a_tmem, bm, id_acc);
-        else
-          mma_ts_w<true>(d, a_tmem, bm, id_acc);
-#pragma unroll
-        for (int kk = 1; kk < L::BQ / 16; ++kk) mma_ts_w<true>(d, a_tmem + kk * 8, sdesc_add(bm, kk * 16 * 128), id_acc);
-      };
-      auto issue_s = [&](int t) {  // S(t) into buffer t % 2
-        issue_xt(tmem + L::T_S + (t & 1) * 64, dK, sdesc_add(dQ0, (t % kStages) * L::QT));
-        mma_commit_w(&bar_s_full[t & 1]);
-      };
-      auto issue_dp = [&](int t) {  // dP(t) into buffer t % 2
-        issue_xt(tmem + L::T_DP + (t & 1) * 64, dV, sdesc_add(dDY0, (t % kStages) * L::QT));
-        mma_commit_w(&bar_dp_full[t & 1]);
-      };
-      bool ok = mbar_wait_warp(&bar_kv, 0, ab);
-      for (int t = 0; t < 2 && t < n && ok; ++t) {
-        if (!(ok = mbar_wait_warp(&bar_full[t], 0, ab))) break;
-        tc_fence_after();
-        issue_s(t);
-        issue_dp(t);
+      for (int kk = 1; kk < DP / 16; ++kk) {
+        const int c = kk >> 2, o = (kk & 3) * 32;
+        mma_ss_w<true>(d, sdesc_add(a, c * (L::BK * 128) + o), sdesc_add(bq, c * (L::BQ * 128) + o), id_s);
       }
-      // Per tile t: dV(t) once P(t) is in; then S(t+2) and dK(t) in whichever
-      // order their inputs arrive; then dP(t+2).  S(t+2) overwrites P(t),
-      // which dV(t) (earlier in the same pipe) consumes, and S(t), which the
-      // group finished reading before it handed P(t) over; dP(t+2) overwrites
-      // dS(t) and dP(t), read by dK(t) and by the group before dS(t) was
-      // handed over.  Issuing dK(t) as soon as dS(t) is ready releases tile
-      // t's stage early: the copies of tile t+3 wait on that release.
+    };
+    // D[128 x DP] (+)= A[128 x 64] (tensor memory, bf16 pairs) * B[64 x DP] (MN-major)
+    auto issue_acc = [&](uint32_t d, uint32_t a_tmem, uint64_t bm, bool first) {
+      if (first)
+        mma_ts_w<false>(d, a_tmem, bm, id_acc);
+      else
+        mma_ts_w<true>(d, a_tmem, bm, id_acc);
+#pragma unroll
+      for (int kk = 1; kk < L::BQ / 16; ++kk) mma_ts_w<true>(d, a_tmem + kk * 8, sdesc_add(bm, kk * 16 * 128), id_acc);
+    };
+    auto issue_s = [&](int g) {  // S(g) into buffer g % 2
+      issue_xt(tmem + L::T_S + (g & 1) * 64, dK, sdesc_add(dQ0, (g % kStages) * L::QT));
+      mma_commit_w(&bar_s_full[g & 1]);
+    };
+    auto issue_dp = [&](int g) {  // dP(g) into buffer g % 2
+      issue_xt(tmem + L::T_DP + (g & 1) * 64, dV, sdesc_add(dDY0, (g % kStages) * L::QT));
+      mma_commit_w(&bar_dp_full[g & 1]);
+    };
+    bool ok = true;
+    int g0 = 0, lv = 0, idx;
+    while (ok && iter.next(&idx)) {
+      const Item it = item_at(p, idx);
+      const int n = it.n;
+      if (n == 0) continue;
+      if (!(ok = mbar_wait_warp(&bar_kv, lv & 1, ab))) break;
+      // the first score and dP tiles of this item go while the epilogue of
+      // the previous item still reads dV and dK
+      for (int t = 0; t < 2 && t < n && ok; ++t) {
+        if (!(ok = mbar_wait_warp(&bar_full[(g0 + t) % kStages], ((g0 + t) / kStages) & 1, ab))) break;
+        tc_fence_after();
+        issue_s(g0 + t);
+        issue_dp(g0 + t);
+      }
+      if (!ok) break;
+      if (n <= 2) mma_commit_w(&bar_kv_free);
+      if (lv > 0 && !(ok = mbar_wait_warp(&bar_acc_free, (lv - 1) & 1, ab))) break;
+      tc_fence_after();
+      // Per tile g: dV(g) once P(g) is in; then S(g+2) and dK(g) in whichever
+      // order their inputs arrive; then dP(g+2).  S(g+2) overwrites P(g),
+      // which dV(g) (earlier in the same pipe) consumes, and S(g), which the
+      // group finished reading before it handed P(g) over; dP(g+2)
+      // overwrites dS(g) and dP(g), read by dK(g) and by the group before
+      // dS(g) was handed over.  Issuing dK(g) as soon as dS(g) is ready
+      // releases tile g's stage early: the copies of tile g+3 wait on it.
       for (int t = 0; t < n && ok; ++t) {
-        const int s = t % kStages, bb = t & 1;
-        if (!(ok = mbar_wait_warp(&bar_p_full[bb], (t >> 1) & 1, ab))) break;
+        const int g = g0 + t, s = g % kStages, bb = g & 1;
+        if (!(ok = mbar_wait_warp(&bar_p_full[bb], (g >> 1) & 1, ab))) break;
         tc_fence_after();
         issue_acc(t_dv, tmem + L::T_S + bb * 64, sdesc_add(dDYm0, s * L::QT), t == 0);
         bool s_next = t + 2 < n, k_now = true;
         PollBudget pb;
         while (s_next || k_now) {
-          if (s_next && mbar_test_warp(&bar_full[(t + 2) % kStages], ((t + 2) / kStages) & 1)) {
+          if (s_next && mbar_test_warp(&bar_full[(g + 2) % kStages], ((g + 2) / kStages) & 1)) {
             tc_fence_after();
-            issue_s(t + 2);
+            issue_s(g + 2);
             s_next = false;
           }
-          if (k_now && mbar_test_warp(&bar_ds_full[bb], (t >> 1) & 1)) {
+          if (k_now && mbar_test_warp(&bar_ds_full[bb], (g >> 1) & 1)) {
             tc_fence_after();
             issue_acc(t_dk, tmem + L::T_DP + bb * 64, sdesc_add(dQm0, s * L::QT), t == 0);
             mma_commit_w(&bar_empty[s]);
@@ -363,112 +424,125 @@ __global__ void __launch_bounds__(384, 1)
           if ((s_next || k_now) && !(ok = pb.check(ab))) break;
         }
         if (!ok) break;
-        if (t + 2 < n) issue_dp(t + 2);
+        if (t + 2 < n) {
+          issue_dp(g + 2);
+          if (t + 3 == n) mma_commit_w(&bar_kv_free);  // the item's last S and dP are issued
+        }
       }
+      if (!ok) break;
       mma_commit_w(&bar_acc);
-      drain_wait(&bar_acc, 0);
+      g0 += n;
+      ++lv;
     }
+    // the last commits arrive before the CTA leaves
+    if (lv > 0) drain_wait(&bar_acc, (lv - 1) & 1);
     __syncwarp();
   } else if (warp >= 4) {
     const int sg = (warp - 4) >> 2;  // compute group: tiles (and S/dP buffers) of parity sg
     const int lg = warp & 3;
     const int row = lg * 32 + lane;  // key row inside the tile == TMEM lane
-    const int key = k0 + row;
     const uint32_t lane_addr = static_cast<uint32_t>(lg * 32) << 16;
-    bool ok = n > 0;
-    if (n > 0) {
-      bool kmasked = false;
-      if (p.has_key_mask && key < p.Sk) kmasked = p.key_mask[static_cast<size_t>(b) * p.Sk + key] < p.mask_thr;
-      const int half = row >> 6, kc = (row & 63) >> 3, kb = (row & 7) * 2;
-      // queries that see this key: [qa, qb] (causal: q + q_off >= key;
-      // window: q + q_off - window <= key; q < Sq; none when key >= Sk)
-      int qa = -(1 << 30), qb = p.Sq - 1;
-      if (p.causal) qa = key - p.q_off;
-      if (p.window >= 0) qb = imin(qb, key + p.window - p.q_off);
-      if (key >= p.Sk) qa = 1 << 30, qb = -(1 << 30);
-      // Each group waits every phase of its own S and dP buffers.  Of the
-      // stage barrier it skips the phases of the other group's tiles; when it
-      // waits for tile t, the phase of tile t - 3 (same stage, other parity)
-      // has completed, since the tensor core issued S(t - 2) after it.
-      for (int t = sg; t < n && ok; t += 2) {
-        const int s = t % kStages, bb = t & 1;
-        const int q0 = (i_lo + t) * L::BQ;
-        uint2 eb = make_uint2(0u, 0u);  // per-element mask: this key's bits of the tile's 64 queries
-        if (ELEM && key < p.Sk)
-          eb = *reinterpret_cast<const uint2*>(p.elem_cols + (static_cast<size_t>(bh) * p.Sk + key) * p.ew_k +
-                                               (q0 >> 5));
-        if (!(ok = mbar_wait_warp(&bar_full[s], (t / kStages) & 1, ab))) break;
-        if (!(ok = mbar_wait_warp(&bar_s_full[bb], (t >> 1) & 1, ab))) break;
-        tc_fence_after();
-        // ---------------------------------------------------- S^T -> P^T
-        const uint32_t tS = tmem + L::T_S + bb * 64 + lane_addr;
-        const float* st = reinterpret_cast<const float*>(sm + L::ST_OFF) + s * 3 * L::BQ;
-        const uint8_t* bias_row = sm + L::BIAS_OFF + s * L::BIAS + half * (L::BQ * 128) + kb;
-        const bool full = tile_fully_visible(p, q0, q0 + L::BQ - 1, k0, k0 + L::BK - 1);
-        const int lo = qa - q0, hi = qb - q0;
-        uint32_t pw[32];
-        if (full)
-          p_row<HAS_BIAS, false, ELEM>(tS, st, bias_row, kc, p.scale_log2, lo, hi, kmasked, eb, pw);
-        else
-          p_row<HAS_BIAS, true, ELEM>(tS, st, bias_row, kc, p.scale_log2, lo, hi, kmasked, eb, pw);
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bar_p_full[bb]);
-        // ---------------------------------------------------- dP^T, P^T -> dS^T
-        if (!(ok = mbar_wait_warp(&bar_dp_full[bb], (t >> 1) & 1, ab))) break;
-        tc_fence_after();
-        const uint32_t tDP = tmem + L::T_DP + bb * 64 + lane_addr;
-        const float* dl = st + L::BQ;
-        // stored dS of tile (key tile, query tile i_lo + t): chunk c of this
-        // key at c * 2048 + row * 16
-        uint4* ds_row = nullptr;
-        if (DS) {
-          const size_t blob = (static_cast<size_t>(bh) * gridDim.y + blockIdx.y) * cdiv(p.Sq, L::BQ) + i_lo + t;
-          ds_row = reinterpret_cast<uint4*>(p.ds_store + blob * (L::BK * 128)) + row;
-        }
-        // two halves of 32 queries: half hf reads dP columns [32hf, 32hf+32)
-        // and writes dS^T (bf16 pairs) to columns [16hf, 16hf+16), which half
-        // 0 has already read
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          uint32_t dr[32], dsw[16];
-          tmem_ld32(tDP + 32 * hf, dr);
-          tmem_ld_wait();
-#pragma unroll
-          for (int c4 = 0; c4 < 8; ++c4) {
-            const float4 d4 = lds_f4(dl + 32 * hf + 4 * c4);
-            const uint32_t w0 = pw[16 * hf + 2 * c4], w1 = pw[16 * hf + 2 * c4 + 1];
-            const uint64_t dp01 = f2_add(f2_pack_u(dr[4 * c4], dr[4 * c4 + 1]), f2_pack(-d4.x, -d4.y));
-            const uint64_t dp23 = f2_add(f2_pack_u(dr[4 * c4 + 2], dr[4 * c4 + 3]), f2_pack(-d4.z, -d4.w));
-            float a0, a1, a2, a3;
-            f2_split(f2_mul(f2_from_bf16x2(w0), dp01), a0, a1);
-            f2_split(f2_mul(f2_from_bf16x2(w1), dp23), a2, a3);
-            dsw[2 * c4] = pack_bf16x2(a0, a1);
-            dsw[2 * c4 + 1] = pack_bf16x2(a2, a3);
-          }
-          tmem_st16(tDP + 16 * hf, dsw);
+    const int half = row >> 6, kc = (row & 63) >> 3, kb = (row & 7) * 2;
+    bool ok = true;
+    int g0 = 0, lv = 0, idx;
+    while (ok && iter.next(&idx)) {
+      const Item it = item_at(p, idx);
+      const int b = it.bh / p.H, h = it.bh - b * p.H, k0 = it.kt * L::BK;
+      const int key = k0 + row;
+      const int n = it.n;
+      if (n > 0) {
+        bool kmasked = false;
+        if (p.has_key_mask && key < p.Sk) kmasked = p.key_mask[static_cast<size_t>(b) * p.Sk + key] < p.mask_thr;
+        // queries that see this key: [qa, qb] (causal: q + q_off >= key;
+        // window: q + q_off - window <= key; q < Sq; none when key >= Sk)
+        int qa = -(1 << 30), qb = p.Sq - 1;
+        if (p.causal) qa = key - p.q_off;
+        if (p.window >= 0) qb = imin(qb, key + p.window - p.q_off);
+        if (key >= p.Sk) qa = 1 << 30, qb = -(1 << 30);
+        // Each group waits every phase of its own S and dP buffers.  Of the
+        // stage barrier it skips the phases of the other group's tiles; when
+        // it waits for tile g, the phase of tile g - 3 (same stage, other
+        // parity) has completed, since the tensor core issued S(g - 2) after
+        // it.
+        for (int t = ((g0 & 1) == sg) ? 0 : 1; t < n && ok; t += 2) {
+          const int g = g0 + t, s = g % kStages, bb = g & 1;
+          const int q0 = (it.i_lo + t) * L::BQ;
+          uint2 eb = make_uint2(0u, 0u);  // per-element mask: this key's bits of the tile's 64 queries
+          if (ELEM && key < p.Sk)
+            eb = *reinterpret_cast<const uint2*>(p.elem_cols + (static_cast<size_t>(it.bh) * p.Sk + key) * p.ew_k +
+                                                 (q0 >> 5));
+          if (!(ok = mbar_wait_warp(&bar_full[s], (g / kStages) & 1, ab))) break;
+          if (!(ok = mbar_wait_warp(&bar_s_full[bb], (g >> 1) & 1, ab))) break;
+          tc_fence_after();
+          // ---------------------------------------------------- S^T -> P^T
+          const uint32_t tS = tmem + L::T_S + bb * 64 + lane_addr;
+          const float* st = reinterpret_cast<const float*>(sm + L::ST_OFF) + s * 3 * L::BQ;
+          const uint8_t* bias_row = sm + L::BIAS_OFF + s * L::BIAS + half * (L::BQ * 128) + kb;
+          const bool full = tile_fully_visible(p, q0, q0 + L::BQ - 1, k0, k0 + L::BK - 1);
+          const int lo = qa - q0, hi = qb - q0;
+          uint32_t pw[32];
+          if (full)
+            p_row<HAS_BIAS, false, ELEM>(tS, st, bias_row, kc, p.scale_log2, lo, hi, kmasked, eb, pw);
+          else
+            p_row<HAS_BIAS, true, ELEM>(tS, st, bias_row, kc, p.scale_log2, lo, hi, kmasked, eb, pw);
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bar_p_full[bb]);
+          // ---------------------------------------------------- dP^T, P^T -> dS^T
+          if (!(ok = mbar_wait_warp(&bar_dp_full[bb], (g >> 1) & 1, ab))) break;
+          tc_fence_after();
+          const uint32_t tDP = tmem + L::T_DP + bb * 64 + lane_addr;
+          const float* dl = st + L::BQ;
+          // stored dS of tile (key tile, query tile i_lo + t): chunk c of this
+          // key at c * 2048 + row * 16
+          uint4* ds_row = nullptr;
           if (DS) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              ds_row[(4 * hf + j) * L::BK] = make_uint4(dsw[4 * j], dsw[4 * j + 1], dsw[4 * j + 2], dsw[4 * j + 3]);
+            const size_t blob = (static_cast<size_t>(it.bh) * nkt + it.kt) * cdiv(p.Sq, L::BQ) + it.i_lo + t;
+            ds_row = reinterpret_cast<uint4*>(p.ds_store + blob * (L::BK * 128)) + row;
           }
+          // two halves of 32 queries: half hf reads dP columns [32hf, 32hf+32)
+          // and writes dS^T (bf16 pairs) to columns [16hf, 16hf+16), which
+          // half 0 has already read
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            uint32_t dr[32], dsw[16];
+            tmem_ld32(tDP + 32 * hf, dr);
+            tmem_ld_wait();
+#pragma unroll
+            for (int c4 = 0; c4 < 8; ++c4) {
+              const float4 d4 = lds_f4(dl + 32 * hf + 4 * c4);
+              const uint32_t w0 = pw[16 * hf + 2 * c4], w1 = pw[16 * hf + 2 * c4 + 1];
+              const uint64_t dp01 = f2_add(f2_pack_u(dr[4 * c4], dr[4 * c4 + 1]), f2_pack(-d4.x, -d4.y));
+              const uint64_t dp23 = f2_add(f2_pack_u(dr[4 * c4 + 2], dr[4 * c4 + 3]), f2_pack(-d4.z, -d4.w));
+              float a0, a1, a2, a3;
+              f2_split(f2_mul(f2_from_bf16x2(w0), dp01), a0, a1);
+              f2_split(f2_mul(f2_from_bf16x2(w1), dp23), a2, a3);
+              dsw[2 * c4] = pack_bf16x2(a0, a1);
+              dsw[2 * c4 + 1] = pack_bf16x2(a2, a3);
+            }
+            tmem_st16(tDP + 16 * hf, dsw);
+            if (DS) {
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                ds_row[(4 * hf + j) * L::BK] = make_uint4(dsw[4 * j], dsw[4 * j + 1], dsw[4 * j + 2], dsw[4 * j + 3]);
+            }
+          }
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bar_ds_full[bb]);
         }
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bar_ds_full[bb]);
+        if (!ok) break;
+        if (!(ok = mbar_wait_warp(&bar_acc, lv & 1, ab))) break;
+        tc_fence_after();
       }
-    }
-    if (n > 0) {
-      if (ok) ok = mbar_wait_warp(&bar_acc, 0, ab);
-      tc_fence_after();
-    }
-    // ------------------------------------------------------------ epilogue
-    // group 0 stores dV, group 1 dK (times the softmax scale); a tile no
-    // query sees gets zeros
-    const bool want = sg == 0 ? (p.wrt & 4u) != 0 : (p.wrt & 2u) != 0;
-    if (want && (ok || n == 0)) {
+      // -------------------------------------------------------- epilogue
+      // group 0 stores dV, group 1 dK (times the softmax scale); a key tile
+      // no query sees gets zeros.  Tensor memory is handed back (acc_free)
+      // as soon as the last chunk is in registers; the next item's products
+      // into dV and dK wait for that.
+      const bool want = sg == 0 ? (p.wrt & 4u) != 0 : (p.wrt & 2u) != 0;
       const int64_t* so = sg == 0 ? p.s_dv : p.s_dk;
       const int64_t roff = static_cast<int64_t>(b) * so[2] + static_cast<int64_t>(h) * so[1] +
                            static_cast<int64_t>(key) * so[0];
@@ -476,7 +550,7 @@ __global__ void __launch_bounds__(384, 1)
       const float f = sg == 0 ? 1.f : p.scale;
       const uint32_t tacc = (sg == 0 ? t_dv : t_dk) + lane_addr;
 #pragma unroll 1
-      for (int cc = 0; cc < DP / 32 && cc * 32 < p.D; ++cc) {
+      for (int cc = 0; want && cc < DP / 32 && cc * 32 < p.D; ++cc) {
         uint32_t r[32];
         if (n > 0) {
           tmem_ld32(tacc + cc * 32, r);
@@ -486,6 +560,13 @@ __global__ void __launch_bounds__(384, 1)
           for (int j = 0; j < 32; ++j) r[j] = 0u;
         }
         if (key < p.Sk) store_out32<false>(out, roff, cc * 32, p.D, r, f);
+      }
+      if (n > 0) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_acc_free);
+        g0 += n;
+        ++lv;
       }
     }
   }
@@ -504,7 +585,11 @@ cudaError_t launch_t(const DenseMaps& m, const DenseParams& p, cudaStream_t s) {
   const int smem = max(L::BYTES + 1024, kSmemOneCtaPerSm);  // all 512 TMEM columns: one CTA per SM
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  dim3 grid(p.B * p.H, cdiv(p.Sk, L::BK));
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  const int items = p.B * p.H * cdiv(p.Sk, L::BK);
+  const int grid = imin(items, imax(sms, 1));  // persistent: one CTA per SM
   kern<<<grid, 384, smem, s>>>(m.q64, m.k128, m.v128, m.dy64, m.bias64, p);
   return cudaGetLastError();
 }
