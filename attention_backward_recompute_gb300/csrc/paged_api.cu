@@ -207,6 +207,41 @@ ATTN_API attn_status_t attn_bwd_paged_compact(const attn_paged_desc* d, const vo
     const cudaError_t e = attn::launch_paged_listed(p, history_pages, num_history_pages, s);
     if (e != cudaSuccess) return api_fail(ATTN_ERR_CUDA, "paged launch failed: %s", cudaGetErrorString(e));
   }
+  if (mla && attn::mla_tc_supported(p)) {
+    // links, zeros for pages no link references, then two CTAs per 128-token
+    // block of every sequence (tcgen05); blocks whose shared pages carry many
+    // links go to the cluster-split kernel first
+    attn::PagedMlaMaps mm;
+    std::memset(&mm, 0, sizeof(mm));
+    const uint64_t slots = uint64_t(d->num_pages) * d->page_size;
+    const uint32_t G = uint32_t(p.G), RT = 32u / G;
+    bool enc = encode3d(&mm.k, k_pool, d->key_dim, d->kv_heads, slots, 64, 1, uint32_t(d->page_size)) &&
+               encode3d(&mm.kp, kp_pool, d->position_dim, d->kv_heads, slots, 64, 1, uint32_t(d->page_size));
+    if (d->num_queries > 0)
+      enc = enc && encode3d(&mm.q, q, d->key_dim, d->heads, d->num_queries, 64, G, RT) &&
+            encode3d(&mm.qp, qp, d->position_dim, d->heads, d->num_queries, 64, G, RT) &&
+            encode3d(&mm.dy, dy, d->value_dim, d->heads, d->num_queries, 64, G, RT);
+    else
+      mm.q = mm.qp = mm.dy = mm.k;
+    if (!enc) return api_fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+    const bool split = attn::mla_mma_supported(p);
+    if (!split) p.heavy = nullptr;
+    attn::timing_mark_begin(5, s);
+    cudaError_t e = attn::launch_paged_prep(p, s);
+    attn::timing_mark(s);
+    if (e == cudaSuccess) e = attn::launch_paged_zero_unlinked(p, compact ? history_pages : nullptr, num_history_pages, s);
+    attn::timing_mark(s);
+    if (split && e == cudaSuccess) e = attn::launch_paged_mla_plan(p, s);
+    if (split && e == cudaSuccess) e = attn::launch_paged_mla_tc_pair_heavy(p, s);
+    attn::timing_mark(s);
+    if (split && e == cudaSuccess) e = attn::launch_paged_mla_mma_split(mm, p, s);
+    attn::timing_mark(s);
+    if (e == cudaSuccess) e = attn::launch_paged_mla_tc(mm, p, s);
+    attn::timing_mark(s);
+    attn::timing_mark_end();
+    if (e != cudaSuccess) return api_fail(ATTN_ERR_CUDA, "paged launch failed: %s", cudaGetErrorString(e));
+    return api_ok();
+  }
   if (mla && attn::mla_mma_supported(p)) {
     // links, zeros for pages no link references, then one CTA per 64-token
     // block of every sequence (warp-level tensor path)

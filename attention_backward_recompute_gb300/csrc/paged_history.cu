@@ -29,6 +29,7 @@
 
 #include "paged_common.cuh"
 #include "paged_launch.h"
+#include "paged_pass.cuh"
 #include "sm103.cuh"
 
 namespace attn {
@@ -54,78 +55,6 @@ struct HistLayout {
   // TMEM: dV [0, DP), dK [DP, 2DP), S^T[2] and dP^T[2] 64 columns each
   static constexpr int T_S = 2 * DP, T_DP = 2 * DP + 128;
   static constexpr int TMEM_COLS = 512;
-};
-
-struct PageInfo {
-  int phys[8];    // physical page (or -1)
-  int off[8];     // first index of the page's link segment
-  int cnt[8];     // links of the page
-  int store[8];   // this CTA stores the page
-};
-
-// One pass = one (sequence, token mapping, live row range); the passes of a CTA
-// are enumerated identically by every role.  After the own pass come, for link
-// index li = 1, 2, ..., the li-th links of the pages this CTA stores; a run of
-// consecutive stored pages whose li-th links are consecutive logical pages of
-// one sequence (a shared prefix) is one pass with all their rows live.  Every
-// page still sees its links in increasing order.
-struct PassIter {
-  const PagedParams* p;
-  const PageInfo* pi;
-  int s0, tb;
-  int j, jn, li, lmax;               // j = -1: own pass; else pages [j, jn) at link index li
-  int seq, tbase, ra, rb, r_begin, r_end, tile, ntiles;
-
-  __device__ void load(int sq, int tbs, int a, int b, int rt) {
-    seq = sq;
-    tbase = tbs;
-    ra = a;
-    rb = b;
-    r_begin = row_begin_of(*p, sq);
-    r_end = row_end_of(*p, sq);
-    tile = 0;
-    ntiles = (r_end - r_begin + rt - 1) / rt;
-  }
-  // advance to the next pass that has at least one tile; false when done
-  __device__ bool next_pass(int rt) {
-    while (true) {
-      if (j < 0) {
-        j = 0;
-        li = 1;
-      } else {
-        j = jn;
-      }
-      while (true) {
-        while (j < 8 && !(pi->store[j] && li < pi->cnt[j])) ++j;
-        if (j < 8) break;
-        if (++li >= lmax) return false;
-        j = 0;
-      }
-      const int link = p->links[pi->off[j] + li];
-      const int s2 = link / p->max_pages, lp2 = link - s2 * p->max_pages;
-      jn = j + 1;
-      while (jn < 8 && pi->store[jn] && li < pi->cnt[jn] && lp2 + (jn - j) < p->max_pages &&
-             p->links[pi->off[jn] + li] == link + (jn - j))
-        ++jn;
-      load(s2, lp2 * p->page_size - 16 * j, 16 * j, 16 * jn, rt);
-      if (ntiles > 0) return true;
-    }
-  }
-  __device__ bool begin(int rt) {
-    j = -1;
-    jn = 0;
-    li = 0;
-    lmax = 0;
-    for (int k = 0; k < 8; ++k)
-      if (pi->store[k] && pi->cnt[k] > lmax) lmax = pi->cnt[k];
-    load(s0, tb * 128, 0, 128, rt);
-    if (ntiles > 0) return true;
-    return next_pass(rt);
-  }
-  __device__ bool advance(int rt) {
-    if (++tile < ntiles) return true;
-    return next_pass(rt);
-  }
 };
 
 __device__ __forceinline__ bool drain_wait(uint64_t* bar, uint32_t parity) {
@@ -225,27 +154,7 @@ __global__ void __launch_bounds__(512, 1)
     }
     mbar_init(&bar_acc, 1);
     mbar_fence_init();
-    for (int j = 0; j < 8; ++j) {
-      const int lp = tb * 8 + j;
-      int ph = -1, off = 0, cnt = 0, st = 0;
-      if (lp < npg) {
-        ph = p.page_table[static_cast<int64_t>(s0) * p.max_pages + lp];
-        if (ph >= 0 && ph < p.num_pages) {
-          off = p.link_off[ph];
-          cnt = p.link_off[ph + 1] - off;
-          st = cnt > 0 && p.links[off] == s0 * p.max_pages + lp && (!p.listed || p.listed[ph]);
-        } else {
-          ph = -1;
-        }
-      }
-      pinfo.phys[j] = ph;
-      pinfo.off[j] = off;
-      pinfo.cnt[j] = cnt;
-      pinfo.store[j] = st;
-    }
-    int any = 0;
-    for (int j = 0; j < 8; ++j) any |= pinfo.store[j];
-    any_store_sh = any;
+    any_store_sh = fill_page_info(p, s0, tb, npg, &pinfo);
     // number of steps over all passes
     PassIter it{&p, &pinfo, s0, tb};
     int n = 0;

@@ -48,6 +48,14 @@ cudaError_t launch_paged_mla_mma_split(const PagedMlaMaps& m, const PagedParams&
 cudaError_t launch_paged_mla_stats_mma(const PagedMlaMaps& m, const PagedParams& p, cudaStream_t s);
 // MLA query side (dQ, dQp) on the same path, from lse / delta; maps as for the statistics
 cudaError_t launch_paged_mla_query_mma(const PagedMlaMaps& m, const PagedParams& p, cudaStream_t s);
+// MLA history on tcgen05 (two CTAs per 128-token block, each accumulating
+// half of the dims); blocks with a heavy 64-token half (p.heavy, when not
+// null) are left to the cluster-split kernel
+bool mla_tc_supported(const PagedParams& p);
+cudaError_t launch_paged_mla_tc(const PagedMlaMaps& m, const PagedParams& p, cudaStream_t s);
+// extends the heavy flags of the split plan to both 64-token halves of a
+// 128-token block
+cudaError_t launch_paged_mla_tc_pair_heavy(const PagedParams& p, cudaStream_t s);
 cudaError_t launch_paged_mla_stats(const PagedParams& p, const void* q, const void* qp, const void* dy,
                                    const void* k_pool, const void* kp_pool, cudaStream_t s);
 

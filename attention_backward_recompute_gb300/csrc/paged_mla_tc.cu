@@ -1,0 +1,498 @@
+// Paged MLA history backward on tcgen05 (dK of the latent and of the position
+// keys), atomic-free.
+//
+// ruDNN src/paged_attention/ordered_kernel.rs (history_backward with `mla`):
+// for query row r, head h and history token t,
+//   s = scale * (q[r,h] . k_lat[t] + qp[r,h] . k_pos[t]),  p = exp(s - lse[r,h])
+//   ds = p * (dY[r,h] . k_lat[t] - delta[r,h]) * scale
+//   dK_lat[t] += ds * q[r,h] + p * dY[r,h]      (the latent is key and value)
+//   dKp[t]    += ds * qp[r,h]
+// summed over the links of the token's page (link order), the visible rows of
+// each linked sequence (t <= pos(r) when causal) and the heads of the group.
+//
+// As tile products: a CTA owns 128 tokens (eight pages) of one sequence and
+// one KV head; a column is one (query row, head of the group) pair and a tile
+// is 32 columns (32/G rows).  Per tile:
+//   S^T  = K_lat Q^T + K_pos Qp^T     [128 x 32], 9 chunks of 64 dims
+//   dP^T = K_lat dY^T                 [128 x 32], 8 chunks
+//   P^T  = exp2(S^T scale log2e - lse log2e),  dS^T = P^T (dP^T - delta) scale
+//   acc  += P^T dY[:, part] + dS^T Q[:, part]   (A operands from tensor memory)
+// The accumulator of 128 tokens x 576 dims does not fit the 512 tensor-memory
+// columns next to the score tiles, so the dims are split over two CTAs
+// (PART 0: latent dims [0, 256); PART 1: latent dims [256, 512) and the 64
+// position dims); each forms the full S^T and dP^T of its tiles.
+//
+// Shared memory: the K tile stays resident (latent + position, 9 chunks of
+// [128 tokens x 64 dims], 144 KiB); Q, Qp and dY arrive as a stream of 4 KiB
+// chunks ([32 columns x 64 dims]) through a 16-stage TMA ring, in the order
+//   S/dP chunks of tile t, then the part's accumulation chunks of tile t - 1
+// so the tensor core forms the scores of tile t while the compute warps turn
+// tile t - 1 into P and dS.  Roles (384 threads): warp 0 TMA producer (also
+// writes each tile's column statistics), warp 1 MMA issuer (whole warp,
+// elect.sync), warps 4..7 / 8..11 compute groups for even / odd tiles (one
+// TMEM lane per token).
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "paged_common.cuh"
+#include "paged_launch.h"
+#include "paged_pass.cuh"
+#include "sm103.cuh"
+
+namespace attn {
+using namespace sm103;
+
+namespace {
+
+constexpr int kLat = 512, kPos = 64;
+constexpr int BT = 128;                  // tokens per CTA (8 pages of 16)
+constexpr int BC = 32;                   // columns per tile
+constexpr int kStages = 16;              // chunk ring
+constexpr int kStatSlots = 4;
+constexpr int KCH = BT * 128;            // K chunk [128 tokens][64 dims], 16 KiB
+constexpr int QCH = BC * 128;            // Q / dY chunk [32 columns][64 dims], 4 KiB
+constexpr int K_OFF = 0;                 // 8 latent chunks + 1 position chunk
+constexpr int RING_OFF = K_OFF + 9 * KCH;
+constexpr int ST_OFF = RING_OFF + kStages * QCH;
+constexpr int ST_SLOT = 3 * BC * 4 + 16;  // -L2, delta, pos per column + pass info
+constexpr int BYTES = ST_OFF + kStatSlots * ST_SLOT;
+static_assert(RING_OFF % 1024 == 0 && QCH % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+// TMEM: accumulator [0, 320) (PART 0 uses [0, 256)), S^T[2], dP^T[2] 32 columns each
+constexpr int T_ACC = 0, T_S = 320, T_DP = 384, TMEM_COLS = 512;
+constexpr int kSdpJobs = 17;             // 9 S chunks + 8 dP chunks per tile
+
+template <int PART>
+struct PartShape {
+  static constexpr int NACC = PART == 0 ? 8 : 9;    // accumulation chunks per tile
+  static constexpr int ACC_COLS = PART == 0 ? 256 : 320;
+};
+
+__device__ __forceinline__ bool drain_wait(uint64_t* bar, uint32_t parity) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_test(bar, parity)) {
+    if (global_timer_ns() - t0 > ATTN_WAIT_TIMEOUT_NS) return false;
+  }
+  return true;
+}
+
+// The chunk of job a of the accumulation of a tile: a < 4: dY latent chunk
+// (4 PART + a), product P^T dY; a >= 4: Q chunk (4 PART + a - 4), or Qp (a ==
+// 8, PART 1 only), product dS^T Q.  Its accumulator chunk (64 columns).
+template <int PART>
+__device__ __forceinline__ int acc_src_chunk(int a) {
+  return a < 4 ? 4 * PART + a : 4 * PART + a - 4;  // 8 = the position chunk
+}
+
+template <int PART>
+__global__ void __launch_bounds__(384, 1)
+    mla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_qp,
+                  const __grid_constant__ CUtensorMap tm_dy, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_kp, const PagedParams p) {
+  using PS = PartShape<PART>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ uint64_t bar_k, bar_full[kStages], bar_empty[kStages], bar_st_full[kStatSlots],
+      bar_st_empty[kStatSlots], bar_s_full[2], bar_dp_full[2], bar_p_full[2], bar_ds_full[2], bar_acc;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_flag;
+  __shared__ PageInfo pinfo;
+  __shared__ int n_tiles_sh, any_store_sh;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = blockIdx.x, tb = blockIdx.y, s0 = blockIdx.z;
+  const int len0 = seq_len_of(p, s0);
+  const int npg = pages_of(len0, p.page_size);
+  if (tb * 8 >= npg) return;  // no token of this sequence in the block (uniform exit)
+  const int RT = BC / p.G;    // query rows per tile
+  const Abort ab{&abort_flag, p.err};
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&bar_k, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bar_full[s], 1);
+      mbar_init(&bar_empty[s], 1);
+    }
+    for (int s = 0; s < kStatSlots; ++s) {
+      mbar_init(&bar_st_full[s], 1);
+      mbar_init(&bar_st_empty[s], 4);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bar_s_full[s], 1);
+      mbar_init(&bar_dp_full[s], 1);
+      mbar_init(&bar_p_full[s], 4);
+      mbar_init(&bar_ds_full[s], 4);
+    }
+    mbar_init(&bar_acc, 1);
+    mbar_fence_init();
+    int any = fill_page_info(p, s0, tb, npg, &pinfo);
+    // a block with a heavy 64-token half belongs to the cluster-split kernel
+    if (any && p.heavy) {
+      const int nb64 = (p.max_pages + 3) / 4;
+      const int64_t h0 = (static_cast<int64_t>(s0) * nb64 + 2 * tb) * p.KVH + g;
+      if (p.heavy[h0] || (2 * tb + 1 < nb64 && p.heavy[h0 + p.KVH])) any = 0;
+    }
+    any_store_sh = any;
+    PassIter it{&p, &pinfo, s0, tb};
+    int n = 0;
+    if (any && it.begin(RT)) {
+      do ++n;
+      while (it.advance(RT));
+    }
+    n_tiles_sh = n;
+  }
+  __syncthreads();
+  // a block whose pages are all stored by other CTAs (their owners) has
+  // nothing to write: leave before taking tensor memory (uniform exit)
+  if (!any_store_sh) return;
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_sh, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+  const int n = n_tiles_sh;
+  const int oob_slot = p.num_pages * p.page_size;  // out-of-range coordinate: TMA fills zeros
+
+  if (n > 0 && warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_map(&tm_q);
+      tma_prefetch_map(&tm_qp);
+      tma_prefetch_map(&tm_dy);
+      tma_prefetch_map(&tm_k);
+      tma_prefetch_map(&tm_kp);
+      mbar_arrive_expect_tx(&bar_k, 9 * KCH);
+      for (int j = 0; j < 8; ++j) {
+        const int slot = pinfo.phys[j] >= 0 ? pinfo.phys[j] * p.page_size : oob_slot;
+        for (int c = 0; c < 8; ++c)
+          tma_load_3d(sm + K_OFF + c * KCH + j * 16 * 128, &tm_k, &bar_k, c * 64, g, slot);
+        tma_load_3d(sm + K_OFF + 8 * KCH + j * 16 * 128, &tm_kp, &bar_k, 0, g, slot);
+      }
+    }
+    PassIter it{&p, &pinfo, s0, tb};
+    it.begin(RT);
+    bool ok = true;
+    int q = 0;          // job (chunk) counter of the ring
+    int prev_row0 = 0;  // first query row of the previous tile
+    int last_use[kStages];
+    for (int i = 0; i < kStages; ++i) last_use[i] = -1;
+    // one chunk into the ring: Q (src 0), Qp (1) or dY (2), latent chunk c
+    auto load_chunk = [&](int src, int c, int row0) -> bool {
+      const int s = q % kStages;
+      if (q >= kStages && !mbar_wait(&bar_empty[s], ((q / kStages) - 1) & 1, ab)) return false;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&bar_full[s], QCH);
+        const CUtensorMap* m = src == 0 ? &tm_q : src == 1 ? &tm_qp : &tm_dy;
+        tma_load_3d(sm + RING_OFF + s * QCH, m, &bar_full[s], src == 1 ? 0 : c * 64, g * p.G, row0);
+      }
+      last_use[s] = q;
+      ++q;
+      return true;
+    };
+    for (int t = 0; t <= n && ok; ++t) {
+      if (t < n) {
+        const int row0 = it.r_begin + it.tile * RT;
+        // column statistics of tile t: -L2, delta, pos per column, plus the
+        // pass's token mapping
+        const int ss = t % kStatSlots;
+        if (t >= kStatSlots && !(ok = mbar_wait(&bar_st_empty[ss], ((t / kStatSlots) - 1) & 1, ab))) break;
+        uint8_t* st = sm + ST_OFF + ss * ST_SLOT;
+        float* snl = reinterpret_cast<float*>(st);
+        float* sdl = snl + BC;
+        int* spos = reinterpret_cast<int*>(sdl + BC);
+        int* sinfo = spos + BC;
+        {
+          const int c = lane;  // one column per lane
+          const int r = row0 + c / p.G;
+          const int hh = g * p.G + c % p.G;
+          float nl2 = -__int_as_float(0x7f800000), dl = 0.f;
+          int pos = -1;
+          if (r < it.r_end) {
+            const float lse = p.lse[static_cast<int64_t>(r) * p.H + hh];
+            if (lse != -__int_as_float(0x7f800000)) {
+              nl2 = -lse * 1.4426950408889634f;
+              dl = p.delta[static_cast<int64_t>(r) * p.H + hh];
+              pos = p.causal ? p.q_pos[r] : 0x7fffffff;
+            }
+          }
+          snl[c] = nl2;
+          sdl[c] = dl;
+          spos[c] = pos;
+        }
+        if (lane == 0) {
+          sinfo[0] = it.tbase;
+          sinfo[1] = it.ra;
+          sinfo[2] = it.rb;
+          sinfo[3] = seq_len_of(p, it.seq);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_st_full[ss]);
+        // S chunks (Q latent 0..7, Qp), then dP chunks (dY 0..7)
+        for (int c = 0; c < 9 && ok; ++c) ok = load_chunk(c < 8 ? 0 : 1, c, row0);
+        for (int c = 0; c < 8 && ok; ++c) ok = load_chunk(2, c, row0);
+        if (!ok) break;
+        if (t >= 1) {
+          for (int a = 0; a < PS::NACC && ok; ++a) {
+            const int c = acc_src_chunk<PART>(a);
+            ok = load_chunk(a < 4 ? 2 : (c == 8 ? 1 : 0), c, prev_row0);
+          }
+        }
+        prev_row0 = row0;
+        it.advance(RT);
+      } else {
+        for (int a = 0; a < PS::NACC && ok; ++a) {
+          const int c = acc_src_chunk<PART>(a);
+          ok = load_chunk(a < 4 ? 2 : (c == 8 ? 1 : 0), c, prev_row0);
+        }
+      }
+    }
+    if (lane == 0) {
+      for (int s = 0; s < kStages; ++s)
+        if (last_use[s] >= 0) drain_wait(&bar_full[s], (last_use[s] / kStages) & 1);
+      drain_wait(&bar_k, 0);
+    }
+  } else if (n > 0 && warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    // the whole warp runs this role (warp-uniform); elected lanes issue
+    constexpr uint32_t id_s = idesc_bf16(128, BC, false, false);   // S^T, dP^T: K-major A and B
+    constexpr uint32_t id_acc = idesc_bf16(128, 64, false, true);  // acc: A from TMEM, B MN-major
+    const uint64_t dK0 = sdesc_sw128(smem_addr(sm + K_OFF), 16, 1024);
+    const uint64_t dR0 = sdesc_sw128(smem_addr(sm + RING_OFF), 16, 1024);            // K-major
+    const uint64_t dRm0 = sdesc_sw128(smem_addr(sm + RING_OFF), BC * 128, 1024);     // MN-major
+    bool ok = mbar_wait_warp(&bar_k, 0, ab);
+    int q = 0;
+    for (int t = 0; t <= n && ok; ++t) {
+      if (t < n) {
+        const int bb = t & 1;
+        // S^T(t) over 9 chunks, dP^T(t) over 8: the buffers of tile t - 2
+        // were consumed by its accumulation, earlier in this stream
+        for (int j = 0; j < kSdpJobs && ok; ++j, ++q) {
+          const int s = q % kStages;
+          if (!(ok = mbar_wait_warp(&bar_full[s], (q / kStages) & 1, ab))) break;
+          tc_fence_after();
+          const bool is_s = j < 9;
+          const int c = is_s ? j : j - 9;
+          const uint32_t d = tmem + (is_s ? T_S : T_DP) + bb * BC;
+          const uint64_t a = sdesc_add(dK0, c * KCH), bq = sdesc_add(dR0, s * QCH);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            if (kk == 0 && (j == 0 || j == 9))
+              mma_ss_w<false>(d, a, bq, id_s);
+            else
+              mma_ss_w<true>(d, sdesc_add(a, kk * 32), sdesc_add(bq, kk * 32), id_s);
+          }
+          mma_commit_w(&bar_empty[s]);
+          if (j == 8) mma_commit_w(&bar_s_full[bb]);
+          if (j == 16) mma_commit_w(&bar_dp_full[bb]);
+        }
+      }
+      if (t >= 1 && ok) {
+        // accumulation of tile u = t - 1: P^T dY chunks once P^T(u) is in,
+        // then dS^T Q chunks once dS^T(u) is in
+        const int u = t - 1, bu = u & 1;
+        if (!(ok = mbar_wait_warp(&bar_p_full[bu], (u >> 1) & 1, ab))) break;
+        tc_fence_after();
+        for (int a = 0; a < PS::NACC && ok; ++a, ++q) {
+          if (a == 4) {
+            if (!(ok = mbar_wait_warp(&bar_ds_full[bu], (u >> 1) & 1, ab))) break;
+            tc_fence_after();
+          }
+          const int s = q % kStages;
+          if (!(ok = mbar_wait_warp(&bar_full[s], (q / kStages) & 1, ab))) break;
+          tc_fence_after();
+          const int c = acc_src_chunk<PART>(a);
+          const uint32_t d = tmem + T_ACC + (c - 4 * PART) * 64;  // chunk 8 (position) -> 256
+          const uint32_t at = tmem + (a < 4 ? T_S : T_DP) + bu * BC;
+          const uint64_t bm = sdesc_add(dRm0, s * QCH);
+          // the first contribution to an accumulator chunk overwrites it:
+          // P^T dY for latent chunks, dS^T Qp for the position chunk
+          const bool first = u == 0 && (a < 4 || c == 8);
+          if (first)
+            mma_ts_w<false>(d, at, bm, id_acc);
+          else
+            mma_ts_w<true>(d, at, bm, id_acc);
+          mma_ts_w<true>(d, at + 8, sdesc_add(bm, 16 * 128), id_acc);
+          mma_commit_w(&bar_empty[s]);
+        }
+      }
+    }
+    mma_commit_w(&bar_acc);
+    drain_wait(&bar_acc, 0);
+    __syncwarp();
+  } else if (warp >= 4) {
+    const int sg = (warp - 4) >> 2;  // compute group: tiles of parity sg
+    const int lg = warp & 3;
+    const int row = lg * 32 + lane;  // token row inside the block == TMEM lane
+    const uint32_t lane_addr = static_cast<uint32_t>(lg * 32) << 16;
+    bool ok = n > 0;
+    for (int t = sg; t < n && ok; t += 2) {
+      const int bb = t & 1, ss = t % kStatSlots;
+      if (!(ok = mbar_wait_warp(&bar_st_full[ss], (t / kStatSlots) & 1, ab))) break;
+      const uint8_t* st = sm + ST_OFF + ss * ST_SLOT;
+      const float* snl = reinterpret_cast<const float*>(st);
+      const float* sdl = snl + BC;
+      const int* spos = reinterpret_cast<const int*>(sdl + BC);
+      const int* sinfo = spos + BC;
+      const int tok = sinfo[0] + row;
+      const bool tok_ok = row >= sinfo[1] && row < sinfo[2] && tok >= 0 && tok < sinfo[3];
+      if (!(ok = mbar_wait_warp(&bar_s_full[bb], (t >> 1) & 1, ab))) break;
+      tc_fence_after();
+      // ---------------------------------------------------- S^T -> P^T
+      const uint32_t tS = tmem + T_S + bb * BC + lane_addr;
+      uint32_t sr[32], pw[16];
+      tmem_ld32(tS, sr);
+      tmem_ld_wait();
+      const uint64_t sl2 = f2_pack(p.scale_log2, p.scale_log2);
+#pragma unroll
+      for (int c4 = 0; c4 < 8; ++c4) {
+        const float4 nl = *reinterpret_cast<const float4*>(snl + 4 * c4);
+        const int4 ps = *reinterpret_cast<const int4*>(spos + 4 * c4);
+        float x0, x1, x2, x3;
+        f2_split(f2_fma(f2_pack_u(sr[4 * c4], sr[4 * c4 + 1]), sl2, f2_pack(nl.x, nl.y)), x0, x1);
+        f2_split(f2_fma(f2_pack_u(sr[4 * c4 + 2], sr[4 * c4 + 3]), sl2, f2_pack(nl.z, nl.w)), x2, x3);
+        const float p0 = (tok_ok && tok <= ps.x) ? ex2_approx(x0) : 0.f;
+        const float p1 = (tok_ok && tok <= ps.y) ? ex2_approx(x1) : 0.f;
+        const float p2 = (tok_ok && tok <= ps.z) ? ex2_approx(x2) : 0.f;
+        const float p3 = (tok_ok && tok <= ps.w) ? ex2_approx(x3) : 0.f;
+        pw[2 * c4] = pack_bf16x2(p0, p1);
+        pw[2 * c4 + 1] = pack_bf16x2(p2, p3);
+      }
+      tmem_st16(tS, pw);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar_p_full[bb]);
+      // ---------------------------------------------------- dP^T, P^T -> dS^T
+      if (!(ok = mbar_wait_warp(&bar_dp_full[bb], (t >> 1) & 1, ab))) break;
+      tc_fence_after();
+      const uint32_t tDP = tmem + T_DP + bb * BC + lane_addr;
+      uint32_t dr[32], dsw[16];
+      tmem_ld32(tDP, dr);
+      tmem_ld_wait();
+      // a masked entry has P = 0 and takes dS = 0 by select: dP of a tail or
+      // unowned slot may be NaN
+#pragma unroll
+      for (int c4 = 0; c4 < 8; ++c4) {
+        const float4 d4 = *reinterpret_cast<const float4*>(sdl + 4 * c4);
+        const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+        float ds[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const uint32_t w = pw[2 * c4 + (e >> 1)];
+          const float pe = __uint_as_float((e & 1) ? (w & 0xffff0000u) : (w << 16));
+          ds[e] = pe != 0.f ? pe * (__uint_as_float(dr[4 * c4 + e]) - dv[e]) * p.scale : 0.f;
+        }
+        dsw[2 * c4] = pack_bf16x2(ds[0], ds[1]);
+        dsw[2 * c4 + 1] = pack_bf16x2(ds[2], ds[3]);
+      }
+      tmem_st16(tDP, dsw);
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&bar_ds_full[bb]);
+        mbar_arrive(&bar_st_empty[ss]);
+      }
+    }
+    if (n > 0) {
+      if (ok) ok = mbar_wait_warp(&bar_acc, 0, ab);
+      tc_fence_after();
+    }
+    // ------------------------------------------------------------ epilogue
+    // 32-column chunks of the accumulator, alternating between the groups:
+    // latent dims [256 PART + 32 cc, ...) for cc < 8, position dims after
+    // that (PART 1); rows of tokens no pass saw are zero
+    if (ok || n == 0) {  // warp-uniform: the tensor-memory loads are warp-collective
+      const int j = row >> 4;
+      const bool mine = pinfo.store[j] != 0;
+      const int64_t prow = (static_cast<int64_t>(pinfo.phys[j]) * p.page_size + (row & 15)) * p.KVH + g;
+#pragma unroll 1
+      for (int cc = sg; cc < PS::ACC_COLS / 32; cc += 2) {
+        const bool pos_chunk = cc >= 8;
+        if (!(p.wrt & (pos_chunk ? 8u : 2u))) continue;
+        uint32_t r[32];
+        if (n > 0) {
+          tmem_ld32(tmem + T_ACC + cc * 32 + lane_addr, r);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r[i] = 0u;
+        }
+        if (mine) {
+          __nv_bfloat16* out = pos_chunk
+                                   ? static_cast<__nv_bfloat16*>(p.dkp_pool) + prow * kPos + (cc - 8) * 32
+                                   : static_cast<__nv_bfloat16*>(p.dk_pool) + prow * kLat + 256 * PART + cc * 32;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(r[8 * i]), __uint_as_float(r[8 * i + 1]));
+            v.y = pack_bf16x2(__uint_as_float(r[8 * i + 2]), __uint_as_float(r[8 * i + 3]));
+            v.z = pack_bf16x2(__uint_as_float(r[8 * i + 4]), __uint_as_float(r[8 * i + 5]));
+            v.w = pack_bf16x2(__uint_as_float(r[8 * i + 6]), __uint_as_float(r[8 * i + 7]));
+            *reinterpret_cast<uint4*>(out + 8 * i) = v;
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+template <int PART>
+cudaError_t launch_part(const PagedMlaMaps& m, const PagedParams& p, cudaStream_t s) {
+  auto kern = mla_tc_kernel<PART>;
+  const int smem = BYTES + 1024;
+  static_assert(BYTES + 1024 >= kSmemOneCtaPerSm, "all 512 TMEM columns: one CTA per SM");
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  const int nblk = (p.max_pages * p.page_size + BT - 1) / BT;
+  dim3 grid(p.KVH, nblk, p.S);
+  kern<<<grid, 384, smem, s>>>(m.q, m.qp, m.dy, m.k, m.kp, p);
+  return cudaGetLastError();
+}
+
+// heavy[] is planned per 64-token block; a 128-token block of this kernel
+// goes to the split kernel when either half is heavy, so both halves are
+// flagged for it
+__global__ void mla_tc_pair_heavy_kernel(const PagedParams p) {
+  const int nb64 = (p.max_pages + 3) / 4;
+  const int nb128 = (nb64 + 1) / 2;
+  const int n = p.S * nb128 * p.KVH;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+    const int g = i % p.KVH, sb = i / p.KVH, s0 = sb / nb128, b = sb - s0 * nb128;
+    const int64_t h0 = (static_cast<int64_t>(s0) * nb64 + 2 * b) * p.KVH + g;
+    const bool second = 2 * b + 1 < nb64;
+    const int h = p.heavy[h0] | (second ? p.heavy[h0 + p.KVH] : 0);
+    p.heavy[h0] = h;
+    if (second) p.heavy[h0 + p.KVH] = h;
+  }
+}
+
+}  // namespace
+
+bool mla_tc_supported(const PagedParams& p) {
+  return p.Dk == kLat && p.Dp == kPos && p.page_size == 16 && p.G >= 1 && p.G <= BC && BC % p.G == 0;
+}
+
+cudaError_t launch_paged_mla_tc_pair_heavy(const PagedParams& p, cudaStream_t s) {
+  if (p.S == 0 || p.max_pages == 0 || p.KVH == 0) return cudaSuccess;
+  mla_tc_pair_heavy_kernel<<<64, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_paged_mla_tc(const PagedMlaMaps& m, const PagedParams& p, cudaStream_t s) {
+  if (p.num_pages == 0 || p.S == 0 || p.max_pages == 0) return cudaSuccess;
+  cudaError_t e = launch_part<0>(m, p, s);
+  if (e == cudaSuccess) e = launch_part<1>(m, p, s);
+  return e;
+}
+
+}  // namespace attn
