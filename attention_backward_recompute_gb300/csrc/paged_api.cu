@@ -214,17 +214,25 @@ ATTN_API attn_status_t attn_bwd_paged_compact(const attn_paged_desc* d, const vo
     attn::PagedMlaMaps mm;
     std::memset(&mm, 0, sizeof(mm));
     const uint64_t slots = uint64_t(d->num_pages) * d->page_size;
-    const uint32_t G = uint32_t(p.G), RT = 32u / G;
+    const bool split = attn::mla_mma_supported(p);
+    // query-side boxes of 64 columns (64/G rows) for the tcgen05 kernel, of
+    // 32 columns for the cluster-split kernel
+    const uint32_t G = uint32_t(p.G), RT = 64u / G, RS = split ? 32u / G : RT;
+    attn::PagedMlaMaps mt;
     bool enc = encode3d(&mm.k, k_pool, d->key_dim, d->kv_heads, slots, 64, 1, uint32_t(d->page_size)) &&
                encode3d(&mm.kp, kp_pool, d->position_dim, d->kv_heads, slots, 64, 1, uint32_t(d->page_size));
     if (d->num_queries > 0)
-      enc = enc && encode3d(&mm.q, q, d->key_dim, d->heads, d->num_queries, 64, G, RT) &&
-            encode3d(&mm.qp, qp, d->position_dim, d->heads, d->num_queries, 64, G, RT) &&
-            encode3d(&mm.dy, dy, d->value_dim, d->heads, d->num_queries, 64, G, RT);
+      enc = enc && encode3d(&mm.q, q, d->key_dim, d->heads, d->num_queries, 64, G, RS) &&
+            encode3d(&mm.qp, qp, d->position_dim, d->heads, d->num_queries, 64, G, RS) &&
+            encode3d(&mm.dy, dy, d->value_dim, d->heads, d->num_queries, 64, G, RS) &&
+            encode3d(&mt.q, q, d->key_dim, d->heads, d->num_queries, 64, G, RT) &&
+            encode3d(&mt.qp, qp, d->position_dim, d->heads, d->num_queries, 64, G, RT) &&
+            encode3d(&mt.dy, dy, d->value_dim, d->heads, d->num_queries, 64, G, RT);
     else
-      mm.q = mm.qp = mm.dy = mm.k;
+      mm.q = mm.qp = mm.dy = mt.q = mt.qp = mt.dy = mm.k;
     if (!enc) return api_fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed");
-    const bool split = attn::mla_mma_supported(p);
+    mt.k = mm.k;
+    mt.kp = mm.kp;
     if (!split) p.heavy = nullptr;
     attn::timing_mark_begin(5, s);
     cudaError_t e = attn::launch_paged_prep(p, s);
@@ -236,7 +244,7 @@ ATTN_API attn_status_t attn_bwd_paged_compact(const attn_paged_desc* d, const vo
     attn::timing_mark(s);
     if (split && e == cudaSuccess) e = attn::launch_paged_mla_mma_split(mm, p, s);
     attn::timing_mark(s);
-    if (e == cudaSuccess) e = attn::launch_paged_mla_tc(mm, p, s);
+    if (e == cudaSuccess) e = attn::launch_paged_mla_tc(mt, p, s);
     attn::timing_mark(s);
     attn::timing_mark_end();
     if (e != cudaSuccess) return api_fail(ATTN_ERR_CUDA, "paged launch failed: %s", cudaGetErrorString(e));

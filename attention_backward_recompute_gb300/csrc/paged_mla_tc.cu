@@ -12,9 +12,9 @@
 //
 // As tile products: a CTA owns 128 tokens (eight pages) of one sequence and
 // one KV head; a column is one (query row, head of the group) pair and a tile
-// is 32 columns (32/G rows).  Per tile:
-//   S^T  = K_lat Q^T + K_pos Qp^T     [128 x 32], 9 chunks of 64 dims
-//   dP^T = K_lat dY^T                 [128 x 32], 8 chunks
+// is 64 columns (64/G rows).  Per tile:
+//   S^T  = K_lat Q^T + K_pos Qp^T     [128 x 64], 9 chunks of 64 dims
+//   dP^T = K_lat dY^T                 [128 x 64], 8 chunks
 //   P^T  = exp2(S^T scale log2e - lse log2e),  dS^T = P^T (dP^T - delta) scale
 //   acc  += P^T dY[:, part] + dS^T Q[:, part]   (A operands from tensor memory)
 // The accumulator of 128 tokens x 576 dims does not fit the 512 tensor-memory
@@ -23,11 +23,15 @@
 // position dims); each forms the full S^T and dP^T of its tiles.
 //
 // Shared memory: the K tile stays resident (latent + position, 9 chunks of
-// [128 tokens x 64 dims], 144 KiB); Q, Qp and dY arrive as a stream of 4 KiB
-// chunks ([32 columns x 64 dims]) through a 16-stage TMA ring, in the order
-//   S/dP chunks of tile t, then the part's accumulation chunks of tile t - 1
+// [128 tokens x 64 dims], 144 KiB); Q, Qp and dY arrive as a stream of 8 KiB
+// chunks ([64 columns x 64 dims]) through an 8-stage TMA ring (released two
+// stages at a time), in the order
+//   S chunks of tile t, the part's accumulation chunks of tile t - 1, dP
+//   chunks of tile t
 // so the tensor core forms the scores of tile t while the compute warps turn
-// tile t - 1 into P and dS.  Roles (384 threads): warp 0 TMA producer (also
+// tile t - 1 into P and dS.  The score tile is double-buffered in tensor
+// memory, the dP tile single-buffered: dP(t) overwrites dS(t - 1) after the
+// accumulation of tile t - 1 has read it.  Roles (384 threads): warp 0 TMA producer (also
 // writes each tile's column statistics), warp 1 MMA issuer (whole warp,
 // elect.sync), warps 4..7 / 8..11 compute groups for even / odd tiles (one
 // TMEM lane per token).
@@ -46,20 +50,19 @@ namespace {
 
 constexpr int kLat = 512, kPos = 64;
 constexpr int BT = 128;                  // tokens per CTA (8 pages of 16)
-constexpr int BC = 32;                   // columns per tile
-constexpr int kStages = 16;              // chunk ring
+constexpr int BC = 64;                   // columns per tile
+constexpr int kStages = 8;               // chunk ring (released in pairs)
 constexpr int kStatSlots = 4;
 constexpr int KCH = BT * 128;            // K chunk [128 tokens][64 dims], 16 KiB
-constexpr int QCH = BC * 128;            // Q / dY chunk [32 columns][64 dims], 4 KiB
+constexpr int QCH = BC * 128;            // Q / dY chunk [64 columns][64 dims], 8 KiB
 constexpr int K_OFF = 0;                 // 8 latent chunks + 1 position chunk
 constexpr int RING_OFF = K_OFF + 9 * KCH;
 constexpr int ST_OFF = RING_OFF + kStages * QCH;
 constexpr int ST_SLOT = 3 * BC * 4 + 16;  // -L2, delta, pos per column + pass info
 constexpr int BYTES = ST_OFF + kStatSlots * ST_SLOT;
 static_assert(RING_OFF % 1024 == 0 && QCH % 1024 == 0, "swizzled tiles need 1024-byte alignment");
-// TMEM: accumulator [0, 320) (PART 0 uses [0, 256)), S^T[2], dP^T[2] 32 columns each
-constexpr int T_ACC = 0, T_S = 320, T_DP = 384, TMEM_COLS = 512;
-constexpr int kSdpJobs = 17;             // 9 S chunks + 8 dP chunks per tile
+// TMEM: accumulator [0, 320) (PART 0 uses [0, 256)), S^T[2] and dP^T 64 columns each
+constexpr int T_ACC = 0, T_S = 320, T_DP = 448, TMEM_COLS = 512;
 
 template <int PART>
 struct PartShape {
@@ -91,8 +94,8 @@ __global__ void __launch_bounds__(384, 1)
   using PS = PartShape<PART>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t bar_k, bar_full[kStages], bar_empty[kStages], bar_st_full[kStatSlots],
-      bar_st_empty[kStatSlots], bar_s_full[2], bar_dp_full[2], bar_p_full[2], bar_ds_full[2], bar_acc;
+  __shared__ uint64_t bar_k, bar_full[kStages], bar_empty[kStages / 2], bar_st_full[kStatSlots],
+      bar_st_empty[kStatSlots], bar_s_full[2], bar_p_full[2], bar_dp_full, bar_ds_full, bar_acc;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
   __shared__ PageInfo pinfo;
@@ -109,20 +112,18 @@ __global__ void __launch_bounds__(384, 1)
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(&bar_k, 1);
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&bar_full[s], 1);
-      mbar_init(&bar_empty[s], 1);
-    }
+    for (int s = 0; s < kStages; ++s) mbar_init(&bar_full[s], 1);
+    for (int s = 0; s < kStages / 2; ++s) mbar_init(&bar_empty[s], 1);
     for (int s = 0; s < kStatSlots; ++s) {
       mbar_init(&bar_st_full[s], 1);
       mbar_init(&bar_st_empty[s], 4);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bar_s_full[s], 1);
-      mbar_init(&bar_dp_full[s], 1);
       mbar_init(&bar_p_full[s], 4);
-      mbar_init(&bar_ds_full[s], 4);
     }
+    mbar_init(&bar_dp_full, 1);
+    mbar_init(&bar_ds_full, 4);
     mbar_init(&bar_acc, 1);
     mbar_fence_init();
     int any = fill_page_info(p, s0, tb, npg, &pinfo);
@@ -182,7 +183,9 @@ __global__ void __launch_bounds__(384, 1)
     // one chunk into the ring: Q (src 0), Qp (1) or dY (2), latent chunk c
     auto load_chunk = [&](int src, int c, int row0) -> bool {
       const int s = q % kStages;
-      if (q >= kStages && !mbar_wait(&bar_empty[s], ((q / kStages) - 1) & 1, ab)) return false;
+      // stages are released in pairs (2j, 2j + 1) by one commit
+      if (q >= kStages && (q & 1) == 0 && !mbar_wait(&bar_empty[s >> 1], ((q / kStages) - 1) & 1, ab))
+        return false;
       if (lane == 0) {
         mbar_arrive_expect_tx(&bar_full[s], QCH);
         const CUtensorMap* m = src == 0 ? &tm_q : src == 1 ? &tm_qp : &tm_dy;
@@ -204,8 +207,7 @@ __global__ void __launch_bounds__(384, 1)
         float* sdl = snl + BC;
         int* spos = reinterpret_cast<int*>(sdl + BC);
         int* sinfo = spos + BC;
-        {
-          const int c = lane;  // one column per lane
+        for (int c = lane; c < BC; c += 32) {  // two columns per lane
           const int r = row0 + c / p.G;
           const int hh = g * p.G + c % p.G;
           float nl2 = -__int_as_float(0x7f800000), dl = 0.f;
@@ -230,16 +232,17 @@ __global__ void __launch_bounds__(384, 1)
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar_st_full[ss]);
-        // S chunks (Q latent 0..7, Qp), then dP chunks (dY 0..7)
+        // S chunks of tile t (Q latent 0..7, Qp), the accumulation chunks of
+        // tile t - 1, then the dP chunks of tile t (dY 0..7)
         for (int c = 0; c < 9 && ok; ++c) ok = load_chunk(c < 8 ? 0 : 1, c, row0);
-        for (int c = 0; c < 8 && ok; ++c) ok = load_chunk(2, c, row0);
-        if (!ok) break;
         if (t >= 1) {
           for (int a = 0; a < PS::NACC && ok; ++a) {
             const int c = acc_src_chunk<PART>(a);
             ok = load_chunk(a < 4 ? 2 : (c == 8 ? 1 : 0), c, prev_row0);
           }
         }
+        for (int c = 0; c < 8 && ok; ++c) ok = load_chunk(2, c, row0);
+        if (!ok) break;
         prev_row0 = row0;
         it.advance(RT);
       } else {
@@ -264,60 +267,72 @@ __global__ void __launch_bounds__(384, 1)
     const uint64_t dRm0 = sdesc_sw128(smem_addr(sm + RING_OFF), BC * 128, 1024);     // MN-major
     bool ok = mbar_wait_warp(&bar_k, 0, ab);
     int q = 0;
-    for (int t = 0; t <= n && ok; ++t) {
-      if (t < n) {
-        const int bb = t & 1;
-        // S^T(t) over 9 chunks, dP^T(t) over 8: the buffers of tile t - 2
-        // were consumed by its accumulation, earlier in this stream
-        for (int j = 0; j < kSdpJobs && ok; ++j, ++q) {
-          const int s = q % kStages;
-          if (!(ok = mbar_wait_warp(&bar_full[s], (q / kStages) & 1, ab))) break;
-          tc_fence_after();
-          const bool is_s = j < 9;
-          const int c = is_s ? j : j - 9;
-          const uint32_t d = tmem + (is_s ? T_S : T_DP) + bb * BC;
-          const uint64_t a = sdesc_add(dK0, c * KCH), bq = sdesc_add(dR0, s * QCH);
+    // a stage's copies are usually in by the time this warp reaches it: a
+    // non-blocking test first, the bounded wait only when it is not
+    auto wait_stage = [&](int qq) -> bool {
+      const int s = qq % kStages;
+      if (mbar_test_warp(&bar_full[s], (qq / kStages) & 1)) return true;
+      return mbar_wait_warp(&bar_full[s], (qq / kStages) & 1, ab);
+    };
+    // after the job of ring index qq: the pair (qq - 1, qq) goes back to the
+    // producer once its products are done
+    auto release = [&](int qq) {
+      if (qq & 1) mma_commit_w(&bar_empty[(qq % kStages) >> 1]);
+    };
+    // S^T(t) (K_SEL 0) or dP^T(t) (1) over its chunks into tensor memory
+    auto xt_jobs = [&](int t, int kind) -> bool {
+      const int nj = kind == 0 ? 9 : 8;
+      const uint32_t d = tmem + (kind == 0 ? T_S + (t & 1) * BC : T_DP);
+      for (int c = 0; c < nj; ++c, ++q) {
+        if (!wait_stage(q)) return false;
+        tc_fence_after();
+        const uint64_t a = sdesc_add(dK0, c * KCH), bq = sdesc_add(dR0, (q % kStages) * QCH);
+        if (c == 0)
+          mma_ss_w<false>(d, a, bq, id_s);
+        else
+          mma_ss_w<true>(d, a, bq, id_s);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            if (kk == 0 && (j == 0 || j == 9))
-              mma_ss_w<false>(d, a, bq, id_s);
-            else
-              mma_ss_w<true>(d, sdesc_add(a, kk * 32), sdesc_add(bq, kk * 32), id_s);
-          }
-          mma_commit_w(&bar_empty[s]);
-          if (j == 8) mma_commit_w(&bar_s_full[bb]);
-          if (j == 16) mma_commit_w(&bar_dp_full[bb]);
-        }
+        for (int kk = 1; kk < 4; ++kk) mma_ss_w<true>(d, sdesc_add(a, kk * 32), sdesc_add(bq, kk * 32), id_s);
+        release(q);
       }
-      if (t >= 1 && ok) {
+      mma_commit_w(kind == 0 ? &bar_s_full[t & 1] : &bar_dp_full);
+      return true;
+    };
+    for (int t = 0; t <= n && ok; ++t) {
+      // S^T(t): its buffer's previous tile (t - 2) was accumulated earlier in
+      // this stream
+      if (t < n && !(ok = xt_jobs(t, 0))) break;
+      if (t >= 1) {
         // accumulation of tile u = t - 1: P^T dY chunks once P^T(u) is in,
         // then dS^T Q chunks once dS^T(u) is in
-        const int u = t - 1, bu = u & 1;
-        if (!(ok = mbar_wait_warp(&bar_p_full[bu], (u >> 1) & 1, ab))) break;
+        const int u = t - 1;
+        if (!(ok = mbar_wait_warp(&bar_p_full[u & 1], (u >> 1) & 1, ab))) break;
         tc_fence_after();
         for (int a = 0; a < PS::NACC && ok; ++a, ++q) {
           if (a == 4) {
-            if (!(ok = mbar_wait_warp(&bar_ds_full[bu], (u >> 1) & 1, ab))) break;
+            if (!(ok = mbar_wait_warp(&bar_ds_full, u & 1, ab))) break;
             tc_fence_after();
           }
-          const int s = q % kStages;
-          if (!(ok = mbar_wait_warp(&bar_full[s], (q / kStages) & 1, ab))) break;
+          if (!(ok = wait_stage(q))) break;
           tc_fence_after();
           const int c = acc_src_chunk<PART>(a);
           const uint32_t d = tmem + T_ACC + (c - 4 * PART) * 64;  // chunk 8 (position) -> 256
-          const uint32_t at = tmem + (a < 4 ? T_S : T_DP) + bu * BC;
-          const uint64_t bm = sdesc_add(dRm0, s * QCH);
+          const uint32_t at = tmem + (a < 4 ? T_S + (u & 1) * BC : T_DP);
+          const uint64_t bm = sdesc_add(dRm0, (q % kStages) * QCH);
           // the first contribution to an accumulator chunk overwrites it:
           // P^T dY for latent chunks, dS^T Qp for the position chunk
-          const bool first = u == 0 && (a < 4 || c == 8);
-          if (first)
+          if (u == 0 && (a < 4 || c == 8))
             mma_ts_w<false>(d, at, bm, id_acc);
           else
             mma_ts_w<true>(d, at, bm, id_acc);
-          mma_ts_w<true>(d, at + 8, sdesc_add(bm, 16 * 128), id_acc);
-          mma_commit_w(&bar_empty[s]);
+#pragma unroll
+          for (int kk = 1; kk < BC / 16; ++kk) mma_ts_w<true>(d, at + kk * 8, sdesc_add(bm, kk * 16 * 128), id_acc);
+          release(q);
         }
+        if (!ok) break;
       }
+      // dP^T(t) overwrites dS^T(t - 1), whose products were just issued
+      if (t < n && !(ok = xt_jobs(t, 1))) break;
     }
     mma_commit_w(&bar_acc);
     drain_wait(&bar_acc, 0);
@@ -341,59 +356,72 @@ __global__ void __launch_bounds__(384, 1)
       if (!(ok = mbar_wait_warp(&bar_s_full[bb], (t >> 1) & 1, ab))) break;
       tc_fence_after();
       // ---------------------------------------------------- S^T -> P^T
+      // two halves of 32 columns: half hf reads S^T columns [32hf, 32hf+32)
+      // and writes P^T (bf16 pairs) to columns [16hf, 16hf+16), which half 0
+      // has already read
       const uint32_t tS = tmem + T_S + bb * BC + lane_addr;
-      uint32_t sr[32], pw[16];
-      tmem_ld32(tS, sr);
-      tmem_ld_wait();
       const uint64_t sl2 = f2_pack(p.scale_log2, p.scale_log2);
+      uint32_t pw[32];
 #pragma unroll
-      for (int c4 = 0; c4 < 8; ++c4) {
-        const float4 nl = *reinterpret_cast<const float4*>(snl + 4 * c4);
-        const int4 ps = *reinterpret_cast<const int4*>(spos + 4 * c4);
-        float x0, x1, x2, x3;
-        f2_split(f2_fma(f2_pack_u(sr[4 * c4], sr[4 * c4 + 1]), sl2, f2_pack(nl.x, nl.y)), x0, x1);
-        f2_split(f2_fma(f2_pack_u(sr[4 * c4 + 2], sr[4 * c4 + 3]), sl2, f2_pack(nl.z, nl.w)), x2, x3);
-        const float p0 = (tok_ok && tok <= ps.x) ? ex2_approx(x0) : 0.f;
-        const float p1 = (tok_ok && tok <= ps.y) ? ex2_approx(x1) : 0.f;
-        const float p2 = (tok_ok && tok <= ps.z) ? ex2_approx(x2) : 0.f;
-        const float p3 = (tok_ok && tok <= ps.w) ? ex2_approx(x3) : 0.f;
-        pw[2 * c4] = pack_bf16x2(p0, p1);
-        pw[2 * c4 + 1] = pack_bf16x2(p2, p3);
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t sr[32];
+        tmem_ld32(tS + 32 * hf, sr);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const int c0 = 32 * hf + 4 * c4;
+          const float4 nl = *reinterpret_cast<const float4*>(snl + c0);
+          const int4 ps = *reinterpret_cast<const int4*>(spos + c0);
+          float x0, x1, x2, x3;
+          f2_split(f2_fma(f2_pack_u(sr[4 * c4], sr[4 * c4 + 1]), sl2, f2_pack(nl.x, nl.y)), x0, x1);
+          f2_split(f2_fma(f2_pack_u(sr[4 * c4 + 2], sr[4 * c4 + 3]), sl2, f2_pack(nl.z, nl.w)), x2, x3);
+          const float p0 = (tok_ok && tok <= ps.x) ? ex2_approx(x0) : 0.f;
+          const float p1 = (tok_ok && tok <= ps.y) ? ex2_approx(x1) : 0.f;
+          const float p2 = (tok_ok && tok <= ps.z) ? ex2_approx(x2) : 0.f;
+          const float p3 = (tok_ok && tok <= ps.w) ? ex2_approx(x3) : 0.f;
+          pw[16 * hf + 2 * c4] = pack_bf16x2(p0, p1);
+          pw[16 * hf + 2 * c4 + 1] = pack_bf16x2(p2, p3);
+        }
+        tmem_st16(tS + 16 * hf, *reinterpret_cast<const uint32_t(*)[16]>(pw + 16 * hf));
       }
-      tmem_st16(tS, pw);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar_p_full[bb]);
       // ---------------------------------------------------- dP^T, P^T -> dS^T
-      if (!(ok = mbar_wait_warp(&bar_dp_full[bb], (t >> 1) & 1, ab))) break;
+      // (one dP buffer: its phase t has completed once this group sees it,
+      // since dP(t - 1) went into the tensor core before S(t) did)
+      if (!(ok = mbar_wait_warp(&bar_dp_full, t & 1, ab))) break;
       tc_fence_after();
-      const uint32_t tDP = tmem + T_DP + bb * BC + lane_addr;
-      uint32_t dr[32], dsw[16];
-      tmem_ld32(tDP, dr);
-      tmem_ld_wait();
+      const uint32_t tDP = tmem + T_DP + lane_addr;
       // a masked entry has P = 0 and takes dS = 0 by select: dP of a tail or
       // unowned slot may be NaN
 #pragma unroll
-      for (int c4 = 0; c4 < 8; ++c4) {
-        const float4 d4 = *reinterpret_cast<const float4*>(sdl + 4 * c4);
-        const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
-        float ds[4];
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t dr[32], dsw[16];
+        tmem_ld32(tDP + 32 * hf, dr);
+        tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const uint32_t w = pw[2 * c4 + (e >> 1)];
-          const float pe = __uint_as_float((e & 1) ? (w & 0xffff0000u) : (w << 16));
-          ds[e] = pe != 0.f ? pe * (__uint_as_float(dr[4 * c4 + e]) - dv[e]) * p.scale : 0.f;
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 d4 = *reinterpret_cast<const float4*>(sdl + 32 * hf + 4 * c4);
+          const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+          float ds[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const uint32_t w = pw[16 * hf + 2 * c4 + (e >> 1)];
+            const float pe = __uint_as_float((e & 1) ? (w & 0xffff0000u) : (w << 16));
+            ds[e] = pe != 0.f ? pe * (__uint_as_float(dr[4 * c4 + e]) - dv[e]) * p.scale : 0.f;
+          }
+          dsw[2 * c4] = pack_bf16x2(ds[0], ds[1]);
+          dsw[2 * c4 + 1] = pack_bf16x2(ds[2], ds[3]);
         }
-        dsw[2 * c4] = pack_bf16x2(ds[0], ds[1]);
-        dsw[2 * c4 + 1] = pack_bf16x2(ds[2], ds[3]);
+        tmem_st16(tDP + 16 * hf, dsw);
       }
-      tmem_st16(tDP, dsw);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(&bar_ds_full[bb]);
+        mbar_arrive(&bar_ds_full);
         mbar_arrive(&bar_st_empty[ss]);
       }
     }
