@@ -24,8 +24,8 @@
 //
 // Shared memory: the K tile stays resident (latent + position, 9 chunks of
 // [128 tokens x 64 dims], 144 KiB); Q, Qp and dY arrive as a stream of 8 KiB
-// chunks ([64 columns x 64 dims]) through an 8-stage TMA ring (released two
-// stages at a time), in the order
+// chunks ([64 columns x 64 dims]) through a 4-stage TMA ring of two chunk
+// slots each (one wait and one release per pair of chunks), in the order
 //   S chunks of tile t, the part's accumulation chunks of tile t - 1, dP
 //   chunks of tile t
 // so the tensor core forms the scores of tile t while the compute warps turn
@@ -51,13 +51,14 @@ namespace {
 constexpr int kLat = 512, kPos = 64;
 constexpr int BT = 128;                  // tokens per CTA (8 pages of 16)
 constexpr int BC = 64;                   // columns per tile
-constexpr int kStages = 8;               // chunk ring (released in pairs)
+constexpr int kStages = 4;               // ring of stages of two chunk slots
 constexpr int kStatSlots = 4;
 constexpr int KCH = BT * 128;            // K chunk [128 tokens][64 dims], 16 KiB
 constexpr int QCH = BC * 128;            // Q / dY chunk [64 columns][64 dims], 8 KiB
 constexpr int K_OFF = 0;                 // 8 latent chunks + 1 position chunk
 constexpr int RING_OFF = K_OFF + 9 * KCH;
-constexpr int ST_OFF = RING_OFF + kStages * QCH;
+constexpr int STAGE = 2 * QCH;
+constexpr int ST_OFF = RING_OFF + kStages * STAGE;
 constexpr int ST_SLOT = 3 * BC * 4 + 16;  // -L2, delta, pos per column + pass info
 constexpr int BYTES = ST_OFF + kStatSlots * ST_SLOT;
 static_assert(RING_OFF % 1024 == 0 && QCH % 1024 == 0, "swizzled tiles need 1024-byte alignment");
@@ -94,7 +95,7 @@ __global__ void __launch_bounds__(384, 1)
   using PS = PartShape<PART>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t bar_k, bar_full[kStages], bar_empty[kStages / 2], bar_st_full[kStatSlots],
+  __shared__ uint64_t bar_k, bar_full[kStages], bar_empty[kStages], bar_st_full[kStatSlots],
       bar_st_empty[kStatSlots], bar_s_full[2], bar_p_full[2], bar_dp_full, bar_ds_full, bar_acc;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
@@ -112,8 +113,10 @@ __global__ void __launch_bounds__(384, 1)
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(&bar_k, 1);
-    for (int s = 0; s < kStages; ++s) mbar_init(&bar_full[s], 1);
-    for (int s = 0; s < kStages / 2; ++s) mbar_init(&bar_empty[s], 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&bar_full[s], 1);
+      mbar_init(&bar_empty[s], 1);
+    }
     for (int s = 0; s < kStatSlots; ++s) {
       mbar_init(&bar_st_full[s], 1);
       mbar_init(&bar_st_empty[s], 4);
@@ -176,30 +179,62 @@ __global__ void __launch_bounds__(384, 1)
     PassIter it{&p, &pinfo, s0, tb};
     it.begin(RT);
     bool ok = true;
-    int q = 0;          // job (chunk) counter of the ring
+    int q = 0;          // job counter of the ring (a job: one or two chunks)
     int prev_row0 = 0;  // first query row of the previous tile
     int last_use[kStages];
     for (int i = 0; i < kStages; ++i) last_use[i] = -1;
-    // one chunk into the ring: Q (src 0), Qp (1) or dY (2), latent chunk c
-    auto load_chunk = [&](int src, int c, int row0) -> bool {
+    // column statistics of a tile (two columns per lane) and its pass's token
+    // mapping, fetched one tile ahead so that their load latency overlaps the
+    // chunk copies of the tile before
+    float f_lse[2], f_dl[2];
+    int f_pos[2], f_info[4];
+    auto fetch = [&](const PassIter& x) {
+      const int row0 = x.r_begin + x.tile * RT;
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int c = lane + 32 * i;
+        const int r = row0 + c / p.G;
+        const bool in = r < x.r_end;
+        const int64_t idx = static_cast<int64_t>(in ? r : 0) * p.H + g * p.G + c % p.G;
+        f_lse[i] = in ? p.lse[idx] : -__int_as_float(0x7f800000);
+        f_dl[i] = in ? p.delta[idx] : 0.f;
+        f_pos[i] = in ? (p.causal ? p.q_pos[r] : 0x7fffffff) : -1;
+      }
+      f_info[0] = x.tbase;
+      f_info[1] = x.ra;
+      f_info[2] = x.rb;
+      f_info[3] = seq_len_of(p, x.seq);
+    };
+    fetch(it);
+    // one job into the ring: chunks c and c + 1 (nch = 2) or c alone of Q
+    // (src 0; chunk 8 is Qp) or dY (src 2)
+    auto load_job = [&](int src, int c, int nch, int row0) -> bool {
       const int s = q % kStages;
-      // stages are released in pairs (2j, 2j + 1) by one commit
-      if (q >= kStages && (q & 1) == 0 && !mbar_wait(&bar_empty[s >> 1], ((q / kStages) - 1) & 1, ab))
-        return false;
+      if (q >= kStages && !mbar_wait(&bar_empty[s], ((q / kStages) - 1) & 1, ab)) return false;
       if (lane == 0) {
-        mbar_arrive_expect_tx(&bar_full[s], QCH);
-        const CUtensorMap* m = src == 0 ? &tm_q : src == 1 ? &tm_qp : &tm_dy;
-        tma_load_3d(sm + RING_OFF + s * QCH, m, &bar_full[s], src == 1 ? 0 : c * 64, g * p.G, row0);
+        mbar_arrive_expect_tx(&bar_full[s], nch * QCH);
+        for (int k = 0; k < nch; ++k) {
+          const int cc = c + k;
+          const CUtensorMap* m = src == 2 ? &tm_dy : cc == 8 ? &tm_qp : &tm_q;
+          tma_load_3d(sm + RING_OFF + s * STAGE + k * QCH, m, &bar_full[s], cc == 8 ? 0 : cc * 64, g * p.G, row0);
+        }
       }
       last_use[s] = q;
       ++q;
       return true;
     };
+    // the accumulation jobs of a tile: dY chunks of the part in pairs, then
+    // its Q chunks in pairs (and Qp alone, PART 1)
+    auto load_acc = [&](int row0) -> bool {
+      for (int a = 0; a < PS::NACC; a += 2)
+        if (!load_job(a < 4 ? 2 : 0, acc_src_chunk<PART>(a), PS::NACC - a >= 2 ? 2 : 1, row0)) return false;
+      return true;
+    };
     for (int t = 0; t <= n && ok; ++t) {
       if (t < n) {
         const int row0 = it.r_begin + it.tile * RT;
-        // column statistics of tile t: -L2, delta, pos per column, plus the
-        // pass's token mapping
+        // column statistics of tile t: -L2, delta, pos per column (a row
+        // with lse = -inf sees no token), plus the pass's token mapping
         const int ss = t % kStatSlots;
         if (t >= kStatSlots && !(ok = mbar_wait(&bar_st_empty[ss], ((t / kStatSlots) - 1) & 1, ab))) break;
         uint8_t* st = sm + ST_OFF + ss * ST_SLOT;
@@ -207,49 +242,37 @@ __global__ void __launch_bounds__(384, 1)
         float* sdl = snl + BC;
         int* spos = reinterpret_cast<int*>(sdl + BC);
         int* sinfo = spos + BC;
-        for (int c = lane; c < BC; c += 32) {  // two columns per lane
-          const int r = row0 + c / p.G;
-          const int hh = g * p.G + c % p.G;
-          float nl2 = -__int_as_float(0x7f800000), dl = 0.f;
-          int pos = -1;
-          if (r < it.r_end) {
-            const float lse = p.lse[static_cast<int64_t>(r) * p.H + hh];
-            if (lse != -__int_as_float(0x7f800000)) {
-              nl2 = -lse * 1.4426950408889634f;
-              dl = p.delta[static_cast<int64_t>(r) * p.H + hh];
-              pos = p.causal ? p.q_pos[r] : 0x7fffffff;
-            }
-          }
-          snl[c] = nl2;
-          sdl[c] = dl;
-          spos[c] = pos;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int c = lane + 32 * i;
+          const bool live = f_lse[i] != -__int_as_float(0x7f800000);
+          snl[c] = live ? -f_lse[i] * 1.4426950408889634f : -__int_as_float(0x7f800000);
+          sdl[c] = live ? f_dl[i] : 0.f;
+          spos[c] = live ? f_pos[i] : -1;
         }
         if (lane == 0) {
-          sinfo[0] = it.tbase;
-          sinfo[1] = it.ra;
-          sinfo[2] = it.rb;
-          sinfo[3] = seq_len_of(p, it.seq);
+          sinfo[0] = f_info[0];
+          sinfo[1] = f_info[1];
+          sinfo[2] = f_info[2];
+          sinfo[3] = f_info[3];
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar_st_full[ss]);
+        PassIter nx = it;
+        if (t + 1 < n) {
+          nx.advance(RT);
+          fetch(nx);
+        }
         // S chunks of tile t (Q latent 0..7, Qp), the accumulation chunks of
         // tile t - 1, then the dP chunks of tile t (dY 0..7)
-        for (int c = 0; c < 9 && ok; ++c) ok = load_chunk(c < 8 ? 0 : 1, c, row0);
-        if (t >= 1) {
-          for (int a = 0; a < PS::NACC && ok; ++a) {
-            const int c = acc_src_chunk<PART>(a);
-            ok = load_chunk(a < 4 ? 2 : (c == 8 ? 1 : 0), c, prev_row0);
-          }
-        }
-        for (int c = 0; c < 8 && ok; ++c) ok = load_chunk(2, c, row0);
+        for (int c = 0; c < 9 && ok; c += 2) ok = load_job(0, c, c < 8 ? 2 : 1, row0);
+        if (t >= 1 && ok) ok = load_acc(prev_row0);
+        for (int c = 0; c < 8 && ok; c += 2) ok = load_job(2, c, 2, row0);
         if (!ok) break;
         prev_row0 = row0;
-        it.advance(RT);
+        it = nx;
       } else {
-        for (int a = 0; a < PS::NACC && ok; ++a) {
-          const int c = acc_src_chunk<PART>(a);
-          ok = load_chunk(a < 4 ? 2 : (c == 8 ? 1 : 0), c, prev_row0);
-        }
+        ok = load_acc(prev_row0);
       }
     }
     if (lane == 0) {
@@ -274,25 +297,27 @@ __global__ void __launch_bounds__(384, 1)
       if (mbar_test_warp(&bar_full[s], (qq / kStages) & 1)) return true;
       return mbar_wait_warp(&bar_full[s], (qq / kStages) & 1, ab);
     };
-    // after the job of ring index qq: the pair (qq - 1, qq) goes back to the
-    // producer once its products are done
-    auto release = [&](int qq) {
-      if (qq & 1) mma_commit_w(&bar_empty[(qq % kStages) >> 1]);
-    };
-    // S^T(t) (K_SEL 0) or dP^T(t) (1) over its chunks into tensor memory
+    // after the job of ring index qq: its stage goes back to the producer
+    // once its products are done
+    auto release = [&](int qq) { mma_commit_w(&bar_empty[qq % kStages]); };
+    // S^T(t) (kind 0, 9 chunks) or dP^T(t) (kind 1, 8 chunks) into tensor
+    // memory, two chunks per job
     auto xt_jobs = [&](int t, int kind) -> bool {
-      const int nj = kind == 0 ? 9 : 8;
+      const int nc = kind == 0 ? 9 : 8;
       const uint32_t d = tmem + (kind == 0 ? T_S + (t & 1) * BC : T_DP);
-      for (int c = 0; c < nj; ++c, ++q) {
+      for (int c0 = 0; c0 < nc; c0 += 2, ++q) {
         if (!wait_stage(q)) return false;
         tc_fence_after();
-        const uint64_t a = sdesc_add(dK0, c * KCH), bq = sdesc_add(dR0, (q % kStages) * QCH);
-        if (c == 0)
-          mma_ss_w<false>(d, a, bq, id_s);
-        else
-          mma_ss_w<true>(d, a, bq, id_s);
+        for (int k = 0; k < 2 && c0 + k < nc; ++k) {
+          const int c = c0 + k;
+          const uint64_t a = sdesc_add(dK0, c * KCH), bq = sdesc_add(dR0, (q % kStages) * STAGE + k * QCH);
+          if (c == 0)
+            mma_ss_w<false>(d, a, bq, id_s);
+          else
+            mma_ss_w<true>(d, a, bq, id_s);
 #pragma unroll
-        for (int kk = 1; kk < 4; ++kk) mma_ss_w<true>(d, sdesc_add(a, kk * 32), sdesc_add(bq, kk * 32), id_s);
+          for (int kk = 1; kk < 4; ++kk) mma_ss_w<true>(d, sdesc_add(a, kk * 32), sdesc_add(bq, kk * 32), id_s);
+        }
         release(q);
       }
       mma_commit_w(kind == 0 ? &bar_s_full[t & 1] : &bar_dp_full);
@@ -308,25 +333,29 @@ __global__ void __launch_bounds__(384, 1)
         const int u = t - 1;
         if (!(ok = mbar_wait_warp(&bar_p_full[u & 1], (u >> 1) & 1, ab))) break;
         tc_fence_after();
-        for (int a = 0; a < PS::NACC && ok; ++a, ++q) {
-          if (a == 4) {
+        for (int a0 = 0; a0 < PS::NACC && ok; a0 += 2, ++q) {
+          if (a0 == 4) {
             if (!(ok = mbar_wait_warp(&bar_ds_full, u & 1, ab))) break;
             tc_fence_after();
           }
           if (!(ok = wait_stage(q))) break;
           tc_fence_after();
-          const int c = acc_src_chunk<PART>(a);
-          const uint32_t d = tmem + T_ACC + (c - 4 * PART) * 64;  // chunk 8 (position) -> 256
-          const uint32_t at = tmem + (a < 4 ? T_S + (u & 1) * BC : T_DP);
-          const uint64_t bm = sdesc_add(dRm0, (q % kStages) * QCH);
-          // the first contribution to an accumulator chunk overwrites it:
-          // P^T dY for latent chunks, dS^T Qp for the position chunk
-          if (u == 0 && (a < 4 || c == 8))
-            mma_ts_w<false>(d, at, bm, id_acc);
-          else
-            mma_ts_w<true>(d, at, bm, id_acc);
+          for (int k = 0; k < 2 && a0 + k < PS::NACC; ++k) {
+            const int a = a0 + k;
+            const int c = acc_src_chunk<PART>(a);
+            const uint32_t d = tmem + T_ACC + (c - 4 * PART) * 64;  // chunk 8 (position) -> 256
+            const uint32_t at = tmem + (a < 4 ? T_S + (u & 1) * BC : T_DP);
+            const uint64_t bm = sdesc_add(dRm0, (q % kStages) * STAGE + k * QCH);
+            // the first contribution to an accumulator chunk overwrites it:
+            // P^T dY for latent chunks, dS^T Qp for the position chunk
+            if (u == 0 && (a < 4 || c == 8))
+              mma_ts_w<false>(d, at, bm, id_acc);
+            else
+              mma_ts_w<true>(d, at, bm, id_acc);
 #pragma unroll
-          for (int kk = 1; kk < BC / 16; ++kk) mma_ts_w<true>(d, at + kk * 8, sdesc_add(bm, kk * 16 * 128), id_acc);
+            for (int kk = 1; kk < BC / 16; ++kk)
+              mma_ts_w<true>(d, at + kk * 8, sdesc_add(bm, kk * 16 * 128), id_acc);
+          }
           release(q);
         }
         if (!ok) break;
