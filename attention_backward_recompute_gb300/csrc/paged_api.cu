@@ -119,6 +119,27 @@ bool encode3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64
   return attn::encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box);
 }
 
+// TMA maps of an MLA call: q, qp, dy as [Nq, H, D] addressed (d, h, r) with
+// box (64, G, rows), latent and position pools as [slots, KVH, D] with box
+// (64, 1, page_size)
+bool encode_mla_maps(attn::PagedMlaMaps* mm, const attn_paged_desc* d, int G, uint32_t rows, const void* q,
+                     const void* qp, const void* dy, const void* k_pool, const void* kp_pool) {
+  std::memset(mm, 0, sizeof(*mm));
+  const uint64_t slots = uint64_t(d->num_pages) * d->page_size;
+  bool enc = true;
+  if (d->num_queries > 0)
+    enc = encode3d(&mm->q, q, d->key_dim, d->heads, d->num_queries, 64, uint32_t(G), rows) &&
+          encode3d(&mm->qp, qp, d->position_dim, d->heads, d->num_queries, 64, uint32_t(G), rows) &&
+          encode3d(&mm->dy, dy, d->value_dim, d->heads, d->num_queries, 64, uint32_t(G), rows);
+  if (slots > 0)
+    enc = enc && encode3d(&mm->k, k_pool, d->key_dim, d->kv_heads, slots, 64, 1, uint32_t(d->page_size)) &&
+          encode3d(&mm->kp, kp_pool, d->position_dim, d->kv_heads, slots, 64, 1, uint32_t(d->page_size));
+  else
+    mm->k = mm->kp = mm->q;
+  if (d->num_queries == 0) mm->q = mm->qp = mm->dy = mm->k;
+  return enc;
+}
+
 }  // namespace
 
 extern "C" {
@@ -349,6 +370,19 @@ ATTN_API attn_status_t attn_paged_row_stats(const attn_paged_desc* d, const void
   if ((st = fill_params(d, z, page_table, seq_meta, workspace, &p)) != ATTN_OK) return st;
   p.lse_out = lse;
   p.delta_out = delta;
+  if (mla && attn::mla_stats_tc_supported(p)) {
+    // tcgen05: 128 columns (128/G rows) per CTA
+    attn::PagedMlaMaps mt;
+    if (!encode_mla_maps(&mt, d, p.G, 128u / uint32_t(p.G), q, qp, dy, k_pool, kp_pool))
+      return api_fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    attn::timing_mark_begin(1, s);
+    cudaError_t e = attn::launch_paged_mla_stats_tc(mt, p, s);
+    attn::timing_mark(s);
+    attn::timing_mark_end();
+    if (e != cudaSuccess) return api_fail(ATTN_ERR_CUDA, "row-statistics launch failed: %s", cudaGetErrorString(e));
+    return api_ok();
+  }
   if (mla && attn::mla_mma_supported(p)) {
     attn::PagedMlaMaps mm;
     std::memset(&mm, 0, sizeof(mm));
@@ -457,8 +491,13 @@ ATTN_API attn_status_t attn_bwd_paged_query(const attn_paged_desc* d, const void
       mm.k = mm.kp = mm.q;
     if (!enc) return api_fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // row statistics on tcgen05 (128 columns per CTA) where it applies
+    attn::PagedMlaMaps mt;
+    const bool stats_tc = attn::mla_stats_tc_supported(p);
+    if (stats_tc && !encode_mla_maps(&mt, d, p.G, 128u / G, q, qp, dy, k_pool, kp_pool))
+      return api_fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed");
     attn::timing_mark_begin(3, s);
-    cudaError_t e = attn::launch_paged_mla_stats_mma(mm, p, s);
+    cudaError_t e = stats_tc ? attn::launch_paged_mla_stats_tc(mt, p, s) : attn::launch_paged_mla_stats_mma(mm, p, s);
     attn::timing_mark(s);
     if (e == cudaSuccess) e = attn::launch_paged_mla_query_mma(mm, p, s);
     attn::timing_mark(s);
