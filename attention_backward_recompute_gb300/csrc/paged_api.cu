@@ -471,9 +471,11 @@ ATTN_API attn_status_t attn_bwd_paged_query(const attn_paged_desc* d, const void
   p.delta_out = delta;
   p.dq = dq;
   if (mla) {
-    // row statistics, then dQ / dQp from them, on the warp-level tensor path
-    if (!attn::mla_mma_supported(p))
-      return api_fail(ATTN_ERR_UNSUPPORTED, "MLA query side needs heads / kv_heads in {4, 8, 16, 32} and page 16");
+    // row statistics, then dQ / dQp from them (tcgen05; the warp-level
+    // tensor path for shapes the tcgen05 kernels do not take)
+    const bool tc = attn::mla_stats_tc_supported(p) && attn::mla_query_tc_supported(p);
+    if (!tc && !attn::mla_mma_supported(p))
+      return api_fail(ATTN_ERR_UNSUPPORTED, "MLA query side needs heads / kv_heads dividing 64 and page 16");
     p.dqp = dqp;
     p.lse = lse;
     p.delta = delta;
@@ -493,13 +495,13 @@ ATTN_API attn_status_t attn_bwd_paged_query(const attn_paged_desc* d, const void
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // row statistics on tcgen05 (128 columns per CTA) where it applies
     attn::PagedMlaMaps mt;
-    const bool stats_tc = attn::mla_stats_tc_supported(p);
+    const bool stats_tc = tc;
     if (stats_tc && !encode_mla_maps(&mt, d, p.G, 128u / G, q, qp, dy, k_pool, kp_pool))
       return api_fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed");
     attn::timing_mark_begin(3, s);
     cudaError_t e = stats_tc ? attn::launch_paged_mla_stats_tc(mt, p, s) : attn::launch_paged_mla_stats_mma(mm, p, s);
     attn::timing_mark(s);
-    if (e == cudaSuccess) e = attn::launch_paged_mla_query_mma(mm, p, s);
+    if (e == cudaSuccess) e = tc ? attn::launch_paged_mla_query_tc(mm, p, s) : attn::launch_paged_mla_query_mma(mm, p, s);
     attn::timing_mark(s);
     if (e == cudaSuccess) e = attn::launch_paged_query_outside(p, s);
     attn::timing_mark(s);

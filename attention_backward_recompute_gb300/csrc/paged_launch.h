@@ -59,6 +59,9 @@ cudaError_t launch_paged_mla_tc_pair_heavy(const PagedParams& p, cudaStream_t s)
 // MLA row statistics on tcgen05; q, qp, dy maps with box (64, G, 128/G)
 bool mla_stats_tc_supported(const PagedParams& p);
 cudaError_t launch_paged_mla_stats_tc(const PagedMlaMaps& m, const PagedParams& p, cudaStream_t s);
+// MLA query side (dQ, dQp) on tcgen05 from lse / delta; maps with box (64, G, 64/G)
+bool mla_query_tc_supported(const PagedParams& p);
+cudaError_t launch_paged_mla_query_tc(const PagedMlaMaps& m, const PagedParams& p, cudaStream_t s);
 cudaError_t launch_paged_mla_stats(const PagedParams& p, const void* q, const void* qp, const void* dy,
                                    const void* k_pool, const void* kp_pool, cudaStream_t s);
 
