@@ -265,7 +265,7 @@ ATTN_API attn_status_t attn_bwd_paged_compact(const attn_paged_desc* d, const vo
     attn::timing_mark(s);
     if (split && e == cudaSuccess) e = attn::launch_paged_mla_mma_split(mm, p, s);
     attn::timing_mark(s);
-    if (e == cudaSuccess) e = attn::launch_paged_mla_tc(mt, p, s);
+    if (e == cudaSuccess) e = attn::launch_paged_mla_tc(mt, p, split, s);
     attn::timing_mark(s);
     attn::timing_mark_end();
     if (e != cudaSuccess) return api_fail(ATTN_ERR_CUDA, "paged launch failed: %s", cudaGetErrorString(e));

@@ -52,7 +52,9 @@ cudaError_t launch_paged_mla_query_mma(const PagedMlaMaps& m, const PagedParams&
 // half of the dims); blocks with a heavy 64-token half (p.heavy, when not
 // null) are left to the cluster-split kernel
 bool mla_tc_supported(const PagedParams& p);
-cudaError_t launch_paged_mla_tc(const PagedMlaMaps& m, const PagedParams& p, cudaStream_t s);
+// after_split: the cluster-split kernel was launched just before (the first
+// part then starts as its programmatic dependent)
+cudaError_t launch_paged_mla_tc(const PagedMlaMaps& m, const PagedParams& p, bool after_split, cudaStream_t s);
 // extends the heavy flags of the split plan to both 64-token halves of a
 // 128-token block
 cudaError_t launch_paged_mla_tc_pair_heavy(const PagedParams& p, cudaStream_t s);

@@ -104,6 +104,14 @@ __global__ void __launch_bounds__(384, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = blockIdx.x, tb = blockIdx.y, s0 = blockIdx.z;
+  // Launched as the programmatic dependent of the kernel before it (the
+  // cluster-split kernel, or PART 0 for PART 1), whose results it does not
+  // read: its own dependent may start at once, and the last CTA waits for the
+  // kernel before, so that this grid completes after it and later work in
+  // the stream sees both.  Without a programmatic launch both are no-ops.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (blockIdx.x == gridDim.x - 1 && blockIdx.y == gridDim.y - 1 && blockIdx.z == gridDim.z - 1)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
   const int len0 = seq_len_of(p, s0);
   const int npg = pages_of(len0, p.page_size);
   if (tb * 8 >= npg) return;  // no token of this sequence in the block (uniform exit)
@@ -504,16 +512,24 @@ __global__ void __launch_bounds__(384, 1)
 }
 
 template <int PART>
-cudaError_t launch_part(const PagedMlaMaps& m, const PagedParams& p, cudaStream_t s) {
+cudaError_t launch_part(const PagedMlaMaps& m, const PagedParams& p, bool dependent, cudaStream_t s) {
   auto kern = mla_tc_kernel<PART>;
   const int smem = BYTES + 1024;
   static_assert(BYTES + 1024 >= kSmemOneCtaPerSm, "all 512 TMEM columns: one CTA per SM");
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int nblk = (p.max_pages * p.page_size + BT - 1) / BT;
-  dim3 grid(p.KVH, nblk, p.S);
-  kern<<<grid, 384, smem, s>>>(m.q, m.qp, m.dy, m.k, m.kp, p);
-  return cudaGetLastError();
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.KVH, nblk, p.S);
+  cfg.blockDim = dim3(384, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = dependent ? at : nullptr;
+  cfg.numAttrs = dependent ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, m.q, m.qp, m.dy, m.k, m.kp, p);
 }
 
 // heavy[] is planned per 64-token block; a 128-token block of this kernel
@@ -545,10 +561,12 @@ cudaError_t launch_paged_mla_tc_pair_heavy(const PagedParams& p, cudaStream_t s)
   return cudaGetLastError();
 }
 
-cudaError_t launch_paged_mla_tc(const PagedMlaMaps& m, const PagedParams& p, cudaStream_t s) {
+cudaError_t launch_paged_mla_tc(const PagedMlaMaps& m, const PagedParams& p, bool after_split, cudaStream_t s) {
   if (p.num_pages == 0 || p.S == 0 || p.max_pages == 0) return cudaSuccess;
-  cudaError_t e = launch_part<0>(m, p, s);
-  if (e == cudaSuccess) e = launch_part<1>(m, p, s);
+  // PART 0 overlaps the cluster-split kernel's tail (when that kernel runs
+  // just before it), PART 1 overlaps PART 0's tail
+  cudaError_t e = launch_part<0>(m, p, after_split, s);
+  if (e == cudaSuccess) e = launch_part<1>(m, p, true, s);
   return e;
 }
 
