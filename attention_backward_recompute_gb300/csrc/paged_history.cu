@@ -6,24 +6,29 @@
 // over the query heads of the KV group:
 //   p  = exp(q.k * scale - lse),  ds = p * (dY.v - delta) * scale
 //   dK += ds * q,   dV += p * dY
-// Here one CTA owns 128 tokens (eight 16-token pages) of one sequence and one
-// KV head and does the same sums as tile products on tcgen05:
+// A work item is 128 tokens (eight 16-token pages) of one sequence and one KV
+// head; the same sums are tile products on tcgen05:
 //   S^T  = K_T Q_c^T,  dP^T = V_T dY_c^T            (M=128 tokens, N=64 columns)
-//   P^T  = exp2(S^T scale log2e - lse log2e)        softmax warpgroups
-//   dS^T = P^T (dP^T - delta)                        dS warpgroup
+//   P^T  = exp2(S^T scale log2e - lse log2e)        written over S^T as bf16
+//   dS^T = P^T (dP^T - delta)                        written over dP^T as bf16
 //   dV_T += P^T dY_c,  dK_T += dS^T Q_c              (A operand from tensor memory)
 // where a column c is one (query row, head of the group) pair.  The K/V tile is
 // gathered page by page with TMA (3-D map over [slots, KVH, D]); pages past the
 // sequence are fetched at an out-of-range coordinate, i.e. read as zeros
-// without touching memory.  Passes: the CTA's own sequence first, then the
+// without touching memory.  Passes: the item's own sequence first, then the
 // other links of the pages it stores, by link index; consecutive pages linked
 // from consecutive logical pages of one sequence share a pass (a shared prefix
 // costs one pass per (sequence, block), not one per page).
 //
-// Roles (512 threads): warp 0 TMA producer (K/V pages once, then Q/dY column
-// tiles through a 4-stage ring with the columns' statistics), warp 1 MMA
-// issuer (whole warp, elect.sync), warps 4..7 / 12..15 softmax of even / odd
-// tiles (one per double-buffered S^T), warps 8..11 dS.
+// The kernel is persistent (one CTA per SM over the items, in a snake order):
+// a scheduler warp works out each item's pages, links and tile count ahead of
+// time into a two-slot item ring, so that the next item's K/V gather and first
+// products overlap the previous item's last tiles and epilogue.
+// Roles (384 threads): warp 0 TMA producer (K/V pages per item, Q/dY column
+// tiles through a 4-stage ring with the columns' statistics, fetched one tile
+// ahead), warp 1 MMA issuer (whole warp, elect.sync), warp 2 item scheduler,
+// warps 4..7 / 8..11 compute groups for even / odd tiles (each forms P and
+// then dS of its tiles; group 0 stores dV, group 1 dK).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -49,12 +54,19 @@ struct HistLayout {
   static constexpr int V_OFF = K_OFF + KV;
   static constexpr int Q_OFF = V_OFF + KV;             // kStages
   static constexpr int DY_OFF = Q_OFF + kStages * QT;  // kStages
-  static constexpr int ST_OFF = DY_OFF + kStages * QT; // kStages x {L2, delta, pos} x 64 + pass info
+  static constexpr int ST_OFF = DY_OFF + kStages * QT; // kStages x {-L2, delta, pos} x 64 + pass info
   static constexpr int ST_STAGE = 3 * BC * 4 + 16;
   static constexpr int BYTES = ST_OFF + kStages * ST_STAGE;
   // TMEM: dV [0, DP), dK [DP, 2DP), S^T[2] and dP^T[2] 64 columns each
   static constexpr int T_S = 2 * DP, T_DP = 2 * DP + 128;
   static constexpr int TMEM_COLS = 512;
+};
+
+// One slot of the item ring: the item's pages and links, its tile count over
+// all passes (n = -1: no more items).
+struct ItemSlot {
+  PageInfo pi;
+  int s0, tb, g, n;
 };
 
 __device__ __forceinline__ bool drain_wait(uint64_t* bar, uint32_t parity) {
@@ -65,109 +77,50 @@ __device__ __forceinline__ bool drain_wait(uint64_t* bar, uint32_t parity) {
   return true;
 }
 
-// Registers written by tcgen05.ld are valid only after tcgen05.wait::ld; this
-// empty asm ties every later use of r to a point after the wait.
-__device__ __forceinline__ void reg_fence16(uint32_t (&r)[16]) {
-#pragma unroll
-  for (int i = 0; i < 16; ++i) asm volatile("" : "+r"(r[i]));
-}
-
-// P^T row of one token over the 64 columns of a tile, S^T read from tensor
-// memory in four 16-column chunks (the next chunk's load in flight); chunk i's
-// 8 bf16 pairs go to columns [8i, 8i+8) of the same buffer.  A column is
-// visible when the token is live and tok <= pos[c] (pos = -1 for a column
-// without visible history).
-__device__ __forceinline__ void p_row_paged(uint32_t tS, const float* l2s, const int* poss, bool tok_ok, int tok,
-                                            float scale_log2) {
-  uint32_t s0[16], s1[16], pw[8];
-  tmem_ld16(tS, s0);
-  tmem_ld_wait();
-  reg_fence16(s0);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    uint32_t(&cur)[16] = (i & 1) ? s1 : s0;
-    uint32_t(&nxt)[16] = (i & 1) ? s0 : s1;
-    if (i < 3) tmem_ld16(tS + 16 * (i + 1), nxt);
-#pragma unroll
-    for (int c4 = 0; c4 < 4; ++c4) {
-      const int c0 = 16 * i + 4 * c4;
-      const float4 l2 = *reinterpret_cast<const float4*>(l2s + c0);
-      const int4 ps = *reinterpret_cast<const int4*>(poss + c0);
-      const float l2v[4] = {l2.x, l2.y, l2.z, l2.w};
-      const int pv4[4] = {ps.x, ps.y, ps.z, ps.w};
-      float pv[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float x = fmaf(__uint_as_float(cur[4 * c4 + e]), scale_log2, -l2v[e]);
-        const float pe = ex2_approx(x);
-        pv[e] = (tok_ok && tok <= pv4[e]) ? pe : 0.f;
-      }
-      pw[2 * c4] = pack_bf16x2(pv[0], pv[1]);
-      pw[2 * c4 + 1] = pack_bf16x2(pv[2], pv[3]);
-    }
-    tmem_st8(tS + 8 * i, pw);
-    if (i < 3) {
-      tmem_ld_wait();
-      reg_fence16(nxt);
-    }
-  }
-}
+__device__ __forceinline__ float4 lds_f4(const float* p) { return *reinterpret_cast<const float4*>(p); }
 
 template <int DP>
-__global__ void __launch_bounds__(512, 1)
+__global__ void __launch_bounds__(384, 1)
     paged_history_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_dy,
                          const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                          const PagedParams p) {
   using L = HistLayout<DP>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t bar_kv, bar_full[kStages], bar_empty[kStages], bar_s_full[2], bar_dp_full[2], bar_p_full[2],
-      bar_p_read[2], bar_ds_full[2], bar_acc;
+  // bar_kv / bar_kv_free / bar_acc / bar_acc_free: phases count items with
+  // tiles (as in the dense persistent kernel); bar_item_*: every item
+  __shared__ uint64_t bar_item_full[2], bar_item_empty[2], bar_kv, bar_kv_free, bar_full[kStages],
+      bar_empty[kStages], bar_s_full[2], bar_dp_full[2], bar_p_full[2], bar_ds_full[2], bar_acc, bar_acc_free;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
-  __shared__ PageInfo pinfo;
-  __shared__ int n_steps_sh, any_store_sh;
+  __shared__ ItemSlot items[2];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // the KV heads of one token block are neighbours in the grid: together they
-  // read (and write) whole slot rows of the same pages
-  const int g = blockIdx.x, tb = blockIdx.y, s0 = blockIdx.z;
-  const int len0 = seq_len_of(p, s0);
-  const int npg = pages_of(len0, p.page_size);
-  if (tb * 8 >= npg) return;  // no token of this sequence in the block (uniform exit)
   const int RT = L::BC / p.G;  // query rows per step
   const Abort ab{&abort_flag, p.err};
+  const int nblk = (p.max_pages * p.page_size + 127) / 128;
+  const int total = p.KVH * nblk * p.S;
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bar_item_full[s], 1);
+      mbar_init(&bar_item_empty[s], 10);  // producer, MMA warp, 8 compute warps
+      mbar_init(&bar_s_full[s], 1);
+      mbar_init(&bar_dp_full[s], 1);
+      mbar_init(&bar_p_full[s], 4);
+      mbar_init(&bar_ds_full[s], 4);
+    }
     mbar_init(&bar_kv, 1);
+    mbar_init(&bar_kv_free, 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&bar_full[s], 2);  // TMA bytes + column statistics written
       mbar_init(&bar_empty[s], 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&bar_s_full[s], 1);
-      mbar_init(&bar_dp_full[s], 1);
-      mbar_init(&bar_p_full[s], 4);
-      mbar_init(&bar_p_read[s], 4);
-      mbar_init(&bar_ds_full[s], 4);
-    }
     mbar_init(&bar_acc, 1);
+    mbar_init(&bar_acc_free, 8);
     mbar_fence_init();
-    any_store_sh = fill_page_info(p, s0, tb, npg, &pinfo);
-    // number of steps over all passes
-    PassIter it{&p, &pinfo, s0, tb};
-    int n = 0;
-    if (it.begin(RT)) {
-      do ++n;
-      while (it.advance(RT));
-    }
-    n_steps_sh = n;
   }
-  __syncthreads();
-  // a block whose pages are all stored by other CTAs (their owners) has
-  // nothing to write: leave before taking tensor memory (uniform exit)
-  if (!any_store_sh) return;
   if (warp == 1) {
     tmem_alloc(&tmem_base_sh, L::TMEM_COLS);
     tmem_relinquish();
@@ -177,202 +130,333 @@ __global__ void __launch_bounds__(512, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
   const uint32_t t_dv = tmem, t_dk = tmem + DP;
-  const int n = n_steps_sh;
   const int oob_slot = p.num_pages * p.page_size;  // out-of-range coordinate: TMA fills zeros
 
-  if (n > 0 && warp == 0) {
+  // every role but the scheduler walks the item ring in order
+  auto item_wait = [&](int ii) -> bool {
+    return mbar_wait_warp(&bar_item_full[ii & 1], (ii >> 1) & 1, ab);
+  };
+  auto item_done = [&](int ii) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&bar_item_empty[ii & 1]);
+  };
+
+  if (warp == 2) {
+    // ------------------------------------------------------------ item scheduler
+    // the CTA's items: index r*G + c (r*G + G-1-c in odd rounds), KV head
+    // fastest, so that the heads of one block of pages run side by side
+    int ii = 0;
+    bool ok = true;
+    for (int r = 0; ok; ++r) {
+      const int base = r * static_cast<int>(gridDim.x);
+      int idx = base + ((r & 1) ? static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x)
+                                : static_cast<int>(blockIdx.x));
+      const bool last_round = base + static_cast<int>(gridDim.x) >= total;
+      if (base >= total) break;
+      if (idx < total) {
+        const int g = idx % p.KVH, tb = (idx / p.KVH) % nblk, s0 = idx / (p.KVH * nblk);
+        const int npg = pages_of(seq_len_of(p, s0), p.page_size);
+        if (tb * 8 < npg) {
+          if (ii >= 2 && !(ok = mbar_wait_warp(&bar_item_empty[ii & 1], ((ii >> 1) - 1) & 1, ab))) break;
+          ItemSlot& it = items[ii & 1];
+          int any = 0;
+          if (lane == 0) any = fill_page_info(p, s0, tb, npg, &it.pi);
+          any = __shfl_sync(0xffffffffu, any, 0);
+          // a block whose pages are all stored by other items (their owners)
+          // has nothing to write
+          if (any) {
+            if (lane == 0) {
+              PassIter pit{&p, &it.pi, s0, tb};
+              int n = 0;
+              if (pit.begin(RT)) {
+                do ++n;
+                while (pit.advance(RT));
+              }
+              it.s0 = s0;
+              it.tb = tb;
+              it.g = g;
+              it.n = n;
+              mbar_arrive(&bar_item_full[ii & 1]);
+            }
+            __syncwarp();
+            ++ii;
+          }
+        }
+      }
+      if (last_round) break;
+    }
+    // end marker
+    if (ok && (ii < 2 || mbar_wait_warp(&bar_item_empty[ii & 1], ((ii >> 1) - 1) & 1, ab))) {
+      if (lane == 0) {
+        items[ii & 1].n = -1;
+        mbar_arrive(&bar_item_full[ii & 1]);
+      }
+    }
+  } else if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       tma_prefetch_map(&tm_q);
       tma_prefetch_map(&tm_dy);
       tma_prefetch_map(&tm_k);
       tma_prefetch_map(&tm_v);
-      mbar_arrive_expect_tx(&bar_kv, 2 * L::KV);
-      for (int j = 0; j < 8; ++j) {
-        const int slot = pinfo.phys[j] >= 0 ? pinfo.phys[j] * p.page_size : oob_slot;
-        for (int c = 0; c < L::NCH; ++c) {
-          tma_load_3d(sm + L::K_OFF + c * (L::BT * 128) + j * 16 * 128, &tm_k, &bar_kv, c * 64, g, slot);
-          tma_load_3d(sm + L::V_OFF + c * (L::BT * 128) + j * 16 * 128, &tm_v, &bar_kv, c * 64, g, slot);
-        }
-      }
     }
-    PassIter it{&p, &pinfo, s0, tb};
-    it.begin(RT);
     int last_use[kStages];
     for (int i = 0; i < kStages; ++i) last_use[i] = -1;
     bool ok = true;
-    for (int t = 0; t < n && ok; ++t) {
-      const int s = t % kStages;
-      if (t >= kStages) ok = mbar_wait_warp(&bar_empty[s], ((t / kStages) - 1) & 1, ab);
-      if (!ok) break;
-      const int row0 = it.r_begin + it.tile * RT;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&bar_full[s], 2 * L::QT);
-        for (int c = 0; c < L::NCH; ++c) {
-          tma_load_3d(sm + L::Q_OFF + s * L::QT + c * (L::BC * 128), &tm_q, &bar_full[s], c * 64, g * p.G, row0);
-          tma_load_3d(sm + L::DY_OFF + s * L::QT + c * (L::BC * 128), &tm_dy, &bar_full[s], c * 64, g * p.G, row0);
-        }
-      }
-      uint8_t* st = sm + L::ST_OFF + s * L::ST_STAGE;
-      float* sl2 = reinterpret_cast<float*>(st);
-      float* sdl = sl2 + L::BC;
-      int* spos = reinterpret_cast<int*>(sdl + L::BC);
-      int* sinfo = spos + L::BC;
-      for (int c = lane; c < L::BC; c += 32) {
+    int gt = 0, lv = 0;  // global tile counter, items with tiles
+    // column statistics of a tile (two columns per lane) and its pass's token
+    // mapping, fetched one tile ahead
+    float f_lse[2], f_dl[2];
+    int f_pos[2], f_info[4];
+    auto fetch = [&](const PassIter& x, int g) {
+      const int row0 = x.r_begin + x.tile * RT;
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int c = lane + 32 * i;
         const int r = row0 + c / p.G;
-        const int hh = g * p.G + c % p.G;
-        const bool in = r < it.r_end;
-        float l2 = __int_as_float(0x7f800000), dl = 0.f;
-        int pos = -1;
-        if (in) {
-          const float lse = p.lse[static_cast<int64_t>(r) * p.H + hh];
-          if (lse != -__int_as_float(0x7f800000)) {
-            l2 = lse * 1.4426950408889634f;
-            dl = p.delta[static_cast<int64_t>(r) * p.H + hh];
-            pos = p.causal ? p.q_pos[r] : 0x7fffffff;
+        const bool in = r < x.r_end;
+        const int64_t idx = static_cast<int64_t>(in ? r : 0) * p.H + g * p.G + c % p.G;
+        f_lse[i] = in ? p.lse[idx] : -__int_as_float(0x7f800000);
+        f_dl[i] = in ? p.delta[idx] : 0.f;
+        f_pos[i] = in ? (p.causal ? p.q_pos[r] : 0x7fffffff) : -1;
+      }
+      f_info[0] = x.tbase;
+      f_info[1] = x.ra;
+      f_info[2] = x.rb;
+      f_info[3] = seq_len_of(p, x.seq);
+    };
+    for (int ii = 0; ok; ++ii) {
+      if (!(ok = item_wait(ii))) break;
+      const ItemSlot& it = items[ii & 1];
+      const int n = it.n;
+      if (n < 0) break;
+      if (n > 0) {
+        const int g = it.g;
+        if (lv > 0 && !(ok = mbar_wait(&bar_kv_free, (lv - 1) & 1, ab))) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&bar_kv, 2 * L::KV);
+          for (int j = 0; j < 8; ++j) {
+            const int slot = it.pi.phys[j] >= 0 ? it.pi.phys[j] * p.page_size : oob_slot;
+            for (int c = 0; c < L::NCH; ++c) {
+              tma_load_3d(sm + L::K_OFF + c * (L::BT * 128) + j * 16 * 128, &tm_k, &bar_kv, c * 64, g, slot);
+              tma_load_3d(sm + L::V_OFF + c * (L::BT * 128) + j * 16 * 128, &tm_v, &bar_kv, c * 64, g, slot);
+            }
           }
         }
-        sl2[c] = l2;
-        sdl[c] = dl;
-        spos[c] = pos;
+        PassIter pit{&p, &it.pi, it.s0, it.tb};
+        pit.begin(RT);
+        fetch(pit, g);
+        for (int t = 0; t < n && ok; ++t) {
+          const int gg = gt + t, s = gg % kStages;
+          if (gg >= kStages && !(ok = mbar_wait(&bar_empty[s], ((gg / kStages) - 1) & 1, ab))) break;
+          const int row0 = pit.r_begin + pit.tile * RT;
+          if (lane == 0) {
+            mbar_arrive_expect_tx(&bar_full[s], 2 * L::QT);
+            for (int c = 0; c < L::NCH; ++c) {
+              tma_load_3d(sm + L::Q_OFF + s * L::QT + c * (L::BC * 128), &tm_q, &bar_full[s], c * 64, g * p.G, row0);
+              tma_load_3d(sm + L::DY_OFF + s * L::QT + c * (L::BC * 128), &tm_dy, &bar_full[s], c * 64, g * p.G,
+                          row0);
+            }
+          }
+          uint8_t* st = sm + L::ST_OFF + s * L::ST_STAGE;
+          float* snl = reinterpret_cast<float*>(st);
+          float* sdl = snl + L::BC;
+          int* spos = reinterpret_cast<int*>(sdl + L::BC);
+          int* sinfo = spos + L::BC;
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            const int c = lane + 32 * i;
+            const bool live = f_lse[i] != -__int_as_float(0x7f800000);
+            snl[c] = live ? -f_lse[i] * 1.4426950408889634f : -__int_as_float(0x7f800000);
+            sdl[c] = live ? f_dl[i] : 0.f;
+            spos[c] = live ? f_pos[i] : -1;
+          }
+          if (lane == 0) {
+            sinfo[0] = f_info[0];
+            sinfo[1] = f_info[1];
+            sinfo[2] = f_info[2];
+            sinfo[3] = f_info[3];
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bar_full[s]);
+          last_use[s] = gg;
+          if (t + 1 < n) {
+            pit.advance(RT);
+            fetch(pit, g);
+          }
+        }
+        gt += n;
+        ++lv;
       }
-      if (lane == 0) {
-        sinfo[0] = it.tbase;
-        sinfo[1] = it.ra;
-        sinfo[2] = it.rb;
-        sinfo[3] = seq_len_of(p, it.seq);
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar_full[s]);
-      last_use[s] = t;
-      it.advance(RT);
+      item_done(ii);
     }
     if (lane == 0) {
       for (int s = 0; s < kStages; ++s)
         if (last_use[s] >= 0) drain_wait(&bar_full[s], (last_use[s] / kStages) & 1);
-      drain_wait(&bar_kv, 0);
+      if (lv > 0) drain_wait(&bar_kv, (lv - 1) & 1);
     }
-  } else if (n > 0 && warp == 1) {
+  } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     // the whole warp runs this role (warp-uniform); elected lanes issue
-    {
-      constexpr uint32_t id_s = idesc_bf16(128, 64, false, false);
-      constexpr uint32_t id_acc = idesc_bf16(128, DP, false, true);
-      const uint64_t dK = sdesc_sw128(smem_addr(sm + L::K_OFF), 16, 1024);
-      const uint64_t dV = sdesc_sw128(smem_addr(sm + L::V_OFF), 16, 1024);
-      const uint64_t dQ0 = sdesc_sw128(smem_addr(sm + L::Q_OFF), 16, 1024);
-      const uint64_t dDY0 = sdesc_sw128(smem_addr(sm + L::DY_OFF), 16, 1024);
-      const uint64_t dQm0 = sdesc_sw128(smem_addr(sm + L::Q_OFF), L::BC * 128, 1024);    // MN-major
-      const uint64_t dDYm0 = sdesc_sw128(smem_addr(sm + L::DY_OFF), L::BC * 128, 1024);  // MN-major
-      // D[128 x 64] = A[128 x DP] * B[64 x DP]^T, both from shared memory, K-major
-      auto issue_xt = [&](uint32_t d, uint64_t a, uint64_t bq) {
-        mma_ss_w<false>(d, a, bq, id_s);
+    constexpr uint32_t id_s = idesc_bf16(128, 64, false, false);
+    constexpr uint32_t id_acc = idesc_bf16(128, DP, false, true);
+    const uint64_t dK = sdesc_sw128(smem_addr(sm + L::K_OFF), 16, 1024);
+    const uint64_t dV = sdesc_sw128(smem_addr(sm + L::V_OFF), 16, 1024);
+    const uint64_t dQ0 = sdesc_sw128(smem_addr(sm + L::Q_OFF), 16, 1024);
+    const uint64_t dDY0 = sdesc_sw128(smem_addr(sm + L::DY_OFF), 16, 1024);
+    const uint64_t dQm0 = sdesc_sw128(smem_addr(sm + L::Q_OFF), L::BC * 128, 1024);    // MN-major
+    const uint64_t dDYm0 = sdesc_sw128(smem_addr(sm + L::DY_OFF), L::BC * 128, 1024);  // MN-major
+    // D[128 x 64] = A[128 x DP] * B[64 x DP]^T, both from shared memory, K-major
+    auto issue_xt = [&](uint32_t d, uint64_t a, uint64_t bq) {
+      mma_ss_w<false>(d, a, bq, id_s);
 #pragma unroll
-        for (int kk = 1; kk < DP / 16; ++kk) {
-          const int c = kk >> 2, o = (kk & 3) * 32;
-          mma_ss_w<true>(d, sdesc_add(a, c * (L::BT * 128) + o), sdesc_add(bq, c * (L::BC * 128) + o), id_s);
-        }
-      };
-      // D[128 x DP] (+)= A[128 x 64] (tensor memory, bf16 pairs) * B[64 x DP] (MN-major)
-      auto issue_acc = [&](uint32_t d, uint32_t a_tmem, uint64_t bm, bool first) {
-        if (first)
-          mma_ts_w<false>(d, a_tmem, bm, id_acc);
-        else
-          mma_ts_w<true>(d, a_tmem, bm, id_acc);
-#pragma unroll
-        for (int kk = 1; kk < L::BC / 16; ++kk) mma_ts_w<true>(d, a_tmem + kk * 8, sdesc_add(bm, kk * 16 * 128), id_acc);
-      };
-      auto issue_s = [&](int t) {
-        issue_xt(tmem + L::T_S + (t & 1) * 64, dK, sdesc_add(dQ0, (t % kStages) * L::QT));
-        mma_commit_w(&bar_s_full[t & 1]);
-      };
-      auto issue_dp = [&](int t) {
-        issue_xt(tmem + L::T_DP + (t & 1) * 64, dV, sdesc_add(dDY0, (t % kStages) * L::QT));
-        mma_commit_w(&bar_dp_full[t & 1]);
-      };
-      bool ok = mbar_wait_warp(&bar_kv, 0, ab);
-      for (int t = 0; t < 2 && t < n && ok; ++t) {
-        if (!(ok = mbar_wait_warp(&bar_full[t], 0, ab))) break;
-        tc_fence_after();
-        issue_s(t);
-        issue_dp(t);
+      for (int kk = 1; kk < DP / 16; ++kk) {
+        const int c = kk >> 2, o = (kk & 3) * 32;
+        mma_ss_w<true>(d, sdesc_add(a, c * (L::BT * 128) + o), sdesc_add(bq, c * (L::BC * 128) + o), id_s);
       }
-      // Issue order per tile t: dV(t), S(t+2), dK(t), dP(t+2) (as in the dense
-      // dK/dV kernel): S(t+2) overwrites P^T(t) once dV(t) (earlier in the
-      // pipe) and the dS warpgroup (p_read) have consumed it; dP(t+2)
-      // overwrites dS^T(t), read by dK(t) just before it.
-      for (int t = 0; t < n && ok; ++t) {
-        const int s = t % kStages, bb = t & 1;
-        if (!(ok = mbar_wait_warp(&bar_p_full[bb], (t >> 1) & 1, ab))) break;
-        tc_fence_after();
-        issue_acc(t_dv, tmem + L::T_S + bb * 64, sdesc_add(dDYm0, s * L::QT), t == 0);
-        if (t + 2 < n) {
-          if (!(ok = mbar_wait_warp(&bar_full[(t + 2) % kStages], ((t + 2) / kStages) & 1, ab))) break;
-          if (!(ok = mbar_wait_warp(&bar_p_read[bb], (t >> 1) & 1, ab))) break;
+    };
+    // D[128 x DP] (+)= A[128 x 64] (tensor memory, bf16 pairs) * B[64 x DP] (MN-major)
+    auto issue_acc = [&](uint32_t d, uint32_t a_tmem, uint64_t bm, bool first) {
+      if (first)
+        mma_ts_w<false>(d, a_tmem, bm, id_acc);
+      else
+        mma_ts_w<true>(d, a_tmem, bm, id_acc);
+#pragma unroll
+      for (int kk = 1; kk < L::BC / 16; ++kk) mma_ts_w<true>(d, a_tmem + kk * 8, sdesc_add(bm, kk * 16 * 128), id_acc);
+    };
+    auto issue_s = [&](int gg) {
+      issue_xt(tmem + L::T_S + (gg & 1) * 64, dK, sdesc_add(dQ0, (gg % kStages) * L::QT));
+      mma_commit_w(&bar_s_full[gg & 1]);
+    };
+    auto issue_dp = [&](int gg) {
+      issue_xt(tmem + L::T_DP + (gg & 1) * 64, dV, sdesc_add(dDY0, (gg % kStages) * L::QT));
+      mma_commit_w(&bar_dp_full[gg & 1]);
+    };
+    bool ok = true;
+    int g0 = 0, lv = 0;
+    for (int ii = 0; ok; ++ii) {
+      if (!(ok = item_wait(ii))) break;
+      const int n = items[ii & 1].n;
+      if (n < 0) break;
+      if (n > 0) {
+        if (!(ok = mbar_wait_warp(&bar_kv, lv & 1, ab))) break;
+        // the first score and dP tiles of this item go while the epilogue of
+        // the previous item still reads dV and dK
+        for (int t = 0; t < 2 && t < n && ok; ++t) {
+          if (!(ok = mbar_wait_warp(&bar_full[(g0 + t) % kStages], ((g0 + t) / kStages) & 1, ab))) break;
           tc_fence_after();
-          issue_s(t + 2);
+          issue_s(g0 + t);
+          issue_dp(g0 + t);
         }
-        if (!(ok = mbar_wait_warp(&bar_ds_full[bb], (t >> 1) & 1, ab))) break;
+        if (!ok) break;
+        if (n <= 2) mma_commit_w(&bar_kv_free);
+        if (lv > 0 && !(ok = mbar_wait_warp(&bar_acc_free, (lv - 1) & 1, ab))) break;
         tc_fence_after();
-        issue_acc(t_dk, tmem + L::T_DP + bb * 64, sdesc_add(dQm0, s * L::QT), t == 0);
-        mma_commit_w(&bar_empty[s]);
-        if (t + 2 < n) issue_dp(t + 2);
+        // Per tile g: dV(g) once P(g) is in; then S(g+2) and dK(g) in
+        // whichever order their inputs arrive; then dP(g+2).  S(g+2)
+        // overwrites P(g), which dV(g) (earlier in the same pipe) consumes,
+        // and S(g), which the group finished reading before it handed P(g)
+        // over; dP(g+2) overwrites dS(g) and dP(g), read by dK(g) and by the
+        // group before dS(g) was handed over.
+        for (int t = 0; t < n && ok; ++t) {
+          const int g = g0 + t, s = g % kStages, bb = g & 1;
+          if (!(ok = mbar_wait_warp(&bar_p_full[bb], (g >> 1) & 1, ab))) break;
+          tc_fence_after();
+          issue_acc(t_dv, tmem + L::T_S + bb * 64, sdesc_add(dDYm0, s * L::QT), t == 0);
+          bool s_next = t + 2 < n, k_now = true;
+          PollBudget pb;
+          while (s_next || k_now) {
+            if (s_next && mbar_test_warp(&bar_full[(g + 2) % kStages], ((g + 2) / kStages) & 1)) {
+              tc_fence_after();
+              issue_s(g + 2);
+              s_next = false;
+            }
+            if (k_now && mbar_test_warp(&bar_ds_full[bb], (g >> 1) & 1)) {
+              tc_fence_after();
+              issue_acc(t_dk, tmem + L::T_DP + bb * 64, sdesc_add(dQm0, s * L::QT), t == 0);
+              mma_commit_w(&bar_empty[s]);
+              k_now = false;
+            }
+            if ((s_next || k_now) && !(ok = pb.check(ab))) break;
+          }
+          if (!ok) break;
+          if (t + 2 < n) {
+            issue_dp(g + 2);
+            if (t + 3 == n) mma_commit_w(&bar_kv_free);  // the item's last S and dP are issued
+          }
+        }
+        if (!ok) break;
+        mma_commit_w(&bar_acc);
+        g0 += n;
+        ++lv;
       }
-      mma_commit_w(&bar_acc);
-      drain_wait(&bar_acc, 0);
+      item_done(ii);
     }
+    if (lv > 0) drain_wait(&bar_acc, (lv - 1) & 1);
     __syncwarp();
   } else if (warp >= 4) {
-    const bool softmax_wg = warp < 8 || warp >= 12;  // warps 4..7, 12..15: P; warps 8..11: dS
-    const int sg = warp >= 12 ? 1 : 0;               // softmax group: tiles (and S buffer) of parity sg
+    const int sg = (warp - 4) >> 2;  // compute group: tiles (and S/dP buffers) of parity sg
     const int lg = warp & 3;
     const int row = lg * 32 + lane;  // token row inside the block == TMEM lane
     const uint32_t lane_addr = static_cast<uint32_t>(lg * 32) << 16;
-    bool ok = n > 0;
-    if (n > 0 && softmax_wg) {
-      // ---------------------------------------------------------- softmax: S^T -> P^T
-      // Each group waits every phase of its own S buffer.  Of the stage
-      // barrier it skips the phases of the other group's tiles; when it waits
-      // for tile t, the phase of tile t - kStages (same stage) has completed,
-      // since the tensor core issued S(t - 2) after it.
-      for (int t = sg; t < n && ok; t += 2) {
-        const int s = t % kStages, bb = t & 1;
-        if (!(ok = mbar_wait_warp(&bar_full[s], (t / kStages) & 1, ab))) break;
+    bool ok = true;
+    int g0 = 0, lv = 0;
+    for (int ii = 0; ok; ++ii) {
+      if (!(ok = item_wait(ii))) break;
+      const ItemSlot& it = items[ii & 1];
+      const int n = it.n;
+      if (n < 0) break;
+      for (int t = ((g0 & 1) == sg) ? 0 : 1; t < n && ok; t += 2) {
+        const int g = g0 + t, s = g % kStages, bb = g & 1;
+        if (!(ok = mbar_wait_warp(&bar_full[s], (g / kStages) & 1, ab))) break;
         const uint8_t* st = sm + L::ST_OFF + s * L::ST_STAGE;
-        const float* sl2 = reinterpret_cast<const float*>(st);
-        const int* spos = reinterpret_cast<const int*>(sl2 + 2 * L::BC);
+        const float* snl = reinterpret_cast<const float*>(st);
+        const float* sdl = snl + L::BC;
+        const int* spos = reinterpret_cast<const int*>(sdl + L::BC);
         const int* sinfo = spos + L::BC;
         const int tok = sinfo[0] + row;
         const bool tok_ok = row >= sinfo[1] && row < sinfo[2] && tok >= 0 && tok < sinfo[3];
-        if (!(ok = mbar_wait_warp(&bar_s_full[bb], (t >> 1) & 1, ab))) break;
+        if (!(ok = mbar_wait_warp(&bar_s_full[bb], (g >> 1) & 1, ab))) break;
         tc_fence_after();
-        p_row_paged(tmem + L::T_S + bb * 64 + lane_addr, sl2, spos, tok_ok, tok, p.scale_log2);
+        // ---------------------------------------------------- S^T -> P^T
+        // two halves of 32 columns: half hf reads S^T columns [32hf, 32hf+32)
+        // and writes P^T (bf16 pairs) to columns [16hf, 16hf+16), which half
+        // 0 has already read
+        const uint32_t tS = tmem + L::T_S + bb * 64 + lane_addr;
+        const uint64_t sl2 = f2_pack(p.scale_log2, p.scale_log2);
+        uint32_t pw[32];
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t sr[32];
+          tmem_ld32(tS + 32 * hf, sr);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c4 = 0; c4 < 8; ++c4) {
+            const int c0 = 32 * hf + 4 * c4;
+            const float4 nl = lds_f4(snl + c0);
+            const int4 ps = *reinterpret_cast<const int4*>(spos + c0);
+            float x0, x1, x2, x3;
+            f2_split(f2_fma(f2_pack_u(sr[4 * c4], sr[4 * c4 + 1]), sl2, f2_pack(nl.x, nl.y)), x0, x1);
+            f2_split(f2_fma(f2_pack_u(sr[4 * c4 + 2], sr[4 * c4 + 3]), sl2, f2_pack(nl.z, nl.w)), x2, x3);
+            const float p0 = (tok_ok && tok <= ps.x) ? ex2_approx(x0) : 0.f;
+            const float p1 = (tok_ok && tok <= ps.y) ? ex2_approx(x1) : 0.f;
+            const float p2 = (tok_ok && tok <= ps.z) ? ex2_approx(x2) : 0.f;
+            const float p3 = (tok_ok && tok <= ps.w) ? ex2_approx(x3) : 0.f;
+            pw[16 * hf + 2 * c4] = pack_bf16x2(p0, p1);
+            pw[16 * hf + 2 * c4 + 1] = pack_bf16x2(p2, p3);
+          }
+          tmem_st16(tS + 16 * hf, *reinterpret_cast<const uint32_t(*)[16]>(pw + 16 * hf));
+        }
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar_p_full[bb]);
-      }
-    } else if (n > 0) {
-      // ---------------------------------------------------------- dS: dP^T, P^T -> dS^T
-      for (int t = 0; t < n && ok; ++t) {
-        const int s = t % kStages, bb = t & 1;
-        if (!(ok = mbar_wait_warp(&bar_full[s], (t / kStages) & 1, ab))) break;
-        if (!(ok = mbar_wait_warp(&bar_dp_full[bb], (t >> 1) & 1, ab))) break;
-        if (!(ok = mbar_wait_warp(&bar_p_full[bb], (t >> 1) & 1, ab))) break;
+        // ---------------------------------------------------- dP^T, P^T -> dS^T
+        if (!(ok = mbar_wait_warp(&bar_dp_full[bb], (g >> 1) & 1, ab))) break;
         tc_fence_after();
         const uint32_t tDP = tmem + L::T_DP + bb * 64 + lane_addr;
-        const uint32_t tS = tmem + L::T_S + bb * 64 + lane_addr;
-        uint32_t pw[32];
-        tmem_ld32(tS, pw);
-        tmem_ld_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bar_p_read[bb]);
-        const float* dl = reinterpret_cast<const float*>(sm + L::ST_OFF + s * L::ST_STAGE) + L::BC;
-        // two halves of 32 columns: half hf reads dP columns [32hf, 32hf+32)
-        // and writes dS^T (bf16 pairs) to columns [16hf, 16hf+16).  A masked
-        // entry has P = 0 and takes dS = 0 by select: dP of a tail or unowned
-        // slot may be NaN.
+        // a masked entry has P = 0 and takes dS = 0 by select: dP of a tail or
+        // unowned slot may be NaN
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           uint32_t dr[32], dsw[16];
@@ -380,13 +464,13 @@ __global__ void __launch_bounds__(512, 1)
           tmem_ld_wait();
 #pragma unroll
           for (int c4 = 0; c4 < 8; ++c4) {
-            const float4 d4 = *reinterpret_cast<const float4*>(dl + 32 * hf + 4 * c4);
+            const float4 d4 = lds_f4(sdl + 32 * hf + 4 * c4);
             const float dv4[4] = {d4.x, d4.y, d4.z, d4.w};
-            const uint32_t w[2] = {pw[16 * hf + 2 * c4], pw[16 * hf + 2 * c4 + 1]};
             float ds[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const float pe = __uint_as_float((e & 1) ? (w[e >> 1] & 0xffff0000u) : (w[e >> 1] << 16));
+              const uint32_t w = pw[16 * hf + 2 * c4 + (e >> 1)];
+              const float pe = __uint_as_float((e & 1) ? (w & 0xffff0000u) : (w << 16));
               ds[e] = pe != 0.f ? pe * (__uint_as_float(dr[4 * c4 + e]) - dv4[e]) : 0.f;
             }
             dsw[2 * c4] = pack_bf16x2(ds[0], ds[1]);
@@ -399,28 +483,25 @@ __global__ void __launch_bounds__(512, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar_ds_full[bb]);
       }
-    }
-    if (n > 0) {
-      if (ok) ok = mbar_wait_warp(&bar_acc, 0, ab);
-      tc_fence_after();
-    }
-    // ------------------------------------------------------------ epilogue
-    // the softmax warpgroups store dV (half of the columns each), the dS
-    // warpgroup dK (times the softmax scale), each row of a page this CTA
-    // stores; rows of tokens no pass saw are zero
-    const int wg = softmax_wg ? 0 : 1;
-    const int j = row >> 4;
-    const bool want = wg == 0 ? (p.wrt & 4u) != 0 : (p.wrt & 2u) != 0;
-    if (want && (ok || n == 0)) {  // warp-uniform: the tensor-memory loads are warp-collective
-      const bool mine = pinfo.store[j] != 0;
-      const int dim = wg == 0 ? p.Dv : p.Dk;
-      const int64_t prow = (static_cast<int64_t>(pinfo.phys[j]) * p.page_size + (row & 15)) * p.KVH + g;
-      __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(wg == 0 ? p.dv_pool : p.dk_pool) + prow * dim;
-      const float f = wg == 0 ? 1.f : p.scale;
-      const uint32_t tacc = (wg == 0 ? t_dv : t_dk) + lane_addr;
-      const int c_lo = wg == 0 ? sg * (DP / 64) : 0, c_hi = wg == 0 ? (sg + 1) * (DP / 64) : DP / 32;
+      if (!ok) break;
+      if (n > 0) {
+        if (!(ok = mbar_wait_warp(&bar_acc, lv & 1, ab))) break;
+        tc_fence_after();
+      }
+      // ---------------------------------------------------------- epilogue
+      // group 0 stores dV, group 1 dK (times the softmax scale), each row of
+      // a page this item stores; rows of tokens no pass saw are zero.  Tensor
+      // memory goes back (acc_free) once the last chunk is in registers.
+      const int j = row >> 4;
+      const bool mine = it.pi.store[j] != 0;
+      const bool want = sg == 0 ? (p.wrt & 4u) != 0 : (p.wrt & 2u) != 0;
+      const int dim = sg == 0 ? p.Dv : p.Dk;
+      const int64_t prow = (static_cast<int64_t>(it.pi.phys[j]) * p.page_size + (row & 15)) * p.KVH + it.g;
+      __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(sg == 0 ? p.dv_pool : p.dk_pool) + prow * dim;
+      const float f = sg == 0 ? 1.f : p.scale;
+      const uint32_t tacc = (sg == 0 ? t_dv : t_dk) + lane_addr;
 #pragma unroll 1
-      for (int cc = c_lo; cc < c_hi && cc * 32 < dim; ++cc) {
+      for (int cc = 0; want && cc < DP / 32 && cc * 32 < dim; ++cc) {  // warp-uniform (tensor-memory loads)
         uint32_t r[32];
         if (n > 0) {
           tmem_ld32(tacc + cc * 32, r);
@@ -441,6 +522,14 @@ __global__ void __launch_bounds__(512, 1)
           }
         }
       }
+      if (n > 0) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar_acc_free);
+        g0 += n;
+        ++lv;
+      }
+      item_done(ii);
     }
   }
   tc_fence_before();
@@ -458,9 +547,14 @@ cudaError_t launch_hist_t(const PagedMaps& m, const PagedParams& p, cudaStream_t
   const int smem = max(L::BYTES + 1024, kSmemOneCtaPerSm);  // all 512 TMEM columns: one CTA per SM
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
   const int nblk = (p.max_pages * p.page_size + 127) / 128;
-  dim3 grid(p.KVH, nblk, p.S);
-  kern<<<grid, 512, smem, s>>>(m.q, m.dy, m.k, m.v, p);
+  const int64_t items = static_cast<int64_t>(p.KVH) * nblk * p.S;
+  const int grid = static_cast<int>(items < sms ? items : sms);  // persistent: one CTA per SM
+  if (grid <= 0) return cudaSuccess;
+  kern<<<grid, 384, smem, s>>>(m.q, m.dy, m.k, m.v, p);
   return cudaGetLastError();
 }
 
