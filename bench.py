@@ -364,6 +364,8 @@ def sweep(args) -> int:
                           ("C5m prefix1024", "paged_mla", {"shared_prefix_pages": 64})):
         if not want(tag):
             continue
+        if args.seqs is not None:
+            ov = dict(ov, num_seqs=args.seqs)
         c = inputs.paged_config(name, **ov)
         tb = lambda x: None if x is None else torch.from_numpy(np.ascontiguousarray(x)).cuda().to(torch.bfloat16)
         dv = dict(q=tb(c.q), dy=tb(c.dy), k=tb(c.k_pool), v=tb(c.v_pool), qp=tb(c.qp), kp=tb(c.kp_pool))
@@ -508,6 +510,9 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--batch", type=int, default=None, help="override B (profiling runs on a smaller case)")
     ap.add_argument("--heads", type=int, default=None, help="override H (profiling runs on a smaller case)")
+    ap.add_argument("--seqs", type=int, default=None,
+                    help="--sweep: override the number of sequences of the paged workloads (profiling runs on a "
+                         "smaller case)")
     ap.add_argument("--sweep", action="store_true",
                     help="time every configuration once against its oracle sample (one JSON line each)")
     ap.add_argument("--recompute-dq", action="store_true",
