@@ -396,7 +396,7 @@ def sweep(args) -> int:
         torch.cuda.synchronize()
         kernel_ms = {n: evs[i].elapsed_time(evs[i + 1]) for i, n in enumerate(names)}
         compact = None
-        if not ov:
+        if "shared_prefix_pages" not in ov:
             # compact history listing the referenced pages only: the zero store
             # of the unreferenced pool pages is skipped
             ref_pages = np.unique(np.concatenate([c.page_table[s_, :(int(c.seq_len[s_]) + c.page_size - 1) // c.page_size]
@@ -446,7 +446,7 @@ def sweep(args) -> int:
                 ph = int(c.page_table[s_, lp])
                 owned[ph * c.page_size:(ph + 1) * c.page_size] = False
         err = max(rel(g, w, owned) for g, w in zip(first, ref))
-        emit({"config": tag, "workload": name, **({"shared_prefix_pages": ov["shared_prefix_pages"]} if ov else {}),
+        emit({"config": tag, "workload": name, **({"shared_prefix_pages": ov["shared_prefix_pages"]} if "shared_prefix_pages" in ov else {}),
               "gpu_ms_median": ms, "gpu_ms_min": ms_min,
               "counted_tflops": flops / (ms * 1e-3) / 1e12,
               "pct_of_bf16_peak": 100.0 * flops / (ms * 1e-3) / 1e12 / peaks["bf16_tflops"],
