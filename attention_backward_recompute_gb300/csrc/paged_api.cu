@@ -40,11 +40,11 @@ attn_status_t check_paged_desc(const attn_paged_desc* d, PagedSizes* z) {
     // MLA: the latent (key_dim) is also the value
     if (d->key_dim != 512 || d->position_dim != 64)
       return api_fail(ATTN_ERR_UNSUPPORTED, "MLA needs key_dim 512 and position_dim 64");
-    if (G > 32) return api_fail(ATTN_ERR_UNSUPPORTED, "MLA needs heads / kv_heads <= 32");
   } else {
-    if (64 % G != 0) return api_fail(ATTN_ERR_UNSUPPORTED, "heads / kv_heads must divide 64");
     if (d->key_dim != 64 && d->key_dim != 128) return api_fail(ATTN_ERR_UNSUPPORTED, "key_dim must be 64 or 128 (GQA)");
   }
+  // a tile of 64 columns holds 64 / G whole query rows
+  if (64 % G != 0) return api_fail(ATTN_ERR_UNSUPPORTED, "heads / kv_heads must divide 64");
   const int64_t lim = int64_t(1) << 30;
   if (d->num_pages * d->page_size >= lim || d->num_queries * d->heads >= lim || d->num_seqs * d->max_pages_per_seq >= lim ||
       d->num_seqs >= 65535 || d->kv_heads >= 65535)
@@ -228,14 +228,15 @@ ATTN_API attn_status_t attn_bwd_paged_compact(const attn_paged_desc* d, const vo
     const cudaError_t e = attn::launch_paged_listed(p, history_pages, num_history_pages, s);
     if (e != cudaSuccess) return api_fail(ATTN_ERR_CUDA, "paged launch failed: %s", cudaGetErrorString(e));
   }
-  if (mla && attn::mla_tc_supported(p)) {
+  if (mla) {
+    if (!attn::mla_tc_supported(p)) return api_fail(ATTN_ERR_UNSUPPORTED, "MLA shape not supported");
     // links, zeros for pages no link references, then two CTAs per 128-token
     // block of every sequence (tcgen05); blocks whose shared pages carry many
     // links go to the cluster-split kernel first
     attn::PagedMlaMaps mm;
     std::memset(&mm, 0, sizeof(mm));
     const uint64_t slots = uint64_t(d->num_pages) * d->page_size;
-    const bool split = attn::mla_mma_supported(p);
+    const bool split = attn::mla_split_supported(p);
     // query-side boxes of 64 columns (64/G rows) for the tcgen05 kernel, of
     // 32 columns for the cluster-split kernel
     const uint32_t G = uint32_t(p.G), RT = 64u / G, RS = split ? 32u / G : RT;
@@ -263,54 +264,9 @@ ATTN_API attn_status_t attn_bwd_paged_compact(const attn_paged_desc* d, const vo
     if (split && e == cudaSuccess) e = attn::launch_paged_mla_plan(p, s);
     if (split && e == cudaSuccess) e = attn::launch_paged_mla_tc_pair_heavy(p, s);
     attn::timing_mark(s);
-    if (split && e == cudaSuccess) e = attn::launch_paged_mla_mma_split(mm, p, s);
+    if (split && e == cudaSuccess) e = attn::launch_paged_mla_split(mm, p, s);
     attn::timing_mark(s);
     if (e == cudaSuccess) e = attn::launch_paged_mla_tc(mt, p, split, s);
-    attn::timing_mark(s);
-    attn::timing_mark_end();
-    if (e != cudaSuccess) return api_fail(ATTN_ERR_CUDA, "paged launch failed: %s", cudaGetErrorString(e));
-    return api_ok();
-  }
-  if (mla && attn::mla_mma_supported(p)) {
-    // links, zeros for pages no link references, then one CTA per 64-token
-    // block of every sequence (warp-level tensor path)
-    attn::PagedMlaMaps mm;
-    std::memset(&mm, 0, sizeof(mm));
-    const uint64_t slots = uint64_t(d->num_pages) * d->page_size;
-    const uint32_t G = uint32_t(p.G), RT = 32u / G;
-    bool enc = encode3d(&mm.k, k_pool, d->key_dim, d->kv_heads, slots, 64, 1, uint32_t(d->page_size)) &&
-               encode3d(&mm.kp, kp_pool, d->position_dim, d->kv_heads, slots, 64, 1, uint32_t(d->page_size));
-    if (d->num_queries > 0)
-      enc = enc && encode3d(&mm.q, q, d->key_dim, d->heads, d->num_queries, 64, G, RT) &&
-            encode3d(&mm.qp, qp, d->position_dim, d->heads, d->num_queries, 64, G, RT) &&
-            encode3d(&mm.dy, dy, d->value_dim, d->heads, d->num_queries, 64, G, RT);
-    else
-      mm.q = mm.qp = mm.dy = mm.k;
-    if (!enc) return api_fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed");
-    attn::timing_mark_begin(5, s);
-    cudaError_t e = attn::launch_paged_prep(p, s);
-    attn::timing_mark(s);
-    if (e == cudaSuccess) e = attn::launch_paged_zero_unlinked(p, compact ? history_pages : nullptr, num_history_pages, s);
-    attn::timing_mark(s);
-    // blocks whose shared pages carry many links: flagged, then split over
-    // clusters, with the other blocks' kernel starting on the SMs left free
-    if (e == cudaSuccess) e = attn::launch_paged_mla_plan(p, s);
-    attn::timing_mark(s);
-    if (e == cudaSuccess) e = attn::launch_paged_mla_mma_split(mm, p, s);
-    attn::timing_mark(s);
-    if (e == cudaSuccess) e = attn::launch_paged_mla_mma(mm, p, s);
-    attn::timing_mark(s);
-    attn::timing_mark_end();
-    if (e != cudaSuccess) return api_fail(ATTN_ERR_CUDA, "paged launch failed: %s", cudaGetErrorString(e));
-    return api_ok();
-  }
-  if (mla) {
-    // links, then one owner CTA per physical page (it stores zeros for slots
-    // no link makes valid, so no separate zero store is needed)
-    attn::timing_mark_begin(2, s);
-    cudaError_t e = attn::launch_paged_prep(p, s);
-    attn::timing_mark(s);
-    if (e == cudaSuccess) e = attn::launch_paged_mla_history(p, q, qp, dy, k_pool, kp_pool, s);
     attn::timing_mark(s);
     attn::timing_mark_end();
     if (e != cudaSuccess) return api_fail(ATTN_ERR_CUDA, "paged launch failed: %s", cudaGetErrorString(e));
@@ -370,7 +326,7 @@ ATTN_API attn_status_t attn_paged_row_stats(const attn_paged_desc* d, const void
   if ((st = fill_params(d, z, page_table, seq_meta, workspace, &p)) != ATTN_OK) return st;
   p.lse_out = lse;
   p.delta_out = delta;
-  if (mla && attn::mla_stats_tc_supported(p)) {
+  if (mla) {
     // tcgen05: 128 columns (128/G rows) per CTA
     attn::PagedMlaMaps mt;
     if (!encode_mla_maps(&mt, d, p.G, 128u / uint32_t(p.G), q, qp, dy, k_pool, kp_pool))
@@ -378,37 +334,6 @@ ATTN_API attn_status_t attn_paged_row_stats(const attn_paged_desc* d, const void
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     attn::timing_mark_begin(1, s);
     cudaError_t e = attn::launch_paged_mla_stats_tc(mt, p, s);
-    attn::timing_mark(s);
-    attn::timing_mark_end();
-    if (e != cudaSuccess) return api_fail(ATTN_ERR_CUDA, "row-statistics launch failed: %s", cudaGetErrorString(e));
-    return api_ok();
-  }
-  if (mla && attn::mla_mma_supported(p)) {
-    attn::PagedMlaMaps mm;
-    std::memset(&mm, 0, sizeof(mm));
-    const uint64_t slots = uint64_t(d->num_pages) * d->page_size;
-    const uint32_t G = uint32_t(p.G), RT2 = 64u / G;
-    bool enc = encode3d(&mm.q, q, d->key_dim, d->heads, d->num_queries, 64, G, RT2) &&
-               encode3d(&mm.qp, qp, d->position_dim, d->heads, d->num_queries, 64, G, RT2) &&
-               encode3d(&mm.dy, dy, d->value_dim, d->heads, d->num_queries, 64, G, RT2);
-    if (slots > 0)
-      enc = enc && encode3d(&mm.k, k_pool, d->key_dim, d->kv_heads, slots, 64, 1, uint32_t(d->page_size)) &&
-            encode3d(&mm.kp, kp_pool, d->position_dim, d->kv_heads, slots, 64, 1, uint32_t(d->page_size));
-    else
-      mm.k = mm.kp = mm.q;
-    if (!enc) return api_fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed");
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    attn::timing_mark_begin(1, s);
-    cudaError_t e = attn::launch_paged_mla_stats_mma(mm, p, s);
-    attn::timing_mark(s);
-    attn::timing_mark_end();
-    if (e != cudaSuccess) return api_fail(ATTN_ERR_CUDA, "row-statistics launch failed: %s", cudaGetErrorString(e));
-    return api_ok();
-  }
-  if (mla) {
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    attn::timing_mark_begin(1, s);
-    cudaError_t e = attn::launch_paged_mla_stats(p, q, qp, dy, k_pool, kp_pool, s);
     attn::timing_mark(s);
     attn::timing_mark_end();
     if (e != cudaSuccess) return api_fail(ATTN_ERR_CUDA, "row-statistics launch failed: %s", cudaGetErrorString(e));
@@ -471,37 +396,20 @@ ATTN_API attn_status_t attn_bwd_paged_query(const attn_paged_desc* d, const void
   p.delta_out = delta;
   p.dq = dq;
   if (mla) {
-    // row statistics, then dQ / dQp from them (tcgen05; the warp-level
-    // tensor path for shapes the tcgen05 kernels do not take)
-    const bool tc = attn::mla_stats_tc_supported(p) && attn::mla_query_tc_supported(p);
-    if (!tc && !attn::mla_mma_supported(p))
-      return api_fail(ATTN_ERR_UNSUPPORTED, "MLA query side needs heads / kv_heads dividing 64 and page 16");
+    // row statistics (128 columns per CTA), then dQ / dQp from them (64
+    // columns per CTA), both on tcgen05
     p.dqp = dqp;
     p.lse = lse;
     p.delta = delta;
-    attn::PagedMlaMaps mm;
-    std::memset(&mm, 0, sizeof(mm));
-    const uint64_t slots = uint64_t(d->num_pages) * d->page_size;
-    const uint32_t G = uint32_t(p.G), RT2 = 64u / G;
-    bool enc = encode3d(&mm.q, q, d->key_dim, d->heads, d->num_queries, 64, G, RT2) &&
-               encode3d(&mm.qp, qp, d->position_dim, d->heads, d->num_queries, 64, G, RT2) &&
-               encode3d(&mm.dy, dy, d->value_dim, d->heads, d->num_queries, 64, G, RT2);
-    if (slots > 0)
-      enc = enc && encode3d(&mm.k, k_pool, d->key_dim, d->kv_heads, slots, 64, 1, uint32_t(d->page_size)) &&
-            encode3d(&mm.kp, kp_pool, d->position_dim, d->kv_heads, slots, 64, 1, uint32_t(d->page_size));
-    else
-      mm.k = mm.kp = mm.q;
-    if (!enc) return api_fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed");
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // row statistics on tcgen05 (128 columns per CTA) where it applies
-    attn::PagedMlaMaps mt;
-    const bool stats_tc = tc;
-    if (stats_tc && !encode_mla_maps(&mt, d, p.G, 128u / G, q, qp, dy, k_pool, kp_pool))
+    attn::PagedMlaMaps ms, mq;
+    if (!encode_mla_maps(&ms, d, p.G, 128u / uint32_t(p.G), q, qp, dy, k_pool, kp_pool) ||
+        !encode_mla_maps(&mq, d, p.G, 64u / uint32_t(p.G), q, qp, dy, k_pool, kp_pool))
       return api_fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
     attn::timing_mark_begin(3, s);
-    cudaError_t e = stats_tc ? attn::launch_paged_mla_stats_tc(mt, p, s) : attn::launch_paged_mla_stats_mma(mm, p, s);
+    cudaError_t e = attn::launch_paged_mla_stats_tc(ms, p, s);
     attn::timing_mark(s);
-    if (e == cudaSuccess) e = tc ? attn::launch_paged_mla_query_tc(mm, p, s) : attn::launch_paged_mla_query_mma(mm, p, s);
+    if (e == cudaSuccess) e = attn::launch_paged_mla_query_tc(mq, p, s);
     attn::timing_mark(s);
     if (e == cudaSuccess) e = attn::launch_paged_query_outside(p, s);
     attn::timing_mark(s);

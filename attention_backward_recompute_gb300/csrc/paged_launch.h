@@ -26,45 +26,33 @@ cudaError_t launch_paged_row_stats(const PagedMaps& m, const PagedParams& p, cud
 cudaError_t launch_paged_query(const PagedMaps& m, const PagedParams& p, cudaStream_t s);
 // rows outside every sequence's range: dq (and dqp) = 0, lse = -inf, delta = 0
 cudaError_t launch_paged_query_outside(const PagedParams& p, cudaStream_t s);
-// MLA (key_dim 512 latent + position_dim 64; the latent is also the value)
-cudaError_t launch_paged_mla_history(const PagedParams& p, const void* q, const void* qp, const void* dy,
-                                     const void* k_pool, const void* kp_pool, cudaStream_t s);
-// MLA on the warp-level tensor path: q, qp, dy as [Nq, H, D] addressed
-// (d, h, r) with box (64, G, 32/G); latent and position pools as [slots, KVH, D]
-// with box (64, 1, 16).
+// MLA (key_dim 512 latent + position_dim 64; the latent is also the value):
+// q, qp, dy as [Nq, H, D] addressed (d, h, r) with box (64, G, rows);
+// latent and position pools as [slots, KVH, D] with box (64, 1, 16).
 struct PagedMlaMaps {
   CUtensorMap q, qp, dy, k, kp;
 };
-bool mla_mma_supported(const PagedParams& p);
-cudaError_t launch_paged_mla_mma(const PagedMlaMaps& m, const PagedParams& p, cudaStream_t s);
 // compact history: p.listed[page] = 1 for the n listed pages (zero otherwise)
 cudaError_t launch_paged_listed(const PagedParams& p, const int32_t* pages, int64_t n, cudaStream_t s);
-// flags the MLA history blocks whose shared pages carry many link tiles (p.heavy)
-cudaError_t launch_paged_mla_plan(const PagedParams& p, cudaStream_t s);
-// the flagged blocks, by clusters of CTAs; launched before launch_paged_mla_mma,
-// which then runs as its programmatic dependent on the SMs the clusters leave
-cudaError_t launch_paged_mla_mma_split(const PagedMlaMaps& m, const PagedParams& p, cudaStream_t s);
-// MLA row statistics on the same path; q, qp, dy maps with box (64, G, 64/G)
-cudaError_t launch_paged_mla_stats_mma(const PagedMlaMaps& m, const PagedParams& p, cudaStream_t s);
-// MLA query side (dQ, dQp) on the same path, from lse / delta; maps as for the statistics
-cudaError_t launch_paged_mla_query_mma(const PagedMlaMaps& m, const PagedParams& p, cudaStream_t s);
 // MLA history on tcgen05 (two CTAs per 128-token block, each accumulating
-// half of the dims); blocks with a heavy 64-token half (p.heavy, when not
-// null) are left to the cluster-split kernel
+// half of the dims); maps with 64-column boxes (64/G rows).  Blocks with a
+// heavy 64-token half (p.heavy, when not null) are left to the split kernel;
+// after_split: that kernel was launched just before (the first part then
+// starts as its programmatic dependent)
 bool mla_tc_supported(const PagedParams& p);
-// after_split: the cluster-split kernel was launched just before (the first
-// part then starts as its programmatic dependent)
 cudaError_t launch_paged_mla_tc(const PagedMlaMaps& m, const PagedParams& p, bool after_split, cudaStream_t s);
-// extends the heavy flags of the split plan to both 64-token halves of a
-// 128-token block
+// flags the MLA history blocks (64 tokens) whose shared pages carry many link
+// tiles (p.heavy), then extends each flag to both halves of a 128-token block
+cudaError_t launch_paged_mla_plan(const PagedParams& p, cudaStream_t s);
 cudaError_t launch_paged_mla_tc_pair_heavy(const PagedParams& p, cudaStream_t s);
-// MLA row statistics on tcgen05; q, qp, dy maps with box (64, G, 128/G)
+// the flagged blocks, by clusters of 16 CTAs (maps with 32-column boxes)
+bool mla_split_supported(const PagedParams& p);
+cudaError_t launch_paged_mla_split(const PagedMlaMaps& m, const PagedParams& p, cudaStream_t s);
+// MLA row statistics on tcgen05; maps with 128-column boxes (128/G rows)
 bool mla_stats_tc_supported(const PagedParams& p);
 cudaError_t launch_paged_mla_stats_tc(const PagedMlaMaps& m, const PagedParams& p, cudaStream_t s);
-// MLA query side (dQ, dQp) on tcgen05 from lse / delta; maps with box (64, G, 64/G)
+// MLA query side (dQ, dQp) on tcgen05 from lse / delta; maps with 64-column boxes
 bool mla_query_tc_supported(const PagedParams& p);
 cudaError_t launch_paged_mla_query_tc(const PagedMlaMaps& m, const PagedParams& p, cudaStream_t s);
-cudaError_t launch_paged_mla_stats(const PagedParams& p, const void* q, const void* qp, const void* dy,
-                                   const void* k_pool, const void* kp_pool, cudaStream_t s);
 
 }  // namespace attn

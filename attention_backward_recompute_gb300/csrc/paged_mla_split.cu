@@ -1,4 +1,8 @@
-// Paged MLA history backward on the warp-level tensor path (mma.sync bf16).
+// Paged MLA history backward for the blocks whose shared pages carry many
+// links (a long prefix shared by many sequences): the link passes of one such
+// block are split over a cluster of 16 CTAs, on the warp-level tensor path
+// (mma.sync bf16).  Every other block runs on the tcgen05 history kernel
+// (paged_mla_tc.cu), which leaves the flagged blocks to this one.
 //
 // ruDNN src/paged_attention/ordered_kernel.rs (history_backward with `mla`):
 // for query row r, head h and history token t,
@@ -9,16 +13,11 @@
 // summed over the links of the token's page (link order), the visible rows of
 // each linked sequence (t <= pos(r) when causal) and the heads of the group.
 //
-// Why mma.sync and not tcgen05: the accumulator of one 64-token block is
-// 64 x 576 fp32 (144 KiB); with the score and dP tiles it does not fit the
-// 512 tensor-memory columns, while 16 warps hold it in registers (72 per
-// thread).  The warp-level tensor path runs at about a quarter of tcgen05's
-// rate on this GPU, which is still far above CUDA-core FMA.
-//
-// One CTA owns 64 tokens (four 16-token pages) of one sequence and one KV head
-// and walks the same passes as the GQA kernel: its own sequence, then the
-// other links of the pages it stores, in link order, consecutive pages of a
-// shared prefix in one pass.
+// A plan kernel flags the 64-token blocks whose link passes exceed 128 tiles.
+// A cluster CTA runs a contiguous share of such a block's tiles with the
+// block's 64 x 576 fp32 accumulator in the registers of its 16 warps (the
+// partial of one CTA does not need tensor memory, which keeps the 16 partials
+// of a cluster side by side in shared memory for the rank-ordered sum).
 // A column is one (query row, head of the group) pair; a tile is 32 columns
 // (32 / G rows).  Per tile:
 //   phase A  warp (token tile tt, column octet n8): S^T and dP^T (16 x 8) with
@@ -222,6 +221,11 @@ __device__ __forceinline__ uint32_t map_rank(uint32_t addr, int rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
   return r;
 }
+__device__ __forceinline__ int ld_cluster_s32(uint32_t addr) {
+  int v;
+  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
 __device__ __forceinline__ float4 ld_cluster_f4(uint32_t addr) {
   float4 v;
   asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
@@ -272,17 +276,15 @@ __global__ void mla_plan_kernel(const PagedParams p) {
   }
 }
 
-// SPLIT = false: one CTA per (64-token block, sequence, KV head); a block it
-// stores is finished here unless the plan flagged its link passes as heavy.
-// SPLIT = true: persistent clusters of kCL CTAs take the flagged blocks (heavy
+// Persistent clusters of kCL CTAs take the blocks the plan flagged (heavy
 // block k to cluster k mod clusters); CTA r of a cluster runs the block's
 // tiles [r n / kCL, (r + 1) n / kCL) of its n, the partial sums meet in
 // shared memory and each CTA adds its BT / kCL tokens' partials over the
 // cluster in rank order (a fixed order: the result does not depend on the
-// number of clusters or on timing).
-template <bool SPLIT>
+// number of clusters or on timing).  Every other block is done by the
+// tcgen05 history kernel, which skips the flagged ones.
 __global__ void __launch_bounds__(kThreads, 1)
-    mla_mma_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_qp,
+    mla_split_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_qp,
                    const __grid_constant__ CUtensorMap tm_dy, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_kp, const PagedParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -290,7 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ uint64_t bar_k, bar_full[2];
   __shared__ int abort_flag;
   __shared__ MPageInfo pinfo;
-  __shared__ int n_tiles_sh, tile0_sh, any_store_sh, heavy_sh;
+  __shared__ int n_tiles_sh, tile0_sh, any_store_sh, abort_any_sh;
   // (the copy iterator lives in shared memory: only thread 0 uses it, and in
   // registers it would be held by every thread)
   __shared__ MPass pf;
@@ -298,8 +300,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = p.G, RT = BC / G;
   const int nblk = (p.max_pages + 3) / 4;
-  const int rank = SPLIT ? cluster_rank() : 0;
-  const int ncta = SPLIT ? kCL : 1;  // CTAs sharing one block's tiles
+  const int rank = cluster_rank();
+  const int ncta = kCL;  // CTAs sharing one block's tiles
   const Abort ab{&abort_flag, p.err};
   const uint32_t sbase = smem_addr(sm);
   const int oob_slot = p.num_pages * p.page_size;  // out-of-range coordinate: TMA fills zeros
@@ -310,18 +312,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const float kInf = __int_as_float(0x7f800000);
   const uint32_t p_base = sbase + P_OFF, ds_base = sbase + P_OFF + PS;
 
-  if (SPLIT) {
-    // the main kernel may start on the SMs these clusters leave free
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  } else {
-    // launched as the split kernel's programmatic dependent: the last CTA
-    // waits for the split grid, so this grid completes after it and later
-    // work in the stream sees both
-    if (blockIdx.x == gridDim.x - 1 && blockIdx.y == gridDim.y - 1 && blockIdx.z == gridDim.z - 1)
-      asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int tb = blockIdx.x, s0 = blockIdx.y;
-    if (tb * 4 >= pages_of(seq_len_of(p, s0), p.page_size)) return;  // no token of the sequence here (uniform)
-  }
+  // the history kernel, launched next as this grid's programmatic dependent,
+  // may start on the SMs these clusters leave free
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(&bar_k, 1);
@@ -329,7 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bar_full[1], 1);
     mbar_fence_init();
   }
-  // thread 0's copy bookkeeping (split: running over the blocks of a persistent CTA)
+  // thread 0's copy bookkeeping (running over the blocks of a persistent CTA)
   int issued[2] = {0, 0}, k_issued = 0;
   int tc = 0;       // tiles this CTA consumed: tile u uses stage u & 1, phase u >> 1
   int k_phase = 0;  // blocks this CTA loaded keys for
@@ -345,19 +338,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         do ++n_all;
         while (it.advance(RT));
       }
-      // heavy blocks (flagged by the plan kernel) belong to the split kernel
-      const int heavy = !SPLIT && any && p.heavy[item] != 0;
       any_store_sh = any;
-      heavy_sh = heavy;
       // this CTA's share of the block's tiles: [t0, t1), contiguous
       const int t0 = rank * n_all / ncta, t1 = (rank + 1) * n_all / ncta;
       tile0_sh = t0;
       n_tiles_sh = t1 - t0;
     }
     __syncthreads();
-    // pages all stored by their owners elsewhere, or a heavy block: nothing to
-    // do here (uniform over the CTA, and over the cluster: same block)
-    if (!any_store_sh || heavy_sh) return;
+    // pages all stored by their owners elsewhere: nothing to do here (uniform
+    // over the CTA, and over the cluster: same block)
+    if (!any_store_sh) return;
     const int n = n_tiles_sh;
     const int tc0 = tc;
 
@@ -373,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(st + (9 + c) * CQ, &tm_dy, bar, c * 64, gkv * G, r0);
       }
       tma_load_3d(st + 8 * CQ, &tm_qp, bar, 0, gkv * G, r0);
-      if (SPLIT) ++issued[stage];
+      ++issued[stage];
     };
     auto pf_next = [&]() -> bool { return pf.advance(RT); };
     if (threadIdx.x == 0 && n > 0 && !abort_flag) {
@@ -383,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_map(&tm_k);
       tma_prefetch_map(&tm_kp);
       mbar_arrive_expect_tx(&bar_k, 9 * CH);
-      if (SPLIT) ++k_issued;
+      ++k_issued;
       for (int j = 0; j < 4; ++j) {
         const int slot = pinfo.phys[j] >= 0 ? pinfo.phys[j] * p.page_size : oob_slot;
         for (int c = 0; c < 8; ++c) tma_load_3d(sm + K_OFF + c * CH + j * 16 * 128, &tm_k, &bar_k, c * 64, gkv, slot);
@@ -520,31 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     (void)live;
     tc = tc0 + n;
-    if (!SPLIT) {
-      // every issued copy was consumed (each tile waited for its stage); store
-      // the pages this CTA owns, one row per token, zeros where nothing was added
-      if (n > 0 && (!ok || abort_flag)) return;
-      if (!pinfo.store[tt]) return;
-      const int slot_base = pinfo.phys[tt] * p.page_size;
-#pragma unroll
-      for (int hr = 0; hr < 2; ++hr) {
-        const int64_t prow = static_cast<int64_t>(slot_base + g8 + 8 * hr) * p.KVH + gkv;
-        if (p.wrt & 2u) {
-          __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.dk_pool) + prow * kLat + 128 * dr + 2 * t4;
-#pragma unroll
-          for (int nt = 0; nt < 16; ++nt)
-            *reinterpret_cast<uint32_t*>(o + nt * 8) = pack_bf16x2(acc[nt][2 * hr], acc[nt][2 * hr + 1]);
-        }
-        if (p.wrt & 8u) {
-          __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.dkp_pool) + prow * kPos + 16 * dr + 2 * t4;
-#pragma unroll
-          for (int nt = 0; nt < 2; ++nt)
-            *reinterpret_cast<uint32_t*>(o + nt * 8) = pack_bf16x2(accp[nt][2 * hr], accp[nt][2 * hr + 1]);
-        }
-      }
-      return;
-    }
-    // split: this CTA's partial sums to shared memory as [64 tokens][576 dims]
+    // this CTA's partial sums to shared memory as [64 tokens][576 dims]
     // (the tiles' buffers are free: the loop ended on a barrier after the last
     // copy was consumed)
     float* red = reinterpret_cast<float*>(sm);
@@ -559,7 +525,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         *reinterpret_cast<float2*>(row + kLat + 16 * dr + 8 * nt + 2 * t4) =
             make_float2(accp[nt][2 * hr], accp[nt][2 * hr + 1]);
     }
+    // every CTA's abort flag is ORed over the cluster: a partial left
+    // incomplete by a timed-out wait must not reach the pool as a finite value
+    if (threadIdx.x == 0) abort_any_sh = abort_flag;
     cluster_sync();
+    if (threadIdx.x == 0) {
+      int any_abort = 0;
+      for (int r = 0; r < kCL; ++r) any_abort |= ld_cluster_s32(map_rank(smem_addr(&abort_any_sh), r));
+      if (any_abort) *ab.flag = 1;
+    }
+    __syncthreads();
     // tokens [4 rank, 4 rank + 4): the partials of CTAs 0..kCL-1 added in that order
     constexpr int kQuads = (kLat + kPos) / 4;
     const bool good = !abort_flag;
@@ -589,11 +564,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     cluster_sync();  // the other CTAs have read this CTA's partial
   };
 
-  if (!SPLIT) {
-    run_block(blockIdx.x, blockIdx.y, blockIdx.z, (blockIdx.y * nblk + blockIdx.x) * p.KVH + blockIdx.z);
-    return;
-  }
-  // split: the flagged blocks in flag order, heavy block k to cluster k mod clusters
+  // the flagged blocks in flag order, heavy block k to cluster k mod clusters
   __shared__ int items_sh[kThreads];
   __shared__ int warp_cnt[kThreads / 32];
   const int cid = cluster_index(), ncl = cluster_count();
@@ -633,484 +604,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-// ---------------------------------------------------------------------------
-// Row statistics (lse, delta) of the MLA history on the same tensor path.
-// One CTA owns 64 columns (64 / G query rows of one sequence, the G heads of
-// one KV head) with their q, qp and dY resident in shared memory, and streams
-// the sequence's keys in 32-token tiles (latent + position, double-buffered).
-// Warp (token tile tt of 16, column octet n8) computes S^T and dP^T for
-// 16 tokens x 8 columns per tile; each thread keeps, for its two columns, the
-// online maximum m, l = sum 2^(x - m) and dsum = sum 2^(x - m) dP over its
-// tokens (x = S * scale * log2 e); the partial triples are merged across lanes
-// and warps at the end:  lse = (m + log2 l) * ln 2,  delta = dsum / l
-// (= rowsum(P dP) = dY . O, the dS row offset of the page's backward).
-// ---------------------------------------------------------------------------
-constexpr int SBT = 32;                   // tokens per step (2 pages)
-constexpr int SBC = 64;                   // columns per CTA
-constexpr int SKC = SBT * 128;            // key chunk: [32 tokens][64 dims]
-constexpr int SK_STAGE = 9 * SKC;         // 8 latent chunks + 1 position chunk
-constexpr int SQC = SBC * 128;            // column chunk: [64 columns][64 dims]
-constexpr int SQ_OFF = 0;                 // q (8 chunks), qp (1), dY (8)
-constexpr int SK_OFF = SQ_OFF + 17 * SQC; // 2 stages
-constexpr int S_BYTES = SK_OFF + 2 * SK_STAGE;
-static_assert(SK_OFF % 1024 == 0 && SK_STAGE % 1024 == 0, "swizzled tiles need 1024-byte alignment");
-
-// merge two online-softmax partials (base-2 maxima)
-__device__ __forceinline__ void merge_stat(float& m, float& l, float& d, float m2, float l2, float d2) {
-  const float kNegInf = -__int_as_float(0x7f800000);
-  const float mm = fmaxf(m, m2);
-  if (mm == kNegInf) return;
-  const float a = m > kNegInf ? ex2_approx(m - mm) : 0.f, b = m2 > kNegInf ? ex2_approx(m2 - mm) : 0.f;
-  l = l * a + l2 * b;
-  d = d * a + d2 * b;
-  m = mm;
-}
-
-__global__ void __launch_bounds__(kThreads, 1)
-    mla_stats_mma_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_qp,
-                         const __grid_constant__ CUtensorMap tm_dy, const __grid_constant__ CUtensorMap tm_k,
-                         const __grid_constant__ CUtensorMap tm_kp, const PagedParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t bar_q, bar_k[2];
-  __shared__ int abort_flag, ntok_sh, seq_sh, r0_sh;
-  __shared__ float mg[3][SBC];  // the second token tile's partials: (m, l, dsum) per column
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int gkv = blockIdx.x;
-  const int G = p.G, RT2 = SBC / G;
-  // this CTA's (sequence, row tile): the row tiles of every sequence, in order
-  if (threadIdx.x == 0) {
-    int idx = blockIdx.y, sq = -1, r0 = 0;
-    for (int q = 0; q < p.S; ++q) {
-      const int tiles = (row_end_of(p, q) - row_begin_of(p, q) + RT2 - 1) / RT2;
-      if (idx < tiles) {
-        sq = q;
-        r0 = row_begin_of(p, q) + idx * RT2;
-        break;
-      }
-      idx -= tiles;
-    }
-    seq_sh = sq;
-    r0_sh = r0;
-  }
-  __syncthreads();
-  const int s = seq_sh, r0 = r0_sh;
-  if (s < 0) return;  // past the last row tile (uniform exit)
-  const int re = row_end_of(p, s);
-  const int len = seq_len_of(p, s);
-  const int npg = pages_of(len, p.page_size);
-  const Abort ab{&abort_flag, p.err};
-  const int oob_slot = p.num_pages * p.page_size;
-  if (threadIdx.x == 0) {
-    abort_flag = 0;
-    mbar_init(&bar_q, 1);
-    mbar_init(&bar_k[0], 1);
-    mbar_init(&bar_k[1], 1);
-    mbar_fence_init();
-    int ntok = len;
-    if (p.causal) {  // tokens past the largest position of the CTA's rows are never visible
-      int mp = -1;
-      for (int r = r0; r < r0 + RT2 && r < re; ++r) mp = max(mp, p.q_pos[r]);
-      ntok = min(len, mp + 1);
-    }
-    ntok_sh = max(ntok, 0);
-  }
-  __syncthreads();
-  const int nt = (ntok_sh + SBT - 1) / SBT;
-  auto issue_keys = [&](int t, int stage) {
-    uint64_t* bar = &bar_k[stage];
-    mbar_arrive_expect_tx(bar, SK_STAGE);
-    uint8_t* dst = sm + SK_OFF + stage * SK_STAGE;
-    for (int j = 0; j < 2; ++j) {
-      const int lp = 2 * t + j;
-      int slot = oob_slot;
-      if (lp < npg) {
-        const int ph = p.page_table[static_cast<int64_t>(s) * p.max_pages + lp];
-        if (ph >= 0 && ph < p.num_pages) slot = ph * p.page_size;
-      }
-      for (int c = 0; c < 8; ++c) tma_load_3d(dst + c * SKC + j * 16 * 128, &tm_k, bar, c * 64, gkv, slot);
-      tma_load_3d(dst + 8 * SKC + j * 16 * 128, &tm_kp, bar, 0, gkv, slot);
-    }
-  };
-  if (threadIdx.x == 0) {
-    mbar_arrive_expect_tx(&bar_q, 17 * SQC);
-    for (int c = 0; c < 8; ++c) {
-      tma_load_3d(sm + SQ_OFF + c * SQC, &tm_q, &bar_q, c * 64, gkv * G, r0);
-      tma_load_3d(sm + SQ_OFF + (9 + c) * SQC, &tm_dy, &bar_q, c * 64, gkv * G, r0);
-    }
-    tma_load_3d(sm + SQ_OFF + 8 * SQC, &tm_qp, &bar_q, 0, gkv * G, r0);
-    for (int t = 0; t < 2 && t < nt; ++t) issue_keys(t, t);
-  }
-
-  const int tt = warp & 1, n8 = warp >> 1;  // 2 token tiles x 8 column octets
-  const int g8 = lane >> 2, t4 = lane & 3;
-  const float kNegInf = -__int_as_float(0x7f800000);
-  int pos_c[2], r_c[2];
-  bool col_ok[2];
-#pragma unroll
-  for (int e = 0; e < 2; ++e) {
-    const int c = n8 * 8 + 2 * t4 + e;
-    r_c[e] = r0 + c / G;
-    col_ok[e] = r_c[e] < re;
-    pos_c[e] = col_ok[e] ? (p.causal ? p.q_pos[r_c[e]] : 0x7fffffff) : -1;
-  }
-  float m[2] = {kNegInf, kNegInf}, l[2] = {0.f, 0.f}, ds[2] = {0.f, 0.f};
-  const uint32_t sbase = smem_addr(sm);
-  bool ok = nt > 0 ? mbar_wait_warp(&bar_q, 0, ab) : true;
-  for (int t = 0; t < nt; ++t) {
-    const int stage = t & 1;
-    const uint32_t kb = sbase + SK_OFF + stage * SK_STAGE;
-    if (ok) ok = mbar_wait_warp(&bar_k[stage], (t >> 1) & 1, ab);
-    if (ok) {
-      float sacc[4] = {0.f, 0.f, 0.f, 0.f}, dpacc[4] = {0.f, 0.f, 0.f, 0.f};
-      const int arow = tt * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
-      const int ahalf = lane >> 4;
-      const int brow = n8 * 8 + (lane & 7);
-      const int bm = lane >> 3;
-#pragma unroll 2
-      for (int kc = 0; kc < 8; ++kc) {
-#pragma unroll
-        for (int kp = 0; kp < 4; ++kp) {
-          uint32_t a[4], bq[4];
-          ldsm_x4(swz(kb + kc * SKC, arow, 2 * kp + ahalf), a);
-          ldsm_x4(swz(sbase + SQ_OFF + ((bm >> 1) ? (9 + kc) : kc) * SQC, brow, 2 * kp + (bm & 1)), bq);
-          mma_16816(sacc, a, bq[0], bq[1]);
-          mma_16816(dpacc, a, bq[2], bq[3]);
-        }
-      }
-#pragma unroll
-      for (int kp = 0; kp < 4; ++kp) {
-        uint32_t a[4], b0, b1;
-        ldsm_x4(swz(kb + 8 * SKC, arow, 2 * kp + ahalf), a);
-        ldsm_x2(swz(sbase + SQ_OFF + 8 * SQC, brow, 2 * kp + (bm & 1)), b0, b1);
-        mma_16816(sacc, a, b0, b1);
-      }
-      // online update of this thread's two columns over its two tokens
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        float x[2];
-#pragma unroll
-        for (int hr = 0; hr < 2; ++hr) {
-          const int tok = t * SBT + tt * 16 + g8 + 8 * hr;
-          const bool vis = col_ok[e] && tok < len && tok <= pos_c[e];
-          x[hr] = vis ? sacc[2 * hr + e] * p.scale_log2 : kNegInf;
-        }
-        const float mt = fmaxf(x[0], x[1]);
-        if (mt > m[e]) {
-          const float a = m[e] > kNegInf ? ex2_approx(m[e] - mt) : 0.f;
-          l[e] *= a;
-          ds[e] *= a;
-          m[e] = mt;
-        }
-        if (m[e] > kNegInf) {
-#pragma unroll
-          for (int hr = 0; hr < 2; ++hr) {
-            const float pe = x[hr] > kNegInf ? ex2_approx(x[hr] - m[e]) : 0.f;
-            l[e] += pe;
-            ds[e] = x[hr] > kNegInf ? fmaf(pe, dpacc[2 * hr + e], ds[e]) : ds[e];
-          }
-        }
-      }
-    }
-    __syncthreads();  // stage free
-    if (threadIdx.x == 0 && t + 2 < nt && ok && !abort_flag) issue_keys(t + 2, stage);
-  }
-  // merge over the 8 lanes that share a column pair (different tokens) ...
-#pragma unroll
-  for (int e = 0; e < 2; ++e) {
-#pragma unroll
-    for (int o = 4; o < 32; o <<= 1) {
-      const float m2 = __shfl_xor_sync(0xffffffffu, m[e], o);
-      const float l2 = __shfl_xor_sync(0xffffffffu, l[e], o);
-      const float d2 = __shfl_xor_sync(0xffffffffu, ds[e], o);
-      merge_stat(m[e], l[e], ds[e], m2, l2, d2);
-    }
-  }
-  // ... and over the two token tiles
-  if (tt == 1 && g8 == 0) {
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int c = n8 * 8 + 2 * t4 + e;
-      mg[0][c] = m[e];
-      mg[1][c] = l[e];
-      mg[2][c] = ds[e];
-    }
-  }
-  __syncthreads();
-  if (nt > 0 && (!ok || abort_flag)) return;
-  if (tt == 0 && g8 == 0) {
-#pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int c = n8 * 8 + 2 * t4 + e;
-      merge_stat(m[e], l[e], ds[e], mg[0][c], mg[1][c], mg[2][c]);
-      if (col_ok[e]) {
-        const size_t idx = static_cast<size_t>(r_c[e]) * p.H + gkv * G + c % G;
-        p.lse_out[idx] = l[e] > 0.f ? (m[e] + __log2f(l[e])) * 0.6931471805599453f : kNegInf;
-        p.delta_out[idx] = l[e] > 0.f ? ds[e] / l[e] : 0.f;
-      }
-    }
-  }
-}
-
-// ---------------------------------------------------------------------------
-// Query side of the MLA backward: dQ (latent, 512) and dQp (position, 64) per
-// (query row, head), from the row statistics lse and delta of the same rows.
-// Same CTA decomposition as the row statistics (64 columns resident, keys in
-// 32-token tiles, double-buffered) and the same phase A; then per tile
-//   dS^T of the warp's 16 tokens x 8 columns -> shared memory as dS[col][token]
-//   phase B  warp (column tile mt of 16, dim quarter dq): dQ[., 128 dq ..+128)
-//            += dS K_lat and dQp[., 16 dq ..+16) += dS K_pos  (K as B operand,
-//            token-major, read with transposing ldmatrix)
-// with the fp32 accumulators (16 x 144 per warp) in registers, stored once.
-// ---------------------------------------------------------------------------
-constexpr int QDS_STRIDE = SBT * 2 + 16;       // dS rows: 32 bf16 + 16 bytes of padding
-constexpr int QDS_OFF = S_BYTES;
-constexpr int Q_BYTES = QDS_OFF + SBC * QDS_STRIDE;
-
-__global__ void __launch_bounds__(kThreads, 1)
-    mla_query_mma_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_qp,
-                         const __grid_constant__ CUtensorMap tm_dy, const __grid_constant__ CUtensorMap tm_k,
-                         const __grid_constant__ CUtensorMap tm_kp, const PagedParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t bar_q, bar_k[2];
-  __shared__ int abort_flag, ntok_sh, seq_sh, r0_sh;
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int gkv = blockIdx.x;
-  const int G = p.G, RT2 = SBC / G;
-  if (threadIdx.x == 0) {
-    int idx = blockIdx.y, sq = -1, r0 = 0;
-    for (int q = 0; q < p.S; ++q) {
-      const int tiles = (row_end_of(p, q) - row_begin_of(p, q) + RT2 - 1) / RT2;
-      if (idx < tiles) {
-        sq = q;
-        r0 = row_begin_of(p, q) + idx * RT2;
-        break;
-      }
-      idx -= tiles;
-    }
-    seq_sh = sq;
-    r0_sh = r0;
-  }
-  __syncthreads();
-  const int s = seq_sh, r0 = r0_sh;
-  if (s < 0) return;  // past the last row tile (uniform exit)
-  const int re = row_end_of(p, s);
-  const int len = seq_len_of(p, s);
-  const int npg = pages_of(len, p.page_size);
-  const Abort ab{&abort_flag, p.err};
-  const int oob_slot = p.num_pages * p.page_size;
-  if (threadIdx.x == 0) {
-    abort_flag = 0;
-    mbar_init(&bar_q, 1);
-    mbar_init(&bar_k[0], 1);
-    mbar_init(&bar_k[1], 1);
-    mbar_fence_init();
-    int ntok = len;
-    if (p.causal) {
-      int mp = -1;
-      for (int r = r0; r < r0 + RT2 && r < re; ++r) mp = max(mp, p.q_pos[r]);
-      ntok = min(len, mp + 1);
-    }
-    ntok_sh = max(ntok, 0);
-  }
-  __syncthreads();
-  const int nt = (ntok_sh + SBT - 1) / SBT;
-  auto issue_keys = [&](int t, int stage) {
-    uint64_t* bar = &bar_k[stage];
-    mbar_arrive_expect_tx(bar, SK_STAGE);
-    uint8_t* dst = sm + SK_OFF + stage * SK_STAGE;
-    for (int j = 0; j < 2; ++j) {
-      const int lp = 2 * t + j;
-      int slot = oob_slot;
-      if (lp < npg) {
-        const int ph = p.page_table[static_cast<int64_t>(s) * p.max_pages + lp];
-        if (ph >= 0 && ph < p.num_pages) slot = ph * p.page_size;
-      }
-      for (int c = 0; c < 8; ++c) tma_load_3d(dst + c * SKC + j * 16 * 128, &tm_k, bar, c * 64, gkv, slot);
-      tma_load_3d(dst + 8 * SKC + j * 16 * 128, &tm_kp, bar, 0, gkv, slot);
-    }
-  };
-  if (threadIdx.x == 0) {
-    mbar_arrive_expect_tx(&bar_q, 17 * SQC);
-    for (int c = 0; c < 8; ++c) {
-      tma_load_3d(sm + SQ_OFF + c * SQC, &tm_q, &bar_q, c * 64, gkv * G, r0);
-      tma_load_3d(sm + SQ_OFF + (9 + c) * SQC, &tm_dy, &bar_q, c * 64, gkv * G, r0);
-    }
-    tma_load_3d(sm + SQ_OFF + 8 * SQC, &tm_qp, &bar_q, 0, gkv * G, r0);
-    for (int t = 0; t < 2 && t < nt; ++t) issue_keys(t, t);
-  }
-
-  const int tt = warp & 1, n8 = warp >> 1;  // phase A: 2 token tiles x 8 column octets
-  const int mt = warp & 3, dq = warp >> 2;  // phase B: 4 column tiles x 4 dim quarters
-  const int g8 = lane >> 2, t4 = lane & 3;
-  const float kInf = __int_as_float(0x7f800000);
-  // phase-A columns of this thread: statistics, position
-  float lse_c[2], dl_c[2];
-  int pos_c[2];
-  bool col_ok[2];
-#pragma unroll
-  for (int e = 0; e < 2; ++e) {
-    const int c = n8 * 8 + 2 * t4 + e;
-    const int r = r0 + c / G, hh = gkv * G + c % G;
-    col_ok[e] = r < re;
-    const size_t si = static_cast<size_t>(col_ok[e] ? r : 0) * p.H + hh;
-    lse_c[e] = col_ok[e] ? p.lse[si] * kLog2e : kInf;
-    dl_c[e] = col_ok[e] ? p.delta[si] : 0.f;
-    pos_c[e] = col_ok[e] ? (p.causal ? p.q_pos[r] : 0x7fffffff) : -1;
-  }
-  float acc[16][4], accp[2][4];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-#pragma unroll
-  for (int i = 0; i < 2; ++i) accp[i][0] = accp[i][1] = accp[i][2] = accp[i][3] = 0.f;
-  const uint32_t sbase = smem_addr(sm);
-  const uint32_t ds_base = sbase + QDS_OFF;
-  bool ok = nt > 0 ? mbar_wait_warp(&bar_q, 0, ab) : true;
-  for (int t = 0; t < nt; ++t) {
-    const int stage = t & 1;
-    const uint32_t kb = sbase + SK_OFF + stage * SK_STAGE;
-    if (ok) ok = mbar_wait_warp(&bar_k[stage], (t >> 1) & 1, ab);
-    if (ok) {
-      // ---------------------------------------------------------------- phase A
-      float sacc[4] = {0.f, 0.f, 0.f, 0.f}, dpacc[4] = {0.f, 0.f, 0.f, 0.f};
-      const int arow = tt * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
-      const int ahalf = lane >> 4;
-      const int brow = n8 * 8 + (lane & 7);
-      const int bm = lane >> 3;
-#pragma unroll 2
-      for (int kc = 0; kc < 8; ++kc) {
-#pragma unroll
-        for (int kp = 0; kp < 4; ++kp) {
-          uint32_t a[4], bq[4];
-          ldsm_x4(swz(kb + kc * SKC, arow, 2 * kp + ahalf), a);
-          ldsm_x4(swz(sbase + SQ_OFF + ((bm >> 1) ? (9 + kc) : kc) * SQC, brow, 2 * kp + (bm & 1)), bq);
-          mma_16816(sacc, a, bq[0], bq[1]);
-          mma_16816(dpacc, a, bq[2], bq[3]);
-        }
-      }
-#pragma unroll
-      for (int kp = 0; kp < 4; ++kp) {
-        uint32_t a[4], b0, b1;
-        ldsm_x4(swz(kb + 8 * SKC, arow, 2 * kp + ahalf), a);
-        ldsm_x2(swz(sbase + SQ_OFF + 8 * SQC, brow, 2 * kp + (bm & 1)), b0, b1);
-        mma_16816(sacc, a, b0, b1);
-      }
-      // dS of this warp's 16 tokens x 8 columns, stored column-major for phase B
-#pragma unroll
-      for (int hr = 0; hr < 2; ++hr) {
-        const int i = tt * 16 + g8 + 8 * hr;  // tile-local token
-        const int tok = t * SBT + i;
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const bool vis = col_ok[e] && tok < len && tok <= pos_c[e] && lse_c[e] < kInf;
-          const float pe = ex2_approx(fmaf(sacc[2 * hr + e], p.scale_log2, -lse_c[e]));
-          // select, not multiply: S and dP of a tail slot may be NaN
-          const float dsv = vis ? pe * (dpacc[2 * hr + e] - dl_c[e]) * p.scale : 0.f;
-          const int c = n8 * 8 + 2 * t4 + e;
-          *reinterpret_cast<__nv_bfloat16*>(sm + QDS_OFF + c * QDS_STRIDE + i * 2) = __float2bfloat16_rn(dsv);
-        }
-      }
-    }
-    __syncthreads();
-    if (t * SBT + SBT > len) {  // uniform: the barrier below is reached by every thread
-      // key rows of tokens past the length inside the last page may hold any
-      // bit pattern; phase B multiplies them by dS = 0, so they are zeroed
-      if (ok) {
-        const int row_lo = max(0, len - t * SBT);
-        const int nvec = (SBT - row_lo) * 9 * 8;
-        for (int i = threadIdx.x; i < nvec; i += kThreads) {
-          const int rw = row_lo + i / 72, rem = i % 72;
-          st_shared_v4(kb + (rem >> 3) * SKC + rw * 128 + (rem & 7) * 16, 0u, 0u, 0u, 0u);
-        }
-      }
-      __syncthreads();
-    }
-    if (ok && !abort_flag) {
-      // ---------------------------------------------------------------- phase B
-      const int arow = mt * 16 + (lane & 7) + 8 * ((lane >> 3) & 1);
-      const int bm = lane >> 3;
-#pragma unroll
-      for (int ks = 0; ks < 2; ++ks) {
-        uint32_t ads[4];
-        ldsm_x4(ds_base + arow * QDS_STRIDE + (ks * 16 + 8 * (lane >> 4)) * 2, ads);
-        const int krow = ks * 16 + (lane & 7) + 8 * (bm & 1);  // token index = B row
-#pragma unroll
-        for (int np = 0; np < 8; ++np) {  // pairs of 8-dim tiles: dims 128 dq + 16 np
-          const int chunk = 2 * dq + (np >> 2);
-          const int piece = 2 * (np & 3) + (bm >> 1);
-          uint32_t bk[4];
-          ldsm_x4_t(swz(kb + chunk * SKC, krow, piece), bk);
-          mma_16816(acc[2 * np], ads, bk[0], bk[1]);
-          mma_16816(acc[2 * np + 1], ads, bk[2], bk[3]);
-        }
-        uint32_t bkp[4];
-        ldsm_x4_t(swz(kb + 8 * SKC, krow, 2 * dq + (bm >> 1)), bkp);
-        mma_16816(accp[0], ads, bkp[0], bkp[1]);
-        mma_16816(accp[1], ads, bkp[2], bkp[3]);
-      }
-    }
-    __syncthreads();  // stage and dS buffer free
-    if (threadIdx.x == 0 && t + 2 < nt && ok && !abort_flag) issue_keys(t + 2, stage);
-  }
-  if (nt > 0 && (!ok || abort_flag)) return;
-  // one store per (row, head): zeros for a column that saw no token
-#pragma unroll
-  for (int hr = 0; hr < 2; ++hr) {
-    const int c = mt * 16 + g8 + 8 * hr;
-    const int r = r0 + c / G, hh = gkv * G + c % G;
-    if (r >= re) continue;
-    const int64_t row = static_cast<int64_t>(r) * p.H + hh;
-    __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.dq) + row * kLat + 128 * dq + 2 * t4;
-#pragma unroll
-    for (int n = 0; n < 16; ++n)
-      *reinterpret_cast<uint32_t*>(o + n * 8) = pack_bf16x2(acc[n][2 * hr], acc[n][2 * hr + 1]);
-    __nv_bfloat16* op = static_cast<__nv_bfloat16*>(p.dqp) + row * kPos + 16 * dq + 2 * t4;
-#pragma unroll
-    for (int n = 0; n < 2; ++n)
-      *reinterpret_cast<uint32_t*>(op + n * 8) = pack_bf16x2(accp[n][2 * hr], accp[n][2 * hr + 1]);
-  }
-}
-
 }  // namespace
 
-bool mla_mma_supported(const PagedParams& p) {
+bool mla_split_supported(const PagedParams& p) {
   return p.Dk == kLat && p.Dp == kPos && p.page_size == 16 && (p.G == 4 || p.G == 8 || p.G == 16 || p.G == 32);
-}
-
-cudaError_t launch_paged_mla_stats_mma(const PagedMlaMaps& m, const PagedParams& p, cudaStream_t s) {
-  if (p.Nq == 0 || p.S == 0) return cudaSuccess;
-  const int smem = S_BYTES + 1024;
-  cudaError_t e = cudaFuncSetAttribute(mla_stats_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  // an upper bound on the row tiles of all sequences; each CTA finds its own
-  const int RT2 = SBC / p.G;
-  dim3 grid(p.KVH, p.Nq / RT2 + p.S + 1, 1);
-  mla_stats_mma_kernel<<<grid, kThreads, smem, s>>>(m.q, m.qp, m.dy, m.k, m.kp, p);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_paged_mla_mma(const PagedMlaMaps& m, const PagedParams& p, cudaStream_t s) {
-  if (p.num_pages == 0 || p.S == 0 || p.max_pages == 0) return cudaSuccess;
-  const int smem = BYTES + 1024;
-  auto kern = mla_mma_kernel<false>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  // programmatic dependent of the split kernel launched just before it: it
-  // may start while the split clusters run (it reads none of their results)
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  at[0].val.programmaticStreamSerializationAllowed = 1;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((p.max_pages + 3) / 4, p.S, p.KVH);
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cfg.attrs = at;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, m.q, m.qp, m.dy, m.k, m.kp, p);
 }
 
 cudaError_t launch_paged_mla_plan(const PagedParams& p, cudaStream_t s) {
@@ -1121,10 +618,10 @@ cudaError_t launch_paged_mla_plan(const PagedParams& p, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-cudaError_t launch_paged_mla_mma_split(const PagedMlaMaps& m, const PagedParams& p, cudaStream_t s) {
+cudaError_t launch_paged_mla_split(const PagedMlaMaps& m, const PagedParams& p, cudaStream_t s) {
   if (p.num_pages == 0 || p.S == 0 || p.max_pages == 0) return cudaSuccess;
   const int smem = BYTES + 1024;
-  auto kern = mla_mma_kernel<true>;
+  auto kern = mla_split_kernel;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   // 16 CTAs per cluster is above the portable 8
@@ -1154,21 +651,6 @@ cudaError_t launch_paged_mla_mma_split(const PagedMlaMaps& m, const PagedParams&
   }
   cfg.gridDim = dim3(ncl * kCL, 1, 1);
   return cudaLaunchKernelEx(&cfg, kern, m.q, m.qp, m.dy, m.k, m.kp, p);
-}
-
-}  // namespace attn
-
-namespace attn {
-
-cudaError_t launch_paged_mla_query_mma(const PagedMlaMaps& m, const PagedParams& p, cudaStream_t s) {
-  if (p.Nq == 0 || p.S == 0) return cudaSuccess;
-  const int smem = Q_BYTES + 1024;
-  cudaError_t e = cudaFuncSetAttribute(mla_query_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  const int RT2 = SBC / p.G;
-  dim3 grid(p.KVH, p.Nq / RT2 + p.S + 1, 1);
-  mla_query_mma_kernel<<<grid, kThreads, smem, s>>>(m.q, m.qp, m.dy, m.k, m.kp, p);
-  return cudaGetLastError();
 }
 
 }  // namespace attn

@@ -19,7 +19,6 @@ namespace sm103 {
 // Device error word codes (OR-ed into the word the host reads back).
 enum : uint32_t {
   DEV_ERR_TIMEOUT = 1u,      // a bounded wait gave up
-  DEV_ERR_BOUNDS = 2u,       // a device-side bounds check failed (debug builds)
 };
 
 __device__ __forceinline__ uint64_t global_timer_ns() {
@@ -254,16 +253,12 @@ __device__ __forceinline__ uint64_t sdesc_none(uint32_t saddr, uint32_t lbo_byte
          (static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32) | (1ull << 46);
 }
 
-// Instruction descriptor for kind::f16 (bf16 x bf16 -> f32) and kind::tf32.
-//   bits 4-5 D format (1 = f32); 7-9 A format; 10-12 B format (f16 kind:
-//   1 = bf16; tf32 kind: 2 = tf32); 15 A MN-major; 16 B MN-major;
+// Instruction descriptor for kind::f16 (bf16 x bf16 -> f32).
+//   bits 4-5 D format (1 = f32); 7-9 A format; 10-12 B format (1 = bf16);
+//   15 A MN-major; 16 B MN-major;
 //   17-22 N >> 3; 24-28 M >> 4.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major, bool b_mn_major) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
-         (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
-}
-__host__ __device__ constexpr uint32_t idesc_tf32(int M, int N, bool a_mn_major, bool b_mn_major) {
-  return (1u << 4) | (2u << 7) | (2u << 10) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
@@ -274,15 +269,6 @@ __device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t adesc, uin
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-__device__ __forceinline__ void mma_tf32_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                            uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }

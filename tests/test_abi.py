@@ -232,3 +232,17 @@ def test_noalloc_refuses_elem_mask(lib):
                                              None))
     assert st == bd.ATTN_ERR_UNSUPPORTED
     assert "per-element" in bd.last_error()
+
+
+def test_paged_mla_shape_checks(lib):
+    """MLA (latent 512 + position 64) takes any number of heads per KV head
+    that divides 64 (a 64-column tile holds whole query rows) and refuses the
+    others, and other latent / position sizes, before any device work; the
+    workspace query returns 0 for a refused descriptor."""
+    ok = bd.make_paged_desc(num_queries=64, num_seqs=4, heads=16, kv_heads=1, page_size=16, num_pages=100,
+                            max_pages_per_seq=10, key_dim=512, value_dim=512, position_dim=64)
+    assert bd.attn_bwd_paged_workspace_bytes(ok) > 0
+    for heads, kv, kd, pd in ((12, 4, 512, 64), (40, 1, 512, 64), (16, 1, 256, 64), (16, 1, 512, 32)):
+        d = bd.make_paged_desc(num_queries=64, num_seqs=4, heads=heads, kv_heads=kv, page_size=16, num_pages=100,
+                               max_pages_per_seq=10, key_dim=kd, value_dim=kd, position_dim=pd)
+        assert bd.attn_bwd_paged_workspace_bytes(d) == 0, (heads, kv, kd, pd)
