@@ -543,7 +543,7 @@ ATTN_API attn_status_t attn_bwd_dense_strided(const attn_dense_desc* d, const at
   if (!want_dq) p.ds_store = nullptr;
   const bool run_dkdv = want_dk || want_dv || store_ds;
 
-  const int nk = (split ? 4 : 0) + (has_elem ? 1 : 0) + 1 + (run_dkdv ? 1 : 0) + (want_dq ? 1 : 0);
+  const int nk = (split ? 1 : 0) + (has_elem ? 1 : 0) + 1 + (run_dkdv ? 1 : 0) + (want_dq ? 1 : 0);
   attn::timing_mark_begin(nk, s);
   cudaError_t e = cudaSuccess;
   if (has_elem) {
@@ -555,10 +555,9 @@ ATTN_API attn_status_t attn_bwd_dense_strided(const attn_dense_desc* d, const at
     const int64_t nq = int64_t(z.q_bytes / 4), nkv = int64_t(z.k_bytes / 4);
     const float* srcs[4] = {static_cast<const float*>(q), static_cast<const float*>(dy), static_cast<const float*>(k),
                             static_cast<const float*>(v)};
-    for (int i = 0; i < 4 && e == cudaSuccess; ++i) {
-      e = attn::launch_split_f32(srcs[i], his[i], los[i], i < 2 ? nq : nkv, s);
-      attn::timing_mark(s);
-    }
+    const int64_t ns[4] = {nq, nq, nkv, nkv};
+    e = attn::launch_split_f32(srcs, his, los, ns, s);
+    attn::timing_mark(s);
   }
   if (e == cudaSuccess) {
     e = o ? attn::launch_delta_only(p, split ? 0 : 1, s)
@@ -656,17 +655,15 @@ ATTN_API attn_status_t attn_fwd_dense_strided(const attn_dense_desc* d, const at
   p.fwd_only = 1;
   p.o_out = o;
   p.lse_out = lse;
-  attn::timing_mark_begin(split ? 4 : 1, s);
+  attn::timing_mark_begin(split ? 2 : 1, s);
   cudaError_t e = cudaSuccess;
   if (split) {
     const int64_t nq = int64_t(z.q_bytes / 4), nkv = int64_t(z.k_bytes / 4);
     const float* srcs[4] = {static_cast<const float*>(q), nullptr, static_cast<const float*>(k),
                             static_cast<const float*>(v)};
-    for (int i = 0; i < 4 && e == cudaSuccess; ++i) {
-      if (i == 1) continue;  // no dY in a forward pass
-      e = attn::launch_split_f32(srcs[i], his[i], los[i], i < 2 ? nq : nkv, s);
-      attn::timing_mark(s);
-    }
+    const int64_t ns[4] = {nq, 0, nkv, nkv};  // no dY in a forward pass
+    e = attn::launch_split_f32(srcs, his, los, ns, s);
+    attn::timing_mark(s);
   }
   if (e == cudaSuccess) {
     e = attn::launch_fwd_stats(m, p, has_bias, s);

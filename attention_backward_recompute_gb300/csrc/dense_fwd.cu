@@ -393,20 +393,32 @@ cudaError_t launch_fwd_t(const DenseMaps& m, const DenseParams& p, cudaStream_t 
   return cudaGetLastError();
 }
 
-// x -> (hi, lo): hi = bf16(x), lo = bf16(x - hi), four elements per thread.
-__global__ void split_f32_kernel(const float* __restrict__ x, __nv_bfloat16* __restrict__ hi,
-                                 __nv_bfloat16* __restrict__ lo, int64_t n) {
-  const int64_t n4 = n / 4;
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n4;
+// x -> (hi, lo): hi = bf16(x), lo = bf16(x - hi), four elements per thread,
+// for up to four tensors in one launch (jobs laid end to end in the index
+// space of the grid-stride loop).
+struct SplitJobs {
+  const float* x[4];
+  __nv_bfloat16* hi[4];
+  __nv_bfloat16* lo[4];
+  int64_t end4[4];  // cumulative element counts / 4
+  int count;
+};
+
+__global__ void split_f32_kernel(const SplitJobs jobs) {
+  const int64_t total = jobs.end4[jobs.count - 1];
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const float4 v = reinterpret_cast<const float4*>(x)[i];
+    int j = 0;
+    while (i >= jobs.end4[j]) ++j;
+    const int64_t k = i - (j > 0 ? jobs.end4[j - 1] : 0);
+    const float4 v = reinterpret_cast<const float4*>(jobs.x[j])[k];
     const __nv_bfloat162 h0 = __floats2bfloat162_rn(v.x, v.y), h1 = __floats2bfloat162_rn(v.z, v.w);
     const __nv_bfloat162 l0 = __floats2bfloat162_rn(v.x - __low2float(h0), v.y - __high2float(h0));
     const __nv_bfloat162 l1 = __floats2bfloat162_rn(v.z - __low2float(h1), v.w - __high2float(h1));
-    reinterpret_cast<__nv_bfloat162*>(hi)[2 * i] = h0;
-    reinterpret_cast<__nv_bfloat162*>(hi)[2 * i + 1] = h1;
-    reinterpret_cast<__nv_bfloat162*>(lo)[2 * i] = l0;
-    reinterpret_cast<__nv_bfloat162*>(lo)[2 * i + 1] = l1;
+    reinterpret_cast<__nv_bfloat162*>(jobs.hi[j])[2 * k] = h0;
+    reinterpret_cast<__nv_bfloat162*>(jobs.hi[j])[2 * k + 1] = h1;
+    reinterpret_cast<__nv_bfloat162*>(jobs.lo[j])[2 * k] = l0;
+    reinterpret_cast<__nv_bfloat162*>(jobs.lo[j])[2 * k + 1] = l1;
   }
 }
 
@@ -454,11 +466,22 @@ cudaError_t launch_fwd_stats(const DenseMaps& m, const DenseParams& p, bool bias
   return bias ? launch_fwd_t<128, true, false>(m, p, s) : launch_fwd_t<128, false, false>(m, p, s);
 }
 
-cudaError_t launch_split_f32(const float* x, void* hi, void* lo, int64_t n, cudaStream_t s) {
-  if (n <= 0) return cudaSuccess;
-  const int64_t blocks = (n / 4 + 255) / 256;
-  split_f32_kernel<<<static_cast<int>(blocks < 152 * 16 ? blocks : 152 * 16), 256, 0, s>>>(
-      x, static_cast<__nv_bfloat16*>(hi), static_cast<__nv_bfloat16*>(lo), n);
+cudaError_t launch_split_f32(const float* const x[4], void* const hi[4], void* const lo[4], const int64_t n[4],
+                             cudaStream_t s) {
+  SplitJobs jobs{};
+  int64_t acc = 0;
+  for (int i = 0; i < 4; ++i) {
+    if (n[i] <= 0) continue;
+    jobs.x[jobs.count] = x[i];
+    jobs.hi[jobs.count] = static_cast<__nv_bfloat16*>(hi[i]);
+    jobs.lo[jobs.count] = static_cast<__nv_bfloat16*>(lo[i]);
+    acc += n[i] / 4;
+    jobs.end4[jobs.count] = acc;
+    ++jobs.count;
+  }
+  if (jobs.count == 0 || acc == 0) return cudaSuccess;
+  const int64_t blocks = (acc + 255) / 256;
+  split_f32_kernel<<<static_cast<int>(blocks < 152 * 16 ? blocks : 152 * 16), 256, 0, s>>>(jobs);
   return cudaGetLastError();
 }
 

@@ -39,7 +39,10 @@ cudaError_t launch_zero_rows(void* x, int64_t sb, int64_t ss, int64_t sh, int64_
                              size_t es, cudaStream_t s);
 cudaError_t launch_delta_only(const DenseParams& p, int dtype_bf16, cudaStream_t s);
 // Split fp32 tensors into hi/lo bf16 copies: hi = bf16(x), lo = bf16(x - hi).
-cudaError_t launch_split_f32(const float* x, void* hi, void* lo, int64_t n, cudaStream_t s);
+// hi = bf16(x), lo = bf16(x - hi) for up to four fp32 tensors of n[i]
+// elements (multiples of 4; a count <= 0 skips the tensor), one launch.
+cudaError_t launch_split_f32(const float* const x[4], void* const hi[4], void* const lo[4], const int64_t n[4],
+                             cudaStream_t s);
 cudaError_t launch_dkdv(const DenseMaps& m, const DenseParams& p, bool bias, cudaStream_t s);
 // bf16 storage: softmax and dS on separate warpgroups, P and dS in tensor memory
 cudaError_t launch_dkdv2(const DenseMaps& m, const DenseParams& p, bool bias, cudaStream_t s);
