@@ -164,12 +164,23 @@ __device__ __forceinline__ void store_row32(uint32_t tile, uint32_t copy_bytes, 
 
 // Store 32 fp32 accumulator values (times f) of one output row, columns
 // col0..col0+31 limited to D: bf16 (round to nearest even) or, with SPLIT
-// (fp32 storage), fp32.  `row_off` is the row's element offset.
+// (fp32 storage), fp32.  `row_off` is the row's element offset.  A whole
+// chunk at a 32-byte aligned address goes out as 32-byte stores.
 template <bool SPLIT>
 __device__ __forceinline__ void store_out32(void* out, int64_t row_off, int col0, int D, const uint32_t (&r)[32],
                                             float f) {
   if (SPLIT) {
     float* o = reinterpret_cast<float*>(out) + row_off + col0;
+    if (col0 + 32 <= D && (reinterpret_cast<uintptr_t>(o) & 31u) == 0) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint32_t v[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] = __float_as_uint(__uint_as_float(r[8 * j + e]) * f);
+        sm103::st_global_v8(o + 8 * j, v);
+      }
+      return;
+    }
 #pragma unroll
     for (int j = 0; j < 8; ++j)
       if (col0 + 4 * j < D)
@@ -177,17 +188,7 @@ __device__ __forceinline__ void store_out32(void* out, int64_t row_off, int col0
             make_float4(__uint_as_float(r[4 * j]) * f, __uint_as_float(r[4 * j + 1]) * f,
                         __uint_as_float(r[4 * j + 2]) * f, __uint_as_float(r[4 * j + 3]) * f);
   } else {
-    __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(out) + row_off + col0;
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-      if (col0 + 8 * j < D) {
-        uint4 v;
-        v.x = sm103::pack_bf16x2(__uint_as_float(r[8 * j]) * f, __uint_as_float(r[8 * j + 1]) * f);
-        v.y = sm103::pack_bf16x2(__uint_as_float(r[8 * j + 2]) * f, __uint_as_float(r[8 * j + 3]) * f);
-        v.z = sm103::pack_bf16x2(__uint_as_float(r[8 * j + 4]) * f, __uint_as_float(r[8 * j + 5]) * f);
-        v.w = sm103::pack_bf16x2(__uint_as_float(r[8 * j + 6]) * f, __uint_as_float(r[8 * j + 7]) * f);
-        *reinterpret_cast<uint4*>(o + 8 * j) = v;
-      }
+    sm103::store_row32_bf16(reinterpret_cast<__nv_bfloat16*>(out) + row_off + col0, r, f, D - col0);
   }
 }
 

@@ -510,17 +510,7 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
           for (int q = 0; q < 32; ++q) r[q] = 0u;
         }
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          if (mine && cc * 32 + q * 8 < dim) {
-            uint4 v;
-            v.x = pack_bf16x2(__uint_as_float(r[8 * q]) * f, __uint_as_float(r[8 * q + 1]) * f);
-            v.y = pack_bf16x2(__uint_as_float(r[8 * q + 2]) * f, __uint_as_float(r[8 * q + 3]) * f);
-            v.z = pack_bf16x2(__uint_as_float(r[8 * q + 4]) * f, __uint_as_float(r[8 * q + 5]) * f);
-            v.w = pack_bf16x2(__uint_as_float(r[8 * q + 6]) * f, __uint_as_float(r[8 * q + 7]) * f);
-            *reinterpret_cast<uint4*>(out + cc * 32 + q * 8) = v;
-          }
-        }
+        if (mine) store_row32_bf16(out + cc * 32, r, f, dim - cc * 32);
       }
       if (n > 0) {
         tc_fence_before();

@@ -490,15 +490,7 @@ __global__ void __launch_bounds__(384, 1)
           __nv_bfloat16* out = pos_chunk
                                    ? static_cast<__nv_bfloat16*>(p.dkp_pool) + prow * kPos + (cc - 8) * 32
                                    : static_cast<__nv_bfloat16*>(p.dk_pool) + prow * kLat + 256 * PART + cc * 32;
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            uint4 v;
-            v.x = pack_bf16x2(__uint_as_float(r[8 * i]), __uint_as_float(r[8 * i + 1]));
-            v.y = pack_bf16x2(__uint_as_float(r[8 * i + 2]), __uint_as_float(r[8 * i + 3]));
-            v.z = pack_bf16x2(__uint_as_float(r[8 * i + 4]), __uint_as_float(r[8 * i + 5]));
-            v.w = pack_bf16x2(__uint_as_float(r[8 * i + 6]), __uint_as_float(r[8 * i + 7]));
-            *reinterpret_cast<uint4*>(out + 8 * i) = v;
-          }
+          store_row32_bf16(out, r, 1.f, 32);
         }
       }
     }

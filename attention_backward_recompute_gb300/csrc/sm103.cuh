@@ -409,6 +409,43 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* r) {
                "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
                : "memory");
 }
+// 32-byte global store (the address must be 32-byte aligned): one full
+// sector per thread, half the row requests of two 16-byte stores when the
+// threads of a warp write different rows.
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t (&v)[8]) {
+  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(v[0]), "r"(v[1]), "r"(v[2]),
+               "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+
+// 32 fp32 values of one output row (times f) as bf16, round to nearest even,
+// to o[0, valid): 32-byte stores when the whole chunk is in range and o is
+// 32-byte aligned, 16-byte stores of 8 values otherwise (o 16-byte aligned).
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi);
+__device__ __forceinline__ void store_row32_bf16(void* o, const uint32_t (&r)[32], float f, int valid) {
+  if (valid >= 32 && (reinterpret_cast<uintptr_t>(o) & 31u) == 0) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      uint32_t v[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        v[e] = pack_bf16x2(__uint_as_float(r[16 * j + 2 * e]) * f, __uint_as_float(r[16 * j + 2 * e + 1]) * f);
+      st_global_v8(static_cast<uint8_t*>(o) + 32 * j, v);
+    }
+    return;
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    if (8 * j < valid) {
+      uint4 v;
+      v.x = pack_bf16x2(__uint_as_float(r[8 * j]) * f, __uint_as_float(r[8 * j + 1]) * f);
+      v.y = pack_bf16x2(__uint_as_float(r[8 * j + 2]) * f, __uint_as_float(r[8 * j + 3]) * f);
+      v.z = pack_bf16x2(__uint_as_float(r[8 * j + 4]) * f, __uint_as_float(r[8 * j + 5]) * f);
+      v.w = pack_bf16x2(__uint_as_float(r[8 * j + 6]) * f, __uint_as_float(r[8 * j + 7]) * f);
+      *reinterpret_cast<uint4*>(static_cast<uint8_t*>(o) + 16 * j) = v;
+    }
+}
+
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 

@@ -302,6 +302,16 @@ def sweep(args) -> int:
                                          key_mask=km, bias=bias, o=o, lse=lse, outputs=outs,
                                          store_ds=bool(opt.get("store_ds")))
         ms, ms_min = timed(call, 20 if c.seq_q * c.seq_k * c.batch * c.heads > 1e7 else 50)
+        # per-kernel split of one call (fp32 storage first splits its inputs)
+        names = (["split"] if c.dtype == "f32" else []) + ["prologue", "dkdv", "dq"]
+        kev = [torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
+        for e in kev:  # CUDA events are created on first record
+            e.record()
+        torch.cuda.synchronize()
+        bd.attn_set_timing_events([e.cuda_event for e in kev])
+        call()
+        torch.cuda.synchronize()
+        kernel_ms = {n: kev[i].elapsed_time(kev[i + 1]) for i, n in enumerate(names)}
         vp = visible_pairs(c.seq_q, c.seq_k, c.causal, c.window)
         flops = 10.0 * c.head_dim * vp * c.batch * c.heads
         heads = [(b, h) for b in range(c.batch) for h in range(c.heads)]
@@ -321,7 +331,7 @@ def sweep(args) -> int:
                 gs = np.stack([gh[b, h] for b, h in sample]); ws = np.stack([w[b, h] for b, h in sample])
             errs.append(float(np.max(np.abs(gs - ws)) / max(np.max(np.abs(ws)), 1e-30)))
         tflops = flops / (ms * 1e-3) / 1e12
-        emit({"config": tag, "workload": name, "gpu_ms_median": ms, "gpu_ms_min": ms_min,
+        emit({"config": tag, "workload": name, "gpu_ms_median": ms, "gpu_ms_min": ms_min, "kernel_ms": kernel_ms,
               "counted_tflops": tflops, "pct_of_bf16_peak": 100.0 * tflops / peaks["bf16_tflops"],
               "max_err_rel": max(errs), "tolerance": 2e-4 if c.dtype == "f32" else 2e-2,
               "oracle_s_sample": t_or, "oracle_sample": f"{len(sample)} of {len(heads)} (batch, head) pairs",
