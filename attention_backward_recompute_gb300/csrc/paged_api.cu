@@ -65,7 +65,7 @@ attn_status_t check_paged_desc(const attn_paged_desc* d, PagedSizes* z) {
   z->off_fill = z->off_off + a256(size_t(d->num_pages + 1) * 4);
   z->off_links = z->off_fill + a256(size_t(d->num_pages) * 4);
   z->off_heavy = z->off_links + a256(size_t(d->num_seqs) * d->max_pages_per_seq * 4 + 4);
-  z->off_listed = z->off_heavy + a256(size_t(d->num_seqs) * ((d->max_pages_per_seq + 3) / 4) * d->kv_heads * 4 + 4);
+  z->off_listed = z->off_heavy + a256(size_t(d->num_seqs) * ((d->max_pages_per_seq + 7) / 8) * d->kv_heads * 4 + 4);
   z->ws_bytes = z->off_listed + a256(size_t(d->num_pages) + 4);
   return ATTN_OK;
 }
@@ -233,40 +233,30 @@ ATTN_API attn_status_t attn_bwd_paged_compact(const attn_paged_desc* d, const vo
     // links, zeros for pages no link references, then two CTAs per 128-token
     // block of every sequence (tcgen05); blocks whose shared pages carry many
     // links go to the cluster-split kernel first
-    attn::PagedMlaMaps mm;
-    std::memset(&mm, 0, sizeof(mm));
-    const uint64_t slots = uint64_t(d->num_pages) * d->page_size;
-    const bool split = attn::mla_split_supported(p);
-    // query-side boxes of 64 columns (64/G rows) for the tcgen05 kernel, of
-    // 32 columns for the cluster-split kernel
-    const uint32_t G = uint32_t(p.G), RT = 64u / G, RS = split ? 32u / G : RT;
     attn::PagedMlaMaps mt;
-    bool enc = encode3d(&mm.k, k_pool, d->key_dim, d->kv_heads, slots, 64, 1, uint32_t(d->page_size)) &&
-               encode3d(&mm.kp, kp_pool, d->position_dim, d->kv_heads, slots, 64, 1, uint32_t(d->page_size));
+    std::memset(&mt, 0, sizeof(mt));
+    const uint64_t slots = uint64_t(d->num_pages) * d->page_size;
+    // query-side boxes of 64 columns (64/G rows)
+    const uint32_t G = uint32_t(p.G), RT = 64u / G;
+    bool enc = encode3d(&mt.k, k_pool, d->key_dim, d->kv_heads, slots, 64, 1, uint32_t(d->page_size)) &&
+               encode3d(&mt.kp, kp_pool, d->position_dim, d->kv_heads, slots, 64, 1, uint32_t(d->page_size));
     if (d->num_queries > 0)
-      enc = enc && encode3d(&mm.q, q, d->key_dim, d->heads, d->num_queries, 64, G, RS) &&
-            encode3d(&mm.qp, qp, d->position_dim, d->heads, d->num_queries, 64, G, RS) &&
-            encode3d(&mm.dy, dy, d->value_dim, d->heads, d->num_queries, 64, G, RS) &&
-            encode3d(&mt.q, q, d->key_dim, d->heads, d->num_queries, 64, G, RT) &&
+      enc = enc && encode3d(&mt.q, q, d->key_dim, d->heads, d->num_queries, 64, G, RT) &&
             encode3d(&mt.qp, qp, d->position_dim, d->heads, d->num_queries, 64, G, RT) &&
             encode3d(&mt.dy, dy, d->value_dim, d->heads, d->num_queries, 64, G, RT);
     else
-      mm.q = mm.qp = mm.dy = mt.q = mt.qp = mt.dy = mm.k;
+      mt.q = mt.qp = mt.dy = mt.k;
     if (!enc) return api_fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed");
-    mt.k = mm.k;
-    mt.kp = mm.kp;
-    if (!split) p.heavy = nullptr;
     attn::timing_mark_begin(5, s);
     cudaError_t e = attn::launch_paged_prep(p, s);
     attn::timing_mark(s);
     if (e == cudaSuccess) e = attn::launch_paged_zero_unlinked(p, compact ? history_pages : nullptr, num_history_pages, s);
     attn::timing_mark(s);
-    if (split && e == cudaSuccess) e = attn::launch_paged_mla_plan(p, s);
-    if (split && e == cudaSuccess) e = attn::launch_paged_mla_tc_pair_heavy(p, s);
+    if (e == cudaSuccess) e = attn::launch_paged_mla_tc_plan(p, s);
     attn::timing_mark(s);
-    if (split && e == cudaSuccess) e = attn::launch_paged_mla_split(mm, p, s);
+    if (e == cudaSuccess) e = attn::launch_paged_mla_tc_split(mt, p, s);
     attn::timing_mark(s);
-    if (e == cudaSuccess) e = attn::launch_paged_mla_tc(mt, p, split, s);
+    if (e == cudaSuccess) e = attn::launch_paged_mla_tc(mt, p, true, s);
     attn::timing_mark(s);
     attn::timing_mark_end();
     if (e != cudaSuccess) return api_fail(ATTN_ERR_CUDA, "paged launch failed: %s", cudaGetErrorString(e));

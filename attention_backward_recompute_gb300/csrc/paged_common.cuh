@@ -41,7 +41,7 @@ struct PagedParams {
   int32_t* link_off;           // [num_pages + 1]
   int32_t* link_fill;          // [num_pages]
   int32_t* links;              // [S * max_pages]: link ids s*max_pages+lp grouped by page
-  int32_t* heavy;              // [S, ceil(max_pages / 4), KVH]: MLA blocks left to the split kernel
+  int32_t* heavy;              // [S, ceil(max_pages / 8), KVH]: MLA blocks left to the split kernel
   uint8_t* listed;             // [num_pages] compact history: 1 = compute and store the page; null = all
   uint32_t* err;
 };

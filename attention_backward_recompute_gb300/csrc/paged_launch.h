@@ -35,19 +35,18 @@ struct PagedMlaMaps {
 // compact history: p.listed[page] = 1 for the n listed pages (zero otherwise)
 cudaError_t launch_paged_listed(const PagedParams& p, const int32_t* pages, int64_t n, cudaStream_t s);
 // MLA history on tcgen05 (two CTAs per 128-token block, each accumulating
-// half of the dims); maps with 64-column boxes (64/G rows).  Blocks with a
-// heavy 64-token half (p.heavy, when not null) are left to the split kernel;
-// after_split: that kernel was launched just before (the first part then
-// starts as its programmatic dependent)
+// half of the dims); maps with 64-column boxes (64/G rows).  Blocks the plan
+// flagged (p.heavy, when not null) are left to the split kernel; after_split:
+// that kernel was launched just before (the first part then starts as its
+// programmatic dependent)
 bool mla_tc_supported(const PagedParams& p);
 cudaError_t launch_paged_mla_tc(const PagedMlaMaps& m, const PagedParams& p, bool after_split, cudaStream_t s);
-// flags the MLA history blocks (64 tokens) whose shared pages carry many link
-// tiles (p.heavy), then extends each flag to both halves of a 128-token block
-cudaError_t launch_paged_mla_plan(const PagedParams& p, cudaStream_t s);
-cudaError_t launch_paged_mla_tc_pair_heavy(const PagedParams& p, cudaStream_t s);
-// the flagged blocks, by clusters of 16 CTAs (maps with 32-column boxes)
-bool mla_split_supported(const PagedParams& p);
-cudaError_t launch_paged_mla_split(const PagedMlaMaps& m, const PagedParams& p, cudaStream_t s);
+// flags the 128-token MLA history blocks whose shared pages carry many link
+// tiles (p.heavy [S, ceil(max_pages / 8), KVH])
+cudaError_t launch_paged_mla_tc_plan(const PagedParams& p, cudaStream_t s);
+// the flagged blocks, by persistent clusters of 8 CTAs on tcgen05 (the same
+// maps as launch_paged_mla_tc)
+cudaError_t launch_paged_mla_tc_split(const PagedMlaMaps& m, const PagedParams& p, cudaStream_t s);
 // MLA row statistics on tcgen05; maps with 128-column boxes (128/G rows)
 bool mla_stats_tc_supported(const PagedParams& p);
 cudaError_t launch_paged_mla_stats_tc(const PagedMlaMaps& m, const PagedParams& p, cudaStream_t s);

@@ -22,6 +22,16 @@
 // (PART 0: latent dims [0, 256); PART 1: latent dims [256, 512) and the 64
 // position dims); each forms the full S^T and dP^T of its tiles.
 //
+// A block whose shared pages carry many link tiles (a long prefix shared by
+// many sequences) would serialise the other sequences' work on its one owner:
+// a plan kernel flags such blocks, the grid kernel leaves them, and a
+// persistent kernel of 8-CTA clusters takes them, one (block, part) per
+// cluster at a time.  CTA r of the cluster runs the r-th contiguous eighth of
+// the block's tiles through the same pipeline into its own tensor-memory
+// accumulator; the eight partial sums meet in shared memory and each CTA adds
+// 16 tokens' partials over the cluster in rank order (distributed shared
+// memory: a fixed order, no atomics, no workspace), then stores them.
+//
 // Shared memory: the K tile stays resident (latent + position, 9 chunks of
 // [128 tokens x 64 dims], 144 KiB); Q, Qp and dY arrive as a stream of 8 KiB
 // chunks ([64 columns x 64 dims]) through a 4-stage TMA ring of two chunk
@@ -37,6 +47,8 @@
 // TMEM lane per token).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+
+#include <atomic>
 
 #include "paged_common.cuh"
 #include "paged_launch.h"
@@ -87,107 +99,87 @@ __device__ __forceinline__ int acc_src_chunk(int a) {
   return a < 4 ? 4 * PART + a : 4 * PART + a - 4;  // 8 = the position chunk
 }
 
+// The barriers of the block pipeline: one set per CTA, reused block after
+// block by a persistent CTA.
+struct TcBars {
+  uint64_t k, full[kStages], empty[kStages], st_full[kStatSlots], st_empty[kStatSlots], s_full[2], p_full[2],
+      dp_full, ds_full, acc;
+};
+
+__device__ __forceinline__ void tc_bars_init(TcBars& b) {
+  mbar_init(&b.k, 1);
+  for (int s = 0; s < kStages; ++s) {
+    mbar_init(&b.full[s], 1);
+    mbar_init(&b.empty[s], 1);
+  }
+  for (int s = 0; s < kStatSlots; ++s) {
+    mbar_init(&b.st_full[s], 1);
+    mbar_init(&b.st_empty[s], 4);
+  }
+  for (int s = 0; s < 2; ++s) {
+    mbar_init(&b.s_full[s], 1);
+    mbar_init(&b.p_full[s], 4);
+  }
+  mbar_init(&b.dp_full, 1);
+  mbar_init(&b.ds_full, 4);
+  mbar_init(&b.acc, 1);
+  mbar_fence_init();
+}
+
+// What the CTA ran before the current block: tiles (score buffers, statistics
+// slots), ring jobs and blocks with at least one tile (key tile, accumulator
+// commit).  Every barrier phase of a block follows from these.
+struct TcEpoch {
+  int T, Q, B;
+};
+
+// ring jobs per tile: S^T chunks in 5 jobs, dP^T in 4, the accumulation in
+// ceil(NACC / 2)
 template <int PART>
-__global__ void __launch_bounds__(384, 1)
-    mla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_qp,
-                  const __grid_constant__ CUtensorMap tm_dy, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_kp, const PagedParams p) {
+__host__ __device__ constexpr int jobs_per_tile() {
+  return 9 + (PartShape<PART>::NACC + 1) / 2;
+}
+
+// Start `it` at tile t of the block's tile sequence (one pass at a time).
+__device__ __forceinline__ bool pass_seek(PassIter& it, int rt, int t) {
+  if (!it.begin(rt)) return false;
+  while (t >= it.ntiles - it.tile) {
+    t -= it.ntiles - it.tile;
+    if (!it.next_pass(rt)) return false;
+  }
+  it.tile += t;
+  return true;
+}
+
+// Tiles [t_begin, t_begin + n) (n > 0) of block tb of sequence s0, KV head
+// g, accumulated into tensor memory [T_ACC, T_ACC + ACC_COLS) (the first
+// contribution overwrites).  Every role of the CTA calls it; when the
+// compute warps return, the accumulator is complete.  Returns false (warp-
+// uniformly) when a wait ran out or the CTA is aborting.
+template <int PART>
+__device__ __forceinline__ bool run_block(const CUtensorMap* tm_q, const CUtensorMap* tm_qp, const CUtensorMap* tm_dy,
+                                          const CUtensorMap* tm_k, const CUtensorMap* tm_kp, const PagedParams& p,
+                                          TcBars& b, uint8_t* sm, uint32_t tmem, const PageInfo& pinfo, int s0, int tb,
+                                          int g, int t_begin, int n, const TcEpoch& ep, const Abort& ab) {
   using PS = PartShape<PART>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t bar_k, bar_full[kStages], bar_empty[kStages], bar_st_full[kStatSlots],
-      bar_st_empty[kStatSlots], bar_s_full[2], bar_p_full[2], bar_dp_full, bar_ds_full, bar_acc;
-  __shared__ uint32_t tmem_base_sh;
-  __shared__ int abort_flag;
-  __shared__ PageInfo pinfo;
-  __shared__ int n_tiles_sh, any_store_sh;
-
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = blockIdx.x, tb = blockIdx.y, s0 = blockIdx.z;
-  // Launched as the programmatic dependent of the kernel before it (the
-  // cluster-split kernel, or PART 0 for PART 1), whose results it does not
-  // read: its own dependent may start at once, and the last CTA waits for the
-  // kernel before, so that this grid completes after it and later work in
-  // the stream sees both.  Without a programmatic launch both are no-ops.
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (blockIdx.x == gridDim.x - 1 && blockIdx.y == gridDim.y - 1 && blockIdx.z == gridDim.z - 1)
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int len0 = seq_len_of(p, s0);
-  const int npg = pages_of(len0, p.page_size);
-  if (tb * 8 >= npg) return;  // no token of this sequence in the block (uniform exit)
-  const int RT = BC / p.G;    // query rows per tile
-  const Abort ab{&abort_flag, p.err};
-
-  if (threadIdx.x == 0) {
-    abort_flag = 0;
-    mbar_init(&bar_k, 1);
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&bar_full[s], 1);
-      mbar_init(&bar_empty[s], 1);
-    }
-    for (int s = 0; s < kStatSlots; ++s) {
-      mbar_init(&bar_st_full[s], 1);
-      mbar_init(&bar_st_empty[s], 4);
-    }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&bar_s_full[s], 1);
-      mbar_init(&bar_p_full[s], 4);
-    }
-    mbar_init(&bar_dp_full, 1);
-    mbar_init(&bar_ds_full, 4);
-    mbar_init(&bar_acc, 1);
-    mbar_fence_init();
-    int any = fill_page_info(p, s0, tb, npg, &pinfo);
-    // a block with a heavy 64-token half belongs to the cluster-split kernel
-    if (any && p.heavy) {
-      const int nb64 = (p.max_pages + 3) / 4;
-      const int64_t h0 = (static_cast<int64_t>(s0) * nb64 + 2 * tb) * p.KVH + g;
-      if (p.heavy[h0] || (2 * tb + 1 < nb64 && p.heavy[h0 + p.KVH])) any = 0;
-    }
-    any_store_sh = any;
-    PassIter it{&p, &pinfo, s0, tb};
-    int n = 0;
-    if (any && it.begin(RT)) {
-      do ++n;
-      while (it.advance(RT));
-    }
-    n_tiles_sh = n;
-  }
-  __syncthreads();
-  // a block whose pages are all stored by other CTAs (their owners) has
-  // nothing to write: leave before taking tensor memory (uniform exit)
-  if (!any_store_sh) return;
-  if (warp == 1) {
-    tmem_alloc(&tmem_base_sh, TMEM_COLS);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = tmem_base_sh;
-  const int n = n_tiles_sh;
+  const int RT = BC / p.G;                         // query rows per tile
   const int oob_slot = p.num_pages * p.page_size;  // out-of-range coordinate: TMA fills zeros
-
-  if (n > 0 && warp == 0) {
+  if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      tma_prefetch_map(&tm_q);
-      tma_prefetch_map(&tm_qp);
-      tma_prefetch_map(&tm_dy);
-      tma_prefetch_map(&tm_k);
-      tma_prefetch_map(&tm_kp);
-      mbar_arrive_expect_tx(&bar_k, 9 * KCH);
+      mbar_arrive_expect_tx(&b.k, 9 * KCH);
       for (int j = 0; j < 8; ++j) {
         const int slot = pinfo.phys[j] >= 0 ? pinfo.phys[j] * p.page_size : oob_slot;
         for (int c = 0; c < 8; ++c)
-          tma_load_3d(sm + K_OFF + c * KCH + j * 16 * 128, &tm_k, &bar_k, c * 64, g, slot);
-        tma_load_3d(sm + K_OFF + 8 * KCH + j * 16 * 128, &tm_kp, &bar_k, 0, g, slot);
+          tma_load_3d(sm + K_OFF + c * KCH + j * 16 * 128, tm_k, &b.k, c * 64, g, slot);
+        tma_load_3d(sm + K_OFF + 8 * KCH + j * 16 * 128, tm_kp, &b.k, 0, g, slot);
       }
     }
     PassIter it{&p, &pinfo, s0, tb};
-    it.begin(RT);
+    pass_seek(it, RT, t_begin);
     bool ok = true;
-    int q = 0;          // job counter of the ring (a job: one or two chunks)
+    int q = ep.Q;       // job counter of the ring (a job: one or two chunks)
     int prev_row0 = 0;  // first query row of the previous tile
     int last_use[kStages];
     for (int i = 0; i < kStages; ++i) last_use[i] = -1;
@@ -218,13 +210,13 @@ __global__ void __launch_bounds__(384, 1)
     // (src 0; chunk 8 is Qp) or dY (src 2)
     auto load_job = [&](int src, int c, int nch, int row0) -> bool {
       const int s = q % kStages;
-      if (q >= kStages && !mbar_wait(&bar_empty[s], ((q / kStages) - 1) & 1, ab)) return false;
+      if (q >= kStages && !mbar_wait(&b.empty[s], ((q / kStages) - 1) & 1, ab)) return false;
       if (lane == 0) {
-        mbar_arrive_expect_tx(&bar_full[s], nch * QCH);
+        mbar_arrive_expect_tx(&b.full[s], nch * QCH);
         for (int k = 0; k < nch; ++k) {
           const int cc = c + k;
-          const CUtensorMap* m = src == 2 ? &tm_dy : cc == 8 ? &tm_qp : &tm_q;
-          tma_load_3d(sm + RING_OFF + s * STAGE + k * QCH, m, &bar_full[s], cc == 8 ? 0 : cc * 64, g * p.G, row0);
+          const CUtensorMap* m = src == 2 ? tm_dy : cc == 8 ? tm_qp : tm_q;
+          tma_load_3d(sm + RING_OFF + s * STAGE + k * QCH, m, &b.full[s], cc == 8 ? 0 : cc * 64, g * p.G, row0);
         }
       }
       last_use[s] = q;
@@ -243,8 +235,8 @@ __global__ void __launch_bounds__(384, 1)
         const int row0 = it.r_begin + it.tile * RT;
         // column statistics of tile t: -L2, delta, pos per column (a row
         // with lse = -inf sees no token), plus the pass's token mapping
-        const int ss = t % kStatSlots;
-        if (t >= kStatSlots && !(ok = mbar_wait(&bar_st_empty[ss], ((t / kStatSlots) - 1) & 1, ab))) break;
+        const int gt = ep.T + t, ss = gt % kStatSlots;
+        if (gt >= kStatSlots && !(ok = mbar_wait(&b.st_empty[ss], ((gt / kStatSlots) - 1) & 1, ab))) break;
         uint8_t* st = sm + ST_OFF + ss * ST_SLOT;
         float* snl = reinterpret_cast<float*>(st);
         float* sdl = snl + BC;
@@ -265,7 +257,7 @@ __global__ void __launch_bounds__(384, 1)
           sinfo[3] = f_info[3];
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bar_st_full[ss]);
+        if (lane == 0) mbar_arrive(&b.st_full[ss]);
         PassIter nx = it;
         if (t + 1 < n) {
           nx.advance(RT);
@@ -285,10 +277,11 @@ __global__ void __launch_bounds__(384, 1)
     }
     if (lane == 0) {
       for (int s = 0; s < kStages; ++s)
-        if (last_use[s] >= 0) drain_wait(&bar_full[s], (last_use[s] / kStages) & 1);
-      drain_wait(&bar_k, 0);
+        if (last_use[s] >= 0) drain_wait(&b.full[s], (last_use[s] / kStages) & 1);
+      drain_wait(&b.k, ep.B & 1);
     }
-  } else if (n > 0 && warp == 1) {
+    return ok;
+  } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     // the whole warp runs this role (warp-uniform); elected lanes issue
     constexpr uint32_t id_s = idesc_bf16(128, BC, false, false);   // S^T, dP^T: K-major A and B
@@ -296,23 +289,24 @@ __global__ void __launch_bounds__(384, 1)
     const uint64_t dK0 = sdesc_sw128(smem_addr(sm + K_OFF), 16, 1024);
     const uint64_t dR0 = sdesc_sw128(smem_addr(sm + RING_OFF), 16, 1024);            // K-major
     const uint64_t dRm0 = sdesc_sw128(smem_addr(sm + RING_OFF), BC * 128, 1024);     // MN-major
-    bool ok = mbar_wait_warp(&bar_k, 0, ab);
-    int q = 0;
+    bool ok = mbar_wait_warp(&b.k, ep.B & 1, ab);
+    int q = ep.Q;
     // a stage's copies are usually in by the time this warp reaches it: a
     // non-blocking test first, the bounded wait only when it is not
     auto wait_stage = [&](int qq) -> bool {
       const int s = qq % kStages;
-      if (mbar_test_warp(&bar_full[s], (qq / kStages) & 1)) return true;
-      return mbar_wait_warp(&bar_full[s], (qq / kStages) & 1, ab);
+      if (mbar_test_warp(&b.full[s], (qq / kStages) & 1)) return true;
+      return mbar_wait_warp(&b.full[s], (qq / kStages) & 1, ab);
     };
     // after the job of ring index qq: its stage goes back to the producer
     // once its products are done
-    auto release = [&](int qq) { mma_commit_w(&bar_empty[qq % kStages]); };
+    auto release = [&](int qq) { mma_commit_w(&b.empty[qq % kStages]); };
     // S^T(t) (kind 0, 9 chunks) or dP^T(t) (kind 1, 8 chunks) into tensor
     // memory, two chunks per job
     auto xt_jobs = [&](int t, int kind) -> bool {
       const int nc = kind == 0 ? 9 : 8;
-      const uint32_t d = tmem + (kind == 0 ? T_S + (t & 1) * BC : T_DP);
+      const int gt = ep.T + t;
+      const uint32_t d = tmem + (kind == 0 ? T_S + (gt & 1) * BC : T_DP);
       for (int c0 = 0; c0 < nc; c0 += 2, ++q) {
         if (!wait_stage(q)) return false;
         tc_fence_after();
@@ -328,7 +322,7 @@ __global__ void __launch_bounds__(384, 1)
         }
         release(q);
       }
-      mma_commit_w(kind == 0 ? &bar_s_full[t & 1] : &bar_dp_full);
+      mma_commit_w(kind == 0 ? &b.s_full[gt & 1] : &b.dp_full);
       return true;
     };
     for (int t = 0; t <= n && ok; ++t) {
@@ -338,12 +332,12 @@ __global__ void __launch_bounds__(384, 1)
       if (t >= 1) {
         // accumulation of tile u = t - 1: P^T dY chunks once P^T(u) is in,
         // then dS^T Q chunks once dS^T(u) is in
-        const int u = t - 1;
-        if (!(ok = mbar_wait_warp(&bar_p_full[u & 1], (u >> 1) & 1, ab))) break;
+        const int u = t - 1, gu = ep.T + u;
+        if (!(ok = mbar_wait_warp(&b.p_full[gu & 1], (gu >> 1) & 1, ab))) break;
         tc_fence_after();
         for (int a0 = 0; a0 < PS::NACC && ok; a0 += 2, ++q) {
           if (a0 == 4) {
-            if (!(ok = mbar_wait_warp(&bar_ds_full, u & 1, ab))) break;
+            if (!(ok = mbar_wait_warp(&b.ds_full, gu & 1, ab))) break;
             tc_fence_after();
           }
           if (!(ok = wait_stage(q))) break;
@@ -352,7 +346,7 @@ __global__ void __launch_bounds__(384, 1)
             const int a = a0 + k;
             const int c = acc_src_chunk<PART>(a);
             const uint32_t d = tmem + T_ACC + (c - 4 * PART) * 64;  // chunk 8 (position) -> 256
-            const uint32_t at = tmem + (a < 4 ? T_S + (u & 1) * BC : T_DP);
+            const uint32_t at = tmem + (a < 4 ? T_S + (gu & 1) * BC : T_DP);
             const uint64_t bm = sdesc_add(dRm0, (q % kStages) * STAGE + k * QCH);
             // the first contribution to an accumulator chunk overwrites it:
             // P^T dY for latent chunks, dS^T Qp for the position chunk
@@ -371,18 +365,19 @@ __global__ void __launch_bounds__(384, 1)
       // dP^T(t) overwrites dS^T(t - 1), whose products were just issued
       if (t < n && !(ok = xt_jobs(t, 1))) break;
     }
-    mma_commit_w(&bar_acc);
-    drain_wait(&bar_acc, 0);
+    mma_commit_w(&b.acc);
+    drain_wait(&b.acc, ep.B & 1);
     __syncwarp();
+    return ok;
   } else if (warp >= 4) {
     const int sg = (warp - 4) >> 2;  // compute group: tiles of parity sg
     const int lg = warp & 3;
     const int row = lg * 32 + lane;  // token row inside the block == TMEM lane
     const uint32_t lane_addr = static_cast<uint32_t>(lg * 32) << 16;
-    bool ok = n > 0;
-    for (int t = sg; t < n && ok; t += 2) {
-      const int bb = t & 1, ss = t % kStatSlots;
-      if (!(ok = mbar_wait_warp(&bar_st_full[ss], (t / kStatSlots) & 1, ab))) break;
+    bool ok = true;
+    for (int t = sg ^ (ep.T & 1); t < n && ok; t += 2) {
+      const int gt = ep.T + t, bb = gt & 1, ss = gt % kStatSlots;
+      if (!(ok = mbar_wait_warp(&b.st_full[ss], (gt / kStatSlots) & 1, ab))) break;
       const uint8_t* st = sm + ST_OFF + ss * ST_SLOT;
       const float* snl = reinterpret_cast<const float*>(st);
       const float* sdl = snl + BC;
@@ -390,7 +385,7 @@ __global__ void __launch_bounds__(384, 1)
       const int* sinfo = spos + BC;
       const int tok = sinfo[0] + row;
       const bool tok_ok = row >= sinfo[1] && row < sinfo[2] && tok >= 0 && tok < sinfo[3];
-      if (!(ok = mbar_wait_warp(&bar_s_full[bb], (t >> 1) & 1, ab))) break;
+      if (!(ok = mbar_wait_warp(&b.s_full[bb], (gt >> 1) & 1, ab))) break;
       tc_fence_after();
       // ---------------------------------------------------- S^T -> P^T
       // two halves of 32 columns: half hf reads S^T columns [32hf, 32hf+32)
@@ -424,11 +419,11 @@ __global__ void __launch_bounds__(384, 1)
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bar_p_full[bb]);
+      if (lane == 0) mbar_arrive(&b.p_full[bb]);
       // ---------------------------------------------------- dP^T, P^T -> dS^T
-      // (one dP buffer: its phase t has completed once this group sees it,
-      // since dP(t - 1) went into the tensor core before S(t) did)
-      if (!(ok = mbar_wait_warp(&bar_dp_full, t & 1, ab))) break;
+      // (one dP buffer: its phase gt has completed once this group sees it,
+      // since dP(gt - 1) went into the tensor core before S(gt) did)
+      if (!(ok = mbar_wait_warp(&b.dp_full, gt & 1, ab))) break;
       tc_fence_after();
       const uint32_t tDP = tmem + T_DP + lane_addr;
       // a masked entry has P = 0 and takes dS = 0 by select: dP of a tail or
@@ -458,14 +453,98 @@ __global__ void __launch_bounds__(384, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(&bar_ds_full);
-        mbar_arrive(&bar_st_empty[ss]);
+        mbar_arrive(&b.ds_full);
+        mbar_arrive(&b.st_empty[ss]);
       }
     }
-    if (n > 0) {
-      if (ok) ok = mbar_wait_warp(&bar_acc, 0, ab);
-      tc_fence_after();
+    if (ok) ok = mbar_wait_warp(&b.acc, ep.B & 1, ab);
+    tc_fence_after();
+    return ok;
+  }
+  return true;
+}
+
+// A 128-token block whose link passes (shared pages) exceed this many tiles
+// goes to the split kernel (its own pass has 64 rows x G heads / 64 columns).
+constexpr int kHeavyLinkTiles = 64;
+constexpr int kSplitCL = 8;                       // CTAs of a split cluster; CTA r sums tokens [16r, 16r + 16)
+constexpr int RED_STRIDE = 324;                   // floats per token row of a staged partial (320 + 4: bank spread)
+static_assert(BT * RED_STRIDE * 4 <= BYTES, "a partial fits the pipeline's shared memory");
+static_assert(BT % kSplitCL == 0, "tokens split evenly over the cluster");
+
+template <int PART>
+__global__ void __launch_bounds__(384, 1)
+    mla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_qp,
+                  const __grid_constant__ CUtensorMap tm_dy, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_kp, const PagedParams p) {
+  using PS = PartShape<PART>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ TcBars bars;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_flag;
+  __shared__ PageInfo pinfo;
+  __shared__ int n_tiles_sh, any_store_sh;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = blockIdx.x, tb = blockIdx.y, s0 = blockIdx.z;
+  // Launched as the programmatic dependent of the kernel before it (the
+  // cluster-split kernel, or PART 0 for PART 1), whose results it does not
+  // read: its own dependent may start at once, and the last CTA waits for the
+  // kernel before, so that this grid completes after it and later work in
+  // the stream sees both.  Without a programmatic launch both are no-ops.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (blockIdx.x == gridDim.x - 1 && blockIdx.y == gridDim.y - 1 && blockIdx.z == gridDim.z - 1)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int len0 = seq_len_of(p, s0);
+  const int npg = pages_of(len0, p.page_size);
+  if (tb * 8 >= npg) return;  // no token of this sequence in the block (uniform exit)
+  const int RT = BC / p.G;    // query rows per tile
+  const Abort ab{&abort_flag, p.err};
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    tc_bars_init(bars);
+    int any = fill_page_info(p, s0, tb, npg, &pinfo);
+    // a block the plan flagged belongs to the cluster-split kernel
+    if (any && p.heavy && p.heavy[(static_cast<int64_t>(s0) * ((p.max_pages + 7) / 8) + tb) * p.KVH + g]) any = 0;
+    any_store_sh = any;
+    PassIter it{&p, &pinfo, s0, tb};
+    int n = 0;
+    if (any && it.begin(RT)) {
+      do ++n;
+      while (it.advance(RT));
     }
+    n_tiles_sh = n;
+  }
+  __syncthreads();
+  // a block whose pages are all stored by other CTAs (their owners) has
+  // nothing to write: leave before taking tensor memory (uniform exit)
+  if (!any_store_sh) return;
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_sh, TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_map(&tm_q);
+    tma_prefetch_map(&tm_qp);
+    tma_prefetch_map(&tm_dy);
+    tma_prefetch_map(&tm_k);
+    tma_prefetch_map(&tm_kp);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+  const int n = n_tiles_sh;
+  bool ok = true;
+  if (n > 0) ok = run_block<PART>(&tm_q, &tm_qp, &tm_dy, &tm_k, &tm_kp, p, bars, sm, tmem, pinfo, s0, tb, g, 0, n,
+                                  TcEpoch{0, 0, 0}, ab);
+  if (warp >= 4) {
+    const int sg = (warp - 4) >> 2;
+    const int lg = warp & 3;
+    const int row = lg * 32 + lane;  // token row inside the block == TMEM lane
+    const uint32_t lane_addr = static_cast<uint32_t>(lg * 32) << 16;
     // ------------------------------------------------------------ epilogue
     // 32-column chunks of the accumulator, alternating between the groups:
     // latent dims [256 PART + 32 cc, ...) for cc < 8, position dims after
@@ -503,6 +582,252 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
+// Cluster primitives of the split kernel.
+__device__ __forceinline__ int cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return static_cast<int>(r);
+}
+__device__ __forceinline__ int cluster_index() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return static_cast<int>(r);
+}
+__device__ __forceinline__ int cluster_count() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return static_cast<int>(r);
+}
+// All threads of all CTAs of the cluster: shared-memory writes before it are
+// visible to the other CTAs' reads after it.  Every CTA of a cluster passes
+// the same number of these (its waits give up after a time limit, so none is
+// held back for ever).
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+// the same shared-memory offset in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t map_rank(uint32_t addr, int rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ int ld_cluster_s32(uint32_t addr) {
+  int v;
+  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ float4 ld_cluster_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+// Plan of the MLA history: heavy[(s0 * nblk + tb) * KVH + g] = 1 when the
+// pages 128-token block tb of sequence s0 stores carry more than
+// kHeavyLinkTiles tiles of other links (counting stops there), else 0; one
+// thread per block.
+__global__ void mla_tc_plan_kernel(const PagedParams p) {
+  const int nblk = (p.max_pages + 7) / 8;
+  const int n = p.S * nblk;
+  const int RT = BC / p.G;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+    const int s0 = i / nblk, tb = i - s0 * nblk;
+    const int npg = pages_of(seq_len_of(p, s0), p.page_size);
+    int heavy = 0;
+    if (tb * 8 < npg) {
+      PageInfo pi;
+      if (fill_page_info(p, s0, tb, npg, &pi)) {
+        PassIter it{&p, &pi, s0, tb};
+        int n_link = 0;
+        if (it.begin(RT)) {
+          do n_link += it.j >= 0 ? 1 : 0;
+          while (n_link <= kHeavyLinkTiles && it.advance(RT));
+        }
+        heavy = n_link > kHeavyLinkTiles;
+      }
+    }
+    for (int g = 0; g < p.KVH; ++g) p.heavy[static_cast<int64_t>(i) * p.KVH + g] = heavy;
+  }
+}
+
+// Persistent clusters of kSplitCL CTAs take the (flagged block, part) units
+// in flag order, unit u to cluster u mod clusters; CTA r of a cluster runs
+// the block's tiles [r n / kSplitCL, (r + 1) n / kSplitCL) of its n into its
+// accumulator, stages the partial in shared memory, and after a cluster
+// barrier adds tokens [16 r, 16 r + 16) over the cluster's partials in rank
+// order (the result does not depend on the number of clusters or on timing).
+__global__ void __launch_bounds__(384, 1)
+    mla_tc_split_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_qp,
+                        const __grid_constant__ CUtensorMap tm_dy, const __grid_constant__ CUtensorMap tm_k,
+                        const __grid_constant__ CUtensorMap tm_kp, const PagedParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  __shared__ TcBars bars;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_flag, abort_any_sh;
+  __shared__ PageInfo pinfo;
+  __shared__ int n_all_sh;
+  __shared__ int items_sh[384];
+  __shared__ int warp_cnt[12];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int RT = BC / p.G;
+  const int rank = cluster_rank(), cid = cluster_index(), ncl = cluster_count();
+  const int nblk = (p.max_pages + 7) / 8;
+  const Abort ab{&abort_flag, p.err};
+  // the grid kernels, launched next as programmatic dependents, may start on
+  // the SMs these clusters leave free
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    tc_bars_init(bars);
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_sh, TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_map(&tm_q);
+    tma_prefetch_map(&tm_qp);
+    tma_prefetch_map(&tm_dy);
+    tma_prefetch_map(&tm_k);
+    tma_prefetch_map(&tm_kp);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base_sh;
+  float* red = reinterpret_cast<float*>(sm);  // staged partial: [BT][RED_STRIDE] fp32
+  TcEpoch ep{0, 0, 0};
+
+  auto run_unit = [&](int item, int part) {
+    const int g = item % p.KVH, rest = item / p.KVH, tb = rest % nblk, s0 = rest / nblk;
+    __syncthreads();  // the previous unit's readers of pinfo are done
+    if (threadIdx.x == 0) {
+      fill_page_info(p, s0, tb, pages_of(seq_len_of(p, s0), p.page_size), &pinfo);
+      PassIter it{&p, &pinfo, s0, tb};
+      int n_all = 0;
+      if (it.begin(RT)) {
+        do ++n_all;
+        while (it.advance(RT));
+      }
+      n_all_sh = n_all;
+    }
+    __syncthreads();
+    const int n_all = n_all_sh;
+    const int t0 = rank * n_all / kSplitCL, n = (rank + 1) * n_all / kSplitCL - t0;
+    const int acc_cols = part == 0 ? PartShape<0>::ACC_COLS : PartShape<1>::ACC_COLS;
+    // (a wait that gives up sets the abort flag, which the cluster reads below)
+    if (n > 0 && part == 0)
+      run_block<0>(&tm_q, &tm_qp, &tm_dy, &tm_k, &tm_kp, p, bars, sm, tmem, pinfo, s0, tb, g, t0, n, ep, ab);
+    else if (n > 0)
+      run_block<1>(&tm_q, &tm_qp, &tm_dy, &tm_k, &tm_kp, p, bars, sm, tmem, pinfo, s0, tb, g, t0, n, ep, ab);
+    // every role is done with the pipeline's shared memory and the
+    // accumulator is complete: stage the partial (zeros without tiles)
+    __syncthreads();
+    if (warp >= 4) {
+      const int sg = (warp - 4) >> 2, lg = warp & 3;
+      const int row = lg * 32 + lane;
+      const uint32_t lane_addr = static_cast<uint32_t>(lg * 32) << 16;
+#pragma unroll 1
+      for (int cc = sg; cc < acc_cols / 32; cc += 2) {  // warp-uniform
+        uint32_t r[32];
+        if (n > 0) {
+          tmem_ld32(tmem + T_ACC + cc * 32 + lane_addr, r);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r[i] = 0u;
+        }
+        float* dst = red + row * RED_STRIDE + cc * 32;
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          *reinterpret_cast<uint4*>(dst + 4 * i) = make_uint4(r[4 * i], r[4 * i + 1], r[4 * i + 2], r[4 * i + 3]);
+      }
+      tc_fence_before();
+    }
+    // every CTA's abort flag is ORed over the cluster: a partial left
+    // incomplete by a timed-out wait must not reach the pool as a finite value
+    if (threadIdx.x == 0) abort_any_sh = abort_flag;
+    cluster_sync();
+    if (threadIdx.x == 0) {
+      int any_abort = 0;
+      for (int r = 0; r < kSplitCL; ++r) any_abort |= ld_cluster_s32(map_rank(smem_addr(&abort_any_sh), r));
+      if (any_abort) abort_flag = 1;
+    }
+    __syncthreads();
+    const bool good = !abort_flag;
+    // tokens [16 rank, 16 rank + 16): the partials of CTAs 0..kSplitCL-1
+    // added in that order; one page per CTA
+    constexpr int kRows = BT / kSplitCL;
+    const int quads = acc_cols / 4;
+    const int j = (kRows * rank) >> 4;
+    if (good && pinfo.store[j]) {
+      for (int idx = threadIdx.x; idx < kRows * quads; idx += blockDim.x) {
+        const int i = kRows * rank + idx / quads, d = 4 * (idx % quads);
+        const uint32_t a = smem_addr(red + i * RED_STRIDE + d);
+        float4 sum = ld_cluster_f4(map_rank(a, 0));
+#pragma unroll
+        for (int r = 1; r < kSplitCL; ++r) {
+          const float4 v = ld_cluster_f4(map_rank(a, r));
+          sum.x += v.x;
+          sum.y += v.y;
+          sum.z += v.z;
+          sum.w += v.w;
+        }
+        const int64_t prow = (static_cast<int64_t>(pinfo.phys[j]) * p.page_size + (i & 15)) * p.KVH + g;
+        const uint2 w = make_uint2(pack_bf16x2(sum.x, sum.y), pack_bf16x2(sum.z, sum.w));
+        if (d < 256) {
+          if (p.wrt & 2u)
+            *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.dk_pool) + prow * kLat + 256 * part + d) = w;
+        } else if (p.wrt & 8u) {
+          *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.dkp_pool) + prow * kPos + (d - 256)) = w;
+        }
+      }
+    }
+    cluster_sync();  // the other CTAs have read this CTA's partial
+    if (n > 0) {
+      ep.T += n;
+      ep.Q += n * (part == 0 ? jobs_per_tile<0>() : jobs_per_tile<1>());
+      ++ep.B;
+    }
+  };
+
+  // the flagged blocks in flag order; units 2k (PART 0) and 2k + 1 (PART 1)
+  // of flagged block k, unit u to cluster u mod clusters
+  const int nitems = p.S * nblk * p.KVH;
+  int base = 0;
+  for (int c0 = 0; c0 < nitems; c0 += blockDim.x) {
+    const int i = c0 + threadIdx.x;
+    const bool f = i < nitems && p.heavy[i] != 0;
+    const uint32_t bal = __ballot_sync(0xffffffffu, f);
+    if (lane == 0) warp_cnt[warp] = __popc(bal);
+    __syncthreads();
+    int before = 0, total = 0;
+    for (int w = 0; w < static_cast<int>(blockDim.x / 32); ++w) {
+      const int c = warp_cnt[w];
+      before += w < warp ? c : 0;
+      total += c;
+    }
+    const int k = base + before + __popc(bal & ((1u << lane) - 1u));
+    if (f) items_sh[k - base] = i;
+    __syncthreads();
+    for (int u = 2 * base; u < 2 * (base + total); ++u)
+      if (u % ncl == cid) run_unit(items_sh[u / 2 - base], u & 1);
+    base += total;
+    __syncthreads();  // items_sh and warp_cnt are rewritten next
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
 template <int PART>
 cudaError_t launch_part(const PagedMlaMaps& m, const PagedParams& p, bool dependent, cudaStream_t s) {
   auto kern = mla_tc_kernel<PART>;
@@ -524,33 +849,51 @@ cudaError_t launch_part(const PagedMlaMaps& m, const PagedParams& p, bool depend
   return cudaLaunchKernelEx(&cfg, kern, m.q, m.qp, m.dy, m.k, m.kp, p);
 }
 
-// heavy[] is planned per 64-token block; a 128-token block of this kernel
-// goes to the split kernel when either half is heavy, so both halves are
-// flagged for it
-__global__ void mla_tc_pair_heavy_kernel(const PagedParams p) {
-  const int nb64 = (p.max_pages + 3) / 4;
-  const int nb128 = (nb64 + 1) / 2;
-  const int n = p.S * nb128 * p.KVH;
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
-    const int g = i % p.KVH, sb = i / p.KVH, s0 = sb / nb128, b = sb - s0 * nb128;
-    const int64_t h0 = (static_cast<int64_t>(s0) * nb64 + 2 * b) * p.KVH + g;
-    const bool second = 2 * b + 1 < nb64;
-    const int h = p.heavy[h0] | (second ? p.heavy[h0 + p.KVH] : 0);
-    p.heavy[h0] = h;
-    if (second) p.heavy[h0 + p.KVH] = h;
-  }
-}
-
 }  // namespace
 
 bool mla_tc_supported(const PagedParams& p) {
   return p.Dk == kLat && p.Dp == kPos && p.page_size == 16 && p.G >= 1 && p.G <= BC && BC % p.G == 0;
 }
 
-cudaError_t launch_paged_mla_tc_pair_heavy(const PagedParams& p, cudaStream_t s) {
-  if (p.S == 0 || p.max_pages == 0 || p.KVH == 0) return cudaSuccess;
-  mla_tc_pair_heavy_kernel<<<64, 256, 0, s>>>(p);
+cudaError_t launch_paged_mla_tc_plan(const PagedParams& p, cudaStream_t s) {
+  const int64_t n = static_cast<int64_t>(p.S) * ((p.max_pages + 7) / 8);
+  if (n == 0 || p.num_pages == 0) return cudaSuccess;
+  const int blocks = static_cast<int>((n + 127) / 128 < 1024 ? (n + 127) / 128 : 1024);
+  mla_tc_plan_kernel<<<blocks, 128, 0, s>>>(p);
   return cudaGetLastError();
+}
+
+cudaError_t launch_paged_mla_tc_split(const PagedMlaMaps& m, const PagedParams& p, cudaStream_t s) {
+  if (p.num_pages == 0 || p.S == 0 || p.max_pages == 0) return cudaSuccess;
+  const int smem = BYTES + 1024;
+  auto kern = mla_tc_split_kernel;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = kSplitCL;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(384, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  // as many clusters as fit the GPU at once (one CTA per SM), cached per
+  // device (host threads may race to fill an entry: they store the same value)
+  static std::atomic<int> clusters[64];
+  int dev = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  int ncl = dev < 64 ? clusters[dev].load(std::memory_order_relaxed) : 0;
+  if (ncl == 0) {
+    cfg.gridDim = dim3(kSplitCL, 1, 1);
+    if ((e = cudaOccupancyMaxActiveClusters(&ncl, kern, &cfg)) != cudaSuccess) return e;
+    if (ncl < 1) return cudaErrorInvalidConfiguration;
+    if (dev < 64) clusters[dev].store(ncl, std::memory_order_relaxed);
+  }
+  cfg.gridDim = dim3(ncl * kSplitCL, 1, 1);
+  return cudaLaunchKernelEx(&cfg, kern, m.q, m.qp, m.dy, m.k, m.kp, p);
 }
 
 cudaError_t launch_paged_mla_tc(const PagedMlaMaps& m, const PagedParams& p, bool after_split, cudaStream_t s) {

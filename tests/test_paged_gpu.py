@@ -72,14 +72,14 @@ CASES = [
          value_dim=512, position_dim=64, causal=False),
     dict(seed=27, num_seqs=4, len_lo=40, len_hi=200, queries_per_seq=8, heads=32, kv_heads=1, key_dim=512,
          value_dim=512, position_dim=64, causal=True, shared_prefix_pages=2),
-    # long shared prefixes: 20 pages (2.5 blocks of 8 pages) and 9 pages (2.25
-    # MLA blocks of 4 pages) shared by every sequence
+    # long shared prefixes: 20 pages (2.5 blocks of 8 pages) and 9 pages (1.1
+    # blocks) shared by every sequence
     dict(seed=28, num_seqs=12, len_lo=330, len_hi=700, queries_per_seq=32, heads=16, kv_heads=4, key_dim=128,
          value_dim=128, causal=True, shared_prefix_pages=20),
     dict(seed=29, num_seqs=10, len_lo=150, len_hi=400, queries_per_seq=6, heads=16, kv_heads=1, key_dim=512,
          value_dim=512, position_dim=64, causal=True, shared_prefix_pages=9),
-    # MLA blocks whose shared pages carry more than 128 link tiles go to the
-    # cluster-split kernel: 11 other sequences x 24 (resp. 12) tiles each
+    # MLA blocks whose shared pages carry more than 64 link tiles go to the
+    # cluster-split kernel: 11 other sequences x 12 (resp. 6) tiles each
     dict(seed=30, num_seqs=12, len_lo=150, len_hi=300, queries_per_seq=24, heads=32, kv_heads=1, key_dim=512,
          value_dim=512, position_dim=64, causal=True, shared_prefix_pages=9),
     dict(seed=32, num_seqs=12, len_lo=150, len_hi=300, queries_per_seq=24, heads=32, kv_heads=2, key_dim=512,
@@ -147,7 +147,8 @@ def test_paged_shared_at_offsets(bd, mla):
 
 
 def test_paged_mla_split_bit_stable(bd):
-    """The cluster-split MLA blocks sum their partials in a fixed order."""
+    """The cluster-split MLA blocks (8-CTA clusters on tcgen05) sum their
+    partials in a fixed order."""
     c = inputs.paged_case(name="t", seed=33, num_seqs=12, len_lo=150, len_hi=300, queries_per_seq=24, heads=32,
                           kv_heads=1, key_dim=512, value_dim=512, position_dim=64, scale=0.5, shared_prefix_pages=6)
     dv = to_dev(c, bd)
