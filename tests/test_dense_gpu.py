@@ -243,6 +243,34 @@ def test_strided_views_match_contiguous(bd):
     assert torch.isnan(obuf[:, :, 0]).all()  # the other slice is untouched
 
 
+@pytest.mark.parametrize("dtype,store_ds", [("bf16", False), ("bf16", True), ("f32", False)],
+                         ids=["bf16", "bf16_store_ds", "f32"])
+def test_outputs_at_16_byte_offsets(bd, dtype, store_ds):
+    """dq, dk, dv written into views whose rows start 16 bytes past a 32-byte
+    boundary (the epilogues then take their 16-byte store path instead of the
+    32-byte one) are bit-identical to the contiguous call; the padding in
+    front of every row is untouched."""
+    bf16 = dtype == "bf16"  # (fp32 storage: head_dim <= 64, no bias)
+    c = inputs.dense_inputs(batch=2, heads=3, seq_q=200, seq_k=328, head_dim=128 if bf16 else 64, dtype=dtype,
+                            seed=93, scale=0.5, causal=True, key_mask_zero_frac=0.1, bias=bf16)
+    tdt = torch.bfloat16 if bf16 else torch.float32
+    pad = 16 // torch.tensor([], dtype=tdt).element_size()
+    q, k, v, dy = (_dev(x, tdt) for x in (c.q, c.k, c.v, c.dy))
+    bias = _dev(c.bias, tdt) if bf16 else None
+    km = torch.from_numpy(c.key_mask).cuda()
+    bufs = [torch.full(x.shape[:-1] + (x.shape[-1] + pad,), float("nan"), dtype=tdt, device="cuda")
+            for x in (q, k, v)]
+    outs = tuple(b[..., pad:] for b in bufs)
+    assert all(o.data_ptr() % 32 == 16 for o in outs)
+    bd.dense_backward(q, k, v, dy, causal=True, key_mask=km, bias=bias, outputs=outs, store_ds=store_ds)
+    ref = bd.dense_backward(q, k, v, dy, causal=True, key_mask=km, bias=bias, store_ds=store_ds)
+    bd.check_device_error()
+    for a, b in zip(outs, ref):
+        assert torch.equal(a, b)
+    for b in bufs:
+        assert torch.isnan(b[..., :pad]).all()
+
+
 def test_strided_head_broadcast_keys(bd):
     """One key/value head shared by all query heads through a head stride of 0
     (inputs may overlap), against the materialised copy."""
