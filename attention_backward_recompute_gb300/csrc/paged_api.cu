@@ -18,7 +18,7 @@ using attn::api_ok;
 struct PagedSizes {
   size_t q_bytes, qp_bytes, dy_bytes, k_bytes, v_bytes, kp_bytes, table_bytes, meta_bytes, stat_bytes;
   size_t ws_bytes;
-  size_t off_count, off_off, off_fill, off_links, off_heavy, off_listed;
+  size_t off_count, off_off, off_fill, off_links, off_heavy, off_listed, off_order;
 };
 
 size_t a256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -66,7 +66,8 @@ attn_status_t check_paged_desc(const attn_paged_desc* d, PagedSizes* z) {
   z->off_links = z->off_fill + a256(size_t(d->num_pages) * 4);
   z->off_heavy = z->off_links + a256(size_t(d->num_seqs) * d->max_pages_per_seq * 4 + 4);
   z->off_listed = z->off_heavy + a256(size_t(d->num_seqs) * ((d->max_pages_per_seq + 7) / 8) * d->kv_heads * 4 + 4);
-  z->ws_bytes = z->off_listed + a256(size_t(d->num_pages) + 4);
+  z->off_order = z->off_listed + a256(size_t(d->num_pages) + 4);
+  z->ws_bytes = z->off_order + a256(size_t(d->num_seqs) * 4 + 4);
   return ATTN_OK;
 }
 
@@ -106,6 +107,7 @@ attn_status_t fill_params(const attn_paged_desc* d, const PagedSizes& z, const i
   p->links = reinterpret_cast<int32_t*>(ws + z.off_links);
   p->heavy = reinterpret_cast<int32_t*>(ws + z.off_heavy);
   p->listed = nullptr;  // every page (the compact call points it at its map)
+  p->order = reinterpret_cast<int32_t*>(ws + z.off_order);
   p->err = attn::device_error_word();
   if (!p->err) return api_fail(ATTN_ERR_CUDA, "no CUDA device / symbol address unavailable");
   return ATTN_OK;
@@ -312,16 +314,22 @@ ATTN_API attn_status_t attn_paged_row_stats(const attn_paged_desc* d, const void
     if (overlap(lse, z.stat_bytes, r.p, r.n) || overlap(delta, z.stat_bytes, r.p, r.n))
       return api_fail(ATTN_ERR_ALIAS, "lse/delta overlap an input or the workspace");
   if (overlap(lse, z.stat_bytes, delta, z.stat_bytes)) return api_fail(ATTN_ERR_ALIAS, "lse and delta overlap");
+  if (!workspace || workspace_bytes < z.ws_bytes)
+    return api_fail(ATTN_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", z.ws_bytes, workspace_bytes);
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return api_fail(ATTN_ERR_WORKSPACE, "workspace must be 256-byte aligned");
   attn::PagedParams p;
   if ((st = fill_params(d, z, page_table, seq_meta, workspace, &p)) != ATTN_OK) return st;
   p.lse_out = lse;
   p.delta_out = delta;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // the row tiles of the longest sequences go first
+  if (const cudaError_t e = attn::launch_paged_seq_order(p, s); e != cudaSuccess)
+    return api_fail(ATTN_ERR_CUDA, "row-statistics launch failed: %s", cudaGetErrorString(e));
   if (mla) {
     // tcgen05: 128 columns (128/G rows) per CTA
     attn::PagedMlaMaps mt;
     if (!encode_mla_maps(&mt, d, p.G, 128u / uint32_t(p.G), q, qp, dy, k_pool, kp_pool))
       return api_fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed");
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
     attn::timing_mark_begin(1, s);
     cudaError_t e = attn::launch_paged_mla_stats_tc(mt, p, s);
     attn::timing_mark(s);
@@ -341,7 +349,6 @@ ATTN_API attn_status_t attn_paged_row_stats(const attn_paged_desc* d, const void
   else
     m.k = m.v = m.q_stats;
   if (!enc) return api_fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed");
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   attn::timing_mark_begin(1, s);
   cudaError_t e = attn::launch_paged_row_stats(m, p, s);
   attn::timing_mark(s);
@@ -380,11 +387,18 @@ ATTN_API attn_status_t attn_bwd_paged_query(const attn_paged_desc* d, const void
   for (int i = 0; i < 4; ++i)
     for (int j = i + 1; j < 4; ++j)
       if (overlap(outs[i].p, outs[i].n, outs[j].p, outs[j].n)) return api_fail(ATTN_ERR_ALIAS, "outputs overlap");
+  if (!workspace || workspace_bytes < z.ws_bytes)
+    return api_fail(ATTN_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", z.ws_bytes, workspace_bytes);
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return api_fail(ATTN_ERR_WORKSPACE, "workspace must be 256-byte aligned");
   attn::PagedParams p;
   if ((st = fill_params(d, z, page_table, seq_meta, workspace, &p)) != ATTN_OK) return st;
   p.lse_out = lse;
   p.delta_out = delta;
   p.dq = dq;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // the row tiles of the longest sequences go first
+  if (const cudaError_t e = attn::launch_paged_seq_order(p, s); e != cudaSuccess)
+    return api_fail(ATTN_ERR_CUDA, "query-side launch failed: %s", cudaGetErrorString(e));
   if (mla) {
     // row statistics (128 columns per CTA), then dQ / dQp from them (64
     // columns per CTA), both on tcgen05
@@ -395,7 +409,6 @@ ATTN_API attn_status_t attn_bwd_paged_query(const attn_paged_desc* d, const void
     if (!encode_mla_maps(&ms, d, p.G, 128u / uint32_t(p.G), q, qp, dy, k_pool, kp_pool) ||
         !encode_mla_maps(&mq, d, p.G, 64u / uint32_t(p.G), q, qp, dy, k_pool, kp_pool))
       return api_fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed");
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
     attn::timing_mark_begin(3, s);
     cudaError_t e = attn::launch_paged_mla_stats_tc(ms, p, s);
     attn::timing_mark(s);
@@ -419,7 +432,6 @@ ATTN_API attn_status_t attn_bwd_paged_query(const attn_paged_desc* d, const void
   else
     m.k = m.v = m.q_stats;
   if (!enc) return api_fail(ATTN_ERR_CUDA, "cuTensorMapEncodeTiled failed");
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   attn::timing_mark_begin(1, s);
   cudaError_t e = attn::launch_paged_query(m, p, s);
   attn::timing_mark(s);

@@ -43,6 +43,7 @@ struct PagedParams {
   int32_t* links;              // [S * max_pages]: link ids s*max_pages+lp grouped by page
   int32_t* heavy;              // [S, ceil(max_pages / 8), KVH]: MLA blocks left to the split kernel
   uint8_t* listed;             // [num_pages] compact history: 1 = compute and store the page; null = all
+  int32_t* order;              // [S] sequences by decreasing length (ties by index): query-side dispatch order
   uint32_t* err;
 };
 
@@ -60,6 +61,23 @@ __device__ __forceinline__ int seq_len_of(const PagedParams& p, int s) {
 __device__ __forceinline__ int row_begin_of(const PagedParams& p, int s) { return min(max(p.q_start[s], 0), p.Nq); }
 __device__ __forceinline__ int row_end_of(const PagedParams& p, int s) {
   return min(max(p.q_start[s + 1], row_begin_of(p, s)), p.Nq);
+}
+// The idx-th tile of rt query rows, counting the row tiles of the sequences
+// in p.order (the longest sequences first, so that the CTAs with the longest
+// sweeps start first): its sequence and first row; sq = -1 past the last.
+__device__ inline void row_tile_at(const PagedParams& p, int idx, int rt, int* sq, int* r0) {
+  for (int k = 0; k < p.S; ++k) {
+    const int s = p.order[k];
+    const int rb = row_begin_of(p, s), tiles = (row_end_of(p, s) - rb + rt - 1) / rt;
+    if (idx < tiles) {
+      *sq = s;
+      *r0 = rb + idx * rt;
+      return;
+    }
+    idx -= tiles;
+  }
+  *sq = -1;
+  *r0 = 0;
 }
 #endif
 

@@ -17,6 +17,9 @@ struct PagedMaps {
 };
 
 cudaError_t launch_paged_prep(const PagedParams& p, cudaStream_t s);
+// p.order: the sequences by decreasing length (the query-side kernels take
+// their row tiles in that order)
+cudaError_t launch_paged_seq_order(const PagedParams& p, cudaStream_t s);
 // zero the pool rows of pages no link references: every page (list null) or
 // the n listed ones (compact history)
 cudaError_t launch_paged_zero_unlinked(const PagedParams& p, const int32_t* list, int64_t n, cudaStream_t s);

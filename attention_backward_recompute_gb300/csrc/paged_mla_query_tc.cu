@@ -78,20 +78,13 @@ __global__ void __launch_bounds__(256, 1)
   __shared__ int abort_flag, ntok_sh, seq_sh, r0_sh;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = blockIdx.x;
+  // block x = tile * KVH + g: row tile `tile` of the sequences in dispatch
+  // order (longest first), KV head g
+  const int g = static_cast<int>(blockIdx.x % p.KVH);
   const int G = p.G, RT = BC / G;
-  // this CTA's (sequence, row tile): the row tiles of every sequence, in order
   if (threadIdx.x == 0) {
-    int idx = blockIdx.y, sq = -1, r0 = 0;
-    for (int s = 0; s < p.S; ++s) {
-      const int tiles = (row_end_of(p, s) - row_begin_of(p, s) + RT - 1) / RT;
-      if (idx < tiles) {
-        sq = s;
-        r0 = row_begin_of(p, s) + idx * RT;
-        break;
-      }
-      idx -= tiles;
-    }
+    int sq, r0;
+    row_tile_at(p, static_cast<int>(blockIdx.x / p.KVH), RT, &sq, &r0);
     seq_sh = sq;
     r0_sh = r0;
   }
@@ -462,7 +455,7 @@ cudaError_t launch_paged_mla_query_tc(const PagedMlaMaps& m, const PagedParams& 
   if (e != cudaSuccess) return e;
   // an upper bound on the row tiles of all sequences; each CTA finds its own
   const int RT = BC / p.G;
-  dim3 grid(p.KVH, p.Nq / RT + p.S + 1, 1);
+  dim3 grid(static_cast<unsigned>((static_cast<int64_t>(p.Nq) / RT + p.S + 1) * p.KVH));
   mla_query_tc_kernel<<<grid, 256, smem, s>>>(m.q, m.qp, m.dy, m.k, m.kp, p);
   return cudaGetLastError();
 }

@@ -131,7 +131,28 @@ __global__ void mark_listed_kernel(PagedParams p, const int32_t* pages, int64_t 
   }
 }
 
+// Query-side dispatch order: order[rank] = s, ranked by decreasing sequence
+// length (ties by index), one thread per sequence (S^2 reads of the lengths).
+__global__ void seq_order_kernel(PagedParams p) {
+  for (int s = blockIdx.x * blockDim.x + threadIdx.x; s < p.S; s += gridDim.x * blockDim.x) {
+    const int len = seq_len_of(p, s);
+    int rank = 0;
+    for (int o = 0; o < p.S; ++o) {
+      const int lo = seq_len_of(p, o);
+      rank += (lo > len || (lo == len && o < s)) ? 1 : 0;
+    }
+    p.order[rank] = s;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_paged_seq_order(const PagedParams& p, cudaStream_t s) {
+  if (p.S <= 0) return cudaSuccess;
+  const int blocks = (p.S + 255) / 256 < 1024 ? (p.S + 255) / 256 : 1024;
+  seq_order_kernel<<<blocks, 256, 0, s>>>(p);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_paged_listed(const PagedParams& p, const int32_t* pages, int64_t n, cudaStream_t s) {
   cudaError_t e;

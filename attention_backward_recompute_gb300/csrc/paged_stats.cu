@@ -60,11 +60,21 @@ __global__ void __launch_bounds__(256, 1)
   __shared__ int max_pos_sh;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int qt = blockIdx.x, sq = blockIdx.y, g = blockIdx.z;
+  __shared__ int tile_sq_sh, tile_r0_sh;
+  // block x = tile * KVH + g: row tile `tile` of the sequences in dispatch
+  // order (longest first), KV head g
+  const int g = static_cast<int>(blockIdx.x % p.KVH);
   const int RT = L::BQ / p.G;  // query rows per tile
-  const int r_begin = row_begin_of(p, sq), r_end = row_end_of(p, sq);
-  const int r0 = r_begin + qt * RT;
-  if (r0 >= r_end) return;  // uniform exit: no rows in this tile
+  if (threadIdx.x == 0) {
+    int sq_, r0_;
+    row_tile_at(p, static_cast<int>(blockIdx.x / p.KVH), RT, &sq_, &r0_);
+    tile_sq_sh = sq_;
+    tile_r0_sh = r0_;
+  }
+  __syncthreads();
+  const int sq = tile_sq_sh, r0 = tile_r0_sh;
+  if (sq < 0) return;  // uniform exit: past the last row tile
+  const int r_end = row_end_of(p, sq);
   const int len = seq_len_of(p, sq);
   const int npg = pages_of(len, p.page_size);
   const Abort ab{&abort_flag, p.err};
@@ -345,7 +355,8 @@ cudaError_t launch_stats_t(const PagedMaps& m, const PagedParams& p, cudaStream_
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int rt = L::BQ / p.G;
-  dim3 grid((p.Nq + rt - 1) / rt, p.S, p.KVH);
+  // row tiles: at most Nq / rt + S (one partial tile per sequence)
+  dim3 grid(static_cast<unsigned>((static_cast<int64_t>(p.Nq) / rt + p.S + 1) * p.KVH));
   kern<<<grid, 256, smem, s>>>(m.q_stats, m.dy_stats, m.k, m.v, p);
   return cudaGetLastError();
 }

@@ -288,7 +288,9 @@ ATTN_API attn_status_t attn_bwd_paged_compact(const attn_paged_desc* d, const vo
  * Row statistics for the paged path by a forward sweep over each sequence's
  * pages: lse[r, h] = log sum_t exp(s_rt) over visible tokens (-inf if none)
  * and delta[r, h] = rowsum(P * dP) = dY . O.  Same arguments as
- * attn_bwd_paged; lse and delta are fp32 [Nq, H] outputs.
+ * attn_bwd_paged; lse and delta are fp32 [Nq, H] outputs.  The workspace
+ * (as for attn_bwd_paged, else ATTN_ERR_WORKSPACE) holds the order in which
+ * the row tiles are dispatched (longest sequences first).
  */
 ATTN_API attn_status_t attn_paged_row_stats(const attn_paged_desc* d, const void* q, const void* qp,
                                             const void* k_pool, const void* v_pool, const void* kp_pool,
@@ -371,9 +373,12 @@ ATTN_API attn_status_t attn_fwd_dense(const attn_dense_desc* d, const void* q, c
  * row is written exactly once: a row with no visible token, or outside every
  * sequence's query range, gets dq = 0, lse = -inf and delta = 0.  Tokens are
  * visited in a fixed order, so the result is bit-identical from run to run.
- * MLA (position_dim > 0) needs heads / kv_heads in {4, 8, 16, 32} and page
- * size 16 (else ATTN_ERR_UNSUPPORTED); qp, kp_pool and dqp are then required.
- * The workspace is that of attn_bwd_paged.
+ * MLA (position_dim > 0) needs heads / kv_heads dividing 64 and page size 16
+ * (else ATTN_ERR_UNSUPPORTED); qp, kp_pool and dqp are then required.
+ * The workspace is that of attn_bwd_paged (at least
+ * attn_bwd_paged_workspace_bytes(d) bytes, 256-byte aligned, else
+ * ATTN_ERR_WORKSPACE): it holds the order in which the row tiles are
+ * dispatched (longest sequences first).
  */
 ATTN_API attn_status_t attn_bwd_paged_query(const attn_paged_desc* d, const void* q, const void* qp,
                                             const void* k_pool, const void* v_pool, const void* kp_pool,

@@ -196,6 +196,25 @@ def test_paged_compact_checks(lib):
     assert _compact_call(d0, FAKE + 34 * MB, 5) == bd.ATTN_OK
 
 
+def test_paged_query_side_needs_workspace(lib):
+    """The row-statistics and query-side calls keep their dispatch order (the
+    sequences by length) in the paged workspace: a missing, short or
+    misaligned one is refused before any device work."""
+    d = bd.make_paged_desc(num_queries=64, num_seqs=4, heads=8, kv_heads=2, page_size=16, num_pages=100,
+                           max_pages_per_seq=10, key_dim=128, value_dim=128)
+    n = bd.attn_bwd_paged_workspace_bytes(d)
+    assert n >= 100 + (4 + 101 + 100 + 40 + 4) * 4
+    L = bd.lib()
+    args = [ctypes.c_void_p(FAKE), None, ctypes.c_void_p(FAKE + 8 * MB), ctypes.c_void_p(FAKE + 16 * MB), None,
+            ctypes.c_void_p(FAKE + 24 * MB), ctypes.c_void_p(FAKE + 30 * MB), ctypes.c_void_p(FAKE + 31 * MB),
+            ctypes.c_void_p(FAKE + 32 * MB), ctypes.c_void_p(FAKE + 33 * MB)]
+    for ws, nb in ((None, 0), (FAKE + 40 * MB, n - 1), (FAKE + 40 * MB + 16, n)):
+        w = ws and ctypes.c_void_p(ws)
+        assert int(L.attn_paged_row_stats(ctypes.byref(d), *args, w, nb, None)) == bd.ATTN_ERR_WORKSPACE
+        assert int(L.attn_bwd_paged_query(ctypes.byref(d), *args, ctypes.c_void_p(FAKE + 34 * MB), None, w, nb,
+                                          None)) == bd.ATTN_ERR_WORKSPACE
+
+
 def test_store_ds_option_checks(lib):
     """ATTN_OPT_STORE_DS grows the workspace by one 128 x 64 bf16 dS tile per
     (batch, head, key tile of 128, query tile of 64); fp32 storage and unknown
