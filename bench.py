@@ -262,6 +262,43 @@ def sweep(args) -> int:
         bd.check_device_error()
         return statistics.median(ts), min(ts)
 
+    flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+
+    def timed_flushed(fn, reps):
+        # a 256 MiB write (twice L2) between repetitions, outside the timed region
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(reps):
+            flush_buf.fill_(1)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return statistics.median(ts)
+
+    def oracle_one_thread(name, heads, over):
+        # the oracle with its BLAS held to one thread, in a child process (the
+        # thread count of a loaded BLAS cannot be changed in place)
+        import subprocess
+        code = ("import json, sys, time; sys.path.insert(0, %r)\n"
+                "from attention_backward_recompute_gb300 import inputs\n"
+                "from oracle import attn_bwd_dense\n"
+                "c = inputs.dense_config(%r)\n"
+                "over = %r\n"
+                "km = None if over.get('no_mask_bias') else c.key_mask\n"
+                "bias = None if over.get('no_mask_bias') else c.bias\n"
+                "t0 = time.perf_counter()\n"
+                "attn_bwd_dense(c.q, c.k, c.v, c.dy, layout=c.layout, causal=c.causal, window=c.window, "
+                "key_mask=km, bias=bias, heads_subset=%r)\n"
+                "print(json.dumps(time.perf_counter() - t0))\n") % (ROOT, name, over, heads)
+        env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+        r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=600)
+        return float(r.stdout.strip().splitlines()[-1]) if r.returncode == 0 else None
+
     def rel(got, want, mask=None):
         g = got.float().cpu().numpy().astype(np.float64)
         if mask is not None:
@@ -277,7 +314,8 @@ def sweep(args) -> int:
         return only is None or only.search(tag) is not None
 
     dense = [("C1", "dense_small_f32", {}), ("C2c", "dense_f32_causal", {}), ("C2w", "dense_f32_window", {}),
-             ("C3", "dense_bf16_s2048", {}), ("C3 O+LSE supplied", "dense_bf16_s2048", {"supplied": True}),
+             ("C3", "dense_bf16_s2048", {}), ("C3 causal only", "dense_bf16_s2048", {"no_mask_bias": True}),
+             ("C3 O+LSE supplied", "dense_bf16_s2048", {"supplied": True}),
              ("C4", "dense_bf16_cross", {}),
              ("C3 stored dS", "dense_bf16_s2048", {"store_ds": True}),
              ("C3 O+LSE supplied, stored dS", "dense_bf16_s2048", {"supplied": True, "store_ds": True}),
@@ -289,6 +327,8 @@ def sweep(args) -> int:
         dt = torch.float32 if c.dtype == "f32" else torch.bfloat16
         t = lambda x: torch.from_numpy(np.ascontiguousarray(x)).cuda().to(dt)
         q, k, v, dy = t(c.q), t(c.k), t(c.v), t(c.dy)
+        if opt.get("no_mask_bias"):  # the same shape without key mask and bias: what the bias reads cost
+            c.key_mask = c.bias = None
         km = None if c.key_mask is None else torch.from_numpy(c.key_mask).cuda()
         bias = None if c.bias is None else t(c.bias)
         o = lse = None
@@ -301,7 +341,9 @@ def sweep(args) -> int:
         call = lambda: bd.dense_backward(q, k, v, dy, layout=c.layout, causal=c.causal, window=c.window,
                                          key_mask=km, bias=bias, o=o, lse=lse, outputs=outs,
                                          store_ds=bool(opt.get("store_ds")))
-        ms, ms_min = timed(call, 20 if c.seq_q * c.seq_k * c.batch * c.heads > 1e7 else 50)
+        reps = 20 if c.seq_q * c.seq_k * c.batch * c.heads > 1e7 else 50
+        ms, ms_min = timed(call, reps)
+        ms_flushed = timed_flushed(call, reps)
         # per-kernel split of one call (fp32 storage first splits its inputs)
         names = (["split"] if c.dtype == "f32" else []) + ["prologue", "dkdv", "dq"]
         kev = [torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
@@ -331,7 +373,23 @@ def sweep(args) -> int:
                 gs = np.stack([gh[b, h] for b, h in sample]); ws = np.stack([w[b, h] for b, h in sample])
             errs.append(float(np.max(np.abs(gs - ws)) / max(np.max(np.abs(ws)), 1e-30)))
         tflops = flops / (ms * 1e-3) / 1e12
+        # algorithmic bytes: q, dy, dq and k, v, dk, dv once, the visible bias once, the key mask
+        es = 4 if c.dtype == "f32" else 2
+        alg_bytes = (es * c.head_dim * c.batch * c.heads * (3 * c.seq_q + 4 * c.seq_k) +
+                     (2 * vp * c.batch * c.heads if c.bias is not None else 0) +
+                     (4 * c.batch * c.seq_k if c.key_mask is not None else 0))
+        one = None
+        if tag in ("C1", "C2c", "C2w", "C3"):
+            h1 = heads[:1] if tag == "C3" else heads
+            t1 = oracle_one_thread(name, h1, dict(opt))
+            if t1 is not None:
+                one = {"s": t1, "sample": f"{len(h1)} of {len(heads)} (batch, head) pairs",
+                       "s_extrapolated": t1 * len(heads) / len(h1)}
         emit({"config": tag, "workload": name, "gpu_ms_median": ms, "gpu_ms_min": ms_min, "kernel_ms": kernel_ms,
+              "gpu_ms_median_l2_flushed": ms_flushed, "l2_flush": "256 MiB write between repetitions",
+              "algorithmic_gbs": alg_bytes / (ms * 1e-3) / 1e9,
+              "pct_of_hbm_peak": 100.0 * alg_bytes / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+              "oracle_one_thread": one,
               "counted_tflops": tflops, "pct_of_bf16_peak": 100.0 * tflops / peaks["bf16_tflops"],
               "max_err_rel": max(errs), "tolerance": 2e-4 if c.dtype == "f32" else 2e-2,
               "oracle_s_sample": t_or, "oracle_sample": f"{len(sample)} of {len(heads)} (batch, head) pairs",
