@@ -256,6 +256,11 @@ ATTN_API attn_status_t attn_bwd_paged_compact(const attn_paged_desc* d, const vo
     attn::timing_mark(s);
     if (e == cudaSuccess) e = attn::launch_paged_mla_tc_plan(p, s);
     attn::timing_mark(s);
+    // The grid kernels start as programmatic dependents of the split kernel:
+    // both launchers skip on the same condition (no pages, sequences or page
+    // table columns), so whenever a grid kernel launches, the split kernel was
+    // the launch just before it; the plan they both read completed before the
+    // split kernel started (plain stream order).
     if (e == cudaSuccess) e = attn::launch_paged_mla_tc_split(mt, p, s);
     attn::timing_mark(s);
     if (e == cudaSuccess) e = attn::launch_paged_mla_tc(mt, p, true, s);
