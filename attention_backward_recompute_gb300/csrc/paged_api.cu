@@ -18,7 +18,7 @@ using attn::api_ok;
 struct PagedSizes {
   size_t q_bytes, qp_bytes, dy_bytes, k_bytes, v_bytes, kp_bytes, table_bytes, meta_bytes, stat_bytes;
   size_t ws_bytes;
-  size_t off_count, off_off, off_fill, off_links, off_heavy, off_listed, off_order;
+  size_t off_count, off_off, off_fill, off_links, off_heavy, off_listed, off_order, off_work, off_split;
 };
 
 size_t a256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -67,7 +67,10 @@ attn_status_t check_paged_desc(const attn_paged_desc* d, PagedSizes* z) {
   z->off_heavy = z->off_links + a256(size_t(d->num_seqs) * d->max_pages_per_seq * 4 + 4);
   z->off_listed = z->off_heavy + a256(size_t(d->num_seqs) * ((d->max_pages_per_seq + 7) / 8) * d->kv_heads * 4 + 4);
   z->off_order = z->off_listed + a256(size_t(d->num_pages) + 4);
-  z->ws_bytes = z->off_order + a256(size_t(d->num_seqs) * 4 + 4);
+  z->off_work = z->off_order + a256(size_t(d->num_seqs) * 4 + 4);
+  z->off_split = z->off_work + a256(size_t(attn::kMlaWorkInts) * 4);
+  // MLA: the split kernel's chunk partials (fp32)
+  z->ws_bytes = z->off_split + (d->position_dim != 0 ? attn::kMlaSplitFloats * 4 : 0);
   return ATTN_OK;
 }
 
@@ -108,6 +111,8 @@ attn_status_t fill_params(const attn_paged_desc* d, const PagedSizes& z, const i
   p->heavy = reinterpret_cast<int32_t*>(ws + z.off_heavy);
   p->listed = nullptr;  // every page (the compact call points it at its map)
   p->order = reinterpret_cast<int32_t*>(ws + z.off_order);
+  p->work = reinterpret_cast<int32_t*>(ws + z.off_work);
+  p->split_part = d->position_dim != 0 ? reinterpret_cast<float*>(ws + z.off_split) : nullptr;
   p->err = attn::device_error_word();
   if (!p->err) return api_fail(ATTN_ERR_CUDA, "no CUDA device / symbol address unavailable");
   return ATTN_OK;

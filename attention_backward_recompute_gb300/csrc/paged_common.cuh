@@ -41,11 +41,23 @@ struct PagedParams {
   int32_t* link_off;           // [num_pages + 1]
   int32_t* link_fill;          // [num_pages]
   int32_t* links;              // [S * max_pages]: link ids s*max_pages+lp grouped by page
-  int32_t* heavy;              // [S, ceil(max_pages / 8), KVH]: MLA blocks left to the split kernel
+  int32_t* heavy;              // [S, ceil(max_pages / 8), KVH]: MLA blocks left to the split kernel (tile count; 0: not flagged)
   uint8_t* listed;             // [num_pages] compact history: 1 = compute and store the page; null = all
   int32_t* order;              // [S] sequences by decreasing length (ties by index): query-side dispatch order
+  // MLA history counters, zeroed by the plan kernel: [0, 2) the grid kernel's
+  // next unit per part, [2, 4) the split kernel's next item per part, then
+  // [part][unit][cluster rank] the chunks of a unit reduced so far
+  int32_t* work;               // [kMlaWorkInts]
+  float* split_part;           // MLA split chunk partials: part 0 [kMlaSplitSlots][128][256], then part 1 [..][128][320]
   uint32_t* err;
 };
+
+// The MLA split kernel cuts a flagged block into chunks when few blocks are
+// flagged; at most this many chunk partials are open per part.
+constexpr int kMlaSplitSlots = 128;
+constexpr int kMlaSplitRanks = 8;  // CTAs of a split cluster
+constexpr int kMlaWorkInts = 4 + 2 * kMlaSplitSlots * kMlaSplitRanks;
+constexpr size_t kMlaSplitFloats = static_cast<size_t>(kMlaSplitSlots) * 128 * (256 + 320);
 
 // device error codes of the paged prep (OR-ed into the error word)
 constexpr uint32_t kErrBadPage = 4u;   // a page-table entry outside [0, num_pages)

@@ -45,10 +45,11 @@ cudaError_t launch_paged_listed(const PagedParams& p, const int32_t* pages, int6
 bool mla_tc_supported(const PagedParams& p);
 cudaError_t launch_paged_mla_tc(const PagedMlaMaps& m, const PagedParams& p, bool after_split, cudaStream_t s);
 // flags the 128-token MLA history blocks whose shared pages carry many link
-// tiles (p.heavy [S, ceil(max_pages / 8), KVH])
+// tiles (p.heavy [S, ceil(max_pages / 8), KVH]: their tile counts) and zeroes
+// the MLA work counters
 cudaError_t launch_paged_mla_tc_plan(const PagedParams& p, cudaStream_t s);
-// the flagged blocks, by persistent clusters of 8 CTAs on tcgen05 (the same
-// maps as launch_paged_mla_tc)
+// the flagged blocks, by persistent clusters of 8 CTAs on tcgen05, cut into
+// chunks when few are flagged (the same maps as launch_paged_mla_tc)
 cudaError_t launch_paged_mla_tc_split(const PagedMlaMaps& m, const PagedParams& p, cudaStream_t s);
 // MLA row statistics on tcgen05; maps with 128-column boxes (128/G rows)
 bool mla_stats_tc_supported(const PagedParams& p);

@@ -25,12 +25,14 @@
 // A block whose shared pages carry many link tiles (a long prefix shared by
 // many sequences) would serialise the other sequences' work on its one owner:
 // a plan kernel flags such blocks, the grid kernel leaves them, and a
-// persistent kernel of 8-CTA clusters takes them, one (block, part) per
-// cluster at a time.  CTA r of the cluster runs the r-th contiguous eighth of
-// the block's tiles through the same pipeline into its own tensor-memory
-// accumulator; the eight partial sums meet in shared memory and each CTA adds
-// 16 tokens' partials over the cluster in rank order (distributed shared
-// memory: a fixed order, no atomics, no workspace), then stores them.
+// persistent kernel of 8-CTA clusters takes them (when few are flagged, cut
+// into chunks of contiguous tiles).  CTA r of the cluster that takes a chunk
+// runs the r-th eighth of its tiles through the same pipeline into its own
+// tensor-memory accumulator; the eight partial sums meet in shared memory and
+// each CTA adds 16 tokens' partials over the cluster in rank order
+// (distributed shared memory), then stores them, or, for a cut block, leaves
+// them in a workspace slot that the block's last chunk adds in chunk order:
+// every sum in a fixed order, no floating-point atomics.
 //
 // Shared memory: the K tile stays resident (latent + position, 9 chunks of
 // [128 tokens x 64 dims], 144 KiB); Q, Qp and dY arrive as a stream of 8 KiB
@@ -468,59 +470,88 @@ __device__ __forceinline__ bool run_block(const CUtensorMap* tm_q, const CUtenso
 // goes to the split kernel (its own pass has 64 rows x G heads / 64 columns).
 constexpr int kHeavyLinkTiles = 64;
 constexpr int kSplitCL = 8;                       // CTAs of a split cluster; CTA r sums tokens [16r, 16r + 16)
+constexpr int kMinPieceTiles = 4;                 // a block is not cut into pieces smaller than this
+constexpr int kItemTiles = 8;                     // fixed cost of a split item, in tiles
 constexpr int RED_STRIDE = 324;                   // floats per token row of a staged partial (320 + 4: bank spread)
 static_assert(BT * RED_STRIDE * 4 <= BYTES, "a partial fits the pipeline's shared memory");
 static_assert(BT % kSplitCL == 0, "tokens split evenly over the cluster");
 
+// The rows of the pages this block stores: 32-column chunks of the part's
+// accumulator, alternating between the compute groups (latent dims [256 PART
+// + 32 cc, ...) for cc < 8, position dims after that, PART 1); rows of tokens
+// no pass saw are zero (n = 0).  Called by the compute warps.
+template <int PART>
+__device__ __forceinline__ void store_block(const PagedParams& p, uint32_t tmem, const PageInfo& pinfo, int g, int n,
+                                            bool ok) {
+  using PS = PartShape<PART>;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int sg = (warp - 4) >> 2;
+  const int lg = warp & 3;
+  const int row = lg * 32 + lane;  // token row inside the block == TMEM lane
+  const uint32_t lane_addr = static_cast<uint32_t>(lg * 32) << 16;
+  if (ok || n == 0) {  // warp-uniform: the tensor-memory loads are warp-collective
+    const int j = row >> 4;
+    const bool mine = pinfo.store[j] != 0;
+    const int64_t prow = (static_cast<int64_t>(pinfo.phys[j]) * p.page_size + (row & 15)) * p.KVH + g;
+#pragma unroll 1
+    for (int cc = sg; cc < PS::ACC_COLS / 32; cc += 2) {
+      const bool pos_chunk = cc >= 8;
+      if (!(p.wrt & (pos_chunk ? 8u : 2u))) continue;
+      uint32_t r[32];
+      if (n > 0) {
+        tmem_ld32(tmem + T_ACC + cc * 32 + lane_addr, r);
+        tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) r[i] = 0u;
+      }
+      if (mine) {
+        __nv_bfloat16* out = pos_chunk
+                                 ? static_cast<__nv_bfloat16*>(p.dkp_pool) + prow * kPos + (cc - 8) * 32
+                                 : static_cast<__nv_bfloat16*>(p.dk_pool) + prow * kLat + 256 * PART + cc * 32;
+        store_row32_bf16(out, r, 1.f, 32);
+      }
+    }
+  }
+}
+
+// The grid part of the MLA history, one launch per part: persistent CTAs (one
+// per SM) take units (sequence, 128-token block, KV head) from the part's
+// counter; a unit runs the block's tiles through the pipeline and stores the
+// rows of the pages it owns.  Blocks the plan flagged
+// belong to the split kernel, blocks past a sequence's end do not exist here.
+// Each unit is computed whole by one CTA, so the results do not depend on
+// which CTA takes it.
 template <int PART>
 __global__ void __launch_bounds__(384, 1)
     mla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_qp,
                   const __grid_constant__ CUtensorMap tm_dy, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_kp, const PagedParams p) {
-  using PS = PartShape<PART>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ TcBars bars;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
   __shared__ PageInfo pinfo;
-  __shared__ int n_tiles_sh, any_store_sh;
+  __shared__ int unit_sh[3], n_tiles_sh, any_store_sh;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = blockIdx.x, tb = blockIdx.y, s0 = blockIdx.z;
-  // Launched as the programmatic dependent of the kernel before it (the
-  // cluster-split kernel, or PART 0 for PART 1), whose results it does not
-  // read: its own dependent may start at once, and the last CTA waits for the
-  // kernel before, so that this grid completes after it and later work in
-  // the stream sees both.  Without a programmatic launch both are no-ops.
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (blockIdx.x == gridDim.x - 1 && blockIdx.y == gridDim.y - 1 && blockIdx.z == gridDim.z - 1)
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int len0 = seq_len_of(p, s0);
-  const int npg = pages_of(len0, p.page_size);
-  if (tb * 8 >= npg) return;  // no token of this sequence in the block (uniform exit)
-  const int RT = BC / p.G;    // query rows per tile
+  const int RT = BC / p.G;  // query rows per tile
+  const int nb128 = (p.max_pages + 7) / 8;
+  constexpr int part = PART;
   const Abort ab{&abort_flag, p.err};
-
+  // Launched as the programmatic dependent of the kernel before it (the
+  // split kernel, or part 0 for part 1), whose results it does not read (the
+  // plan it reads completed before the split kernel started): its own
+  // dependent may start at once, on the SMs it leaves free, and its last CTA
+  // waits for the kernel before after its own units, so that this grid
+  // completes after it and later work in the stream sees both.  Without a
+  // programmatic launch both are no-ops.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x == 0) {
     abort_flag = 0;
     tc_bars_init(bars);
-    int any = fill_page_info(p, s0, tb, npg, &pinfo);
-    // a block the plan flagged belongs to the cluster-split kernel
-    if (any && p.heavy && p.heavy[(static_cast<int64_t>(s0) * ((p.max_pages + 7) / 8) + tb) * p.KVH + g]) any = 0;
-    any_store_sh = any;
-    PassIter it{&p, &pinfo, s0, tb};
-    int n = 0;
-    if (any && it.begin(RT)) {
-      do ++n;
-      while (it.advance(RT));
-    }
-    n_tiles_sh = n;
   }
-  __syncthreads();
-  // a block whose pages are all stored by other CTAs (their owners) has
-  // nothing to write: leave before taking tensor memory (uniform exit)
-  if (!any_store_sh) return;
   if (warp == 1) {
     tmem_alloc(&tmem_base_sh, TMEM_COLS);
     tmem_relinquish();
@@ -536,44 +567,58 @@ __global__ void __launch_bounds__(384, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
-  const int n = n_tiles_sh;
-  bool ok = true;
-  if (n > 0) ok = run_block<PART>(&tm_q, &tm_qp, &tm_dy, &tm_k, &tm_kp, p, bars, sm, tmem, pinfo, s0, tb, g, 0, n,
-                                  TcEpoch{0, 0, 0}, ab);
-  if (warp >= 4) {
-    const int sg = (warp - 4) >> 2;
-    const int lg = warp & 3;
-    const int row = lg * 32 + lane;  // token row inside the block == TMEM lane
-    const uint32_t lane_addr = static_cast<uint32_t>(lg * 32) << 16;
-    // ------------------------------------------------------------ epilogue
-    // 32-column chunks of the accumulator, alternating between the groups:
-    // latent dims [256 PART + 32 cc, ...) for cc < 8, position dims after
-    // that (PART 1); rows of tokens no pass saw are zero
-    if (ok || n == 0) {  // warp-uniform: the tensor-memory loads are warp-collective
-      const int j = row >> 4;
-      const bool mine = pinfo.store[j] != 0;
-      const int64_t prow = (static_cast<int64_t>(pinfo.phys[j]) * p.page_size + (row & 15)) * p.KVH + g;
-#pragma unroll 1
-      for (int cc = sg; cc < PS::ACC_COLS / 32; cc += 2) {
-        const bool pos_chunk = cc >= 8;
-        if (!(p.wrt & (pos_chunk ? 8u : 2u))) continue;
-        uint32_t r[32];
-        if (n > 0) {
-          tmem_ld32(tmem + T_ACC + cc * 32 + lane_addr, r);
-          tmem_ld_wait();
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) r[i] = 0u;
+  TcEpoch ep{0, 0, 0};
+  while (true) {
+    __syncthreads();  // the previous unit's readers of pinfo and unit_sh are done
+    if (threadIdx.x == 0) {
+      // unit k of the part: sequences in order, each with blocks x KV heads
+      int k = atomicAdd(p.work + part, 1), s0 = -1;
+      for (int s = 0; s < p.S; ++s) {
+        const int units = ((seq_len_of(p, s) + BT - 1) / BT) * p.KVH;
+        if (k < units) {
+          s0 = s;
+          break;
         }
-        if (mine) {
-          __nv_bfloat16* out = pos_chunk
-                                   ? static_cast<__nv_bfloat16*>(p.dkp_pool) + prow * kPos + (cc - 8) * 32
-                                   : static_cast<__nv_bfloat16*>(p.dk_pool) + prow * kLat + 256 * PART + cc * 32;
-          store_row32_bf16(out, r, 1.f, 32);
+        k -= units;
+      }
+      unit_sh[0] = s0;
+      int any = 0, n = 0;
+      if (s0 >= 0) {
+        const int g = k % p.KVH, tb = k / p.KVH;
+        unit_sh[1] = tb;
+        unit_sh[2] = g;
+        any = fill_page_info(p, s0, tb, pages_of(seq_len_of(p, s0), p.page_size), &pinfo);
+        // a block the plan flagged belongs to the cluster-split kernel
+        if (any && p.heavy[(static_cast<int64_t>(s0) * nb128 + tb) * p.KVH + g]) any = 0;
+        PassIter it{&p, &pinfo, s0, tb};
+        if (any && it.begin(RT)) {
+          do ++n;
+          while (it.advance(RT));
         }
       }
+      any_store_sh = any;
+      n_tiles_sh = n;
+    }
+    __syncthreads();
+    if (unit_sh[0] < 0) break;  // no units left (uniform)
+    // a block whose pages are all stored by other CTAs (their owners) has
+    // nothing to write (uniform)
+    if (!any_store_sh) continue;
+    const int s0 = unit_sh[0], tb = unit_sh[1], g = unit_sh[2];
+    const int n = n_tiles_sh;
+    bool ok = true;
+    if (n > 0) ok = run_block<PART>(&tm_q, &tm_qp, &tm_dy, &tm_k, &tm_kp, p, bars, sm, tmem, pinfo, s0, tb, g, 0, n, ep, ab);
+    if (warp >= 4) {
+      store_block<PART>(p, tmem, pinfo, g, n, ok);
+      tc_fence_before();
+    }
+    if (n > 0) {
+      ep.T += n;
+      ep.Q += n * jobs_per_tile<PART>();
+      ++ep.B;
     }
   }
+  if (blockIdx.x == gridDim.x - 1) asm volatile("griddepcontrol.wait;" ::: "memory");
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -586,11 +631,6 @@ __global__ void __launch_bounds__(384, 1)
 __device__ __forceinline__ int cluster_rank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return static_cast<int>(r);
-}
-__device__ __forceinline__ int cluster_index() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
   return static_cast<int>(r);
 }
 __device__ __forceinline__ int cluster_count() {
@@ -625,61 +665,107 @@ __device__ __forceinline__ float4 ld_cluster_f4(uint32_t addr) {
   return v;
 }
 
-// Plan of the MLA history: heavy[(s0 * nblk + tb) * KVH + g] = 1 when the
-// pages 128-token block tb of sequence s0 stores carry more than
-// kHeavyLinkTiles tiles of other links (counting stops there), else 0; one
-// thread per block.
+// Tiles of the passes at link index li >= 1 of a block (the stored pages
+// pi): the passes PassIter::next_pass enumerates at that index, each run of
+// consecutive stored pages whose li-th links are consecutive logical pages
+// of one sequence counting that sequence's row tiles once.
+__device__ int link_tiles_at(const PagedParams& p, const PageInfo& pi, int li, int rt) {
+  int n = 0;
+  for (int j = 0; j < 8;) {
+    if (!(pi.store[j] && li < pi.cnt[j])) {
+      ++j;
+      continue;
+    }
+    const int link = p.links[pi.off[j] + li];
+    const int s2 = link / p.max_pages, lp2 = link - s2 * p.max_pages;
+    int jn = j + 1;
+    while (jn < 8 && pi.store[jn] && li < pi.cnt[jn] && lp2 + (jn - j) < p.max_pages &&
+           p.links[pi.off[jn] + li] == link + (jn - j))
+      ++jn;
+    const int rb = row_begin_of(p, s2);
+    n += (row_end_of(p, s2) - rb + rt - 1) / rt;
+    j = jn;
+  }
+  return n;
+}
+
+// Plan of the MLA history: heavy[(s0 * nblk + tb) * KVH + g] = the block's
+// tile count when the pages 128-token block tb of sequence s0 stores carry
+// more than kHeavyLinkTiles tiles of other links, else 0; one warp per block,
+// its lanes taking the link indices.
 __global__ void mla_tc_plan_kernel(const PagedParams p) {
   const int nblk = (p.max_pages + 7) / 8;
   const int n = p.S * nblk;
   const int RT = BC / p.G;
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+  const int lane = threadIdx.x & 31, wpb = static_cast<int>(blockDim.x >> 5);
+  if (blockIdx.x == 0)  // the grid and split kernels' counters
+    for (int i = threadIdx.x; i < kMlaWorkInts; i += blockDim.x) p.work[i] = 0;
+  for (int i = blockIdx.x * wpb + static_cast<int>(threadIdx.x >> 5); i < n; i += gridDim.x * wpb) {  // warp-uniform
     const int s0 = i / nblk, tb = i - s0 * nblk;
     const int npg = pages_of(seq_len_of(p, s0), p.page_size);
     int heavy = 0;
     if (tb * 8 < npg) {
       PageInfo pi;
       if (fill_page_info(p, s0, tb, npg, &pi)) {
-        PassIter it{&p, &pi, s0, tb};
+        int lmax = 0;
+        for (int k = 0; k < 8; ++k)
+          if (pi.store[k] && pi.cnt[k] > lmax) lmax = pi.cnt[k];
         int n_link = 0;
-        if (it.begin(RT)) {
-          do n_link += it.j >= 0 ? 1 : 0;
-          while (n_link <= kHeavyLinkTiles && it.advance(RT));
-        }
-        heavy = n_link > kHeavyLinkTiles;
+        for (int li = 1 + lane; li < lmax; li += 32) n_link += link_tiles_at(p, pi, li, RT);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) n_link += __shfl_xor_sync(0xffffffffu, n_link, o);
+        const int rb = row_begin_of(p, s0);
+        const int n_own = (row_end_of(p, s0) - rb + RT - 1) / RT;  // the block's own pass
+        heavy = n_link > kHeavyLinkTiles ? n_own + n_link : 0;
       }
     }
-    for (int g = 0; g < p.KVH; ++g) p.heavy[static_cast<int64_t>(i) * p.KVH + g] = heavy;
+    for (int g = lane; g < p.KVH; g += 32) p.heavy[static_cast<int64_t>(i) * p.KVH + g] = heavy;
   }
 }
 
-// Persistent clusters of kSplitCL CTAs take the (flagged block, part) units
-// in flag order, unit u to cluster u mod clusters; CTA r of a cluster runs
-// the block's tiles [r n / kSplitCL, (r + 1) n / kSplitCL) of its n into its
-// accumulator, stages the partial in shared memory, and after a cluster
-// barrier adds tokens [16 r, 16 r + 16) over the cluster's partials in rank
-// order (the result does not depend on the number of clusters or on timing).
+// Persistent clusters of kSplitCL CTAs, one launch per part (a kernel holding
+// both parts' pipelines needs more registers and ran slower).  The work of a
+// part is nflag x C items: item k is chunk c = k / nflag of the (k mod
+// nflag)-th flagged block in flag order, and the clusters take items from the
+// part's counter.  C minimises the rounds of the clusters times the item
+// cost (its tiles plus a fixed cost): 1 when the blocks already fill whole
+// rounds, more when a few heavy blocks would leave clusters idle.
+//
+// The block's n tiles form 8C contiguous pieces; CTA r of the cluster that
+// takes chunk c runs piece 8c + r into its tensor-memory accumulator, stages
+// the partial in shared memory, and after a cluster barrier adds tokens
+// [16 r, 16 r + 16) over the cluster's partials in rank order.  With C = 1
+// that sum is stored; otherwise it goes to the chunk's fp32 slot, and the CTA
+// of rank r that completes a block's last chunk (a per-rank counter) adds the
+// block's C slots in chunk order and stores the sum.  Every sum has a fixed
+// order, so the result does not depend on which cluster takes which item.
+template <int PART>
 __global__ void __launch_bounds__(384, 1)
     mla_tc_split_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_qp,
                         const __grid_constant__ CUtensorMap tm_dy, const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_kp, const PagedParams p) {
+  static_assert(kSplitCL == kMlaSplitRanks, "the counters hold one entry per cluster rank");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ TcBars bars;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag, abort_any_sh;
   __shared__ PageInfo pinfo;
-  __shared__ int n_all_sh;
-  __shared__ int items_sh[384];
+  __shared__ int item_sh, k_sh, found_sh, last_sh, min_tiles_sh;
+  constexpr int kListed = kMlaSplitSlots / 2;  // more flagged blocks than this: C = 1
+  __shared__ int listed_sh[kListed];
   __shared__ int warp_cnt[12];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int RT = BC / p.G;
-  const int rank = cluster_rank(), cid = cluster_index(), ncl = cluster_count();
+  const int nwarps = static_cast<int>(blockDim.x >> 5);
+  const int rank = cluster_rank(), ncl = cluster_count();
   const int nblk = (p.max_pages + 7) / 8;
+  const int nitems = p.S * nblk * p.KVH;
+  constexpr int acc_cols = PartShape<PART>::ACC_COLS;
   const Abort ab{&abort_flag, p.err};
-  // the grid kernels, launched next as programmatic dependents, may start on
-  // the SMs these clusters leave free
+  // the kernels launched next (part 1, then the grid kernels) as programmatic
+  // dependents may start on the SMs these clusters leave free; part 1's last
+  // CTA waits for part 0 at the end, so that the chain completes in order
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x == 0) {
     abort_flag = 0;
@@ -701,30 +787,80 @@ __global__ void __launch_bounds__(384, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
   float* red = reinterpret_cast<float*>(sm);  // staged partial: [BT][RED_STRIDE] fp32
+  float* slots = p.split_part + (PART == 1 ? static_cast<size_t>(kMlaSplitSlots) * BT * 256 : 0);
+  int32_t* done = p.work + 4 + PART * kMlaSplitSlots * kMlaSplitRanks;
   TcEpoch ep{0, 0, 0};
 
-  auto run_unit = [&](int item, int part) {
-    const int g = item % p.KVH, rest = item / p.KVH, tb = rest % nblk, s0 = rest / nblk;
-    __syncthreads();  // the previous unit's readers of pinfo are done
-    if (threadIdx.x == 0) {
-      fill_page_info(p, s0, tb, pages_of(seq_len_of(p, s0), p.page_size), &pinfo);
-      PassIter it{&p, &pinfo, s0, tb};
-      int n_all = 0;
-      if (it.begin(RT)) {
-        do ++n_all;
-        while (it.advance(RT));
-      }
-      n_all_sh = n_all;
-    }
+  // One window of blockDim.x block indices from c0: the flagged ones are
+  // ranked in index order from `base`; returns the window's flagged count and
+  // records in found_sh the index ranked `want` if it lies in the window.
+  auto window = [&](int c0, int base, int want) {
+    const int i = c0 + threadIdx.x;
+    const int h = i < nitems ? p.heavy[i] : 0;
+    const bool f = h != 0;
+    if (want < 0 && f) atomicMin(&min_tiles_sh, h);  // the counting pass
+    const uint32_t bal = __ballot_sync(0xffffffffu, f);
+    if (lane == 0) warp_cnt[warp] = __popc(bal);
     __syncthreads();
-    const int n_all = n_all_sh;
-    const int t0 = rank * n_all / kSplitCL, n = (rank + 1) * n_all / kSplitCL - t0;
-    const int acc_cols = part == 0 ? PartShape<0>::ACC_COLS : PartShape<1>::ACC_COLS;
+    int before = 0, total = 0;
+    for (int w = 0; w < nwarps; ++w) {
+      const int c = warp_cnt[w];
+      before += w < warp ? c : 0;
+      total += c;
+    }
+    const int at = base + before + __popc(bal & ((1u << lane) - 1u));
+    if (f && at == want) found_sh = i;
+    if (want < 0 && f && at < kListed) listed_sh[at] = i;  // the counting pass
+    __syncthreads();  // warp_cnt is rewritten by the next window
+    return total;
+  };
+  if (threadIdx.x == 0) min_tiles_sh = 0x7fffffff;
+  __syncthreads();
+  int nflag = 0;
+  for (int c0 = 0; c0 < nitems; c0 += blockDim.x) nflag += window(c0, nflag, -1);
+  // C: the fewest rounds of the clusters, each item costing its tiles plus a
+  // fixed kItemTiles (key tile, pipeline fill and drain, the partials'
+  // exchange), no piece of the smallest flagged block below kMinPieceTiles
+  // tiles and at most kMlaSplitSlots open chunk partials
+  int C = 1;
+  if (nflag > 0) {
+    const int cmax = max(1, min(kMlaSplitSlots / nflag, min_tiles_sh / (kSplitCL * kMinPieceTiles)));
+    int64_t best = -1;
+    for (int c = 1; c <= cmax; ++c) {
+      const int64_t rounds = (static_cast<int64_t>(nflag) * c + ncl - 1) / ncl;
+      const int64_t cost = rounds * ((min_tiles_sh + kSplitCL * c - 1) / (kSplitCL * c) + kItemTiles);
+      if (best < 0 || cost < best) {
+        best = cost;
+        C = c;
+      }
+    }
+  }
+  const int n_work = nflag * C;
+  // the u-th flagged block: listed when u < kListed (always when C > 1),
+  // else searched from where the last search ended (with C = 1 a cluster's
+  // items, and so its u, increase)
+  int scan_c0 = 0, scan_base = 0;
+
+  auto run_item = [&](int u, int c) {
+    int item = u < kListed ? listed_sh[u] : -1;
+    while (item < 0 && scan_c0 < nitems) {  // uniform: every thread sees the same windows
+      const int total = window(scan_c0, scan_base, u);
+      if (u < scan_base + total) {
+        item = found_sh;
+      } else {
+        scan_base += total;
+        scan_c0 += blockDim.x;
+      }
+    }
+    if (item < 0) return;  // not reached: u < nflag
+    const int g = item % p.KVH, rest = item / p.KVH, tb = rest % nblk, s0 = rest / nblk;
+    __syncthreads();  // found_sh is read; the previous item's readers of pinfo are done
+    if (threadIdx.x == 0) fill_page_info(p, s0, tb, pages_of(seq_len_of(p, s0), p.page_size), &pinfo);
+    __syncthreads();
+    const int64_t n_all = p.heavy[item], pieces = static_cast<int64_t>(kSplitCL) * C, q = static_cast<int64_t>(c) * kSplitCL + rank;
+    const int t0 = static_cast<int>(q * n_all / pieces), n = static_cast<int>((q + 1) * n_all / pieces) - t0;
     // (a wait that gives up sets the abort flag, which the cluster reads below)
-    if (n > 0 && part == 0)
-      run_block<0>(&tm_q, &tm_qp, &tm_dy, &tm_k, &tm_kp, p, bars, sm, tmem, pinfo, s0, tb, g, t0, n, ep, ab);
-    else if (n > 0)
-      run_block<1>(&tm_q, &tm_qp, &tm_dy, &tm_k, &tm_kp, p, bars, sm, tmem, pinfo, s0, tb, g, t0, n, ep, ab);
+    if (n > 0) run_block<PART>(&tm_q, &tm_qp, &tm_dy, &tm_k, &tm_kp, p, bars, sm, tmem, pinfo, s0, tb, g, t0, n, ep, ab);
     // every role is done with the pipeline's shared memory and the
     // accumulator is complete: stage the partial (zeros without tiles)
     __syncthreads();
@@ -760,12 +896,24 @@ __global__ void __launch_bounds__(384, 1)
     }
     __syncthreads();
     const bool good = !abort_flag;
-    // tokens [16 rank, 16 rank + 16): the partials of CTAs 0..kSplitCL-1
-    // added in that order; one page per CTA
+    // tokens [16 rank, 16 rank + 16), one page: the partials of CTAs
+    // 0..kSplitCL-1 added in that order
     constexpr int kRows = BT / kSplitCL;
-    const int quads = acc_cols / 4;
+    constexpr int quads = acc_cols / 4;
     const int j = (kRows * rank) >> 4;
-    if (good && pinfo.store[j]) {
+    auto store4 = [&](int i, int d, float4 sum) {
+      const int64_t prow = (static_cast<int64_t>(pinfo.phys[j]) * p.page_size + (i & 15)) * p.KVH + g;
+      const uint2 w = make_uint2(pack_bf16x2(sum.x, sum.y), pack_bf16x2(sum.z, sum.w));
+      if (d < 256) {
+        if (p.wrt & 2u)
+          *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.dk_pool) + prow * kLat + 256 * PART + d) = w;
+      } else if (p.wrt & 8u) {
+        *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.dkp_pool) + prow * kPos + (d - 256)) = w;
+      }
+    };
+    const bool mine = good && pinfo.store[j] != 0;
+    float* slot = C > 1 ? slots + (static_cast<size_t>(u) * C + c) * BT * acc_cols : nullptr;
+    if (mine) {
       for (int idx = threadIdx.x; idx < kRows * quads; idx += blockDim.x) {
         const int i = kRows * rank + idx / quads, d = 4 * (idx % quads);
         const uint32_t a = smem_addr(red + i * RED_STRIDE + d);
@@ -778,48 +926,61 @@ __global__ void __launch_bounds__(384, 1)
           sum.z += v.z;
           sum.w += v.w;
         }
-        const int64_t prow = (static_cast<int64_t>(pinfo.phys[j]) * p.page_size + (i & 15)) * p.KVH + g;
-        const uint2 w = make_uint2(pack_bf16x2(sum.x, sum.y), pack_bf16x2(sum.z, sum.w));
-        if (d < 256) {
-          if (p.wrt & 2u)
-            *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.dk_pool) + prow * kLat + 256 * part + d) = w;
-        } else if (p.wrt & 8u) {
-          *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.dkp_pool) + prow * kPos + (d - 256)) = w;
-        }
+        if (C == 1)
+          store4(i, d, sum);
+        else
+          *reinterpret_cast<float4*>(slot + i * acc_cols + d) = sum;
       }
+      if (C > 1) __threadfence();  // the slot rows, before this CTA's count below
     }
     cluster_sync();  // the other CTAs have read this CTA's partial
     if (n > 0) {
       ep.T += n;
-      ep.Q += n * (part == 0 ? jobs_per_tile<0>() : jobs_per_tile<1>());
+      ep.Q += n * jobs_per_tile<PART>();
       ++ep.B;
+    }
+    if (C > 1 && mine) {
+      // the last of the block's C chunks to reach this rank adds the slots
+      if (threadIdx.x == 0) {
+        last_sh = atomicAdd(done + u * kMlaSplitRanks + rank, 1) == C - 1;
+        __threadfence();
+      }
+      __syncthreads();
+      if (last_sh) {
+        const float* first = slots + static_cast<size_t>(u) * C * BT * acc_cols;
+        for (int idx = threadIdx.x; idx < kRows * quads; idx += blockDim.x) {
+          const int i = kRows * rank + idx / quads, d = 4 * (idx % quads);
+          const float* src = first + i * acc_cols + d;
+          float4 sum = __ldcg(reinterpret_cast<const float4*>(src));
+#pragma unroll 4
+          for (int c2 = 1; c2 < C; ++c2) {
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(src + static_cast<size_t>(c2) * BT * acc_cols));
+            sum.x += v.x;
+            sum.y += v.y;
+            sum.z += v.z;
+            sum.w += v.w;
+          }
+          store4(i, d, sum);
+        }
+      }
     }
   };
 
-  // the flagged blocks in flag order; units 2k (PART 0) and 2k + 1 (PART 1)
-  // of flagged block k, unit u to cluster u mod clusters
-  const int nitems = p.S * nblk * p.KVH;
-  int base = 0;
-  for (int c0 = 0; c0 < nitems; c0 += blockDim.x) {
-    const int i = c0 + threadIdx.x;
-    const bool f = i < nitems && p.heavy[i] != 0;
-    const uint32_t bal = __ballot_sync(0xffffffffu, f);
-    if (lane == 0) warp_cnt[warp] = __popc(bal);
+  while (true) {
+    // rank 0 takes the cluster's next item; the others read it from rank 0
+    // (its next write comes after the item's cluster barriers)
+    if (rank == 0 && threadIdx.x == 0) item_sh = atomicAdd(p.work + 2 + PART, 1);
+    cluster_sync();
+    if (threadIdx.x == 0) k_sh = ld_cluster_s32(map_rank(smem_addr(&item_sh), 0));
     __syncthreads();
-    int before = 0, total = 0;
-    for (int w = 0; w < static_cast<int>(blockDim.x / 32); ++w) {
-      const int c = warp_cnt[w];
-      before += w < warp ? c : 0;
-      total += c;
-    }
-    const int k = base + before + __popc(bal & ((1u << lane) - 1u));
-    if (f) items_sh[k - base] = i;
-    __syncthreads();
-    for (int u = 2 * base; u < 2 * (base + total); ++u)
-      if (u % ncl == cid) run_unit(items_sh[u / 2 - base], u & 1);
-    base += total;
-    __syncthreads();  // items_sh and warp_cnt are rewritten next
+    const int k = k_sh;
+    if (k >= n_work) break;  // cluster-uniform
+    // chunk-major: the clusters running at one time work on the same chunk
+    // of different blocks, whose passes read the same query rows (L2 reuse)
+    run_item(k % nflag, k / nflag);
   }
+  cluster_sync();  // rank 0's shared memory outlives the others' last read of it
+  if (PART == 1 && blockIdx.x == gridDim.x - 1) asm volatile("griddepcontrol.wait;" ::: "memory");
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -829,18 +990,72 @@ __global__ void __launch_bounds__(384, 1)
 }
 
 template <int PART>
-cudaError_t launch_part(const PagedMlaMaps& m, const PagedParams& p, bool dependent, cudaStream_t s) {
+cudaError_t launch_split(const PagedMlaMaps& m, const PagedParams& p, int ncl, bool dependent, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(mla_tc_split_kernel<PART>, cudaFuncAttributeMaxDynamicSharedMemorySize, BYTES + 1024);
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = kSplitCL;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[1].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(ncl * kSplitCL, 1, 1);
+  cfg.blockDim = dim3(384, 1, 1);
+  cfg.dynamicSmemBytes = BYTES + 1024;
+  cfg.stream = s;
+  cfg.attrs = at;
+  cfg.numAttrs = dependent ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, mla_tc_split_kernel<PART>, m.q, m.qp, m.dy, m.k, m.kp, p);
+}
+
+// How many kSplitCL-CTA clusters of the split kernel fit the GPU at once (one
+// CTA per SM), cached per device (host threads may race to fill an entry:
+// they store the same value).
+cudaError_t split_clusters(int* ncl) {
+  static std::atomic<int> cached[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  *ncl = dev < 64 ? cached[dev].load(std::memory_order_relaxed) : 0;
+  if (*ncl > 0) return cudaSuccess;
+  const int smem = BYTES + 1024;
+  if ((e = cudaFuncSetAttribute(mla_tc_split_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess ||
+      (e = cudaFuncSetAttribute(mla_tc_split_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
+    return e;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = kSplitCL;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kSplitCL, 1, 1);
+  cfg.blockDim = dim3(384, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  if ((e = cudaOccupancyMaxActiveClusters(ncl, mla_tc_split_kernel<1>, &cfg)) != cudaSuccess) return e;
+  if (*ncl < 1) return cudaErrorInvalidConfiguration;
+  if (dev < 64) cached[dev].store(*ncl, std::memory_order_relaxed);
+  return cudaSuccess;
+}
+
+template <int PART>
+cudaError_t launch_grid(const PagedMlaMaps& m, const PagedParams& p, bool dependent, cudaStream_t s) {
   auto kern = mla_tc_kernel<PART>;
   const int smem = BYTES + 1024;
   static_assert(BYTES + 1024 >= kSmemOneCtaPerSm, "all 512 TMEM columns: one CTA per SM");
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  const int nblk = (p.max_pages * p.page_size + BT - 1) / BT;
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.KVH, nblk, p.S);
+  cfg.gridDim = dim3(sms > 0 ? sms : 1, 1, 1);
   cfg.blockDim = dim3(384, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
@@ -858,50 +1073,32 @@ bool mla_tc_supported(const PagedParams& p) {
 cudaError_t launch_paged_mla_tc_plan(const PagedParams& p, cudaStream_t s) {
   const int64_t n = static_cast<int64_t>(p.S) * ((p.max_pages + 7) / 8);
   if (n == 0 || p.num_pages == 0) return cudaSuccess;
-  const int blocks = static_cast<int>((n + 127) / 128 < 1024 ? (n + 127) / 128 : 1024);
+  const int blocks = static_cast<int>((n + 3) / 4 < 2048 ? (n + 3) / 4 : 2048);  // a warp per block
   mla_tc_plan_kernel<<<blocks, 128, 0, s>>>(p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_paged_mla_tc_split(const PagedMlaMaps& m, const PagedParams& p, cudaStream_t s) {
   if (p.num_pages == 0 || p.S == 0 || p.max_pages == 0) return cudaSuccess;
-  const int smem = BYTES + 1024;
-  auto kern = mla_tc_split_kernel;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  // the clusters that fit are shared between the parts (part 1, the larger
+  // accumulator, gets the odd one), and part 1 is the programmatic dependent
+  // of part 0, so that both run at once and the grid kernels after them
+  // start on the SMs the clusters leave free
+  int ncl = 0;
+  cudaError_t e = split_clusters(&ncl);
   if (e != cudaSuccess) return e;
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = kSplitCL;
-  at[0].val.clusterDim.y = 1;
-  at[0].val.clusterDim.z = 1;
-  cudaLaunchConfig_t cfg = {};
-  cfg.blockDim = dim3(384, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cfg.attrs = at;
-  cfg.numAttrs = 1;
-  // as many clusters as fit the GPU at once (one CTA per SM), cached per
-  // device (host threads may race to fill an entry: they store the same value)
-  static std::atomic<int> clusters[64];
-  int dev = 0;
-  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-  int ncl = dev < 64 ? clusters[dev].load(std::memory_order_relaxed) : 0;
-  if (ncl == 0) {
-    cfg.gridDim = dim3(kSplitCL, 1, 1);
-    if ((e = cudaOccupancyMaxActiveClusters(&ncl, kern, &cfg)) != cudaSuccess) return e;
-    if (ncl < 1) return cudaErrorInvalidConfiguration;
-    if (dev < 64) clusters[dev].store(ncl, std::memory_order_relaxed);
-  }
-  cfg.gridDim = dim3(ncl * kSplitCL, 1, 1);
-  return cudaLaunchKernelEx(&cfg, kern, m.q, m.qp, m.dy, m.k, m.kp, p);
+  const int ncl0 = ncl > 1 ? ncl / 2 : 1, ncl1 = ncl > 1 ? ncl - ncl0 : 1;
+  e = launch_split<0>(m, p, ncl0, false, s);
+  if (e == cudaSuccess) e = launch_split<1>(m, p, ncl1, true, s);
+  return e;
 }
 
 cudaError_t launch_paged_mla_tc(const PagedMlaMaps& m, const PagedParams& p, bool after_split, cudaStream_t s) {
   if (p.num_pages == 0 || p.S == 0 || p.max_pages == 0) return cudaSuccess;
-  // PART 0 overlaps the cluster-split kernel's tail (when that kernel runs
-  // just before it), PART 1 overlaps PART 0's tail
-  cudaError_t e = launch_part<0>(m, p, after_split, s);
-  if (e == cudaSuccess) e = launch_part<1>(m, p, true, s);
+  // part 0 overlaps the cluster-split kernel's tail (when that kernel runs
+  // just before it), part 1 overlaps part 0's tail
+  cudaError_t e = launch_grid<0>(m, p, after_split, s);
+  if (e == cudaSuccess) e = launch_grid<1>(m, p, true, s);
   return e;
 }
 

@@ -25,7 +25,7 @@
  * Paged (ruDNN src/paged_attention/ordered_kernel.rs, fn history_backward):
  * the same backward for packed query rows against a KV history stored in
  * pages of a pool, producing dK, dV (GQA) or dK_latent, dKp (MLA) for every
- * pool row with no atomics and a fixed summation order.
+ * pool row with no floating-point atomics and a fixed summation order.
  *
  * Conventions for every entry point:
  *   - All tensor pointers are DEVICE pointers on the current CUDA device,
@@ -235,7 +235,9 @@ typedef struct attn_paged_desc {
   int32_t reserved;          /* must be 0 */
 } attn_paged_desc;
 
-/* Bytes of workspace attn_bwd_paged / attn_paged_row_stats need. */
+/* Bytes of workspace attn_bwd_paged / attn_paged_row_stats need (the link
+ * structure of the pool and counters; for MLA also 36 MiB of fp32 partial
+ * sums of the shared-page blocks that are cut into chunks). */
 ATTN_API size_t attn_bwd_paged_workspace_bytes(const attn_paged_desc* d);
 
 /*
@@ -251,7 +253,8 @@ ATTN_API size_t attn_bwd_paged_workspace_bytes(const attn_paged_desc* d);
  *   valid token (unreferenced pages, tail slots past a sequence's length) get
  *   zero, so no clearing pass is needed.  wrt_mask selects among ATTN_WRT_DK,
  *   ATTN_WRT_DV (GQA) and ATTN_WRT_DKP (MLA).
- * The result is bit-identical from run to run (no atomics; fixed order).
+ * The result is bit-identical from run to run: no floating-point atomics,
+ * every sum in a fixed order (integer counters only hand out work).
  */
 ATTN_API attn_status_t attn_bwd_paged(const attn_paged_desc* d, const void* q, const void* qp, const void* k_pool,
                                       const void* v_pool, const void* kp_pool, const void* dy,

@@ -196,6 +196,16 @@ def test_paged_compact_checks(lib):
     assert _compact_call(d0, FAKE + 34 * MB, 5) == bd.ATTN_OK
 
 
+def test_paged_mla_workspace_holds_split_partials(lib):
+    """MLA: the workspace also holds the split kernel's fp32 chunk partials
+    (128 slots of 128 tokens x (256 + 320) dims) next to the GQA layout."""
+    kw = dict(num_queries=64, num_seqs=4, heads=8, kv_heads=1, page_size=16, num_pages=100, max_pages_per_seq=10,
+              key_dim=512, value_dim=512)
+    mla = bd.attn_bwd_paged_workspace_bytes(bd.make_paged_desc(position_dim=64, **kw))
+    gqa_layout = bd.attn_bwd_paged_workspace_bytes(bd.make_paged_desc(**dict(kw, key_dim=128, value_dim=128)))
+    assert mla == gqa_layout + 128 * 128 * (256 + 320) * 4
+
+
 def test_paged_query_side_needs_workspace(lib):
     """The row-statistics and query-side calls keep their dispatch order (the
     sequences by length) in the paged workspace: a missing, short or

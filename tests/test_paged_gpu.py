@@ -79,11 +79,17 @@ CASES = [
     dict(seed=29, num_seqs=10, len_lo=150, len_hi=400, queries_per_seq=6, heads=16, kv_heads=1, key_dim=512,
          value_dim=512, position_dim=64, causal=True, shared_prefix_pages=9),
     # MLA blocks whose shared pages carry more than 64 link tiles go to the
-    # cluster-split kernel: 11 other sequences x 12 (resp. 6) tiles each
+    # cluster-split kernel: 11 other sequences x 12 (resp. 6) tiles each; few
+    # such blocks, so each is cut into chunks summed through the workspace
     dict(seed=30, num_seqs=12, len_lo=150, len_hi=300, queries_per_seq=24, heads=32, kv_heads=1, key_dim=512,
          value_dim=512, position_dim=64, causal=True, shared_prefix_pages=9),
     dict(seed=32, num_seqs=12, len_lo=150, len_hi=300, queries_per_seq=24, heads=32, kv_heads=2, key_dim=512,
          value_dim=512, position_dim=64, causal=False, shared_prefix_pages=5),
+    # 64 flagged (block, KV head) units (8 blocks of a 64-page prefix shared by
+    # 40 sequences, 8 KV heads, 39 x 2 link tiles each): enough units that the
+    # split kernel takes them whole instead of cutting them into chunks
+    dict(seed=34, num_seqs=40, len_lo=1030, len_hi=1100, queries_per_seq=32, heads=32, kv_heads=8, key_dim=512,
+         value_dim=512, position_dim=64, causal=True, shared_prefix_pages=64),
 ]
 
 
@@ -147,8 +153,8 @@ def test_paged_shared_at_offsets(bd, mla):
 
 
 def test_paged_mla_split_bit_stable(bd):
-    """The cluster-split MLA blocks (8-CTA clusters on tcgen05) sum their
-    partials in a fixed order."""
+    """The cluster-split MLA blocks (8-CTA clusters on tcgen05, each block
+    cut into chunks) sum their partials in a fixed order."""
     c = inputs.paged_case(name="t", seed=33, num_seqs=12, len_lo=150, len_hi=300, queries_per_seq=24, heads=32,
                           kv_heads=1, key_dim=512, value_dim=512, position_dim=64, scale=0.5, shared_prefix_pages=6)
     dv = to_dev(c, bd)
