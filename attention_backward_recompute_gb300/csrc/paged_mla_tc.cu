@@ -13,10 +13,11 @@
 // As tile products: a CTA owns 128 tokens (eight pages) of one sequence and
 // one KV head; a column is one (query row, head of the group) pair and a tile
 // is 64 columns (64/G rows).  Per tile:
-//   S^T  = K_lat Q^T + K_pos Qp^T     [128 x 64], 9 chunks of 64 dims
-//   dP^T = K_lat dY^T                 [128 x 64], 8 chunks
+//   [S^T | dP^T] = K_lat [Q | dY]^T   [128 x 128], 8 chunks of 64 dims
+//   S^T += K_pos Qp^T                 [128 x 64], 1 chunk
 //   P^T  = exp2(S^T scale log2e - lse log2e),  dS^T = P^T (dP^T - delta) scale
-//   acc  += P^T dY[:, part] + dS^T Q[:, part]   (A operands from tensor memory)
+//   acc  += P^T dY[:, part] + dS^T Q[:, part]   (A operands from tensor
+//                                                memory, chunk pairs: N = 128)
 // The accumulator of 128 tokens x 576 dims does not fit the 512 tensor-memory
 // columns next to the score tiles, so the dims are split over two CTAs
 // (PART 0: latent dims [0, 256); PART 1: latent dims [256, 512) and the 64
@@ -37,16 +38,18 @@
 // Shared memory: the K tile stays resident (latent + position, 9 chunks of
 // [128 tokens x 64 dims], 144 KiB); Q, Qp and dY arrive as a stream of 8 KiB
 // chunks ([64 columns x 64 dims]) through a 4-stage TMA ring of two chunk
-// slots each (one wait and one release per pair of chunks), in the order
-//   S chunks of tile t, the part's accumulation chunks of tile t - 1, dP
-//   chunks of tile t
-// so the tensor core forms the scores of tile t while the compute warps turn
-// tile t - 1 into P and dS.  The score tile is double-buffered in tensor
-// memory, the dP tile single-buffered: dP(t) overwrites dS(t - 1) after the
-// accumulation of tile t - 1 has read it.  Roles (384 threads): warp 0 TMA producer (also
-// writes each tile's column statistics), warp 1 MMA issuer (whole warp,
-// elect.sync), warps 4..7 / 8..11 compute groups for even / odd tiles (one
-// TMEM lane per token).
+// slots each, in the order
+//   (Q, dY) pairs of latent chunk c = 0..7 and Qp of tile t (the pair is the
+//   B operand [Q | dY]^T of one N = 128 product), then the part's
+//   accumulation chunk pairs of tile t - 1
+// Tensor memory: the accumulator, one [S^T | dP^T] tile, and P^T, dS^T as
+// bf16 pairs.  The compute warps load [S^T | dP^T](t) and release it at
+// once, so the tensor core forms [S|dP](t + 1) while they turn tile t into
+// P^T and dS^T, which the accumulation of tile t then reads.  Roles (384
+// threads): warp 0 TMA producer (also writes each tile's column statistics),
+// warp 1 MMA issuer (whole warp, elect.sync), warps 4..11 compute (every
+// tile: warps 4..7 its columns [0, 32), warps 8..11 [32, 64); one TMEM lane
+// per token).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -76,8 +79,11 @@ constexpr int ST_OFF = RING_OFF + kStages * STAGE;
 constexpr int ST_SLOT = 3 * BC * 4 + 16;  // -L2, delta, pos per column + pass info
 constexpr int BYTES = ST_OFF + kStatSlots * ST_SLOT;
 static_assert(RING_OFF % 1024 == 0 && QCH % 1024 == 0, "swizzled tiles need 1024-byte alignment");
-// TMEM: accumulator [0, 320) (PART 0 uses [0, 256)), S^T[2] and dP^T 64 columns each
-constexpr int T_ACC = 0, T_S = 320, T_DP = 448, TMEM_COLS = 512;
+// TMEM: accumulator [0, 320) (PART 0 uses [0, 256)); [S^T | dP^T] of the
+// current tile [320, 448) (one N = 128 product per key chunk); P^T and dS^T
+// as bf16 pairs [448, 480) and [480, 512), the A operands of the
+// accumulation
+constexpr int T_ACC = 0, T_SDP = 320, T_P = 448, T_DS = 480, TMEM_COLS = 512;
 
 template <int PART>
 struct PartShape {
@@ -104,8 +110,8 @@ __device__ __forceinline__ int acc_src_chunk(int a) {
 // The barriers of the block pipeline: one set per CTA, reused block after
 // block by a persistent CTA.
 struct TcBars {
-  uint64_t k, full[kStages], empty[kStages], st_full[kStatSlots], st_empty[kStatSlots], s_full[2], p_full[2],
-      dp_full, ds_full, acc;
+  uint64_t k, full[kStages], empty[kStages], st_full[kStatSlots], st_empty[kStatSlots], sdp_full, sdp_free,
+      pds_full, pds_free, acc;
 };
 
 __device__ __forceinline__ void tc_bars_init(TcBars& b) {
@@ -116,14 +122,12 @@ __device__ __forceinline__ void tc_bars_init(TcBars& b) {
   }
   for (int s = 0; s < kStatSlots; ++s) {
     mbar_init(&b.st_full[s], 1);
-    mbar_init(&b.st_empty[s], 4);
+    mbar_init(&b.st_empty[s], 8);  // the eight compute warps
   }
-  for (int s = 0; s < 2; ++s) {
-    mbar_init(&b.s_full[s], 1);
-    mbar_init(&b.p_full[s], 4);
-  }
-  mbar_init(&b.dp_full, 1);
-  mbar_init(&b.ds_full, 4);
+  mbar_init(&b.sdp_full, 1);  // tensor-core commit
+  mbar_init(&b.sdp_free, 8);  // every compute warp has read [S^T | dP^T]
+  mbar_init(&b.pds_full, 8);  // every compute warp has written P^T, dS^T
+  mbar_init(&b.pds_free, 1);  // tensor-core commit: the accumulation read them
   mbar_init(&b.acc, 1);
   mbar_fence_init();
 }
@@ -158,6 +162,15 @@ __device__ __forceinline__ bool pass_seek(PassIter& it, int rt, int t) {
 // contribution overwrites).  Every role of the CTA calls it; when the
 // compute warps return, the accumulator is complete.  Returns false (warp-
 // uniformly) when a wait ran out or the CTA is aborting.
+//
+// Per tile the tensor core forms [S^T | dP^T] = K_c [Q_c | dY_c]^T over the
+// eight latent key chunks c (one N = 128 product each: the ring stage holds
+// the Q chunk and the dY chunk of the same dims back to back) plus
+// K_pos Qp^T into the S^T half, then, once the compute warps have written
+// P^T and dS^T, the accumulation in N = 128 products over chunk pairs.  The
+// compute warps release [S^T | dP^T] as soon as they have loaded it, so the
+// products of tile t + 1 run while they turn tile t into P^T and dS^T: the
+// tensor core sees [S|dP](t + 1), acc(t), [S|dP](t + 2), acc(t + 1), ...
 template <int PART>
 __device__ __forceinline__ bool run_block(const CUtensorMap* tm_q, const CUtensorMap* tm_qp, const CUtensorMap* tm_dy,
                                           const CUtensorMap* tm_k, const CUtensorMap* tm_kp, const PagedParams& p,
@@ -208,18 +221,15 @@ __device__ __forceinline__ bool run_block(const CUtensorMap* tm_q, const CUtenso
       f_info[3] = seq_len_of(p, x.seq);
     };
     fetch(it);
-    // one job into the ring: chunks c and c + 1 (nch = 2) or c alone of Q
-    // (src 0; chunk 8 is Qp) or dY (src 2)
-    auto load_job = [&](int src, int c, int nch, int row0) -> bool {
+    // one job into the ring: chunk (m0, dims x0) into the stage's first slot
+    // and, when m1 is not null, chunk (m1, dims x1) into its second
+    auto load_job = [&](const CUtensorMap* m0, int x0, const CUtensorMap* m1, int x1, int row0) -> bool {
       const int s = q % kStages;
       if (q >= kStages && !mbar_wait(&b.empty[s], ((q / kStages) - 1) & 1, ab)) return false;
       if (lane == 0) {
-        mbar_arrive_expect_tx(&b.full[s], nch * QCH);
-        for (int k = 0; k < nch; ++k) {
-          const int cc = c + k;
-          const CUtensorMap* m = src == 2 ? tm_dy : cc == 8 ? tm_qp : tm_q;
-          tma_load_3d(sm + RING_OFF + s * STAGE + k * QCH, m, &b.full[s], cc == 8 ? 0 : cc * 64, g * p.G, row0);
-        }
+        mbar_arrive_expect_tx(&b.full[s], (m1 ? 2 : 1) * QCH);
+        tma_load_3d(sm + RING_OFF + s * STAGE, m0, &b.full[s], x0, g * p.G, row0);
+        if (m1) tma_load_3d(sm + RING_OFF + s * STAGE + QCH, m1, &b.full[s], x1, g * p.G, row0);
       }
       last_use[s] = q;
       ++q;
@@ -228,8 +238,12 @@ __device__ __forceinline__ bool run_block(const CUtensorMap* tm_q, const CUtenso
     // the accumulation jobs of a tile: dY chunks of the part in pairs, then
     // its Q chunks in pairs (and Qp alone, PART 1)
     auto load_acc = [&](int row0) -> bool {
-      for (int a = 0; a < PS::NACC; a += 2)
-        if (!load_job(a < 4 ? 2 : 0, acc_src_chunk<PART>(a), PS::NACC - a >= 2 ? 2 : 1, row0)) return false;
+      for (int a = 0; a < PS::NACC; a += 2) {
+        const int c = acc_src_chunk<PART>(a);
+        const CUtensorMap* m = a < 4 ? tm_dy : c == 8 ? tm_qp : tm_q;
+        const bool pair = PS::NACC - a >= 2;
+        if (!load_job(m, c == 8 ? 0 : c * 64, pair ? m : nullptr, (c + 1) * 64, row0)) return false;
+      }
       return true;
     };
     for (int t = 0; t <= n && ok; ++t) {
@@ -265,11 +279,11 @@ __device__ __forceinline__ bool run_block(const CUtensorMap* tm_q, const CUtenso
           nx.advance(RT);
           fetch(nx);
         }
-        // S chunks of tile t (Q latent 0..7, Qp), the accumulation chunks of
-        // tile t - 1, then the dP chunks of tile t (dY 0..7)
-        for (int c = 0; c < 9 && ok; c += 2) ok = load_job(0, c, c < 8 ? 2 : 1, row0);
+        // [S | dP] chunks of tile t: (Q, dY) latent chunk pairs, then Qp
+        for (int c = 0; c < 8 && ok; ++c) ok = load_job(tm_q, c * 64, tm_dy, c * 64, row0);
+        if (ok) ok = load_job(tm_qp, 0, nullptr, 0, row0);
+        // the accumulation chunks of tile t - 1
         if (t >= 1 && ok) ok = load_acc(prev_row0);
-        for (int c = 0; c < 8 && ok; c += 2) ok = load_job(2, c, 2, row0);
         if (!ok) break;
         prev_row0 = row0;
         it = nx;
@@ -286,11 +300,13 @@ __device__ __forceinline__ bool run_block(const CUtensorMap* tm_q, const CUtenso
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     // the whole warp runs this role (warp-uniform); elected lanes issue
-    constexpr uint32_t id_s = idesc_bf16(128, BC, false, false);   // S^T, dP^T: K-major A and B
-    constexpr uint32_t id_acc = idesc_bf16(128, 64, false, true);  // acc: A from TMEM, B MN-major
+    constexpr uint32_t id_sdp = idesc_bf16(128, 2 * BC, false, false);  // [S^T | dP^T]: K-major A and B
+    constexpr uint32_t id_s = idesc_bf16(128, BC, false, false);        // S^T += K_pos Qp^T
+    constexpr uint32_t id_acc2 = idesc_bf16(128, 128, false, true);     // acc, a chunk pair: A from TMEM, B MN-major
+    constexpr uint32_t id_acc1 = idesc_bf16(128, 64, false, true);      // acc, one chunk (Qp)
     const uint64_t dK0 = sdesc_sw128(smem_addr(sm + K_OFF), 16, 1024);
-    const uint64_t dR0 = sdesc_sw128(smem_addr(sm + RING_OFF), 16, 1024);            // K-major
-    const uint64_t dRm0 = sdesc_sw128(smem_addr(sm + RING_OFF), BC * 128, 1024);     // MN-major
+    const uint64_t dR0 = sdesc_sw128(smem_addr(sm + RING_OFF), 16, 1024);         // K-major, 128 rows per stage
+    const uint64_t dRm0 = sdesc_sw128(smem_addr(sm + RING_OFF), QCH, 1024);       // MN-major, chunks QCH apart
     bool ok = mbar_wait_warp(&b.k, ep.B & 1, ab);
     int q = ep.Q;
     // a stage's copies are usually in by the time this warp reaches it: a
@@ -303,82 +319,73 @@ __device__ __forceinline__ bool run_block(const CUtensorMap* tm_q, const CUtenso
     // after the job of ring index qq: its stage goes back to the producer
     // once its products are done
     auto release = [&](int qq) { mma_commit_w(&b.empty[qq % kStages]); };
-    // S^T(t) (kind 0, 9 chunks) or dP^T(t) (kind 1, 8 chunks) into tensor
-    // memory, two chunks per job
-    auto xt_jobs = [&](int t, int kind) -> bool {
-      const int nc = kind == 0 ? 9 : 8;
-      const int gt = ep.T + t;
-      const uint32_t d = tmem + (kind == 0 ? T_S + (gt & 1) * BC : T_DP);
-      for (int c0 = 0; c0 < nc; c0 += 2, ++q) {
-        if (!wait_stage(q)) return false;
-        tc_fence_after();
-        for (int k = 0; k < 2 && c0 + k < nc; ++k) {
-          const int c = c0 + k;
-          const uint64_t a = sdesc_add(dK0, c * KCH), bq = sdesc_add(dR0, (q % kStages) * STAGE + k * QCH);
-          if (c == 0)
-            mma_ss_w<false>(d, a, bq, id_s);
-          else
-            mma_ss_w<true>(d, a, bq, id_s);
-#pragma unroll
-          for (int kk = 1; kk < 4; ++kk) mma_ss_w<true>(d, sdesc_add(a, kk * 32), sdesc_add(bq, kk * 32), id_s);
-        }
-        release(q);
-      }
-      mma_commit_w(kind == 0 ? &b.s_full[gt & 1] : &b.dp_full);
-      return true;
-    };
     for (int t = 0; t <= n && ok; ++t) {
-      // S^T(t): its buffer's previous tile (t - 2) was accumulated earlier in
-      // this stream
-      if (t < n && !(ok = xt_jobs(t, 0))) break;
-      if (t >= 1) {
-        // accumulation of tile u = t - 1: P^T dY chunks once P^T(u) is in,
-        // then dS^T Q chunks once dS^T(u) is in
-        const int u = t - 1, gu = ep.T + u;
-        if (!(ok = mbar_wait_warp(&b.p_full[gu & 1], (gu >> 1) & 1, ab))) break;
+      if (t < n) {
+        // [S^T | dP^T](t) once the compute warps have loaded tile t - 1's
+        const int gt = ep.T + t;
+        if (gt >= 1 && !(ok = mbar_wait_warp(&b.sdp_free, (gt - 1) & 1, ab))) break;
         tc_fence_after();
-        for (int a0 = 0; a0 < PS::NACC && ok; a0 += 2, ++q) {
-          if (a0 == 4) {
-            if (!(ok = mbar_wait_warp(&b.ds_full, gu & 1, ab))) break;
-            tc_fence_after();
-          }
+        const uint32_t d = tmem + T_SDP;
+        for (int c = 0; c < 9 && ok; ++c, ++q) {
           if (!(ok = wait_stage(q))) break;
           tc_fence_after();
-          for (int k = 0; k < 2 && a0 + k < PS::NACC; ++k) {
-            const int a = a0 + k;
-            const int c = acc_src_chunk<PART>(a);
-            const uint32_t d = tmem + T_ACC + (c - 4 * PART) * 64;  // chunk 8 (position) -> 256
-            const uint32_t at = tmem + (a < 4 ? T_S + (gu & 1) * BC : T_DP);
-            const uint64_t bm = sdesc_add(dRm0, (q % kStages) * STAGE + k * QCH);
-            // the first contribution to an accumulator chunk overwrites it:
-            // P^T dY for latent chunks, dS^T Qp for the position chunk
-            if (u == 0 && (a < 4 || c == 8))
-              mma_ts_w<false>(d, at, bm, id_acc);
-            else
-              mma_ts_w<true>(d, at, bm, id_acc);
+          const uint64_t a = sdesc_add(dK0, c * KCH), bq = sdesc_add(dR0, (q % kStages) * STAGE);
+          const uint32_t id = c < 8 ? id_sdp : id_s;
+          if (c == 0)
+            mma_ss_w<false>(d, a, bq, id);
+          else
+            mma_ss_w<true>(d, a, bq, id);
 #pragma unroll
-            for (int kk = 1; kk < BC / 16; ++kk)
-              mma_ts_w<true>(d, at + kk * 8, sdesc_add(bm, kk * 16 * 128), id_acc);
-          }
+          for (int kk = 1; kk < 4; ++kk) mma_ss_w<true>(d, sdesc_add(a, kk * 32), sdesc_add(bq, kk * 32), id);
           release(q);
         }
         if (!ok) break;
+        mma_commit_w(&b.sdp_full);
       }
-      // dP^T(t) overwrites dS^T(t - 1), whose products were just issued
-      if (t < n && !(ok = xt_jobs(t, 1))) break;
+      if (t >= 1) {
+        // accumulation of tile u = t - 1 once its P^T and dS^T are in: P^T dY
+        // chunk pairs, then dS^T Q chunk pairs (and dS^T Qp, PART 1)
+        const int u = t - 1, gu = ep.T + u;
+        if (!(ok = mbar_wait_warp(&b.pds_full, gu & 1, ab))) break;
+        tc_fence_after();
+        for (int a0 = 0; a0 < PS::NACC && ok; a0 += 2, ++q) {
+          if (!(ok = wait_stage(q))) break;
+          tc_fence_after();
+          const int c = acc_src_chunk<PART>(a0);
+          const uint32_t d = tmem + T_ACC + (c - 4 * PART) * 64;  // chunk 8 (position) -> 256
+          const uint32_t at = tmem + (a0 < 4 ? T_P : T_DS);
+          const uint64_t bm = sdesc_add(dRm0, (q % kStages) * STAGE);
+          const uint32_t id = PS::NACC - a0 >= 2 ? id_acc2 : id_acc1;
+          // the first contribution to an accumulator chunk overwrites it:
+          // P^T dY for latent chunks, dS^T Qp for the position chunk
+          if (u == 0 && (a0 < 4 || c == 8))
+            mma_ts_w<false>(d, at, bm, id);
+          else
+            mma_ts_w<true>(d, at, bm, id);
+#pragma unroll
+          for (int kk = 1; kk < BC / 16; ++kk) mma_ts_w<true>(d, at + kk * 8, sdesc_add(bm, kk * 16 * 128), id);
+          release(q);
+        }
+        if (!ok) break;
+        mma_commit_w(&b.pds_free);
+      }
     }
     mma_commit_w(&b.acc);
     drain_wait(&b.acc, ep.B & 1);
     __syncwarp();
     return ok;
   } else if (warp >= 4) {
-    const int sg = (warp - 4) >> 2;  // compute group: tiles of parity sg
+    // ------------------------------------------------------------ compute
+    // every tile: warps 4..7 take its columns [0, 32), warps 8..11 [32, 64),
+    // one TMEM lane (token) per thread
+    const int sg = (warp - 4) >> 2;
     const int lg = warp & 3;
     const int row = lg * 32 + lane;  // token row inside the block == TMEM lane
     const uint32_t lane_addr = static_cast<uint32_t>(lg * 32) << 16;
+    const int cb = 32 * sg;  // first column of this group
     bool ok = true;
-    for (int t = sg ^ (ep.T & 1); t < n && ok; t += 2) {
-      const int gt = ep.T + t, bb = gt & 1, ss = gt % kStatSlots;
+    for (int t = 0; t < n && ok; ++t) {
+      const int gt = ep.T + t, ss = gt % kStatSlots;
       if (!(ok = mbar_wait_warp(&b.st_full[ss], (gt / kStatSlots) & 1, ab))) break;
       const uint8_t* st = sm + ST_OFF + ss * ST_SLOT;
       const float* snl = reinterpret_cast<const float*>(st);
@@ -387,75 +394,61 @@ __device__ __forceinline__ bool run_block(const CUtensorMap* tm_q, const CUtenso
       const int* sinfo = spos + BC;
       const int tok = sinfo[0] + row;
       const bool tok_ok = row >= sinfo[1] && row < sinfo[2] && tok >= 0 && tok < sinfo[3];
-      if (!(ok = mbar_wait_warp(&b.s_full[bb], (gt >> 1) & 1, ab))) break;
+      if (!(ok = mbar_wait_warp(&b.sdp_full, gt & 1, ab))) break;
       tc_fence_after();
-      // ---------------------------------------------------- S^T -> P^T
-      // two halves of 32 columns: half hf reads S^T columns [32hf, 32hf+32)
-      // and writes P^T (bf16 pairs) to columns [16hf, 16hf+16), which half 0
-      // has already read
-      const uint32_t tS = tmem + T_S + bb * BC + lane_addr;
-      const uint64_t sl2 = f2_pack(p.scale_log2, p.scale_log2);
-      uint32_t pw[32];
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        uint32_t sr[32];
-        tmem_ld32(tS + 32 * hf, sr);
-        tmem_ld_wait();
-#pragma unroll
-        for (int c4 = 0; c4 < 8; ++c4) {
-          const int c0 = 32 * hf + 4 * c4;
-          const float4 nl = *reinterpret_cast<const float4*>(snl + c0);
-          const int4 ps = *reinterpret_cast<const int4*>(spos + c0);
-          float x0, x1, x2, x3;
-          f2_split(f2_fma(f2_pack_u(sr[4 * c4], sr[4 * c4 + 1]), sl2, f2_pack(nl.x, nl.y)), x0, x1);
-          f2_split(f2_fma(f2_pack_u(sr[4 * c4 + 2], sr[4 * c4 + 3]), sl2, f2_pack(nl.z, nl.w)), x2, x3);
-          const float p0 = (tok_ok && tok <= ps.x) ? ex2_approx(x0) : 0.f;
-          const float p1 = (tok_ok && tok <= ps.y) ? ex2_approx(x1) : 0.f;
-          const float p2 = (tok_ok && tok <= ps.z) ? ex2_approx(x2) : 0.f;
-          const float p3 = (tok_ok && tok <= ps.w) ? ex2_approx(x3) : 0.f;
-          pw[16 * hf + 2 * c4] = pack_bf16x2(p0, p1);
-          pw[16 * hf + 2 * c4 + 1] = pack_bf16x2(p2, p3);
-        }
-        tmem_st16(tS + 16 * hf, *reinterpret_cast<const uint32_t(*)[16]>(pw + 16 * hf));
-      }
-      tmem_st_wait();
+      uint32_t sr[32], dr[32];
+      tmem_ld32(tmem + T_SDP + cb + lane_addr, sr);
+      tmem_ld32(tmem + T_SDP + BC + cb + lane_addr, dr);
+      tmem_ld_wait();
+      // [S^T | dP^T] may now take the next tile's products
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&b.p_full[bb]);
+      if (lane == 0) mbar_arrive(&b.sdp_free);
+      // ---------------------------------------------------- S^T -> P^T
+      const uint64_t sl2 = f2_pack(p.scale_log2, p.scale_log2);
+      uint32_t pw[16], dsw[16];
+#pragma unroll
+      for (int c4 = 0; c4 < 8; ++c4) {
+        const int c0 = cb + 4 * c4;
+        const float4 nl = *reinterpret_cast<const float4*>(snl + c0);
+        const int4 ps = *reinterpret_cast<const int4*>(spos + c0);
+        float x0, x1, x2, x3;
+        f2_split(f2_fma(f2_pack_u(sr[4 * c4], sr[4 * c4 + 1]), sl2, f2_pack(nl.x, nl.y)), x0, x1);
+        f2_split(f2_fma(f2_pack_u(sr[4 * c4 + 2], sr[4 * c4 + 3]), sl2, f2_pack(nl.z, nl.w)), x2, x3);
+        const float p0 = (tok_ok && tok <= ps.x) ? ex2_approx(x0) : 0.f;
+        const float p1 = (tok_ok && tok <= ps.y) ? ex2_approx(x1) : 0.f;
+        const float p2 = (tok_ok && tok <= ps.z) ? ex2_approx(x2) : 0.f;
+        const float p3 = (tok_ok && tok <= ps.w) ? ex2_approx(x3) : 0.f;
+        pw[2 * c4] = pack_bf16x2(p0, p1);
+        pw[2 * c4 + 1] = pack_bf16x2(p2, p3);
+      }
       // ---------------------------------------------------- dP^T, P^T -> dS^T
-      // (one dP buffer: its phase gt has completed once this group sees it,
-      // since dP(gt - 1) went into the tensor core before S(gt) did)
-      if (!(ok = mbar_wait_warp(&b.dp_full, gt & 1, ab))) break;
-      tc_fence_after();
-      const uint32_t tDP = tmem + T_DP + lane_addr;
       // a masked entry has P = 0 and takes dS = 0 by select: dP of a tail or
       // unowned slot may be NaN
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        uint32_t dr[32], dsw[16];
-        tmem_ld32(tDP + 32 * hf, dr);
-        tmem_ld_wait();
+      for (int c4 = 0; c4 < 8; ++c4) {
+        const float4 d4 = *reinterpret_cast<const float4*>(sdl + cb + 4 * c4);
+        const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
+        float ds[4];
 #pragma unroll
-        for (int c4 = 0; c4 < 8; ++c4) {
-          const float4 d4 = *reinterpret_cast<const float4*>(sdl + 32 * hf + 4 * c4);
-          const float dv[4] = {d4.x, d4.y, d4.z, d4.w};
-          float ds[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const uint32_t w = pw[16 * hf + 2 * c4 + (e >> 1)];
-            const float pe = __uint_as_float((e & 1) ? (w & 0xffff0000u) : (w << 16));
-            ds[e] = pe != 0.f ? pe * (__uint_as_float(dr[4 * c4 + e]) - dv[e]) * p.scale : 0.f;
-          }
-          dsw[2 * c4] = pack_bf16x2(ds[0], ds[1]);
-          dsw[2 * c4 + 1] = pack_bf16x2(ds[2], ds[3]);
+        for (int e = 0; e < 4; ++e) {
+          const uint32_t w = pw[2 * c4 + (e >> 1)];
+          const float pe = __uint_as_float((e & 1) ? (w & 0xffff0000u) : (w << 16));
+          ds[e] = pe != 0.f ? pe * (__uint_as_float(dr[4 * c4 + e]) - dv[e]) * p.scale : 0.f;
         }
-        tmem_st16(tDP + 16 * hf, dsw);
+        dsw[2 * c4] = pack_bf16x2(ds[0], ds[1]);
+        dsw[2 * c4 + 1] = pack_bf16x2(ds[2], ds[3]);
       }
+      // P^T and dS^T of tile gt - 1 have been read by its accumulation
+      if (gt >= 1 && !(ok = mbar_wait_warp(&b.pds_free, (gt - 1) & 1, ab))) break;
+      tc_fence_after();
+      tmem_st16(tmem + T_P + cb / 2 + lane_addr, pw);
+      tmem_st16(tmem + T_DS + cb / 2 + lane_addr, dsw);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(&b.ds_full);
+        mbar_arrive(&b.pds_full);
         mbar_arrive(&b.st_empty[ss]);
       }
     }
