@@ -13,7 +13,10 @@
 // group); Q, Qp and dY of the tile stay resident in shared memory.  The sweep
 // runs over 128-token blocks of the row's sequence (eight pages gathered by
 // TMA), with the tokens on the tensor-memory lanes:
-//   S^T  = K Q^T, dP^T = K_lat dY^T   [128 tokens x 64 columns]
+//   [S^T | dP^T] = K_lat [Q | dY]^T   [128 tokens x 128], one N = 128
+//                                     product per latent chunk (Q and dY
+//                                     chunks of the same dims resident back
+//                                     to back), S^T += K_pos Qp^T
 //   dS^T = P^T (dP^T - delta) scale   compute warps, bf16 into shared memory
 //   dQ^T += K^T dS^T                  [576 dims x 64 columns], 4.5 blocks of
 //                                     128 dims, A = K chunk pairs (MN-major)
@@ -28,7 +31,8 @@
 // pass on even slots; the position block reads rows 64..127 of its A operand
 // from that slot and stores only rows 0..63).
 // Tensor memory: dQ^T [0, 320) (latent blocks 64 columns each, position block
-// at 256), S^T[2] [320, 448), dP^T [448, 512).
+// at 256), [S^T | dP^T] [320, 448), single-buffered: the compute warps load
+// it and release it at once, so the next block's products overlap their dS.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -48,15 +52,15 @@ constexpr int kStages = 4;
 constexpr int kSlots = 10;              // ring slots per pass
 constexpr int QCH = BC * 128;           // Q / dY chunk [64 columns][64 dims], 8 KiB
 constexpr int KCH = BT * 128;           // K chunk [128 tokens][64 dims], 16 KiB
-constexpr int Q_OFF = 0;                // 9 chunks (8 latent + position)
-constexpr int DY_OFF = Q_OFF + 9 * QCH; // 8 chunks
-constexpr int RING_OFF = DY_OFF + 8 * QCH;
+constexpr int QD_OFF = 0;               // (Q, dY) latent chunk pairs, 16 KiB each
+constexpr int QP_OFF = QD_OFF + 16 * QCH; // the position chunk of Q
+constexpr int RING_OFF = QP_OFF + QCH;
 constexpr int DS_OFF = RING_OFF + kStages * KCH;  // dS^T [128 tokens][64 columns] bf16
 constexpr int ST_OFF = DS_OFF + BT * 128;         // -L2, delta, pos per column
 constexpr int BYTES = ST_OFF + 3 * BC * 4;
-static_assert(9 * QCH >= BC * kDims * 2, "the output tile is staged in the Q slots");
+static_assert(17 * QCH >= BC * kDims * 2, "the output tile is staged in the Q / dY slots");
 static_assert(RING_OFF % 1024 == 0 && DS_OFF % 1024 == 0, "swizzled tiles need 1024-byte alignment");
-constexpr int T_DQ = 0, T_S = 320, T_DP = 448, TMEM_COLS = 512;
+constexpr int T_DQ = 0, T_SDP = 320, TMEM_COLS = 512;
 
 __device__ __forceinline__ bool drain_wait(uint64_t* bar, uint32_t parity) {
   const uint64_t t0 = global_timer_ns();
@@ -72,8 +76,8 @@ __global__ void __launch_bounds__(256, 1)
                         const __grid_constant__ CUtensorMap tm_kp, const PagedParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t bar_qdy, bar_full[kStages], bar_empty[kStages], bar_s_full[2], bar_s_read[2], bar_dp_full,
-      bar_dp_read, bar_ds_ready, bar_ds_free, bar_acc;
+  __shared__ uint64_t bar_qdy, bar_full[kStages], bar_empty[kStages], bar_sdp_full, bar_sdp_read, bar_ds_ready,
+      bar_ds_free, bar_acc;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag, ntok_sh, seq_sh, r0_sh;
 
@@ -103,12 +107,8 @@ __global__ void __launch_bounds__(256, 1)
       mbar_init(&bar_full[s], 1);
       mbar_init(&bar_empty[s], 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&bar_s_full[s], 1);
-      mbar_init(&bar_s_read[s], 4);
-    }
-    mbar_init(&bar_dp_full, 1);
-    mbar_init(&bar_dp_read, 4);
+    mbar_init(&bar_sdp_full, 1);
+    mbar_init(&bar_sdp_read, 4);
     mbar_init(&bar_ds_ready, 4);
     mbar_init(&bar_ds_free, 1);
     mbar_init(&bar_acc, 1);
@@ -148,10 +148,10 @@ __global__ void __launch_bounds__(256, 1)
         tma_prefetch_map(&tm_kp);
         mbar_arrive_expect_tx(&bar_qdy, 17 * QCH);
         for (int c = 0; c < 8; ++c) {
-          tma_load_3d(sm + Q_OFF + c * QCH, &tm_q, &bar_qdy, c * 64, g * G, r0);
-          tma_load_3d(sm + DY_OFF + c * QCH, &tm_dy, &bar_qdy, c * 64, g * G, r0);
+          tma_load_3d(sm + QD_OFF + 2 * c * QCH, &tm_q, &bar_qdy, c * 64, g * G, r0);
+          tma_load_3d(sm + QD_OFF + (2 * c + 1) * QCH, &tm_dy, &bar_qdy, c * 64, g * G, r0);
         }
-        tma_load_3d(sm + Q_OFF + 8 * QCH, &tm_qp, &bar_qdy, 0, g * G, r0);
+        tma_load_3d(sm + QP_OFF, &tm_qp, &bar_qdy, 0, g * G, r0);
       }
       for (int c = lane; c < BC; c += 32) {  // column statistics, two per lane
         const int r = r0 + c / G;
@@ -220,10 +220,11 @@ __global__ void __launch_bounds__(256, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (nb > 0) {
-      constexpr uint32_t id_x = idesc_bf16(128, BC, false, false);  // S^T, dP^T: K-major A and B
-      constexpr uint32_t id_q = idesc_bf16(128, BC, true, true);    // dQ^T: MN-major A and B
-      const uint64_t dQ0 = sdesc_sw128(smem_addr(sm + Q_OFF), 16, 1024);
-      const uint64_t dDY0 = sdesc_sw128(smem_addr(sm + DY_OFF), 16, 1024);
+      constexpr uint32_t id_sdp = idesc_bf16(128, 2 * BC, false, false);  // [S^T | dP^T]: K-major A and B
+      constexpr uint32_t id_s = idesc_bf16(128, BC, false, false);         // S^T += K_pos Qp^T
+      constexpr uint32_t id_q = idesc_bf16(128, BC, true, true);           // dQ^T: MN-major A and B
+      const uint64_t dQD0 = sdesc_sw128(smem_addr(sm + QD_OFF), 16, 1024);  // 128 rows: Q_c then dY_c
+      const uint64_t dQP = sdesc_sw128(smem_addr(sm + QP_OFF), 16, 1024);
       const uint64_t dR0 = sdesc_sw128(smem_addr(sm + RING_OFF), 16, 1024);
       const uint64_t dRm0 = sdesc_sw128(smem_addr(sm + RING_OFF), KCH, 1024);  // MN-major, chunk pairs
       const uint64_t dDS = sdesc_sw128(smem_addr(sm + DS_OFF), 16 * 1024, 1024);  // MN-major
@@ -235,47 +236,31 @@ __global__ void __launch_bounds__(256, 1)
         if (mbar_test_warp(&bar_full[s], (qq / kStages) & 1)) return true;
         return mbar_wait_warp(&bar_full[s], (qq / kStages) & 1, ab);
       };
+      const uint32_t tSDP = tmem + T_SDP;
       for (int b = 0; b <= nb && ok; ++b) {
         if (b < nb) {
-          // ------------------------------------------- S^T(b), dP^T(b)
-          const int bb = b & 1;
-          const uint32_t tS = tmem + T_S + bb * BC;
-          if (b >= 2 && !(ok = mbar_wait_warp(&bar_s_read[bb], ((b - 2) >> 1) & 1, ab))) break;
-          bool dp_free = b == 0;
+          // ------------------------------------------- [S^T | dP^T](b)
+          // once the compute warps have loaded block b - 1's
+          if (b >= 1 && !(ok = mbar_wait_warp(&bar_sdp_read, (b - 1) & 1, ab))) break;
+          tc_fence_after();
           for (int c = 0; c < kSlots && ok; ++c, ++q) {
             if (!(ok = stage_in(q))) break;
             tc_fence_after();
             const uint64_t a = sdesc_add(dR0, (q % kStages) * KCH);
             if (c < 9) {
-              const uint64_t bq = sdesc_add(dQ0, c * QCH);
+              const uint64_t bq = c < 8 ? sdesc_add(dQD0, 2 * c * QCH) : dQP;
+              const uint32_t id = c < 8 ? id_sdp : id_s;
               if (c == 0)
-                mma_ss_w<false>(tS, a, bq, id_x);
+                mma_ss_w<false>(tSDP, a, bq, id);
               else
-                mma_ss_w<true>(tS, a, bq, id_x);
+                mma_ss_w<true>(tSDP, a, bq, id);
 #pragma unroll
-              for (int kk = 1; kk < 4; ++kk) mma_ss_w<true>(tS, sdesc_add(a, kk * 32), sdesc_add(bq, kk * 32), id_x);
-            }
-            if (c < 8) {
-              // dP^T(b) overwrites dP^T(b - 1): wait until its group has read it
-              if (!dp_free) {
-                if (!(ok = mbar_wait_warp(&bar_dp_read, (b - 1) & 1, ab))) break;
-                tc_fence_after();
-                dp_free = true;
-              }
-              const uint64_t bd = sdesc_add(dDY0, c * QCH);
-              if (c == 0)
-                mma_ss_w<false>(tmem + T_DP, a, bd, id_x);
-              else
-                mma_ss_w<true>(tmem + T_DP, a, bd, id_x);
-#pragma unroll
-              for (int kk = 1; kk < 4; ++kk)
-                mma_ss_w<true>(tmem + T_DP, sdesc_add(a, kk * 32), sdesc_add(bd, kk * 32), id_x);
+              for (int kk = 1; kk < 4; ++kk) mma_ss_w<true>(tSDP, sdesc_add(a, kk * 32), sdesc_add(bq, kk * 32), id);
             }
             mma_commit_w(&bar_empty[q % kStages]);
           }
           if (!ok) break;
-          mma_commit_w(&bar_s_full[bb]);
-          mma_commit_w(&bar_dp_full);
+          mma_commit_w(&bar_sdp_full);
         }
         if (b >= 1) {
           // ------------------------------------------- dQ^T += K^T dS^T(b - 1)
@@ -327,57 +312,44 @@ __global__ void __launch_bounds__(256, 1)
     if (nb > 0) ok = mbar_wait_warp(&bar_qdy, 0, ab);
     const uint64_t sl2 = f2_pack(p.scale_log2, p.scale_log2);
     for (int b = 0; b < nb && ok; ++b) {
-      const int bb = b & 1;
-      if (!(ok = mbar_wait_warp(&bar_s_full[bb], (b >> 1) & 1, ab))) break;
-      // the dP commit follows the S commit of the same block
-      if (!(ok = mbar_wait_warp(&bar_dp_full, b & 1, ab))) break;
+      if (!(ok = mbar_wait_warp(&bar_sdp_full, b & 1, ab))) break;
       tc_fence_after();
-      uint32_t dr[64];
-      tmem_ld32(tmem + T_DP + lane_addr, *reinterpret_cast<uint32_t(*)[32]>(dr));
-      tmem_ld32(tmem + T_DP + 32 + lane_addr, *reinterpret_cast<uint32_t(*)[32]>(dr + 32));
+      uint32_t sr[64], dr[64];
+      tmem_ld32(tmem + T_SDP + lane_addr, *reinterpret_cast<uint32_t(*)[32]>(sr));
+      tmem_ld32(tmem + T_SDP + 32 + lane_addr, *reinterpret_cast<uint32_t(*)[32]>(sr + 32));
+      tmem_ld32(tmem + T_SDP + BC + lane_addr, *reinterpret_cast<uint32_t(*)[32]>(dr));
+      tmem_ld32(tmem + T_SDP + BC + 32 + lane_addr, *reinterpret_cast<uint32_t(*)[32]>(dr + 32));
       tmem_ld_wait();
 #pragma unroll
-      for (int i = 0; i < 64; ++i) asm volatile("" : "+r"(dr[i]));
+      for (int i = 0; i < 64; ++i) asm volatile("" : "+r"(sr[i]), "+r"(dr[i]));
+      // [S^T | dP^T] may now take the next block's products
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&bar_dp_read);
+      if (lane == 0) mbar_arrive(&bar_sdp_read);
       const int tok = b * BT + row;
       const bool tok_ok = tok < len;
       uint32_t dsw[32];
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        uint32_t sr[32];
-        tmem_ld32(tmem + T_S + bb * BC + 32 * hf + lane_addr, sr);
-        tmem_ld_wait();
+      for (int c4 = 0; c4 < 16; ++c4) {
+        const int c0 = 4 * c4;
+        const float4 nl = *reinterpret_cast<const float4*>(snl + c0);
+        const float4 dl = *reinterpret_cast<const float4*>(sdl + c0);
+        const int4 ps = *reinterpret_cast<const int4*>(spos + c0);
+        float x[4];
+        f2_split(f2_fma(f2_pack_u(sr[c0], sr[c0 + 1]), sl2, f2_pack(nl.x, nl.y)), x[0], x[1]);
+        f2_split(f2_fma(f2_pack_u(sr[c0 + 2], sr[c0 + 3]), sl2, f2_pack(nl.z, nl.w)), x[2], x[3]);
+        const int pv[4] = {ps.x, ps.y, ps.z, ps.w};
+        const float dv[4] = {dl.x, dl.y, dl.z, dl.w};
+        float ds[4];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) asm volatile("" : "+r"(sr[i]));
-        if (hf == 1) {
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&bar_s_read[bb]);
+        for (int e = 0; e < 4; ++e) {
+          const bool vis = tok_ok && tok <= pv[e];
+          const float pe = ex2_approx(x[e]);
+          // a hidden token's scores may be NaN (tail or unowned slot): select
+          ds[e] = vis ? pe * (__uint_as_float(dr[c0 + e]) - dv[e]) * p.scale : 0.f;
         }
-#pragma unroll
-        for (int c4 = 0; c4 < 8; ++c4) {
-          const int c0 = 32 * hf + 4 * c4;
-          const float4 nl = *reinterpret_cast<const float4*>(snl + c0);
-          const float4 dl = *reinterpret_cast<const float4*>(sdl + c0);
-          const int4 ps = *reinterpret_cast<const int4*>(spos + c0);
-          float x[4];
-          f2_split(f2_fma(f2_pack_u(sr[4 * c4], sr[4 * c4 + 1]), sl2, f2_pack(nl.x, nl.y)), x[0], x[1]);
-          f2_split(f2_fma(f2_pack_u(sr[4 * c4 + 2], sr[4 * c4 + 3]), sl2, f2_pack(nl.z, nl.w)), x[2], x[3]);
-          const int pv[4] = {ps.x, ps.y, ps.z, ps.w};
-          const float dv[4] = {dl.x, dl.y, dl.z, dl.w};
-          float ds[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const bool vis = tok_ok && tok <= pv[e];
-            const float pe = ex2_approx(x[e]);
-            // a hidden token's scores may be NaN (tail or unowned slot): select
-            ds[e] = vis ? pe * (__uint_as_float(dr[c0 + e]) - dv[e]) * p.scale : 0.f;
-          }
-          dsw[16 * hf + 2 * c4] = pack_bf16x2(ds[0], ds[1]);
-          dsw[16 * hf + 2 * c4 + 1] = pack_bf16x2(ds[2], ds[3]);
-        }
+        dsw[2 * c4] = pack_bf16x2(ds[0], ds[1]);
+        dsw[2 * c4 + 1] = pack_bf16x2(ds[2], ds[3]);
       }
       // dS^T(b) into shared memory once the products of dS^T(b - 1) are done
       if (b >= 1 && !(ok = mbar_wait_warp(&bar_ds_free, (b - 1) & 1, ab))) break;
@@ -397,7 +369,7 @@ __global__ void __launch_bounds__(256, 1)
     // dQ^T (lane = dim) -> shared memory [column][576 dims] bf16 in the Q
     // slots, then row-contiguous stores of dQ and dQp; a tile with no
     // visible token stores zeros
-    __nv_bfloat16* stg = reinterpret_cast<__nv_bfloat16*>(sm + Q_OFF);
+    __nv_bfloat16* stg = reinterpret_cast<__nv_bfloat16*>(sm + QD_OFF);
     if (ok || nb == 0) {
       for (int j = 0; j < 5; ++j) {
         const int dim = (j < 4 ? 128 * j : kLat) + row;
