@@ -37,7 +37,7 @@
 //
 // Shared memory: the K tile stays resident (latent + position, 9 chunks of
 // [128 tokens x 64 dims], 144 KiB); Q, Qp and dY arrive as a stream of 8 KiB
-// chunks ([64 columns x 64 dims]) through a 4-stage TMA ring of two chunk
+// chunks ([64 columns x 64 dims]) through a 5-stage TMA ring of two chunk
 // slots each, in the order
 //   (Q, dY) pairs of latent chunk c = 0..7 and Qp of tile t (the pair is the
 //   B operand [Q | dY]^T of one N = 128 product), then the part's
@@ -68,8 +68,8 @@ namespace {
 constexpr int kLat = 512, kPos = 64;
 constexpr int BT = 128;                  // tokens per CTA (8 pages of 16)
 constexpr int BC = 64;                   // columns per tile
-constexpr int kStages = 4;               // ring of stages of two chunk slots
-constexpr int kStatSlots = 4;
+constexpr int kStages = 5;               // ring of stages of two chunk slots
+constexpr int kStatSlots = 2;
 constexpr int KCH = BT * 128;            // K chunk [128 tokens][64 dims], 16 KiB
 constexpr int QCH = BC * 128;            // Q / dY chunk [64 columns][64 dims], 8 KiB
 constexpr int K_OFF = 0;                 // 8 latent chunks + 1 position chunk
@@ -79,6 +79,10 @@ constexpr int ST_OFF = RING_OFF + kStages * STAGE;
 constexpr int ST_SLOT = 3 * BC * 4 + 16;  // -L2, delta, pos per column + pass info
 constexpr int BYTES = ST_OFF + kStatSlots * ST_SLOT;
 static_assert(RING_OFF % 1024 == 0 && QCH % 1024 == 0, "swizzled tiles need 1024-byte alignment");
+// dynamic shared memory starts 1024-aligned after the static variables (one
+// 1 KiB granule): no alignment pad, checked at run time
+constexpr int kStaticSmem = 1024;
+static_assert(BYTES + kStaticSmem <= 232448, "the layout fits one CTA's shared memory");
 // TMEM: accumulator [0, 320) (PART 0 uses [0, 256)); [S^T | dP^T] of the
 // current tile [320, 448) (one N = 128 product per key chunk); P^T and dS^T
 // as bf16 pairs [448, 480) and [480, 512), the A operands of the
@@ -249,8 +253,14 @@ __device__ __forceinline__ bool run_block(const CUtensorMap* tm_q, const CUtenso
     for (int t = 0; t <= n && ok; ++t) {
       if (t < n) {
         const int row0 = it.r_begin + it.tile * RT;
+        // [S | dP] chunks of tile t: (Q, dY) latent chunk pairs, then Qp
+        for (int c = 0; c < 8 && ok; ++c) ok = load_job(tm_q, c * 64, tm_dy, c * 64, row0);
+        if (ok) ok = load_job(tm_qp, 0, nullptr, 0, row0);
+        if (!ok) break;
         // column statistics of tile t: -L2, delta, pos per column (a row
-        // with lse = -inf sees no token), plus the pass's token mapping
+        // with lse = -inf sees no token), plus the pass's token mapping;
+        // after its chunk copies, so that waiting for the slot (tile t - 2
+        // done) never holds them back
         const int gt = ep.T + t, ss = gt % kStatSlots;
         if (gt >= kStatSlots && !(ok = mbar_wait(&b.st_empty[ss], ((gt / kStatSlots) - 1) & 1, ab))) break;
         uint8_t* st = sm + ST_OFF + ss * ST_SLOT;
@@ -279,11 +289,8 @@ __device__ __forceinline__ bool run_block(const CUtensorMap* tm_q, const CUtenso
           nx.advance(RT);
           fetch(nx);
         }
-        // [S | dP] chunks of tile t: (Q, dY) latent chunk pairs, then Qp
-        for (int c = 0; c < 8 && ok; ++c) ok = load_job(tm_q, c * 64, tm_dy, c * 64, row0);
-        if (ok) ok = load_job(tm_qp, 0, nullptr, 0, row0);
         // the accumulation chunks of tile t - 1
-        if (t >= 1 && ok) ok = load_acc(prev_row0);
+        if (t >= 1) ok = load_acc(prev_row0);
         if (!ok) break;
         prev_row0 = row0;
         it = nx;
@@ -520,13 +527,17 @@ __global__ void __launch_bounds__(384, 1)
     mla_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_qp,
                   const __grid_constant__ CUtensorMap tm_dy, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_kp, const PagedParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sm = smem_raw;
   __shared__ TcBars bars;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
   __shared__ PageInfo pinfo;
   __shared__ int unit_sh[3], n_tiles_sh, any_store_sh;
+  if (smem_addr(smem_raw) & 1023u) {  // uniform: the swizzled tiles need 1024-byte alignment
+    if (threadIdx.x == 0 && p.err) atomicOr(p.err, DEV_ERR_LAYOUT);
+    return;
+  }
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int RT = BC / p.G;  // query rows per tile
@@ -738,8 +749,8 @@ __global__ void __launch_bounds__(384, 1)
                         const __grid_constant__ CUtensorMap tm_dy, const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_kp, const PagedParams p) {
   static_assert(kSplitCL == kMlaSplitRanks, "the counters hold one entry per cluster rank");
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sm = smem_raw;
   __shared__ TcBars bars;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag, abort_any_sh;
@@ -756,6 +767,10 @@ __global__ void __launch_bounds__(384, 1)
   const int nitems = p.S * nblk * p.KVH;
   constexpr int acc_cols = PartShape<PART>::ACC_COLS;
   const Abort ab{&abort_flag, p.err};
+  if (smem_addr(smem_raw) & 1023u) {  // every CTA alike: the swizzled tiles need 1024-byte alignment
+    if (threadIdx.x == 0 && p.err) atomicOr(p.err, DEV_ERR_LAYOUT);
+    return;
+  }
   // the kernels launched next (part 1, then the grid kernels) as programmatic
   // dependents may start on the SMs these clusters leave free; part 1's last
   // CTA waits for part 0 at the end, so that the chain completes in order
@@ -984,7 +999,7 @@ __global__ void __launch_bounds__(384, 1)
 
 template <int PART>
 cudaError_t launch_split(const PagedMlaMaps& m, const PagedParams& p, int ncl, bool dependent, cudaStream_t s) {
-  cudaError_t e = cudaFuncSetAttribute(mla_tc_split_kernel<PART>, cudaFuncAttributeMaxDynamicSharedMemorySize, BYTES + 1024);
+  cudaError_t e = cudaFuncSetAttribute(mla_tc_split_kernel<PART>, cudaFuncAttributeMaxDynamicSharedMemorySize, BYTES);
   if (e != cudaSuccess) return e;
   cudaLaunchAttribute at[2];
   at[0].id = cudaLaunchAttributeClusterDimension;
@@ -996,7 +1011,7 @@ cudaError_t launch_split(const PagedMlaMaps& m, const PagedParams& p, int ncl, b
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(ncl * kSplitCL, 1, 1);
   cfg.blockDim = dim3(384, 1, 1);
-  cfg.dynamicSmemBytes = BYTES + 1024;
+  cfg.dynamicSmemBytes = BYTES;
   cfg.stream = s;
   cfg.attrs = at;
   cfg.numAttrs = dependent ? 2 : 1;
@@ -1013,7 +1028,7 @@ cudaError_t split_clusters(int* ncl) {
   if (e != cudaSuccess) return e;
   *ncl = dev < 64 ? cached[dev].load(std::memory_order_relaxed) : 0;
   if (*ncl > 0) return cudaSuccess;
-  const int smem = BYTES + 1024;
+  const int smem = BYTES;
   if ((e = cudaFuncSetAttribute(mla_tc_split_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess ||
       (e = cudaFuncSetAttribute(mla_tc_split_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
     return e;
@@ -1037,8 +1052,8 @@ cudaError_t split_clusters(int* ncl) {
 template <int PART>
 cudaError_t launch_grid(const PagedMlaMaps& m, const PagedParams& p, bool dependent, cudaStream_t s) {
   auto kern = mla_tc_kernel<PART>;
-  const int smem = BYTES + 1024;
-  static_assert(BYTES + 1024 >= kSmemOneCtaPerSm, "all 512 TMEM columns: one CTA per SM");
+  const int smem = BYTES;
+  static_assert(BYTES >= kSmemOneCtaPerSm, "all 512 TMEM columns: one CTA per SM");
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;

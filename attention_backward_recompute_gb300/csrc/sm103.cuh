@@ -19,6 +19,7 @@ namespace sm103 {
 // Device error word codes (OR-ed into the word the host reads back).
 enum : uint32_t {
   DEV_ERR_TIMEOUT = 1u,      // a bounded wait gave up
+  DEV_ERR_LAYOUT = 8u,       // dynamic shared memory not at the alignment the kernel's layout needs
 };
 
 __device__ __forceinline__ uint64_t global_timer_ns() {
