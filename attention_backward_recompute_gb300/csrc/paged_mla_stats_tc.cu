@@ -18,7 +18,7 @@
 //   dP = dY K_lat^T          : A = dY resident in shared memory (128 KiB)
 // and the compute warps (thread = column) keep an online maximum, the
 // denominator and the dP-weighted sum.  K arrives in chunks of [64 tokens x 64
-// dims] through a 4-stage ring of two chunks per stage.  Tensor memory: Q
+// dims] through a 6-stage ring of two chunks per stage.  Tensor memory: Q
 // [0, 288), S[2] [288, 416), dP [416, 480) (single buffer: the group reads
 // the whole dP tile into registers before it works on S).
 #include <cuda_bf16.h>
@@ -36,7 +36,7 @@ namespace {
 constexpr int kLat = 512, kPos = 64;
 constexpr int BC = 128;                 // columns per CTA
 constexpr int BT = 64;                  // tokens per tile (4 pages of 16)
-constexpr int kStages = 4;
+constexpr int kStages = 6;
 constexpr int QCH = BC * 128;           // Q / dY chunk [128 columns][64 dims], 16 KiB
 constexpr int KCH = BT * 128;           // K chunk [64 tokens][64 dims], 8 KiB
 constexpr int STAGE = 2 * KCH;
@@ -44,6 +44,9 @@ constexpr int DY_OFF = 0;               // 8 chunks (Q latent chunks while stagi
 constexpr int RING_OFF = DY_OFF + 8 * QCH;  // 4 stages (the Qp chunk while staging)
 constexpr int BYTES = RING_OFF + kStages * STAGE;
 static_assert(kStages * STAGE >= QCH, "the Qp chunk is staged through the ring");
+// dynamic shared memory starts 1024-aligned after the static variables (at
+// most 2 KiB here): no alignment pad, checked at run time
+static_assert(BYTES + 2048 <= 232448, "the layout fits one CTA's shared memory");
 constexpr int T_Q = 0, T_S = 288, T_DP = 416, TMEM_COLS = 512;
 constexpr float kRescaleThreshold = 8.0f;
 
@@ -65,8 +68,8 @@ __global__ void __launch_bounds__(384, 1)
     mla_stats_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_qp,
                         const __grid_constant__ CUtensorMap tm_dy, const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_kp, const PagedParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sm = smem_raw;
   __shared__ uint64_t bar_q, bar_q_staged, bar_dy, bar_full[kStages], bar_empty[kStages], bar_s_full[2],
       bar_s_read[2], bar_dp_full, bar_dp_read;
   __shared__ uint32_t tmem_base_sh;
@@ -86,6 +89,10 @@ __global__ void __launch_bounds__(384, 1)
   __syncthreads();
   const int s0 = seq_sh, r0 = r0_sh;
   if (s0 < 0) return;  // past the last row tile (uniform exit)
+  if (smem_addr(smem_raw) & 1023u) {  // uniform: the swizzled tiles need 1024-byte alignment
+    if (threadIdx.x == 0 && p.err) atomicOr(p.err, DEV_ERR_LAYOUT);
+    return;
+  }
   const int re = row_end_of(p, s0);
   const int len = seq_len_of(p, s0);
   const int npg = pages_of(len, p.page_size);
@@ -380,8 +387,8 @@ bool mla_stats_tc_supported(const PagedParams& p) {
 
 cudaError_t launch_paged_mla_stats_tc(const PagedMlaMaps& m, const PagedParams& p, cudaStream_t s) {
   if (p.Nq == 0 || p.S == 0) return cudaSuccess;
-  const int smem = BYTES + 1024;
-  static_assert(BYTES + 1024 >= kSmemOneCtaPerSm, "all 512 TMEM columns: one CTA per SM");
+  const int smem = BYTES;
+  static_assert(BYTES >= kSmemOneCtaPerSm, "all 512 TMEM columns: one CTA per SM");
   cudaError_t e = cudaFuncSetAttribute(mla_stats_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   // an upper bound on the row tiles of all sequences; each CTA finds its own
