@@ -21,12 +21,14 @@
 // costs one pass per (sequence, block), not one per page).
 //
 // The kernel is persistent (one CTA per SM over the items, in a snake order):
-// a scheduler warp works out each item's pages, links and tile count ahead of
-// time into a two-slot item ring, so that the next item's K/V gather and first
-// products overlap the previous item's last tiles and epilogue.
+// a scheduler warp works out each item's pages (eight lanes, one page each),
+// links and tile count ahead of time into a four-slot item ring, and the K/V
+// tiles are double-buffered, so that the next item's gather runs while the
+// current item computes.
 // Roles (384 threads): warp 0 TMA producer (K/V pages per item, Q/dY column
-// tiles through a 4-stage ring with the columns' statistics, fetched one tile
-// ahead), warp 1 MMA issuer (whole warp, elect.sync), warp 2 item scheduler,
+// tiles through a 3-stage ring (4 for D = 64), the columns' statistics through
+// a 2-slot ring, fetched one tile ahead), warp 1 MMA issuer (whole warp,
+// elect.sync), warp 2 item scheduler,
 // warps 4..7 / 8..11 compute groups for even / odd tiles (each forms P and
 // then dS of its tiles; group 0 stores dV, group 1 dK).
 #include <cuda_bf16.h>
@@ -42,21 +44,30 @@ using namespace sm103;
 
 namespace {
 
-constexpr int kStages = 4;
+constexpr int kStatSlots = 2;
+constexpr int kItemSlots = 4;  // items the scheduler prepares ahead
 
+// Two K/V buffers (the next item's pages are gathered while this item runs),
+// a ring of Q/dY column tiles, and the column statistics in their own
+// two-slot ring.
 template <int DP>
 struct HistLayout {
   static constexpr int NCH = DP / 64;
   static constexpr int BT = 128, BC = 64;        // tokens x columns per step
+  static constexpr int STAGES = DP == 64 ? 4 : 3;
   static constexpr int KV = NCH * BT * 128;
   static constexpr int QT = NCH * BC * 128;
   static constexpr int K_OFF = 0;
   static constexpr int V_OFF = K_OFF + KV;
-  static constexpr int Q_OFF = V_OFF + KV;             // kStages
-  static constexpr int DY_OFF = Q_OFF + kStages * QT;  // kStages
-  static constexpr int ST_OFF = DY_OFF + kStages * QT; // kStages x {-L2, delta, pos} x 64 + pass info
+  static constexpr int KVB = 2 * KV;                   // K/V buffer b at b * KVB
+  static constexpr int Q_OFF = 2 * KVB;                // STAGES
+  static constexpr int DY_OFF = Q_OFF + STAGES * QT;   // STAGES
+  static constexpr int ST_OFF = DY_OFF + STAGES * QT;  // kStatSlots x {-L2, delta, pos} x 64 + pass info
   static constexpr int ST_STAGE = 3 * BC * 4 + 16;
-  static constexpr int BYTES = ST_OFF + kStages * ST_STAGE;
+  static constexpr int BYTES = ST_OFF + kStatSlots * ST_STAGE;
+  // dynamic shared memory starts 1024-aligned after the static variables
+  // (one 1 KiB granule): no alignment pad, checked at run time
+  static_assert(BYTES + 1024 <= 232448, "the layout fits one CTA's shared memory");
   // TMEM: dV [0, DP), dK [DP, 2DP), S^T[2] and dP^T[2] 64 columns each
   static constexpr int T_S = 2 * DP, T_DP = 2 * DP + 128;
   static constexpr int TMEM_COLS = 512;
@@ -85,15 +96,22 @@ __global__ void __launch_bounds__(384, 1)
                          const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                          const PagedParams p) {
   using L = HistLayout<DP>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  // bar_kv / bar_kv_free / bar_acc / bar_acc_free: phases count items with
-  // tiles (as in the dense persistent kernel); bar_item_*: every item
-  __shared__ uint64_t bar_item_full[2], bar_item_empty[2], bar_kv, bar_kv_free, bar_full[kStages],
-      bar_empty[kStages], bar_s_full[2], bar_dp_full[2], bar_p_full[2], bar_ds_full[2], bar_acc, bar_acc_free;
+  constexpr int kStages = L::STAGES;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sm = smem_raw;
+  // bar_acc / bar_acc_free: phases count items with tiles (as in the dense
+  // persistent kernel); bar_kv[b] / bar_kv_free[b]: the items with tiles
+  // that use K/V buffer b (item lv uses buffer lv & 1); bar_item_*: every item
+  __shared__ uint64_t bar_item_full[kItemSlots], bar_item_empty[kItemSlots], bar_kv[2], bar_kv_free[2],
+      bar_full[kStages], bar_empty[kStages], bar_st_full[kStatSlots], bar_st_empty[kStatSlots], bar_s_full[2],
+      bar_dp_full[2], bar_p_full[2], bar_ds_full[2], bar_acc, bar_acc_free;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
-  __shared__ ItemSlot items[2];
+  __shared__ ItemSlot items[kItemSlots];
+  if (smem_addr(smem_raw) & 1023u) {  // uniform: the swizzled tiles need 1024-byte alignment
+    if (threadIdx.x == 0 && p.err) atomicOr(p.err, DEV_ERR_LAYOUT);
+    return;
+  }
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int RT = L::BC / p.G;  // query rows per step
@@ -103,19 +121,27 @@ __global__ void __launch_bounds__(384, 1)
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kItemSlots; ++s) {
       mbar_init(&bar_item_full[s], 1);
       mbar_init(&bar_item_empty[s], 10);  // producer, MMA warp, 8 compute warps
+    }
+    for (int s = 0; s < 2; ++s) {
       mbar_init(&bar_s_full[s], 1);
       mbar_init(&bar_dp_full[s], 1);
       mbar_init(&bar_p_full[s], 4);
       mbar_init(&bar_ds_full[s], 4);
     }
-    mbar_init(&bar_kv, 1);
-    mbar_init(&bar_kv_free, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bar_kv[b], 1);
+      mbar_init(&bar_kv_free[b], 1);
+    }
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&bar_full[s], 2);  // TMA bytes + column statistics written
+      mbar_init(&bar_full[s], 1);
       mbar_init(&bar_empty[s], 1);
+    }
+    for (int s = 0; s < kStatSlots; ++s) {
+      mbar_init(&bar_st_full[s], 1);
+      mbar_init(&bar_st_empty[s], 4);  // the four warps of the tile's compute group
     }
     mbar_init(&bar_acc, 1);
     mbar_init(&bar_acc_free, 8);
@@ -134,11 +160,11 @@ __global__ void __launch_bounds__(384, 1)
 
   // every role but the scheduler walks the item ring in order
   auto item_wait = [&](int ii) -> bool {
-    return mbar_wait_warp(&bar_item_full[ii & 1], (ii >> 1) & 1, ab);
+    return mbar_wait_warp(&bar_item_full[ii % kItemSlots], (ii / kItemSlots) & 1, ab);
   };
   auto item_done = [&](int ii) {
     __syncwarp();
-    if (lane == 0) mbar_arrive(&bar_item_empty[ii & 1]);
+    if (lane == 0) mbar_arrive(&bar_item_empty[ii % kItemSlots]);
   };
 
   if (warp == 2) {
@@ -157,11 +183,14 @@ __global__ void __launch_bounds__(384, 1)
         const int g = idx % p.KVH, tb = (idx / p.KVH) % nblk, s0 = idx / (p.KVH * nblk);
         const int npg = pages_of(seq_len_of(p, s0), p.page_size);
         if (tb * 8 < npg) {
-          if (ii >= 2 && !(ok = mbar_wait_warp(&bar_item_empty[ii & 1], ((ii >> 1) - 1) & 1, ab))) break;
-          ItemSlot& it = items[ii & 1];
-          int any = 0;
-          if (lane == 0) any = fill_page_info(p, s0, tb, npg, &it.pi);
-          any = __shfl_sync(0xffffffffu, any, 0);
+          if (ii >= kItemSlots &&
+              !(ok = mbar_wait_warp(&bar_item_empty[ii % kItemSlots], ((ii / kItemSlots) - 1) & 1, ab)))
+            break;
+          ItemSlot& it = items[ii % kItemSlots];
+          // lanes 0..7 fetch the eight pages' entries side by side
+          const int st = lane < 8 ? fill_page_entry(p, s0, tb, npg, lane, &it.pi) : 0;
+          const int any = __any_sync(0xffffffffu, st != 0);
+          __syncwarp();
           // a block whose pages are all stored by other items (their owners)
           // has nothing to write
           if (any) {
@@ -169,14 +198,14 @@ __global__ void __launch_bounds__(384, 1)
               PassIter pit{&p, &it.pi, s0, tb};
               int n = 0;
               if (pit.begin(RT)) {
-                do ++n;
-                while (pit.advance(RT));
+                do n += pit.ntiles;
+                while (pit.next_pass(RT));
               }
               it.s0 = s0;
               it.tb = tb;
               it.g = g;
               it.n = n;
-              mbar_arrive(&bar_item_full[ii & 1]);
+              mbar_arrive(&bar_item_full[ii % kItemSlots]);
             }
             __syncwarp();
             ++ii;
@@ -186,10 +215,11 @@ __global__ void __launch_bounds__(384, 1)
       if (last_round) break;
     }
     // end marker
-    if (ok && (ii < 2 || mbar_wait_warp(&bar_item_empty[ii & 1], ((ii >> 1) - 1) & 1, ab))) {
+    if (ok && (ii < kItemSlots ||
+               mbar_wait_warp(&bar_item_empty[ii % kItemSlots], ((ii / kItemSlots) - 1) & 1, ab))) {
       if (lane == 0) {
-        items[ii & 1].n = -1;
-        mbar_arrive(&bar_item_full[ii & 1]);
+        items[ii % kItemSlots].n = -1;
+        mbar_arrive(&bar_item_full[ii % kItemSlots]);
       }
     }
   } else if (warp == 0) {
@@ -227,19 +257,22 @@ __global__ void __launch_bounds__(384, 1)
     };
     for (int ii = 0; ok; ++ii) {
       if (!(ok = item_wait(ii))) break;
-      const ItemSlot& it = items[ii & 1];
+      const ItemSlot& it = items[ii % kItemSlots];
       const int n = it.n;
       if (n < 0) break;
       if (n > 0) {
         const int g = it.g;
-        if (lv > 0 && !(ok = mbar_wait(&bar_kv_free, (lv - 1) & 1, ab))) break;
+        // buffer lv & 1: free once item lv - 2's products are done
+        const int kb = lv & 1;
+        if (lv >= 2 && !(ok = mbar_wait(&bar_kv_free[kb], ((lv >> 1) - 1) & 1, ab))) break;
         if (lane == 0) {
-          mbar_arrive_expect_tx(&bar_kv, 2 * L::KV);
+          uint8_t* kvb = sm + kb * L::KVB;
+          mbar_arrive_expect_tx(&bar_kv[kb], 2 * L::KV);
           for (int j = 0; j < 8; ++j) {
             const int slot = it.pi.phys[j] >= 0 ? it.pi.phys[j] * p.page_size : oob_slot;
             for (int c = 0; c < L::NCH; ++c) {
-              tma_load_3d(sm + L::K_OFF + c * (L::BT * 128) + j * 16 * 128, &tm_k, &bar_kv, c * 64, g, slot);
-              tma_load_3d(sm + L::V_OFF + c * (L::BT * 128) + j * 16 * 128, &tm_v, &bar_kv, c * 64, g, slot);
+              tma_load_3d(kvb + L::K_OFF + c * (L::BT * 128) + j * 16 * 128, &tm_k, &bar_kv[kb], c * 64, g, slot);
+              tma_load_3d(kvb + L::V_OFF + c * (L::BT * 128) + j * 16 * 128, &tm_v, &bar_kv[kb], c * 64, g, slot);
             }
           }
         }
@@ -258,7 +291,11 @@ __global__ void __launch_bounds__(384, 1)
                           row0);
             }
           }
-          uint8_t* st = sm + L::ST_OFF + s * L::ST_STAGE;
+          // the tile's column statistics, after its copies are issued: slot
+          // gg mod 2 is free once its group has formed dS of tile gg - 2
+          const int ss = gg % kStatSlots;
+          if (gg >= kStatSlots && !(ok = mbar_wait(&bar_st_empty[ss], ((gg / kStatSlots) - 1) & 1, ab))) break;
+          uint8_t* st = sm + L::ST_OFF + ss * L::ST_STAGE;
           float* snl = reinterpret_cast<float*>(st);
           float* sdl = snl + L::BC;
           int* spos = reinterpret_cast<int*>(sdl + L::BC);
@@ -278,7 +315,7 @@ __global__ void __launch_bounds__(384, 1)
             sinfo[3] = f_info[3];
           }
           __syncwarp();
-          if (lane == 0) mbar_arrive(&bar_full[s]);
+          if (lane == 0) mbar_arrive(&bar_st_full[ss]);
           last_use[s] = gg;
           if (t + 1 < n) {
             pit.advance(RT);
@@ -293,15 +330,16 @@ __global__ void __launch_bounds__(384, 1)
     if (lane == 0) {
       for (int s = 0; s < kStages; ++s)
         if (last_use[s] >= 0) drain_wait(&bar_full[s], (last_use[s] / kStages) & 1);
-      if (lv > 0) drain_wait(&bar_kv, (lv - 1) & 1);
+      for (int u = max(lv - 2, 0); u < lv; ++u) drain_wait(&bar_kv[u & 1], (u >> 1) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     // the whole warp runs this role (warp-uniform); elected lanes issue
     constexpr uint32_t id_s = idesc_bf16(128, 64, false, false);
     constexpr uint32_t id_acc = idesc_bf16(128, DP, false, true);
-    const uint64_t dK = sdesc_sw128(smem_addr(sm + L::K_OFF), 16, 1024);
-    const uint64_t dV = sdesc_sw128(smem_addr(sm + L::V_OFF), 16, 1024);
+    const uint64_t dK0 = sdesc_sw128(smem_addr(sm + L::K_OFF), 16, 1024);
+    const uint64_t dV0 = sdesc_sw128(smem_addr(sm + L::V_OFF), 16, 1024);
+    uint64_t dK = dK0, dV = dV0;  // the current item's K/V buffer
     const uint64_t dQ0 = sdesc_sw128(smem_addr(sm + L::Q_OFF), 16, 1024);
     const uint64_t dDY0 = sdesc_sw128(smem_addr(sm + L::DY_OFF), 16, 1024);
     const uint64_t dQm0 = sdesc_sw128(smem_addr(sm + L::Q_OFF), L::BC * 128, 1024);    // MN-major
@@ -336,10 +374,13 @@ __global__ void __launch_bounds__(384, 1)
     int g0 = 0, lv = 0;
     for (int ii = 0; ok; ++ii) {
       if (!(ok = item_wait(ii))) break;
-      const int n = items[ii & 1].n;
+      const int n = items[ii % kItemSlots].n;
       if (n < 0) break;
       if (n > 0) {
-        if (!(ok = mbar_wait_warp(&bar_kv, lv & 1, ab))) break;
+        const int kb = lv & 1;
+        if (!(ok = mbar_wait_warp(&bar_kv[kb], (lv >> 1) & 1, ab))) break;
+        dK = sdesc_add(dK0, kb * L::KVB);
+        dV = sdesc_add(dV0, kb * L::KVB);
         // the first score and dP tiles of this item go while the epilogue of
         // the previous item still reads dV and dK
         for (int t = 0; t < 2 && t < n && ok; ++t) {
@@ -349,7 +390,7 @@ __global__ void __launch_bounds__(384, 1)
           issue_dp(g0 + t);
         }
         if (!ok) break;
-        if (n <= 2) mma_commit_w(&bar_kv_free);
+        if (n <= 2) mma_commit_w(&bar_kv_free[kb]);
         if (lv > 0 && !(ok = mbar_wait_warp(&bar_acc_free, (lv - 1) & 1, ab))) break;
         tc_fence_after();
         // Per tile g: dV(g) once P(g) is in; then S(g+2) and dK(g) in
@@ -382,7 +423,7 @@ __global__ void __launch_bounds__(384, 1)
           if (!ok) break;
           if (t + 2 < n) {
             issue_dp(g + 2);
-            if (t + 3 == n) mma_commit_w(&bar_kv_free);  // the item's last S and dP are issued
+            if (t + 3 == n) mma_commit_w(&bar_kv_free[kb]);  // the item's last S and dP are issued
           }
         }
         if (!ok) break;
@@ -403,13 +444,13 @@ __global__ void __launch_bounds__(384, 1)
     int g0 = 0, lv = 0;
     for (int ii = 0; ok; ++ii) {
       if (!(ok = item_wait(ii))) break;
-      const ItemSlot& it = items[ii & 1];
+      const ItemSlot& it = items[ii % kItemSlots];
       const int n = it.n;
       if (n < 0) break;
       for (int t = ((g0 & 1) == sg) ? 0 : 1; t < n && ok; t += 2) {
-        const int g = g0 + t, s = g % kStages, bb = g & 1;
-        if (!(ok = mbar_wait_warp(&bar_full[s], (g / kStages) & 1, ab))) break;
-        const uint8_t* st = sm + L::ST_OFF + s * L::ST_STAGE;
+        const int g = g0 + t, bb = g & 1, ss = g % kStatSlots;
+        if (!(ok = mbar_wait_warp(&bar_st_full[ss], (g / kStatSlots) & 1, ab))) break;
+        const uint8_t* st = sm + L::ST_OFF + ss * L::ST_STAGE;
         const float* snl = reinterpret_cast<const float*>(st);
         const float* sdl = snl + L::BC;
         const int* spos = reinterpret_cast<const int*>(sdl + L::BC);
@@ -481,7 +522,10 @@ __global__ void __launch_bounds__(384, 1)
         tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bar_ds_full[bb]);
+        if (lane == 0) {
+          mbar_arrive(&bar_ds_full[bb]);
+          mbar_arrive(&bar_st_empty[ss]);
+        }
       }
       if (!ok) break;
       if (n > 0) {
@@ -534,7 +578,7 @@ template <int DP>
 cudaError_t launch_hist_t(const PagedMaps& m, const PagedParams& p, cudaStream_t s) {
   using L = HistLayout<DP>;
   auto kern = paged_history_kernel<DP>;
-  const int smem = max(L::BYTES + 1024, kSmemOneCtaPerSm);  // all 512 TMEM columns: one CTA per SM
+  const int smem = max(L::BYTES, kSmemOneCtaPerSm);  // all 512 TMEM columns: one CTA per SM
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;

@@ -86,31 +86,35 @@ struct PassIter {
 };
 
 
-// The eight pages of token block tb of sequence s0 (npg pages in the
-// sequence): physical page, link segment, and whether this block stores the
-// page (its first link is this one and, in compact history, it is listed).
-// Returns whether the block stores any page.
+// Page j of token block tb of sequence s0 (npg pages in the sequence):
+// physical page, link segment, and whether this block stores the page (its
+// first link is this one and, in compact history, it is listed).  Returns
+// whether the block stores it.
+__device__ inline int fill_page_entry(const PagedParams& p, int s0, int tb, int npg, int j, PageInfo* pi) {
+  const int lp = tb * 8 + j;
+  int ph = -1, off = 0, cnt = 0, st = 0;
+  if (lp < npg) {
+    ph = p.page_table[static_cast<int64_t>(s0) * p.max_pages + lp];
+    if (ph >= 0 && ph < p.num_pages) {
+      off = p.link_off[ph];
+      cnt = p.link_off[ph + 1] - off;
+      st = cnt > 0 && p.links[off] == s0 * p.max_pages + lp && (!p.listed || p.listed[ph]);
+    } else {
+      ph = -1;
+    }
+  }
+  pi->phys[j] = ph;
+  pi->off[j] = off;
+  pi->cnt[j] = cnt;
+  pi->store[j] = st;
+  return st;
+}
+
+// The eight pages of the block (see fill_page_entry); returns whether the
+// block stores any page.
 __device__ inline int fill_page_info(const PagedParams& p, int s0, int tb, int npg, PageInfo* pi) {
   int any = 0;
-  for (int j = 0; j < 8; ++j) {
-    const int lp = tb * 8 + j;
-    int ph = -1, off = 0, cnt = 0, st = 0;
-    if (lp < npg) {
-      ph = p.page_table[static_cast<int64_t>(s0) * p.max_pages + lp];
-      if (ph >= 0 && ph < p.num_pages) {
-        off = p.link_off[ph];
-        cnt = p.link_off[ph + 1] - off;
-        st = cnt > 0 && p.links[off] == s0 * p.max_pages + lp && (!p.listed || p.listed[ph]);
-      } else {
-        ph = -1;
-      }
-    }
-    pi->phys[j] = ph;
-    pi->off[j] = off;
-    pi->cnt[j] = cnt;
-    pi->store[j] = st;
-    any |= st;
-  }
+  for (int j = 0; j < 8; ++j) any |= fill_page_entry(p, s0, tb, npg, j, pi);
   return any;
 }
 
