@@ -29,11 +29,17 @@ struct StatLayout {
   static constexpr int PT = BQ * 128;
   static constexpr int Q_OFF = 0;
   static constexpr int DY_OFF = Q_OFF + QT;
-  static constexpr int K_OFF = DY_OFF + QT;        // 2 stages
-  static constexpr int V_OFF = K_OFF + 2 * KT;     // 2 stages
-  static constexpr int P_OFF = V_OFF + 2 * KT;     // 2 buffers
+  // K/V stages: 4 at D = 128 (one CTA per SM either way); 2 at D = 64,
+  // where the smaller layout lets two CTAs share an SM
+  static constexpr int KS = DP == 64 ? 2 : 4;
+  static constexpr int K_OFF = DY_OFF + QT;        // KS stages
+  static constexpr int V_OFF = K_OFF + KS * KT;    // KS stages
+  static constexpr int P_OFF = V_OFF + KS * KT;    // 2 buffers
   static constexpr int BYTES = P_OFF + 2 * PT;
   static constexpr int TMEM_COLS = 256;
+  // dynamic shared memory starts 1024-aligned after the static variables
+  // (one 1 KiB granule): no alignment pad, checked at run time
+  static_assert(BYTES + 1024 <= 232448, "the layout fits one CTA's shared memory");
 };
 
 constexpr float kRescaleThreshold = 8.0f;
@@ -52,9 +58,10 @@ __global__ void __launch_bounds__(256, 1)
                        const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                        const PagedParams p) {
   using L = StatLayout<DP>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t bar_q, bar_dy, bar_full[2], bar_empty[2], bar_s_full[2], bar_p_full[2], bar_p_free[2];
+  constexpr int KS = L::KS;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sm = smem_raw;
+  __shared__ uint64_t bar_q, bar_dy, bar_full[KS], bar_empty[KS], bar_s_full[2], bar_p_full[2], bar_p_free[2];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
   __shared__ int max_pos_sh;
@@ -74,6 +81,10 @@ __global__ void __launch_bounds__(256, 1)
   __syncthreads();
   const int sq = tile_sq_sh, r0 = tile_r0_sh;
   if (sq < 0) return;  // uniform exit: past the last row tile
+  if (smem_addr(smem_raw) & 1023u) {  // uniform: the swizzled tiles need 1024-byte alignment
+    if (threadIdx.x == 0 && p.err) atomicOr(p.err, DEV_ERR_LAYOUT);
+    return;
+  }
   const int r_end = row_end_of(p, sq);
   const int len = seq_len_of(p, sq);
   const int npg = pages_of(len, p.page_size);
@@ -83,9 +94,11 @@ __global__ void __launch_bounds__(256, 1)
     abort_flag = 0;
     mbar_init(&bar_q, 1);
     mbar_init(&bar_dy, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < KS; ++s) {
       mbar_init(&bar_full[s], 1);
       mbar_init(&bar_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
       mbar_init(&bar_s_full[s], 1);
       mbar_init(&bar_p_full[s], 4);
       mbar_init(&bar_p_free[s], 1);
@@ -118,11 +131,12 @@ __global__ void __launch_bounds__(256, 1)
       mbar_arrive_expect_tx(&bar_q, L::QT);
       for (int c = 0; c < L::NCH; ++c)
         tma_load_3d(sm + L::Q_OFF + c * (L::BQ * 128), &tm_q, &bar_q, c * 64, g * p.G, r0);
-      int last_use[2] = {-1, -1};
+      int last_use[KS];
+      for (int i = 0; i < KS; ++i) last_use[i] = -1;
       bool ok = true;
       for (int t = 0; t < n && ok; ++t) {
-        const int s = t & 1;
-        if (t >= 2) ok = mbar_wait(&bar_empty[s], ((t >> 1) - 1) & 1, ab);
+        const int s = t % KS;
+        if (t >= KS) ok = mbar_wait(&bar_empty[s], ((t / KS) - 1) & 1, ab);
         if (!ok) break;
         mbar_arrive_expect_tx(&bar_full[s], 2 * L::KT);
         for (int i = 0; i < L::BK / 16; ++i) {
@@ -146,8 +160,8 @@ __global__ void __launch_bounds__(256, 1)
             tma_load_3d(sm + L::DY_OFF + c * (L::BQ * 128), &tm_dy, &bar_dy, c * 64, g * p.G, r0);
         }
       }
-      for (int s = 0; s < 2; ++s)
-        if (last_use[s] >= 0) drain_wait(&bar_full[s], (last_use[s] >> 1) & 1);
+      for (int s = 0; s < KS; ++s)
+        if (last_use[s] >= 0) drain_wait(&bar_full[s], (last_use[s] / KS) & 1);
       drain_wait(&bar_q, 0);
       if (last_use[0] >= 0) drain_wait(&bar_dy, 0);
     }
@@ -160,13 +174,14 @@ __global__ void __launch_bounds__(256, 1)
       auto k_at = [&](int s) { return smem_addr(sm + L::K_OFF + s * L::KT); };
       auto v_at = [&](int s) { return smem_addr(sm + L::V_OFF + s * L::KT); };
       auto p_at = [&](int s) { return smem_addr(sm + L::P_OFF + s * L::PT); };
+      // S(t) into S buffer t & 1 from K stage t mod KS
       auto issue_s = [&](int t) {
-        const int s = t & 1;
+        const int s = t & 1, ks = t % KS;
 #pragma unroll
         for (int kk = 0; kk < DP / 16; ++kk) {
           const int c = kk >> 2, o = (kk & 3) * 32;
           const uint64_t ad = sdesc_sw128(sQ + c * (L::BQ * 128) + o, 16, 1024);
-          const uint64_t bd = sdesc_sw128(k_at(s) + c * (L::BK * 128) + o, 16, 1024);
+          const uint64_t bd = sdesc_sw128(k_at(ks) + c * (L::BK * 128) + o, 16, 1024);
           mma_bf16_ss(t_s0 + s * 64, ad, bd, id_s, kk > 0 ? 1u : 0u);
         }
         mma_commit(&bar_s_full[s]);
@@ -185,19 +200,20 @@ __global__ void __launch_bounds__(256, 1)
         }
       }
       for (int t = 0; t < n && ok; ++t) {
-        const int s = t & 1;
+        const int s = t & 1, ks = t % KS;
         if (!(ok = mbar_wait(&bar_p_full[s], (t >> 1) & 1, ab))) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < L::BK / 16; ++kk) {
           const uint64_t ad = sdesc_sw128(p_at(s) + kk * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(v_at(s) + kk * 16 * 128, L::BK * 128, 1024);
+          const uint64_t bd = sdesc_sw128(v_at(ks) + kk * 16 * 128, L::BK * 128, 1024);
           mma_bf16_ss(t_o, ad, bd, id_o, (t == 0 && kk == 0) ? 0u : 1u);
         }
         mma_commit(&bar_p_free[s]);
-        mma_commit(&bar_empty[s]);
+        mma_commit(&bar_empty[ks]);
         if (t + 2 < n) {
-          if (!(ok = mbar_wait(&bar_full[s], ((t + 2) >> 1) & 1, ab))) break;
+          const int k2 = (t + 2) % KS;
+          if (!(ok = mbar_wait(&bar_full[k2], ((t + 2) / KS) & 1, ab))) break;
           tc_fence_after();
           issue_s(t + 2);
         }
@@ -279,10 +295,10 @@ __global__ void __launch_bounds__(256, 1)
       // O += P V, so their V rows are zeroed before the product reads them.
       if (tk0 + L::BK > len) {
         // the stage's copies have landed (observed here, not only by the MMA thread)
-        if (!(ok = mbar_wait_warp(&bar_full[s], (t >> 1) & 1, ab))) break;
+        if (!(ok = mbar_wait_warp(&bar_full[t % KS], (t / KS) & 1, ab))) break;
         const int row_lo = max(0, len - tk0);
         const int nvec = (L::BK - row_lo) * L::NCH * 8;
-        uint8_t* vt = sm + L::V_OFF + s * L::KT;
+        uint8_t* vt = sm + L::V_OFF + (t % KS) * L::KT;
         for (int i = threadIdx.x - 128; i < nvec; i += 128) {
           const int rw = row_lo + i / (L::NCH * 8), rem = i % (L::NCH * 8);
           const int ch = rem >> 3, seg = rem & 7;
@@ -351,7 +367,7 @@ template <int DP>
 cudaError_t launch_stats_t(const PagedMaps& m, const PagedParams& p, cudaStream_t s) {
   using L = StatLayout<DP>;
   auto kern = paged_stats_kernel<DP>;
-  const int smem = L::BYTES + 1024;
+  const int smem = L::BYTES;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int rt = L::BQ / p.G;
