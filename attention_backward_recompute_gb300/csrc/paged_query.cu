@@ -40,10 +40,14 @@ struct QueryLayout {
   static constexpr int PT = BQ * 128;
   static constexpr int Q_OFF = 0;
   static constexpr int DY_OFF = Q_OFF + QT;
-  static constexpr int K_OFF = DY_OFF + QT;     // 2 stages
-  static constexpr int V_OFF = K_OFF + 2 * KT;  // 2 stages
-  static constexpr int P_OFF = V_OFF + 2 * KT;  // 2 buffers: P (sweep 1), dS (sweep 2)
+  static constexpr int KS = DP == 64 ? 2 : 4;   // K/V stages
+  static constexpr int K_OFF = DY_OFF + QT;     // KS stages
+  static constexpr int V_OFF = K_OFF + KS * KT; // KS stages
+  static constexpr int P_OFF = V_OFF + KS * KT; // 2 buffers: P (sweep 1), dS (sweep 2)
   static constexpr int BYTES = P_OFF + 2 * PT;
+  // dynamic shared memory starts 1024-aligned after the static variables
+  // (one 1 KiB granule): no alignment pad, checked at run time
+  static_assert(BYTES + 1024 <= 232448, "the layout fits one CTA's shared memory");
   // TMEM: O [0, 128), dQ [128, 256), S[2] [256, 384), dP[2] [384, 512)
   static constexpr int T_O = 0, T_DQ = 128, T_S = 256, T_DP = 384, TMEM_COLS = 512;
 };
@@ -79,9 +83,10 @@ __global__ void __launch_bounds__(256, 1)
                        const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                        const PagedParams p) {
   using L = QueryLayout<DP>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ uint64_t bar_q, bar_dy, bar_full[2], bar_empty[2], bar_s_full[2], bar_p_full[2], bar_p_free[2];
+  constexpr int KS = L::KS;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sm = smem_raw;
+  __shared__ uint64_t bar_q, bar_dy, bar_full[KS], bar_empty[KS], bar_s_full[2], bar_p_full[2], bar_p_free[2];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
   __shared__ int max_pos_sh;
@@ -101,6 +106,10 @@ __global__ void __launch_bounds__(256, 1)
   __syncthreads();
   const int sq = tile_sq_sh, r0 = tile_r0_sh;
   if (sq < 0) return;  // uniform exit: past the last row tile
+  if (smem_addr(smem_raw) & 1023u) {  // uniform: the swizzled tiles need 1024-byte alignment
+    if (threadIdx.x == 0 && p.err) atomicOr(p.err, DEV_ERR_LAYOUT);
+    return;
+  }
   const int r_end = row_end_of(p, sq);
   const int len = seq_len_of(p, sq);
   const int npg = pages_of(len, p.page_size);
@@ -110,9 +119,11 @@ __global__ void __launch_bounds__(256, 1)
     abort_flag = 0;
     mbar_init(&bar_q, 1);
     mbar_init(&bar_dy, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < KS; ++s) {
       mbar_init(&bar_full[s], 1);
       mbar_init(&bar_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
       mbar_init(&bar_s_full[s], 1);
       mbar_init(&bar_p_full[s], 4);
       mbar_init(&bar_p_free[s], 1);
@@ -148,9 +159,9 @@ __global__ void __launch_bounds__(256, 1)
         tma_load_3d(sm + L::Q_OFF + c * (L::BQ * 128), &tm_q, &bar_q, c * 64, g * p.G, r0);
       bool ok = true;
       for (int t = 0; t < NT && ok; ++t) {
-        const int s = t & 1;
+        const int s = t % KS;
         const int u = t < n ? t : t - n;
-        if (t >= 2) ok = mbar_wait(&bar_empty[s], ((t >> 1) - 1) & 1, ab);
+        if (t >= KS) ok = mbar_wait(&bar_empty[s], ((t / KS) - 1) & 1, ab);
         if (!ok) break;
         mbar_arrive_expect_tx(&bar_full[s], 2 * L::KT);
         for (int i = 0; i < L::BK / 16; ++i) {
@@ -174,7 +185,7 @@ __global__ void __launch_bounds__(256, 1)
         }
       }
       // every copy issued has landed before the CTA can leave
-      for (int t = max(0, NT - 2); t < NT; ++t) drain_wait(&bar_full[t & 1], (t >> 1) & 1);
+      for (int t = max(0, NT - KS); t < NT; ++t) drain_wait(&bar_full[t % KS], (t / KS) & 1);
       drain_wait(&bar_q, 0);
       drain_wait(&bar_dy, 0);
     }
@@ -198,11 +209,12 @@ __global__ void __launch_bounds__(256, 1)
           mma_bf16_ss(d, ad, bd, id_s, kk > 0 ? 1u : 0u);
         }
       };
-      // tile t: S (both sweeps) and dP (sweep 2) into buffer t % 2
+      // tile t: S (both sweeps) and dP (sweep 2) into buffer t % 2, from
+      // K/V stage t mod KS
       auto issue_tile = [&](int t) {
-        const int s = t & 1;
-        issue_xt(tmem + L::T_S + s * 64, sQ, k_at(s));
-        if (t >= n) issue_xt(tmem + L::T_DP + s * 64, sDY, v_at(s));
+        const int s = t & 1, ks = t % KS;
+        issue_xt(tmem + L::T_S + s * 64, sQ, k_at(ks));
+        if (t >= n) issue_xt(tmem + L::T_DP + s * 64, sDY, v_at(ks));
         mma_commit(&bar_s_full[s]);
       };
       bool ok = mbar_wait(&bar_q, 0, ab);
@@ -214,13 +226,13 @@ __global__ void __launch_bounds__(256, 1)
         issue_tile(t);
       }
       for (int t = 0; t < NT && ok; ++t) {
-        const int s = t & 1;
+        const int s = t & 1, ks = t % KS;
         if (!(ok = mbar_wait(&bar_p_full[s], (t >> 1) & 1, ab))) break;
         tc_fence_after();
         // sweep 1: O += P V; sweep 2: dQ += dS K (B = the V or K tile, MN-major)
         const bool fwd = t < n;
         const uint32_t d = tmem + (fwd ? L::T_O : L::T_DQ);
-        const uint32_t b = fwd ? v_at(s) : k_at(s);
+        const uint32_t b = fwd ? v_at(ks) : k_at(ks);
 #pragma unroll
         for (int kk = 0; kk < L::BK / 16; ++kk) {
           const uint64_t ad = sdesc_sw128(p_at(s) + kk * 32, 16, 1024);
@@ -228,9 +240,9 @@ __global__ void __launch_bounds__(256, 1)
           mma_bf16_ss(d, ad, bd, id_o, ((t == 0 || t == n) && kk == 0) ? 0u : 1u);
         }
         mma_commit(&bar_p_free[s]);
-        mma_commit(&bar_empty[s]);
+        mma_commit(&bar_empty[ks]);
         if (t + 2 < NT) {
-          if (!(ok = mbar_wait(&bar_full[s], ((t + 2) >> 1) & 1, ab))) break;
+          if (!(ok = mbar_wait(&bar_full[(t + 2) % KS], ((t + 2) / KS) & 1, ab))) break;
           if (t + 2 >= n && !dy_ready && !(ok = dy_ready = mbar_wait(&bar_dy, 0, ab))) break;
           tc_fence_after();
           issue_tile(t + 2);
@@ -353,8 +365,8 @@ __global__ void __launch_bounds__(256, 1)
         }
         if (tk0 + L::BK > len) {
           // the stage's copies have landed (observed here, not only by the MMA thread)
-          if (!(ok = mbar_wait_warp(&bar_full[s], (t >> 1) & 1, ab))) break;
-          zero_tail_rows<DP>(sm + L::V_OFF + s * L::KT, max(0, len - tk0));
+          if (!(ok = mbar_wait_warp(&bar_full[t % KS], (t / KS) & 1, ab))) break;
+          zero_tail_rows<DP>(sm + L::V_OFF + (t % KS) * L::KT, max(0, len - tk0));
         }
         if (t >= 2 && !(ok = mbar_wait_warp(&bar_p_free[s], ((t - 2) >> 1) & 1, ab))) break;
         const uint32_t sp = smem_addr(sm + L::P_OFF + s * L::PT);
@@ -366,8 +378,8 @@ __global__ void __launch_bounds__(256, 1)
       } else {
         // ---------------------------------------------- sweep 2: S, dP -> dS, dQ += dS K
         if (tk0 + L::BK > len) {
-          if (!(ok = mbar_wait_warp(&bar_full[s], (t >> 1) & 1, ab))) break;
-          zero_tail_rows<DP>(sm + L::K_OFF + s * L::KT, max(0, len - tk0));
+          if (!(ok = mbar_wait_warp(&bar_full[t % KS], (t / KS) & 1, ab))) break;
+          zero_tail_rows<DP>(sm + L::K_OFF + (t % KS) * L::KT, max(0, len - tk0));
         }
         if (t >= 2 && !(ok = mbar_wait_warp(&bar_p_free[s], ((t - 2) >> 1) & 1, ab))) break;
         const uint32_t sp = smem_addr(sm + L::P_OFF + s * L::PT);
@@ -469,7 +481,7 @@ template <int DP>
 cudaError_t launch_query_t(const PagedMaps& m, const PagedParams& p, cudaStream_t s) {
   using L = QueryLayout<DP>;
   auto kern = paged_query_kernel<DP>;
-  const int smem = max(L::BYTES + 1024, kSmemOneCtaPerSm);  // all 512 TMEM columns: one CTA per SM
+  const int smem = max(L::BYTES, kSmemOneCtaPerSm);  // all 512 TMEM columns: one CTA per SM
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   const int rt = L::BQ / p.G;
