@@ -85,11 +85,12 @@ CASES = [
          value_dim=512, position_dim=64, causal=True, shared_prefix_pages=9),
     dict(seed=32, num_seqs=12, len_lo=150, len_hi=300, queries_per_seq=24, heads=32, kv_heads=2, key_dim=512,
          value_dim=512, position_dim=64, causal=False, shared_prefix_pages=5),
-    # 64 flagged (block, KV head) units (8 blocks of a 64-page prefix shared by
+    # 72 flagged (block, KV head) units (9 blocks of a 72-page prefix shared by
     # 40 sequences, 8 KV heads, 39 x 2 link tiles each): enough units that the
-    # split kernel takes them whole instead of cutting them into chunks
-    dict(seed=34, num_seqs=40, len_lo=1030, len_hi=1100, queries_per_seq=32, heads=32, kv_heads=8, key_dim=512,
-         value_dim=512, position_dim=64, causal=True, shared_prefix_pages=64),
+    # split kernel takes them whole instead of cutting them into chunks, and
+    # more than it lists up front (units past the 64th are found by search)
+    dict(seed=34, num_seqs=40, len_lo=1160, len_hi=1230, queries_per_seq=32, heads=32, kv_heads=8, key_dim=512,
+         value_dim=512, position_dim=64, causal=True, shared_prefix_pages=72),
 ]
 
 
