@@ -37,17 +37,35 @@ __global__ void count_links_kernel(PagedParams p) {
   }
 }
 
-// single-CTA exclusive scan of link_count into link_off[0..num_pages]
+// single-CTA exclusive scan of link_count into link_off[0..num_pages]: each
+// thread scans kScanPer consecutive counts in registers, the block scans the
+// thread totals, one chunk of 1024 x kScanPer pages after another
+constexpr int kScanPer = 16;
 __global__ void __launch_bounds__(1024) scan_links_kernel(PagedParams p) {
   __shared__ int warp_sums[32];
-  __shared__ int carry;
-  if (threadIdx.x == 0) carry = 0;
-  __syncthreads();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  for (int base = 0; base < p.num_pages; base += 1024) {
-    const int i = base + threadIdx.x;
-    const int v = i < p.num_pages ? p.link_count[i] : 0;
-    int x = v;
+  int carry = 0;  // sum of the chunks before (the same in every thread)
+  for (int base = 0; base < p.num_pages; base += 1024 * kScanPer) {
+    const int i0 = base + static_cast<int>(threadIdx.x) * kScanPer;
+    int v[kScanPer];
+    if (i0 + kScanPer <= p.num_pages) {  // 64-byte aligned: the workspace arrays are 256-byte aligned
+      const int4* src = reinterpret_cast<const int4*>(p.link_count + i0);
+#pragma unroll
+      for (int k = 0; k < kScanPer / 4; ++k) {
+        const int4 w = src[k];
+        v[4 * k] = w.x;
+        v[4 * k + 1] = w.y;
+        v[4 * k + 2] = w.z;
+        v[4 * k + 3] = w.w;
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < kScanPer; ++k) v[k] = i0 + k < p.num_pages ? p.link_count[i0 + k] : 0;
+    }
+    int tot = 0;
+#pragma unroll
+    for (int k = 0; k < kScanPer; ++k) tot += v[k];
+    int x = tot;  // inclusive scan of the thread totals within the warp
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int y = __shfl_up_sync(0xffffffffu, x, o);
@@ -65,11 +83,14 @@ __global__ void __launch_bounds__(1024) scan_links_kernel(PagedParams p) {
       warp_sums[lane] = w;
     }
     __syncthreads();
-    const int incl = x + (warp > 0 ? warp_sums[warp - 1] : 0) + carry;
-    if (i < p.num_pages) p.link_off[i] = incl - v;
-    __syncthreads();
-    if (threadIdx.x == 1023) carry = incl;
-    __syncthreads();
+    int run = carry + x - tot + (warp > 0 ? warp_sums[warp - 1] : 0);  // exclusive prefix of this thread
+#pragma unroll
+    for (int k = 0; k < kScanPer; ++k) {
+      if (i0 + k < p.num_pages) p.link_off[i0 + k] = run;
+      run += v[k];
+    }
+    carry += warp_sums[31];
+    __syncthreads();  // warp_sums is rewritten by the next chunk
   }
   if (threadIdx.x == 0) p.link_off[p.num_pages] = carry;
 }
