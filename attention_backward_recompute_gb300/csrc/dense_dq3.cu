@@ -67,7 +67,12 @@ __device__ __forceinline__ void dq3_item(const DenseParams& p, int w, int nqt128
   *it = nqt128 - 1 - w / BH;
 }
 
-// Persistent: CTA c takes work items c, c + gridDim.x, ...; the copy ring and
+// Work item of CTA c in round r: r*G + c, or r*G + G-1-c in odd rounds (a
+// snake over the longest-first order, which evens out the CTAs' totals of
+// key tiles; it grows with r, so the first index past the end ends the walk).
+__device__ __forceinline__ int dq3_round_item(int r, int c, int G) { return r * G + ((r & 1) ? G - 1 - c : c); }
+
+// Persistent: CTA c takes its work items round by round; the copy ring and
 // its phases run on across items, and the two dQ accumulators alternate, so
 // one item's epilogue overlaps the next item's copies and products.
 template <int DP>
@@ -120,7 +125,8 @@ __global__ void __launch_bounds__(256, 1)
     for (int i = 0; i < kStages; ++i) last_use[i] = -1;
     bool ok = true;
     int g = 0;  // running tile number of this CTA
-    for (int w = blockIdx.x; w < items && ok; w += gridDim.x) {
+    for (int r = 0, w = dq3_round_item(0, blockIdx.x, gridDim.x); w < items && ok;
+         ++r, w = dq3_round_item(r, blockIdx.x, gridDim.x)) {
       int bh, it, j_lo, j_hi;
       dq3_item(p, w, nqt128, &bh, &it);
       tiles_of(it, &j_lo, &j_hi);
@@ -176,7 +182,8 @@ __global__ void __launch_bounds__(256, 1)
     const uint64_t dB = sdesc_sw128(smem_addr(sm + L::DS), L::BK * 128, 1024);  // MN-major: 64-dim chunks
     bool ok = true;
     int g = 0, li = 0;
-    for (int w = blockIdx.x; w < items && ok; w += gridDim.x, ++li) {
+    for (int r = 0, w = dq3_round_item(0, blockIdx.x, gridDim.x); w < items && ok;
+         ++r, ++li, w = dq3_round_item(r, blockIdx.x, gridDim.x)) {
       int bh, it, j_lo, j_hi;
       dq3_item(p, w, nqt128, &bh, &it);
       tiles_of(it, &j_lo, &j_hi);
@@ -210,7 +217,8 @@ __global__ void __launch_bounds__(256, 1)
     const uint32_t lane_addr = static_cast<uint32_t>((warp & 3) * 32) << 16;
     bool ok = true;
     int li = 0;
-    for (int w = blockIdx.x; w < items && ok; w += gridDim.x, ++li) {
+    for (int r = 0, w = dq3_round_item(0, blockIdx.x, gridDim.x); w < items && ok;
+         ++r, ++li, w = dq3_round_item(r, blockIdx.x, gridDim.x)) {
       int bh, it, j_lo, j_hi;
       dq3_item(p, w, nqt128, &bh, &it);
       tiles_of(it, &j_lo, &j_hi);
