@@ -153,6 +153,36 @@ def test_paged_shared_at_offsets(bd, mla):
     assert all(torch.equal(a, b) for a, b in zip((dk, dvv), again))
 
 
+def test_paged_mla_split_irregular_links(bd):
+    """Cluster-split MLA blocks over links that do not follow one another:
+    sequence 2 maps its logical pages 0..P-2 to sequence 0's pages 1..P-1 and
+    sequence 3 swaps two shared pages, so the split kernel's tile counts (taken
+    by link index in the plan) meet runs of pages that break and shift."""
+    P = 11
+    c = inputs.paged_case(name="t", seed=36, num_seqs=12, len_lo=200, len_hi=320, queries_per_seq=24, heads=32,
+                          kv_heads=1, key_dim=512, value_dim=512, position_dim=64, scale=0.5, causal=True,
+                          shared_prefix_pages=P)
+    t = c.page_table.copy()
+    used = {int(t[s, lp]) for s in range(c.num_seqs) for lp in range(-(-int(c.seq_len[s]) // c.page_size))}
+    free = [q for q in range(c.num_pages) if q not in used]
+    t[2, :P - 1] = c.page_table[0, 1:P]
+    t[2, P - 1] = free[0]
+    t[3, [1, 3]] = t[3, [3, 1]]
+    c.page_table = t
+    src, ps = int(c.page_table[0, 0]), c.page_size
+    for pool in (c.k_pool, c.kp_pool):
+        pool[free[0] * ps:(free[0] + 1) * ps] = pool[src * ps:(src + 1) * ps]
+    dv = to_dev(c, bd)
+    dk_ref, dkp_ref, lse_ref, delta_ref = oracle(c)
+    lse, delta = gpu_stats(bd, c, dv)
+    dk, dkp = gpu_bwd(bd, c, dv, lse, delta)
+    bd.check_device_error()
+    assert rel(dk, dk_ref) < TOL
+    assert rel(dkp, dkp_ref) < TOL
+    again = gpu_bwd(bd, c, dv, lse, delta)
+    assert all(torch.equal(a, b) for a, b in zip((dk, dkp), again))
+
+
 def test_paged_mla_split_bit_stable(bd):
     """The cluster-split MLA blocks (8-CTA clusters on tcgen05, each block
     cut into chunks) sum their partials in a fixed order."""
