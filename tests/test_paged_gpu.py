@@ -85,6 +85,10 @@ CASES = [
          value_dim=512, position_dim=64, causal=True, shared_prefix_pages=9),
     dict(seed=32, num_seqs=12, len_lo=150, len_hi=300, queries_per_seq=24, heads=32, kv_heads=2, key_dim=512,
          value_dim=512, position_dim=64, causal=False, shared_prefix_pages=5),
+    # a pool of ~28,800 pages, almost all unreferenced: the link build and the
+    # zero store over a pool far larger than the pages in use
+    dict(seed=37, num_seqs=4, len_lo=60, len_hi=200, queries_per_seq=16, heads=4, kv_heads=1, key_dim=64,
+         value_dim=64, causal=True, pool_factor=800),
     # 72 flagged (block, KV head) units (9 blocks of a 72-page prefix shared by
     # 40 sequences, 8 KV heads, 39 x 2 link tiles each): enough units that the
     # split kernel takes them whole instead of cutting them into chunks, and
