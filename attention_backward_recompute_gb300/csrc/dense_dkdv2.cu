@@ -30,22 +30,24 @@ using namespace sm103;
 
 namespace {
 
-constexpr int kStages = 3;
 
-template <int DP>
+template <int DP, bool HAS_BIAS>
 struct Dkdv2Layout {
   static constexpr int NCH = DP / 64;
   static constexpr int BK = 128, BQ = 64;
+  // stages of the Q / dY (and bias) ring: 3 with a bias tile in each stage,
+  // 4 without
+  static constexpr int STAGES = HAS_BIAS ? 3 : 4;
   static constexpr int KV = NCH * BK * 128;       // K (or V) tile
   static constexpr int QT = NCH * BQ * 128;       // Q (or dY) tile
-  static constexpr int BIAS = 2 * BQ * 128;       // two 64-key halves x 64 query rows
+  static constexpr int BIAS = HAS_BIAS ? 2 * BQ * 128 : 0;  // two 64-key halves x 64 query rows
   static constexpr int K_OFF = 0;
   static constexpr int V_OFF = K_OFF + KV;
-  static constexpr int Q_OFF = V_OFF + KV;                 // kStages
-  static constexpr int DY_OFF = Q_OFF + kStages * QT;      // kStages
-  static constexpr int BIAS_OFF = DY_OFF + kStages * QT;   // kStages
-  static constexpr int ST_OFF = BIAS_OFF + kStages * BIAS; // kStages x {-L2, delta, pm} x 64 floats
-  static constexpr int BYTES = ST_OFF + kStages * 3 * BQ * 4;
+  static constexpr int Q_OFF = V_OFF + KV;                 // STAGES
+  static constexpr int DY_OFF = Q_OFF + STAGES * QT;       // STAGES
+  static constexpr int BIAS_OFF = DY_OFF + STAGES * QT;    // STAGES (with a bias)
+  static constexpr int ST_OFF = BIAS_OFF + STAGES * BIAS;  // STAGES x {-L2, delta, pm} x 64 floats
+  static constexpr int BYTES = ST_OFF + STAGES * 3 * BQ * 4;
   // TMEM: dV [0, DP), dK [DP, 2DP), S[2] and dP[2] 64 columns each after that
   static constexpr int T_S = 2 * DP, T_DP = 2 * DP + 128;
   static constexpr int TMEM_COLS = 2 * DP + 256 <= 256 ? 256 : 512;
@@ -204,7 +206,8 @@ __global__ void __launch_bounds__(384, 1)
     dkdv2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_dy,
                  const __grid_constant__ CUtensorMap tm_bias, const DenseParams p) {
-  using L = Dkdv2Layout<DP>;
+  using L = Dkdv2Layout<DP, HAS_BIAS>;
+  constexpr int kStages = L::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   // bar_kv: K/V of a live item loaded; bar_kv_free: every S/dP product of
@@ -580,7 +583,7 @@ __global__ void __launch_bounds__(384, 1)
 
 template <int DP, bool HAS_BIAS, bool ELEM, bool DS>
 cudaError_t launch_t(const DenseMaps& m, const DenseParams& p, cudaStream_t s) {
-  using L = Dkdv2Layout<DP>;
+  using L = Dkdv2Layout<DP, HAS_BIAS>;
   auto kern = dkdv2_kernel<DP, HAS_BIAS, ELEM, DS>;
   const int smem = max(L::BYTES + 1024, kSmemOneCtaPerSm);  // all 512 TMEM columns: one CTA per SM
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
