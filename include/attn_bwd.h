@@ -57,7 +57,7 @@ extern "C" {
 typedef int32_t attn_status_t;
 #define ATTN_OK 0
 #define ATTN_ERR_INVALID_ARG 1 /* null pointer, negative size, bad enum, ... */
-#define ATTN_ERR_UNSUPPORTED 2 /* valid request this build does not implement */
+#define ATTN_ERR_UNSUPPORTED 2 /* valid request the library does not implement */
 #define ATTN_ERR_ALIAS 3       /* an output overlaps an input or another output */
 #define ATTN_ERR_WORKSPACE 4   /* workspace missing, too small or misaligned */
 #define ATTN_ERR_CUDA 5        /* a CUDA runtime/driver call or launch failed */

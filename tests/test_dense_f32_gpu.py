@@ -40,7 +40,7 @@ def oracle(c):
 
 def check(res, ref, tol=TOL_F32):
     # An exactly-zero reference (e.g. dQ with a single key, where dS = P (dP - delta)
-    # cancels exactly) is judged against the largest gradient of the same call.
+    # cancels exactly) is measured against the largest gradient of the same call.
     scale = max(float(np.max(np.abs(w))) for w in ref)
     for n, g, w in zip(("dq", "dk", "dv"), res, ref):
         g = g.cpu().numpy().astype(np.float64)

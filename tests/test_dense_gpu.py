@@ -53,7 +53,7 @@ def rel_err(got, want, floor=0.0):
 
 def assert_close(res, ref, tol=TOL_BF16, names=("dq", "dk", "dv")):
     # An exactly-zero reference (e.g. dQ with a single key, where dS = P (dP - delta)
-    # cancels exactly) is judged against the largest gradient of the same call.
+    # cancels exactly) is measured against the largest gradient of the same call.
     scale = max(float(np.max(np.abs(w))) if w.size else 0.0 for w in ref)
     for n, g, w in zip(names, res, ref):
         if g is None:
