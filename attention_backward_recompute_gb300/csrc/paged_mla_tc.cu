@@ -574,34 +574,56 @@ __global__ void __launch_bounds__(384, 1)
   TcEpoch ep{0, 0, 0};
   while (true) {
     __syncthreads();  // the previous unit's readers of pinfo and unit_sh are done
-    if (threadIdx.x == 0) {
-      // unit k of the part: sequences in order, each with blocks x KV heads
-      int k = atomicAdd(p.work + part, 1), s0 = -1;
-      for (int s = 0; s < p.S; ++s) {
-        const int units = ((seq_len_of(p, s) + BT - 1) / BT) * p.KVH;
-        if (k < units) {
-          s0 = s;
-          break;
+    if (warp == 0) {
+      // unit k of the part: sequences in order, each with blocks x KV heads;
+      // the warp finds the sequence 32 at a time (a prefix sum of their
+      // units) and its lanes 0..7 resolve the block's eight pages
+      int k = 0;
+      if (lane == 0) k = atomicAdd(p.work + part, 1);
+      k = __shfl_sync(0xffffffffu, k, 0);
+      int s0 = -1, base = 0;
+      for (int c0 = 0; c0 < p.S && s0 < 0; c0 += 32) {  // warp-uniform
+        const int s = c0 + lane;
+        const int u = s < p.S ? ((seq_len_of(p, s) + BT - 1) / BT) * p.KVH : 0;
+        int x = u;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, x, o);
+          if (lane >= o) x += y;
         }
-        k -= units;
+        const int excl = base + x - u;
+        const unsigned hit = __ballot_sync(0xffffffffu, k >= excl && k < excl + u);
+        if (hit) {
+          const int l = __ffs(hit) - 1;
+          s0 = c0 + l;
+          k -= __shfl_sync(0xffffffffu, excl, l);
+        }
+        base += __shfl_sync(0xffffffffu, x, 31);
       }
-      unit_sh[0] = s0;
-      int any = 0, n = 0;
+      int any = 0, n = 0, g = 0, tb = 0;
       if (s0 >= 0) {
-        const int g = k % p.KVH, tb = k / p.KVH;
-        unit_sh[1] = tb;
-        unit_sh[2] = g;
-        any = fill_page_info(p, s0, tb, pages_of(seq_len_of(p, s0), p.page_size), &pinfo);
+        g = k % p.KVH;
+        tb = k / p.KVH;
+        const int st = lane < 8 ? fill_page_entry(p, s0, tb, pages_of(seq_len_of(p, s0), p.page_size), lane, &pinfo) : 0;
+        any = __any_sync(0xffffffffu, st != 0);
+        __syncwarp();
         // a block the plan flagged belongs to the cluster-split kernel
         if (any && p.heavy[(static_cast<int64_t>(s0) * nb128 + tb) * p.KVH + g]) any = 0;
-        PassIter it{&p, &pinfo, s0, tb};
-        if (any && it.begin(RT)) {
-          do ++n;
-          while (it.advance(RT));
+        if (lane == 0 && any) {
+          PassIter it{&p, &pinfo, s0, tb};
+          if (it.begin(RT)) {
+            do n += it.ntiles;
+            while (it.next_pass(RT));
+          }
         }
       }
-      any_store_sh = any;
-      n_tiles_sh = n;
+      if (lane == 0) {
+        unit_sh[0] = s0;
+        unit_sh[1] = tb;
+        unit_sh[2] = g;
+        any_store_sh = any;
+        n_tiles_sh = n;
+      }
     }
     __syncthreads();
     if (unit_sh[0] < 0) break;  // no units left (uniform)
@@ -863,7 +885,8 @@ __global__ void __launch_bounds__(384, 1)
     if (item < 0) return;  // not reached: u < nflag
     const int g = item % p.KVH, rest = item / p.KVH, tb = rest % nblk, s0 = rest / nblk;
     __syncthreads();  // found_sh is read; the previous item's readers of pinfo are done
-    if (threadIdx.x == 0) fill_page_info(p, s0, tb, pages_of(seq_len_of(p, s0), p.page_size), &pinfo);
+    if (warp == 0 && lane < 8)  // the block's eight pages side by side
+      fill_page_entry(p, s0, tb, pages_of(seq_len_of(p, s0), p.page_size), lane, &pinfo);
     __syncthreads();
     const int64_t n_all = p.heavy[item], pieces = static_cast<int64_t>(kSplitCL) * C, q = static_cast<int64_t>(c) * kSplitCL + rank;
     const int t0 = static_cast<int>(q * n_all / pieces), n = static_cast<int>((q + 1) * n_all / pieces) - t0;
