@@ -77,16 +77,35 @@ __device__ __forceinline__ int row_end_of(const PagedParams& p, int s) {
 // The idx-th tile of rt query rows, counting the row tiles of the sequences
 // in p.order (the longest sequences first, so that the CTAs with the longest
 // sweeps start first): its sequence and first row; sq = -1 past the last.
-__device__ inline void row_tile_at(const PagedParams& p, int idx, int rt, int* sq, int* r0) {
-  for (int k = 0; k < p.S; ++k) {
-    const int s = p.order[k];
-    const int rb = row_begin_of(p, s), tiles = (row_end_of(p, s) - rb + rt - 1) / rt;
-    if (idx < tiles) {
-      *sq = s;
-      *r0 = rb + idx * rt;
+// Called by a whole warp (every lane gets the result): the lanes take 32
+// sequences of the order at a time and find the tile's sequence by a prefix
+// sum of their tile counts.
+__device__ inline void row_tile_at_warp(const PagedParams& p, int idx, int rt, int* sq, int* r0) {
+  const int lane = threadIdx.x & 31;
+  int base = 0;
+  for (int c0 = 0; c0 < p.S; c0 += 32) {  // warp-uniform
+    const int k = c0 + lane;
+    int s = 0, rb = 0, tiles = 0;
+    if (k < p.S) {
+      s = p.order[k];
+      rb = row_begin_of(p, s);
+      tiles = (row_end_of(p, s) - rb + rt - 1) / rt;
+    }
+    int x = tiles;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    const int excl = base + x - tiles;
+    const unsigned hit = __ballot_sync(0xffffffffu, idx >= excl && idx < excl + tiles);
+    if (hit) {
+      const int l = __ffs(hit) - 1;
+      *sq = __shfl_sync(0xffffffffu, s, l);
+      *r0 = __shfl_sync(0xffffffffu, rb + (idx - excl) * rt, l);
       return;
     }
-    idx -= tiles;
+    base += __shfl_sync(0xffffffffu, x, 31);
   }
   *sq = -1;
   *r0 = 0;

@@ -80,11 +80,13 @@ __global__ void __launch_bounds__(384, 1)
   // order (longest first), KV head g
   const int g = static_cast<int>(blockIdx.x % p.KVH);
   const int G = p.G, RT = BC / G;
-  if (threadIdx.x == 0) {
+  if (threadIdx.x < 32) {  // warp 0
     int sq, r0;
-    row_tile_at(p, static_cast<int>(blockIdx.x / p.KVH), RT, &sq, &r0);
-    seq_sh = sq;
-    r0_sh = r0;
+    row_tile_at_warp(p, static_cast<int>(blockIdx.x / p.KVH), RT, &sq, &r0);
+    if (threadIdx.x == 0) {
+      seq_sh = sq;
+      r0_sh = r0;
+    }
   }
   __syncthreads();
   const int s0 = seq_sh, r0 = r0_sh;

@@ -72,11 +72,13 @@ __global__ void __launch_bounds__(256, 1)
   // order (longest first), KV head g
   const int g = static_cast<int>(blockIdx.x % p.KVH);
   const int RT = L::BQ / p.G;  // query rows per tile
-  if (threadIdx.x == 0) {
+  if (threadIdx.x < 32) {  // warp 0
     int sq_, r0_;
-    row_tile_at(p, static_cast<int>(blockIdx.x / p.KVH), RT, &sq_, &r0_);
-    tile_sq_sh = sq_;
-    tile_r0_sh = r0_;
+    row_tile_at_warp(p, static_cast<int>(blockIdx.x / p.KVH), RT, &sq_, &r0_);
+    if (threadIdx.x == 0) {
+      tile_sq_sh = sq_;
+      tile_r0_sh = r0_;
+    }
   }
   __syncthreads();
   const int sq = tile_sq_sh, r0 = tile_r0_sh;
