@@ -17,7 +17,11 @@
 // any more, so the score tile of i + 2 can be formed while the group works on
 // dS^T(i).  Q, dY, bias and the row statistics come through a 3-stage TMA
 // ring.  Warp 0: TMA producer, warp 1: MMA issuer (whole warp, elect.sync),
-// warps 4..7: group 0, warps 8..11: group 1.
+// warp 2: row statistics of each stage (global loads, one tile ahead),
+// warps 4..7: group 0, warps 8..11: group 1.  The statistics have a warp of
+// their own because their global loads, issued beside the compute warps'
+// shared-memory traffic, took ~2,000 cycles per tile in the producer's loop,
+// which then released each stage's copies that much later.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -262,21 +266,6 @@ __global__ void __launch_bounds__(384, 1)
       tma_prefetch_map(&tm_dy);
       if (HAS_BIAS) tma_prefetch_map(&tm_bias);
     }
-    // row statistics (-L2, delta, pm) of rows lane and lane + 32 of a tile,
-    // loaded one tile ahead within an item so their latency overlaps the
-    // wait for a stage
-    float pre[6];
-    auto load_stats = [&](int bh, int qb0) {
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const int q = qb0 + lane + 32 * i;
-        const bool in = q < p.Sq;
-        const size_t idx = static_cast<size_t>(bh) * p.Sq + (in ? q : 0);
-        pre[3 * i] = in ? -p.L2[idx] : -__int_as_float(0x7f800000);
-        pre[3 * i + 1] = in ? p.delta[idx] : 0.f;
-        pre[3 * i + 2] = (in && p.has_custom) ? p.pm[idx] : 0.f;
-      }
-    };
     int last_use[kStages];
     for (int i = 0; i < kStages; ++i) last_use[i] = -1;
     bool ok = true;
@@ -293,7 +282,6 @@ __global__ void __launch_bounds__(384, 1)
           tma_load_4d(sm + L::V_OFF + c * (L::BK * 128), &tm_v, &bar_kv, c * 64, k0, h, b);
         }
       }
-      load_stats(it.bh, it.i_lo * L::BQ);
       for (int t = 0; t < it.n && ok; ++t) {
         const int g = g0 + t, s = g % kStages;
         if (g >= kStages && !(ok = mbar_wait(&bar_empty[s], ((g / kStages) - 1) & 1, ab))) break;
@@ -321,6 +309,42 @@ __global__ void __launch_bounds__(384, 1)
             }
           }
         }
+        last_use[s] = g;
+      }
+      g0 += it.n;
+      ++lv;
+    }
+    if (lane == 0) {
+      for (int s = 0; s < kStages; ++s)
+        if (last_use[s] >= 0) drain_wait(&bar_full[s], (last_use[s] / kStages) & 1);
+      if (lv > 0) drain_wait(&bar_kv, (lv - 1) & 1);
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------------------ statistics
+    // (-L2, delta, pm) of rows lane and lane + 32 of each tile into its
+    // stage (the second arrival on the stage's full barrier), loaded one tile
+    // ahead so their latency overlaps the wait for the stage
+    float pre[6];
+    auto load_stats = [&](int bh, int qb0) {
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const int q = qb0 + lane + 32 * i;
+        const bool in = q < p.Sq;
+        const size_t idx = static_cast<size_t>(bh) * p.Sq + (in ? q : 0);
+        pre[3 * i] = in ? -p.L2[idx] : -__int_as_float(0x7f800000);
+        pre[3 * i + 1] = in ? p.delta[idx] : 0.f;
+        pre[3 * i + 2] = (in && p.has_custom) ? p.pm[idx] : 0.f;
+      }
+    };
+    bool ok = true;
+    int g0 = 0, idx;
+    while (ok && iter.next(&idx)) {
+      const Item it = item_at(p, idx);
+      if (it.n == 0) continue;
+      load_stats(it.bh, it.i_lo * L::BQ);
+      for (int t = 0; t < it.n && ok; ++t) {
+        const int g = g0 + t, s = g % kStages;
+        if (g >= kStages && !(ok = mbar_wait(&bar_empty[s], ((g / kStages) - 1) & 1, ab))) break;
         float* st = reinterpret_cast<float*>(sm + L::ST_OFF) + s * 3 * L::BQ;
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
@@ -330,16 +354,9 @@ __global__ void __launch_bounds__(384, 1)
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar_full[s]);
-        last_use[s] = g;
-        if (t + 1 < it.n) load_stats(it.bh, q0 + L::BQ);
+        if (t + 1 < it.n) load_stats(it.bh, (it.i_lo + t + 1) * L::BQ);
       }
       g0 += it.n;
-      ++lv;
-    }
-    if (lane == 0) {
-      for (int s = 0; s < kStages; ++s)
-        if (last_use[s] >= 0) drain_wait(&bar_full[s], (last_use[s] / kStages) & 1);
-      if (lv > 0) drain_wait(&bar_kv, (lv - 1) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
