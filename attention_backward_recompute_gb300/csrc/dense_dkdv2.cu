@@ -65,7 +65,20 @@ __device__ __forceinline__ bool drain_wait(uint64_t* bar, uint32_t parity) {
   return true;
 }
 
-__device__ __forceinline__ float4 lds_f4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+// shared-memory loads through 32-bit shared addresses (ld.shared, not a
+// generic load that must first resolve its address space)
+__device__ __forceinline__ float4 lds_f4(const float* p) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(smem_addr(p)));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+  return v;
+}
 
 // Registers written by tcgen05.ld are valid only after tcgen05.wait::ld; this
 // empty asm ties every later use of r to a point after the wait.
@@ -76,13 +89,13 @@ __device__ __forceinline__ void reg_fence16(uint32_t (&r)[16]) {
 
 // 16 queries [c0, c0+16) of the P^T row of one key: exp2(S*scale*log2e +
 // bias*log2e - L2) as 8 bf16 pairs, the arithmetic on fp32 pairs.  st holds
-// -L2 per query.  bq[m] points at this key's bias of query m (m < 8) of the
+// -L2 per query.  bq[m] is the shared address of this key's bias of query m (m < 8) of the
 // chunk; query m + 8 is 8 rows further on.  CHECK: zero the queries outside
 // [lo, hi] (tile-local range of queries that see this key).  kmasked: the key
 // is custom-masked; its visible entries take the row's masked-key
 // probability pm instead.
 template <bool HAS_BIAS, bool CHECK, bool ELEM>
-__device__ __forceinline__ void p_chunk(const uint32_t (&sr)[16], int c0, const float* st, const uint8_t* const* bq,
+__device__ __forceinline__ void p_chunk(const uint32_t (&sr)[16], int c0, const float* st, const uint32_t* bq,
                                         float scale_log2, int lo, int hi, bool kmasked, uint32_t ebits,
                                         uint32_t* pw) {
   const uint64_t sl2 = f2_pack(scale_log2, scale_log2);
@@ -97,8 +110,8 @@ __device__ __forceinline__ void p_chunk(const uint32_t (&sr)[16], int c0, const 
 #pragma unroll
       for (int h2 = 0; h2 < 2; ++h2) {
         const int m0 = 4 * c4 + 2 * h2;  // query of the chunk, 0..15
-        const uint32_t b0 = *reinterpret_cast<const uint16_t*>(bq[m0 & 7] + (m0 >> 3) * 1024);
-        const uint32_t b1 = *reinterpret_cast<const uint16_t*>(bq[(m0 + 1) & 7] + ((m0 + 1) >> 3) * 1024);
+        const uint32_t b0 = lds_u16(bq[m0 & 7] + (m0 >> 3) * 1024);
+        const uint32_t b1 = lds_u16(bq[(m0 + 1) & 7] + ((m0 + 1) >> 3) * 1024);
         x[h2] = f2_fma(f2_pack_u(b0 << 16, b1 << 16), l2e, x[h2]);
       }
     }
@@ -137,9 +150,9 @@ template <bool HAS_BIAS, bool CHECK, bool ELEM>
 __device__ __forceinline__ void p_row(uint32_t tS, const float* st, const uint8_t* bias_row, int kc,
                                       float scale_log2, int lo, int hi, bool kmasked, uint2 eb, uint32_t (&pw)[32]) {
   // the 128-byte swizzle moves query m's 16-byte chunk to chunk kc ^ (m % 8)
-  const uint8_t* bq[8];
+  uint32_t bq[8];
 #pragma unroll
-  for (int m = 0; m < 8; ++m) bq[m] = bias_row + m * 128 + (((kc ^ m) & 7) << 4);
+  for (int m = 0; m < 8; ++m) bq[m] = smem_addr(bias_row) + m * 128 + (((kc ^ m) & 7) << 4);
   uint32_t s0[16], s1[16];
   tmem_ld16(tS, s0);
   tmem_ld_wait();
@@ -212,8 +225,10 @@ __global__ void __launch_bounds__(384, 1)
                  const __grid_constant__ CUtensorMap tm_bias, const DenseParams p) {
   using L = Dkdv2Layout<DP, HAS_BIAS>;
   constexpr int kStages = L::STAGES;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // dynamic shared memory starts 1024-aligned after the static variables'
+  // granule on this GPU; the kernel checks it (the swizzled tiles need it)
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sm = smem_raw;
   // bar_kv: K/V of a live item loaded; bar_kv_free: every S/dP product of
   // the item done (K/V slots free); bar_acc: every product of the item done;
   // bar_acc_free: the epilogue has read dV and dK out of tensor memory.
@@ -222,6 +237,10 @@ __global__ void __launch_bounds__(384, 1)
       bar_p_full[2], bar_ds_full[2], bar_acc, bar_acc_free;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
+  if (smem_addr(smem_raw) & 1023u) {  // uniform
+    if (threadIdx.x == 0 && p.err) atomicOr(p.err, DEV_ERR_LAYOUT);
+    return;
+  }
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nkt = cdiv(p.Sk, L::BK);
@@ -602,7 +621,9 @@ template <int DP, bool HAS_BIAS, bool ELEM, bool DS>
 cudaError_t launch_t(const DenseMaps& m, const DenseParams& p, cudaStream_t s) {
   using L = Dkdv2Layout<DP, HAS_BIAS>;
   auto kern = dkdv2_kernel<DP, HAS_BIAS, ELEM, DS>;
-  const int smem = max(L::BYTES + 1024, kSmemOneCtaPerSm);  // all 512 TMEM columns: one CTA per SM
+  // the static variables take one 1 KiB granule before the dynamic part
+  static_assert(L::BYTES + 1024 <= 232448, "the layout fits one CTA's shared memory");
+  const int smem = max(L::BYTES, kSmemOneCtaPerSm);  // all 512 TMEM columns: one CTA per SM
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;
