@@ -74,8 +74,14 @@ __global__ void __launch_bounds__(256, 1)
     mla_query_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_qp,
                         const __grid_constant__ CUtensorMap tm_dy, const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_kp, const PagedParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // dynamic shared memory starts 1024-aligned after the static variables'
+  // granule on this GPU; the kernel checks it (the swizzled tiles need it)
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sm = smem_raw;
+  if (smem_addr(smem_raw) & 1023u) {  // uniform
+    if (threadIdx.x == 0 && p.err) atomicOr(p.err, DEV_ERR_LAYOUT);
+    return;
+  }
   __shared__ uint64_t bar_qdy, bar_full[kStages], bar_empty[kStages], bar_sdp_full, bar_sdp_read, bar_ds_ready,
       bar_ds_free, bar_acc;
   __shared__ uint32_t tmem_base_sh;
@@ -423,8 +429,10 @@ bool mla_query_tc_supported(const PagedParams& p) {
 
 cudaError_t launch_paged_mla_query_tc(const PagedMlaMaps& m, const PagedParams& p, cudaStream_t s) {
   if (p.Nq == 0 || p.S == 0) return cudaSuccess;
-  const int smem = BYTES + 1024;
-  static_assert(BYTES + 1024 >= kSmemOneCtaPerSm, "all 512 TMEM columns: one CTA per SM");
+  // the static variables take one 1 KiB granule before the dynamic part
+  static_assert(BYTES + 1024 <= 232448, "the layout fits one CTA's shared memory");
+  static_assert(BYTES >= kSmemOneCtaPerSm, "all 512 TMEM columns: one CTA per SM");
+  const int smem = BYTES;
   cudaError_t e = cudaFuncSetAttribute(mla_query_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   // an upper bound on the row tiles of all sequences; each CTA finds its own
