@@ -139,8 +139,14 @@ __global__ void __launch_bounds__(512, 1)
                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_dy,
                const __grid_constant__ CUtensorMap tm_bias, const DenseParams p) {
   using L = Dq2Layout<DP>;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // dynamic shared memory starts 1024-aligned after the static variables'
+  // granule on this GPU; the kernel checks it (the swizzled tiles need it)
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sm = smem_raw;
+  if (smem_addr(smem_raw) & 1023u) {  // uniform
+    if (threadIdx.x == 0 && p.err) atomicOr(p.err, DEV_ERR_LAYOUT);
+    return;
+  }
   __shared__ uint64_t bar_qdy, bar_a_ready, bar_full[kStages], bar_empty[kStages], bar_s_full[2], bar_dp_full[2],
       bar_p_full[2], bar_p_read[2], bar_ds_full[2], bar_acc;
   __shared__ uint32_t tmem_base_sh;
@@ -452,7 +458,9 @@ template <int DP, bool HAS_BIAS, bool ELEM>
 cudaError_t launch_t(const DenseMaps& m, const DenseParams& p, cudaStream_t s) {
   using L = Dq2Layout<DP>;
   auto kern = dq2_kernel<DP, HAS_BIAS, ELEM>;
-  const int smem = max(L::BYTES + 1024, kSmemOneCtaPerSm);  // all 512 TMEM columns: one CTA per SM
+  // the static variables take one 1 KiB granule before the dynamic part
+  static_assert(L::BYTES + 1024 <= 232448, "the layout fits one CTA's shared memory");
+  const int smem = max(L::BYTES, kSmemOneCtaPerSm);  // all 512 TMEM columns: one CTA per SM
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   dim3 grid(p.B * p.H, cdiv(p.Sq, L::BQ));
