@@ -399,8 +399,11 @@ ATTN_API const char* attn_status_string(attn_status_t s);
  * Synchronise `stream` and report device-side errors raised since the last
  * check by kernels of this library on the current device: ATTN_ERR_TIMEOUT if
  * a bounded wait expired (the kernel stopped early and its outputs are
- * invalid), ATTN_ERR_CUDA if the stream itself failed, else ATTN_OK.  Clears
- * the device error word.
+ * invalid), ATTN_ERR_CUDA if the stream itself failed or a kernel raised
+ * another device error (the message gives the error word: 0x4 a page-table
+ * entry outside [0, num_pages), skipped; 0x8 dynamic shared memory not at the
+ * 1024-byte alignment a kernel's layout needs, the kernel did nothing), else
+ * ATTN_OK.  Clears the device error word.
  */
 ATTN_API attn_status_t attn_check_device_error(void* stream);
 
