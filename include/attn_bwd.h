@@ -424,9 +424,12 @@ ATTN_API attn_status_t attn_selftest_wait_timeout(void* stream);
  * first kernel and events[i] after its i-th kernel (events are cudaEvent_t
  * handles created by the caller; `count` must cover every kernel of the call
  * plus one, else the call records nothing).  The hook applies to ONE call and
- * is then cleared.  The dense call launches, in order: (fp32 storage only)
- * four split kernels for q, dy, k, v; the row-statistics prologue; the dK/dV
- * kernel (if dK or dV is requested); the dQ kernel (if dQ is requested).  The
+ * is then cleared.  The dense call launches, in order: (ATTN_MASK_ELEM only)
+ * the kernel that packs the mask into row and column bits; (fp32 storage
+ * only) one kernel that splits q, dy, k and v into bf16 hi + lo; the
+ * row-statistics prologue (the delta-only kernel when O and LSE are given);
+ * the dK/dV kernel (if dK or dV is requested, or dS is stored for dQ); the dQ
+ * kernel (if dQ is requested).  The
  * paged backward launches its link preparation, the zero store of unlinked
  * pages and the history kernel (MLA: a plan kernel that flags the blocks whose
  * shared pages carry many links, the cluster-split kernel of those blocks,
