@@ -135,3 +135,24 @@ def test_store_ds_with_o_lse_and_strided_views(bd):
     for x, y in zip(a, b):
         assert torch.equal(x, y)
     _close(a, attn_bwd_dense(c.q, c.k, c.v, c.dy, causal=True, key_mask=c.key_mask, bias=c.bias))
+
+
+@pytest.mark.parametrize("window", [None, 128])
+def test_many_items_per_cta(bd, window):
+    """40 heads x 9 key tiles = 360 items for the persistent dK/dV kernel's
+    152 CTAs, so each CTA walks two or three items (its producer, statistics
+    and compute warps in step across item switches); with the window, the six
+    key tiles before the window hold no visible query (items with no tile).
+    Ragged Sq and Sk (a bias needs Sk * 2 bytes to be a multiple of 16), key
+    mask and bias; both dQ paths against the oracle, dK and dV
+    bit-identical between them."""
+    from oracle import attn_bwd_dense
+    c = inputs.dense_inputs(batch=2, heads=20, seq_q=200, seq_k=1096, head_dim=128, layout="bshd", seed=870,
+                            scale=0.5, causal=True, window=window, key_mask_zero_frac=0.1, bias=True)
+    ref = attn_bwd_dense(c.q, c.k, c.v, c.dy, layout="bshd", causal=True, window=window, key_mask=c.key_mask,
+                         bias=c.bias)
+    res = _run(bd, c, False, True)
+    _close(res, ref)
+    base = _run(bd, c, False, False)
+    _close(base, ref)
+    assert torch.equal(res[1], base[1]) and torch.equal(res[2], base[2])
