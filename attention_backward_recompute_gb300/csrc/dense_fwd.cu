@@ -457,6 +457,68 @@ __global__ void __launch_bounds__(256) delta_only_kernel(const DenseParams p) {
   }
 }
 
+// The same per row with 16-byte loads: LPR lanes (a power of two, at most 32)
+// share a row, lane l of the row reading elements [V l, V l + V), [V (l +
+// LPR), ...) of dY and O (V = 16 bytes of T), so a warp covers 32 / LPR rows
+// at a time.  Used when the rows start 16-byte aligned and D is a multiple of
+// V (the launcher checks); the sums then run in another order than the scalar
+// kernel's, which does not change what the library guarantees (one writer per
+// row, the same order from run to run).
+template <typename T, int LPR>
+__global__ void __launch_bounds__(256) delta_only_vec_kernel(const DenseParams p) {
+  constexpr int V = 16 / static_cast<int>(sizeof(T));
+  constexpr int RPW = 32 / LPR;  // rows per warp at a time
+  const int64_t rows = static_cast<int64_t>(p.B) * p.H * p.Sq;
+  const int lane = threadIdx.x & 31, sub = lane % LPR;
+  const int64_t w0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+  const float kInf = __int_as_float(0x7f800000);
+  const int nv = p.D / V;  // 16-byte vectors per row
+  for (int64_t r0 = w0 * RPW; r0 < rows; r0 += nw * RPW) {
+    const int64_t r = r0 + lane / LPR;
+    const bool valid = r < rows;
+    float acc = 0.f;
+    // 32-bit row arithmetic (the launcher takes this kernel only for fewer
+    // than 2^31 rows): a 64-bit division per row made the kernel issue-bound
+    const uint32_t ru = static_cast<uint32_t>(r), sq = static_cast<uint32_t>(p.Sq);
+    const int q = static_cast<int>(ru % sq);
+    if (valid) {
+      const uint32_t bh = ru / sq;
+      const int h = static_cast<int>(bh % static_cast<uint32_t>(p.H)), b = static_cast<int>(bh / static_cast<uint32_t>(p.H));
+      const T* dy = reinterpret_cast<const T*>(p.dy) + b * p.s_dy[2] + h * p.s_dy[1] + static_cast<int64_t>(q) * p.s_dy[0];
+      const T* o = reinterpret_cast<const T*>(p.o) + b * p.s_o[2] + h * p.s_o[1] + static_cast<int64_t>(q) * p.s_o[0];
+      for (int c = sub; c < nv; c += LPR) {
+        const uint4 a = *reinterpret_cast<const uint4*>(dy + c * V);
+        const uint4 e = *reinterpret_cast<const uint4*>(o + c * V);
+        const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, ew[4] = {e.x, e.y, e.z, e.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          if (sizeof(T) == 2) {
+            acc = fmaf(__uint_as_float(aw[i] << 16), __uint_as_float(ew[i] << 16), acc);
+            acc = fmaf(__uint_as_float(aw[i] & 0xffff0000u), __uint_as_float(ew[i] & 0xffff0000u), acc);
+          } else {
+            acc = fmaf(__uint_as_float(aw[i]), __uint_as_float(ew[i]), acc);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int sft = LPR / 2; sft > 0; sft >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, sft);
+    if (valid && sub == 0) {
+      const float lse = p.lse[r];
+      const int nvis = visible_keys(p, q);
+      const bool empty = nvis == 0 || lse == -kInf;
+      p.L2[r] = empty ? kInf : lse * kLog2e;
+      p.delta[r] = empty ? 0.f : acc;
+      if (p.has_custom) {
+        float pm = 0.f;
+        if (!empty) pm = (lse == p.mask_neg) ? 1.f / static_cast<float>(nvis) : ex2_approx((p.mask_neg - lse) * kLog2e);
+        p.pm[r] = pm;
+      }
+    }
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_fwd_stats(const DenseMaps& m, const DenseParams& p, bool bias, cudaStream_t s) {
@@ -565,6 +627,42 @@ cudaError_t launch_fill_f32(float* x, float value, int64_t n, cudaStream_t s) {
 cudaError_t launch_delta_only(const DenseParams& p, int dtype_bf16, cudaStream_t s) {
   const int64_t rows = static_cast<int64_t>(p.B) * p.H * p.Sq;
   if (rows == 0) return cudaSuccess;
+  // 16-byte loads when every row of dY and O starts 16-byte aligned and D is
+  // a multiple of 16 bytes of elements
+  const int es = dtype_bf16 ? 2 : 4, V = 16 / es;
+  auto a16 = [](const void* x, const int64_t* st, int es_) {
+    return (reinterpret_cast<uintptr_t>(x) & 15u) == 0 && (st[0] * es_) % 16 == 0 && (st[1] * es_) % 16 == 0 &&
+           (st[2] * es_) % 16 == 0;
+  };
+  if (p.D % V == 0 && rows < (int64_t(1) << 31) && a16(p.dy, p.s_dy, es) && a16(p.o, p.s_o, es)) {
+    const int nv = p.D / V;
+    const int lpr = nv >= 32 ? 32 : nv >= 16 ? 16 : nv >= 8 ? 8 : nv >= 4 ? 4 : nv >= 2 ? 2 : 1;
+    const int64_t warps = (rows * lpr + 31) / 32;
+    const int64_t b64 = (warps * 32 + 255) / 256;
+    const int blocks = static_cast<int>(b64 < 152 * 16 ? b64 : 152 * 16);
+#define ATTN_DELTA_VEC(T_, L_) delta_only_vec_kernel<T_, L_><<<blocks, 256, 0, s>>>(p)
+    if (dtype_bf16) {
+      switch (lpr) {
+        case 32: ATTN_DELTA_VEC(__nv_bfloat16, 32); break;
+        case 16: ATTN_DELTA_VEC(__nv_bfloat16, 16); break;
+        case 8: ATTN_DELTA_VEC(__nv_bfloat16, 8); break;
+        case 4: ATTN_DELTA_VEC(__nv_bfloat16, 4); break;
+        case 2: ATTN_DELTA_VEC(__nv_bfloat16, 2); break;
+        default: ATTN_DELTA_VEC(__nv_bfloat16, 1); break;
+      }
+    } else {
+      switch (lpr) {
+        case 32: ATTN_DELTA_VEC(float, 32); break;
+        case 16: ATTN_DELTA_VEC(float, 16); break;
+        case 8: ATTN_DELTA_VEC(float, 8); break;
+        case 4: ATTN_DELTA_VEC(float, 4); break;
+        case 2: ATTN_DELTA_VEC(float, 2); break;
+        default: ATTN_DELTA_VEC(float, 1); break;
+      }
+    }
+#undef ATTN_DELTA_VEC
+    return cudaGetLastError();
+  }
   const int64_t blocks64 = (rows * 32 + 255) / 256;
   const int blocks = static_cast<int>(blocks64 < 152 * 64 ? blocks64 : 152 * 64);
   if (dtype_bf16)
