@@ -482,6 +482,8 @@ __global__ void __launch_bounds__(256) delta_only_vec_kernel(const DenseParams p
     // than 2^31 rows): a 64-bit division per row made the kernel issue-bound
     const uint32_t ru = static_cast<uint32_t>(r), sq = static_cast<uint32_t>(p.Sq);
     const int q = static_cast<int>(ru % sq);
+    // the row's LSE is loaded beside dY and O, not after the reduction
+    const float lse = (valid && sub == 0) ? p.lse[r] : 0.f;
     if (valid) {
       const uint32_t bh = ru / sq;
       const int h = static_cast<int>(bh % static_cast<uint32_t>(p.H)), b = static_cast<int>(bh / static_cast<uint32_t>(p.H));
@@ -505,7 +507,6 @@ __global__ void __launch_bounds__(256) delta_only_vec_kernel(const DenseParams p
 #pragma unroll
     for (int sft = LPR / 2; sft > 0; sft >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, sft);
     if (valid && sub == 0) {
-      const float lse = p.lse[r];
       const int nvis = visible_keys(p, q);
       const bool empty = nvis == 0 || lse == -kInf;
       p.L2[r] = empty ? kInf : lse * kLog2e;
